@@ -1,0 +1,210 @@
+"""CPU oracle of the pooled-indexer sparse-attention path (ctypes over oracle.c).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` import this package.  The CUDA library never
+imports, links or calls it, and it shares no code with the library.
+
+Every function takes and returns numpy arrays; bf16 tensors are uint16 bit
+patterns.  Arithmetic is fp64 (see oracle.c for the step-by-step definition
+and the passages of the release notes each step follows).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain gcc)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _declare(lib):
+    P, I32, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.oracle_bf16_from_double.argtypes = [D]
+    lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+    lib.oracle_pool_keys.argtypes = [P, I64, P, I64, P, I32, I32, I32, P, I64]
+    lib.oracle_visible_counts.argtypes = [P, P, I32, I32, I32, P]
+    lib.oracle_index_scores.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, I32, I64, P]
+    lib.oracle_topk.argtypes = [P, P, I64, I64, I32, P]
+    lib.oracle_sparse_attn.argtypes = [P, P, I64, P, I64, P, P, I32, I32, I32, I32, I32,
+                                       I32, I32, D, P, P]
+    lib.oracle_retrieval_step.argtypes = [P, P, P, I64, P, P, I64, P, I64, P, P, I32, I32,
+                                          I32, I32, I32, I64, I32, I32, I32, I32, D, P, P,
+                                          P, P]
+    for f in ("oracle_pool_keys", "oracle_visible_counts", "oracle_index_scores",
+              "oracle_topk", "oracle_sparse_attn", "oracle_retrieval_step"):
+        getattr(lib, f).restype = None
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def compile_variant(src_text: str, so_path: str) -> None:
+    """Compile a (deliberately altered) copy of oracle.c for mutation tests."""
+    c_path = so_path[:-3] + ".c"
+    with open(c_path, "w") as f:
+        f.write(src_text)
+    subprocess.check_call(["gcc", *_CFLAGS, "-o", so_path, c_path, "-lm"])
+
+
+class use_library:
+    """Context manager: route this module's functions to another oracle build."""
+
+    def __init__(self, so_path: str):
+        self.path = so_path
+
+    def __enter__(self):
+        global _lib
+        self.saved = _lib
+        _lib = _declare(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    a = np.asarray(a)
+    assert a.dtype == np.dtype(dtype), (a.dtype, dtype)
+    return np.ascontiguousarray(a)
+
+
+def bf16_from_double(x: float) -> int:
+    return int(_load().oracle_bf16_from_double(float(x)))
+
+
+def pool_keys(k_idx, pool_w, seq_len, P, out=None):
+    """kbar[b,g,:] = bf16(sum_j alpha[b,g,j] * k[b,P*g+j,:]) for g < seq_len[b]//P."""
+    k_idx = _c(k_idx, np.uint16)
+    pool_w = _c(pool_w, np.float32)
+    seq_len = _c(seq_len, np.int32)
+    B, L_max, d = k_idx.shape
+    G_max = pool_w.shape[1]
+    assert pool_w.shape == (B, G_max, P)
+    if out is None:
+        out = np.zeros((B, G_max, d), np.uint16)
+    _load().oracle_pool_keys(_p(k_idx), L_max * d, _p(pool_w), G_max * P, _p(seq_len), B, d, P,
+                             _p(out), out.shape[1] * d)
+    return out
+
+
+def visible_counts(seq_len, q_pos, B, T, P):
+    seq_len = _c(seq_len, np.int32)
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    out = np.zeros((B, T), np.int32)
+    _load().oracle_visible_counts(_p(seq_len), _p(qp), B, T, P, _p(out))
+    return out
+
+
+def index_scores(q_idx, w_head, k_pooled, seq_len, P, q_pos=None):
+    """s[b,t,g] = sum_h w[b,t,h] * relu(q[b,t,h,:] . kbar[b,g,:]); -inf if not visible."""
+    q_idx = _c(q_idx, np.uint16)
+    w_head = _c(w_head, np.float32)
+    k_pooled = _c(k_pooled, np.uint16)
+    seq_len = _c(seq_len, np.int32)
+    B, T, H_i, d = q_idx.shape
+    G_max = k_pooled.shape[1]
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    out = np.empty((B, T, G_max), np.float32)
+    _load().oracle_index_scores(_p(q_idx), _p(w_head), _p(k_pooled), G_max * d, _p(seq_len),
+                                _p(qp), B, T, H_i, d, P, G_max, _p(out))
+    return out
+
+
+def topk(scores, n_valid, k):
+    """Top-k visible groups per row (ties -> lower index), ascending, -1 padded."""
+    scores = _c(scores, np.float32)
+    n_valid = _c(n_valid, np.int32)
+    G_max = scores.shape[-1]
+    rows = int(np.prod(scores.shape[:-1]))
+    assert n_valid.size == rows
+    out = np.empty(scores.shape[:-1] + (k,), np.int32)
+    _load().oracle_topk(_p(scores), _p(n_valid), rows, G_max, k, _p(out))
+    return out
+
+
+def sparse_attn(q, K, V, seq_len, idx, P, scale):
+    """Attention of every query head over the tokens of the selected groups."""
+    q = _c(q, np.uint16)
+    K = _c(K, np.uint16)
+    V = _c(V, np.uint16)
+    seq_len = _c(seq_len, np.int32)
+    idx = _c(idx, np.int32)
+    B, T, H_q, d_qk = q.shape
+    d_v = V.shape[2]
+    k = idx.shape[-1]
+    out = np.empty((B, T, H_q, d_v), np.uint16)
+    lse = np.empty((B, T, H_q), np.float32)
+    _load().oracle_sparse_attn(_p(q), _p(K), K.shape[1] * d_qk, _p(V), V.shape[1] * d_v,
+                               _p(seq_len), _p(idx), B, T, H_q, d_qk, d_v, P, k, float(scale),
+                               _p(out), _p(lse))
+    return out, lse
+
+
+def retrieval_step(q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale, q_pos=None):
+    """score -> select -> attend over already pooled keys.
+
+    Returns dict(scores, idx, out, lse).
+    """
+    q_idx = _c(q_idx, np.uint16)
+    w_head = _c(w_head, np.float32)
+    k_pooled = _c(k_pooled, np.uint16)
+    q = _c(q, np.uint16)
+    K = _c(K, np.uint16)
+    V = _c(V, np.uint16)
+    seq_len = _c(seq_len, np.int32)
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    B, T, H_i, d_idx = q_idx.shape
+    H_q, d_qk = q.shape[2], q.shape[3]
+    d_v = V.shape[2]
+    G_max = k_pooled.shape[1]
+    scores = np.empty((B, T, G_max), np.float32)
+    idx = np.empty((B, T, k), np.int32)
+    out = np.empty((B, T, H_q, d_v), np.uint16)
+    lse = np.empty((B, T, H_q), np.float32)
+    _load().oracle_retrieval_step(_p(q_idx), _p(w_head), _p(k_pooled), G_max * d_idx, _p(q),
+                                  _p(K), K.shape[1] * d_qk, _p(V), V.shape[1] * d_v,
+                                  _p(seq_len), _p(qp), B, T, H_i, d_idx, P, G_max, k, H_q, d_qk,
+                                  d_v, float(scale), _p(scores), _p(idx), _p(out), _p(lse))
+    return dict(scores=scores, idx=idx, out=out, lse=lse)
+
+
+def decode_case(case: dict, k_pooled=None):
+    """Oracle of one generated workload (synth.generate output): pool, then step."""
+    if k_pooled is None:
+        k_pooled = pool_keys(case["k_idx"], case["pool_w"], case["seq_len"], case["P"])
+    r = retrieval_step(case["q_idx"], case["w_head"], k_pooled, case["q"], case["K"], case["V"],
+                       case["seq_len"], case["P"], case["k"], case["scale"], case["q_pos"])
+    r["k_pooled"] = k_pooled
+    return r

@@ -1,0 +1,309 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU reference of the global-retrieval
+ * half of the hybrid attention described for GLM-5.3-Flash.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this code.  The CUDA library shares nothing with it
+ * (no header, helper, table or constant) and never calls it.
+ *
+ * What it computes, step by step, in the order of the DSA layer diagram
+ * (page "G2C Brief -- GLM-5.3-Flash", section "DSA keeps selected global access
+ * in eleven layers"): full token history -> IndexPool -> learned sparse
+ * selection (top-k) -> attention over the selected history.
+ *
+ *   pool    kbar[b,g,:] = sum_{j<P} alpha[b,g,j] * k[b, P*g+j, :]
+ *           ("four indexer key vectors into one via weighted pooling";
+ *            reading notes "GLM-5.3-Flash: Hybrid Attention, IndexPool, and
+ *            Vision-in-the-Loop", section 2 sub-head "IndexPool").
+ *   score   s[b,t,g] = sum_h w[b,t,h] * max(0, q[b,t,h,:] . kbar[b,g,:])
+ *           (the lightweight multi-head indexer; the pages name it only by
+ *            its DSA-indexer lineage, section 2 of the reading notes, and give
+ *            no formula, so this is the DSA indexer's ReLU-weighted form).
+ *   mask    decode: every complete group g < L_b/P is visible; chunked
+ *           prefill: group g is visible to the query at absolute position p
+ *           iff P*g + P - 1 <= p (only complete past groups).
+ *   select  the k visible groups of largest s; equal scores -> lower g first;
+ *           emitted in ascending g, padded with -1 when fewer than k are
+ *           visible ("learned sparse selection (top 2048)", index_topk 2048 =
+ *           512 groups of 4 tokens).
+ *   attend  softmax attention of every query head over the P*k tokens the
+ *           selected groups cover, one shared K/V head ("attention over
+ *           selected history").
+ *
+ * Arithmetic: every product and sum in double; each result rounded once to
+ * its storage type (bf16 round-to-nearest-even from the exact binary value,
+ * fp32 by C's double->float conversion).  Compile with -ffp-contract=off.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- bf16 --- */
+
+static double bf16_value(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Nearest bf16 to x (8 significant bits, ties to even), from the format's
+ * definition: scale |x| so that its quantum becomes 1, round to an integer
+ * with ties to even (rint in the default rounding mode), scale back. */
+uint16_t oracle_bf16_from_double(double x)
+{
+    if (isnan(x))
+        return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return sign | 0x7F80u;
+    int e;
+    frexp(a, &e);             /* a = f * 2^e, f in [0.5, 1)          */
+    int qe = e - 8;           /* quantum of an 8-significant-bit value */
+    if (qe < -133)
+        qe = -133;            /* bf16 subnormal quantum 2^-133          */
+    double r = rint(ldexp(a, -qe));
+    double y = ldexp(r, qe);
+    if (y >= 0x1p128)
+        return sign | 0x7F80u;
+    float f = (float)y;       /* exact: y has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)((u >> 16) & 0x7FFFu);
+}
+
+/* ---------------------------------------------------------------- pool --- */
+
+/* IndexPool over every complete group of every sequence.
+ * k_idx [B][*][d] (batch stride sk_b elements), pool_w [B][*][P] (stride sw_b),
+ * k_pooled [B][*][d] (stride sp_b).  Groups g >= seq_len[b]/P are untouched. */
+void oracle_pool_keys(const uint16_t *k_idx, int64_t sk_b, const float *pool_w, int64_t sw_b,
+                      const int32_t *seq_len, int B, int d, int P,
+                      uint16_t *k_pooled, int64_t sp_b)
+{
+    for (int b = 0; b < B; ++b) {
+        int64_t G = seq_len[b] / P;
+        for (int64_t g = 0; g < G; ++g) {
+            const float *alpha = pool_w + b * sw_b + g * P;
+            for (int i = 0; i < d; ++i) {
+                double s = 0.0;
+                for (int j = 0; j < P; ++j) {
+                    double kv = bf16_value(k_idx[b * sk_b + (P * g + j) * (int64_t)d + i]);
+                    s += (double)alpha[j] * kv;
+                }
+                k_pooled[b * sp_b + g * (int64_t)d + i] = oracle_bf16_from_double(s);
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------- visible --- */
+
+/* Number of visible groups for query t of sequence b (a prefix [0, n)). */
+static int64_t visible_groups(const int32_t *seq_len, const int32_t *q_pos, int b, int T, int t, int P)
+{
+    int64_t n = seq_len[b] / P;
+    if (q_pos) {
+        int64_t p = q_pos[(int64_t)b * T + t];
+        int64_t m = (p + 1) / P;   /* groups whose last token P*g+P-1 <= p */
+        if (p < 0)
+            m = 0;
+        if (m < n)
+            n = m;
+    }
+    return n;
+}
+
+void oracle_visible_counts(const int32_t *seq_len, const int32_t *q_pos, int B, int T, int P,
+                           int32_t *n_valid)
+{
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t)
+            n_valid[(int64_t)b * T + t] = (int32_t)visible_groups(seq_len, q_pos, b, T, t, P);
+}
+
+/* --------------------------------------------------------------- score --- */
+
+/* s[b][t][g] for g < visible count; -inf elsewhere.  -0 is stored as +0. */
+void oracle_index_scores(const uint16_t *q_idx, const float *w_head,
+                         const uint16_t *k_pooled, int64_t sp_b,
+                         const int32_t *seq_len, const int32_t *q_pos,
+                         int B, int T, int H_i, int d, int P, int64_t G_max, float *scores)
+{
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < T; ++t) {
+            int64_t n = visible_groups(seq_len, q_pos, b, T, t, P);
+            const uint16_t *qt = q_idx + ((int64_t)b * T + t) * H_i * d;
+            const float *wt = w_head + ((int64_t)b * T + t) * H_i;
+            float *st = scores + ((int64_t)b * T + t) * G_max;
+            for (int64_t g = 0; g < G_max; ++g) {
+                if (g >= n) {
+                    st[g] = -INFINITY;
+                    continue;
+                }
+                const uint16_t *kg = k_pooled + b * sp_b + g * d;
+                double s = 0.0;
+                for (int h = 0; h < H_i; ++h) {
+                    double dot = 0.0;
+                    for (int i = 0; i < d; ++i)
+                        dot += bf16_value(qt[h * d + i]) * bf16_value(kg[i]);
+                    double relu = dot > 0.0 ? dot : 0.0;
+                    s += (double)wt[h] * relu;
+                }
+                float f = (float)s;
+                st[g] = (f == 0.0f) ? 0.0f : f;
+            }
+        }
+    }
+}
+
+/* -------------------------------------------------------------- select --- */
+
+typedef struct {
+    float s;
+    int32_t g;
+} cand_t;
+
+/* larger score first; equal scores (including -0 == +0): lower index first */
+static int by_score_desc(const void *pa, const void *pb)
+{
+    const cand_t *a = (const cand_t *)pa, *b = (const cand_t *)pb;
+    if (a->s > b->s)
+        return -1;
+    if (a->s < b->s)
+        return 1;
+    return (a->g < b->g) ? -1 : (a->g > b->g);
+}
+
+static int by_index_asc(const void *pa, const void *pb)
+{
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a > b) - (a < b);
+}
+
+/* Per row: the min(k, n_valid) visible groups of largest score, ascending by
+ * index, then -1 padding.  Rows are [rows][G_max]; valid groups are the prefix
+ * [0, n_valid[row]). */
+void oracle_topk(const float *scores, const int32_t *n_valid, int64_t rows, int64_t G_max, int k,
+                 int32_t *idx)
+{
+    cand_t *c = (cand_t *)malloc(sizeof(cand_t) * (size_t)(G_max > 0 ? G_max : 1));
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t n = n_valid[r];
+        if (n > G_max)
+            n = G_max;
+        const float *sr = scores + r * G_max;
+        for (int64_t g = 0; g < n; ++g) {
+            c[g].s = sr[g];
+            c[g].g = (int32_t)g;
+        }
+        qsort(c, (size_t)n, sizeof(cand_t), by_score_desc);
+        int64_t m = n < k ? n : k;
+        int32_t *out = idx + r * k;
+        for (int64_t j = 0; j < m; ++j)
+            out[j] = c[j].g;
+        qsort(out, (size_t)m, sizeof(int32_t), by_index_asc);
+        for (int64_t j = m; j < k; ++j)
+            out[j] = -1;
+    }
+    free(c);
+}
+
+/* -------------------------------------------------------------- attend --- */
+
+/* For each (b, t) and query head h: softmax over the tokens of the selected
+ * groups (entries < 0 or >= seq_len[b]/P are skipped), one shared K/V head.
+ * out [B][T][H_q][d_v] bf16, lse [B][T][H_q] natural-log sum of exp (nullable).
+ * No selected token: output 0, lse -inf. */
+void oracle_sparse_attn(const uint16_t *q, const uint16_t *K, int64_t sK_b,
+                        const uint16_t *V, int64_t sV_b, const int32_t *seq_len,
+                        const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v, int P, int k,
+                        double scale, uint16_t *out, float *lse)
+{
+    int64_t max_tok = (int64_t)k * P;
+    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_tok > 0 ? max_tok : 1));
+    double *z = (double *)malloc(sizeof(double) * (size_t)(max_tok > 0 ? max_tok : 1));
+    double *o = (double *)malloc(sizeof(double) * (size_t)d_v);
+    for (int b = 0; b < B; ++b) {
+        int64_t G = seq_len[b] / P;
+        for (int t = 0; t < T; ++t) {
+            const int32_t *sel = idx + ((int64_t)b * T + t) * k;
+            int64_t n = 0;
+            for (int j = 0; j < k; ++j) {
+                int64_t g = sel[j];
+                if (g < 0 || g >= G)
+                    continue;
+                for (int i = 0; i < P; ++i)
+                    tok[n++] = P * g + i;
+            }
+            for (int h = 0; h < H_q; ++h) {
+                const uint16_t *qh = q + (((int64_t)b * T + t) * H_q + h) * d_qk;
+                uint16_t *oh = out + (((int64_t)b * T + t) * H_q + h) * d_v;
+                float *lh = lse ? lse + ((int64_t)b * T + t) * H_q + h : NULL;
+                if (n == 0) {
+                    for (int i = 0; i < d_v; ++i)
+                        oh[i] = 0;
+                    if (lh)
+                        *lh = -INFINITY;
+                    continue;
+                }
+                double m = -INFINITY;
+                for (int64_t j = 0; j < n; ++j) {
+                    const uint16_t *kj = K + b * sK_b + tok[j] * d_qk;
+                    double dot = 0.0;
+                    for (int i = 0; i < d_qk; ++i)
+                        dot += bf16_value(qh[i]) * bf16_value(kj[i]);
+                    z[j] = scale * dot;
+                    if (z[j] > m)
+                        m = z[j];
+                }
+                double l = 0.0;
+                for (int i = 0; i < d_v; ++i)
+                    o[i] = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    double p = exp(z[j] - m);
+                    l += p;
+                    const uint16_t *vj = V + b * sV_b + tok[j] * d_v;
+                    for (int i = 0; i < d_v; ++i)
+                        o[i] += p * bf16_value(vj[i]);
+                }
+                for (int i = 0; i < d_v; ++i)
+                    oh[i] = oracle_bf16_from_double(o[i] / l);
+                if (lh)
+                    *lh = (float)(m + log(l));
+            }
+        }
+    }
+    free(o);
+    free(z);
+    free(tok);
+}
+
+/* ---------------------------------------------------------- whole step --- */
+
+/* One retrieval step over already pooled keys: score -> select -> attend.
+ * scores [B][T][G_max] and idx [B][T][k] are outputs (scores is also the
+ * working buffer of the selection). */
+void oracle_retrieval_step(const uint16_t *q_idx, const float *w_head,
+                           const uint16_t *k_pooled, int64_t sp_b,
+                           const uint16_t *q, const uint16_t *K, int64_t sK_b,
+                           const uint16_t *V, int64_t sV_b,
+                           const int32_t *seq_len, const int32_t *q_pos,
+                           int B, int T, int H_i, int d_idx, int P, int64_t G_max, int k,
+                           int H_q, int d_qk, int d_v, double scale,
+                           float *scores, int32_t *idx, uint16_t *out, float *lse)
+{
+    int32_t *n_valid = (int32_t *)malloc(sizeof(int32_t) * (size_t)B * (size_t)T);
+    oracle_index_scores(q_idx, w_head, k_pooled, sp_b, seq_len, q_pos, B, T, H_i, d_idx, P,
+                        G_max, scores);
+    oracle_visible_counts(seq_len, q_pos, B, T, P, n_valid);
+    oracle_topk(scores, n_valid, (int64_t)B * T, G_max, k, idx);
+    oracle_sparse_attn(q, K, sK_b, V, sV_b, seq_len, idx, B, T, H_q, d_qk, d_v, P, k, scale,
+                       out, lse);
+    free(n_valid);
+}

@@ -1,0 +1,74 @@
+"""Planted mistakes: each altered copy of the oracle must fail at least one pin.
+
+Every mutant below is a plausible slip (a dropped term, a wrong sign or index,
+a transposed operand, a skipped step) planted in a temporary copy of
+oracle.c, compiled with gcc on the CPU.  The pins in test_oracle_pins.py are
+then run against the mutant; the test passes only if some pin catches it.
+"""
+import inspect
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+MUTANTS = {
+    "pool_drop_last_term": ("for (int j = 0; j < P; ++j) {", "for (int j = 0; j < P - 1; ++j) {"),
+    "pool_wrong_token_index": ("(P * g + j) * (int64_t)d + i", "(g + j) * (int64_t)d + i"),
+    "pool_weights_reversed": ("s += (double)alpha[j] * kv;", "s += (double)alpha[P - 1 - j] * kv;"),
+    "bf16_truncates": ("double r = rint(ldexp(a, -qe));", "double r = floor(ldexp(a, -qe));"),
+    "score_no_relu": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot;"),
+    "score_wrong_head_weight": ("s += (double)wt[h] * relu;", "s += (double)wt[0] * relu;"),
+    "score_query_transposed": ("dot += bf16_value(qt[h * d + i]) * bf16_value(kg[i]);",
+                               "dot += bf16_value(qt[i * H_i + h]) * bf16_value(kg[i]);"),
+    "mask_off_by_one": ("int64_t m = (p + 1) / P;", "int64_t m = p / P + 1;"),
+    "select_ascending": ("    if (a->s > b->s)\n        return -1;\n    if (a->s < b->s)\n        return 1;",
+                         "    if (a->s < b->s)\n        return -1;\n    if (a->s > b->s)\n        return 1;"),
+    "select_ties_to_higher_index": ("return (a->g < b->g) ? -1 : (a->g > b->g);",
+                                    "return (a->g > b->g) ? -1 : (a->g < b->g);"),
+    "select_unsorted_output": ("qsort(out, (size_t)m, sizeof(int32_t), by_index_asc);", ""),
+    "attn_no_scale": ("z[j] = scale * dot;", "z[j] = dot;"),
+    "attn_unnormalised": ("oh[i] = oracle_bf16_from_double(o[i] / l);",
+                          "oh[i] = oracle_bf16_from_double(o[i]);"),
+    "attn_values_from_keys": ("const uint16_t *vj = V + b * sV_b + tok[j] * d_v;",
+                              "const uint16_t *vj = K + b * sK_b + tok[j] * d_qk;"),
+    "attn_lse_sign": ("*lh = (float)(m + log(l));", "*lh = (float)(m - log(l));"),
+}
+
+
+def _pin_calls():
+    calls = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        params = inspect.signature(fn).parameters
+        if "j" in params:
+            calls.append((name, lambda fn=fn: fn(1)))
+        elif not params:
+            calls.append((name, fn))
+    return calls
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(mutant, tmp_path):
+    old, new = MUTANTS[mutant]
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation anchor not unique/absent: {mutant}"
+    so = str(tmp_path / f"oracle_{mutant}.so")
+    oracle.compile_variant(src.replace(old, new), so)
+    caught = []
+    with oracle.use_library(so):
+        for name, call in _pin_calls():
+            try:
+                call()
+            except Exception:
+                caught.append(name)
+    assert caught, f"no pin caught mutant {mutant}"
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    so = str(tmp_path / "oracle_copy.so")
+    oracle.compile_variant(oracle.source(), so)
+    with oracle.use_library(so):
+        for name, call in _pin_calls():
+            call()
