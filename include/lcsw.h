@@ -1,0 +1,261 @@
+/*
+ * lcsw.h -- C ABI of liblcsw.so: the global-retrieval half of a hybrid
+ * long-context attention (pooled indexer keys -> indexer scores -> top-k
+ * groups -> sparse attention over the selected tokens), for NVIDIA B300
+ * (sm_103a).
+ *
+ * The operation chain is the DSA layer of the GLM-5.3-Flash release
+ * ("G2C Brief -- GLM-5.3-Flash", section "DSA keeps selected global access in
+ * eleven layers": full token history -> IndexPool -> learned sparse selection
+ * (top 2048) -> attention over selected history; config index_kpool 4,
+ * index_topk 2048).  IndexPool is described in the reading notes
+ * "GLM-5.3-Flash: Hybrid Attention, IndexPool, and Vision-in-the-Loop",
+ * section 2, sub-head "IndexPool".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers      Device pointers unless stated otherwise, owned by the caller;
+ *               the library allocates and frees nothing.  Scratch space, when
+ *               a call needs any, is a caller-provided workspace whose size a
+ *               *_workspace_size query returns.
+ * Types         lcsw_bf16 is the raw 16-bit pattern of a bfloat16 value.
+ *               Weights, scores and lse are IEEE fp32; indices are int32.
+ * Layouts       Row-major and contiguous, except that the batch dimension of
+ *               per-token caches takes an explicit stride in ELEMENTS (so a
+ *               cache may be allocated with more rows than it holds).
+ * Alignment     Every bf16 tensor base and batch stride must give 16-byte
+ *               aligned rows; fp32/int32 arrays must be 4-byte aligned.
+ * Lengths       seq_len[b] (device int32, [B]) is the number of valid tokens
+ *               of sequence b.  Group g of sequence b covers tokens
+ *               [P*g, P*g+P); only complete groups (g < seq_len[b]/P) exist.
+ * Asynchrony    Every call only enqueues work on `stream` and returns; it
+ *               never synchronises the host (lcsw_get_status excepted).
+ * Errors        Every call returns an lcsw_status; nothing aborts and no C++
+ *               exception crosses the ABI.  On a nonzero status,
+ *               lcsw_last_error() returns a message (thread-local).  Argument
+ *               errors are detected on the host before anything is enqueued.
+ *               Device-side failures (a bounded wait that ran out) are
+ *               recorded in the workspace's status word and reported by
+ *               lcsw_get_status().
+ */
+#ifndef LCSW_H
+#define LCSW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lcsw_bf16;
+/* Same handle as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *lcsw_stream;
+
+typedef enum {
+    LCSW_OK = 0,
+    LCSW_ERR_INVALID_ARG = 1,  /* null pointer, bad dimension, misalignment      */
+    LCSW_ERR_CUDA = 2,         /* a CUDA runtime call or kernel launch failed     */
+    LCSW_ERR_UNSUPPORTED = 3,  /* valid but not implemented shape/device          */
+    LCSW_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out              */
+    LCSW_ERR_WORKSPACE = 5     /* workspace missing, too small or misaligned      */
+} lcsw_status;
+
+/* Message describing the last failing call on this thread ("" if none). */
+const char *lcsw_last_error(void);
+
+/* Library version string. */
+const char *lcsw_version(void);
+
+/* ---------------------------------------------------------------------------
+ * IndexPool (reading notes, section 2 "IndexPool": four indexer key vectors
+ * become one by weighted pooling; index_kpool 4).
+ *
+ *   k_pooled[b][g][:] = bf16( sum_{j<P} pool_w[b][g][j] * k_idx[b][P*g+j][:] )
+ *
+ * The sum is formed exactly and rounded once to bf16 (nearest, ties to even).
+ * Groups g in [g0_b, min(g0_b + g_span, seq_len[b]/P)) are written, where
+ * g0_b = g_begin ? g_begin[b] : 0; every other row of k_pooled is untouched.
+ *
+ *   k_idx     [B][*][d_idx] bf16, batch stride sk_b elements (raw indexer keys)
+ *   pool_w    [B][*][P] fp32, batch stride sw_b elements (pooling weights,
+ *             used as given: no normalisation is applied)
+ *   seq_len   [B] int32 device
+ *   g_begin   [B] int32 device, or NULL for 0
+ *   k_pooled  [B][*][d_idx] bf16, batch stride sp_b elements (output)
+ *   P in {1, 2, 4, 8}; d_idx a multiple of 8; g_span >= 0.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_pool_keys(const lcsw_bf16 *k_idx, int64_t sk_b,
+                           const float *pool_w, int64_t sw_b,
+                           const int32_t *seq_len, const int32_t *g_begin,
+                           int B, int g_span, int d_idx, int P,
+                           lcsw_bf16 *k_pooled, int64_t sp_b, lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Indexer scores (reading notes, section 2: a lightweight indexer picks the
+ * relevant slices; DSA-indexer form).
+ *
+ *   scores[b][t][g] = sum_h w_head[b][t][h] * max(0, q_idx[b][t][h][:] . k_pooled[b][g][:])
+ *
+ * for visible groups, -inf for the others (g < G_max).  Group g is visible to
+ * query t of sequence b iff g < seq_len[b]/P and, when q_pos is given,
+ * P*g + P - 1 <= q_pos[b][t] (causal at group granularity).  A score of -0 is
+ * written as +0.  Products bf16 x bf16 are exact; sums are fp32 (tensor-core
+ * accumulation), so results agree with an exact evaluation to about 1e-6
+ * relative.
+ *
+ *   q_idx     [B][T][H_i][d_idx] bf16      w_head [B][T][H_i] fp32
+ *   k_pooled  [B][*][d_idx] bf16, batch stride sp_b elements
+ *   q_pos     [B][T] int32 device or NULL (decode: all complete groups visible)
+ *   scores    [B][T][G_max] fp32 (output)
+ *   d_idx == 64; 1 <= H_i <= 16; P in {1, 2, 4, 8}.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_index_scores(const lcsw_bf16 *q_idx, const float *w_head,
+                              const lcsw_bf16 *k_pooled, int64_t sp_b,
+                              const int32_t *seq_len, const int32_t *q_pos,
+                              int B, int T, int H_i, int d_idx, int P, int G_max,
+                              float *scores, lcsw_stream stream);
+
+/* Visible group counts n_valid[b][t] (seq_len[b]/P, capped causally by q_pos
+ * as above); the per-row valid prefix that lcsw_topk_groups takes. */
+lcsw_status lcsw_visible_counts(const int32_t *seq_len, const int32_t *q_pos,
+                                int B, int T, int P, int32_t *n_valid, lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Top-k groups ("learned sparse selection (top 2048)", index_topk 2048 read as
+ * 512 groups of P = 4 tokens).
+ *
+ * For each row r: among groups [0, n_valid[r]) take the min(k, n_valid[r])
+ * of largest score; equal scores (-0 equals +0) go to the lower index.  The
+ * chosen indices are written in ascending order to idx[r][0..), and the
+ * remaining entries are -1.  Scores must not be NaN.
+ *
+ *   scores [rows][G_max] fp32      n_valid [rows] int32 device
+ *   idx    [rows][k] int32 (output)
+ *   ws     device workspace of lcsw_topk_workspace_size(rows, G_max, k) bytes
+ *          (may be NULL when that size is 0)
+ * ------------------------------------------------------------------------- */
+size_t lcsw_topk_workspace_size(int64_t rows, int G_max, int k);
+lcsw_status lcsw_topk_groups(const float *scores, const int32_t *n_valid,
+                             int64_t rows, int G_max, int k, int32_t *idx,
+                             void *ws, size_t ws_bytes, lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Sparse attention over the selected history ("attention over selected
+ * history"; one shared K/V head serves every query head).
+ *
+ * For row (b, t) the token set is {P*g + i : g in idx[b][t][:], 0 <= g <
+ * seq_len[b]/P, 0 <= i < P}; entries outside that range (e.g. -1 padding)
+ * are skipped.  For each query head h:
+ *   z_j = scale * q[b][t][h][:] . K[b][j][:],  p = softmax(z),
+ *   out[b][t][h][:] = bf16( sum_j p_j V[b][j][:] ),
+ *   lse[b][t][h] = ln sum_j exp(z_j).
+ * An empty token set gives out = 0 and lse = -inf.  The token set is split
+ * across thread blocks (split-K) and the partial softmax states are merged.
+ *
+ *   q    [B][T][H_q][d_qk] bf16
+ *   K    [B][*][d_qk] bf16 (batch stride sK_b elements); V [B][*][d_v] (sV_b)
+ *   idx  [B][T][k] int32 device
+ *   out  [B][T][H_q][d_v] bf16 (output); lse [B][T][H_q] fp32 or NULL
+ *   ws   device workspace of lcsw_sparse_attn_workspace_size(...) bytes
+ *   H_q a multiple of 16, at most 128; d_qk in {64, 128, 192, 256};
+ *   d_v in {64, 128}.
+ * ------------------------------------------------------------------------- */
+size_t lcsw_sparse_attn_workspace_size(int B, int T, int H_q, int d_v, int k, int P);
+lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_b,
+                             const lcsw_bf16 *V, int64_t sV_b, const int32_t *seq_len,
+                             const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
+                             int P, int k, float scale, lcsw_bf16 *out, float *lse,
+                             void *ws, size_t ws_bytes, lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * One decode step of the whole retrieval path (one query token per sequence):
+ * [append] -> scores -> top-k -> sparse attention, as one persistent kernel.
+ *
+ * Append: when k_idx is not NULL and seq_len[b] is a multiple of P, the group
+ * that the newest token completes (g = seq_len[b]/P - 1) is pooled from
+ * k_idx/pool_w into k_pooled before it is scored (same arithmetic as
+ * lcsw_pool_keys).  Then every complete group is scored, the top k groups are
+ * selected (rules of lcsw_topk_groups) and the query heads attend over their
+ * tokens (rules of lcsw_sparse_attn).
+ *
+ * The workspace must be zero-filled once before its first use; the call
+ * leaves it ready for the next call.  After LCSW_ERR_TIMEOUT from
+ * lcsw_get_status it must be zero-filled again.  Calls that share a
+ * workspace must not overlap on the device.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const lcsw_bf16 *q_idx;    /* [B][H_i][d_idx]                              */
+    const float *w_head;       /* [B][H_i]                                     */
+    lcsw_bf16 *k_pooled;       /* [B][*][d_idx], batch stride sp_b; in/out     */
+    int64_t sp_b;
+    const lcsw_bf16 *k_idx;    /* [B][*][d_idx] raw keys (stride sk_b) or NULL */
+    int64_t sk_b;
+    const float *pool_w;       /* [B][*][P] (stride sw_b); needed with k_idx   */
+    int64_t sw_b;
+    const lcsw_bf16 *q;        /* [B][H_q][d_qk]                               */
+    const lcsw_bf16 *K;        /* [B][*][d_qk], batch stride sK_b              */
+    int64_t sK_b;
+    const lcsw_bf16 *V;        /* [B][*][d_v], batch stride sV_b               */
+    int64_t sV_b;
+    const int32_t *seq_len;    /* [B]                                          */
+    int B, G_max, H_i, d_idx, P, k, H_q, d_qk, d_v;
+    float scale;
+    lcsw_bf16 *out;            /* [B][H_q][d_v] output                         */
+    float *lse;                /* [B][H_q] output or NULL                      */
+    int32_t *idx_out;          /* [B][k] selected groups (ascending) or NULL   */
+    float *scores_out;         /* [B][G_max] indexer scores or NULL            */
+} lcsw_decode_args;
+
+size_t lcsw_decode_workspace_size(const lcsw_decode_args *a);
+/* Number of kernel launches one lcsw_decode_fused call with these arguments
+ * enqueues (0 if the arguments are invalid). */
+int lcsw_decode_launches(const lcsw_decode_args *a);
+lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_bytes,
+                              lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Chunked prefill: T new query tokens per sequence, the last T tokens of the
+ * cache (positions seq_len[b]-T .. seq_len[b]-1), causal at group
+ * granularity.  Pools the groups the chunk completes (from the group holding
+ * token seq_len[b]-T onwards), scores every visible group for every query
+ * with a tensor-core GEMM, selects the top k per query and attends.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const lcsw_bf16 *q_idx;    /* [B][T][H_i][d_idx]                           */
+    const float *w_head;       /* [B][T][H_i]                                  */
+    lcsw_bf16 *k_pooled;       /* [B][*][d_idx] (stride sp_b); in/out          */
+    int64_t sp_b;
+    const lcsw_bf16 *k_idx;    /* [B][*][d_idx] raw keys (stride sk_b)         */
+    int64_t sk_b;
+    const float *pool_w;       /* [B][*][P] (stride sw_b)                      */
+    int64_t sw_b;
+    const lcsw_bf16 *q;        /* [B][T][H_q][d_qk]                            */
+    const lcsw_bf16 *K;        /* [B][*][d_qk] (stride sK_b)                   */
+    int64_t sK_b;
+    const lcsw_bf16 *V;        /* [B][*][d_v] (stride sV_b)                    */
+    int64_t sV_b;
+    const int32_t *seq_len;    /* [B] tokens including the new chunk           */
+    int B, T, G_max, H_i, d_idx, P, k, H_q, d_qk, d_v;
+    float scale;
+    lcsw_bf16 *out;            /* [B][T][H_q][d_v]                             */
+    float *lse;                /* [B][T][H_q] or NULL                          */
+    int32_t *idx_out;          /* [B][T][k] or NULL                            */
+} lcsw_prefill_args;
+
+size_t lcsw_prefill_workspace_size(const lcsw_prefill_args *a);
+lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
+                         lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Device status word of a workspace (decode / prefill).  Synchronises
+ * `stream`, then returns LCSW_OK, or LCSW_ERR_TIMEOUT if a bounded device
+ * wait ran out during an earlier call on that workspace.  Clears the word.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_get_status(void *ws, lcsw_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCSW_H */

@@ -1,0 +1,328 @@
+"""Python binding of liblcsw.so: pooled-indexer sparse attention on B300.
+
+Argument marshalling only.  Every step of the path runs in the library's CUDA
+kernels; tensors are torch CUDA tensors (torch supplies device memory and the
+current stream).  There is no CPU fallback: if liblcsw.so is missing or fails
+to load, importing a function raises.
+
+bf16 tensors may be torch.bfloat16 or int16/uint16 views of bf16 bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblcsw.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "lcsw.h")
+
+OK, ERR_INVALID_ARG, ERR_CUDA, ERR_UNSUPPORTED, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
+
+_lib = None
+
+_vp, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                              ctypes.c_size_t)
+
+
+class DecodeArgs(ctypes.Structure):
+    """Mirror of lcsw_decode_args."""
+    _fields_ = [
+        ("q_idx", _vp), ("w_head", _vp), ("k_pooled", _vp), ("sp_b", _i64),
+        ("k_idx", _vp), ("sk_b", _i64), ("pool_w", _vp), ("sw_b", _i64),
+        ("q", _vp), ("K", _vp), ("sK_b", _i64), ("V", _vp), ("sV_b", _i64),
+        ("seq_len", _vp),
+        ("B", _i32), ("G_max", _i32), ("H_i", _i32), ("d_idx", _i32), ("P", _i32), ("k", _i32),
+        ("H_q", _i32), ("d_qk", _i32), ("d_v", _i32), ("scale", _f32),
+        ("out", _vp), ("lse", _vp), ("idx_out", _vp), ("scores_out", _vp),
+    ]
+
+
+class PrefillArgs(ctypes.Structure):
+    """Mirror of lcsw_prefill_args."""
+    _fields_ = [
+        ("q_idx", _vp), ("w_head", _vp), ("k_pooled", _vp), ("sp_b", _i64),
+        ("k_idx", _vp), ("sk_b", _i64), ("pool_w", _vp), ("sw_b", _i64),
+        ("q", _vp), ("K", _vp), ("sK_b", _i64), ("V", _vp), ("sV_b", _i64),
+        ("seq_len", _vp),
+        ("B", _i32), ("T", _i32), ("G_max", _i32), ("H_i", _i32), ("d_idx", _i32), ("P", _i32),
+        ("k", _i32), ("H_q", _i32), ("d_qk", _i32), ("d_v", _i32), ("scale", _f32),
+        ("out", _vp), ("lse", _vp), ("idx_out", _vp),
+    ]
+
+
+_SIGNATURES = {
+    "lcsw_last_error": ([], ctypes.c_char_p),
+    "lcsw_version": ([], ctypes.c_char_p),
+    "lcsw_pool_keys": ([_vp, _i64, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i64, _vp],
+                       _i32),
+    "lcsw_index_scores": ([_vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                           _vp, _vp], _i32),
+    "lcsw_visible_counts": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
+    "lcsw_topk_workspace_size": ([_i64, _i32, _i32], _sz),
+    "lcsw_topk_groups": ([_vp, _vp, _i64, _i32, _i32, _vp, _vp, _sz, _vp], _i32),
+    "lcsw_sparse_attn_workspace_size": ([_i32, _i32, _i32, _i32, _i32, _i32], _sz),
+    "lcsw_sparse_attn": ([_vp, _vp, _i64, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                          _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp], _i32),
+    "lcsw_decode_workspace_size": ([ctypes.POINTER(DecodeArgs)], _sz),
+    "lcsw_decode_fused": ([ctypes.POINTER(DecodeArgs), _vp, _sz, _vp], _i32),
+    "lcsw_decode_launches": ([ctypes.POINTER(DecodeArgs)], _i32),
+    "lcsw_prefill_workspace_size": ([ctypes.POINTER(PrefillArgs)], _sz),
+    "lcsw_prefill": ([ctypes.POINTER(PrefillArgs), _vp, _sz, _vp], _i32),
+    "lcsw_get_status": ([_vp, _vp], _i32),
+}
+
+
+class LcswError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"lcsw status {status}: {msg}")
+        self.status = status
+
+
+def lib():
+    """The loaded liblcsw.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing; build it with "
+                               "`python -m long_context_sparse_weighted_b300._build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise LcswError(status, lib().lcsw_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+_BF16_OK = (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def _bf16(t: torch.Tensor, name: str, ndim: int, inner_contig: bool = True):
+    if t.dtype not in _BF16_OK:
+        raise TypeError(f"{name} must be bf16 (or its 16-bit view), got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if inner_contig and t.shape[0] > 0 and not t[0].is_contiguous():
+        raise ValueError(f"{name} must be contiguous apart from its batch stride")
+    return t
+
+
+def _dense(t: torch.Tensor, dtype, name: str):
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    return t
+
+
+def version() -> str:
+    return lib().lcsw_version().decode()
+
+
+# --------------------------------------------------------------- primitives --
+
+def pool_keys(k_idx, pool_w, seq_len, P, k_pooled, g_begin=None, g_span=None, stream=None):
+    """IndexPool: k_pooled[b, g] = bf16(sum_j pool_w[b, g, j] * k_idx[b, P*g + j])."""
+    _bf16(k_idx, "k_idx", 3)
+    _bf16(k_pooled, "k_pooled", 3)
+    if pool_w.dtype != torch.float32 or not pool_w[0].is_contiguous():
+        raise ValueError("pool_w must be float32 [B][G][P], contiguous per sequence")
+    _dense(seq_len, torch.int32, "seq_len")
+    B, _, d = k_idx.shape
+    if g_span is None:
+        g_span = k_pooled.shape[1]
+    _check(lib().lcsw_pool_keys(_ptr(k_idx), k_idx.stride(0), _ptr(pool_w), pool_w.stride(0),
+                                _ptr(seq_len), _ptr(g_begin), B, int(g_span), d, P,
+                                _ptr(k_pooled), k_pooled.stride(0), _stream(stream)))
+    return k_pooled
+
+
+def index_scores(q_idx, w_head, k_pooled, seq_len, P, G_max=None, q_pos=None, out=None,
+                 stream=None):
+    """Indexer scores [B][T][G_max] (fp32, -inf where not visible)."""
+    _bf16(q_idx, "q_idx", 4)
+    _bf16(k_pooled, "k_pooled", 3)
+    _dense(w_head, torch.float32, "w_head")
+    _dense(seq_len, torch.int32, "seq_len")
+    B, T, H_i, d = q_idx.shape
+    if G_max is None:
+        G_max = k_pooled.shape[1]
+    if out is None:
+        out = torch.empty(B, T, G_max, dtype=torch.float32, device=q_idx.device)
+    _check(lib().lcsw_index_scores(_ptr(q_idx), _ptr(w_head), _ptr(k_pooled),
+                                   k_pooled.stride(0), _ptr(seq_len), _ptr(q_pos), B, T, H_i, d,
+                                   P, int(G_max), _ptr(out), _stream(stream)))
+    return out
+
+
+def visible_counts(seq_len, q_pos, B, T, P, stream=None):
+    out = torch.empty(B, T, dtype=torch.int32, device=seq_len.device)
+    _check(lib().lcsw_visible_counts(_ptr(seq_len), _ptr(q_pos), B, T, P, _ptr(out),
+                                     _stream(stream)))
+    return out
+
+
+def topk_groups(scores, n_valid, k, out=None, stream=None):
+    """Top-k groups per row, ascending, -1 padded (rows = all leading dims)."""
+    _dense(scores, torch.float32, "scores")
+    _dense(n_valid, torch.int32, "n_valid")
+    G_max = scores.shape[-1]
+    rows = scores.numel() // G_max if G_max else 0
+    if out is None:
+        out = torch.empty(*scores.shape[:-1], k, dtype=torch.int32, device=scores.device)
+    nbytes = lib().lcsw_topk_workspace_size(rows, G_max, k)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=scores.device) if nbytes else None
+    _check(lib().lcsw_topk_groups(_ptr(scores), _ptr(n_valid), rows, G_max, k, _ptr(out),
+                                  _ptr(ws), nbytes, _stream(stream)))
+    return out
+
+
+def sparse_attn(q, K, V, seq_len, idx, P, scale, out=None, lse=None, ws=None, stream=None):
+    """Attention of every query head over the tokens of the selected groups."""
+    _bf16(q, "q", 4)
+    _bf16(K, "K", 3)
+    _bf16(V, "V", 3)
+    _dense(idx, torch.int32, "idx")
+    _dense(seq_len, torch.int32, "seq_len")
+    B, T, H_q, d_qk = q.shape
+    d_v = V.shape[2]
+    k = idx.shape[-1]
+    if out is None:
+        out = torch.empty(B, T, H_q, d_v, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, H_q, dtype=torch.float32, device=q.device)
+    nbytes = lib().lcsw_sparse_attn_workspace_size(B, T, H_q, d_v, k, P)
+    if ws is None and nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(lib().lcsw_sparse_attn(_ptr(q), _ptr(K), K.stride(0), _ptr(V), V.stride(0),
+                                  _ptr(seq_len), _ptr(idx), B, T, H_q, d_qk, d_v, P, k,
+                                  float(scale), _ptr(out), _ptr(lse), _ptr(ws), nbytes,
+                                  _stream(stream)))
+    return out, lse
+
+
+# ------------------------------------------------------------ decode step ---
+
+class Decoder:
+    """One decode step of the whole path through lcsw_decode_fused.
+
+    Holds the argument struct and a zero-initialised workspace; tensors are
+    bound once and may be refilled in place between calls.
+    """
+
+    def __init__(self, q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale,
+                 k_idx=None, pool_w=None, out=None, lse=None, idx_out=None, scores_out=None,
+                 G_max=None):
+        _bf16(q_idx, "q_idx", 3)
+        _bf16(k_pooled, "k_pooled", 3)
+        _bf16(q, "q", 3)
+        _bf16(K, "K", 3)
+        _bf16(V, "V", 3)
+        _dense(w_head, torch.float32, "w_head")
+        _dense(seq_len, torch.int32, "seq_len")
+        B, H_i, d_idx = q_idx.shape
+        H_q, d_qk = q.shape[1], q.shape[2]
+        d_v = V.shape[2]
+        dev = q.device
+        self.out = out if out is not None else torch.empty(B, H_q, d_v, dtype=torch.bfloat16,
+                                                           device=dev)
+        self.lse = lse if lse is not None else torch.empty(B, H_q, dtype=torch.float32,
+                                                           device=dev)
+        self.idx_out, self.scores_out = idx_out, scores_out
+        self._keep = (q_idx, w_head, k_pooled, q, K, V, seq_len, k_idx, pool_w)
+        a = DecodeArgs()
+        a.q_idx, a.w_head = q_idx.data_ptr(), w_head.data_ptr()
+        a.k_pooled, a.sp_b = k_pooled.data_ptr(), k_pooled.stride(0)
+        if k_idx is not None:
+            _bf16(k_idx, "k_idx", 3)
+            a.k_idx, a.sk_b = k_idx.data_ptr(), k_idx.stride(0)
+            a.pool_w, a.sw_b = pool_w.data_ptr(), pool_w.stride(0)
+        a.q = q.data_ptr()
+        a.K, a.sK_b = K.data_ptr(), K.stride(0)
+        a.V, a.sV_b = V.data_ptr(), V.stride(0)
+        a.seq_len = seq_len.data_ptr()
+        a.B, a.G_max = B, int(G_max if G_max is not None else k_pooled.shape[1])
+        a.H_i, a.d_idx, a.P, a.k = H_i, d_idx, P, k
+        a.H_q, a.d_qk, a.d_v, a.scale = H_q, d_qk, d_v, float(scale)
+        a.out, a.lse = self.out.data_ptr(), self.lse.data_ptr()
+        a.idx_out = idx_out.data_ptr() if idx_out is not None else None
+        a.scores_out = scores_out.data_ptr() if scores_out is not None else None
+        self.args = a
+        self.ws_bytes = lib().lcsw_decode_workspace_size(ctypes.byref(a))
+        self.launches_per_call = lib().lcsw_decode_launches(ctypes.byref(a))
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    def rebind(self, **tensors):
+        """Point the step at other tensors of identical shape (e.g. rotated caches)."""
+        a = self.args
+        for name, t in tensors.items():
+            setattr(a, name, t.data_ptr())
+        self._rebound = tensors
+
+    def __call__(self, stream=None):
+        _check(lib().lcsw_decode_fused(ctypes.byref(self.args), ctypes.c_void_p(self.ws.data_ptr()),
+                                       self.ws_bytes, _stream(stream)))
+        return self.out, self.lse
+
+    def status(self, stream=None):
+        _check(lib().lcsw_get_status(ctypes.c_void_p(self.ws.data_ptr()), _stream(stream)))
+
+
+def decode_fused(q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale, **kw):
+    """One-shot decode step; returns (out, lse, decoder)."""
+    d = Decoder(q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale, **kw)
+    out, lse = d()
+    return out, lse, d
+
+
+def prefill(q_idx, w_head, k_pooled, k_idx, pool_w, q, K, V, seq_len, P, k, scale,
+            out=None, lse=None, idx_out=None, G_max=None, stream=None):
+    """Chunked prefill of T query tokens per sequence (the last T of each cache)."""
+    _bf16(q_idx, "q_idx", 4)
+    _bf16(q, "q", 4)
+    B, T, H_i, d_idx = q_idx.shape
+    H_q, d_qk = q.shape[2], q.shape[3]
+    d_v = V.shape[2]
+    dev = q.device
+    if out is None:
+        out = torch.empty(B, T, H_q, d_v, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(B, T, H_q, dtype=torch.float32, device=dev)
+    a = PrefillArgs()
+    a.q_idx, a.w_head = q_idx.data_ptr(), w_head.data_ptr()
+    a.k_pooled, a.sp_b = k_pooled.data_ptr(), k_pooled.stride(0)
+    a.k_idx, a.sk_b = k_idx.data_ptr(), k_idx.stride(0)
+    a.pool_w, a.sw_b = pool_w.data_ptr(), pool_w.stride(0)
+    a.q = q.data_ptr()
+    a.K, a.sK_b = K.data_ptr(), K.stride(0)
+    a.V, a.sV_b = V.data_ptr(), V.stride(0)
+    a.seq_len = seq_len.data_ptr()
+    a.B, a.T = B, T
+    a.G_max = int(G_max if G_max is not None else k_pooled.shape[1])
+    a.H_i, a.d_idx, a.P, a.k = H_i, d_idx, P, k
+    a.H_q, a.d_qk, a.d_v, a.scale = H_q, d_qk, d_v, float(scale)
+    a.out, a.lse = out.data_ptr(), lse.data_ptr()
+    a.idx_out = idx_out.data_ptr() if idx_out is not None else None
+    nbytes = lib().lcsw_prefill_workspace_size(ctypes.byref(a))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    _check(lib().lcsw_prefill(ctypes.byref(a), ctypes.c_void_p(ws.data_ptr()), nbytes,
+                              _stream(stream)))
+    _check(lib().lcsw_get_status(ctypes.c_void_p(ws.data_ptr()), _stream(stream)))
+    return out, lse

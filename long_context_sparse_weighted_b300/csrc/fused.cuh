@@ -1,0 +1,17 @@
+// Persistent fused decode step (append -> score -> top-k -> attention).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/lcsw.h"
+
+namespace lcsw {
+
+bool fused_decode_supported(int B, int G_max, int H_i, int H_q, int d_qk, int d_v, int k, int P);
+size_t fused_decode_ws_bytes(int B, int G_max, int H_q, int d_v, int k, int P);
+cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status,
+                                cudaStream_t st);
+
+}  // namespace lcsw

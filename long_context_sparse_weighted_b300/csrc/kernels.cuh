@@ -1,0 +1,57 @@
+// Internal launchers of the liblcsw kernels.  Arguments are validated by the
+// C-ABI layer (lcsw_api.cu) before any of these is called; each returns the
+// launch's cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace lcsw {
+
+// IndexPool.  mode 0: groups [g_begin[b] (or 0), +g_span); mode 1: only the
+// group completed by the newest token (g = L/P - 1 when L % P == 0); mode 2:
+// groups from the one holding token L - tail on, g_span of them.
+cudaError_t launch_pool_keys(const uint16_t *k_idx, int64_t sk_b, const float *pool_w,
+                             int64_t sw_b, const int32_t *seq_len, const int32_t *g_begin,
+                             int B, int g_span, int d_idx, int P, int mode, int tail,
+                             uint16_t *k_pooled, int64_t sp_b, cudaStream_t st);
+
+// q_pos[b][t] = seq_len[b] - T + t (the chunk's absolute positions).
+cudaError_t launch_prefill_positions(const int32_t *seq_len, int B, int T, int32_t *q_pos,
+                                     cudaStream_t st);
+
+// Indexer scores with mma.sync (decode / short query blocks).
+cudaError_t launch_index_scores_mma(const uint16_t *q_idx, const float *w_head,
+                                    const uint16_t *k_pooled, int64_t sp_b,
+                                    const int32_t *seq_len, const int32_t *q_pos, int B, int T,
+                                    int H_i, int P, int G_max, float *scores, cudaStream_t st);
+
+// Indexer scores as a tcgen05/TMEM GEMM fed by TMA (chunked prefill).
+// Returns cudaErrorNotSupported when the shape is outside its envelope.
+cudaError_t launch_index_scores_tc(const uint16_t *q_idx, const float *w_head,
+                                   const uint16_t *k_pooled, int64_t sp_b,
+                                   const int32_t *seq_len, const int32_t *q_pos, int B, int T,
+                                   int H_i, int P, int G_max, float *scores, int *status,
+                                   cudaStream_t st);
+bool index_scores_tc_supported(int B, int T, int H_i, int G_max, int64_t sp_b);
+
+cudaError_t launch_visible_counts(const int32_t *seq_len, const int32_t *q_pos, int B, int T,
+                                  int P, int32_t *n_valid, cudaStream_t st);
+
+// Top-k per row, one thread block per row.  n_valid may be NULL, in which case
+// row r = b*T + t has seq_len[b]/P valid groups (seq_len/P/T must be given).
+cudaError_t launch_topk_rows(const float *scores, const int32_t *n_valid,
+                             const int32_t *seq_len, int P, int T, int64_t rows, int G_max,
+                             int k, int32_t *idx, cudaStream_t st);
+
+// Split-K sparse attention + combine.
+int sparse_attn_splits(int64_t rows, int H_q, int k, int P);
+size_t sparse_attn_ws_bytes(int64_t rows, int H_q, int d_v, int k, int P);
+cudaError_t launch_sparse_attn(const uint16_t *q, const uint16_t *K, int64_t sK_b,
+                               const uint16_t *V, int64_t sV_b, const int32_t *seq_len,
+                               const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
+                               int P, int k, float scale, uint16_t *out, float *lse, void *ws,
+                               cudaStream_t st);
+
+}  // namespace lcsw

@@ -1,0 +1,387 @@
+// C ABI of liblcsw.so (declared in include/lcsw.h): argument validation,
+// workspace carving and kernel sequencing.  No entry point allocates device
+// memory, synchronises the host (lcsw_get_status excepted) or lets a C++
+// exception escape.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/lcsw.h"
+#include "fused.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+lcsw_status fail(lcsw_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+lcsw_status cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return LCSW_OK;
+    return fail(LCSW_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool p_ok(int P) { return P == 1 || P == 2 || P == 4 || P == 8; }
+
+#define CHECK(cond, ...)                                   \
+    do {                                                   \
+        if (!(cond)) return fail(LCSW_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+
+// bf16 tensor with rows of `row_elems` and batch stride `sb` elements: base and
+// every row must be 16-byte aligned.
+bool bf16_rows_ok(const void *p, int64_t row_elems, int64_t sb) {
+    return aligned(p, 16) && (row_elems * 2) % 16 == 0 && (sb * 2) % 16 == 0;
+}
+
+// Workspace layout shared by decode and prefill:
+//   [0, 256)            status word (int) + reserved
+//   then 256-byte aligned regions, in order of request.
+struct Carver {
+    char *base;
+    size_t off = 256;
+    explicit Carver(void *b) : base(static_cast<char *>(b)) {}
+    void *take(size_t bytes) {
+        void *p = base ? base + off : nullptr;
+        off += (bytes + 255) & ~size_t(255);
+        return p;
+    }
+};
+
+bool attn_shape_ok(int H_q, int d_qk, int d_v) {
+    const bool heads = H_q > 0 && H_q % 16 == 0 && (H_q <= 32 || H_q % 64 == 0);
+    const bool dims = (d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128);
+    return heads && dims;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lcsw_last_error(void) { return g_err; }
+
+const char *lcsw_version(void) { return "lcsw 0.1 (sm_103a)"; }
+
+lcsw_status lcsw_pool_keys(const lcsw_bf16 *k_idx, int64_t sk_b, const float *pool_w,
+                           int64_t sw_b, const int32_t *seq_len, const int32_t *g_begin, int B,
+                           int g_span, int d_idx, int P, lcsw_bf16 *k_pooled, int64_t sp_b,
+                           lcsw_stream stream) {
+    CHECK(B >= 0 && g_span >= 0, "B and g_span must be >= 0");
+    CHECK(p_ok(P), "P must be 1, 2, 4 or 8 (got %d)", P);
+    CHECK(d_idx > 0 && d_idx % 8 == 0, "d_idx must be a positive multiple of 8");
+    if (B == 0 || g_span == 0) return LCSW_OK;
+    CHECK(k_idx && pool_w && seq_len && k_pooled, "null pointer argument");
+    CHECK(bf16_rows_ok(k_idx, d_idx, sk_b) && bf16_rows_ok(k_pooled, d_idx, sp_b),
+          "k_idx/k_pooled rows must be 16-byte aligned");
+    CHECK(aligned(pool_w, 4) && aligned(seq_len, 4) && (!g_begin || aligned(g_begin, 4)),
+          "fp32/int32 arrays must be 4-byte aligned");
+    CHECK(sk_b >= 0 && sw_b >= 0 && sp_b >= 0, "strides must be >= 0");
+    return cuda_status(lcsw::launch_pool_keys(k_idx, sk_b, pool_w, sw_b, seq_len, g_begin, B,
+                                              g_span, d_idx, P, 0, 0, k_pooled, sp_b,
+                                              (cudaStream_t)stream),
+                       "pool_keys launch");
+}
+
+lcsw_status lcsw_visible_counts(const int32_t *seq_len, const int32_t *q_pos, int B, int T,
+                                int P, int32_t *n_valid, lcsw_stream stream) {
+    CHECK(B >= 0 && T >= 0 && p_ok(P), "bad B/T/P");
+    if (int64_t(B) * T == 0) return LCSW_OK;
+    CHECK(seq_len && n_valid, "null pointer argument");
+    return cuda_status(lcsw::launch_visible_counts(seq_len, q_pos, B, T, P, n_valid,
+                                                   (cudaStream_t)stream),
+                       "visible_counts launch");
+}
+
+lcsw_status lcsw_index_scores(const lcsw_bf16 *q_idx, const float *w_head,
+                              const lcsw_bf16 *k_pooled, int64_t sp_b, const int32_t *seq_len,
+                              const int32_t *q_pos, int B, int T, int H_i, int d_idx, int P,
+                              int G_max, float *scores, lcsw_stream stream) {
+    CHECK(B >= 0 && T >= 0 && G_max >= 0, "negative dimension");
+    CHECK(d_idx == 64, "d_idx must be 64 (got %d)", d_idx);
+    CHECK(H_i >= 1 && H_i <= 16, "H_i must be in [1, 16] (got %d)", H_i);
+    CHECK(p_ok(P), "P must be 1, 2, 4 or 8");
+    if (int64_t(B) * T * G_max == 0) return LCSW_OK;
+    CHECK(q_idx && w_head && k_pooled && seq_len && scores, "null pointer argument");
+    CHECK(bf16_rows_ok(q_idx, d_idx, 0) && bf16_rows_ok(k_pooled, d_idx, sp_b),
+          "q_idx/k_pooled rows must be 16-byte aligned");
+    CHECK(aligned(w_head, 4) && aligned(scores, 4) && aligned(seq_len, 4), "misaligned array");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T > 1 && lcsw::index_scores_tc_supported(B, T, H_i, G_max, sp_b)) {
+        return cuda_status(lcsw::launch_index_scores_tc(q_idx, w_head, k_pooled, sp_b, seq_len,
+                                                        q_pos, B, T, H_i, P, G_max, scores,
+                                                        nullptr, st),
+                           "index_scores (tcgen05) launch");
+    }
+    CHECK(int64_t(B) * ((T + 3) / 4) <= 65535, "B * ceil(T/4) must be <= 65535");
+    return cuda_status(lcsw::launch_index_scores_mma(q_idx, w_head, k_pooled, sp_b, seq_len,
+                                                     q_pos, B, T, H_i, P, G_max, scores, st),
+                       "index_scores launch");
+}
+
+size_t lcsw_topk_workspace_size(int64_t rows, int G_max, int k) {
+    (void)rows; (void)G_max; (void)k;
+    return 0;
+}
+
+lcsw_status lcsw_topk_groups(const float *scores, const int32_t *n_valid, int64_t rows,
+                             int G_max, int k, int32_t *idx, void *ws, size_t ws_bytes,
+                             lcsw_stream stream) {
+    (void)ws; (void)ws_bytes;
+    CHECK(rows >= 0 && G_max >= 0, "negative dimension");
+    CHECK(k >= 1, "k must be >= 1 (got %d)", k);
+    CHECK(rows <= 0x7FFFFFFF, "too many rows");
+    if (rows == 0) return LCSW_OK;
+    CHECK(scores && n_valid && idx, "null pointer argument");
+    CHECK(aligned(scores, 4) && aligned(n_valid, 4) && aligned(idx, 4), "misaligned array");
+    return cuda_status(lcsw::launch_topk_rows(scores, n_valid, nullptr, 1, 1, rows, G_max, k,
+                                              idx, (cudaStream_t)stream),
+                       "topk launch");
+}
+
+size_t lcsw_sparse_attn_workspace_size(int B, int T, int H_q, int d_v, int k, int P) {
+    if (B <= 0 || T <= 0 || H_q <= 0 || d_v <= 0 || k <= 0 || !p_ok(P)) return 0;
+    return lcsw::sparse_attn_ws_bytes(int64_t(B) * T, H_q, d_v, k, P);
+}
+
+lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_b,
+                             const lcsw_bf16 *V, int64_t sV_b, const int32_t *seq_len,
+                             const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
+                             int P, int k, float scale, lcsw_bf16 *out, float *lse, void *ws,
+                             size_t ws_bytes, lcsw_stream stream) {
+    CHECK(B >= 0 && T >= 0, "negative dimension");
+    CHECK(k >= 1, "k must be >= 1");
+    CHECK(p_ok(P), "P must be 1, 2, 4 or 8");
+    CHECK(attn_shape_ok(H_q, d_qk, d_v),
+          "unsupported attention shape H_q=%d d_qk=%d d_v=%d (H_q in {16,32} or a multiple of "
+          "64; d_qk in {64,128,192}; d_v in {64,128})", H_q, d_qk, d_v);
+    const int64_t rows = int64_t(B) * T;
+    if (rows == 0) return LCSW_OK;
+    CHECK(rows <= 65535, "B*T must be <= 65535");
+    CHECK(q && K && V && seq_len && idx && out, "null pointer argument");
+    CHECK(bf16_rows_ok(q, d_qk, 0) && bf16_rows_ok(K, d_qk, sK_b) && bf16_rows_ok(V, d_v, sV_b) &&
+              bf16_rows_ok(out, d_v, 0),
+          "q/K/V/out rows must be 16-byte aligned");
+    CHECK(aligned(idx, 4) && aligned(seq_len, 4) && (!lse || aligned(lse, 4)), "misaligned array");
+    const size_t need = lcsw::sparse_attn_ws_bytes(rows, H_q, d_v, k, P);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16)))
+        return fail(LCSW_ERR_WORKSPACE, "sparse_attn needs a 16-byte aligned workspace of %zu bytes",
+                    need);
+    return cuda_status(lcsw::launch_sparse_attn(q, K, sK_b, V, sV_b, seq_len, idx, B, T, H_q,
+                                                d_qk, d_v, P, k, scale, out, lse, ws,
+                                                (cudaStream_t)stream),
+                       "sparse_attn launch");
+}
+
+// ------------------------------------------------------------------ decode --
+
+static lcsw_status check_decode(const lcsw_decode_args *a) {
+    CHECK(a, "null args");
+    CHECK(a->B >= 0 && a->G_max >= 0, "negative dimension");
+    CHECK(a->d_idx == 64, "d_idx must be 64");
+    CHECK(a->H_i >= 1 && a->H_i <= 16, "H_i must be in [1, 16]");
+    CHECK(p_ok(a->P), "P must be 1, 2, 4 or 8");
+    CHECK(a->k >= 1, "k must be >= 1");
+    CHECK(attn_shape_ok(a->H_q, a->d_qk, a->d_v), "unsupported attention shape");
+    if (a->B == 0) return LCSW_OK;
+    CHECK(a->B <= 65535, "B must be <= 65535");
+    CHECK(a->q_idx && a->w_head && a->k_pooled && a->q && a->K && a->V && a->seq_len && a->out,
+          "null pointer argument");
+    CHECK(!a->k_idx || a->pool_w, "pool_w is required with k_idx");
+    CHECK(bf16_rows_ok(a->q_idx, 64, 0) && bf16_rows_ok(a->k_pooled, 64, a->sp_b) &&
+              (!a->k_idx || bf16_rows_ok(a->k_idx, 64, a->sk_b)) &&
+              bf16_rows_ok(a->q, a->d_qk, 0) && bf16_rows_ok(a->K, a->d_qk, a->sK_b) &&
+              bf16_rows_ok(a->V, a->d_v, a->sV_b) && bf16_rows_ok(a->out, a->d_v, 0),
+          "bf16 rows must be 16-byte aligned");
+    CHECK(aligned(a->w_head, 4) && aligned(a->seq_len, 4) && (!a->lse || aligned(a->lse, 4)) &&
+              (!a->idx_out || aligned(a->idx_out, 4)) &&
+              (!a->scores_out || aligned(a->scores_out, 4)) &&
+              (!a->pool_w || aligned(a->pool_w, 4)),
+          "misaligned fp32/int32 array");
+    return LCSW_OK;
+}
+
+struct DecodeWs {
+    int *status;
+    float *scores;
+    int32_t *idx;
+    void *attn;
+    void *fused;
+    size_t total;
+};
+
+static DecodeWs carve_decode(const lcsw_decode_args *a, void *ws) {
+    Carver c(ws);
+    DecodeWs w;
+    w.status = static_cast<int *>(ws);
+    w.scores = static_cast<float *>(c.take(size_t(a->B) * a->G_max * sizeof(float)));
+    w.idx = static_cast<int32_t *>(c.take(size_t(a->B) * a->k * sizeof(int32_t)));
+    w.attn = c.take(lcsw::sparse_attn_ws_bytes(a->B, a->H_q, a->d_v, a->k, a->P));
+    w.fused = c.take(lcsw::fused_decode_ws_bytes(a->B, a->G_max, a->H_q, a->d_v, a->k, a->P));
+    w.total = c.off;
+    return w;
+}
+
+size_t lcsw_decode_workspace_size(const lcsw_decode_args *a) {
+    if (!a || a->B <= 0 || a->G_max < 0 || a->k < 1 || !p_ok(a->P)) return 256;
+    return carve_decode(a, nullptr).total;
+}
+
+int lcsw_decode_launches(const lcsw_decode_args *a) {
+    if (check_decode(a) != LCSW_OK) return 0;
+    if (a->B == 0) return 0;
+    if (lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P))
+        return 1;
+    const int S = lcsw::sparse_attn_splits(a->B, a->H_q, a->k, a->P);
+    return (a->k_idx ? 1 : 0) + 3 + (S > 1 ? 1 : 0);
+}
+
+lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_bytes,
+                              lcsw_stream stream) {
+    lcsw_status s = check_decode(a);
+    if (s != LCSW_OK || a->B == 0) return s;
+    const size_t need = lcsw_decode_workspace_size(a);
+    if (!ws || ws_bytes < need || !aligned(ws, 256))
+        return fail(LCSW_ERR_WORKSPACE, "decode needs a 256-byte aligned workspace of %zu bytes",
+                    need);
+    cudaStream_t st = (cudaStream_t)stream;
+    DecodeWs w = carve_decode(a, ws);
+    float *scores = a->scores_out ? a->scores_out : w.scores;
+    int32_t *idx = a->idx_out ? a->idx_out : w.idx;
+
+    if (lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P)) {
+        return cuda_status(lcsw::launch_fused_decode(a, w.fused, w.status, st), "fused decode");
+    }
+    // Multi-kernel path (same results): append, score, select, attend.
+    if (a->k_idx) {
+        cudaError_t e = lcsw::launch_pool_keys(a->k_idx, a->sk_b, a->pool_w, a->sw_b, a->seq_len,
+                                               nullptr, a->B, 1, 64, a->P, 1, 0, a->k_pooled,
+                                               a->sp_b, st);
+        if (e != cudaSuccess) return cuda_status(e, "decode append");
+    }
+    cudaError_t e = lcsw::launch_index_scores_mma(a->q_idx, a->w_head, a->k_pooled, a->sp_b,
+                                                  a->seq_len, nullptr, a->B, 1, a->H_i, a->P,
+                                                  a->G_max, scores, st);
+    if (e != cudaSuccess) return cuda_status(e, "decode scores");
+    e = lcsw::launch_topk_rows(scores, nullptr, a->seq_len, a->P, 1, a->B, a->G_max, a->k, idx, st);
+    if (e != cudaSuccess) return cuda_status(e, "decode top-k");
+    e = lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B, 1,
+                                 a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale, a->out, a->lse,
+                                 w.attn, st);
+    return cuda_status(e, "decode attention");
+}
+
+// ----------------------------------------------------------------- prefill --
+
+struct PrefillWs {
+    int *status;
+    float *scores;
+    int32_t *idx;
+    int32_t *q_pos;
+    int32_t *n_valid;
+    void *attn;
+    size_t total;
+};
+
+static PrefillWs carve_prefill(const lcsw_prefill_args *a, void *ws) {
+    Carver c(ws);
+    PrefillWs w;
+    const size_t rows = size_t(a->B) * a->T;
+    w.status = static_cast<int *>(ws);
+    w.scores = static_cast<float *>(c.take(rows * a->G_max * sizeof(float)));
+    w.idx = static_cast<int32_t *>(c.take(rows * a->k * sizeof(int32_t)));
+    w.q_pos = static_cast<int32_t *>(c.take(rows * sizeof(int32_t)));
+    w.n_valid = static_cast<int32_t *>(c.take(rows * sizeof(int32_t)));
+    w.attn = c.take(lcsw::sparse_attn_ws_bytes(int64_t(rows), a->H_q, a->d_v, a->k, a->P));
+    w.total = c.off;
+    return w;
+}
+
+size_t lcsw_prefill_workspace_size(const lcsw_prefill_args *a) {
+    if (!a || a->B <= 0 || a->T <= 0 || a->G_max < 0 || a->k < 1 || !p_ok(a->P)) return 256;
+    return carve_prefill(a, nullptr).total;
+}
+
+lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
+                         lcsw_stream stream) {
+    CHECK(a, "null args");
+    CHECK(a->B >= 0 && a->T >= 0 && a->G_max >= 0, "negative dimension");
+    CHECK(a->d_idx == 64, "d_idx must be 64");
+    CHECK(a->H_i >= 1 && a->H_i <= 16, "H_i must be in [1, 16]");
+    CHECK(p_ok(a->P), "P must be 1, 2, 4 or 8");
+    CHECK(a->k >= 1, "k must be >= 1");
+    CHECK(attn_shape_ok(a->H_q, a->d_qk, a->d_v), "unsupported attention shape");
+    const int64_t rows = int64_t(a->B) * a->T;
+    if (rows == 0) return LCSW_OK;
+    CHECK(rows <= 65535, "B*T must be <= 65535");
+    CHECK(a->q_idx && a->w_head && a->k_pooled && a->k_idx && a->pool_w && a->q && a->K && a->V &&
+              a->seq_len && a->out,
+          "null pointer argument");
+    CHECK(bf16_rows_ok(a->q_idx, 64, 0) && bf16_rows_ok(a->k_pooled, 64, a->sp_b) &&
+              bf16_rows_ok(a->k_idx, 64, a->sk_b) && bf16_rows_ok(a->q, a->d_qk, 0) &&
+              bf16_rows_ok(a->K, a->d_qk, a->sK_b) && bf16_rows_ok(a->V, a->d_v, a->sV_b) &&
+              bf16_rows_ok(a->out, a->d_v, 0),
+          "bf16 rows must be 16-byte aligned");
+    CHECK(aligned(a->w_head, 4) && aligned(a->seq_len, 4) && aligned(a->pool_w, 4) &&
+              (!a->lse || aligned(a->lse, 4)) && (!a->idx_out || aligned(a->idx_out, 4)),
+          "misaligned fp32/int32 array");
+    const size_t need = lcsw_prefill_workspace_size(a);
+    if (!ws || ws_bytes < need || !aligned(ws, 256))
+        return fail(LCSW_ERR_WORKSPACE, "prefill needs a 256-byte aligned workspace of %zu bytes",
+                    need);
+    cudaStream_t st = (cudaStream_t)stream;
+    PrefillWs w = carve_prefill(a, ws);
+    int32_t *idx = a->idx_out ? a->idx_out : w.idx;
+
+    // pool the groups the new chunk completes (and the one it finishes)
+    cudaError_t e = lcsw::launch_pool_keys(a->k_idx, a->sk_b, a->pool_w, a->sw_b, a->seq_len,
+                                           nullptr, a->B, a->T / a->P + 1, 64, a->P, 2, a->T,
+                                           a->k_pooled, a->sp_b, st);
+    if (e != cudaSuccess) return cuda_status(e, "prefill pool");
+    e = lcsw::launch_prefill_positions(a->seq_len, a->B, a->T, w.q_pos, st);
+    if (e != cudaSuccess) return cuda_status(e, "prefill positions");
+    if (lcsw::index_scores_tc_supported(a->B, a->T, a->H_i, a->G_max, a->sp_b)) {
+        e = lcsw::launch_index_scores_tc(a->q_idx, a->w_head, a->k_pooled, a->sp_b, a->seq_len,
+                                         w.q_pos, a->B, a->T, a->H_i, a->P, a->G_max, w.scores,
+                                         w.status, st);
+    } else {
+        CHECK(int64_t(a->B) * ((a->T + 3) / 4) <= 65535, "B * ceil(T/4) must be <= 65535");
+        e = lcsw::launch_index_scores_mma(a->q_idx, a->w_head, a->k_pooled, a->sp_b, a->seq_len,
+                                          w.q_pos, a->B, a->T, a->H_i, a->P, a->G_max, w.scores,
+                                          st);
+    }
+    if (e != cudaSuccess) return cuda_status(e, "prefill scores");
+    e = lcsw::launch_visible_counts(a->seq_len, w.q_pos, a->B, a->T, a->P, w.n_valid, st);
+    if (e != cudaSuccess) return cuda_status(e, "prefill visible counts");
+    e = lcsw::launch_topk_rows(w.scores, w.n_valid, nullptr, a->P, a->T, rows, a->G_max, a->k,
+                               idx, st);
+    if (e != cudaSuccess) return cuda_status(e, "prefill top-k");
+    e = lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B, a->T,
+                                 a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale, a->out, a->lse,
+                                 w.attn, st);
+    return cuda_status(e, "prefill attention");
+}
+
+lcsw_status lcsw_get_status(void *ws, lcsw_stream stream) {
+    CHECK(ws && aligned(ws, 4), "null or misaligned workspace");
+    cudaStream_t st = (cudaStream_t)stream;
+    int word = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e, "stream synchronize");
+    e = cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e, "status read");
+    if (word == 0) return LCSW_OK;
+    const int zero = 0;
+    e = cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_status(e, "status clear");
+    return fail(LCSW_ERR_TIMEOUT, "a device-side bounded wait ran out (code %d); zero-fill the "
+                "workspace before reusing it", word);
+}
+
+}  // extern "C"

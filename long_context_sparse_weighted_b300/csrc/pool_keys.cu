@@ -1,0 +1,148 @@
+// IndexPool: merge each group of P consecutive cached indexer keys into one
+// pooled key by weighted pooling (reading notes "GLM-5.3-Flash: Hybrid
+// Attention, IndexPool, and Vision-in-the-Loop", section 2, sub-head
+// "IndexPool"; index_kpool 4 in "G2C Brief -- GLM-5.3-Flash", DSA section).
+//
+//   kbar[b][g][i] = bf16( sum_{j<P} alpha[b][g][j] * k[b][P*g+j][i] )
+//
+// The sum is evaluated exactly (error-free product and sum transformations in
+// fp32) and rounded once to bf16, nearest with ties to even.
+//
+// Memory: a pure stream.  One thread owns 16 bytes (8 dims) of one group's
+// output row and issues P independent 16-byte coalesced loads (one per source
+// row; the 8 threads of a row read 128 contiguous bytes), so the bound is HBM
+// bandwidth: P*d*2 + P*4 bytes read and d*2 bytes written per group.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace lcsw {
+namespace {
+
+// a*b == p + e exactly (fp32 has a fused multiply-add).
+__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
+    p = __fmul_rn(a, b);
+    e = __fmaf_rn(a, b, -p);
+}
+
+// a+b == s + e exactly (Knuth's branch-free two-sum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Nearest bf16 (ties to even) of hi + lo, where hi = fl(hi + lo).  The bf16
+// grid is a subset of the fp32 grid, so rounding hi gives the right answer
+// unless hi sits exactly on a bf16 midpoint while lo != 0; then lo says on
+// which side of the midpoint the exact value lies.
+__device__ __forceinline__ uint32_t round_bf16_exact(float hi, float lo) {
+    uint32_t u = __float_as_uint(hi);
+    if ((u & 0xFFFFu) == 0x8000u && lo != 0.0f) {
+        bool away = (lo > 0.0f) == (hi > 0.0f);
+        return (u >> 16) + (away ? 1u : 0u);
+    }
+    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+template <int P>
+__device__ __forceinline__ uint32_t pool_pair(const float (&a)[P], const uint32_t (&w)[P],
+                                              bool high) {
+    float s = 0.0f, c = 0.0f;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+        float kv = high ? bf_hi(w[j]) : bf_lo(w[j]);
+        float p, e, t, err;
+        two_prod(a[j], kv, p, e);
+        two_sum(s, p, t, err);
+        s = t;
+        c = __fadd_rn(c, __fadd_rn(err, e));
+    }
+    float hi, lo;
+    two_sum(s, c, hi, lo);
+    return round_bf16_exact(hi, lo);
+}
+
+template <int P>
+__global__ void __launch_bounds__(256) pool_keys_kernel(
+    const uint16_t *__restrict__ k_idx, int64_t sk_b, const float *__restrict__ pool_w,
+    int64_t sw_b, const int32_t *__restrict__ seq_len, const int32_t *__restrict__ g_begin,
+    int B, int g_span, int d_idx, int mode, int tail, uint16_t *__restrict__ k_pooled,
+    int64_t sp_b) {
+    const int cpr = d_idx >> 3;  // 16-byte chunks per key row
+    const int64_t per_b = int64_t(g_span) * cpr;
+    const int64_t total = per_b * B;
+    for (int64_t it = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; it < total;
+         it += int64_t(gridDim.x) * blockDim.x) {
+        const int b = int(it / per_b);
+        const int64_t rem = it - int64_t(b) * per_b;
+        const int64_t gi = rem / cpr;
+        const int c = int(rem - gi * cpr);
+        const int L = __ldg(seq_len + b);
+        const int64_t G = L / P;
+        int64_t g0;
+        if (mode == 1)
+            g0 = (L % P == 0 && G > 0) ? G - 1 : G;
+        else if (mode == 2)
+            g0 = (L > tail ? L - tail : 0) / P;
+        else
+            g0 = g_begin ? int64_t(__ldg(g_begin + b)) : 0;
+        const int64_t g = g0 + gi;
+        if (g < 0 || g >= G) continue;
+
+        const uint16_t *src = k_idx + int64_t(b) * sk_b + (g * P) * d_idx + c * 8;
+        uint4 rows[P];
+#pragma unroll
+        for (int j = 0; j < P; ++j) rows[j] = ld_stream16(src + int64_t(j) * d_idx);
+        float a[P];
+        const float *wp = pool_w + int64_t(b) * sw_b + g * P;
+#pragma unroll
+        for (int j = 0; j < P; ++j) a[j] = __ldg(wp + j);
+
+        uint32_t wx[P], wy[P], wz[P], ww[P];
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            wx[j] = rows[j].x;
+            wy[j] = rows[j].y;
+            wz[j] = rows[j].z;
+            ww[j] = rows[j].w;
+        }
+        uint4 o;
+        o.x = pool_pair<P>(a, wx, false) | (pool_pair<P>(a, wx, true) << 16);
+        o.y = pool_pair<P>(a, wy, false) | (pool_pair<P>(a, wy, true) << 16);
+        o.z = pool_pair<P>(a, wz, false) | (pool_pair<P>(a, wz, true) << 16);
+        o.w = pool_pair<P>(a, ww, false) | (pool_pair<P>(a, ww, true) << 16);
+        *reinterpret_cast<uint4 *>(k_pooled + int64_t(b) * sp_b + g * d_idx + c * 8) = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pool_keys(const uint16_t *k_idx, int64_t sk_b, const float *pool_w,
+                             int64_t sw_b, const int32_t *seq_len, const int32_t *g_begin,
+                             int B, int g_span, int d_idx, int P, int mode, int tail,
+                             uint16_t *k_pooled, int64_t sp_b, cudaStream_t st) {
+    const int64_t total = int64_t(B) * g_span * (d_idx / 8);
+    if (total == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = int64_t(sms) * 8;  // 8 resident blocks of 256 per SM
+    if (blocks > cap) blocks = cap;
+#define LCSW_POOL(PP)                                                                   \
+    pool_keys_kernel<PP><<<unsigned(blocks), threads, 0, st>>>(                         \
+        k_idx, sk_b, pool_w, sw_b, seq_len, g_begin, B, g_span, d_idx, mode, tail, k_pooled,  \
+        sp_b)
+    switch (P) {
+        case 1: LCSW_POOL(1); break;
+        case 2: LCSW_POOL(2); break;
+        case 4: LCSW_POOL(4); break;
+        case 8: LCSW_POOL(8); break;
+        default: return cudaErrorInvalidValue;
+    }
+#undef LCSW_POOL
+    return cudaGetLastError();
+}
+
+}  // namespace lcsw

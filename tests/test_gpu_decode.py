@@ -1,0 +1,133 @@
+"""Whole decode step (lcsw_decode_fused) and chunked prefill (lcsw_prefill)
+against the CPU oracle, on the named workloads (shrunk where the full size is
+covered by test_gpu_fullsize.py) and on edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_sparse_weighted_b300 as lcsw
+import oracle
+import synth
+from gpu_util import (assert_attn_close, assert_lse_close, assert_scores_close, dev, dev_bf16,
+                      host_bits, selection_diff, upload_case)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode(c, kp, append=False, corrupt_last=False):
+    """Upload one generated decode workload and run the fused step."""
+    d = upload_case(c)
+    B, G_max, k = c["B"], c["G_max"], c["k"]
+    kp_dev = dev_bf16(kp).clone()
+    if corrupt_last:
+        for b in range(B):
+            G = int(c["seq_len"][b]) // c["P"]
+            if G:
+                kp_dev[b, G - 1] = 7.0
+    idx = torch.empty(B, k, dtype=torch.int32, device="cuda")
+    scores = torch.empty(B, G_max, dtype=torch.float32, device="cuda")
+    kw = dict(idx_out=idx, scores_out=scores)
+    if append:
+        kw.update(k_idx=d["k_idx"], pool_w=d["pool_w"])
+    dec = lcsw.Decoder(d["q_idx"][:, 0], d["w_head"][:, 0], kp_dev, d["q"][:, 0], d["K"], d["V"],
+                       d["seq_len"], c["P"], k, c["scale"], **kw)
+    out, lse = dec()
+    dec.status()
+    return dict(out=host_bits(out), lse=lse.cpu().numpy(), idx=idx.cpu().numpy(),
+                scores=scores.cpu().numpy(), k_pooled=host_bits(kp_dev))
+
+
+def check_against_oracle(c, got, ref, exact=False):
+    if exact:
+        assert np.array_equal(got["scores"], ref["scores"][:, 0])
+        assert np.array_equal(got["idx"], ref["idx"][:, 0])
+    else:
+        assert_scores_close(got["scores"], ref["scores"][:, 0])
+        nd = selection_diff(got["idx"], ref["idx"][:, 0], ref["scores"][:, 0])
+        assert nd == 0, f"{nd} rows selected a different (near-tie) set"
+    assert_attn_close(got["out"], ref["out"][:, 0])
+    assert_lse_close(got["lse"], ref["lse"][:, 0])
+
+
+def test_decode_tiny_bit_exact_selection():
+    c = synth.generate(synth.named("tiny"))
+    ref = oracle.decode_case(c)
+    got = run_decode(c, ref["k_pooled"])
+    check_against_oracle(c, got, ref, exact=True)
+
+
+@pytest.mark.parametrize("name,factor", [("decode_b8", 16), ("decode_1m", 32),
+                                         ("ragged_b64", 32)])
+def test_decode_workloads_shrunk(name, factor):
+    spec = synth.shrink(synth.named(name), factor)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_decode(c, ref["k_pooled"])
+    check_against_oracle(c, got, ref)
+
+
+def test_decode_append_repools_newest_group():
+    spec = synth.Spec(B=3, lengths=[4096, 1024, 2000], H_i=8, k=128, H_q=32, seed=200)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_decode(c, ref["k_pooled"], append=True, corrupt_last=True)
+    assert np.array_equal(got["k_pooled"], ref["k_pooled"])
+    check_against_oracle(c, got, ref)
+
+
+def test_decode_fewer_groups_than_k():
+    spec = synth.Spec(B=2, lengths=[64, 8], L_cap=1024, H_i=4, k=64, H_q=16, seed=201)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_decode(c, ref["k_pooled"])
+    assert (got["idx"][0, 16:] == -1).all() and (got["idx"][1, 2:] == -1).all()
+    check_against_oracle(c, got, ref)
+
+
+def test_decode_repeated_calls_reuse_workspace():
+    spec = synth.Spec(B=2, lengths=[8192, 6000], H_i=8, k=256, H_q=64, seed=202)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    d = upload_case(c)
+    dec = lcsw.Decoder(d["q_idx"][:, 0], d["w_head"][:, 0], dev_bf16(ref["k_pooled"]),
+                       d["q"][:, 0], d["K"], d["V"], d["seq_len"], 4, c["k"], c["scale"])
+    outs = [host_bits(dec()[0]).copy() for _ in range(3)]
+    dec.status()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    assert_attn_close(outs[0], ref["out"][:, 0])
+
+
+# ----------------------------------------------------------------- prefill --
+
+def run_prefill(c, kp_cached):
+    d = upload_case(c)
+    B, T, k = c["B"], c["T"], c["k"]
+    kp = dev_bf16(kp_cached).clone()
+    idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
+    out, lse = lcsw.prefill(d["q_idx"], d["w_head"], kp, d["k_idx"], d["pool_w"], d["q"], d["K"],
+                            d["V"], d["seq_len"], c["P"], k, c["scale"], idx_out=idx)
+    return dict(out=host_bits(out), lse=lse.cpu().numpy(), idx=idx.cpu().numpy(),
+                k_pooled=host_bits(kp))
+
+
+def _cached_part(kp_full, c):
+    """Pooled cache as it stood before the chunk: the chunk's groups zeroed."""
+    kp = kp_full.copy()
+    for b in range(c["B"]):
+        g0 = (int(c["seq_len"][b]) - c["T"]) // c["P"]
+        kp[b, g0:] = 0
+    return kp
+
+
+@pytest.mark.parametrize("lengths,T,k", [([16384 + 256], 256, 512), ([3001, 2050], 48, 100)])
+def test_prefill_reduced(lengths, T, k):
+    spec = synth.Spec(B=len(lengths), lengths=lengths, T=T, prefill=True, H_i=8, k=k, H_q=32,
+                      seed=210 + T)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_prefill(c, _cached_part(ref["k_pooled"], c))
+    assert np.array_equal(got["k_pooled"], ref["k_pooled"])
+    nd = selection_diff(got["idx"], ref["idx"], ref["scores"])
+    assert nd == 0, f"{nd} rows differ by near-ties"
+    assert_attn_close(got["out"], ref["out"])
+    assert_lse_close(got["lse"], ref["lse"])
