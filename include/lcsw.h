@@ -205,7 +205,20 @@ typedef struct {
     float *lse;                /* [B][H_q] output or NULL                      */
     int32_t *idx_out;          /* [B][k] selected groups (ascending) or NULL   */
     float *scores_out;         /* [B][G_max] indexer scores or NULL            */
+    int flags;                 /* 0, or LCSW_DECODE_* bits below (testing)     */
 } lcsw_decode_args;
+
+/* lcsw_decode_args.flags: alternative internal paths with identical results,
+ * for tests.  FORCE_MULTIPASS_SELECT makes the persistent kernel take its
+ * exact multi-pass selection (used when candidates overflow shared memory);
+ * FORCE_MULTIKERNEL runs the step as separate kernels (score, top-k, attend). */
+#define LCSW_DECODE_FORCE_MULTIPASS_SELECT 1
+#define LCSW_DECODE_FORCE_MULTIKERNEL 2
+/* Failure-detection test: the last block of each sequence returns before the
+ * first cross-block barrier, so the others' bounded waits run out; the call
+ * then reports LCSW_ERR_TIMEOUT through lcsw_get_status (workspace must be
+ * zero-filled again afterwards). */
+#define LCSW_DECODE_TEST_SKIP_ARRIVE 4
 
 size_t lcsw_decode_workspace_size(const lcsw_decode_args *a);
 /* Number of kernel launches one lcsw_decode_fused call with these arguments

@@ -37,7 +37,13 @@ class DecodeArgs(ctypes.Structure):
         ("B", _i32), ("G_max", _i32), ("H_i", _i32), ("d_idx", _i32), ("P", _i32), ("k", _i32),
         ("H_q", _i32), ("d_qk", _i32), ("d_v", _i32), ("scale", _f32),
         ("out", _vp), ("lse", _vp), ("idx_out", _vp), ("scores_out", _vp),
+        ("flags", _i32),
     ]
+
+
+FORCE_MULTIPASS_SELECT = 1
+FORCE_MULTIKERNEL = 2
+TEST_SKIP_ARRIVE = 4
 
 
 class PrefillArgs(ctypes.Structure):
@@ -229,7 +235,7 @@ class Decoder:
 
     def __init__(self, q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale,
                  k_idx=None, pool_w=None, out=None, lse=None, idx_out=None, scores_out=None,
-                 G_max=None):
+                 G_max=None, flags=0):
         _bf16(q_idx, "q_idx", 3)
         _bf16(k_pooled, "k_pooled", 3)
         _bf16(q, "q", 3)
@@ -264,6 +270,7 @@ class Decoder:
         a.out, a.lse = self.out.data_ptr(), self.lse.data_ptr()
         a.idx_out = idx_out.data_ptr() if idx_out is not None else None
         a.scores_out = scores_out.data_ptr() if scores_out is not None else None
+        a.flags = int(flags)
         self.args = a
         self.ws_bytes = lib().lcsw_decode_workspace_size(ctypes.byref(a))
         self.launches_per_call = lib().lcsw_decode_launches(ctypes.byref(a))

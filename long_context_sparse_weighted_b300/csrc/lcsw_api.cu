@@ -236,7 +236,8 @@ size_t lcsw_decode_workspace_size(const lcsw_decode_args *a) {
 int lcsw_decode_launches(const lcsw_decode_args *a) {
     if (check_decode(a) != LCSW_OK) return 0;
     if (a->B == 0) return 0;
-    if (lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P))
+    if (!(a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) &&
+        lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P))
         return 1;
     const int S = lcsw::sparse_attn_splits(a->B, a->H_q, a->k, a->P);
     return (a->k_idx ? 1 : 0) + 3 + (S > 1 ? 1 : 0);
@@ -255,7 +256,8 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
     float *scores = a->scores_out ? a->scores_out : w.scores;
     int32_t *idx = a->idx_out ? a->idx_out : w.idx;
 
-    if (lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P)) {
+    if (!(a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) &&
+        lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P)) {
         return cuda_status(lcsw::launch_fused_decode(a, w.fused, w.status, st), "fused decode");
     }
     // Multi-kernel path (same results): append, score, select, attend.

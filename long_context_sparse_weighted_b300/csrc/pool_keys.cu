@@ -14,53 +14,10 @@
 // bandwidth: P*d*2 + P*4 bytes read and d*2 bytes written per group.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "pool_core.cuh"
 
 namespace lcsw {
 namespace {
-
-// a*b == p + e exactly (fp32 has a fused multiply-add).
-__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
-    p = __fmul_rn(a, b);
-    e = __fmaf_rn(a, b, -p);
-}
-
-// a+b == s + e exactly (Knuth's branch-free two-sum).
-__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
-    s = __fadd_rn(a, b);
-    float bb = __fsub_rn(s, a);
-    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-
-// Nearest bf16 (ties to even) of hi + lo, where hi = fl(hi + lo).  The bf16
-// grid is a subset of the fp32 grid, so rounding hi gives the right answer
-// unless hi sits exactly on a bf16 midpoint while lo != 0; then lo says on
-// which side of the midpoint the exact value lies.
-__device__ __forceinline__ uint32_t round_bf16_exact(float hi, float lo) {
-    uint32_t u = __float_as_uint(hi);
-    if ((u & 0xFFFFu) == 0x8000u && lo != 0.0f) {
-        bool away = (lo > 0.0f) == (hi > 0.0f);
-        return (u >> 16) + (away ? 1u : 0u);
-    }
-    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
-}
-
-template <int P>
-__device__ __forceinline__ uint32_t pool_pair(const float (&a)[P], const uint32_t (&w)[P],
-                                              bool high) {
-    float s = 0.0f, c = 0.0f;
-#pragma unroll
-    for (int j = 0; j < P; ++j) {
-        float kv = high ? bf_hi(w[j]) : bf_lo(w[j]);
-        float p, e, t, err;
-        two_prod(a[j], kv, p, e);
-        two_sum(s, p, t, err);
-        s = t;
-        c = __fadd_rn(c, __fadd_rn(err, e));
-    }
-    float hi, lo;
-    two_sum(s, c, hi, lo);
-    return round_bf16_exact(hi, lo);
-}
 
 template <int P>
 __global__ void __launch_bounds__(256) pool_keys_kernel(
@@ -98,19 +55,7 @@ __global__ void __launch_bounds__(256) pool_keys_kernel(
 #pragma unroll
         for (int j = 0; j < P; ++j) a[j] = __ldg(wp + j);
 
-        uint32_t wx[P], wy[P], wz[P], ww[P];
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-            wx[j] = rows[j].x;
-            wy[j] = rows[j].y;
-            wz[j] = rows[j].z;
-            ww[j] = rows[j].w;
-        }
-        uint4 o;
-        o.x = pool_pair<P>(a, wx, false) | (pool_pair<P>(a, wx, true) << 16);
-        o.y = pool_pair<P>(a, wy, false) | (pool_pair<P>(a, wy, true) << 16);
-        o.z = pool_pair<P>(a, wz, false) | (pool_pair<P>(a, wz, true) << 16);
-        o.w = pool_pair<P>(a, ww, false) | (pool_pair<P>(a, ww, true) << 16);
+        const uint4 o = pool_chunk<P>(a, rows);
         *reinterpret_cast<uint4 *>(k_pooled + int64_t(b) * sp_b + g * d_idx + c * 8) = o;
     }
 }

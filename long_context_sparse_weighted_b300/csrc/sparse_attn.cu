@@ -14,6 +14,7 @@
 //
 // Kernel 2 (combine): one warp per (row, head) merges the S partial states:
 // M = max m_s, L = sum exp2(m_s - M) l_s, out = sum exp2(m_s - M) o_s / L.
+#include "attn_core.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -21,7 +22,6 @@ namespace lcsw {
 namespace {
 
 constexpr int kAttnThreads = 128;
-constexpr int kChunk = 64;        // tokens per chunk
 constexpr int kHeadGroup = 64;    // heads per thread block (4 warps x 16)
 constexpr int kTargetBlocks = 296;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -39,8 +39,6 @@ struct AttnSmem {
     static constexpr int body = kv_bytes > state_bytes ? kv_bytes : state_bytes;
     static constexpr int total = q_bytes + body + 2 * kChunk * 4;
 };
-
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
 template <int DQK, int DV>
 __global__ void __launch_bounds__(kAttnThreads) sparse_attn_split_kernel(
@@ -62,223 +60,72 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_split_kernel(
     const int hg0 = blockIdx.z * kHeadGroup;
     const int HG = min(kHeadGroup, H_q - hg0);
     const int b = int(row / T);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int G = __ldg(seq_len + b) / P;
     const int gps = (k + S - 1) / S;
     const int j0 = s * gps, j1 = min(k, j0 + gps);
     const int gpc = kChunk / P;  // groups per chunk
     const int nchunks = j1 > j0 ? (j1 - j0 + gpc - 1) / gpc : 0;
     const int32_t *irow = idx + row * k;
+    const uint16_t *kb = K + int64_t(b) * sK_b;
+    const uint16_t *vb = V + int64_t(b) * sV_b;
 
     // warp -> (head tile, token quarter)
-    const int MT = HG / 16;                 // 1, 2 or 4
-    const int TS = 4 / MT;                  // token splits of a chunk
+    const int MT = HG / 16;  // 1, 2 or 4
+    const int TS = 4 / MT;   // token splits of a chunk
     const int mt = warp % MT, ts = warp / MT;
-    const int ntok = kChunk / TS;           // 64, 32 or 16 tokens per warp
+    const int ntok = kChunk / TS;
     const int tok0 = ts * ntok;
 
-    // ---- Q tile to shared, then A fragments to registers -----------------
     const uint16_t *qrow = q + (row * H_q + hg0) * DQK;
     for (int p = tid; p < HG * (DQK / 8); p += kAttnThreads) {
         const int h = p / (DQK / 8), c8 = p % (DQK / 8);
         *reinterpret_cast<uint4 *>(sq + h * L::QP + c8 * 8) =
             ld_nc16(qrow + int64_t(h) * DQK + c8 * 8);
     }
-
-    auto issue_chunk = [&](int ci, int buf) {
+    auto issue = [&](int ci, int buf) {
         const int jb = j0 + ci * gpc;
-        if (tid < gpc) {
-            const int j = jb + tid;
-            int g = (j < j1) ? __ldg(irow + j) : -1;
-            sgrp[buf * kChunk + tid] = (g >= 0 && g < G) ? g : -1;
-        }
-        uint16_t *dk = sk + buf * kChunk * L::QP;
-        uint16_t *dv = sv + buf * kChunk * L::VP;
-        const uint16_t *kb = K + int64_t(b) * sK_b;
-        const uint16_t *vb = V + int64_t(b) * sV_b;
-        for (int p = tid; p < kChunk * (DQK / 8); p += kAttnThreads) {
-            const int tr = p / (DQK / 8), c8 = p % (DQK / 8);
-            const int j = jb + tr / P;
-            int g = (j < j1) ? __ldg(irow + j) : -1;
-            const bool ok = g >= 0 && g < G;
-            const uint16_t *src = ok ? kb + (int64_t(g) * P + tr % P) * DQK + c8 * 8 : kb;
-            cp_async16(smem_u32(dk + tr * L::QP + c8 * 8), src, ok ? 16 : 0);
-        }
-        for (int p = tid; p < kChunk * (DV / 8); p += kAttnThreads) {
-            const int tr = p / (DV / 8), c8 = p % (DV / 8);
-            const int j = jb + tr / P;
-            int g = (j < j1) ? __ldg(irow + j) : -1;
-            const bool ok = g >= 0 && g < G;
-            const uint16_t *src = ok ? vb + (int64_t(g) * P + tr % P) * DV + c8 * 8 : vb;
-            cp_async16(smem_u32(dv + tr * L::VP + c8 * 8), src, ok ? 16 : 0);
-        }
-        cp_async_commit();
+        gather_chunk<DQK, DV>(sk + buf * kChunk * L::QP, sv + buf * kChunk * L::VP,
+                              sgrp + buf * kChunk, irow + jb, min(gpc, j1 - jb), P, G, kb, vb,
+                              L::QP, L::VP, tid, kAttnThreads);
     };
-
-    if (nchunks > 0) issue_chunk(0, 0);
+    if (nchunks > 0) issue(0, 0);
     __syncthreads();  // Q in shared
 
     uint32_t qa[DQK / 16][4];
-    {
-        const int r = mt * 16 + (lane & 15), cc = (lane >> 4) * 8;
-#pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk)
-            ldmatrix_x4(smem_u32(sq + r * L::QP + kk * 16 + cc), qa[kk][0], qa[kk][1], qa[kk][2],
-                        qa[kk][3]);
-    }
-
-    float o[DV / 8][4];
-#pragma unroll
-    for (int i = 0; i < DV / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const int c = lane & 3;
-
+    load_q_frags<DQK>(qa, sq, L::QP, mt);
+    AttnWarpState<DV> st;
+    st.init();
     for (int ci = 0; ci < nchunks; ++ci) {
         const int buf = ci & 1;
         if (ci + 1 < nchunks) {
-            issue_chunk(ci + 1, buf ^ 1);
+            issue(ci + 1, buf ^ 1);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
         }
         __syncthreads();
-        const uint16_t *ck = sk + buf * kChunk * L::QP;
-        const uint16_t *cv = sv + buf * kChunk * L::VP;
-        const int *cg = sgrp + buf * kChunk;
-
-        constexpr int MAXNT = kChunk / 8;  // 8 n-tiles max
-        float sacc[MAXNT][4];
-#pragma unroll
-        for (int nt = 0; nt < MAXNT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < MAXNT; ++nt) {
-            if (nt * 8 >= ntok) break;
-            const int trow = tok0 + nt * 8 + (lane & 7);
-#pragma unroll
-            for (int kk = 0; kk < DQK / 16; kk += 2) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(smem_u32(ck + trow * L::QP + kk * 16 + (lane >> 3) * 8), b0, b1, b2, b3);
-                mma_bf16_16816(sacc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                if (kk + 1 < DQK / 16)
-                    mma_bf16_16816(sacc[nt], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2],
-                                   qa[kk + 1][3], b2, b3);
-            }
-        }
-        // scale, mask, online softmax
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < MAXNT; ++nt) {
-            if (nt * 8 >= ntok) break;
-            const int n0 = tok0 + nt * 8 + 2 * c;
-            const bool v0 = cg[n0 / P] >= 0, v1 = cg[(n0 + 1) / P] >= 0;
-            sacc[nt][0] = v0 ? sacc[nt][0] * scale_log2 : -INFINITY;
-            sacc[nt][1] = v1 ? sacc[nt][1] * scale_log2 : -INFINITY;
-            sacc[nt][2] = v0 ? sacc[nt][2] * scale_log2 : -INFINITY;
-            sacc[nt][3] = v1 ? sacc[nt][3] * scale_log2 : -INFINITY;
-            mx0 = fmaxf(mx0, fmaxf(sacc[nt][0], sacc[nt][1]));
-            mx1 = fmaxf(mx1, fmaxf(sacc[nt][2], sacc[nt][3]));
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m0 - ref0), al1 = fast_exp2(m1 - ref1);
-        m0 = mn0;
-        m1 = mn1;
-        l0 *= al0;
-        l1 *= al1;
-#pragma unroll
-        for (int i = 0; i < DV / 8; ++i) {
-            o[i][0] *= al0; o[i][1] *= al0;
-            o[i][2] *= al1; o[i][3] *= al1;
-        }
-#pragma unroll
-        for (int nt = 0; nt < MAXNT; ++nt) {
-            if (nt * 8 >= ntok) break;
-            sacc[nt][0] = fast_exp2(sacc[nt][0] - ref0);
-            sacc[nt][1] = fast_exp2(sacc[nt][1] - ref0);
-            sacc[nt][2] = fast_exp2(sacc[nt][2] - ref1);
-            sacc[nt][3] = fast_exp2(sacc[nt][3] - ref1);
-            l0 += sacc[nt][0] + sacc[nt][1];
-            l1 += sacc[nt][2] + sacc[nt][3];
-        }
-        // O += P V
-#pragma unroll
-        for (int kt = 0; kt < MAXNT / 2; ++kt) {
-            if (kt * 16 >= ntok) break;
-            const uint32_t pa0 = pack_bf2(sacc[2 * kt][0], sacc[2 * kt][1]);
-            const uint32_t pa1 = pack_bf2(sacc[2 * kt][2], sacc[2 * kt][3]);
-            const uint32_t pa2 = pack_bf2(sacc[2 * kt + 1][0], sacc[2 * kt + 1][1]);
-            const uint32_t pa3 = pack_bf2(sacc[2 * kt + 1][2], sacc[2 * kt + 1][3]);
-            const int vrow = tok0 + kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-            for (int dt = 0; dt < DV / 8; dt += 2) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(smem_u32(cv + vrow * L::VP + (dt + (lane >> 4)) * 8), b0, b1,
-                                  b2, b3);
-                mma_bf16_16816(o[dt], pa0, pa1, pa2, pa3, b0, b1);
-                mma_bf16_16816(o[dt + 1], pa0, pa1, pa2, pa3, b2, b3);
-            }
-        }
+        attn_chunk<DQK, DV>(st, qa, sk + buf * kChunk * L::QP, sv + buf * kChunk * L::VP,
+                            sgrp + buf * kChunk, L::QP, L::VP, P, tok0, ntok, scale_log2);
         __syncthreads();  // buffer reuse
     }
-
-    // ---- per-warp state -> shared, merge warps of the same head tile ------
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    store_warp_state<DV>(st, state + warp * 16 * (DV + 2));
     __syncthreads();
-    {
-        float *ws_ = state + warp * 16 * (DV + 2);
-        const int r0 = lane >> 2;
-#pragma unroll
-        for (int i = 0; i < DV / 8; ++i) {
-            ws_[r0 * (DV + 2) + i * 8 + 2 * c] = o[i][0];
-            ws_[r0 * (DV + 2) + i * 8 + 2 * c + 1] = o[i][1];
-            ws_[(r0 + 8) * (DV + 2) + i * 8 + 2 * c] = o[i][2];
-            ws_[(r0 + 8) * (DV + 2) + i * 8 + 2 * c + 1] = o[i][3];
-        }
-        if (c == 0) {
-            ws_[r0 * (DV + 2) + DV] = m0;
-            ws_[r0 * (DV + 2) + DV + 1] = l0;
-            ws_[(r0 + 8) * (DV + 2) + DV] = m1;
-            ws_[(r0 + 8) * (DV + 2) + DV + 1] = l1;
-        }
-    }
-    __syncthreads();
-    // one thread per (head, 2 dims)
     for (int p = tid; p < HG * (DV / 2); p += kAttnThreads) {
         const int hl = p / (DV / 2), d2 = (p % (DV / 2)) * 2;
-        const int tile = hl / 16, rr = hl % 16;
-        float M = -INFINITY;
-        for (int t2 = 0; t2 < TS; ++t2) {
-            const float *st = state + (t2 * MT + tile) * 16 * (DV + 2) + rr * (DV + 2);
-            M = fmaxf(M, st[DV]);
-        }
-        const float ref = M == -INFINITY ? 0.f : M;
-        float Lsum = 0.f, oa = 0.f, ob = 0.f;
-        for (int t2 = 0; t2 < TS; ++t2) {
-            const float *st = state + (t2 * MT + tile) * 16 * (DV + 2) + rr * (DV + 2);
-            const float f = fast_exp2(st[DV] - ref);
-            Lsum += f * st[DV + 1];
-            oa += f * st[d2];
-            ob += f * st[d2 + 1];
-        }
+        float Lsum;
+        const float4 r = merge_states<DV>(state, MT, TS, hl, d2, Lsum);
         const int h = hg0 + hl;
         if (S == 1) {
             const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
             *reinterpret_cast<uint32_t *>(out + (row * H_q + h) * DV + d2) =
-                pack_bf2(oa * inv, ob * inv);
+                pack_bf2(r.z * inv, r.w * inv);
             if (lse && d2 == 0)
-                lse[row * H_q + h] = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+                lse[row * H_q + h] = Lsum > 0.f ? (r.x + log2f(Lsum)) * kLn2 : -INFINITY;
         } else {
             const int64_t pi = (row * S + s) * H_q + h;
-            *reinterpret_cast<float2 *>(part_o + pi * DV + d2) = make_float2(oa, ob);
-            if (d2 == 0) part_ml[pi] = make_float2(M, Lsum);
+            *reinterpret_cast<float2 *>(part_o + pi * DV + d2) = make_float2(r.z, r.w);
+            if (d2 == 0) part_ml[pi] = make_float2(r.x, Lsum);
         }
     }
 }
@@ -313,7 +160,7 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(
 #pragma unroll
     for (int i = 0; i < PER; i += 2)
         *reinterpret_cast<uint32_t *>(orow + i) = pack_bf2(acc[i] * inv, acc[i + 1] * inv);
-    if (lse && lane == 0) lse[row * H_q + h] = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+    if (lse && lane == 0) lse[row * H_q + h] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
 }
 
 template <int DQK, int DV>

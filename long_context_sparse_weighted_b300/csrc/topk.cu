@@ -14,60 +14,13 @@
 // across the four passes.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "select_core.cuh"
 
 namespace lcsw {
 namespace {
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = kSelThreads;
 constexpr int kBins = 2048;
-
-__device__ __forceinline__ void hist_add(unsigned *hist, unsigned bin, bool on) {
-    // lanes that hit the same bin add once, by the lowest such lane
-    const unsigned act = __ballot_sync(0xffffffffu, on);
-    if (!on) return;
-    const unsigned peers = __match_any_sync(act, bin);
-    const int lane = threadIdx.x & 31;
-    if ((__ffs(peers) - 1) == lane) atomicAdd(hist + bin, __popc(peers));
-}
-
-// Among the bins, find D such that (count of bins > D) < need <= (count of
-// bins >= D).  Returns D; *above = count of bins > D.  512 threads x 4 bins.
-__device__ int find_digit(const unsigned *hist, int nbins, unsigned need, unsigned *above,
-                          int *scratch, int *res) {
-    const int tid = threadIdx.x;
-    const int per = nbins / kTopkThreads;  // 4 (11-bit) or 2 (10-bit)
-    // thread tid owns bins [tid*per, tid*per+per); suffix sums over threads run
-    // from the top, so scan thread (511 - tid)'s sums in increasing order.
-    unsigned mine = 0;
-    for (int i = 0; i < per; ++i) mine += hist[tid * per + i];
-    // exclusive scan in reversed thread order
-    const int rt = kTopkThreads - 1 - tid;
-    // scan by "rt" order: emulate with a scan over values placed at rt
-    __shared__ unsigned rev[kTopkThreads];
-    rev[rt] = mine;
-    __syncthreads();
-    int tot;
-    const unsigned before_rev = unsigned(block_exclusive_scan(int(rev[tid]), scratch, &tot));
-    // before_rev at position tid (in reversed order) = sum over reversed
-    // positions < tid = sum over threads with larger index than (511 - tid)
-    __shared__ unsigned suffix[kTopkThreads];
-    suffix[kTopkThreads - 1 - tid] = before_rev;
-    __syncthreads();
-    unsigned cum = suffix[tid];  // count in bins owned by threads > tid
-    for (int i = per - 1; i >= 0; --i) {
-        const unsigned h = hist[tid * per + i];
-        if (cum < need && cum + h >= need) {
-            res[0] = tid * per + i;
-            res[1] = int(cum);
-        }
-        cum += h;
-    }
-    __syncthreads();
-    *above = unsigned(res[1]);
-    const int d = res[0];
-    __syncthreads();
-    return d;
-}
 
 __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(
     const float *__restrict__ scores, const int32_t *__restrict__ n_valid,

@@ -14,7 +14,7 @@ from gpu_util import (assert_attn_close, assert_lse_close, assert_scores_close, 
 pytestmark = pytest.mark.gpu
 
 
-def run_decode(c, kp, append=False, corrupt_last=False):
+def run_decode(c, kp, append=False, corrupt_last=False, flags=0):
     """Upload one generated decode workload and run the fused step."""
     d = upload_case(c)
     B, G_max, k = c["B"], c["G_max"], c["k"]
@@ -26,7 +26,7 @@ def run_decode(c, kp, append=False, corrupt_last=False):
                 kp_dev[b, G - 1] = 7.0
     idx = torch.empty(B, k, dtype=torch.int32, device="cuda")
     scores = torch.empty(B, G_max, dtype=torch.float32, device="cuda")
-    kw = dict(idx_out=idx, scores_out=scores)
+    kw = dict(idx_out=idx, scores_out=scores, flags=flags)
     if append:
         kw.update(k_idx=d["k_idx"], pool_w=d["pool_w"])
     dec = lcsw.Decoder(d["q_idx"][:, 0], d["w_head"][:, 0], kp_dev, d["q"][:, 0], d["K"], d["V"],
@@ -34,7 +34,8 @@ def run_decode(c, kp, append=False, corrupt_last=False):
     out, lse = dec()
     dec.status()
     return dict(out=host_bits(out), lse=lse.cpu().numpy(), idx=idx.cpu().numpy(),
-                scores=scores.cpu().numpy(), k_pooled=host_bits(kp_dev))
+                scores=scores.cpu().numpy(), k_pooled=host_bits(kp_dev),
+                launches=dec.launches_per_call)
 
 
 def check_against_oracle(c, got, ref, exact=False):
@@ -64,6 +65,59 @@ def test_decode_workloads_shrunk(name, factor):
     ref = oracle.decode_case(c)
     got = run_decode(c, ref["k_pooled"])
     check_against_oracle(c, got, ref)
+
+
+PATHS = {"persistent": 0, "persistent_multipass_select": lcsw.FORCE_MULTIPASS_SELECT,
+         "multikernel": lcsw.FORCE_MULTIKERNEL}
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_decode_every_path_matches_oracle(path):
+    spec = synth.Spec(B=3, lengths=[40000, 9000, 123456 // 4 * 4], H_i=8, k=512, H_q=64,
+                      plant_frac=0.05, seed=205)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_decode(c, ref["k_pooled"], append=True, corrupt_last=True, flags=PATHS[path])
+    assert (got["launches"] == 1) == (path != "multikernel")
+    assert np.array_equal(got["k_pooled"], ref["k_pooled"])
+    check_against_oracle(c, got, ref)
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("G", [3000, 20000])
+def test_decode_all_scores_tied(path, G):
+    # zero indexer queries: every score is +0, so the top k are groups 0..k-1
+    spec = synth.Spec(B=1, lengths=[4 * G], H_i=4, k=300, H_q=16, seed=206)
+    c = synth.generate(spec)
+    c["q_idx"][:] = 0
+    ref = oracle.decode_case(c)
+    assert (ref["idx"][0, 0] == np.arange(300)).all()
+    got = run_decode(c, ref["k_pooled"], flags=PATHS[path])
+    assert np.array_equal(got["idx"], ref["idx"][:, 0])
+    check_against_oracle(c, got, ref, exact=True)
+
+
+def test_decode_bounded_wait_reports_timeout():
+    """A block that never arrives at a cross-block barrier: the other blocks'
+    bounded waits run out, the call returns, and the status reads TIMEOUT."""
+    spec = synth.Spec(B=1, lengths=[65536], H_i=8, k=64, H_q=16, seed=207)
+    c = synth.generate(spec)
+    d = upload_case(c)
+    kp = dev_bf16(oracle.pool_keys(c["k_idx"], c["pool_w"], c["seq_len"], 4))
+    dec = lcsw.Decoder(d["q_idx"][:, 0], d["w_head"][:, 0], kp, d["q"][:, 0], d["K"], d["V"],
+                       d["seq_len"], 4, 64, c["scale"], flags=lcsw.TEST_SKIP_ARRIVE)
+    assert dec.launches_per_call == 1
+    dec()
+    with pytest.raises(lcsw.LcswError) as ei:
+        dec.status()
+    assert ei.value.status == lcsw.ERR_TIMEOUT
+    # the context is still usable: re-zero the workspace and run normally
+    dec.ws.zero_()
+    dec.args.flags = 0
+    out, _ = dec()
+    dec.status()
+    ref = oracle.decode_case(c)
+    assert_attn_close(host_bits(out), ref["out"][:, 0])
 
 
 def test_decode_append_repools_newest_group():
