@@ -124,7 +124,8 @@ class ClockSampler:
 
     def summary(self):
         if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None,
+                    "reasons": [f"nvml unavailable: {getattr(self, 'err', '?')}"]}
         names = [n for bit, n in self.NAMES.items() if self.reasons & bit]
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}

@@ -16,7 +16,7 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "liblcsw.so")
+LIB_PATH = os.environ.get("LCSW_LIBRARY") or os.path.join(_HERE, "liblcsw.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "lcsw.h")
 
 OK, ERR_INVALID_ARG, ERR_CUDA, ERR_UNSUPPORTED, ERR_TIMEOUT, ERR_WORKSPACE = range(6)

@@ -56,14 +56,15 @@ constexpr int kFine = 65536, kCoarse = 256, kHistWords = kFine + kCoarse;
 constexpr int kChunkCap = 12288;   // scores of a block's chunk kept in shared memory
 constexpr int kSelCap = 8192;      // candidates selected in shared memory
 constexpr int kMaxK = 2048;        // selected groups per sequence
-constexpr int kCtlWords = 64;      // control words per sequence
+constexpr int kCtlWords = 32;      // control words per sequence
 constexpr int kMaxCtas = 160;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// control word indices (per sequence)
-constexpr int kFlushed = 0;
-constexpr int kBarA = 2, kBarB = 4, kBarC = 6, kBarD = 8, kBarAtt = 10;  // (count, gen) pairs
+// control words (per sequence): arrival counters of the step's sync points,
+// reset to zero by the last block to leave the kernel
+constexpr int kFlushed = 0, kCands = 1, kSlowB = 2, kSlowC = 3, kSlowD = 4, kSlowE = 5,
+              kAtt = 6, kDepart = 7, kNumCounters = 8;
 
 // shared memory map (bytes)
 constexpr int kU = 0;                                 // 128 KB union region
@@ -100,7 +101,7 @@ struct Params {
     float *scores_out;
     // workspace
     unsigned *ctl;        // [B][kCtlWords]
-    unsigned *hist;       // [B][2][kHistWords]
+    unsigned *hist;       // [B][2][kHistWords]: level 1, level 2 (zero between calls)
     unsigned *cand_key;   // [B][G_max]
     int32_t *cand_g;      // [B][G_max]
     float *gscore;        // [B][G_max] spill of scores past kChunkCap
@@ -112,15 +113,41 @@ struct Params {
     int *abort_flag;      // ws word 1
 };
 
+// ------------------------------------------------------------ phase timers -
+// Built with -DLCSW_PHASE_TIMERS, block 0 thread 0 of every block records the
+// first and last %globaltimer reading of each phase mark across blocks.
+#ifdef LCSW_PHASE_TIMERS
+__device__ unsigned long long g_phase_first[16];
+__device__ unsigned long long g_phase_last[16];
+__device__ unsigned g_dbg_max[4];
+#define DBG_MAX(i, v)                                   \
+    do {                                                \
+        if (threadIdx.x == 0) atomicMax(&g_dbg_max[i], unsigned(v)); \
+    } while (0)
+#define PHASE_MARK(i)                                                           \
+    do {                                                                        \
+        if (threadIdx.x == 0) {                                                 \
+            unsigned long long t_;                                              \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));              \
+            atomicMin(&g_phase_first[i], t_);                                   \
+            atomicMax(&g_phase_last[i], t_);                                    \
+        }                                                                       \
+    } while (0)
+#else
+#define PHASE_MARK(i) \
+    do {              \
+    } while (0)
+#define DBG_MAX(i, v) \
+    do {              \
+    } while (0)
+#endif
+
 // ------------------------------------------------------------ coherence ----
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ unsigned ld_cg(const unsigned *p) {
     unsigned v;
@@ -147,30 +174,24 @@ __device__ void raise_timeout(const Params &p, int where) {
     atomicExch(p.abort_flag, 1);
 }
 
-// Sense-reversal barrier over `n` blocks of one sequence.  All threads call
-// it.  The last arriver resets the count (and runs `on_last`) before releasing
-// the generation.  Returns false if the wait ran out or another block aborted.
-template <typename F>
-__device__ bool seq_barrier(const Params &p, unsigned *cnt, unsigned *gen, unsigned n, int where,
-                            F on_last, int *s_ok) {
+// Sync points are arrival counters: a block makes its global writes visible
+// (fence) and adds 1 without waiting for the result; a block that needs the
+// others' writes polls until the count reaches its target (bounded wait).
+__device__ __forceinline__ void arrive(unsigned *cnt) {
     __threadfence();
     __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(cnt, 1u);  // result unused: a fire-and-forget reduction
+}
+
+__device__ bool wait_count(const Params &p, const unsigned *cnt, unsigned target, int where,
+                           int *s_ok) {
     if (threadIdx.x == 0) {
         int ok = 1;
-        const unsigned g = ld_acquire(gen);
-        const unsigned arrived = atomicAdd(cnt, 1u) + 1u;
-        if (arrived == n) {
-            atomicExch(cnt, 0u);
-            on_last();
-            __threadfence();
-            st_release(gen, g + 1u);
-        } else {
-            const long long t0 = clock64();
-            while (ld_acquire(gen) == g) {
-                if (aborted(p.abort_flag)) { ok = 0; break; }
-                if (clock64() - t0 > kSpinBudget) { raise_timeout(p, where); ok = 0; break; }
-                __nanosleep(32);
-            }
+        const long long t0 = clock64();
+        while (ld_acquire(cnt) < target) {
+            if (aborted(p.abort_flag)) { ok = 0; break; }
+            if (clock64() - t0 > kSpinBudget) { raise_timeout(p, where); ok = 0; break; }
+            __nanosleep(20);
         }
         *s_ok = ok;
     }
@@ -199,6 +220,53 @@ __device__ __forceinline__ int warp_find_from_top(const unsigned *bins, unsigned
     const unsigned excl = suf - mine;  // lanes above
     const bool here = excl < need && suf >= need;
     const unsigned bal = __ballot_sync(0xffffffffu, here);
+    if (bal == 0) return -1;
+    const int src = __ffs(bal) - 1;
+    int bin = -1;
+    unsigned ab = 0;
+    if (lane == src) {
+        unsigned cum = excl;
+        for (int i = 7; i >= 0; --i) {
+            if (cum + v[i] >= need) { bin = lane * 8 + i; ab = cum; break; }
+            cum += v[i];
+        }
+    }
+    bin = __shfl_sync(0xffffffffu, bin, src);
+    *above = __shfl_sync(0xffffffffu, ab, src);
+    return bin;
+}
+
+// The same search over shared memory: 256 u32 counts, or (pairs) 128 words
+// of two 16-bit counts.
+__device__ __forceinline__ int smem_find_from_top(const unsigned *bins, unsigned need,
+                                                  unsigned *above, bool pairs) {
+    const int lane = threadIdx.x & 31;
+    unsigned v[8];
+    if (pairs) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(bins + lane * 4);
+        const unsigned w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = w[i] & 0xFFFFu;
+            v[2 * i + 1] = w[i] >> 16;
+        }
+    } else {
+        const uint4 a = *reinterpret_cast<const uint4 *>(bins + lane * 8);
+        const uint4 b = *reinterpret_cast<const uint4 *>(bins + lane * 8 + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    unsigned mine = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mine += v[i];
+    unsigned suf = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += y;
+    }
+    const unsigned excl = suf - mine;
+    const unsigned bal = __ballot_sync(0xffffffffu, excl < need && suf >= need);
     if (bal == 0) return -1;
     const int src = __ffs(bal) - 1;
     int bin = -1;
@@ -270,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     uint16_t *sq = reinterpret_cast<uint16_t *>(smem + kQ);
     constexpr int kMisc = kQ + 64 * QP * 2;
     uint16_t *newkey = reinterpret_cast<uint16_t *>(smem + kMisc);   // [64], 16-byte aligned
-    int *cta_begin = reinterpret_cast<int *>(smem + kMisc + 128);    // [kMaxCtas + 1]
+    unsigned *ccoarse = reinterpret_cast<unsigned *>(smem + kMisc + 128);  // [kCoarse]
+    int *cta_begin = reinterpret_cast<int *>(smem + kMisc + 128 + kCoarse * 4);  // [kMaxCtas + 1]
     int *offs = cta_begin + kMaxCtas + 1;                            // [kMaxCtas + 1]
     int *sv = offs + kMaxCtas + 1;                                   // scalars [64]
     int *scratch = sv + 64;                                          // [40]
@@ -278,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x, ncta = gridDim.x;
     const int B = p.B, P = p.P;
+    PHASE_MARK(0);
     if (aborted(p.abort_flag)) return;
 
     // ---- roles: blocks per sequence, proportional to its groups ------------
@@ -345,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     const int n_att = min(items, n_b);
     const bool has_items = j < n_att;
 
+    PHASE_MARK(11);
     // ---- append: pool the group the newest token completes ------------------
     int g_new = -1;
     if (p.k_idx && G_b > 0 && L_b % P == 0) g_new = G_b - 1;
@@ -398,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     }
     clear_smem(smem + kU, kUBytes);
     __syncthreads();
+    PHASE_MARK(12);
 
     // ---- phase 1: stream pooled keys, score, histogram -----------------------
     const uint16_t *kb = p.k_pooled + int64_t(b) * p.sp_b;
@@ -463,40 +535,100 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
     };
     {
+        // warp w scores tiles w, w+16, w+32, ...: two per iteration, with the
+        // next two already in flight
         int t = warp;
-        uint4 cur[4];
-        if (t < n_tiles) load_tile(t, cur);
-        for (; t < n_tiles; t += kWarps) {
-            uint4 nxt[4];
-            const bool more = t + kWarps < n_tiles;
-            if (more) load_tile(t + kWarps, nxt);
-            score_tile(t, cur);
-            if (more) {
+        uint4 c0[4], c1[4];
+        if (t < n_tiles) load_tile(t, c0);
+        if (t + kWarps < n_tiles) load_tile(t + kWarps, c1);
+        for (; t < n_tiles; t += 2 * kWarps) {
+            uint4 n0[4], n1[4];
+            const bool m0 = t + 2 * kWarps < n_tiles, m1 = t + 3 * kWarps < n_tiles;
+            if (m0) load_tile(t + 2 * kWarps, n0);
+            if (m1) load_tile(t + 3 * kWarps, n1);
+            score_tile(t, c0);
+            if (t + kWarps < n_tiles) score_tile(t + kWarps, c1);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+            for (int i = 0; i < 4; ++i) {
+                if (m0) c0[i] = n0[i];
+                if (m1) c1[i] = n1[i];
             }
         }
     }
     if (p.scores_out && j == 0)  // -inf past the last complete group: the full row
         for (int g = G_b + tid; g < p.G_max; g += kThreads) p.scores_out[seg + g] = -INFINITY;
     __syncthreads();
+    for (int cbin = warp; cbin < kCoarse; cbin += kWarps) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(h16 + cbin * 128 + lane * 4);
+        unsigned s = (w.x & 0xFFFFu) + (w.x >> 16) + (w.y & 0xFFFFu) + (w.y >> 16) +
+                     (w.z & 0xFFFFu) + (w.z >> 16) + (w.w & 0xFFFFu) + (w.w >> 16);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) ccoarse[cbin] = s;
+    }
+    __syncthreads();
+    PHASE_MARK(1);
     auto score_at = [&](int li) -> float {
         return li < kChunkCap ? sscore[li] : ld_cg_f(p.gscore + seg + g_lo + li);
     };
 
     // ---- flush histogram, lower bound from >= half of the sequence ----------
-    flush_hist(h16, hist1);
-    __threadfence();
+    // Flush only the block's m largest keys (by 16-bit prefix bin): the union
+    // over blocks of local top-m sets is a subset of all keys, so the k-th
+    // largest key it gives is still a lower bound, and with m a few times
+    // k / n_b it is usually the exact k-th -- at a few atomics per block.
+    if (warp == 0 && nloc > 0 && k_b > 0) {
+        const int m = min(nloc, 4 * ((k_b + n_b - 1) / n_b) + 8);
+        unsigned ab_c = 0, ab_f = 0;
+        const int cm = smem_find_from_top(ccoarse, unsigned(m), &ab_c, false);
+        const int fm = cm < 0 ? 0 : smem_find_from_top(h16 + cm * 128, unsigned(m) - ab_c, &ab_f, true);
+        if (lane == 0) { sv[16] = cm; sv[17] = fm; }
+    }
     __syncthreads();
+    // mode 0: add the top-m bins; 1: add the other bins; 2: zero the top-m bins
+    auto level1_bins = [&](int mode) {
+        if (nloc == 0 || k_b == 0) return;
+        const int cm = sv[16] < 0 ? 0 : sv[16], fm = sv[16] < 0 ? 0 : sv[17];
+        const int c_stop = mode == 1 ? 0 : cm;
+        for (int cbin = kCoarse - 1 - warp; cbin >= c_stop; cbin -= kWarps) {
+            if (ccoarse[cbin] == 0) continue;
+            if (mode == 1 && cbin > cm) continue;
+            const uint4 w = *reinterpret_cast<const uint4 *>(h16 + cbin * 128 + lane * 4);
+            const unsigned ws[4] = {w.x, w.y, w.z, w.w};
+            unsigned sum = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const unsigned cnt = hf ? ws[e] >> 16 : ws[e] & 0xFFFFu;
+                    const int fb = (lane * 4 + e) * 2 + hf;
+                    const bool top = cbin > cm || (cbin == cm && fb >= fm);
+                    if (cnt && top == (mode != 1)) {
+                        if (mode == 2) hist1[cbin * 256 + fb] = 0u;
+                        else atomicAdd(hist1 + cbin * 256 + fb, cnt);
+                        sum += cnt;
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0 && sum) {
+                if (mode == 2) hist1[kFine + cbin] = 0u;
+                else atomicAdd(hist1 + kFine + cbin, sum);
+            }
+        }
+    };
+    level1_bins(0);
+    arrive(ctl + kFlushed);
+    PHASE_MARK(2);
     if (tid == 0) {
-        atomicAdd(ctl + kFlushed, 1u);
         const unsigned half = unsigned(n_b + 1) / 2;
         const long long t0 = clock64();
         int ok = 1;
         while (ld_acquire(ctl + kFlushed) < half) {
             if (aborted(p.abort_flag)) { ok = 0; break; }
             if (clock64() - t0 > kSpinBudget) { raise_timeout(p, 1); ok = 0; break; }
-            __nanosleep(32);
+            __nanosleep(20);
         }
         *s_ok = ok;
     }
@@ -512,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         cp_async_commit();
     }
     __syncthreads();
+    PHASE_MARK(3);
     if (!*s_ok) { cp_async_wait<0>(); return; }
     if (warp == 0) {
         unsigned above = 0;
@@ -520,6 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     }
     __syncthreads();
     const unsigned lb_bin = unsigned(sv[3]);
+    PHASE_MARK(4);
 
     // ---- candidates: keys with prefix >= lb, ascending, to the segment ------
     {
@@ -545,11 +679,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         cp_async_wait<0>();
         return;
     }
-    if (!seq_barrier(p, ctl + kBarA, ctl + kBarA + 1, unsigned(n_b), 2,
-                     [&] { atomicExch(ctl + kFlushed, 0u); }, s_ok)) {
+    PHASE_MARK(5);
+    arrive(ctl + kCands);
+    if (!wait_count(p, ctl + kCands, unsigned(n_b), 2, s_ok)) {
         cp_async_wait<0>();
         return;
     }
+    PHASE_MARK(6);
 
     // ---- exact selection ------------------------------------------------------
     // candidate counts and segment offsets of the sequence's blocks
@@ -571,37 +707,54 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     }
     __syncthreads();
     const int n_cand = sv[4];
+    DBG_MAX(0, n_cand);
+    DBG_MAX(1, sv[3]);
     const bool fast = !p.force_slow && n_cand <= kSelCap;
     int32_t *sel_g = reinterpret_cast<int32_t *>(smem + kSelG);
     int32_t *idx_list = p.idx_out ? p.idx_out : p.idx_ws;
 
-    auto cleanup_level1 = [&]() {
-        for (int i = tid; i < nloc; i += kThreads) {
-            const unsigned bin = score_key(score_at(i)) >> 16;
-            hist1[bin] = 0u;
-            hist1[kFine + (bin >> 8)] = 0u;
-        }
-    };
-
     if (fast) {
-        cleanup_level1();  // nobody reads the level-1 histogram after barrier A
+        level1_bins(2);  // nobody reads the level-1 histogram after barrier A
+        __syncthreads();
         if (has_items) {
             unsigned *ckey = reinterpret_cast<unsigned *>(smem + kCandKey);
             int32_t *cgrp = reinterpret_cast<int32_t *>(smem + kCandG);
             unsigned *rh = reinterpret_cast<unsigned *>(smem + kRHist);
-            for (int jj = warp; jj < n_b; jj += kWarps) {
-                const int cnt = offs[jj + 1] - offs[jj];
-                const int64_t sg0 = seg + chunk_lo(jj);
-                for (int i = lane; i < cnt; i += 32) {
-                    ckey[offs[jj] + i] = ld_cg(p.cand_key + sg0 + i);
-                    cgrp[offs[jj] + i] = int32_t(ld_cg(reinterpret_cast<const unsigned *>(p.cand_g) + sg0 + i));
+            // all candidate loads of a thread are issued before any is stored, so
+            // the copy costs one L2 round trip per 8 entries a thread
+            for (int i0 = tid; i0 < n_cand; i0 += kThreads * 8) {
+                unsigned kv[8], gv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * kThreads;
+                    kv[u] = gv[u] = 0u;
+                    if (i < n_cand) {
+                        int lo = 0, hi = n_b;  // segment jj with offs[jj] <= i < offs[jj+1]
+                        while (hi - lo > 1) {
+                            const int mid = (lo + hi) >> 1;
+                            if (offs[mid] <= i) lo = mid; else hi = mid;
+                        }
+                        const int64_t src = seg + chunk_lo(lo) + (i - offs[lo]);
+                        kv[u] = ld_cg(p.cand_key + src);
+                        gv[u] = ld_cg(reinterpret_cast<const unsigned *>(p.cand_g) + src);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * kThreads;
+                    if (i < n_cand) {
+                        ckey[i] = kv[u];
+                        cgrp[i] = int32_t(gv[u]);
+                    }
                 }
             }
             __syncthreads();
+            PHASE_MARK(13);
             unsigned take_eq = 0;
             const unsigned kth = k_b > 0 ? radix_select_smem(ckey, n_cand, unsigned(k_b), rh,
                                                              scratch, sv + 8, &take_eq)
                                          : 0xFFFFFFFFu;
+            PHASE_MARK(14);
             // ordered compaction (candidates are in ascending group order)
             if (tid == 0) { sv[5] = 0; sv[6] = 0; }
             __syncthreads();
@@ -646,6 +799,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
     } else {
         // -------- exact multi-pass selection over the sequence's blocks --------
+        level1_bins(1);  // complete the level-1 histogram
+        arrive(ctl + kSlowB);
+        if (!wait_count(p, ctl + kSlowB, unsigned(n_b), 3, s_ok)) {
+            cp_async_wait<0>();
+            return;
+        }
         if (warp == 0) {
             unsigned above = 0;
             const int t1 = k_b > 0 ? hist_walk(hist1, unsigned(k_b), true, &above) : -1;
@@ -665,7 +824,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
         __syncthreads();
         flush_hist(h16, hist2);
-        if (!seq_barrier(p, ctl + kBarB, ctl + kBarB + 1, unsigned(n_b), 3, [] {}, s_ok)) {
+        arrive(ctl + kSlowC);
+        if (!wait_count(p, ctl + kSlowC, unsigned(n_b), 4, s_ok)) {
             cp_async_wait<0>();
             return;
         }
@@ -694,7 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 p.cta_cnt[2 * ncta + cta] = unsigned(teq);
             }
         }
-        if (!seq_barrier(p, ctl + kBarC, ctl + kBarC + 1, unsigned(n_b), 4, [] {}, s_ok)) {
+        arrive(ctl + kSlowD);
+        if (!wait_count(p, ctl + kSlowD, unsigned(n_b), 5, s_ok)) {
             cp_async_wait<0>();
             return;
         }
@@ -753,16 +914,25 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             if (j == 0)
                 for (int i = k_b + tid; i < p.k; i += kThreads) idx_list[int64_t(b) * p.k + i] = -1;
         }
-        // level-1 and level-2 histograms are no longer read by anyone
-        cleanup_level1();
-        for (int i = tid; i < nloc; i += kThreads) {
-            const unsigned key = score_key(score_at(i));
-            if (int(key >> 16) == t1) {
-                hist2[key & 0xFFFFu] = 0u;
-                hist2[kFine + ((key & 0xFFFFu) >> 8)] = 0u;
-            }
+        // neither histogram is read by anyone any more: zero this block's slice of
+        // the level-1 histogram, and the level-2 fine bins this block counted
+        // (still in shared memory) plus a slice of the level-2 coarse bins
+        {
+            const int w0 = int((long long)kHistWords / 4 * j / n_b) * 4;
+            const int w1 = int((long long)kHistWords / 4 * (j + 1) / n_b) * 4;
+            for (int w = w0 + tid * 4; w < w1; w += kThreads * 4)
+                *reinterpret_cast<uint4 *>(hist1 + w) = make_uint4(0, 0, 0, 0);
         }
-        if (!seq_barrier(p, ctl + kBarD, ctl + kBarD + 1, unsigned(n_b), 5, [] {}, s_ok)) {
+        for (int w = tid; w < kFine / 2; w += kThreads) {
+            const unsigned v = h16[w];
+            if (v & 0xFFFFu) hist2[2 * w] = 0u;
+            if (v >> 16) hist2[2 * w + 1] = 0u;
+        }
+        for (int cbin = int((long long)kCoarse * j / n_b) + tid;
+             cbin < int((long long)kCoarse * (j + 1) / n_b); cbin += kThreads)
+            hist2[kFine + cbin] = 0u;
+        arrive(ctl + kSlowE);
+        if (!wait_count(p, ctl + kSlowE, unsigned(n_b), 7, s_ok)) {
             cp_async_wait<0>();
             return;
         }
@@ -774,6 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         __syncthreads();
     }
 
+    PHASE_MARK(7);
     // ---- attention items -------------------------------------------------------
     if (has_items) {
         const int gps = (k_b + S_b - 1) / S_b;
@@ -831,6 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                                                  VP, P, tok0, ntok, p.scale_log2, sq, mt);
                 __syncthreads();
             }
+            PHASE_MARK(15);
             if (warp < n_aw) store_warp_state<DV>(st, state + warp * 16 * (DV + 2));
             __syncthreads();
             for (int e = tid; e < HG * (DV / 2); e += kThreads) {
@@ -855,32 +1027,60 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         cp_async_wait<0>();
     }
 
+    PHASE_MARK(8);
     // ---- combine the partial states ---------------------------------------------
     if (S_b > 1 && has_items) {
-        if (!seq_barrier(p, ctl + kBarAtt, ctl + kBarAtt + 1, unsigned(n_att), 6, [] {}, s_ok))
-            return;
+        arrive(ctl + kAtt);
+        if (!wait_count(p, ctl + kAtt, unsigned(n_att), 6, s_ok)) return;
+        PHASE_MARK(9);
         constexpr int PER = DV / 32;
+        float *fw = reinterpret_cast<float *>(smem + kState) + warp * kMaxCtas;  // split weights
         for (int h = j + n_att * warp; h < p.H_q; h += n_att * kWarps) {
+            const float2 *mlh = p.part_ml + int64_t(b) * p.S_max * p.H_q + h;
             float M = -INFINITY;
-            for (int s = 0; s < S_b; ++s) {
-                const float m = ld_cg_f(reinterpret_cast<const float *>(
-                    p.part_ml + (int64_t(b) * p.S_max + s) * p.H_q + h));
+            for (int s0 = 0; s0 < S_b; s0 += 32) {
+                const int s = s0 + lane;
+                float m = -INFINITY;
+                if (s < S_b) m = ld_cg_f(reinterpret_cast<const float *>(mlh + int64_t(s) * p.H_q));
                 M = fmaxf(M, m);
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             const float ref = M == -INFINITY ? 0.f : M;
+            float Lsum = 0.f;
+            for (int s0 = 0; s0 < S_b; s0 += 32) {
+                const int s = s0 + lane;
+                float wgt = 0.f;
+                if (s < S_b) {
+                    const float *ml = reinterpret_cast<const float *>(mlh + int64_t(s) * p.H_q);
+                    wgt = exp2f(ld_cg_f(ml) - ref);
+                    Lsum += wgt * ld_cg_f(ml + 1);
+                    fw[s] = wgt;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+            __syncwarp();
             float acc[PER];
 #pragma unroll
             for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-            float Lsum = 0.f;
-            for (int s = 0; s < S_b; ++s) {
-                const int64_t pi = (int64_t(b) * p.S_max + s) * p.H_q + h;
-                const float *ml = reinterpret_cast<const float *>(p.part_ml + pi);
-                const float f = exp2f(ld_cg_f(ml) - ref);
-                Lsum += f * ld_cg_f(ml + 1);
-                const float *po = p.part_o + pi * DV + lane * PER;
+            const float *po = p.part_o + (int64_t(b) * p.S_max * p.H_q + h) * DV + lane * PER;
+            const int64_t sstride = int64_t(p.H_q) * DV;
+            int s = 0;
+            for (; s + 8 <= S_b; s += 8) {
+                float v[8][PER];
 #pragma unroll
-                for (int i = 0; i < PER; ++i) acc[i] += f * ld_cg_f(po + i);
+                for (int u = 0; u < 8; ++u)
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) v[u][i] = ld_cg_f(po + (s + u) * sstride + i);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) acc[i] += fw[s + u] * v[u][i];
             }
+            for (; s < S_b; ++s)
+#pragma unroll
+                for (int i = 0; i < PER; ++i) acc[i] += fw[s] * ld_cg_f(po + s * sstride + i);
             const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
             uint16_t *orow = p.out + (int64_t(b) * p.H_q + h) * DV + lane * PER;
 #pragma unroll
@@ -888,7 +1088,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 *reinterpret_cast<uint32_t *>(orow + i) = pack_bf2(acc[i] * inv, acc[i + 1] * inv);
             if (p.lse && lane == 0)
                 p.lse[int64_t(b) * p.H_q + h] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+            __syncwarp();
         }
+    }
+    PHASE_MARK(10);
+    __syncthreads();
+    if (tid == 0 && atomicAdd(ctl + kDepart, 1u) == unsigned(n_b) - 1u) {
+        for (int i = 0; i < kNumCounters; ++i) ctl[i] = 0u;  // every block is done with them
     }
 }
 
@@ -906,7 +1112,7 @@ int s_max_for(int k, int P, int ncta) {
 
 template <int DQK>
 constexpr int smem_bytes() {
-    return kQ + 64 * (DQK + 8) * 2 + 128 + (2 * (kMaxCtas + 1) + 64 + 40) * 4;
+    return kQ + 64 * (DQK + 8) * 2 + 128 + kCoarse * 4 + (2 * (kMaxCtas + 1) + 64 + 40) * 4;
 }
 
 struct WsLayout {
@@ -977,6 +1183,32 @@ static cudaError_t launch_t(const Params &prm, int ncta, cudaStream_t st) {
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
+
+#ifdef LCSW_PHASE_TIMERS
+extern "C" int lcsw_debug_counters(unsigned *out, int reset) {
+    cudaDeviceSynchronize();
+    cudaMemcpyFromSymbol(out, g_dbg_max, sizeof(unsigned) * 4);
+    if (reset) {
+        unsigned z[4] = {0, 0, 0, 0};
+        cudaMemcpyToSymbol(g_dbg_max, z, sizeof z);
+    }
+    return int(cudaGetLastError());
+}
+
+extern "C" int lcsw_debug_phase_times(unsigned long long *first, unsigned long long *last,
+                                      int reset) {
+    cudaDeviceSynchronize();
+    cudaMemcpyFromSymbol(first, g_phase_first, sizeof(unsigned long long) * 16);
+    cudaMemcpyFromSymbol(last, g_phase_last, sizeof(unsigned long long) * 16);
+    if (reset) {
+        unsigned long long hi[16], lo[16];
+        for (int i = 0; i < 16; ++i) { hi[i] = ~0ull; lo[i] = 0ull; }
+        cudaMemcpyToSymbol(g_phase_first, hi, sizeof hi);
+        cudaMemcpyToSymbol(g_phase_last, lo, sizeof lo);
+    }
+    return int(cudaGetLastError());
+}
+#endif
 
 cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status,
                                 cudaStream_t st) {
