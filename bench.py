@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--copies", type=int, default=0,
+                    help="rotated input copies (0: enough to exceed 3x L2)")
     return ap.parse_args()
 
 
@@ -68,67 +70,66 @@ def alg_bytes(lengths, P, H_i, d_idx, k, H_q, d_qk, d_v):
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML during a region."""
+    """Samples SM clock and clock-event reasons during a region (nvidia-smi -lms)."""
 
-    NAMES = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-             0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
-             0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-             0x100: "display_clock_setting"}
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    FLAG_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, torch_device):
-        self.samples, self.reasons, self.ok = [], 0, False
-        self.max_mhz = None
+        import shutil
+        import torch
+        self.ok = shutil.which("nvidia-smi") is not None
+        self.proc, self.err = None, None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            import torch
-            self.h = None
-            try:
-                p = torch.cuda.get_device_properties(torch_device)
-                bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
-                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-            except Exception:
-                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-                ids = [v for v in vis.split(",") if v.strip()]
-                index = int(ids[torch_device]) if ids and ids[torch_device].isdigit() else torch_device
-                self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.nv = pynvml
-            self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # no NVML: report what we could not sample
+            p = torch.cuda.get_device_properties(torch_device)
+            self.bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except Exception as e:  # fall back to the visible-device index
+            vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+            self.bus = vis[torch_device] if vis else str(torch_device)
             self.err = repr(e)
 
-    def _run(self):
-        nv = self.nv
-        while not self._stop.is_set():
-            try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                self.reasons |= self._reasons_fn(self.h)
-            except Exception:
-                pass
-            time.sleep(0.01)
-
     def __enter__(self):
+        import subprocess
+        import tempfile
         if self.ok:
-            self._stop = threading.Event()
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+            self.tmp = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.bus, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)  # let the sampler start before the region
         return self
 
     def __exit__(self, *a):
-        if self.ok:
-            self._stop.set()
-            self._t.join()
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None,
-                    "reasons": [f"nvml unavailable: {getattr(self, 'err', '?')}"]}
-        names = [n for bit, n in self.NAMES.items() if self.reasons & bit]
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+        if not self.ok or self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.seek(0)
+        sm, smax, reasons = [], None, set()
+        for line in self.tmp.read().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except ValueError:
+                continue
+            for name, flag in zip(self.FLAG_NAMES, f[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # -------------------------------------------------------------- profiles ---
@@ -286,7 +287,7 @@ def run_lcsw(args, world, rank, local):
     B = spec.B
     L2 = torch.cuda.get_device_properties(local).L2_cache_size
     ab = alg_bytes(spec.lengths, P, spec.H_i, spec.d_idx, k, spec.H_q, spec.d_qk, spec.d_v)
-    copies = max(2, math.ceil(3 * L2 / ab))
+    copies = args.copies if args.copies > 0 else max(2, math.ceil(3 * L2 / ab))
 
     # -- build the pooled cache on the device (K1) and time it --------------
     pool_info = {}
@@ -312,7 +313,8 @@ def run_lcsw(args, world, rank, local):
     if launches == 1:
         kern_ms = time_launches(torch, decs, 200)
         kern_name, kern_bytes = "lcsw_decode_fused (persistent kernel)", ab
-        sha_files = ["decode_fused.cu", "fused.cuh", "common.cuh"]
+        sha_files = ["decode_fused.cu", "fused.cuh", "common.cuh", "attn_core.cuh",
+                     "pool_core.cuh", "select_core.cuh"]
         prof_file = f"decode_fused_{args.workload}.md"
     else:
         # multi-kernel path: the indexer scoring kernel moves ~97% of the bytes

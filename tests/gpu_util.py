@@ -47,7 +47,7 @@ def assert_scores_close(got: np.ndarray, ref: np.ndarray, rtol=SCORE_RTOL):
     assert np.array_equal(np.isfinite(got), fin), "visibility mask differs"
     assert (got[~fin] == ref[~fin]).all()
     scale = np.maximum(1.0, np.abs(np.where(fin, ref, 0.0)).max(axis=1, keepdims=True))
-    err = np.where(fin, np.abs(got.astype(np.float64) - ref), 0.0)
+    err = np.abs(np.where(fin, got, 0.0).astype(np.float64) - np.where(fin, ref, 0.0))
     worst = (err / scale).max()
     assert worst <= rtol, f"score error {worst:.3g} x row scale > {rtol}"
     return worst
