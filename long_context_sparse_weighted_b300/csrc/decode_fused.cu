@@ -1,45 +1,41 @@
-// Persistent fused decode step: [append] -> indexer scores -> top-k groups ->
-// sparse attention -> split-K combine, in one cooperative launch of one
-// thread block per SM (the DSA retrieval chain of "G2C Brief --
+// Persistent fused decode step: [append] -> indexer scores -> exact top-k
+// groups -> sparse attention -> split-K combine, in one cooperative launch of
+// one thread block per SM (the DSA retrieval chain of "G2C Brief --
 // GLM-5.3-Flash", section "DSA keeps selected global access in eleven
 // layers"; IndexPool from the reading notes, section 2).
 //
 // Work split.  Every sequence b gets a contiguous set of n_b >= 1 blocks,
 // proportional to its number of pooled groups G_b; block j of the set owns a
-// contiguous chunk of 16-group tiles.  All cross-block waits are per sequence
-// and bounded (clock64 budget; on expiry the block records LCSW_ERR_TIMEOUT in
-// the workspace status word, raises an abort flag that every other wait
-// honours, and returns).
+// contiguous chunk of 16-group tiles.  Cross-block sync points are per
+// sequence arrival counters (fence + fire-and-forget add; bounded polling).
+// On a wait that runs out the block records LCSW_ERR_TIMEOUT in the workspace
+// status word, raises an abort flag every other wait honours, and returns.
 //
 // Phase 1 (HBM stream).  Warps stream their tiles' pooled keys straight into
-// mma.sync A fragments (the k-permuted layout of index_scores.cu, one tile of
-// prefetch in flight per warp), compute the scores, keep them in shared
-// memory, and count them in a 65536-bin histogram of the top 16 bits of the
-// order-preserving score key (two 16-bit counters per shared word).  The block
+// mma.sync A fragments (the k-permuted layout of index_scores.cu, two tile
+// pairs in flight per warp), keep the scores in shared memory and count them in
+// a histogram of the top 16 bits of the order-preserving score key.  The block
 // that owns the group completed by the newest token pools it first (the exact
 // arithmetic of the pooling kernel) and scores that fresh key.
 //
-// Selection.  Each block adds its histogram to the sequence's global one, waits
-// until half of the sequence's blocks have done so, and reads a lower bound LB
-// on the k-th largest key off whatever the global histogram holds: any subset
-// of the scores has a k-th largest no larger than the full set's, so every
-// member of the true top k has its 16-bit key prefix >= LB.  The block writes
-// its keys with prefix >= LB, in ascending group order, to its segment of the
-// candidate list and arrives at barrier A.  After A, if the candidates of the
-// sequence fit in shared memory, every block that has attention work loads
-// them (in ascending group order), radix-selects the exact k-th key K*, and
-// keeps keys > K* plus the lowest-indexed keys == K* -- the exact top k,
-// ascending.  Otherwise all blocks of the sequence run the exact multi-pass
-// selection over their own scores (full level-1 histogram, a level-2
-// histogram of the low 16 bits, per-block counts for the tie rule and the
-// output offsets), with three more sequence barriers.
+// Selection.  Each block publishes its local top-m keys (by 16-bit bin, with
+// m = 2*ceil(k/n_b) + 8) in ascending group order, together with the largest
+// key it left out, and starts gathering the K/V rows of its own best
+// candidates into shared memory.  After one sync point every block loads the
+// union of candidates and selects the exact k-th key K* (a histogram relative
+// to the smallest published bin, then a rank count inside the threshold bin).
+// If K* exceeds every left-out key, the union holds the true top k and the
+// selection is exact; every block then knows which of its own groups are
+// selected.  Otherwise (keys clustered in one block, or too many candidates)
+// all blocks of the sequence run the exact multi-pass selection over their own
+// scores: full level-1 histogram, level-2 histogram of the low 16 bits,
+// per-block counts for the tie rule and the output order.
 //
-// Attention.  The selected groups are split into S_b slices of >= 64 tokens
-// (x head groups of 64 heads); slice items go round-robin to the sequence's
-// blocks, which gather K/V rows with cp.async into double-buffered shared
-// memory and run the mma.sync online-softmax tile of attn_core.cuh.  With
-// S_b > 1 the partial (m, l, o) states meet at a sequence barrier and the
-// participating blocks each merge a subset of the heads.
+// Attention.  Each block attends over its own selected groups -- already in
+// shared memory when they were among its prefetched candidates -- with the
+// mma.sync online-softmax tile of attn_core.cuh, writes its partial (m, l, o)
+// per head, and after a second sync point the blocks merge the partial states
+// head by head.
 #include "attn_core.cuh"
 #include "common.cuh"
 #include "fused.cuh"
@@ -54,7 +50,11 @@ constexpr int kThreads = kSelThreads;  // 512
 constexpr int kWarps = kThreads / 32;
 constexpr int kFine = 65536, kCoarse = 256, kHistWords = kFine + kCoarse;
 constexpr int kChunkCap = 12288;   // scores of a block's chunk kept in shared memory
-constexpr int kSelCap = 8192;      // candidates selected in shared memory
+constexpr int kSelCap = 4096;      // candidates selected in shared memory (fast path)
+constexpr int kSlot = 24;          // candidates published in a block's fixed slot
+constexpr int kSlotBytes = 16 + kSlot * 8;
+constexpr int kSpecTok = 64;       // tokens of own candidates prefetched into shared memory
+constexpr int kTieCap = 256;       // threshold-bin candidates resolved by rank counting
 constexpr int kMaxK = 2048;        // selected groups per sequence
 constexpr int kCtlWords = 32;      // control words per sequence
 constexpr int kMaxCtas = 160;
@@ -63,20 +63,27 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // control words (per sequence): arrival counters of the step's sync points,
 // reset to zero by the last block to leave the kernel
-constexpr int kFlushed = 0, kCands = 1, kSlowB = 2, kSlowC = 3, kSlowD = 4, kSlowE = 5,
-              kAtt = 6, kDepart = 7, kNumCounters = 8;
+constexpr int kCands = 0, kSlowB = 1, kSlowC = 2, kSlowD = 3, kAtt = 4, kDepart = 5,
+              kNumCounters = 6;
 
-// shared memory map (bytes)
-constexpr int kU = 0;                                 // 128 KB union region
-constexpr int kUBytes = kFine * 2;                    // 16-bit counters
-constexpr int kSelG = kU;                             // selected groups [kMaxK]
-constexpr int kCandKey = kU + kMaxK * 4;              // [kSelCap]
-constexpr int kCandG = kCandKey + kSelCap * 4;        // [kSelCap]
-constexpr int kRHist = kCandG + kSelCap * 4;          // [2048]
-constexpr int kKV = kU + kMaxK * 4;                   // attention K/V buffers
-constexpr int kState = kU + kMaxK * 4;                // merge state (after the chunks)
+// shared memory map (bytes); region U is reused phase by phase
+constexpr int kU = 0;
+constexpr int kUBytes = kFine * 2;                    // phase 1: 16-bit-pair histogram
+constexpr int kSpec = kU;                             // prefetched own K/V [64 tok]
+constexpr int kSpecBytes = kSpecTok * (192 + 8 + 128 + 8) * 2;
+constexpr int kStage = kSpec + kSpecBytes;            // published slots [n_b][kSlotBytes]
+constexpr int kCKey = kStage + kMaxCtas * kSlotBytes; // candidate keys [kSelCap]
+constexpr int kCG = kCKey + kSelCap * 4;              // candidate groups [kSelCap]
+constexpr int kSelHist = kCG + kSelCap * 4;           // [2048]
+constexpr int kTie = kSelHist + 2048 * 4;             // [kTieCap] (key, index)
+constexpr int kState = kSpec + kSpecBytes;            // merge state (after compute)
+constexpr int kGather = kU;                           // gathered chunks (no prefetch hit)
+constexpr int kSelG = kU + kUBytes - kMaxK * 4;       // own selected groups [kMaxK]
 constexpr int kScores = kU + kUBytes;                 // [kChunkCap] floats
 constexpr int kQ = kScores + kChunkCap * 4;           // Q tile [64][QP]
+static_assert(kTie + kTieCap * 8 <= kSelG, "shared-memory map overlap");
+static_assert(kState + 8 * 16 * (128 + 2) * 4 <= kSelG, "merge state overlap");
+static_assert(kGather + 2 * kChunk * (192 + 8 + 128 + 8) * 2 <= kSelG, "gather overlap");
 
 struct Params {
     const uint16_t *q_idx;
@@ -93,7 +100,7 @@ struct Params {
     const uint16_t *V;
     int64_t sV_b;
     const int32_t *seq_len;
-    int B, G_max, H_i, P, k, H_q, S_max, force_slow, skip_arrive;
+    int B, G_max, H_i, P, k, H_q, force_slow, skip_arrive;
     float scale_log2;
     uint16_t *out;
     float *lse;
@@ -102,13 +109,14 @@ struct Params {
     // workspace
     unsigned *ctl;        // [B][kCtlWords]
     unsigned *hist;       // [B][2][kHistWords]: level 1, level 2 (zero between calls)
-    unsigned *cand_key;   // [B][G_max]
+    unsigned char *slots; // [ncta][kSlotBytes]: count, max left-out key, bin, -, entries
+    unsigned *cand_key;   // [B][G_max] candidates past a slot's capacity
     int32_t *cand_g;      // [B][G_max]
     float *gscore;        // [B][G_max] spill of scores past kChunkCap
-    unsigned *cta_cnt;    // [3][ncta]: candidate count, > K*, == K*
+    unsigned *cta_cnt;    // [2][ncta]: keys > K*, keys == K* (exact path)
     int32_t *idx_ws;      // [B][k]
-    float *part_o;        // [B][S_max][H_q][d_v]
-    float2 *part_ml;      // [B][S_max][H_q]
+    float *part_o;        // [ncta][H_q][d_v]
+    float2 *part_ml;      // [ncta][H_q]
     int *status;          // ws word 0
     int *abort_flag;      // ws word 1
 };
@@ -117,21 +125,15 @@ struct Params {
 // Built with -DLCSW_PHASE_TIMERS, block 0 thread 0 of every block records the
 // first and last %globaltimer reading of each phase mark across blocks.
 #ifdef LCSW_PHASE_TIMERS
-__device__ unsigned long long g_phase_first[16];
-__device__ unsigned long long g_phase_last[16];
+__device__ long long g_stamp[160][40];
 __device__ unsigned g_dbg_max[4];
-#define DBG_MAX(i, v)                                   \
-    do {                                                \
-        if (threadIdx.x == 0) atomicMax(&g_dbg_max[i], unsigned(v)); \
+#define DBG_MAX(i, v)                                                    \
+    do {                                                                 \
+        if (threadIdx.x == 0) atomicMax(&g_dbg_max[i], unsigned(v));     \
     } while (0)
-#define PHASE_MARK(i)                                                           \
-    do {                                                                        \
-        if (threadIdx.x == 0) {                                                 \
-            unsigned long long t_;                                              \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));              \
-            atomicMin(&g_phase_first[i], t_);                                   \
-            atomicMax(&g_phase_last[i], t_);                                    \
-        }                                                                       \
+#define PHASE_MARK(i)                                                    \
+    do {                                                                 \
+        if (threadIdx.x == 0) g_stamp[blockIdx.x][i] = clock64();        \
     } while (0)
 #else
 #define PHASE_MARK(i) \
@@ -157,6 +159,18 @@ __device__ __forceinline__ unsigned ld_cg(const unsigned *p) {
 __device__ __forceinline__ float ld_cg_f(const float *p) {
     float v;
     asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float2 ld_cg_f2(const float2 *p) {
+    float2 v;
+    asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float4 ld_cg_f4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
     return v;
 }
 __device__ __forceinline__ uint4 ld_cg4(const void *p) {
@@ -332,17 +346,21 @@ __device__ __forceinline__ void clear_smem(unsigned char *base, int bytes) {
 template <int NT, int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params p) {
     extern __shared__ __align__(1024) unsigned char smem[];
+    constexpr int QP = DQK + 8, VP = DV + 8;
     unsigned *h16 = reinterpret_cast<unsigned *>(smem + kU);
     float *sscore = reinterpret_cast<float *>(smem + kScores);
-    constexpr int QP = DQK + 8, VP = DV + 8;
     uint16_t *sq = reinterpret_cast<uint16_t *>(smem + kQ);
     constexpr int kMisc = kQ + 64 * QP * 2;
-    uint16_t *newkey = reinterpret_cast<uint16_t *>(smem + kMisc);   // [64], 16-byte aligned
-    unsigned *ccoarse = reinterpret_cast<unsigned *>(smem + kMisc + 128);  // [kCoarse]
-    int *cta_begin = reinterpret_cast<int *>(smem + kMisc + 128 + kCoarse * 4);  // [kMaxCtas + 1]
-    int *offs = cta_begin + kMaxCtas + 1;                            // [kMaxCtas + 1]
-    int *sv = offs + kMaxCtas + 1;                                   // scalars [64]
-    int *scratch = sv + 64;                                          // [40]
+    uint16_t *newkey = reinterpret_cast<uint16_t *>(smem + kMisc);            // [64]
+    unsigned *ccoarse = reinterpret_cast<unsigned *>(smem + kMisc + 128);     // [kCoarse]
+    int *cta_begin = reinterpret_cast<int *>(ccoarse + kCoarse);              // [kMaxCtas + 1]
+    int *offs = cta_begin + kMaxCtas + 1;                                     // [kMaxCtas + 1]
+    int *lens = offs + kMaxCtas + 1;                                          // [kMaxCtas]
+    int *spec_g = lens + kMaxCtas;                                            // [kSpecTok]
+    int *spec_sg = spec_g + kSpecTok;                                         // [kSpecTok]
+    int *sv = spec_sg + kSpecTok;                                             // scalars [64]
+    int *scratch = sv + 64;                                                   // [40]
+    float *sred = reinterpret_cast<float *>(scratch + 40);                    // [64]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x, ncta = gridDim.x;
@@ -350,51 +368,35 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     PHASE_MARK(0);
     if (aborted(p.abort_flag)) return;
 
-    // ---- roles: blocks per sequence, proportional to its groups ------------
-    if (warp == 0) {
-        // prefix sums of G_b over b (B <= ncta <= kMaxCtas), 5 per lane
-        unsigned run = 0;
-        for (int base = 0; base < B; base += 32) {
-            const int b = base + lane;
-            unsigned g = 0;
-            if (b < B) {
-                int G = __ldg(p.seq_len + b) / P;
-                G = G < 0 ? 0 : (G > p.G_max ? p.G_max : G);
-                g = unsigned(G);
-            }
-            unsigned x = g;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if (b < B) offs[b] = int(run + x - g);  // exclusive prefix
-            run += __shfl_sync(0xffffffffu, x, 31);
+    // ---- roles: blocks per sequence, proportional to its groups --------------
+    {
+        int gv = 0;
+        if (tid < B) {
+            const int L = __ldg(p.seq_len + tid);
+            lens[tid] = L;
+            int G = L / P;
+            gv = G < 0 ? 0 : (G > p.G_max ? p.G_max : G);
         }
-        if (lane == 0) sv[0] = int(run);
-    }
-    __syncthreads();
-    {
-        const long long total = sv[0] > 0 ? sv[0] : 1;
-        const long long R = ncta - B;
-        for (int b = tid; b <= B; b += kThreads)
-            cta_begin[b] = b == B ? ncta : b + int(R * (long long)offs[b] / total);
-    }
-    __syncthreads();
-    int b = 0;
-    {
-        // largest b with cta_begin[b] <= cta
-        for (int i = tid; i < B; i += kThreads)
-            if (cta_begin[i] <= cta && cta < cta_begin[i + 1]) sv[1] = i;
+        clear_smem(smem + kU, kUBytes);  // overlaps the length load
+        int total;
+        const int pre = block_exclusive_scan(gv, scratch, &total);
+        if (tid < B) offs[tid] = pre;
+        if (tid == 0) { offs[B] = total; sv[0] = total; }
         __syncthreads();
-        b = sv[1];
+        const long long tot = total > 0 ? total : 1;
+        for (int bb = tid; bb <= B; bb += kThreads)
+            cta_begin[bb] = bb == B ? ncta : bb + int((long long)(ncta - B) * offs[bb] / tot);
+        __syncthreads();
+        for (int bb = tid; bb < B; bb += kThreads)
+            if (cta_begin[bb] <= cta && cta < cta_begin[bb + 1]) sv[1] = bb;
+        __syncthreads();
     }
+    const int b = sv[1];
     const int cb0 = cta_begin[b];
     const int n_b = cta_begin[b + 1] - cb0;
     const int j = cta - cb0;
-    const int L_b = __ldg(p.seq_len + b);
-    int G_b = L_b / P;
-    G_b = G_b < 0 ? 0 : (G_b > p.G_max ? p.G_max : G_b);
+    const int L_b = lens[b];
+    const int G_b = offs[b + 1] - offs[b];
     const int tiles_b = (G_b + 15) / 16;
     auto chunk_lo = [&](int jj) { return 16 * int((long long)tiles_b * jj / n_b); };
     const int g_lo = chunk_lo(j);
@@ -405,22 +407,58 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     unsigned *hist1 = p.hist + size_t(b) * 2 * kHistWords;
     unsigned *hist2 = hist1 + kHistWords;
     const int64_t seg = int64_t(b) * p.G_max;
+    const uint16_t *Kb = p.K + int64_t(b) * p.sK_b;
+    const uint16_t *Vb = p.V + int64_t(b) * p.sV_b;
     int *s_ok = sv + 2;
+    PHASE_MARK(1);
 
-    // attention items of this sequence
-    const int HGs = (p.H_q + 63) / 64;
-    int S_b = (k_b * P + kChunk - 1) / kChunk;
-    S_b = max(1, min(S_b, min(n_b, p.S_max)));
-    const int items = S_b * HGs;
-    const int n_att = min(items, n_b);
-    const bool has_items = j < n_att;
+    // ---- phase-1 prologue: first tiles, indexer query, append ----------------
+    const int r = lane >> 2, c = lane & 3;
+    const uint16_t *kb = p.k_pooled + int64_t(b) * p.sp_b;
+    const int n_tiles = (nloc + 15) / 16;
+    auto load_tile = [&](int t, uint4 (&A)[4]) {
+        const int ga = g_lo + t * 16 + r, gb = ga + 8;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        A[0] = A[1] = A[2] = A[3] = z;
+        if (ga < g_hi) {
+            A[0] = ld_stream16(kb + int64_t(ga) * 64 + 8 * c);
+            A[1] = ld_stream16(kb + int64_t(ga) * 64 + 32 + 8 * c);
+        }
+        if (gb < g_hi) {
+            A[2] = ld_stream16(kb + int64_t(gb) * 64 + 8 * c);
+            A[3] = ld_stream16(kb + int64_t(gb) * 64 + 32 + 8 * c);
+        }
+    };
+    uint4 c0[4], c1[4];
+    if (warp < n_tiles) load_tile(warp, c0);
+    if (warp + kWarps < n_tiles) load_tile(warp + kWarps, c1);
 
-    PHASE_MARK(11);
-    // ---- append: pool the group the newest token completes ------------------
+    uint32_t bq[NT][4][2];
+    float wv[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int head = nt * 8 + r;
+        uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+        if (head < p.H_i) {
+            const uint16_t *qp = p.q_idx + (int64_t(b) * p.H_i + head) * 64;
+            h0 = ld_nc16(qp + 8 * c);
+            h1 = ld_nc16(qp + 32 + 8 * c);
+        }
+        bq[nt][0][0] = h0.x; bq[nt][0][1] = h0.y;
+        bq[nt][1][0] = h0.z; bq[nt][1][1] = h0.w;
+        bq[nt][2][0] = h1.x; bq[nt][2][1] = h1.y;
+        bq[nt][3][0] = h1.z; bq[nt][3][1] = h1.w;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = nt * 8 + 2 * c + e;
+            wv[nt][e] = h < p.H_i ? __ldg(p.w_head + int64_t(b) * p.H_i + h) : 0.f;
+        }
+    }
+
+    // append: the block owning the group the newest token completes pools it
     int g_new = -1;
     if (p.k_idx && G_b > 0 && L_b % P == 0) g_new = G_b - 1;
-    const bool own_new = g_new >= g_lo && g_new < g_hi;
-    if (own_new && tid < 8) {
+    if (g_new >= g_lo && g_new < g_hi && tid < 8) {
         const uint16_t *src = p.k_idx + int64_t(b) * p.sk_b + int64_t(g_new) * P * 64 + tid * 8;
         const float *wp = p.pool_w + int64_t(b) * p.sw_b + int64_t(g_new) * P;
         uint4 o;
@@ -443,61 +481,20 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         *reinterpret_cast<uint4 *>(p.k_pooled + int64_t(b) * p.sp_b + int64_t(g_new) * 64 +
                                    tid * 8) = o;
     }
-
-    // ---- query fragments of the indexer ------------------------------------
-    const int r = lane >> 2, c = lane & 3;
-    uint32_t bq[NT][4][2];
-    float wv[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int head = nt * 8 + r;
-        uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
-        if (head < p.H_i) {
-            const uint16_t *qp = p.q_idx + (int64_t(b) * p.H_i + head) * 64;
-            h0 = ld_nc16(qp + 8 * c);
-            h1 = ld_nc16(qp + 32 + 8 * c);
-        }
-        bq[nt][0][0] = h0.x; bq[nt][0][1] = h0.y;
-        bq[nt][1][0] = h0.z; bq[nt][1][1] = h0.w;
-        bq[nt][2][0] = h1.x; bq[nt][2][1] = h1.y;
-        bq[nt][3][0] = h1.z; bq[nt][3][1] = h1.w;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int h = nt * 8 + 2 * c + e;
-            wv[nt][e] = h < p.H_i ? __ldg(p.w_head + int64_t(b) * p.H_i + h) : 0.f;
-        }
-    }
-    clear_smem(smem + kU, kUBytes);
     __syncthreads();
-    PHASE_MARK(12);
+    PHASE_MARK(2);
 
-    // ---- phase 1: stream pooled keys, score, histogram -----------------------
-    const uint16_t *kb = p.k_pooled + int64_t(b) * p.sp_b;
-    const int n_tiles = (nloc + 15) / 16;
-    auto load_tile = [&](int t, uint4 (&A)[4]) {
+    // ---- phase 1: stream pooled keys, score, histogram -------------------------
+    auto score_tile = [&](int t, uint4 (&A)[4]) {
         const int ga = g_lo + t * 16 + r, gb = ga + 8;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        A[0] = A[1] = A[2] = A[3] = z;
-        if (ga < g_hi) {
-            if (ga == g_new) {
-                A[0] = *reinterpret_cast<const uint4 *>(newkey + 8 * c);
-                A[1] = *reinterpret_cast<const uint4 *>(newkey + 32 + 8 * c);
-            } else {
-                A[0] = ld_stream16(kb + int64_t(ga) * 64 + 8 * c);
-                A[1] = ld_stream16(kb + int64_t(ga) * 64 + 32 + 8 * c);
-            }
+        if (ga == g_new) {  // the freshly pooled key replaces the stale cache row
+            A[0] = *reinterpret_cast<const uint4 *>(newkey + 8 * c);
+            A[1] = *reinterpret_cast<const uint4 *>(newkey + 32 + 8 * c);
         }
-        if (gb < g_hi) {
-            if (gb == g_new) {
-                A[2] = *reinterpret_cast<const uint4 *>(newkey + 8 * c);
-                A[3] = *reinterpret_cast<const uint4 *>(newkey + 32 + 8 * c);
-            } else {
-                A[2] = ld_stream16(kb + int64_t(gb) * 64 + 8 * c);
-                A[3] = ld_stream16(kb + int64_t(gb) * 64 + 32 + 8 * c);
-            }
+        if (gb == g_new) {
+            A[2] = *reinterpret_cast<const uint4 *>(newkey + 8 * c);
+            A[3] = *reinterpret_cast<const uint4 *>(newkey + 32 + 8 * c);
         }
-    };
-    auto score_tile = [&](int t, const uint4 (&A)[4]) {
         const uint32_t A0[4] = {A[0].x, A[0].z, A[1].x, A[1].z};
         const uint32_t A2[4] = {A[0].y, A[0].w, A[1].y, A[1].w};
         const uint32_t A1[4] = {A[2].x, A[2].z, A[3].x, A[3].z};
@@ -534,166 +531,176 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             }
         }
     };
-    {
-        // warp w scores tiles w, w+16, w+32, ...: two per iteration, with the
-        // next two already in flight
-        int t = warp;
-        uint4 c0[4], c1[4];
-        if (t < n_tiles) load_tile(t, c0);
-        if (t + kWarps < n_tiles) load_tile(t + kWarps, c1);
-        for (; t < n_tiles; t += 2 * kWarps) {
-            uint4 n0[4], n1[4];
-            const bool m0 = t + 2 * kWarps < n_tiles, m1 = t + 3 * kWarps < n_tiles;
-            if (m0) load_tile(t + 2 * kWarps, n0);
-            if (m1) load_tile(t + 3 * kWarps, n1);
-            score_tile(t, c0);
-            if (t + kWarps < n_tiles) score_tile(t + kWarps, c1);
+    for (int t = warp; t < n_tiles; t += 2 * kWarps) {
+        uint4 n0[4], n1[4];
+        const bool m0 = t + 2 * kWarps < n_tiles, m1 = t + 3 * kWarps < n_tiles;
+        if (m0) load_tile(t + 2 * kWarps, n0);
+        if (m1) load_tile(t + 3 * kWarps, n1);
+        score_tile(t, c0);
+        if (t + kWarps < n_tiles) score_tile(t + kWarps, c1);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (m0) c0[i] = n0[i];
-                if (m1) c1[i] = n1[i];
-            }
+        for (int i = 0; i < 4; ++i) {
+            if (m0) c0[i] = n0[i];
+            if (m1) c1[i] = n1[i];
         }
     }
     if (p.scores_out && j == 0)  // -inf past the last complete group: the full row
         for (int g = G_b + tid; g < p.G_max; g += kThreads) p.scores_out[seg + g] = -INFINITY;
     __syncthreads();
-    for (int cbin = warp; cbin < kCoarse; cbin += kWarps) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(h16 + cbin * 128 + lane * 4);
-        unsigned s = (w.x & 0xFFFFu) + (w.x >> 16) + (w.y & 0xFFFFu) + (w.y >> 16) +
-                     (w.z & 0xFFFFu) + (w.z >> 16) + (w.w & 0xFFFFu) + (w.w >> 16);
+    auto coarse_from_fine = [&]() {
+        for (int cbin = warp; cbin < kCoarse; cbin += kWarps) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(h16 + cbin * 128 + lane * 4);
+            unsigned s = (w.x & 0xFFFFu) + (w.x >> 16) + (w.y & 0xFFFFu) + (w.y >> 16) +
+                         (w.z & 0xFFFFu) + (w.z >> 16) + (w.w & 0xFFFFu) + (w.w >> 16);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) ccoarse[cbin] = s;
-    }
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) ccoarse[cbin] = s;
+        }
+    };
+    coarse_from_fine();
     __syncthreads();
-    PHASE_MARK(1);
+    PHASE_MARK(3);
     auto score_at = [&](int li) -> float {
         return li < kChunkCap ? sscore[li] : ld_cg_f(p.gscore + seg + g_lo + li);
     };
 
-    // ---- flush histogram, lower bound from >= half of the sequence ----------
-    // Flush only the block's m largest keys (by 16-bit prefix bin): the union
-    // over blocks of local top-m sets is a subset of all keys, so the k-th
-    // largest key it gives is still a lower bound, and with m a few times
-    // k / n_b it is usually the exact k-th -- at a few atomics per block.
-    if (warp == 0 && nloc > 0 && k_b > 0) {
-        const int m = min(nloc, 4 * ((k_b + n_b - 1) / n_b) + 8);
-        unsigned ab_c = 0, ab_f = 0;
-        const int cm = smem_find_from_top(ccoarse, unsigned(m), &ab_c, false);
-        const int fm = cm < 0 ? 0 : smem_find_from_top(h16 + cm * 128, unsigned(m) - ab_c, &ab_f, true);
-        if (lane == 0) { sv[16] = cm; sv[17] = fm; }
+    // ---- local candidates: the block's top-m keys by 16-bit bin -----------------
+    const int spec_cap = kSpecTok / P;
+    if (warp == 0) {
+        int pj = kFine, p2 = kFine;  // bins >= pj are published; >= p2 prefetched
+        if (nloc > 0 && k_b > 0) {
+            const int m = min(nloc, 2 * ((k_b + n_b - 1) / n_b) + 8);
+            unsigned ab_c = 0, ab_f = 0;
+            const int cm = smem_find_from_top(ccoarse, unsigned(m), &ab_c, false);
+            const int fm = smem_find_from_top(h16 + cm * 128, unsigned(m) - ab_c, &ab_f, true);
+            pj = cm * 256 + fm;
+            const unsigned binv = (h16[pj >> 1] >> ((pj & 1) * 16)) & 0xFFFFu;
+            const unsigned cnt = ab_c + ab_f + binv;  // keys at or above bin pj
+            p2 = pj;
+            if (cnt > unsigned(spec_cap)) {
+                unsigned a2 = 0, f2 = 0;
+                const int c2 = smem_find_from_top(ccoarse, unsigned(spec_cap), &a2, false);
+                const int ff = smem_find_from_top(h16 + c2 * 128, unsigned(spec_cap) - a2, &f2, true);
+                p2 = c2 * 256 + ff;
+            }
+        }
+        if (lane == 0) { sv[3] = pj; sv[4] = p2; }
     }
     __syncthreads();
-    // mode 0: add the top-m bins; 1: add the other bins; 2: zero the top-m bins
-    auto level1_bins = [&](int mode) {
-        if (nloc == 0 || k_b == 0) return;
-        const int cm = sv[16] < 0 ? 0 : sv[16], fm = sv[16] < 0 ? 0 : sv[17];
-        const int c_stop = mode == 1 ? 0 : cm;
-        for (int cbin = kCoarse - 1 - warp; cbin >= c_stop; cbin -= kWarps) {
-            if (ccoarse[cbin] == 0) continue;
-            if (mode == 1 && cbin > cm) continue;
-            const uint4 w = *reinterpret_cast<const uint4 *>(h16 + cbin * 128 + lane * 4);
-            const unsigned ws[4] = {w.x, w.y, w.z, w.w};
-            unsigned sum = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const unsigned cnt = hf ? ws[e] >> 16 : ws[e] & 0xFFFFu;
-                    const int fb = (lane * 4 + e) * 2 + hf;
-                    const bool top = cbin > cm || (cbin == cm && fb >= fm);
-                    if (cnt && top == (mode != 1)) {
-                        if (mode == 2) hist1[cbin * 256 + fb] = 0u;
-                        else atomicAdd(hist1 + cbin * 256 + fb, cnt);
-                        sum += cnt;
-                    }
+    PHASE_MARK(4);
+    {
+        const unsigned pj = unsigned(sv[3]), p2 = unsigned(sv[4]);
+        const int per = (nloc + kThreads - 1) / kThreads;
+        const int i0 = min(nloc, tid * per), i1 = min(nloc, i0 + per);
+        int nc = 0, ns = 0;
+        unsigned maxex = 0;
+        for (int i = i0; i < i1; ++i) {
+            const unsigned key = score_key(score_at(i));
+            if ((key >> 16) >= pj) {
+                ++nc;
+                ns += (key >> 16) >= p2;
+            } else {
+                maxex = max(maxex, key);
+            }
+        }
+        int tot_s;
+        const unsigned packed = unsigned(block_exclusive_scan(nc | (ns << 16), scratch, &tot_s));
+        const unsigned tot = unsigned(tot_s);  // low half: candidates, high half: prefetched
+        int pos = int(packed & 0xFFFFu), spos = int(packed >> 16);
+        unsigned char *slot = p.slots + size_t(cta) * kSlotBytes;
+        unsigned *ent = reinterpret_cast<unsigned *>(slot + 16);
+        for (int i = i0; i < i1; ++i) {
+            const unsigned key = score_key(score_at(i));
+            if ((key >> 16) >= pj) {
+                if (pos < kSlot) {
+                    ent[2 * pos] = key;
+                    ent[2 * pos + 1] = unsigned(g_lo + i);
+                } else {
+                    p.cand_key[seg + g_lo + pos - kSlot] = key;
+                    p.cand_g[seg + g_lo + pos - kSlot] = g_lo + i;
+                }
+                ++pos;
+                if ((key >> 16) >= p2) {
+                    if (spos < spec_cap) spec_g[spos] = g_lo + i;
+                    ++spos;
                 }
             }
+        }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            if (lane == 0 && sum) {
-                if (mode == 2) hist1[kFine + cbin] = 0u;
-                else atomicAdd(hist1 + kFine + cbin, sum);
-            }
+        for (int o = 16; o > 0; o >>= 1) maxex = max(maxex, __shfl_xor_sync(0xffffffffu, maxex, o));
+        if (lane == 0) scratch[warp] = int(maxex);
+        __syncthreads();
+        if (tid == 0) {
+            unsigned mx = 0;
+            for (int w = 0; w < kWarps; ++w) mx = max(mx, unsigned(scratch[w]));
+            *reinterpret_cast<uint4 *>(slot) = make_uint4(tot & 0xFFFFu, mx, pj, 0u);
+            sv[5] = min(int(tot >> 16), spec_cap);  // prefetched groups
         }
-    };
-    level1_bins(0);
-    arrive(ctl + kFlushed);
-    PHASE_MARK(2);
-    if (tid == 0) {
-        const unsigned half = unsigned(n_b + 1) / 2;
-        const long long t0 = clock64();
-        int ok = 1;
-        while (ld_acquire(ctl + kFlushed) < half) {
-            if (aborted(p.abort_flag)) { ok = 0; break; }
-            if (clock64() - t0 > kSpinBudget) { raise_timeout(p, 1); ok = 0; break; }
-            __nanosleep(20);
-        }
-        *s_ok = ok;
     }
-    // Q tile of the first attention item (prefetch; waited before attention)
-    if (has_items && S_b * HGs > 0) {
-        const int hg = (j % items) / S_b;
-        const int h0 = hg * 64, HG = min(64, p.H_q - h0);
-        const uint16_t *qrow = p.q + (int64_t(b) * p.H_q + h0) * DQK;
-        for (int e = tid; e < HG * (DQK / 8); e += kThreads) {
+    __syncthreads();
+    PHASE_MARK(5);
+    // prefetch this block's best candidates' K/V and the first head group's Q
+    const int n_spec = sv[5];
+    uint16_t *spk = reinterpret_cast<uint16_t *>(smem + kSpec);
+    uint16_t *spv = spk + kChunk * QP;
+    gather_chunk<DQK, DV>(spk, spv, spec_sg, spec_g, n_spec, P, G_b, Kb, Vb, QP, VP, tid, kThreads);
+    {
+        const int HG0 = min(64, p.H_q);
+        const uint16_t *qrow = p.q + int64_t(b) * p.H_q * DQK;
+        for (int e = tid; e < HG0 * (DQK / 8); e += kThreads) {
             const int h = e / (DQK / 8), c8 = e % (DQK / 8);
             cp_async16(smem_u32(sq + h * QP + c8 * 8), qrow + int64_t(h) * DQK + c8 * 8, 16);
         }
         cp_async_commit();
     }
-    __syncthreads();
-    PHASE_MARK(3);
-    if (!*s_ok) { cp_async_wait<0>(); return; }
-    if (warp == 0) {
-        unsigned above = 0;
-        int lb = hist_walk(hist1, unsigned(k_b), false, &above);
-        if (lane == 0) sv[3] = lb < 0 ? 0 : lb;
-    }
-    __syncthreads();
-    const unsigned lb_bin = unsigned(sv[3]);
-    PHASE_MARK(4);
-
-    // ---- candidates: keys with prefix >= lb, ascending, to the segment ------
-    {
-        const int per = (nloc + kThreads - 1) / kThreads;
-        const int i0 = min(nloc, tid * per), i1 = min(nloc, i0 + per);
-        int cnt = 0;
-        for (int i = i0; i < i1; ++i) cnt += (score_key(score_at(i)) >> 16) >= lb_bin;
-        int total;
-        int pos = block_exclusive_scan(cnt, scratch, &total);
-        unsigned *ck = p.cand_key + seg + g_lo;
-        int32_t *cg = p.cand_g + seg + g_lo;
-        for (int i = i0; i < i1; ++i) {
-            const unsigned key = score_key(score_at(i));
-            if ((key >> 16) >= lb_bin) {
-                ck[pos] = key;
-                cg[pos] = g_lo + i;
-                ++pos;
-            }
-        }
-        if (tid == 0) p.cta_cnt[cta] = unsigned(total);
-    }
+    PHASE_MARK(6);
     if (p.skip_arrive && j == n_b - 1 && n_b > 1) {  // failure-detection test only
         cp_async_wait<0>();
         return;
     }
-    PHASE_MARK(5);
     arrive(ctl + kCands);
+    PHASE_MARK(7);
+
+    // ---- selection: exact top k from the published candidates -----------------
     if (!wait_count(p, ctl + kCands, unsigned(n_b), 2, s_ok)) {
         cp_async_wait<0>();
         return;
     }
-    PHASE_MARK(6);
-
-    // ---- exact selection ------------------------------------------------------
-    // candidate counts and segment offsets of the sequence's blocks
+    PHASE_MARK(8);
+    unsigned char *stage = smem + kStage;
+    {
+        const int n16 = n_b * (kSlotBytes / 16);
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.slots + size_t(cb0) * kSlotBytes);
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = tid + u * kThreads;
+            if (i < n16) v[u] = ld_cg4(src + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = tid + u * kThreads;
+            if (i < n16) reinterpret_cast<uint4 *>(stage)[i] = v[u];
+        }
+        for (int i = tid + 4 * kThreads; i < n16; i += kThreads)
+            reinterpret_cast<uint4 *>(stage)[i] = ld_cg4(src + i);
+    }
+    __syncthreads();
+    auto hdr = [&](int jj) { return reinterpret_cast<const unsigned *>(stage + jj * kSlotBytes); };
     if (warp == 0) {
         int run = 0;
+        unsigned minp = kFine, mx = 0;
+        int over = 0;
         for (int base = 0; base < n_b; base += 32) {
             const int jj = base + lane;
-            const int v = jj < n_b ? int(ld_cg(p.cta_cnt + cb0 + jj)) : 0;
+            int v = 0;
+            if (jj < n_b) {
+                const unsigned *h = hdr(jj);
+                v = int(h[0]);
+                mx = max(mx, h[1]);
+                if (v > 0) minp = min(minp, h[2]);
+                over |= v > kSlot;
+            }
             int x = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -703,116 +710,228 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             if (jj < n_b) offs[jj] = run + x - v;
             run += __shfl_sync(0xffffffffu, x, 31);
         }
-        if (lane == 0) { offs[n_b] = run; sv[4] = run; }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            minp = min(minp, __shfl_xor_sync(0xffffffffu, minp, o));
+            over |= __shfl_xor_sync(0xffffffffu, over, o);
+        }
+        if (lane == 0) {
+            offs[n_b] = run;
+            sv[6] = run;
+            sv[7] = int(mx);
+            sv[8] = int(minp);
+            sv[9] = over;
+        }
     }
     __syncthreads();
-    const int n_cand = sv[4];
+    const int n_cand = sv[6];
+    const unsigned maxex_all = unsigned(sv[7]);
+    bool fast = !p.force_slow && n_cand <= kSelCap && n_cand >= k_b;
+    unsigned kth = 0xFFFFFFFFu, take_eq = 0;
+    unsigned *ckey = reinterpret_cast<unsigned *>(smem + kCKey);
+    int32_t *cgrp = reinterpret_cast<int32_t *>(smem + kCG);
     DBG_MAX(0, n_cand);
-    DBG_MAX(1, sv[3]);
-    const bool fast = !p.force_slow && n_cand <= kSelCap;
-    int32_t *sel_g = reinterpret_cast<int32_t *>(smem + kSelG);
-    int32_t *idx_list = p.idx_out ? p.idx_out : p.idx_ws;
-
     if (fast) {
-        level1_bins(2);  // nobody reads the level-1 histogram after barrier A
-        __syncthreads();
-        if (has_items) {
-            unsigned *ckey = reinterpret_cast<unsigned *>(smem + kCandKey);
-            int32_t *cgrp = reinterpret_cast<int32_t *>(smem + kCandG);
-            unsigned *rh = reinterpret_cast<unsigned *>(smem + kRHist);
-            // all candidate loads of a thread are issued before any is stored, so
-            // the copy costs one L2 round trip per 8 entries a thread
-            for (int i0 = tid; i0 < n_cand; i0 += kThreads * 8) {
-                unsigned kv[8], gv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int i = i0 + u * kThreads;
-                    kv[u] = gv[u] = 0u;
-                    if (i < n_cand) {
-                        int lo = 0, hi = n_b;  // segment jj with offs[jj] <= i < offs[jj+1]
-                        while (hi - lo > 1) {
-                            const int mid = (lo + hi) >> 1;
-                            if (offs[mid] <= i) lo = mid; else hi = mid;
-                        }
-                        const int64_t src = seg + chunk_lo(lo) + (i - offs[lo]);
-                        kv[u] = ld_cg(p.cand_key + src);
-                        gv[u] = ld_cg(reinterpret_cast<const unsigned *>(p.cand_g) + src);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int i = i0 + u * kThreads;
-                    if (i < n_cand) {
-                        ckey[i] = kv[u];
-                        cgrp[i] = int32_t(gv[u]);
-                    }
+        for (int jj = warp; jj < n_b; jj += kWarps) {
+            const unsigned *h = hdr(jj);
+            const int cnt = int(h[0]), o0 = offs[jj];
+            for (int e = lane; e < min(cnt, kSlot); e += 32) {
+                ckey[o0 + e] = h[4 + 2 * e];
+                cgrp[o0 + e] = int32_t(h[5 + 2 * e]);
+            }
+        }
+        if (sv[9]) {  // candidates past a slot's capacity come from the block's segment
+            for (int jj = warp; jj < n_b; jj += kWarps) {
+                const int cnt = int(hdr(jj)[0]), o0 = offs[jj];
+                const int64_t s0 = seg + chunk_lo(jj);
+                for (int e = kSlot + lane; e < cnt; e += 32) {
+                    ckey[o0 + e] = ld_cg(p.cand_key + s0 + e - kSlot);
+                    cgrp[o0 + e] = int32_t(ld_cg(reinterpret_cast<const unsigned *>(p.cand_g) + s0 + e - kSlot));
                 }
             }
+        }
+        __syncthreads();
+        PHASE_MARK(9);
+        if (k_b > 0) {
+            // histogram of the 16-bit bin relative to the smallest published bin
+            unsigned *sh = reinterpret_cast<unsigned *>(smem + kSelHist);
+            const unsigned minp = unsigned(sv[8]);
+            for (int i = tid; i < 2048; i += kThreads) sh[i] = 0u;
+            if (tid == 0) sv[10] = 0;
             __syncthreads();
-            PHASE_MARK(13);
-            unsigned take_eq = 0;
-            const unsigned kth = k_b > 0 ? radix_select_smem(ckey, n_cand, unsigned(k_b), rh,
-                                                             scratch, sv + 8, &take_eq)
-                                         : 0xFFFFFFFFu;
-            PHASE_MARK(14);
-            // ordered compaction (candidates are in ascending group order)
-            if (tid == 0) { sv[5] = 0; sv[6] = 0; }
+            for (int i = tid; i < ((n_cand + 31) & ~31); i += kThreads) {
+                unsigned d = 0;
+                bool on = i < n_cand;
+                if (on) d = min(2047u, (ckey[i] >> 16) - minp);
+                hist_add(sh, d, on);
+            }
+            __syncthreads();
+            PHASE_MARK(10);
+            unsigned above;
+            const int T = find_digit(sh, 2048, unsigned(k_b), &above, scratch, sv + 12);
+            PHASE_MARK(11);
+            const unsigned need_t = unsigned(k_b) - above;
+            const int m_t = int(sh[T]);
+            if (T < 2047 && m_t <= kTieCap) {
+                unsigned *tie = reinterpret_cast<unsigned *>(smem + kTie);
+                for (int i = tid; i < n_cand; i += kThreads) {
+                    if (min(2047u, (ckey[i] >> 16) - minp) == unsigned(T)) {
+                        const int s = atomicAdd(sv + 10, 1);
+                        tie[2 * s] = ckey[i];
+                        tie[2 * s + 1] = unsigned(i);
+                    }
+                }
+                __syncthreads();
+                if (tid < m_t) {
+                    const unsigned ke = tie[2 * tid], ie = tie[2 * tid + 1];
+                    unsigned rank = 0;
+                    for (int f = 0; f < m_t; ++f) {
+                        const unsigned kf = tie[2 * f], jf = tie[2 * f + 1];
+                        rank += kf > ke || (kf == ke && jf < ie);
+                    }
+                    if (rank == need_t - 1) sv[14] = int(ke);  // the k-th largest key
+                }
+                __syncthreads();
+                kth = unsigned(sv[14]);
+                if (tid == 0) sv[15] = 0;
+                __syncthreads();
+                if (tid < m_t) {
+                    const unsigned ke = tie[2 * tid], ie = tie[2 * tid + 1];
+                    if (ke == kth) {
+                        unsigned rank = 0;
+                        for (int f = 0; f < m_t; ++f) {
+                            const unsigned kf = tie[2 * f], jf = tie[2 * f + 1];
+                            rank += kf > ke || (kf == ke && jf < ie);
+                        }
+                        if (rank < need_t) atomicAdd(sv + 15, 1);
+                    }
+                }
+                __syncthreads();
+                take_eq = unsigned(sv[15]);
+            } else {
+                kth = radix_select_smem(ckey, n_cand, unsigned(k_b), sh, scratch, sv + 12,
+                                        &take_eq);
+            }
+            fast = kth > maxex_all;  // the union of local top-m sets holds the true top k
+        }
+    }
+    PHASE_MARK(12);
+    int32_t *own = reinterpret_cast<int32_t *>(smem + kSelG);
+    int n_own = 0;
+    bool use_spec = false;
+    if (fast) {
+        // this block's selected groups, ascending: its candidates are the range
+        // [offs[j], offs[j+1]); ties at K* go to the lowest candidate index
+        const int o0 = offs[j], o1 = offs[j + 1];
+        int eqb = 0;
+        for (int i = tid; i < o0; i += kThreads) eqb += ckey[i] == kth;
+        int tot;
+        block_exclusive_scan(eqb, scratch, &tot);
+        const int eq_before_own = tot;
+        const int per = (o1 - o0 + kThreads - 1) / kThreads;
+        const int i0 = min(o1, o0 + tid * per), i1 = min(o1, i0 + per);
+        int n_eq = 0;
+        for (int i = i0; i < i1; ++i) n_eq += ckey[i] == kth;
+        int tq;
+        const int eq_start = eq_before_own + block_exclusive_scan(n_eq, scratch, &tq);
+        int eqr = eq_start, nsel = 0;
+        for (int i = i0; i < i1; ++i) {
+            const unsigned kk = ckey[i];
+            nsel += kk > kth || (kk == kth && unsigned(eqr++) < take_eq);
+        }
+        int tsel;
+        int pos = block_exclusive_scan(nsel, scratch, &tsel);
+        eqr = eq_start;
+        for (int i = i0; i < i1; ++i) {
+            const unsigned kk = ckey[i];
+            if (kk > kth || (kk == kth && unsigned(eqr++) < take_eq)) own[pos++] = cgrp[i];
+        }
+        n_own = tsel;
+        PHASE_MARK(13);
+        // the full ascending selection, for the optional index output
+        if (p.idx_out && j == 0) {
+            if (tid == 0) { sv[16] = 0; sv[17] = 0; }
             __syncthreads();
             for (int base = 0; base < n_cand; base += kThreads * 4) {
                 unsigned kk[4];
-                int n_eq = 0;
+                int ne = 0;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = base + tid * 4 + e;
                     kk[e] = i < n_cand ? ckey[i] : 0u;
-                    n_eq += (i < n_cand && kk[e] == kth);
+                    ne += (i < n_cand && kk[e] == kth);
                 }
-                const int eq_seen = sv[5], written = sv[6];
-                int tot_eq;
-                int eq_before = eq_seen + block_exclusive_scan(n_eq, scratch, &tot_eq);
+                const int eq_seen = sv[16], written = sv[17];
+                int te;
+                int eb = eq_seen + block_exclusive_scan(ne, scratch, &te);
                 bool sel[4];
-                int n_sel = 0;
+                int ns = 0;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = base + tid * 4 + e;
                     bool keep = false;
                     if (i < n_cand) {
                         if (kk[e] > kth) keep = true;
-                        else if (kk[e] == kth) keep = unsigned(eq_before++) < take_eq;
+                        else if (kk[e] == kth) keep = unsigned(eb++) < take_eq;
                     }
                     sel[e] = keep;
-                    n_sel += keep;
+                    ns += keep;
                 }
-                int tot_sel;
-                int pos = written + block_exclusive_scan(n_sel, scratch, &tot_sel);
+                int ts;
+                int ps = written + block_exclusive_scan(ns, scratch, &ts);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (sel[e]) {
-                        if (pos < k_b) sel_g[pos] = cgrp[base + tid * 4 + e];
-                        ++pos;
+                        if (ps < k_b) p.idx_out[int64_t(b) * p.k + ps] = cgrp[base + tid * 4 + e];
+                        ++ps;
                     }
-                if (tid == 0) { sv[5] = eq_seen + tot_eq; sv[6] = written + tot_sel; }
+                if (tid == 0) { sv[16] = eq_seen + te; sv[17] = written + ts; }
                 __syncthreads();
             }
-            if (p.idx_out && j == 0)
-                for (int i = tid; i < p.k; i += kThreads) p.idx_out[int64_t(b) * p.k + i] = i < k_b ? sel_g[i] : -1;
+            for (int i = k_b + tid; i < p.k; i += kThreads) p.idx_out[int64_t(b) * p.k + i] = -1;
         }
+        // the prefetched groups serve as the attention chunk if they cover ours
+        if (tid == 0) sv[18] = 1;
+        __syncthreads();
+        for (int i = tid; i < n_own; i += kThreads) {
+            bool found = false;
+            for (int s = 0; s < n_spec; ++s) found |= spec_g[s] == own[i];
+            if (!found) sv[18] = 0;
+        }
+        __syncthreads();
+        use_spec = sv[18] != 0 && n_own <= spec_cap;
+        if (use_spec && tid < spec_cap) {
+            bool keep = false;
+            if (tid < n_spec)
+                for (int i = 0; i < n_own; ++i) keep |= own[i] == spec_g[tid];
+            if (!keep) spec_sg[tid] = -1;  // prefetched but not selected: masked
+        }
+        __syncthreads();
     } else {
-        // -------- exact multi-pass selection over the sequence's blocks --------
-        level1_bins(1);  // complete the level-1 histogram
-        arrive(ctl + kSlowB);
-        if (!wait_count(p, ctl + kSlowB, unsigned(n_b), 3, s_ok)) {
-            cp_async_wait<0>();
-            return;
+        // ---------- exact multi-pass selection over the sequence's blocks ----------
+        // level 1: the full 16-bit-bin histogram of every block's scores
+        cp_async_wait<0>();
+        __syncthreads();
+        clear_smem(smem + kU, kUBytes);
+        __syncthreads();
+        for (int i = tid; i < nloc; i += kThreads) {
+            const unsigned bin = score_key(score_at(i)) >> 16;
+            atomicAdd(h16 + (bin >> 1), (bin & 1u) ? 0x10000u : 1u);
         }
+        __syncthreads();
+        flush_hist(h16, hist1);
+        arrive(ctl + kSlowB);
+        if (!wait_count(p, ctl + kSlowB, unsigned(n_b), 3, s_ok)) return;
         if (warp == 0) {
             unsigned above = 0;
             const int t1 = k_b > 0 ? hist_walk(hist1, unsigned(k_b), true, &above) : -1;
-            if (lane == 0) { sv[10] = t1; sv[11] = int(above); }
+            if (lane == 0) { sv[20] = t1; sv[21] = int(above); }
         }
         __syncthreads();
-        const int t1 = sv[10];
-        const unsigned need2 = unsigned(k_b) - unsigned(sv[11]);
+        const int t1 = sv[20];
+        const unsigned need2 = unsigned(k_b) - unsigned(sv[21]);
+        // level 2: low 16 bits of the keys in the threshold bin
         clear_smem(smem + kU, kUBytes);
         __syncthreads();
         for (int i = tid; i < nloc; i += kThreads) {
@@ -825,20 +944,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         __syncthreads();
         flush_hist(h16, hist2);
         arrive(ctl + kSlowC);
-        if (!wait_count(p, ctl + kSlowC, unsigned(n_b), 4, s_ok)) {
-            cp_async_wait<0>();
-            return;
-        }
+        if (!wait_count(p, ctl + kSlowC, unsigned(n_b), 4, s_ok)) return;
         if (warp == 0) {
             unsigned above = 0;
             const int lo = (k_b > 0 && t1 >= 0) ? hist_walk(hist2, need2, true, &above) : -1;
-            if (lane == 0) { sv[12] = lo; sv[13] = int(above); }
+            if (lane == 0) { sv[22] = lo; sv[23] = int(above); }
         }
         __syncthreads();
-        const bool none = k_b == 0 || t1 < 0 || sv[12] < 0;
-        const unsigned kth = none ? 0xFFFFFFFFu : (unsigned(t1) << 16) | unsigned(sv[12]);
-        const unsigned take_eq = none ? 0u : need2 - unsigned(sv[13]);
-        // own counts for the tie rule and the output offsets
+        const bool none = k_b == 0 || t1 < 0 || sv[22] < 0;
+        kth = none ? 0xFFFFFFFFu : (unsigned(t1) << 16) | unsigned(sv[22]);
+        take_eq = none ? 0u : need2 - unsigned(sv[23]);
         {
             int gt = 0, eq = 0;
             for (int i = tid; i < nloc; i += kThreads) {
@@ -850,23 +965,20 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             block_exclusive_scan(gt, scratch, &tgt);
             block_exclusive_scan(eq, scratch, &teq);
             if (tid == 0) {
-                p.cta_cnt[ncta + cta] = unsigned(tgt);
-                p.cta_cnt[2 * ncta + cta] = unsigned(teq);
+                p.cta_cnt[cta] = unsigned(tgt);
+                p.cta_cnt[ncta + cta] = unsigned(teq);
             }
         }
         arrive(ctl + kSlowD);
-        if (!wait_count(p, ctl + kSlowD, unsigned(n_b), 5, s_ok)) {
-            cp_async_wait<0>();
-            return;
-        }
+        if (!wait_count(p, ctl + kSlowD, unsigned(n_b), 5, s_ok)) return;
         if (warp == 0) {
             // offsets of the blocks before this one: each takes its keys > K* and
             // the next ties in group order (blocks hold ascending group ranges)
             unsigned out_off = 0, eq_run = 0;
             for (int base = 0; base < j; base += 32) {
                 const int jj = base + lane;
-                const unsigned gtj = jj < j ? ld_cg(p.cta_cnt + ncta + cb0 + jj) : 0u;
-                const unsigned eqj = jj < j ? ld_cg(p.cta_cnt + 2 * ncta + cb0 + jj) : 0u;
+                const unsigned gtj = jj < j ? ld_cg(p.cta_cnt + cb0 + jj) : 0u;
+                const unsigned eqj = jj < j ? ld_cg(p.cta_cnt + ncta + cb0 + jj) : 0u;
                 unsigned x = eqj;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -882,85 +994,85 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 eq_run += __shfl_sync(0xffffffffu, x, 31);
             }
             if (lane == 0) {
-                sv[14] = int(out_off);
-                sv[15] = int(take_eq > eq_run ? take_eq - eq_run : 0u);  // my ties to take
+                sv[24] = int(out_off);
+                sv[25] = int(take_eq > eq_run ? take_eq - eq_run : 0u);  // my ties to take
             }
         }
         __syncthreads();
         {
+            int32_t *idx_list = p.idx_out ? p.idx_out : p.idx_ws;
             const int per = (nloc + kThreads - 1) / kThreads;
             const int i0 = min(nloc, tid * per), i1 = min(nloc, i0 + per);
             int n_eq = 0;
             for (int i = i0; i < i1; ++i) n_eq += score_key(score_at(i)) == kth;
             int tot;
             const int eq_start = block_exclusive_scan(n_eq, scratch, &tot);
-            int eq_before = eq_start;
-            const unsigned my_take = unsigned(sv[15]);
-            int n_sel = 0;
+            const unsigned my_take = unsigned(sv[25]);
+            int eqr = eq_start, n_sel = 0;
             for (int i = i0; i < i1; ++i) {
                 const unsigned key = score_key(score_at(i));
-                n_sel += key > kth || (key == kth && unsigned(eq_before++) < my_take);
+                n_sel += key > kth || (key == kth && unsigned(eqr++) < my_take);
             }
-            int pos = sv[14] + block_exclusive_scan(n_sel, scratch, &tot);
-            eq_before = eq_start;
+            int tsel;
+            int lpos = block_exclusive_scan(n_sel, scratch, &tsel);
+            int gpos = sv[24] + lpos;
+            eqr = eq_start;
             for (int i = i0; i < i1; ++i) {
                 const unsigned key = score_key(score_at(i));
-                const bool keep = key > kth || (key == kth && unsigned(eq_before++) < my_take);
-                if (keep) {
-                    if (pos < k_b) idx_list[int64_t(b) * p.k + pos] = g_lo + i;
-                    ++pos;
+                if (key > kth || (key == kth && unsigned(eqr++) < my_take)) {
+                    if (lpos < kMaxK) own[lpos] = g_lo + i;
+                    if (gpos < k_b) idx_list[int64_t(b) * p.k + gpos] = g_lo + i;
+                    ++lpos;
+                    ++gpos;
                 }
             }
+            n_own = min(tsel, kMaxK);
             if (j == 0)
                 for (int i = k_b + tid; i < p.k; i += kThreads) idx_list[int64_t(b) * p.k + i] = -1;
         }
         // neither histogram is read by anyone any more: zero this block's slice of
-        // the level-1 histogram, and the level-2 fine bins this block counted
-        // (still in shared memory) plus a slice of the level-2 coarse bins
+        // the level-1 histogram, the level-2 fine bins it counted (still in shared
+        // memory) and a slice of the level-2 coarse bins
         {
             const int w0 = int((long long)kHistWords / 4 * j / n_b) * 4;
             const int w1 = int((long long)kHistWords / 4 * (j + 1) / n_b) * 4;
             for (int w = w0 + tid * 4; w < w1; w += kThreads * 4)
                 *reinterpret_cast<uint4 *>(hist1 + w) = make_uint4(0, 0, 0, 0);
-        }
-        for (int w = tid; w < kFine / 2; w += kThreads) {
-            const unsigned v = h16[w];
-            if (v & 0xFFFFu) hist2[2 * w] = 0u;
-            if (v >> 16) hist2[2 * w + 1] = 0u;
-        }
-        for (int cbin = int((long long)kCoarse * j / n_b) + tid;
-             cbin < int((long long)kCoarse * (j + 1) / n_b); cbin += kThreads)
-            hist2[kFine + cbin] = 0u;
-        arrive(ctl + kSlowE);
-        if (!wait_count(p, ctl + kSlowE, unsigned(n_b), 7, s_ok)) {
-            cp_async_wait<0>();
-            return;
-        }
-        if (has_items) {
-            for (int i = tid; i < k_b; i += kThreads)
-                sel_g[i] = int32_t(ld_cg(reinterpret_cast<const unsigned *>(idx_list) +
-                                         int64_t(b) * p.k + i));
+            for (int w = tid; w < kFine / 2; w += kThreads) {
+                const unsigned v = h16[w];
+                if (v & 0xFFFFu) hist2[2 * w] = 0u;
+                if (v >> 16) hist2[2 * w + 1] = 0u;
+            }
+            for (int cbin = int((long long)kCoarse * j / n_b) + tid;
+                 cbin < int((long long)kCoarse * (j + 1) / n_b); cbin += kThreads)
+                hist2[kFine + cbin] = 0u;
         }
         __syncthreads();
+        // Q of the first head group (the prefetch was drained above)
+        {
+            const int HG0 = min(64, p.H_q);
+            const uint16_t *qrow = p.q + int64_t(b) * p.H_q * DQK;
+            for (int e = tid; e < HG0 * (DQK / 8); e += kThreads) {
+                const int h = e / (DQK / 8), c8 = e % (DQK / 8);
+                cp_async16(smem_u32(sq + h * QP + c8 * 8), qrow + int64_t(h) * DQK + c8 * 8, 16);
+            }
+            cp_async_commit();
+        }
     }
+    PHASE_MARK(14);
 
-    PHASE_MARK(7);
-    // ---- attention items -------------------------------------------------------
-    if (has_items) {
-        const int gps = (k_b + S_b - 1) / S_b;
-        const uint16_t *Kb = p.K + int64_t(b) * p.sK_b;
-        const uint16_t *Vb = p.V + int64_t(b) * p.sV_b;
-        uint16_t *skb = reinterpret_cast<uint16_t *>(smem + kKV);
-        uint16_t *svb = skb + 2 * kChunk * QP;
-        int *sgrp = reinterpret_cast<int *>(svb + 2 * kChunk * VP);
+    // ---- attention over this block's selected groups ----------------------------
+    {
         float *state = reinterpret_cast<float *>(smem + kState);
-        bool first = true;
-        for (int it = j; it < items; it += n_b) {
-            const int s = it % S_b, hg = it / S_b;
-            const int h0 = hg * 64, HG = min(64, p.H_q - h0);
-            const int MT = HG / 16, TS = 4;
-            const int n_aw = MT * TS;  // attention warps
-            if (!first) {
+        uint16_t *gk = reinterpret_cast<uint16_t *>(smem + kGather);
+        uint16_t *gvb = gk + 2 * kChunk * QP;
+        int *gsg = reinterpret_cast<int *>(smem + kSelG) - 2 * kChunk;  // [2][kChunk]
+        const int gpc = kChunk / P;
+        const int nchunks = use_spec ? 1 : (n_own + gpc - 1) / gpc;
+        for (int h0 = 0; h0 < p.H_q; h0 += 64) {
+            const int HG = min(64, p.H_q - h0);
+            const int MT = HG / 16, TS = 2, n_aw = MT * TS;
+            if (h0 > 0) {
                 __syncthreads();
                 const uint16_t *qrow = p.q + (int64_t(b) * p.H_q + h0) * DQK;
                 for (int e = tid; e < HG * (DQK / 8); e += kThreads) {
@@ -969,19 +1081,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 }
                 cp_async_commit();
             }
-            first = false;
-            const int j0 = s * gps, j1 = min(k_b, j0 + gps);
-            const int gpc = kChunk / P;
-            const int nchunks = j1 > j0 ? (j1 - j0 + gpc - 1) / gpc : 0;
             auto issue = [&](int ci, int buf) {
-                const int jb = j0 + ci * gpc;
-                gather_chunk<DQK, DV>(skb + buf * kChunk * QP, svb + buf * kChunk * VP,
-                                      sgrp + buf * kChunk, sel_g + jb, min(gpc, j1 - jb), P,
-                                      G_b, Kb, Vb, QP, VP, tid, kThreads);
+                const int jb = ci * gpc;
+                gather_chunk<DQK, DV>(gk + buf * kChunk * QP, gvb + buf * kChunk * VP,
+                                      gsg + buf * kChunk, own + jb, min(gpc, n_own - jb), P, G_b,
+                                      Kb, Vb, QP, VP, tid, kThreads);
             };
             cp_async_wait<0>();
             __syncthreads();
-            if (nchunks > 0) issue(0, 0);
+            PHASE_MARK(15);
+            if (!use_spec && nchunks > 0) issue(0, 0);
             const int mt = warp % MT, ts = warp / MT;
             const int ntok = kChunk / TS, tok0 = ts * ntok;
             uint32_t qa[DQK / 16][4];  // unused: fragments come from shared memory
@@ -989,109 +1098,110 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             st.init();
             for (int ci = 0; ci < nchunks; ++ci) {
                 const int buf = ci & 1;
-                if (ci + 1 < nchunks) {
-                    issue(ci + 1, buf ^ 1);
-                    cp_async_wait<1>();
-                } else {
-                    cp_async_wait<0>();
+                const uint16_t *ck = use_spec ? spk : gk + buf * kChunk * QP;
+                const uint16_t *cv = use_spec ? spv : gvb + buf * kChunk * VP;
+                const int *cg = use_spec ? spec_sg : gsg + buf * kChunk;
+                if (!use_spec) {
+                    if (ci + 1 < nchunks) {
+                        issue(ci + 1, buf ^ 1);
+                        cp_async_wait<1>();
+                    } else {
+                        cp_async_wait<0>();
+                    }
+                    __syncthreads();
                 }
-                __syncthreads();
                 if (warp < n_aw)
-                    attn_chunk<DQK, DV, 2, true>(st, qa, skb + buf * kChunk * QP,
-                                                 svb + buf * kChunk * VP, sgrp + buf * kChunk, QP,
-                                                 VP, P, tok0, ntok, p.scale_log2, sq, mt);
+                    attn_chunk<DQK, DV, 4, true>(st, qa, ck, cv, cg, QP, VP, P, tok0, ntok,
+                                                 p.scale_log2, sq, mt);
                 __syncthreads();
             }
-            PHASE_MARK(15);
+            PHASE_MARK(16);
             if (warp < n_aw) store_warp_state<DV>(st, state + warp * 16 * (DV + 2));
             __syncthreads();
             for (int e = tid; e < HG * (DV / 2); e += kThreads) {
                 const int hl = e / (DV / 2), d2 = (e % (DV / 2)) * 2;
                 float Lsum;
                 const float4 rr = merge_states<DV>(state, MT, TS, hl, d2, Lsum);
-                const int h = h0 + hl;
-                if (S_b == 1) {
-                    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-                    *reinterpret_cast<uint32_t *>(p.out + (int64_t(b) * p.H_q + h) * DV + d2) =
-                        pack_bf2(rr.z * inv, rr.w * inv);
-                    if (p.lse && d2 == 0)
-                        p.lse[int64_t(b) * p.H_q + h] =
-                            Lsum > 0.f ? (rr.x + log2f(Lsum)) * kLn2 : -INFINITY;
-                } else {
-                    const int64_t pi = (int64_t(b) * p.S_max + s) * p.H_q + h;
+                const int64_t pi = int64_t(cta) * p.H_q + h0 + hl;
+                if (Lsum > 0.f)
                     *reinterpret_cast<float2 *>(p.part_o + pi * DV + d2) = make_float2(rr.z, rr.w);
-                    if (d2 == 0) p.part_ml[pi] = make_float2(rr.x, Lsum);
-                }
+                if (d2 == 0) p.part_ml[pi] = make_float2(Lsum > 0.f ? rr.x : -INFINITY, Lsum);
             }
         }
-        cp_async_wait<0>();
     }
+    arrive(ctl + kAtt);
+    PHASE_MARK(17);
 
-    PHASE_MARK(8);
-    // ---- combine the partial states ---------------------------------------------
-    if (S_b > 1 && has_items) {
-        arrive(ctl + kAtt);
-        if (!wait_count(p, ctl + kAtt, unsigned(n_att), 6, s_ok)) return;
-        PHASE_MARK(9);
-        constexpr int PER = DV / 32;
-        float *fw = reinterpret_cast<float *>(smem + kState) + warp * kMaxCtas;  // split weights
-        for (int h = j + n_att * warp; h < p.H_q; h += n_att * kWarps) {
-            const float2 *mlh = p.part_ml + int64_t(b) * p.S_max * p.H_q + h;
-            float M = -INFINITY;
-            for (int s0 = 0; s0 < S_b; s0 += 32) {
-                const int s = s0 + lane;
-                float m = -INFINITY;
-                if (s < S_b) m = ld_cg_f(reinterpret_cast<const float *>(mlh + int64_t(s) * p.H_q));
-                M = fmaxf(M, m);
-            }
+    // ---- merge the blocks' partial states, head by head ---------------------------
+    if (!wait_count(p, ctl + kAtt, unsigned(n_b), 6, s_ok)) return;
+    PHASE_MARK(18);
+    {
+        float *wsm = reinterpret_cast<float *>(smem + kU);       // [kMaxCtas] weights
+        float *lsm = wsm + kMaxCtas;                              // [kMaxCtas] l
+        float *red = lsm + kMaxCtas;                              // [ngrp][DV]
+        constexpr int D4 = DV / 4;                                // float4 columns
+        const int sg = tid / D4, dc = tid % D4;                   // split group, column
+        const int ngrp = kThreads / D4;                           // 16 (DV=128) or 32 (DV=64)
+        for (int h = j; h < p.H_q; h += n_b) {
+            float2 ml = make_float2(-INFINITY, 0.f);
+            if (tid < n_b) ml = ld_cg_f2(p.part_ml + int64_t(cb0 + tid) * p.H_q + h);
+            float4 ov[(kMaxCtas + 15) / 16];
+            const int nu = (n_b - sg + ngrp - 1) / ngrp;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            const float ref = M == -INFINITY ? 0.f : M;
-            float Lsum = 0.f;
-            for (int s0 = 0; s0 < S_b; s0 += 32) {
-                const int s = s0 + lane;
-                float wgt = 0.f;
-                if (s < S_b) {
-                    const float *ml = reinterpret_cast<const float *>(mlh + int64_t(s) * p.H_q);
-                    wgt = exp2f(ld_cg_f(ml) - ref);
-                    Lsum += wgt * ld_cg_f(ml + 1);
-                    fw[s] = wgt;
+            for (int u = 0; u < (kMaxCtas + 15) / 16; ++u) {
+                ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (u < nu) {
+                    const int s = sg + u * ngrp;
+                    ov[u] = ld_cg_f4(p.part_o + (int64_t(cb0 + s) * p.H_q + h) * DV + dc * 4);
                 }
             }
+            float m = ml.x;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-            __syncwarp();
-            float acc[PER];
-#pragma unroll
-            for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-            const float *po = p.part_o + (int64_t(b) * p.S_max * p.H_q + h) * DV + lane * PER;
-            const int64_t sstride = int64_t(p.H_q) * DV;
-            int s = 0;
-            for (; s + 8 <= S_b; s += 8) {
-                float v[8][PER];
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-#pragma unroll
-                    for (int i = 0; i < PER; ++i) v[u][i] = ld_cg_f(po + (s + u) * sstride + i);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-#pragma unroll
-                    for (int i = 0; i < PER; ++i) acc[i] += fw[s + u] * v[u][i];
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) sred[warp] = m;
+            __syncthreads();
+            float M = -INFINITY;
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sred[w]);
+            const float ref = M == -INFINITY ? 0.f : M;
+            if (tid < n_b) {
+                const float wgt = ml.y > 0.f ? exp2f(ml.x - ref) : 0.f;
+                wsm[tid] = wgt;
+                lsm[tid] = wgt * ml.y;
             }
-            for (; s < S_b; ++s)
+            __syncthreads();
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < PER; ++i) acc[i] += fw[s] * ld_cg_f(po + s * sstride + i);
-            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-            uint16_t *orow = p.out + (int64_t(b) * p.H_q + h) * DV + lane * PER;
-#pragma unroll
-            for (int i = 0; i < PER; i += 2)
-                *reinterpret_cast<uint32_t *>(orow + i) = pack_bf2(acc[i] * inv, acc[i + 1] * inv);
-            if (p.lse && lane == 0)
-                p.lse[int64_t(b) * p.H_q + h] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
-            __syncwarp();
+            for (int u = 0; u < (kMaxCtas + 15) / 16; ++u) {
+                if (u < nu) {
+                    const float wgt = wsm[sg + u * ngrp];
+                    if (wgt != 0.f) {
+                        acc.x += wgt * ov[u].x;
+                        acc.y += wgt * ov[u].y;
+                        acc.z += wgt * ov[u].z;
+                        acc.w += wgt * ov[u].w;
+                    }
+                }
+            }
+            *reinterpret_cast<float4 *>(red + sg * DV + dc * 4) = acc;
+            __syncthreads();
+            if (tid < DV / 2) {
+                float L = 0.f;
+                for (int s = 0; s < n_b; ++s) L += lsm[s];
+                float a0 = 0.f, a1 = 0.f;
+                for (int g2 = 0; g2 < ngrp; ++g2) {
+                    a0 += red[g2 * DV + 2 * tid];
+                    a1 += red[g2 * DV + 2 * tid + 1];
+                }
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                *reinterpret_cast<uint32_t *>(p.out + (int64_t(b) * p.H_q + h) * DV + 2 * tid) =
+                    pack_bf2(a0 * inv, a1 * inv);
+                if (p.lse && tid == 0)
+                    p.lse[int64_t(b) * p.H_q + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+            }
+            __syncthreads();
         }
     }
-    PHASE_MARK(10);
+    PHASE_MARK(19);
     __syncthreads();
     if (tid == 0 && atomicAdd(ctl + kDepart, 1u) == unsigned(n_b) - 1u) {
         for (int i = 0; i < kNumCounters; ++i) ctl[i] = 0u;  // every block is done with them
@@ -1105,21 +1215,17 @@ int num_sms() {
     return sms;
 }
 
-int s_max_for(int k, int P, int ncta) {
-    int s = (k * P + kChunk - 1) / kChunk;
-    return max(1, min(s, ncta));
-}
-
 template <int DQK>
 constexpr int smem_bytes() {
-    return kQ + 64 * (DQK + 8) * 2 + 128 + kCoarse * 4 + (2 * (kMaxCtas + 1) + 64 + 40) * 4;
+    return kQ + 64 * (DQK + 8) * 2 + 128 + kCoarse * 4 +
+           (2 * (kMaxCtas + 1) + kMaxCtas + 2 * kSpecTok + 64 + 40 + 64) * 4;
 }
 
 struct WsLayout {
-    size_t ctl, hist, cand_key, cand_g, gscore, cta_cnt, idx_ws, part_o, part_ml, total;
+    size_t ctl, hist, slots, cand_key, cand_g, gscore, cta_cnt, idx_ws, part_o, part_ml, total;
 };
 
-WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int P, int ncta) {
+WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int ncta) {
     WsLayout w;
     size_t off = 256;  // status + abort words
     auto take = [&](size_t bytes) {
@@ -1127,16 +1233,16 @@ WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int P, int ncta) {
         off += (bytes + 255) & ~size_t(255);
         return o;
     };
-    const int S_max = s_max_for(k, P, ncta);
     w.ctl = take(size_t(B) * kCtlWords * 4);
     w.hist = take(size_t(B) * 2 * kHistWords * 4);
+    w.slots = take(size_t(ncta) * kSlotBytes);
     w.cand_key = take(size_t(B) * G_max * 4);
     w.cand_g = take(size_t(B) * G_max * 4);
     w.gscore = take(size_t(B) * G_max * 4);
-    w.cta_cnt = take(size_t(3) * ncta * 4);
+    w.cta_cnt = take(size_t(2) * ncta * 4);
     w.idx_ws = take(size_t(B) * k * 4);
-    w.part_o = take(size_t(B) * S_max * H_q * d_v * 4);
-    w.part_ml = take(size_t(B) * S_max * H_q * 8);
+    w.part_o = take(size_t(ncta) * H_q * d_v * 4);
+    w.part_ml = take(size_t(ncta) * H_q * 8);
     w.total = off;
     return w;
 }
@@ -1158,7 +1264,7 @@ bool fused_decode_supported(int B, int G_max, int H_i, int H_q, int d_qk, int d_
 
 size_t fused_decode_ws_bytes(int B, int G_max, int H_q, int d_v, int k, int P) {
     if (!fused_decode_supported(B, G_max, 1, H_q, 128, d_v, k, P)) return 0;
-    return ws_layout(B, G_max, H_q, d_v, k, P, num_sms()).total;
+    return ws_layout(B, G_max, H_q, d_v, k, num_sms()).total;
 }
 
 template <int NT, int DQK, int DV>
@@ -1195,17 +1301,11 @@ extern "C" int lcsw_debug_counters(unsigned *out, int reset) {
     return int(cudaGetLastError());
 }
 
-extern "C" int lcsw_debug_phase_times(unsigned long long *first, unsigned long long *last,
-                                      int reset) {
+extern "C" int lcsw_debug_stamps(long long *out) {
     cudaDeviceSynchronize();
-    cudaMemcpyFromSymbol(first, g_phase_first, sizeof(unsigned long long) * 16);
-    cudaMemcpyFromSymbol(last, g_phase_last, sizeof(unsigned long long) * 16);
-    if (reset) {
-        unsigned long long hi[16], lo[16];
-        for (int i = 0; i < 16; ++i) { hi[i] = ~0ull; lo[i] = 0ull; }
-        cudaMemcpyToSymbol(g_phase_first, hi, sizeof hi);
-        cudaMemcpyToSymbol(g_phase_last, lo, sizeof lo);
-    }
+    cudaMemcpyFromSymbol(out, g_stamp, sizeof(long long) * 160 * 40);
+    long long z[160 * 40] = {0};
+    cudaMemcpyToSymbol(g_stamp, z, sizeof z);
     return int(cudaGetLastError());
 }
 #endif
@@ -1213,7 +1313,7 @@ extern "C" int lcsw_debug_phase_times(unsigned long long *first, unsigned long l
 cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status,
                                 cudaStream_t st) {
     const int ncta = num_sms();
-    const WsLayout w = ws_layout(a->B, a->G_max, a->H_q, a->d_v, a->k, a->P, ncta);
+    const WsLayout w = ws_layout(a->B, a->G_max, a->H_q, a->d_v, a->k, ncta);
     char *base = static_cast<char *>(ws);
     Params prm;
     prm.q_idx = a->q_idx;
@@ -1236,7 +1336,6 @@ cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status
     prm.P = a->P;
     prm.k = a->k;
     prm.H_q = a->H_q;
-    prm.S_max = s_max_for(a->k, a->P, ncta);
     prm.force_slow = (a->flags & LCSW_DECODE_FORCE_MULTIPASS_SELECT) ? 1 : 0;
     prm.skip_arrive = (a->flags & LCSW_DECODE_TEST_SKIP_ARRIVE) ? 1 : 0;
     prm.scale_log2 = a->scale * kLog2e;
@@ -1246,6 +1345,7 @@ cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status
     prm.scores_out = a->scores_out;
     prm.ctl = reinterpret_cast<unsigned *>(base + w.ctl);
     prm.hist = reinterpret_cast<unsigned *>(base + w.hist);
+    prm.slots = reinterpret_cast<unsigned char *>(base + w.slots);
     prm.cand_key = reinterpret_cast<unsigned *>(base + w.cand_key);
     prm.cand_g = reinterpret_cast<int32_t *>(base + w.cand_g);
     prm.gscore = reinterpret_cast<float *>(base + w.gscore);
