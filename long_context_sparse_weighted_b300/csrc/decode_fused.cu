@@ -11,25 +11,31 @@
 // On a wait that runs out the block records LCSW_ERR_TIMEOUT in the workspace
 // status word, raises an abort flag every other wait honours, and returns.
 //
-// Phase 1 (HBM stream).  Warps stream their tiles' pooled keys straight into
-// mma.sync A fragments (the k-permuted layout of index_scores.cu, two tile
-// pairs in flight per warp), keep the scores in shared memory and count them in
-// a histogram of the top 16 bits of the order-preserving score key.  The block
-// that owns the group completed by the newest token pools it first (the exact
-// arithmetic of the pooling kernel) and scores that fresh key.
+// Phase 1 (HBM stream).  All 16 warps stream their tiles' pooled keys
+// straight into mma.sync A fragments (the k-permuted layout of
+// index_scores.cu, two tile pairs in flight per warp) and keep the scores in
+// shared memory.  The block that owns the group completed by the newest token
+// pools it first (the exact arithmetic of the pooling kernel) and scores that
+// fresh key.
 //
-// Selection.  Each block publishes its local top-m keys (by 16-bit bin, with
-// m = 2*ceil(k/n_b) + 8) in ascending group order, together with the largest
-// key it left out, and starts gathering the K/V rows of its own best
-// candidates into shared memory.  After one sync point every block loads the
-// union of candidates and selects the exact k-th key K* (a histogram relative
-// to the smallest published bin, then a rank count inside the threshold bin).
-// If K* exceeds every left-out key, the union holds the true top k and the
-// selection is exact; every block then knows which of its own groups are
-// selected.  Otherwise (keys clustered in one block, or too many candidates)
-// all blocks of the sequence run the exact multi-pass selection over their own
-// scores: full level-1 histogram, level-2 histogram of the low 16 bits,
-// per-block counts for the tie rule and the output order.
+// Threshold guess.  After its first tile pair every warp publishes, as one
+// 64-bit word, the 16-bit bins of the four largest keys it has seen.  The words
+// validate themselves (0 = not yet written), so no fence or counter is needed.
+// Once done streaming, each block reads every sample word of its sequence and
+// takes the bin where the count from the top reaches need ~ 1.5 k x (sample
+// size)/G_b.  All blocks of a sequence compute the same guess.
+//
+// Selection.  Each block publishes its keys at or above the guess (a fixed
+// slot, overflow to a per-sequence segment) and starts gathering its own
+// candidates' K/V rows into shared memory.  After one sync point every block
+// loads the candidates and selects the exact k-th key K* (a histogram relative
+// to the guess, then a rank count inside the threshold bin).  If at least k
+// keys cleared the guess and K* lies at or above it, the candidates hold the
+// true top k and the selection is exact; every block then knows which of its
+// own groups are selected.  Otherwise (a guess too high, or too many
+// candidates) all blocks of the sequence run the exact multi-pass selection
+// over their own scores: full level-1 histogram, level-2 histogram of the low
+// 16 bits, per-block counts for the tie rule and the output order.
 //
 // Attention.  Each block attends over its own selected groups -- already in
 // shared memory when they were among its prefetched candidates -- with the
@@ -65,6 +71,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // reset to zero by the last block to leave the kernel
 constexpr int kCands = 0, kSlowB = 1, kSlowC = 2, kSlowD = 3, kAtt = 4, kDepart = 5,
               kNumCounters = 6;
+constexpr int kStream = kWarps;    // streaming warps
+constexpr int kSampW = 4;          // sample bins each warp publishes (one 64-bit word)
+constexpr int kSampleN = 2 * kStream * 16;  // sample: the first groups of each block's chunk
 
 // shared memory map (bytes); region U is reused phase by phase
 constexpr int kU = 0;
@@ -109,6 +118,7 @@ struct Params {
     // workspace
     unsigned *ctl;        // [B][kCtlWords]
     unsigned *hist;       // [B][2][kHistWords]: level 1, level 2 (zero between calls)
+    unsigned long long *samp;  // [ncta][kWarps]: each warp's sample bins (zero between calls)
     unsigned char *slots; // [ncta][kSlotBytes]: count, max left-out key, bin, -, entries
     unsigned *cand_key;   // [B][G_max] candidates past a slot's capacity
     int32_t *cand_g;      // [B][G_max]
@@ -180,6 +190,23 @@ __device__ __forceinline__ uint4 ld_cg4(const void *p) {
                  : "l"(p));
     return r;
 }
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ bool all_u16_nonzero(uint4 v) {
+    const unsigned w[4] = {v.x, v.y, v.z, v.w};
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ok = ok && (w[i] & 0xFFFFu) != 0u && (w[i] >> 16) != 0u;
+    return ok;
+}
 __device__ __forceinline__ bool aborted(const int *f) {
     return *reinterpret_cast<const volatile int *>(f) != 0;
 }
@@ -202,10 +229,10 @@ __device__ bool wait_count(const Params &p, const unsigned *cnt, unsigned target
     if (threadIdx.x == 0) {
         int ok = 1;
         const long long t0 = clock64();
-        while (ld_acquire(cnt) < target) {
-            if (aborted(p.abort_flag)) { ok = 0; break; }
+        for (int spin = 0; ld_acquire(cnt) < target; ++spin) {
+            if ((spin & 63) == 63 && aborted(p.abort_flag)) { ok = 0; break; }
             if (clock64() - t0 > kSpinBudget) { raise_timeout(p, where); ok = 0; break; }
-            __nanosleep(20);
+            __nanosleep(64);
         }
         *s_ok = ok;
     }
@@ -217,11 +244,9 @@ __device__ bool wait_count(const Params &p, const unsigned *cnt, unsigned target
 // the count from the top reaches `need`.  One warp.  Returns the bin
 // (0..255) or -1 if the slice holds fewer than `need`; *above = count of bins
 // above it.
-__device__ __forceinline__ int warp_find_from_top(const unsigned *bins, unsigned need,
-                                                  unsigned *above) {
+__device__ __forceinline__ int find_from_top8(const unsigned (&v)[8], unsigned need,
+                                              unsigned *above) {
     const int lane = threadIdx.x & 31;
-    const uint4 a = ld_cg4(bins + lane * 8), b = ld_cg4(bins + lane * 8 + 4);
-    const unsigned v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     unsigned mine = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) mine += v[i];
@@ -249,53 +274,14 @@ __device__ __forceinline__ int warp_find_from_top(const unsigned *bins, unsigned
     *above = __shfl_sync(0xffffffffu, ab, src);
     return bin;
 }
-
-// The same search over shared memory: 256 u32 counts, or (pairs) 128 words
-// of two 16-bit counts.
-__device__ __forceinline__ int smem_find_from_top(const unsigned *bins, unsigned need,
-                                                  unsigned *above, bool pairs) {
+__device__ __forceinline__ int warp_find_from_top(const unsigned *bins, unsigned need,
+                                                  unsigned *above) {
     const int lane = threadIdx.x & 31;
-    unsigned v[8];
-    if (pairs) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(bins + lane * 4);
-        const unsigned w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[2 * i] = w[i] & 0xFFFFu;
-            v[2 * i + 1] = w[i] >> 16;
-        }
-    } else {
-        const uint4 a = *reinterpret_cast<const uint4 *>(bins + lane * 8);
-        const uint4 b = *reinterpret_cast<const uint4 *>(bins + lane * 8 + 4);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-    unsigned mine = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mine += v[i];
-    unsigned suf = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_down_sync(0xffffffffu, suf, o);
-        if (lane + o < 32) suf += y;
-    }
-    const unsigned excl = suf - mine;
-    const unsigned bal = __ballot_sync(0xffffffffu, excl < need && suf >= need);
-    if (bal == 0) return -1;
-    const int src = __ffs(bal) - 1;
-    int bin = -1;
-    unsigned ab = 0;
-    if (lane == src) {
-        unsigned cum = excl;
-        for (int i = 7; i >= 0; --i) {
-            if (cum + v[i] >= need) { bin = lane * 8 + i; ab = cum; break; }
-            cum += v[i];
-        }
-    }
-    bin = __shfl_sync(0xffffffffu, bin, src);
-    *above = __shfl_sync(0xffffffffu, ab, src);
-    return bin;
+    const uint4 a = ld_cg4(bins + lane * 8), b = ld_cg4(bins + lane * 8 + 4);
+    const unsigned v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    return find_from_top8(v, need, above);
 }
+
 
 // 16-bit key prefix whose bin holds the need-th largest entry of a
 // (coarse, fine) global histogram.  Returns -1 if it holds fewer than need;
@@ -369,7 +355,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     if (aborted(p.abort_flag)) return;
 
     // ---- roles: blocks per sequence, proportional to its groups --------------
-    {
+    int b, cb0, n_b, L_b, G_b;
+    if (B == 1) {
+        L_b = __ldg(p.seq_len);
+        G_b = L_b / P;
+        G_b = G_b < 0 ? 0 : (G_b > p.G_max ? p.G_max : G_b);
+        b = 0;
+        cb0 = 0;
+        n_b = ncta;
+        if (tid == 0) { sv[19] = 0; sv[26] = 0; sv[27] = 0; }
+        __syncthreads();
+    } else {
         int gv = 0;
         if (tid < B) {
             const int L = __ldg(p.seq_len + tid);
@@ -377,26 +373,26 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             int G = L / P;
             gv = G < 0 ? 0 : (G > p.G_max ? p.G_max : G);
         }
-        clear_smem(smem + kU, kUBytes);  // overlaps the length load
+        if (tid == 0) { sv[19] = 0; sv[26] = 0; sv[27] = 0; }
         int total;
         const int pre = block_exclusive_scan(gv, scratch, &total);
         if (tid < B) offs[tid] = pre;
-        if (tid == 0) { offs[B] = total; sv[0] = total; }
+        if (tid == 0) offs[B] = total;
         __syncthreads();
-        const long long tot = total > 0 ? total : 1;
+        const double tot = total > 0 ? double(total) : 1.0;
         for (int bb = tid; bb <= B; bb += kThreads)
-            cta_begin[bb] = bb == B ? ncta : bb + int((long long)(ncta - B) * offs[bb] / tot);
+            cta_begin[bb] = bb == B ? ncta : bb + int(double(ncta - B) * double(offs[bb]) / tot);
         __syncthreads();
         for (int bb = tid; bb < B; bb += kThreads)
             if (cta_begin[bb] <= cta && cta < cta_begin[bb + 1]) sv[1] = bb;
         __syncthreads();
+        b = sv[1];
+        cb0 = cta_begin[b];
+        n_b = cta_begin[b + 1] - cb0;
+        L_b = lens[b];
+        G_b = offs[b + 1] - offs[b];
     }
-    const int b = sv[1];
-    const int cb0 = cta_begin[b];
-    const int n_b = cta_begin[b + 1] - cb0;
     const int j = cta - cb0;
-    const int L_b = lens[b];
-    const int G_b = offs[b + 1] - offs[b];
     const int tiles_b = (G_b + 15) / 16;
     auto chunk_lo = [&](int jj) { return 16 * int((long long)tiles_b * jj / n_b); };
     const int g_lo = chunk_lo(j);
@@ -431,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     };
     uint4 c0[4], c1[4];
     if (warp < n_tiles) load_tile(warp, c0);
-    if (warp + kWarps < n_tiles) load_tile(warp + kWarps, c1);
+    if (warp + kStream < n_tiles) load_tile(warp + kStream, c1);
 
     uint32_t bq[NT][4][2];
     float wv[NT][2];
@@ -481,11 +477,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         *reinterpret_cast<uint4 *>(p.k_pooled + int64_t(b) * p.sp_b + int64_t(g_new) * 64 +
                                    tid * 8) = o;
     }
+    // total sample size of the sequence (the chunk split is known to every
+    // block; tiles_b * n_b < 2^32 within the supported sizes)
+    if (tid < n_b) {
+        const int lo = 16 * int(unsigned(tiles_b) * unsigned(tid) / unsigned(n_b));
+        const int hi = min(G_b, 16 * int(unsigned(tiles_b) * unsigned(tid + 1) / unsigned(n_b)));
+        atomicAdd(sv + 26, min(max(hi - lo, 0), kSampleN));
+    }
     __syncthreads();
     PHASE_MARK(2);
 
     // ---- phase 1: stream pooled keys, score, histogram -------------------------
-    auto score_tile = [&](int t, uint4 (&A)[4]) {
+    auto score_tile = [&](int t, uint4 (&A)[4]) -> unsigned {
         const int ga = g_lo + t * 16 + r, gb = ga + 8;
         if (ga == g_new) {  // the freshly pooled key replaces the stale cache row
             A[0] = *reinterpret_cast<const uint4 *>(newkey + 8 * c);
@@ -519,99 +522,149 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         pb = __fadd_rn(pb, __shfl_xor_sync(0xffffffffu, pb, 1));
         pa = __fadd_rn(pa, __shfl_xor_sync(0xffffffffu, pa, 2));
         pb = __fadd_rn(pb, __shfl_xor_sync(0xffffffffu, pb, 2));
-        if (c < 2) {
-            const int li = t * 16 + r + 8 * c;
-            const float sc = __fadd_rn(c == 0 ? pa : pb, 0.0f);
-            if (g_lo + li < g_hi) {
-                if (li < kChunkCap) sscore[li] = sc;
-                else p.gscore[seg + g_lo + li] = sc;
-                if (p.scores_out) p.scores_out[seg + g_lo + li] = sc;
-                const unsigned bin = score_key(sc) >> 16;
-                atomicAdd(h16 + (bin >> 1), (bin & 1u) ? 0x10000u : 1u);
-            }
+        const int li = t * 16 + r + 8 * c;
+        const bool mine = c < 2 && g_lo + li < g_hi;
+        const float sc = __fadd_rn(c == 0 ? pa : pb, 0.0f);
+        if (mine) {
+            if (li < kChunkCap) sscore[li] = sc;
+            else p.gscore[seg + g_lo + li] = sc;
+            if (p.scores_out) p.scores_out[seg + g_lo + li] = sc;
         }
+        return mine ? score_key(sc) >> 16 : 0u;
     };
-    for (int t = warp; t < n_tiles; t += 2 * kWarps) {
+    // Sample: every warp publishes the bins of the kSampW largest keys of its
+    // first two tiles as one 64-bit word of 16-bit entries (a finite score's
+    // bin is at least 0x007F; 1 = no key; 0 = not yet written).  The words are
+    // self-validating, so readers need no fence or arrival counter.
+    auto publish_sample = [&](unsigned ka, unsigned kc) {
+        unsigned long long word = 0;
+#pragma unroll
+        for (int e = 0; e < kSampW; ++e) {
+            const unsigned wm = __reduce_max_sync(0xffffffffu, max(ka, kc));
+            const unsigned hit = __ballot_sync(0xffffffffu, ka == wm || kc == wm);
+            if (lane == __ffs(hit) - 1) {
+                if (ka == wm) ka = 0u;
+                else kc = 0u;
+            }
+            word |= (unsigned long long)max(wm, 1u) << (16 * e);
+        }
+        if (lane == 0) st_relaxed_u64(p.samp + size_t(cta) * kWarps + warp, word);
+    };
+    bool first = true;
+    for (int t = warp; t < n_tiles; t += 2 * kStream) {
         uint4 n0[4], n1[4];
-        const bool m0 = t + 2 * kWarps < n_tiles, m1 = t + 3 * kWarps < n_tiles;
-        if (m0) load_tile(t + 2 * kWarps, n0);
-        if (m1) load_tile(t + 3 * kWarps, n1);
-        score_tile(t, c0);
-        if (t + kWarps < n_tiles) score_tile(t + kWarps, c1);
+        const bool m0 = t + 2 * kStream < n_tiles, m1 = t + 3 * kStream < n_tiles;
+        if (m0) load_tile(t + 2 * kStream, n0);
+        if (m1) load_tile(t + 3 * kStream, n1);
+        const unsigned s0 = score_tile(t, c0);
+        const unsigned s1 = t + kStream < n_tiles ? score_tile(t + kStream, c1) : 0u;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (m0) c0[i] = n0[i];
             if (m1) c1[i] = n1[i];
         }
+        if (first) {
+            publish_sample(s0, s1);
+            first = false;
+        }
     }
+    if (first) publish_sample(0u, 0u);
+    PHASE_MARK(4);
+
+    // The guess: the need-th largest published bin of the sequence, need ~
+    // 1.5 k x (sample size)/G.  Each warp loads its share of the sequence's
+    // sample words once done streaming; the block then selects in shared memory.
+    // It is only a guess: the selection checks that at least k keys cleared it.
+    // Each thread loads its share of the sequence's sample words once its warp is
+    // done streaming (polling until every entry is written), then the block
+    // counts the entries in 2048 bins below the largest one and picks the bin
+    // where the count from the top reaches need.
+    constexpr int kQ16 = (kMaxCtas * kWarps / 2 + kThreads - 1) / kThreads;
+    const int n_q = n_b * kWarps / 2;  // 16-byte chunks of entries
+    uint4 v[kQ16];
+    unsigned emax = 1;
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.samp + size_t(cb0) * kWarps);
+#pragma unroll
+        for (int u = 0; u < kQ16; ++u)
+            if (tid + u * kThreads < n_q) v[u] = ld_relaxed_v4(src + tid + u * kThreads);
+        const long long t0 = clock64();
+        bool ok = true;
+#pragma unroll
+        for (int u = 0; u < kQ16; ++u) {
+            const int q = tid + u * kThreads;
+            if (q >= n_q) break;
+            for (int spin = 0; ok && !all_u16_nonzero(v[u]); ++spin) {
+                if (clock64() - t0 > kSpinBudget || ((spin & 63) == 63 && aborted(p.abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(64);
+                v[u] = ld_relaxed_v4(src + q);
+            }
+            const unsigned w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) emax = max(emax, max(w[e] & 0xFFFFu, w[e] >> 16));
+        }
+        if (!ok) {
+            raise_timeout(p, 1);
+            sv[19] = 1;
+        }
+        emax = __reduce_max_sync(0xffffffffu, emax);
+        if (lane == 0) atomicMax(sv + 27, int(emax));
+    }
+    unsigned *sh = reinterpret_cast<unsigned *>(smem + kSelHist);
+    for (int i = tid; i < 2048; i += kThreads) sh[i] = 0u;
+    __syncthreads();
+    PHASE_MARK(20);
+    if (sv[19]) return;  // the sample never completed
+    int sguess = 0;
+    const unsigned need = unsigned(max(1ull, (3ull * unsigned(k_b) * unsigned(sv[26]) + 2ull * G_b - 1) /
+                                                 (2ull * G_b)));
+    if (k_b > 0 && n_b > 1 && need <= unsigned(n_q * 8)) {
+        const unsigned base = unsigned(max(0, sv[27] - 2047));
+#pragma unroll
+        for (int u = 0; u < kQ16; ++u) {
+            if (tid + u * kThreads >= n_q) break;
+            const unsigned w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                atomicAdd(sh + (max(w[e] & 0xFFFFu, base) - base), 1u);
+                atomicAdd(sh + (max(w[e] >> 16, base) - base), 1u);
+            }
+        }
+        __syncthreads();
+        PHASE_MARK(21);
+        unsigned above = 0;
+        sguess = int(base) + find_digit(sh, 2048, need, &above, scratch, sv + 12);
+        PHASE_MARK(22);
+    }
+    if (tid == 0) sv[3] = sguess;
     if (p.scores_out && j == 0)  // -inf past the last complete group: the full row
         for (int g = G_b + tid; g < p.G_max; g += kThreads) p.scores_out[seg + g] = -INFINITY;
-    __syncthreads();
-    auto coarse_from_fine = [&]() {
-        for (int cbin = warp; cbin < kCoarse; cbin += kWarps) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(h16 + cbin * 128 + lane * 4);
-            unsigned s = (w.x & 0xFFFFu) + (w.x >> 16) + (w.y & 0xFFFFu) + (w.y >> 16) +
-                         (w.z & 0xFFFFu) + (w.z >> 16) + (w.w & 0xFFFFu) + (w.w >> 16);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) ccoarse[cbin] = s;
-        }
-    };
-    coarse_from_fine();
     __syncthreads();
     PHASE_MARK(3);
     auto score_at = [&](int li) -> float {
         return li < kChunkCap ? sscore[li] : ld_cg_f(p.gscore + seg + g_lo + li);
     };
 
-    // ---- local candidates: the block's top-m keys by 16-bit bin -----------------
+    // ---- candidates: this block's keys at or above the guess --------------------
     const int spec_cap = kSpecTok / P;
-    if (warp == 0) {
-        int pj = kFine, p2 = kFine;  // bins >= pj are published; >= p2 prefetched
-        if (nloc > 0 && k_b > 0) {
-            const int m = min(nloc, 2 * ((k_b + n_b - 1) / n_b) + 8);
-            unsigned ab_c = 0, ab_f = 0;
-            const int cm = smem_find_from_top(ccoarse, unsigned(m), &ab_c, false);
-            const int fm = smem_find_from_top(h16 + cm * 128, unsigned(m) - ab_c, &ab_f, true);
-            pj = cm * 256 + fm;
-            const unsigned binv = (h16[pj >> 1] >> ((pj & 1) * 16)) & 0xFFFFu;
-            const unsigned cnt = ab_c + ab_f + binv;  // keys at or above bin pj
-            p2 = pj;
-            if (cnt > unsigned(spec_cap)) {
-                unsigned a2 = 0, f2 = 0;
-                const int c2 = smem_find_from_top(ccoarse, unsigned(spec_cap), &a2, false);
-                const int ff = smem_find_from_top(h16 + c2 * 128, unsigned(spec_cap) - a2, &f2, true);
-                p2 = c2 * 256 + ff;
-            }
-        }
-        if (lane == 0) { sv[3] = pj; sv[4] = p2; }
-    }
-    __syncthreads();
-    PHASE_MARK(4);
+    const unsigned guess = unsigned(sv[3]);
     {
-        const unsigned pj = unsigned(sv[3]), p2 = unsigned(sv[4]);
         const int per = (nloc + kThreads - 1) / kThreads;
         const int i0 = min(nloc, tid * per), i1 = min(nloc, i0 + per);
-        int nc = 0, ns = 0;
-        unsigned maxex = 0;
-        for (int i = i0; i < i1; ++i) {
-            const unsigned key = score_key(score_at(i));
-            if ((key >> 16) >= pj) {
-                ++nc;
-                ns += (key >> 16) >= p2;
-            } else {
-                maxex = max(maxex, key);
-            }
-        }
-        int tot_s;
-        const unsigned packed = unsigned(block_exclusive_scan(nc | (ns << 16), scratch, &tot_s));
-        const unsigned tot = unsigned(tot_s);  // low half: candidates, high half: prefetched
-        int pos = int(packed & 0xFFFFu), spos = int(packed >> 16);
+        int nc = 0;
+        for (int i = i0; i < i1; ++i) nc += (score_key(score_at(i)) >> 16) >= guess;
+        PHASE_MARK(5);
+        int tot;
+        int pos = block_exclusive_scan(nc, scratch, &tot);
+        PHASE_MARK(6);
         unsigned char *slot = p.slots + size_t(cta) * kSlotBytes;
         unsigned *ent = reinterpret_cast<unsigned *>(slot + 16);
         for (int i = i0; i < i1; ++i) {
             const unsigned key = score_key(score_at(i));
-            if ((key >> 16) >= pj) {
+            if ((key >> 16) >= guess) {
                 if (pos < kSlot) {
                     ent[2 * pos] = key;
                     ent[2 * pos + 1] = unsigned(g_lo + i);
@@ -619,30 +672,26 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                     p.cand_key[seg + g_lo + pos - kSlot] = key;
                     p.cand_g[seg + g_lo + pos - kSlot] = g_lo + i;
                 }
+                if (pos < spec_cap) spec_g[pos] = g_lo + i;
                 ++pos;
-                if ((key >> 16) >= p2) {
-                    if (spos < spec_cap) spec_g[spos] = g_lo + i;
-                    ++spos;
-                }
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) maxex = max(maxex, __shfl_xor_sync(0xffffffffu, maxex, o));
-        if (lane == 0) scratch[warp] = int(maxex);
-        __syncthreads();
+        PHASE_MARK(7);
         if (tid == 0) {
-            unsigned mx = 0;
-            for (int w = 0; w < kWarps; ++w) mx = max(mx, unsigned(scratch[w]));
-            *reinterpret_cast<uint4 *>(slot) = make_uint4(tot & 0xFFFFu, mx, pj, 0u);
-            sv[5] = min(int(tot >> 16), spec_cap);  // prefetched groups
+            *reinterpret_cast<uint4 *>(slot) = make_uint4(unsigned(tot), 0u, guess, 0u);
+            sv[5] = min(tot, spec_cap);  // prefetched groups (the first ones)
         }
     }
     __syncthreads();
-    PHASE_MARK(5);
-    // prefetch this block's best candidates' K/V and the first head group's Q
+    PHASE_MARK(8);
     const int n_spec = sv[5];
     uint16_t *spk = reinterpret_cast<uint16_t *>(smem + kSpec);
     uint16_t *spv = spk + kChunk * QP;
+    if (p.skip_arrive && j == n_b - 1 && n_b > 1) {  // failure-detection test only
+        return;
+    }
+    arrive(ctl + kCands);
+    // prefetch this block's candidates' K/V and the first head group's Q
     gather_chunk<DQK, DV>(spk, spv, spec_sg, spec_g, n_spec, P, G_b, Kb, Vb, QP, VP, tid, kThreads);
     {
         const int HG0 = min(64, p.H_q);
@@ -653,20 +702,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
         cp_async_commit();
     }
-    PHASE_MARK(6);
-    if (p.skip_arrive && j == n_b - 1 && n_b > 1) {  // failure-detection test only
-        cp_async_wait<0>();
-        return;
-    }
-    arrive(ctl + kCands);
-    PHASE_MARK(7);
+    PHASE_MARK(9);
 
     // ---- selection: exact top k from the published candidates -----------------
     if (!wait_count(p, ctl + kCands, unsigned(n_b), 2, s_ok)) {
         cp_async_wait<0>();
         return;
     }
-    PHASE_MARK(8);
+    PHASE_MARK(10);
+    // everyone has read the sample words: clear this block's for the next call
+    if (tid < kWarps) st_relaxed_u64(p.samp + size_t(cta) * kWarps + tid, 0ull);
     unsigned char *stage = smem + kStage;
     {
         const int n16 = n_b * (kSlotBytes / 16);
@@ -688,45 +733,56 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     __syncthreads();
     auto hdr = [&](int jj) { return reinterpret_cast<const unsigned *>(stage + jj * kSlotBytes); };
     if (warp == 0) {
-        int run = 0;
-        unsigned minp = kFine, mx = 0;
+        // counts -> offsets (each lane owns up to 5 consecutive blocks)
+        constexpr int kPer = (kMaxCtas + 31) / 32;
+        int v[kPer];
+        int s = 0;
+        unsigned minp = kFine, maxp = 0;
         int over = 0;
-        for (int base = 0; base < n_b; base += 32) {
-            const int jj = base + lane;
-            int v = 0;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int jj = lane * kPer + u;
+            v[u] = 0;
             if (jj < n_b) {
                 const unsigned *h = hdr(jj);
-                v = int(h[0]);
-                mx = max(mx, h[1]);
-                if (v > 0) minp = min(minp, h[2]);
-                over |= v > kSlot;
+                v[u] = int(h[0]);
+                minp = min(minp, h[2]);
+                maxp = max(maxp, h[2]);
+                over |= v[u] > kSlot;
             }
-            int x = v;
+            s += v[u];
+        }
+        int x = s;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if (jj < n_b) offs[jj] = run + x - v;
-            run += __shfl_sync(0xffffffffu, x, 31);
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        int run = x - s;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int jj = lane * kPer + u;
+            if (jj < n_b) offs[jj] = run;
+            run += v[u];
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             minp = min(minp, __shfl_xor_sync(0xffffffffu, minp, o));
+            maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
             over |= __shfl_xor_sync(0xffffffffu, over, o);
         }
+        const int total = __shfl_sync(0xffffffffu, x, 31);
         if (lane == 0) {
-            offs[n_b] = run;
-            sv[6] = run;
-            sv[7] = int(mx);
+            offs[n_b] = total;
+            sv[6] = total;
+            sv[7] = int(maxp);
             sv[8] = int(minp);
             sv[9] = over;
         }
     }
     __syncthreads();
     const int n_cand = sv[6];
-    const unsigned maxex_all = unsigned(sv[7]);
+    const unsigned maxguess = unsigned(sv[7]);
     bool fast = !p.force_slow && n_cand <= kSelCap && n_cand >= k_b;
     unsigned kth = 0xFFFFFFFFu, take_eq = 0;
     unsigned *ckey = reinterpret_cast<unsigned *>(smem + kCKey);
@@ -752,25 +808,19 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             }
         }
         __syncthreads();
-        PHASE_MARK(9);
+        PHASE_MARK(11);
         if (k_b > 0) {
-            // histogram of the 16-bit bin relative to the smallest published bin
+            // histogram of the 16-bit bin relative to the smallest guess
             unsigned *sh = reinterpret_cast<unsigned *>(smem + kSelHist);
             const unsigned minp = unsigned(sv[8]);
             for (int i = tid; i < 2048; i += kThreads) sh[i] = 0u;
             if (tid == 0) sv[10] = 0;
             __syncthreads();
-            for (int i = tid; i < ((n_cand + 31) & ~31); i += kThreads) {
-                unsigned d = 0;
-                bool on = i < n_cand;
-                if (on) d = min(2047u, (ckey[i] >> 16) - minp);
-                hist_add(sh, d, on);
-            }
+            for (int i = tid; i < n_cand; i += kThreads)
+                atomicAdd(sh + min(2047u, (ckey[i] >> 16) - minp), 1u);
             __syncthreads();
-            PHASE_MARK(10);
             unsigned above;
             const int T = find_digit(sh, 2048, unsigned(k_b), &above, scratch, sv + 12);
-            PHASE_MARK(11);
             const unsigned need_t = unsigned(k_b) - above;
             const int m_t = int(sh[T]);
             if (T < 2047 && m_t <= kTieCap) {
@@ -783,37 +833,29 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                     }
                 }
                 __syncthreads();
+                unsigned rank = 0, ke = 0;
                 if (tid < m_t) {
-                    const unsigned ke = tie[2 * tid], ie = tie[2 * tid + 1];
-                    unsigned rank = 0;
+                    ke = tie[2 * tid];
+                    const unsigned ie = tie[2 * tid + 1];
                     for (int f = 0; f < m_t; ++f) {
                         const unsigned kf = tie[2 * f], jf = tie[2 * f + 1];
                         rank += kf > ke || (kf == ke && jf < ie);
                     }
                     if (rank == need_t - 1) sv[14] = int(ke);  // the k-th largest key
                 }
-                __syncthreads();
-                kth = unsigned(sv[14]);
                 if (tid == 0) sv[15] = 0;
                 __syncthreads();
-                if (tid < m_t) {
-                    const unsigned ke = tie[2 * tid], ie = tie[2 * tid + 1];
-                    if (ke == kth) {
-                        unsigned rank = 0;
-                        for (int f = 0; f < m_t; ++f) {
-                            const unsigned kf = tie[2 * f], jf = tie[2 * f + 1];
-                            rank += kf > ke || (kf == ke && jf < ie);
-                        }
-                        if (rank < need_t) atomicAdd(sv + 15, 1);
-                    }
-                }
+                kth = unsigned(sv[14]);
+                if (tid < m_t && ke == kth && rank < need_t) atomicAdd(sv + 15, 1);
                 __syncthreads();
                 take_eq = unsigned(sv[15]);
             } else {
                 kth = radix_select_smem(ckey, n_cand, unsigned(k_b), sh, scratch, sv + 12,
                                         &take_eq);
             }
-            fast = kth > maxex_all;  // the union of local top-m sets holds the true top k
+            // exact iff every block's guess was at or below K*: then every key a
+            // block left out is below K* and cannot be in the top k
+            fast = (kth >> 16) >= maxguess;
         }
     }
     PHASE_MARK(12);
@@ -826,28 +868,47 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         const int o0 = offs[j], o1 = offs[j + 1];
         int eqb = 0;
         for (int i = tid; i < o0; i += kThreads) eqb += ckey[i] == kth;
-        int tot;
-        block_exclusive_scan(eqb, scratch, &tot);
-        const int eq_before_own = tot;
-        const int per = (o1 - o0 + kThreads - 1) / kThreads;
-        const int i0 = min(o1, o0 + tid * per), i1 = min(o1, i0 + per);
-        int n_eq = 0;
-        for (int i = i0; i < i1; ++i) n_eq += ckey[i] == kth;
-        int tq;
-        const int eq_start = eq_before_own + block_exclusive_scan(n_eq, scratch, &tq);
-        int eqr = eq_start, nsel = 0;
-        for (int i = i0; i < i1; ++i) {
-            const unsigned kk = ckey[i];
-            nsel += kk > kth || (kk == kth && unsigned(eqr++) < take_eq);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) eqb += __shfl_xor_sync(0xffffffffu, eqb, o);
+        if (lane == 0) scratch[warp] = eqb;
+        __syncthreads();
+        if (warp == 0) {
+            int eqr = lane < kWarps ? scratch[lane] : 0;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) eqr += __shfl_xor_sync(0xffffffffu, eqr, o);
+            int np = 0;
+            for (int base = o0; base < o1; base += 32) {
+                const int i = base + lane;
+                const unsigned kk = i < o1 ? ckey[i] : 0u;
+                const bool gt = i < o1 && kk > kth, eq = i < o1 && kk == kth;
+                const unsigned beq = __ballot_sync(0xffffffffu, eq);
+                const int eq_rank = eqr + __popc(beq & ((1u << lane) - 1u));
+                const bool sel = gt || (eq && unsigned(eq_rank) < take_eq);
+                const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+                if (sel) own[np + __popc(bsel & ((1u << lane) - 1u))] = cgrp[i];
+                np += __popc(bsel);
+                eqr += __popc(beq);
+            }
+            // the prefetched groups serve as the attention chunk if they cover ours
+            __syncwarp();
+            bool ok_l = true;
+            for (int i = lane; i < np; i += 32) {
+                bool found = false;
+                for (int s2 = 0; s2 < n_spec; ++s2) found |= spec_g[s2] == own[i];
+                ok_l = ok_l && found;
+            }
+            const bool cover = np <= n_spec && __all_sync(0xffffffffu, ok_l);
+            if (lane == 0) { sv[16] = np; sv[18] = cover ? 1 : 0; }
         }
-        int tsel;
-        int pos = block_exclusive_scan(nsel, scratch, &tsel);
-        eqr = eq_start;
-        for (int i = i0; i < i1; ++i) {
-            const unsigned kk = ckey[i];
-            if (kk > kth || (kk == kth && unsigned(eqr++) < take_eq)) own[pos++] = cgrp[i];
+        __syncthreads();
+        n_own = sv[16];
+        use_spec = sv[18] != 0 && n_own <= spec_cap;
+        if (use_spec && tid < spec_cap) {
+            bool keep = false;
+            if (tid < n_spec)
+                for (int i = 0; i < n_own; ++i) keep |= own[i] == spec_g[tid];
+            if (!keep) spec_sg[tid] = -1;  // prefetched but not selected: masked
         }
-        n_own = tsel;
         PHASE_MARK(13);
         // the full ascending selection, for the optional index output
         if (p.idx_out && j == 0) {
@@ -890,22 +951,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 __syncthreads();
             }
             for (int i = k_b + tid; i < p.k; i += kThreads) p.idx_out[int64_t(b) * p.k + i] = -1;
-        }
-        // the prefetched groups serve as the attention chunk if they cover ours
-        if (tid == 0) sv[18] = 1;
-        __syncthreads();
-        for (int i = tid; i < n_own; i += kThreads) {
-            bool found = false;
-            for (int s = 0; s < n_spec; ++s) found |= spec_g[s] == own[i];
-            if (!found) sv[18] = 0;
-        }
-        __syncthreads();
-        use_spec = sv[18] != 0 && n_own <= spec_cap;
-        if (use_spec && tid < spec_cap) {
-            bool keep = false;
-            if (tid < n_spec)
-                for (int i = 0; i < n_own; ++i) keep |= own[i] == spec_g[tid];
-            if (!keep) spec_sg[tid] = -1;  // prefetched but not selected: masked
         }
         __syncthreads();
     } else {
@@ -1222,7 +1267,7 @@ constexpr int smem_bytes() {
 }
 
 struct WsLayout {
-    size_t ctl, hist, slots, cand_key, cand_g, gscore, cta_cnt, idx_ws, part_o, part_ml, total;
+    size_t ctl, hist, samp, slots, cand_key, cand_g, gscore, cta_cnt, idx_ws, part_o, part_ml, total;
 };
 
 WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int ncta) {
@@ -1235,6 +1280,7 @@ WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int ncta) {
     };
     w.ctl = take(size_t(B) * kCtlWords * 4);
     w.hist = take(size_t(B) * 2 * kHistWords * 4);
+    w.samp = take(size_t(ncta) * kWarps * 8);
     w.slots = take(size_t(ncta) * kSlotBytes);
     w.cand_key = take(size_t(B) * G_max * 4);
     w.cand_g = take(size_t(B) * G_max * 4);
@@ -1345,6 +1391,7 @@ cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status
     prm.scores_out = a->scores_out;
     prm.ctl = reinterpret_cast<unsigned *>(base + w.ctl);
     prm.hist = reinterpret_cast<unsigned *>(base + w.hist);
+    prm.samp = reinterpret_cast<unsigned long long *>(base + w.samp);
     prm.slots = reinterpret_cast<unsigned char *>(base + w.slots);
     prm.cand_key = reinterpret_cast<unsigned *>(base + w.cand_key);
     prm.cand_g = reinterpret_cast<int32_t *>(base + w.cand_g);
