@@ -169,6 +169,36 @@ lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_
                              void *ws, size_t ws_bytes, lcsw_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * lcsw_sparse_attn without a caller workspace.  The pages have no counterpart
+ * of this entry point: it serves callers that cannot allocate device memory
+ * per call -- a plain-C host over this header with no device allocator of its
+ * own, or a runtime whose device memory is budgeted up front -- and callers
+ * that must not let a cudaMalloc/cudaFree synchronise the device mid-step.
+ *
+ * Arguments, results and errors are those of lcsw_sparse_attn, minus ws and
+ * ws_bytes.  The split-K partial states go to a fixed scratch array of
+ * LCSW_NOALLOC_SCRATCH_BYTES in the library's device memory, one per device.
+ *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
+ *   - A shape whose lcsw_sparse_attn_workspace_size(...) exceeds
+ *     LCSW_NOALLOC_SCRATCH_BYTES is rejected with LCSW_ERR_UNSUPPORTED (the
+ *     message gives both sizes) before any device work.
+ *   - Set-up: the first call on each device, with that device current, looks
+ *     up the array's address (cudaGetSymbolAddress; a failure returns
+ *     LCSW_ERR_CUDA).  That first call must come before any stream capture.
+ *   - Nothing in the scratch has to start at zero: a call writes every partial
+ *     state it reads.
+ *   - One scratch per device: calls that overlap in time on the same device
+ *     (two streams, or two host threads) race on it and give wrong results.
+ *     Order them (one stream, or an event between them).
+ * ------------------------------------------------------------------------- */
+#define LCSW_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
+lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_b,
+                                     const lcsw_bf16 *V, int64_t sV_b, const int32_t *seq_len,
+                                     const int32_t *idx, int B, int T, int H_q, int d_qk,
+                                     int d_v, int P, int k, float scale, lcsw_bf16 *out,
+                                     float *lse, lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
  * One decode step of the whole retrieval path (one query token per sequence):
  * [append] -> scores -> top-k -> sparse attention, as one persistent kernel.
  *

@@ -72,6 +72,8 @@ _SIGNATURES = {
     "lcsw_sparse_attn_workspace_size": ([_i32, _i32, _i32, _i32, _i32, _i32], _sz),
     "lcsw_sparse_attn": ([_vp, _vp, _i64, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                           _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp], _i32),
+    "lcsw_sparse_attn_noalloc": ([_vp, _vp, _i64, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
+                                  _i32, _i32, _i32, _f32, _vp, _vp, _vp], _i32),
     "lcsw_decode_workspace_size": ([ctypes.POINTER(DecodeArgs)], _sz),
     "lcsw_decode_fused": ([ctypes.POINTER(DecodeArgs), _vp, _sz, _vp], _i32),
     "lcsw_decode_launches": ([ctypes.POINTER(DecodeArgs)], _i32),
@@ -221,6 +223,30 @@ def sparse_attn(q, K, V, seq_len, idx, P, scale, out=None, lse=None, ws=None, st
                                   _ptr(seq_len), _ptr(idx), B, T, H_q, d_qk, d_v, P, k,
                                   float(scale), _ptr(out), _ptr(lse), _ptr(ws), nbytes,
                                   _stream(stream)))
+    return out, lse
+
+
+def sparse_attn_noalloc(q, K, V, seq_len, idx, P, scale, out, lse=None, stream=None):
+    """sparse_attn through the entry point that takes no workspace.
+
+    The library keeps the split-K scratch in a fixed per-device array, so this
+    call allocates nothing on the device: `out` (and `lse`, if wanted) are the
+    caller's.  Calls that overlap in time on one device race on that scratch.
+    """
+    _bf16(q, "q", 4)
+    _bf16(K, "K", 3)
+    _bf16(V, "V", 3)
+    _bf16(out, "out", 4)
+    _dense(idx, torch.int32, "idx")
+    _dense(seq_len, torch.int32, "seq_len")
+    if lse is not None:
+        _dense(lse, torch.float32, "lse")
+    B, T, H_q, d_qk = q.shape
+    d_v = V.shape[2]
+    k = idx.shape[-1]
+    _check(lib().lcsw_sparse_attn_noalloc(_ptr(q), _ptr(K), K.stride(0), _ptr(V), V.stride(0),
+                                          _ptr(seq_len), _ptr(idx), B, T, H_q, d_qk, d_v, P, k,
+                                          float(scale), _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
 
 

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/lcsw.h"
 #include "fused.cuh"
@@ -59,6 +60,43 @@ bool attn_shape_ok(int H_q, int d_qk, int d_v) {
     const bool heads = H_q > 0 && H_q % 16 == 0 && (H_q <= 32 || H_q % 64 == 0);
     const bool dims = (d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128);
     return heads && dims;
+}
+
+}  // namespace
+
+// ------------------------------------------------ fixed split-K scratch ----
+// Device memory of lcsw_sparse_attn_noalloc: the split-K partial states live
+// in this file-scope array (one instance per device, created with the
+// library's module), so that entry point needs no workspace and allocates
+// nothing.  Nothing in it has to start at zero: each call writes every partial
+// state it reads.  Calls that overlap in time on one device share it and race.
+static __device__ __align__(256) unsigned char g_attn_scratch[LCSW_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Set-up, once per device, with that device current: look up the array's
+// device address.  Runs inside the first lcsw_sparse_attn_noalloc call on the
+// device.
+lcsw_status attn_scratch(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(LCSW_ERR_UNSUPPORTED, "device ordinal %d above the %d the fixed scratch covers",
+                    dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(split-K scratch)");
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return LCSW_OK;
 }
 
 }  // namespace
@@ -368,6 +406,27 @@ lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
                                  a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale, a->out, a->lse,
                                  w.attn, st);
     return cuda_status(e, "prefill attention");
+}
+
+lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_b,
+                                     const lcsw_bf16 *V, int64_t sV_b, const int32_t *seq_len,
+                                     const int32_t *idx, int B, int T, int H_q, int d_qk,
+                                     int d_v, int P, int k, float scale, lcsw_bf16 *out,
+                                     float *lse, lcsw_stream stream) {
+    // the size check needs no device: an oversized call launches nothing
+    if (B > 0 && T > 0 && H_q > 0 && d_v > 0 && k > 0 && p_ok(P)) {
+        const size_t need = lcsw_sparse_attn_workspace_size(B, T, H_q, d_v, k, P);
+        if (need > size_t(LCSW_NOALLOC_SCRATCH_BYTES))
+            return fail(LCSW_ERR_UNSUPPORTED,
+                        "sparse_attn_noalloc: this shape needs %zu bytes of split-K scratch, above "
+                        "the fixed %zu; call lcsw_sparse_attn with a workspace instead",
+                        need, size_t(LCSW_NOALLOC_SCRATCH_BYTES));
+    }
+    void *scratch = nullptr;
+    const lcsw_status s = attn_scratch(&scratch);
+    if (s != LCSW_OK) return s;
+    return lcsw_sparse_attn(q, K, sK_b, V, sV_b, seq_len, idx, B, T, H_q, d_qk, d_v, P, k, scale,
+                            out, lse, scratch, size_t(LCSW_NOALLOC_SCRATCH_BYTES), stream);
 }
 
 lcsw_status lcsw_get_status(void *ws, lcsw_stream stream) {
