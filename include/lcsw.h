@@ -211,8 +211,10 @@ lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int
  *
  * The workspace must be zero-filled once before its first use; the call
  * leaves it ready for the next call.  After LCSW_ERR_TIMEOUT from
- * lcsw_get_status it must be zero-filled again.  Calls that share a
- * workspace must not overlap on the device.
+ * lcsw_get_status it must be zero-filled again, and so before it serves
+ * arguments of another shape (B, G_max, k, H_q, d_v): it carries state from
+ * one call to the next.  Calls that share a workspace must not overlap on the
+ * device.
  * ------------------------------------------------------------------------- */
 typedef struct {
     const lcsw_bf16 *q_idx;    /* [B][H_i][d_idx]                              */

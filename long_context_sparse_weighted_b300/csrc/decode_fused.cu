@@ -6,10 +6,15 @@
 //
 // Work split.  Every sequence b gets a contiguous set of n_b >= 1 blocks,
 // proportional to its number of pooled groups G_b; block j of the set owns a
-// contiguous chunk of 16-group tiles.  Cross-block sync points are per
-// sequence arrival counters (fence + fire-and-forget add; bounded polling).
-// On a wait that runs out the block records LCSW_ERR_TIMEOUT in the workspace
-// status word, raises an abort flag every other wait honours, and returns.
+// contiguous chunk of 16-group tiles.  Blocks exchange data (sample words,
+// candidate slots, partial attention states) through words that are nonzero
+// once written: a reader polls the data itself, with no fence or arrival
+// counter.  Sample and candidate words are double-buffered by a per-call parity
+// (each block clears its own words of the idle buffer); partial states are
+// cleared by the one block that reads them.  Only the exact fallback selection
+// syncs through arrival counters.  On a wait that runs out the block records
+// LCSW_ERR_TIMEOUT in the workspace status word, raises an abort flag every
+// other wait honours, and returns.
 //
 // Phase 1 (HBM stream).  All 16 warps stream their tiles' pooled keys
 // straight into mma.sync A fragments (the k-permuted layout of
@@ -57,8 +62,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kFine = 65536, kCoarse = 256, kHistWords = kFine + kCoarse;
 constexpr int kChunkCap = 12288;   // scores of a block's chunk kept in shared memory
 constexpr int kSelCap = 4096;      // candidates selected in shared memory (fast path)
-constexpr int kSlot = 24;          // candidates published in a block's fixed slot
-constexpr int kSlotBytes = 16 + kSlot * 8;
+constexpr int kSlot = 25;          // candidates published in a block's fixed slot
+constexpr int kSlotWords = 1 + kSlot;  // 64-bit words: header, entries
+constexpr int kSlotBytes = kSlotWords * 8;
 constexpr int kSpecTok = 64;       // tokens of own candidates prefetched into shared memory
 constexpr int kTieCap = 256;       // threshold-bin candidates resolved by rank counting
 constexpr int kMaxK = 2048;        // selected groups per sequence
@@ -69,8 +75,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // control words (per sequence): arrival counters of the step's sync points,
 // reset to zero by the last block to leave the kernel
-constexpr int kCands = 0, kSlowB = 1, kSlowC = 2, kSlowD = 3, kAtt = 4, kDepart = 5,
-              kNumCounters = 6;
+constexpr int kSlowB = 1, kSlowC = 2, kSlowD = 3, kNumCounters = 4;
 constexpr int kStream = kWarps;    // streaming warps
 constexpr int kSampW = 4;          // sample bins each warp publishes (one 64-bit word)
 constexpr int kSampleN = 2 * kStream * 16;  // sample: the first groups of each block's chunk
@@ -118,10 +123,16 @@ struct Params {
     // workspace
     unsigned *ctl;        // [B][kCtlWords]
     unsigned *hist;       // [B][2][kHistWords]: level 1, level 2 (zero between calls)
-    unsigned long long *samp;  // [ncta][kWarps]: each warp's sample bins (zero between calls)
-    unsigned char *slots; // [ncta][kSlotBytes]: count, max left-out key, bin, -, entries
-    unsigned *cand_key;   // [B][G_max] candidates past a slot's capacity
-    int32_t *cand_g;      // [B][G_max]
+    // Exchange buffers, two of each: a call uses buffer `parity` and clears its
+    // own words of the other one, which the next call uses.  Every word is
+    // written once per call and is nonzero once written, so a reader polls the
+    // data itself (no fence, no arrival counter).
+    unsigned long long *samp;  // [2][ncta][kWarps]: each warp's sample bins
+    unsigned long long *slots; // [2][ncta][kSlotWords]: (count+1 | guess<<32), (key | g<<32)...
+    unsigned long long *cand;  // [2][B][G_max]: entries past a slot's capacity, at g_lo + i
+    int2 *ovf;                 // [2][ncta]: (first index, count) of a block's entries in cand
+    unsigned *parity;          // ws word 2: buffer of this call, flipped by the last block
+    unsigned *gdepart;         // ws word 3: blocks done with this call
     float *gscore;        // [B][G_max] spill of scores past kChunkCap
     unsigned *cta_cnt;    // [2][ncta]: keys > K*, keys == K* (exact path)
     int32_t *idx_ws;      // [B][k]
@@ -200,6 +211,37 @@ __device__ __forceinline__ uint4 ld_relaxed_v4(const uint4 *p) {
                  : "l"(p));
     return r;
 }
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long r;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(r) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ ulonglong2 ld_relaxed_u64x2(const unsigned long long *p) {
+    ulonglong2 r;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(r.x), "=l"(r.y) : "l"(p));
+    return r;
+}
+// Partial attention states travel as (float bits) ^ kPartTag: a stored 0 is a
+// word not yet written (the tag is a signalling-NaN pattern no arithmetic
+// produces).
+constexpr unsigned kPartTag = 0x7FBFFFFFu;
+__device__ __forceinline__ void st_part2(float *p, float a, float b) {
+    asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(p),
+                 "r"(__float_as_uint(a) ^ kPartTag), "r"(__float_as_uint(b) ^ kPartTag)
+                 : "memory");
+}
+__device__ __forceinline__ uint2 ld_relaxed_u32x2(const void *p) {
+    uint2 r;
+    asm volatile("ld.relaxed.gpu.global.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st_relaxed_zero2(void *p) {
+    asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%1};" ::"l"(p), "r"(0u) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_zero4(void *p) {
+    asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%1,%1,%1};" ::"l"(p), "r"(0u) : "memory");
+}
+__device__ __forceinline__ float part_dec(unsigned w) { return __uint_as_float(w ^ kPartTag); }
 __device__ __forceinline__ bool all_u16_nonzero(uint4 v) {
     const unsigned w[4] = {v.x, v.y, v.z, v.w};
     bool ok = true;
@@ -352,7 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     const int cta = blockIdx.x, ncta = gridDim.x;
     const int B = p.B, P = p.P;
     PHASE_MARK(0);
-    if (aborted(p.abort_flag)) return;
+    // this call's exchange buffers (the previous call's last block flipped it)
+    const int par = int(ld_cg(p.parity) & 1u);
+    unsigned long long *samp_cur = p.samp + size_t(par) * ncta * kWarps;
+    unsigned long long *slots_cur = p.slots + size_t(par) * ncta * kSlotWords;
+    unsigned long long *cand_cur = p.cand + size_t(par) * p.B * p.G_max;
+    // where this block's overflow entries went in the previous call (cleared at
+    // the end of this one)
+    const int2 ovf_old = p.ovf[(par ^ 1) * ncta + cta];
 
     // ---- roles: blocks per sequence, proportional to its groups --------------
     int b, cb0, n_b, L_b, G_b;
@@ -451,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
     }
 
+    PHASE_MARK(23);
     // append: the block owning the group the newest token completes pools it
     int g_new = -1;
     if (p.k_idx && G_b > 0 && L_b % P == 0) g_new = G_b - 1;
@@ -477,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         *reinterpret_cast<uint4 *>(p.k_pooled + int64_t(b) * p.sp_b + int64_t(g_new) * 64 +
                                    tid * 8) = o;
     }
+    PHASE_MARK(24);
     // total sample size of the sequence (the chunk split is known to every
     // block; tiles_b * n_b < 2^32 within the supported sizes)
     if (tid < n_b) {
@@ -548,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             }
             word |= (unsigned long long)max(wm, 1u) << (16 * e);
         }
-        if (lane == 0) st_relaxed_u64(p.samp + size_t(cta) * kWarps + warp, word);
+        if (lane == 0) st_relaxed_u64(samp_cur + size_t(cta) * kWarps + warp, word);
     };
     bool first = true;
     for (int t = warp; t < n_tiles; t += 2 * kStream) {
@@ -584,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     uint4 v[kQ16];
     unsigned emax = 1;
     {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.samp + size_t(cb0) * kWarps);
+        const uint4 *src = reinterpret_cast<const uint4 *>(samp_cur + size_t(cb0) * kWarps);
 #pragma unroll
         for (int u = 0; u < kQ16; ++u)
             if (tid + u * kThreads < n_q) v[u] = ld_relaxed_v4(src + tid + u * kThreads);
@@ -660,26 +711,21 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         int tot;
         int pos = block_exclusive_scan(nc, scratch, &tot);
         PHASE_MARK(6);
-        unsigned char *slot = p.slots + size_t(cta) * kSlotBytes;
-        unsigned *ent = reinterpret_cast<unsigned *>(slot + 16);
+        unsigned long long *slot = slots_cur + size_t(cta) * kSlotWords;
         for (int i = i0; i < i1; ++i) {
             const unsigned key = score_key(score_at(i));
             if ((key >> 16) >= guess) {
-                if (pos < kSlot) {
-                    ent[2 * pos] = key;
-                    ent[2 * pos + 1] = unsigned(g_lo + i);
-                } else {
-                    p.cand_key[seg + g_lo + pos - kSlot] = key;
-                    p.cand_g[seg + g_lo + pos - kSlot] = g_lo + i;
-                }
+                const unsigned long long e = key | ((unsigned long long)(g_lo + i) << 32);
+                if (pos < kSlot) st_relaxed_u64(slot + 1 + pos, e);
+                else st_relaxed_u64(cand_cur + seg + g_lo + pos - kSlot, e);
                 if (pos < spec_cap) spec_g[pos] = g_lo + i;
                 ++pos;
             }
         }
         PHASE_MARK(7);
         if (tid == 0) {
-            *reinterpret_cast<uint4 *>(slot) = make_uint4(unsigned(tot), 0u, guess, 0u);
             sv[5] = min(tot, spec_cap);  // prefetched groups (the first ones)
+            sv[28] = tot;
         }
     }
     __syncthreads();
@@ -690,7 +736,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     if (p.skip_arrive && j == n_b - 1 && n_b > 1) {  // failure-detection test only
         return;
     }
-    arrive(ctl + kCands);
+    if (tid == 0) {  // the header: count + 1 (nonzero once written) and the guess
+        st_relaxed_u64(slots_cur + size_t(cta) * kSlotWords,
+                       (unsigned(sv[28]) + 1u) | ((unsigned long long)guess << 32));
+        p.ovf[par * ncta + cta] = make_int2(int(seg + g_lo), max(0, sv[28] - kSlot));
+    }
     // prefetch this block's candidates' K/V and the first head group's Q
     gather_chunk<DQK, DV>(spk, spv, spec_sg, spec_g, n_spec, P, G_b, Kb, Vb, QP, VP, tid, kThreads);
     {
@@ -705,32 +755,60 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     PHASE_MARK(9);
 
     // ---- selection: exact top k from the published candidates -----------------
-    if (!wait_count(p, ctl + kCands, unsigned(n_b), 2, s_ok)) {
-        cp_async_wait<0>();
-        return;
-    }
-    PHASE_MARK(10);
-    // everyone has read the sample words: clear this block's for the next call
-    if (tid < kWarps) st_relaxed_u64(p.samp + size_t(cta) * kWarps + tid, 0ull);
+    // Load every slot of the sequence into shared memory, polling until the
+    // header and the entries it announces are written.
     unsigned char *stage = smem + kStage;
     {
-        const int n16 = n_b * (kSlotBytes / 16);
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.slots + size_t(cb0) * kSlotBytes);
-        uint4 v[4];
+        constexpr int kC = kSlotBytes / 16;  // 16-byte chunks per slot
+        constexpr int kQ = (kMaxCtas * kC + kThreads - 1) / kThreads;
+        const int n16 = n_b * kC;
+        const unsigned long long *src = slots_cur + size_t(cb0) * kSlotWords;
+        unsigned pend = 0;  // chunks still to load, bit u <-> chunk tid + u*kThreads
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = tid + u * kThreads;
-            if (i < n16) v[u] = ld_cg4(src + i);
-        }
+        for (int u = 0; u < kQ; ++u)
+            if (tid + u * kThreads < n16) pend |= 1u << u;
+        const long long t0 = clock64();
+        for (int spin = 0;; ++spin) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = tid + u * kThreads;
-            if (i < n16) reinterpret_cast<uint4 *>(stage)[i] = v[u];
+            for (int u = 0; u < kQ; ++u) {
+                if (!(pend >> u & 1u)) continue;
+                const int q = tid + u * kThreads;
+                reinterpret_cast<ulonglong2 *>(stage)[q] = ld_relaxed_u64x2(src + 2 * q);
+            }
+            __syncthreads();
+            // a chunk is complete once its slot's header is written and so is
+            // every entry the header announces
+#pragma unroll
+            for (int u = 0; u < kQ; ++u) {
+                if (!(pend >> u & 1u)) continue;
+                const int q = tid + u * kThreads;
+                const int jj = q / kC, w0 = 2 * (q % kC);
+                const unsigned long long *sl =
+                    reinterpret_cast<const unsigned long long *>(stage) + jj * kSlotWords;
+                const unsigned h = unsigned(sl[0]);
+                bool ok = h != 0u;
+                if (ok) {
+                    const int nw = 1 + min(int(h) - 1, kSlot);
+#pragma unroll
+                    for (int w = 0; w < 2; ++w)
+                        if (w0 + w < nw && unsigned(sl[w0 + w]) == 0u) ok = false;
+                }
+                if (ok) pend &= ~(1u << u);
+            }
+            if (!__syncthreads_or(pend != 0u)) break;
+            // thread 0 decides for the block whether to give up
+            const bool give_up = tid == 0 && (clock64() - t0 > kSpinBudget ||
+                                              ((spin & 63) == 63 && aborted(p.abort_flag)));
+            if (__syncthreads_or(give_up)) {
+                if (tid == 0) raise_timeout(p, 2);
+                cp_async_wait<0>();
+                return;
+            }
+            __nanosleep(64);
         }
-        for (int i = tid + 4 * kThreads; i < n16; i += kThreads)
-            reinterpret_cast<uint4 *>(stage)[i] = ld_cg4(src + i);
     }
-    __syncthreads();
+    PHASE_MARK(10);
+    // slot jj as 32-bit words: [0] count + 1, [1] guess, [2 + 2e] key, [3 + 2e] group
     auto hdr = [&](int jj) { return reinterpret_cast<const unsigned *>(stage + jj * kSlotBytes); };
     if (warp == 0) {
         // counts -> offsets (each lane owns up to 5 consecutive blocks)
@@ -745,9 +823,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             v[u] = 0;
             if (jj < n_b) {
                 const unsigned *h = hdr(jj);
-                v[u] = int(h[0]);
-                minp = min(minp, h[2]);
-                maxp = max(maxp, h[2]);
+                v[u] = int(h[0]) - 1;
+                minp = min(minp, h[1]);
+                maxp = max(maxp, h[1]);
                 over |= v[u] > kSlot;
             }
             s += v[u];
@@ -791,24 +869,41 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     if (fast) {
         for (int jj = warp; jj < n_b; jj += kWarps) {
             const unsigned *h = hdr(jj);
-            const int cnt = int(h[0]), o0 = offs[jj];
+            const int cnt = int(h[0]) - 1, o0 = offs[jj];
             for (int e = lane; e < min(cnt, kSlot); e += 32) {
-                ckey[o0 + e] = h[4 + 2 * e];
-                cgrp[o0 + e] = int32_t(h[5 + 2 * e]);
+                ckey[o0 + e] = h[2 + 2 * e];
+                cgrp[o0 + e] = int32_t(h[3 + 2 * e]);
             }
         }
         if (sv[9]) {  // candidates past a slot's capacity come from the block's segment
+            const long long t0 = clock64();
+            bool ok = true;
             for (int jj = warp; jj < n_b; jj += kWarps) {
-                const int cnt = int(hdr(jj)[0]), o0 = offs[jj];
-                const int64_t s0 = seg + chunk_lo(jj);
+                const int cnt = int(hdr(jj)[0]) - 1, o0 = offs[jj];
+                const unsigned long long *s0 = cand_cur + seg + chunk_lo(jj) - kSlot;
                 for (int e = kSlot + lane; e < cnt; e += 32) {
-                    ckey[o0 + e] = ld_cg(p.cand_key + s0 + e - kSlot);
-                    cgrp[o0 + e] = int32_t(ld_cg(reinterpret_cast<const unsigned *>(p.cand_g) + s0 + e - kSlot));
+                    unsigned long long w = ld_relaxed_u64(s0 + e);
+                    for (int spin = 0; unsigned(w) == 0u && ok; ++spin) {
+                        if (clock64() - t0 > kSpinBudget ||
+                            ((spin & 63) == 63 && aborted(p.abort_flag))) ok = false;
+                        __nanosleep(64);
+                        w = ld_relaxed_u64(s0 + e);
+                    }
+                    ckey[o0 + e] = unsigned(w);
+                    cgrp[o0 + e] = int32_t(w >> 32);
                 }
+            }
+            if (!ok) {
+                raise_timeout(p, 2);
+                sv[19] = 1;
             }
         }
         __syncthreads();
         PHASE_MARK(11);
+        if (sv[19]) {  // an overflow entry never arrived
+            cp_async_wait<0>();
+            return;
+        }
         if (k_b > 0) {
             // histogram of the 16-bit bin relative to the smallest guess
             unsigned *sh = reinterpret_cast<unsigned *>(smem + kSelHist);
@@ -820,7 +915,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 atomicAdd(sh + min(2047u, (ckey[i] >> 16) - minp), 1u);
             __syncthreads();
             unsigned above;
+            PHASE_MARK(28);
             const int T = find_digit(sh, 2048, unsigned(k_b), &above, scratch, sv + 12);
+            PHASE_MARK(29);
             const unsigned need_t = unsigned(k_b) - above;
             const int m_t = int(sh[T]);
             if (T < 2047 && m_t <= kTieCap) {
@@ -1155,65 +1252,122 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                     }
                     __syncthreads();
                 }
+                PHASE_MARK(25);
                 if (warp < n_aw)
                     attn_chunk<DQK, DV, 4, true>(st, qa, ck, cv, cg, QP, VP, P, tok0, ntok,
                                                  p.scale_log2, sq, mt);
+                PHASE_MARK(26);
                 __syncthreads();
             }
             PHASE_MARK(16);
             if (warp < n_aw) store_warp_state<DV>(st, state + warp * 16 * (DV + 2));
             __syncthreads();
+            PHASE_MARK(27);
             for (int e = tid; e < HG * (DV / 2); e += kThreads) {
                 const int hl = e / (DV / 2), d2 = (e % (DV / 2)) * 2;
                 float Lsum;
                 const float4 rr = merge_states<DV>(state, MT, TS, hl, d2, Lsum);
                 const int64_t pi = int64_t(cta) * p.H_q + h0 + hl;
-                if (Lsum > 0.f)
-                    *reinterpret_cast<float2 *>(p.part_o + pi * DV + d2) = make_float2(rr.z, rr.w);
-                if (d2 == 0) p.part_ml[pi] = make_float2(Lsum > 0.f ? rr.x : -INFINITY, Lsum);
+                const bool any = Lsum > 0.f;
+                st_part2(p.part_o + pi * DV + d2, any ? rr.z : 0.f, any ? rr.w : 0.f);
+                if (d2 == 0)
+                    st_part2(reinterpret_cast<float *>(p.part_ml + pi), any ? rr.x : -INFINITY, Lsum);
             }
         }
     }
-    arrive(ctl + kAtt);
     PHASE_MARK(17);
 
     // ---- merge the blocks' partial states, head by head ---------------------------
-    if (!wait_count(p, ctl + kAtt, unsigned(n_b), 6, s_ok)) return;
+    // The head's combining block polls the partial words of every block of the
+    // sequence until all are written, then clears them for the next call.
     PHASE_MARK(18);
     {
         float *wsm = reinterpret_cast<float *>(smem + kU);       // [kMaxCtas] weights
-        float *lsm = wsm + kMaxCtas;                              // [kMaxCtas] l
+        float *lsm = wsm + kMaxCtas;                              // [kWarps] sums of w l
         float *red = lsm + kMaxCtas;                              // [ngrp][DV]
         constexpr int D4 = DV / 4;                                // float4 columns
         const int sg = tid / D4, dc = tid % D4;                   // split group, column
         const int ngrp = kThreads / D4;                           // 16 (DV=128) or 32 (DV=64)
         for (int h = j; h < p.H_q; h += n_b) {
-            float2 ml = make_float2(-INFINITY, 0.f);
-            if (tid < n_b) ml = ld_cg_f2(p.part_ml + int64_t(cb0 + tid) * p.H_q + h);
-            float4 ov[(kMaxCtas + 15) / 16];
+            constexpr int kU4 = (kMaxCtas + 15) / 16;
             const int nu = (n_b - sg + ngrp - 1) / ngrp;
+            float2 *mlp = p.part_ml + int64_t(cb0 + tid) * p.H_q + h;
+            auto op_at = [&](int u) {
+                return p.part_o + (int64_t(cb0 + sg + u * ngrp) * p.H_q + h) * DV + dc * 4;
+            };
+            uint2 mlw = make_uint2(1u, 1u);
+            if (tid < n_b) mlw = ld_relaxed_u32x2(mlp);
+            uint4 ow[kU4];
 #pragma unroll
-            for (int u = 0; u < (kMaxCtas + 15) / 16; ++u) {
-                ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (u < nu) {
-                    const int s = sg + u * ngrp;
-                    ov[u] = ld_cg_f4(p.part_o + (int64_t(cb0 + s) * p.H_q + h) * DV + dc * 4);
+            for (int u = 0; u < kU4; ++u) {
+                ow[u] = make_uint4(1u, 1u, 1u, 1u);
+                if (u < nu) ow[u] = ld_relaxed_v4(reinterpret_cast<const uint4 *>(op_at(u)));
+            }
+            {
+                const long long t0 = clock64();
+                for (int spin = 0;; ++spin) {
+                    bool bad = false;
+                    if (mlw.x == 0u || mlw.y == 0u) {
+                        bad = true;
+                        mlw = ld_relaxed_u32x2(mlp);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kU4; ++u) {
+                        if (ow[u].x == 0u || ow[u].y == 0u || ow[u].z == 0u || ow[u].w == 0u) {
+                            bad = true;
+                            ow[u] = ld_relaxed_v4(reinterpret_cast<const uint4 *>(op_at(u)));
+                        }
+                    }
+                    if (!bad) break;
+                    if (clock64() - t0 > kSpinBudget ||
+                        ((spin & 63) == 63 && aborted(p.abort_flag))) {
+                        raise_timeout(p, 6);
+                        sv[19] = 1;
+                        break;
+                    }
+                    __nanosleep(32);
                 }
             }
+            PHASE_MARK(30);
+            float2 ml = make_float2(-INFINITY, 0.f);
+            if (tid < n_b) {
+                ml = make_float2(part_dec(mlw.x), part_dec(mlw.y));
+                st_relaxed_zero2(mlp);
+            }
+            float4 ov[kU4];
+#pragma unroll
+            for (int u = 0; u < kU4; ++u) {
+                ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (u < nu) {
+                    ov[u] = make_float4(part_dec(ow[u].x), part_dec(ow[u].y), part_dec(ow[u].z),
+                                        part_dec(ow[u].w));
+                    st_relaxed_zero4(op_at(u));
+                }
+            }
+            // M = max over blocks (warp max, then over the warps' maxima)
             float m = ml.x;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             if (lane == 0) sred[warp] = m;
             __syncthreads();
-            float M = -INFINITY;
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sred[w]);
+            if (sv[19]) return;  // a partial state never arrived
+            PHASE_MARK(31);
+            float M = lane < kWarps ? sred[lane] : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             const float ref = M == -INFINITY ? 0.f : M;
+            // block weights 2^(m_s - M) and L = sum of w_s l_s (warp sums first)
+            float wl = 0.f;
             if (tid < n_b) {
                 const float wgt = ml.y > 0.f ? exp2f(ml.x - ref) : 0.f;
                 wsm[tid] = wgt;
-                lsm[tid] = wgt * ml.y;
+                wl = wgt * ml.y;
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
+            if (lane == 0) lsm[warp] = wl;
             __syncthreads();
+            PHASE_MARK(32);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int u = 0; u < (kMaxCtas + 15) / 16; ++u) {
@@ -1231,7 +1385,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             __syncthreads();
             if (tid < DV / 2) {
                 float L = 0.f;
-                for (int s = 0; s < n_b; ++s) L += lsm[s];
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) L += lsm[w];
                 float a0 = 0.f, a1 = 0.f;
                 for (int g2 = 0; g2 < ngrp; ++g2) {
                     a0 += red[g2 * DV + 2 * tid];
@@ -1248,8 +1403,24 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     }
     PHASE_MARK(19);
     __syncthreads();
-    if (tid == 0 && atomicAdd(ctl + kDepart, 1u) == unsigned(n_b) - 1u) {
-        for (int i = 0; i < kNumCounters; ++i) ctl[i] = 0u;  // every block is done with them
+    // this block's words of the other buffers were read during the previous
+    // call: clear them for the next one
+    {
+        const int op = par ^ 1;
+        if (tid < kSlotWords)
+            st_relaxed_u64(p.slots + (size_t(op) * ncta + cta) * kSlotWords + tid, 0ull);
+        else if (tid >= 32 && tid < 32 + kWarps)
+            st_relaxed_u64(p.samp + (size_t(op) * ncta + cta) * kWarps + (tid - 32), 0ull);
+        unsigned long long *cold = p.cand + size_t(op) * p.B * p.G_max + ovf_old.x;
+        for (int i = tid; i < ovf_old.y; i += kThreads) st_relaxed_u64(cold + i, 0ull);
+    }
+    // the last block of the grid to finish resets the counters and flips the
+    // exchange buffers for the next call
+    if (tid == 0 && atomicAdd(p.gdepart, 1u) == unsigned(ncta) - 1u) {
+        for (int bb = 0; bb < B; ++bb)
+            for (int i = 0; i < kNumCounters; ++i) p.ctl[size_t(bb) * kCtlWords + i] = 0u;
+        *p.parity = unsigned(par ^ 1);
+        *p.gdepart = 0u;
     }
 }
 
@@ -1267,7 +1438,7 @@ constexpr int smem_bytes() {
 }
 
 struct WsLayout {
-    size_t ctl, hist, samp, slots, cand_key, cand_g, gscore, cta_cnt, idx_ws, part_o, part_ml, total;
+    size_t ctl, hist, samp, slots, cand, ovf, gscore, cta_cnt, idx_ws, part_o, part_ml, total;
 };
 
 WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int ncta) {
@@ -1280,10 +1451,10 @@ WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int ncta) {
     };
     w.ctl = take(size_t(B) * kCtlWords * 4);
     w.hist = take(size_t(B) * 2 * kHistWords * 4);
-    w.samp = take(size_t(ncta) * kWarps * 8);
-    w.slots = take(size_t(ncta) * kSlotBytes);
-    w.cand_key = take(size_t(B) * G_max * 4);
-    w.cand_g = take(size_t(B) * G_max * 4);
+    w.samp = take(size_t(2) * ncta * kWarps * 8);
+    w.slots = take(size_t(2) * ncta * kSlotBytes);
+    w.cand = take(size_t(2) * B * G_max * 8);
+    w.ovf = take(size_t(2) * ncta * 8);
     w.gscore = take(size_t(B) * G_max * 4);
     w.cta_cnt = take(size_t(2) * ncta * 4);
     w.idx_ws = take(size_t(B) * k * 4);
@@ -1392,9 +1563,9 @@ cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status
     prm.ctl = reinterpret_cast<unsigned *>(base + w.ctl);
     prm.hist = reinterpret_cast<unsigned *>(base + w.hist);
     prm.samp = reinterpret_cast<unsigned long long *>(base + w.samp);
-    prm.slots = reinterpret_cast<unsigned char *>(base + w.slots);
-    prm.cand_key = reinterpret_cast<unsigned *>(base + w.cand_key);
-    prm.cand_g = reinterpret_cast<int32_t *>(base + w.cand_g);
+    prm.slots = reinterpret_cast<unsigned long long *>(base + w.slots);
+    prm.cand = reinterpret_cast<unsigned long long *>(base + w.cand);
+    prm.ovf = reinterpret_cast<int2 *>(base + w.ovf);
     prm.gscore = reinterpret_cast<float *>(base + w.gscore);
     prm.cta_cnt = reinterpret_cast<unsigned *>(base + w.cta_cnt);
     prm.idx_ws = reinterpret_cast<int32_t *>(base + w.idx_ws);
@@ -1402,6 +1573,8 @@ cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status
     prm.part_ml = reinterpret_cast<float2 *>(base + w.part_ml);
     prm.status = status;
     prm.abort_flag = status + 1;
+    prm.parity = reinterpret_cast<unsigned *>(status + 2);
+    prm.gdepart = reinterpret_cast<unsigned *>(status + 3);
     const int NT = a->H_i > 8 ? 2 : 1;
 #define LCSW_FD(NTT, DQ, DVV)                                                         \
     if (NT == NTT && a->d_qk == DQ && a->d_v == DVV) return launch_t<NTT, DQ, DVV>(prm, ncta, st);
