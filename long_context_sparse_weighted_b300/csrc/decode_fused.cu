@@ -53,6 +53,7 @@
 #include "kernels.cuh"
 #include "pool_core.cuh"
 #include "select_core.cuh"
+#include "tc_core.cuh"
 
 namespace lcsw {
 namespace {
@@ -70,6 +71,7 @@ constexpr int kTieCap = 256;       // threshold-bin candidates resolved by rank 
 constexpr int kMaxK = 2048;        // selected groups per sequence
 constexpr int kCtlWords = 32;      // control words per sequence
 constexpr int kMaxCtas = 160;
+constexpr long long kMbarBudget = 1ll << 22;  // polls of a tensor-core completion wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -90,14 +92,28 @@ constexpr int kCKey = kStage + kMaxCtas * kSlotBytes; // candidate keys [kSelCap
 constexpr int kCG = kCKey + kSelCap * 4;              // candidate groups [kSelCap]
 constexpr int kSelHist = kCG + kSelCap * 4;           // [2048]
 constexpr int kTie = kSelHist + 2048 * 4;             // [kTieCap] (key, index)
-constexpr int kState = kSpec + kSpecBytes;            // merge state (after compute)
 constexpr int kGather = kU;                           // gathered chunks (no prefetch hit)
 constexpr int kSelG = kU + kUBytes - kMaxK * 4;       // own selected groups [kMaxK]
 constexpr int kScores = kU + kUBytes;                 // [kChunkCap] floats
-constexpr int kQ = kScores + kChunkCap * 4;           // Q tile [64][QP]
+constexpr int kMisc = kScores + kChunkCap * 4;        // small arrays and scalars (< 8 KB)
+constexpr int kQT = kMisc + 8192;                     // Q tile, tensor-core layout
+// Attention operand tiles (128-byte-swizzled, see tc_core.cuh).  Q: K-major,
+// DQK/64 atom columns of 64 head rows (8 KB each); the MMA reads 128 rows, so
+// rows 64..127 of the last column fall on the 8 KB after the tile (values
+// unused).  P: K-major, 128 head rows x 64 tokens (16 KB), on the scores,
+// which are dead by then.  K: K-major, DQK/64 atom columns of 64 token rows.
+// V: MN-major, DV/64 atoms of 8 token groups x 1024 B (LBO 8192 between atoms,
+// SBO 1024 between token groups).
+constexpr int kMiscBytes = 128 + kCoarse * 4 +
+                           (2 * (kMaxCtas + 1) + kMaxCtas + 2 * kSpecTok + 64 + 40 + 64 +
+                            2 * kChunk + 4 * 128) * 4 + 2 * 8 + 4;
+static_assert(kMiscBytes <= 8192, "small arrays overflow their region");
+template <int DQK> constexpr int q_tile_bytes() { return (DQK / 64) * 8192; }
+template <int DQK, int DV> constexpr int kv_tile_bytes() { return (DQK / 64 + DV / 64) * 8192; }
+constexpr int kPT = kScores;
 static_assert(kTie + kTieCap * 8 <= kSelG, "shared-memory map overlap");
-static_assert(kState + 8 * 16 * (128 + 2) * 4 <= kSelG, "merge state overlap");
-static_assert(kGather + 2 * kChunk * (192 + 8 + 128 + 8) * 2 <= kSelG, "gather overlap");
+static_assert((192 / 64 + 128 / 64) * 8192 <= kSpecBytes, "prefetch tile overlap");
+static_assert(kGather + 2 * (192 / 64 + 128 / 64) * 8192 <= kSelG, "gather overlap");
 
 struct Params {
     const uint16_t *q_idx;
@@ -182,18 +198,6 @@ __device__ __forceinline__ float ld_cg_f(const float *p) {
     asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
     return v;
 }
-__device__ __forceinline__ float2 ld_cg_f2(const float2 *p) {
-    float2 v;
-    asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ float4 ld_cg_f4(const float *p) {
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
-}
 __device__ __forceinline__ uint4 ld_cg4(const void *p) {
     uint4 r;
     asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -228,6 +232,12 @@ constexpr unsigned kPartTag = 0x7FBFFFFFu;
 __device__ __forceinline__ void st_part2(float *p, float a, float b) {
     asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(p),
                  "r"(__float_as_uint(a) ^ kPartTag), "r"(__float_as_uint(b) ^ kPartTag)
+                 : "memory");
+}
+__device__ __forceinline__ void st_part4(float *p, float4 v) {
+    asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p),
+                 "r"(__float_as_uint(v.x) ^ kPartTag), "r"(__float_as_uint(v.y) ^ kPartTag),
+                 "r"(__float_as_uint(v.z) ^ kPartTag), "r"(__float_as_uint(v.w) ^ kPartTag)
                  : "memory");
 }
 __device__ __forceinline__ uint2 ld_relaxed_u32x2(const void *p) {
@@ -366,6 +376,41 @@ __device__ __forceinline__ void flush_hist(const unsigned *h16, unsigned *g) {
     }
 }
 
+// Gather the K and V rows of one 64-token chunk -- the tokens of groups
+// glist[0..n) (n <= 64/P) of a sequence whose complete groups are [0, G) --
+// into the attention operand tiles (layouts above kv_tile_bytes).  Invalid
+// or missing groups are zero-filled and marked -1 in sg.
+template <int DQK, int DV>
+__device__ __forceinline__ void gather_tc(unsigned char *tk, int *sg, const int32_t *glist, int n,
+                                          int P, int G, const uint16_t *kb, const uint16_t *vb) {
+    const int tid = threadIdx.x, gpc = kChunk / P;
+    unsigned char *tv = tk + (DQK / 64) * 8192;
+    if (tid < gpc) {
+        const int g = tid < n ? glist[tid] : -1;
+        sg[tid] = (g >= 0 && g < G) ? g : -1;
+    }
+    for (int e = tid; e < kChunk * (DQK / 8); e += kThreads) {
+        const int t = e / (DQK / 8), c8 = e % (DQK / 8);
+        const int q = t / P;
+        const int g = q < n ? glist[q] : -1;
+        const bool ok = g >= 0 && g < G;
+        const uint16_t *src = ok ? kb + (int64_t(g) * P + t % P) * DQK + c8 * 8 : kb;
+        cp_async16(smem_u32(tk + (c8 / 8) * 8192 + sw128_offset(t, (c8 % 8) * 8, 1024)), src,
+                   ok ? 16 : 0);
+    }
+    for (int e = tid; e < kChunk * (DV / 8); e += kThreads) {
+        const int t = e / (DV / 8), c8 = e % (DV / 8);
+        const int q = t / P;
+        const int g = q < n ? glist[q] : -1;
+        const bool ok = g >= 0 && g < G;
+        const uint16_t *src = ok ? vb + (int64_t(g) * P + t % P) * DV + c8 * 8 : vb;
+        // MN-major: token t is row t%8 of token group t/8, dv chunk c8%8 of atom c8/8
+        cp_async16(smem_u32(tv + (c8 / 8) * 8192 + sw128_offset(t, (c8 % 8) * 8, 1024)), src,
+                   ok ? 16 : 0);
+    }
+    cp_async_commit();
+}
+
 __device__ __forceinline__ void clear_smem(unsigned char *base, int bytes) {
     for (int i = threadIdx.x * 16; i < bytes; i += kThreads * 16)
         *reinterpret_cast<uint4 *>(base + i) = make_uint4(0, 0, 0, 0);
@@ -374,11 +419,10 @@ __device__ __forceinline__ void clear_smem(unsigned char *base, int bytes) {
 template <int NT, int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params p) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    constexpr int QP = DQK + 8, VP = DV + 8;
     unsigned *h16 = reinterpret_cast<unsigned *>(smem + kU);
     float *sscore = reinterpret_cast<float *>(smem + kScores);
-    uint16_t *sq = reinterpret_cast<uint16_t *>(smem + kQ);
-    constexpr int kMisc = kQ + 64 * QP * 2;
+    unsigned char *qt = smem + kQT;           // Q operand tile
+    unsigned char *pt = smem + kPT;           // P operand tile (on the dead scores)
     uint16_t *newkey = reinterpret_cast<uint16_t *>(smem + kMisc);            // [64]
     unsigned *ccoarse = reinterpret_cast<unsigned *>(smem + kMisc + 128);     // [kCoarse]
     int *cta_begin = reinterpret_cast<int *>(ccoarse + kCoarse);              // [kMaxCtas + 1]
@@ -389,11 +433,20 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     int *sv = spec_sg + kSpecTok;                                             // scalars [64]
     int *scratch = sv + 64;                                                   // [40]
     float *sred = reinterpret_cast<float *>(scratch + 40);                    // [64]
+    int *gsg = reinterpret_cast<int *>(sred + 64);                            // [2][kChunk]
+    float *lpart = reinterpret_cast<float *>(gsg + 2 * kChunk);               // [4][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(lpart + 4 * 128);           // [2]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 2);                 // TMEM base
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x, ncta = gridDim.x;
     const int B = p.B, P = p.P;
     PHASE_MARK(0);
+    // the operand tiles' swizzle assumes 1024-byte-aligned shared memory
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, int(LCSW_ERR_UNSUPPORTED) * 256);
+        return;
+    }
     // this call's exchange buffers (the previous call's last block flipped it)
     const int par = int(ld_cg(p.parity) & 1u);
     unsigned long long *samp_cur = p.samp + size_t(par) * ncta * kWarps;
@@ -731,8 +784,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     __syncthreads();
     PHASE_MARK(8);
     const int n_spec = sv[5];
-    uint16_t *spk = reinterpret_cast<uint16_t *>(smem + kSpec);
-    uint16_t *spv = spk + kChunk * QP;
     if (p.skip_arrive && j == n_b - 1 && n_b > 1) {  // failure-detection test only
         return;
     }
@@ -741,17 +792,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                        (unsigned(sv[28]) + 1u) | ((unsigned long long)guess << 32));
         p.ovf[par * ncta + cta] = make_int2(int(seg + g_lo), max(0, sv[28] - kSlot));
     }
-    // prefetch this block's candidates' K/V and the first head group's Q
-    gather_chunk<DQK, DV>(spk, spv, spec_sg, spec_g, n_spec, P, G_b, Kb, Vb, QP, VP, tid, kThreads);
-    {
-        const int HG0 = min(64, p.H_q);
+    // prefetch this block's candidates' K/V and the heads' Q into operand tiles
+    auto load_q_tile = [&]() {
         const uint16_t *qrow = p.q + int64_t(b) * p.H_q * DQK;
-        for (int e = tid; e < HG0 * (DQK / 8); e += kThreads) {
+        for (int e = tid; e < p.H_q * (DQK / 8); e += kThreads) {
             const int h = e / (DQK / 8), c8 = e % (DQK / 8);
-            cp_async16(smem_u32(sq + h * QP + c8 * 8), qrow + int64_t(h) * DQK + c8 * 8, 16);
+            cp_async16(smem_u32(qt + (c8 / 8) * 8192 + sw128_offset(h, (c8 % 8) * 8, 1024)),
+                       qrow + int64_t(h) * DQK + c8 * 8, 16);
         }
         cp_async_commit();
-    }
+    };
+    gather_tc<DQK, DV>(smem + kSpec, spec_sg, spec_g, n_spec, P, G_b, Kb, Vb);
+    load_q_tile();
     PHASE_MARK(9);
 
     // ---- selection: exact top k from the published candidates -----------------
@@ -866,14 +918,31 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     unsigned *ckey = reinterpret_cast<unsigned *>(smem + kCKey);
     int32_t *cgrp = reinterpret_cast<int32_t *>(smem + kCG);
     DBG_MAX(0, n_cand);
+    // With one common guess and at least k candidates, the candidates hold the
+    // true top k; a block then only needs the rank of each of its own
+    // candidates (keys descending, groups ascending), here the order of the
+    // packed value (key << 32) | ~group.  The k-th key K* is computed only for
+    // the optional full index output or past 32 own candidates.
+    const int own0 = offs[j], m_own = offs[j + 1] - offs[j];
+    const bool by_rank = fast && k_b > 0 && m_own <= 32 && sv[8] == sv[7] && !(p.idx_out && j == 0);
+    // packed candidates on the scores, which the rank path no longer needs
+    unsigned long long *crank = reinterpret_cast<unsigned long long *>(smem + kScores);
+    int *rank = reinterpret_cast<int *>(lpart);  // [32] ranks of the own candidates
+    auto put_cand = [&](int o, unsigned key, unsigned g) {
+        if (by_rank) {
+            crank[o] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - g);
+        } else {
+            ckey[o] = key;
+            cgrp[o] = int32_t(g);
+        }
+    };
     if (fast) {
-        for (int jj = warp; jj < n_b; jj += kWarps) {
+        if (tid < 32) rank[tid] = 0;
+        // all candidates, in slot order (= ascending group): one thread per slot entry
+        for (int q = tid; q < n_b * kSlot; q += kThreads) {
+            const int jj = q / kSlot, e = q - jj * kSlot;
             const unsigned *h = hdr(jj);
-            const int cnt = int(h[0]) - 1, o0 = offs[jj];
-            for (int e = lane; e < min(cnt, kSlot); e += 32) {
-                ckey[o0 + e] = h[2 + 2 * e];
-                cgrp[o0 + e] = int32_t(h[3 + 2 * e]);
-            }
+            if (e < int(h[0]) - 1) put_cand(offs[jj] + e, h[2 + 2 * e], h[3 + 2 * e]);
         }
         if (sv[9]) {  // candidates past a slot's capacity come from the block's segment
             const long long t0 = clock64();
@@ -889,8 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                         __nanosleep(64);
                         w = ld_relaxed_u64(s0 + e);
                     }
-                    ckey[o0 + e] = unsigned(w);
-                    cgrp[o0 + e] = int32_t(w >> 32);
+                    put_cand(o0 + e, unsigned(w), unsigned(w >> 32));
                 }
             }
             if (!ok) {
@@ -904,6 +972,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             cp_async_wait<0>();
             return;
         }
+    }
+    if (fast && !by_rank) {
         if (k_b > 0) {
             // histogram of the 16-bit bin relative to the smallest guess
             unsigned *sh = reinterpret_cast<unsigned *>(smem + kSelHist);
@@ -959,7 +1029,34 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     int32_t *own = reinterpret_cast<int32_t *>(smem + kSelG);
     int n_own = 0;
     bool use_spec = false;
-    if (fast) {
+    if (by_rank) {
+        // rank of each own candidate: lane l of every warp holds own candidate l;
+        // warp w counts the candidates of its slice that rank above it
+        const unsigned long long rl = lane < m_own ? crank[own0 + lane] : ~0ull;
+        const int per = (n_cand + kWarps - 1) / kWarps;
+        const int e0 = warp * per, e1 = min(n_cand, e0 + per);
+        unsigned cnt = 0;
+#pragma unroll 8
+        for (int e = e0; e < e1; ++e) cnt += crank[e] > rl ? 1u : 0u;
+        if (lane < m_own && cnt) atomicAdd(rank + lane, int(cnt));
+        __syncthreads();
+        if (warp == 0) {
+            const bool sel = lane < m_own && rank[lane] < k_b;
+            const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+            if (sel) own[__popc(bsel & ((1u << lane) - 1u))] = int(0xFFFFFFFFu - unsigned(rl));
+            // the prefetch holds this block's first n_spec candidates
+            const bool cover = n_spec >= 32 || (bsel >> n_spec) == 0u;
+            if (lane == 0) {
+                sv[16] = __popc(bsel);
+                sv[18] = cover ? 1 : 0;
+            }
+        }
+        __syncthreads();
+        n_own = sv[16];
+        use_spec = sv[18] != 0;
+        if (use_spec && tid < spec_cap && !(tid < m_own && rank[tid] < k_b))
+            spec_sg[tid] = -1;  // prefetched but not selected: masked
+    } else if (fast) {
         // this block's selected groups, ascending: its candidates are the range
         // [offs[j], offs[j+1]); ties at K* go to the lowest candidate index
         const int o0 = offs[j], o1 = offs[j + 1];
@@ -1190,89 +1287,178 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 hist2[kFine + cbin] = 0u;
         }
         __syncthreads();
-        // Q of the first head group (the prefetch was drained above)
-        {
-            const int HG0 = min(64, p.H_q);
-            const uint16_t *qrow = p.q + int64_t(b) * p.H_q * DQK;
-            for (int e = tid; e < HG0 * (DQK / 8); e += kThreads) {
-                const int h = e / (DQK / 8), c8 = e % (DQK / 8);
-                cp_async16(smem_u32(sq + h * QP + c8 * 8), qrow + int64_t(h) * DQK + c8 * 8, 16);
-            }
-            cp_async_commit();
-        }
+        load_q_tile();  // the prefetch was drained above
     }
     PHASE_MARK(14);
 
-    // ---- attention over this block's selected groups ----------------------------
+    // ---- attention over this block's selected groups (tensor cores) ------------
+    // Per 64-token chunk: S = Q K^T (M = 128 head rows, N = 64 tokens) into TMEM;
+    // each warpgroup reads its head rows' scores, takes the row maximum over
+    // the chunk, exponentiates its own 16 token columns into the P tile; then
+    // O_c = P V (N = DV) into TMEM, folded into the running output in
+    // registers (warpgroup g keeps columns [g DV/4, (g+1) DV/4) of its row).
     {
-        float *state = reinterpret_cast<float *>(smem + kState);
-        uint16_t *gk = reinterpret_cast<uint16_t *>(smem + kGather);
-        uint16_t *gvb = gk + 2 * kChunk * QP;
-        int *gsg = reinterpret_cast<int *>(smem + kSelG) - 2 * kChunk;  // [2][kChunk]
+        constexpr int kTK = (DQK / 64) * 8192;
+        constexpr int OC = DV / 4;
         const int gpc = kChunk / P;
-        const int nchunks = use_spec ? 1 : (n_own + gpc - 1) / gpc;
-        for (int h0 = 0; h0 < p.H_q; h0 += 64) {
-            const int HG = min(64, p.H_q - h0);
-            const int MT = HG / 16, TS = 2, n_aw = MT * TS;
-            if (h0 > 0) {
-                __syncthreads();
-                const uint16_t *qrow = p.q + (int64_t(b) * p.H_q + h0) * DQK;
-                for (int e = tid; e < HG * (DQK / 8); e += kThreads) {
-                    const int h = e / (DQK / 8), c8 = e % (DQK / 8);
-                    cp_async16(smem_u32(sq + h * QP + c8 * 8), qrow + int64_t(h) * DQK + c8 * 8, 16);
+        const int nchunks = use_spec ? (n_own > 0 ? 1 : 0) : (n_own + gpc - 1) / gpc;
+        unsigned char *gbuf = smem + kGather;  // two chunk buffers (when not prefetched)
+        auto issue = [&](int ci, int buf) {
+            const int jb = ci * gpc;
+            gather_tc<DQK, DV>(gbuf + buf * kv_tile_bytes<DQK, DV>(), gsg + buf * kChunk, own + jb,
+                               min(gpc, n_own - jb), P, G_b, Kb, Vb);
+        };
+        cp_async_wait<0>();  // prefetched K/V and Q
+        fence_async_smem();
+        if (tid == 0) {
+            mbar_init(bars, 1);
+            mbar_init(bars + 1, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        if (nchunks > 0 && warp == 0) tmem_alloc(tslot, 256);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        PHASE_MARK(15);
+        const uint32_t tb = *tslot;  // S: columns 0..63, O_c: 64..64+DV
+        const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
+        const uint32_t lane_addr = tb + (uint32_t((warp & 3) * 32) << 16);
+        if (!use_spec && nchunks > 0) issue(0, 0);
+        float o[OC];
+#pragma unroll
+        for (int c2 = 0; c2 < OC; ++c2) o[c2] = 0.f;
+        float m = -INFINITY, lp = 0.f;  // running max; sum of this warpgroup's columns
+        bool ok = true;
+        for (int ci = 0; ci < nchunks; ++ci) {
+            const int buf = ci & 1;
+            unsigned char *tk = use_spec ? smem + kSpec : gbuf + buf * kv_tile_bytes<DQK, DV>();
+            const int *cg = use_spec ? spec_sg : gsg + buf * kChunk;
+            if (!use_spec) {
+                if (ci + 1 < nchunks) {
+                    issue(ci + 1, buf ^ 1);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
                 }
-                cp_async_commit();
-            }
-            auto issue = [&](int ci, int buf) {
-                const int jb = ci * gpc;
-                gather_chunk<DQK, DV>(gk + buf * kChunk * QP, gvb + buf * kChunk * VP,
-                                      gsg + buf * kChunk, own + jb, min(gpc, n_own - jb), P, G_b,
-                                      Kb, Vb, QP, VP, tid, kThreads);
-            };
-            cp_async_wait<0>();
-            __syncthreads();
-            PHASE_MARK(15);
-            if (!use_spec && nchunks > 0) issue(0, 0);
-            const int mt = warp % MT, ts = warp / MT;
-            const int ntok = kChunk / TS, tok0 = ts * ntok;
-            uint32_t qa[DQK / 16][4];  // unused: fragments come from shared memory
-            AttnWarpState<DV> st;
-            st.init();
-            for (int ci = 0; ci < nchunks; ++ci) {
-                const int buf = ci & 1;
-                const uint16_t *ck = use_spec ? spk : gk + buf * kChunk * QP;
-                const uint16_t *cv = use_spec ? spv : gvb + buf * kChunk * VP;
-                const int *cg = use_spec ? spec_sg : gsg + buf * kChunk;
-                if (!use_spec) {
-                    if (ci + 1 < nchunks) {
-                        issue(ci + 1, buf ^ 1);
-                        cp_async_wait<1>();
-                    } else {
-                        cp_async_wait<0>();
-                    }
-                    __syncthreads();
-                }
-                PHASE_MARK(25);
-                if (warp < n_aw)
-                    attn_chunk<DQK, DV, 4, true>(st, qa, ck, cv, cg, QP, VP, P, tok0, ntok,
-                                                 p.scale_log2, sq, mt);
-                PHASE_MARK(26);
+                fence_async_smem();
+                tc_fence_before();
                 __syncthreads();
+                tc_fence_after();
             }
-            PHASE_MARK(16);
-            if (warp < n_aw) store_warp_state<DV>(st, state + warp * 16 * (DV + 2));
+            if (tid == 0) {  // S = Q K^T
+                const uint32_t id = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+                for (int ks = 0; ks < DQK / 16; ++ks) {
+                    const uint32_t ko = (ks / 4) * 8192 + (ks % 4) * 32;
+                    tc_mma_bf16(tb, smem_desc(smem_u32(qt) + ko, 16, 1024),
+                                smem_desc(smem_u32(tk) + ko, 16, 1024), id, ks > 0);
+                }
+                tc_commit(bars);
+            }
+            // validity of the chunk's 64 tokens (the same for every row)
+            const unsigned long long vmask =
+                (unsigned long long)__ballot_sync(0xffffffffu, cg[lane / P] >= 0) |
+                ((unsigned long long)__ballot_sync(0xffffffffu, cg[(lane + 32) / P] >= 0) << 32);
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(bars, ci & 1, kMbarBudget));
+            tc_fence_after();
+            PHASE_MARK(25);
+            float al = 0.f;
+            if (ok) {
+                float mx = -INFINITY;
+                uint32_t r[16];
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    tc_ld16(lane_addr + c0, r);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        if (vmask >> (c0 + t) & 1ull)
+                            mx = fmaxf(mx, __uint_as_float(r[t]) * p.scale_log2);
+                }
+                const float mn = fmaxf(m, mx);
+                const float ref = mn == -INFINITY ? 0.f : mn;
+                al = exp2f(m - ref);
+                m = mn;
+                tc_ld16(lane_addr + 16 * wg, r);  // this warpgroup's 16 token columns
+                tc_wait_ld();
+                float pv[16];
+                float ls = 0.f;
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    pv[t] = (vmask >> (16 * wg + t) & 1ull)
+                                ? exp2f(__uint_as_float(r[t]) * p.scale_log2 - ref)
+                                : 0.f;
+                    ls += pv[t];
+                }
+                lp = lp * al + ls;
+                uint4 w0, w1;
+                w0.x = pack_bf2(pv[0], pv[1]);   w0.y = pack_bf2(pv[2], pv[3]);
+                w0.z = pack_bf2(pv[4], pv[5]);   w0.w = pack_bf2(pv[6], pv[7]);
+                w1.x = pack_bf2(pv[8], pv[9]);   w1.y = pack_bf2(pv[10], pv[11]);
+                w1.z = pack_bf2(pv[12], pv[13]); w1.w = pack_bf2(pv[14], pv[15]);
+                *reinterpret_cast<uint4 *>(pt + sw128_offset(row, 16 * wg, 1024)) = w0;
+                *reinterpret_cast<uint4 *>(pt + sw128_offset(row, 16 * wg + 8, 1024)) = w1;
+            }
+            fence_async_smem();
+            tc_fence_before();
             __syncthreads();
+            tc_fence_after();
+            PHASE_MARK(26);
+            if (tid == 0) {  // O_c = P V
+                const uint32_t id = idesc_bf16_f32(128, DV, false, true);
+#pragma unroll
+                for (int ks = 0; ks < kChunk / 16; ++ks)
+                    tc_mma_bf16(tb + 64, smem_desc(smem_u32(pt) + ks * 32, 16, 1024),
+                                smem_desc(smem_u32(tk + kTK) + ks * 2048, 8192, 1024), id, ks > 0);
+                tc_commit(bars + 1);
+            }
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(bars + 1, ci & 1, kMbarBudget));
+            tc_fence_after();
             PHASE_MARK(27);
-            for (int e = tid; e < HG * (DV / 2); e += kThreads) {
-                const int hl = e / (DV / 2), d2 = (e % (DV / 2)) * 2;
-                float Lsum;
-                const float4 rr = merge_states<DV>(state, MT, TS, hl, d2, Lsum);
-                const int64_t pi = int64_t(cta) * p.H_q + h0 + hl;
-                const bool any = Lsum > 0.f;
-                st_part2(p.part_o + pi * DV + d2, any ? rr.z : 0.f, any ? rr.w : 0.f);
-                if (d2 == 0)
-                    st_part2(reinterpret_cast<float *>(p.part_ml + pi), any ? rr.x : -INFINITY, Lsum);
+            if (ok) {
+                uint32_t r[16];
+#pragma unroll
+                for (int c0 = 0; c0 < OC; c0 += 16) {
+                    tc_ld16(lane_addr + 64 + wg * OC + c0, r);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) o[c0 + t] = o[c0 + t] * al + __uint_as_float(r[t]);
+                }
             }
+            tc_fence_before();
+        }
+        PHASE_MARK(16);
+        if (!ok) {
+            raise_timeout(p, 5);
+            sv[19] = 1;
+        }
+        // stage the O rows in shared memory (the chunk buffers are done) so the
+        // partial state goes out in contiguous rows
+        constexpr int kOP = DV + 4;  // staged row pitch (floats)
+        float *ostage = reinterpret_cast<float *>(smem + kGather);
+        lpart[wg * 128 + row] = lp;
+        if (row < p.H_q) {
+#pragma unroll
+            for (int c2 = 0; c2 < OC; c2 += 4)
+                *reinterpret_cast<float4 *>(ostage + row * kOP + wg * OC + c2) =
+                    make_float4(o[c2], o[c2 + 1], o[c2 + 2], o[c2 + 3]);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (nchunks > 0 && warp == 0) tmem_free(tb, 256);
+        if (sv[19]) return;  // a tensor-core step never completed
+        // the block's partial state of each head: (m, l) and the unnormalised O row
+        const int64_t pbase = int64_t(cta) * p.H_q;
+        for (int e = tid; e < p.H_q * (DV / 4); e += kThreads) {
+            const int h = e / (DV / 4), c4 = e % (DV / 4);
+            const float l = lpart[h] + lpart[128 + h] + lpart[256 + h] + lpart[384 + h];
+            const float4 v = l > 0.f ? *reinterpret_cast<const float4 *>(ostage + h * kOP + c4 * 4)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            st_part4(p.part_o + (pbase + h) * DV + c4 * 4, v);
+        }
+        if (wg == 0 && row < p.H_q) {
+            const float l = lpart[row] + lpart[128 + row] + lpart[256 + row] + lpart[384 + row];
+            st_part2(reinterpret_cast<float *>(p.part_ml + pbase + row), l > 0.f ? m : -INFINITY, l);
         }
     }
     PHASE_MARK(17);
@@ -1433,8 +1619,7 @@ int num_sms() {
 
 template <int DQK>
 constexpr int smem_bytes() {
-    return kQ + 64 * (DQK + 8) * 2 + 128 + kCoarse * 4 +
-           (2 * (kMaxCtas + 1) + kMaxCtas + 2 * kSpecTok + 64 + 40 + 64) * 4;
+    return kQT + q_tile_bytes<DQK>() + 8192;
 }
 
 struct WsLayout {
@@ -1471,7 +1656,7 @@ bool fused_decode_supported(int B, int G_max, int H_i, int H_q, int d_qk, int d_
     if (ncta > kMaxCtas || B < 1 || 2 * B > ncta) return false;
     if (H_i > 16 || k > kMaxK || k < 1) return false;
     if (!((d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128))) return false;
-    if (!(H_q % 16 == 0 && (H_q <= 32 || H_q % 64 == 0))) return false;
+    if (!(H_q % 16 == 0 && H_q <= 64)) return false;  // one M = 128 tensor-core tile of heads
     // 16-bit shared counters: a block's chunk must stay below 65536 groups
     const long long bound = (long long)B * G_max / (ncta - B) + 32;
     if (bound >= 65535) return false;
