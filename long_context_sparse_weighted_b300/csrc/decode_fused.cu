@@ -383,7 +383,7 @@ __device__ __forceinline__ void flush_hist(const unsigned *h16, unsigned *g) {
 template <int DQK, int DV>
 __device__ __forceinline__ void gather_tc(unsigned char *tk, int *sg, const int32_t *glist, int n,
                                           int P, int G, const uint16_t *kb, const uint16_t *vb) {
-    const int tid = threadIdx.x, gpc = kChunk / P;
+    const int tid = threadIdx.x, lp2 = 31 - __clz(P), gpc = kChunk >> lp2;
     unsigned char *tv = tk + (DQK / 64) * 8192;
     if (tid < gpc) {
         const int g = tid < n ? glist[tid] : -1;
@@ -391,19 +391,19 @@ __device__ __forceinline__ void gather_tc(unsigned char *tk, int *sg, const int3
     }
     for (int e = tid; e < kChunk * (DQK / 8); e += kThreads) {
         const int t = e / (DQK / 8), c8 = e % (DQK / 8);
-        const int q = t / P;
+        const int q = t >> lp2;
         const int g = q < n ? glist[q] : -1;
         const bool ok = g >= 0 && g < G;
-        const uint16_t *src = ok ? kb + (int64_t(g) * P + t % P) * DQK + c8 * 8 : kb;
+        const uint16_t *src = ok ? kb + (int64_t(g) * P + (t & (P - 1))) * DQK + c8 * 8 : kb;
         cp_async16(smem_u32(tk + (c8 / 8) * 8192 + sw128_offset(t, (c8 % 8) * 8, 1024)), src,
                    ok ? 16 : 0);
     }
     for (int e = tid; e < kChunk * (DV / 8); e += kThreads) {
         const int t = e / (DV / 8), c8 = e % (DV / 8);
-        const int q = t / P;
+        const int q = t >> lp2;
         const int g = q < n ? glist[q] : -1;
         const bool ok = g >= 0 && g < G;
-        const uint16_t *src = ok ? vb + (int64_t(g) * P + t % P) * DV + c8 * 8 : vb;
+        const uint16_t *src = ok ? vb + (int64_t(g) * P + (t & (P - 1))) * DV + c8 * 8 : vb;
         // MN-major: token t is row t%8 of token group t/8, dv chunk c8%8 of atom c8/8
         cp_async16(smem_u32(tv + (c8 / 8) * 8192 + sw128_offset(t, (c8 % 8) * 8, 1024)), src,
                    ok ? 16 : 0);
@@ -860,6 +860,49 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
     }
     PHASE_MARK(10);
+    // Speculative S = Q K^T over this block's prefetched candidates, issued by
+    // the last warp while the block ranks its candidates (the softmax masks the
+    // ones not selected).  TMEM is held from here to the end of the attention;
+    // every exit on the way frees it.
+    cp_async_wait<0>();
+    fence_async_smem();
+    if (tid == 0) {
+        mbar_init(bars, 1);      // S ready
+        mbar_init(bars + 1, 1);  // O_c ready
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *tslot;  // S: columns 0..63, O_c: 64..64+DV
+    auto release_tmem = [&]() {  // uniform: every thread of the block
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_free(tb, 256);
+    };
+    constexpr int kMmaWarp = kWarps - 1;  // issues the tensor-core work
+    auto issue_s = [&](const unsigned char *tk) {
+        if (warp == kMmaWarp) {
+            const uint32_t id = idesc_bf16_f32(128, 64, false, false);
+            const uint32_t qa = smem_u32(qt), ka = smem_u32(tk);
+            if (elect_one()) {
+#pragma unroll
+                for (int ks = 0; ks < DQK / 16; ++ks) {
+                    const uint32_t ko = (ks / 4) * 8192 + (ks % 4) * 32;
+                    tc_mma_bf16(tb, smem_desc(qa + ko, 16, 1024), smem_desc(ka + ko, 16, 1024), id,
+                                ks > 0);
+                }
+                tc_commit(bars);
+            }
+            __syncwarp();
+        }
+    };
+    int n_s = 0;  // S products committed so far (phases of bars[0])
+    if (n_spec > 0) {
+        issue_s(smem + kSpec);
+        n_s = 1;
+    }
     // slot jj as 32-bit words: [0] count + 1, [1] guess, [2 + 2e] key, [3 + 2e] group
     auto hdr = [&](int jj) { return reinterpret_cast<const unsigned *>(stage + jj * kSlotBytes); };
     if (warp == 0) {
@@ -969,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         __syncthreads();
         PHASE_MARK(11);
         if (sv[19]) {  // an overflow entry never arrived
-            cp_async_wait<0>();
+            release_tmem();
             return;
         }
     }
@@ -1149,9 +1192,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         __syncthreads();
     } else {
         // ---------- exact multi-pass selection over the sequence's blocks ----------
-        // level 1: the full 16-bit-bin histogram of every block's scores
-        cp_async_wait<0>();
-        __syncthreads();
+        // level 1: the full 16-bit-bin histogram of every block's scores.  The
+        // speculative S product reads shared memory about to be reused: wait
+        // for it first.
+        const bool s_done = n_s == 0 || mbar_wait(bars, 0, kMbarBudget);
+        if (!__syncthreads_and(s_done)) {
+            raise_timeout(p, 3);
+            release_tmem();
+            return;
+        }
         clear_smem(smem + kU, kUBytes);
         __syncthreads();
         for (int i = tid; i < nloc; i += kThreads) {
@@ -1161,7 +1210,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         __syncthreads();
         flush_hist(h16, hist1);
         arrive(ctl + kSlowB);
-        if (!wait_count(p, ctl + kSlowB, unsigned(n_b), 3, s_ok)) return;
+        if (!wait_count(p, ctl + kSlowB, unsigned(n_b), 3, s_ok)) {
+            release_tmem();
+            return;
+        }
         if (warp == 0) {
             unsigned above = 0;
             const int t1 = k_b > 0 ? hist_walk(hist1, unsigned(k_b), true, &above) : -1;
@@ -1183,7 +1235,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         __syncthreads();
         flush_hist(h16, hist2);
         arrive(ctl + kSlowC);
-        if (!wait_count(p, ctl + kSlowC, unsigned(n_b), 4, s_ok)) return;
+        if (!wait_count(p, ctl + kSlowC, unsigned(n_b), 4, s_ok)) {
+            release_tmem();
+            return;
+        }
         if (warp == 0) {
             unsigned above = 0;
             const int lo = (k_b > 0 && t1 >= 0) ? hist_walk(hist2, need2, true, &above) : -1;
@@ -1209,7 +1264,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             }
         }
         arrive(ctl + kSlowD);
-        if (!wait_count(p, ctl + kSlowD, unsigned(n_b), 5, s_ok)) return;
+        if (!wait_count(p, ctl + kSlowD, unsigned(n_b), 5, s_ok)) {
+            release_tmem();
+            return;
+        }
         if (warp == 0) {
             // offsets of the blocks before this one: each takes its keys > K* and
             // the next ties in group order (blocks hold ascending group ranges)
@@ -1308,27 +1366,23 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             gather_tc<DQK, DV>(gbuf + buf * kv_tile_bytes<DQK, DV>(), gsg + buf * kChunk, own + jb,
                                min(gpc, n_own - jb), P, G_b, Kb, Vb);
         };
-        cp_async_wait<0>();  // prefetched K/V and Q
+        cp_async_wait<0>();  // Q (reloaded on the exact fallback path)
         fence_async_smem();
-        if (tid == 0) {
-            mbar_init(bars, 1);
-            mbar_init(bars + 1, 1);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        }
-        if (nchunks > 0 && warp == 0) tmem_alloc(tslot, 256);
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
         PHASE_MARK(15);
-        const uint32_t tb = *tslot;  // S: columns 0..63, O_c: 64..64+DV
         const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
+        const int lp2 = 31 - __clz(P);  // P is a power of two
         const uint32_t lane_addr = tb + (uint32_t((warp & 3) * 32) << 16);
         if (!use_spec && nchunks > 0) issue(0, 0);
         float o[OC];
 #pragma unroll
         for (int c2 = 0; c2 < OC; ++c2) o[c2] = 0.f;
         float m = -INFINITY, lp = 0.f;  // running max; sum of this warpgroup's columns
-        bool ok = true;
+        // a parity wait only tells the last two phases apart: let the unused
+        // speculative product complete before new ones are issued
+        bool ok = use_spec || n_s == 0 || __all_sync(0xffffffffu, mbar_wait(bars, 0, kMbarBudget));
         for (int ci = 0; ci < nchunks; ++ci) {
             const int buf = ci & 1;
             unsigned char *tk = use_spec ? smem + kSpec : gbuf + buf * kv_tile_bytes<DQK, DV>();
@@ -1345,21 +1399,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 __syncthreads();
                 tc_fence_after();
             }
-            if (tid == 0) {  // S = Q K^T
-                const uint32_t id = idesc_bf16_f32(128, 64, false, false);
-#pragma unroll
-                for (int ks = 0; ks < DQK / 16; ++ks) {
-                    const uint32_t ko = (ks / 4) * 8192 + (ks % 4) * 32;
-                    tc_mma_bf16(tb, smem_desc(smem_u32(qt) + ko, 16, 1024),
-                                smem_desc(smem_u32(tk) + ko, 16, 1024), id, ks > 0);
-                }
-                tc_commit(bars);
+            if (!use_spec) {  // the prefetched chunk's S was issued speculatively
+                issue_s(tk);
+                ++n_s;
             }
             // validity of the chunk's 64 tokens (the same for every row)
             const unsigned long long vmask =
-                (unsigned long long)__ballot_sync(0xffffffffu, cg[lane / P] >= 0) |
-                ((unsigned long long)__ballot_sync(0xffffffffu, cg[(lane + 32) / P] >= 0) << 32);
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(bars, ci & 1, kMbarBudget));
+                (unsigned long long)__ballot_sync(0xffffffffu, cg[lane >> lp2] >= 0) |
+                ((unsigned long long)__ballot_sync(0xffffffffu, cg[(lane + 32) >> lp2] >= 0) << 32);
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(bars, (n_s - 1) & 1, kMbarBudget));
             tc_fence_after();
             PHASE_MARK(25);
             float al = 0.f;
@@ -1404,13 +1452,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             __syncthreads();
             tc_fence_after();
             PHASE_MARK(26);
-            if (tid == 0) {  // O_c = P V
+            if (warp == 0) {  // O_c = P V
                 const uint32_t id = idesc_bf16_f32(128, DV, false, true);
+                const uint32_t pa = smem_u32(pt), va = smem_u32(tk + kTK);
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < kChunk / 16; ++ks)
-                    tc_mma_bf16(tb + 64, smem_desc(smem_u32(pt) + ks * 32, 16, 1024),
-                                smem_desc(smem_u32(tk + kTK) + ks * 2048, 8192, 1024), id, ks > 0);
-                tc_commit(bars + 1);
+                    for (int ks = 0; ks < kChunk / 16; ++ks)
+                        tc_mma_bf16(tb + 64, smem_desc(pa + ks * 32, 16, 1024),
+                                    smem_desc(va + ks * 2048, 8192, 1024), id, ks > 0);
+                    tc_commit(bars + 1);
+                }
+                __syncwarp();
             }
             ok = __all_sync(0xffffffffu, ok && mbar_wait(bars + 1, ci & 1, kMbarBudget));
             tc_fence_after();
@@ -1445,7 +1497,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
         tc_fence_before();
         __syncthreads();
-        if (nchunks > 0 && warp == 0) tmem_free(tb, 256);
+        if (warp == 0) tmem_free(tb, 256);
         if (sv[19]) return;  // a tensor-core step never completed
         // the block's partial state of each head: (m, l) and the unnormalised O row
         const int64_t pbase = int64_t(cta) * p.H_q;
