@@ -319,7 +319,7 @@ def run_lcsw(args, world, rank, local):
         single_ms = time_launches(torch, decs, 50)
         kern_name, kern_bytes = "lcsw_decode_fused (persistent kernel)", ab
         sha_files = ["decode_fused.cu", "fused.cuh", "common.cuh", "attn_core.cuh",
-                     "pool_core.cuh", "select_core.cuh"]
+                     "pool_core.cuh", "select_core.cuh", "tc_core.cuh"]
         prof_file = f"decode_fused_{args.workload}.md"
     else:
         # multi-kernel path: the indexer scoring kernel moves ~97% of the bytes
@@ -406,8 +406,7 @@ def run_e2e(args, torch, lcsw, c, decs, keep, spec, world):
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     n = args.e2e_steps
 
-    def one(i):
-        r = i % R
+    def one_ops(r):
         kp, K, V, qi, w, q = keep["keep"][r]
         hs = host[r]
         qi.copy_(hs["qi"], non_blocking=True)
@@ -420,6 +419,9 @@ def run_e2e(args, torch, lcsw, c, decs, keep, spec, world):
         out, lse = decs[r]()
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
+
+    def one(i):
+        one_ops(i % R)
         torch.cuda.current_stream().synchronize()
 
     for i in range(5):
@@ -428,11 +430,33 @@ def run_e2e(args, torch, lcsw, c, decs, keep, spec, world):
     t0 = time.perf_counter()
     for i in range(n):
         one(i)
+    dt_eager = allreduce_max(time.perf_counter() - t0, world)
+
+    # the same step captured once per rotation as a CUDA graph (copies in, the
+    # decode call, copies out); each step is one graph launch and a sync
+    graphs = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one_ops(r)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    for i in range(5):
+        graphs[i % R].replay()
+        stream.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(n):
+        graphs[i % R].replay()
+        stream.synchronize()
     dt = allreduce_max(time.perf_counter() - t0, world)
     return {"value": round(world * B * n / dt, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n,
+            "eager_value": round(world * B * n / dt_eager, 1),
             "note": "host wall clock; per step: pinned H2D of query tensors and the newest "
-                    "token's rows, lcsw_decode_fused, D2H of out+lse, stream sync"}
+                    "token's rows, lcsw_decode_fused, D2H of out+lse, stream sync; value: the "
+                    "step as one captured CUDA graph launch; eager_value: issued call by call"}
 
 
 def run_ablation(torch, lcsw, c, spec, L2):
