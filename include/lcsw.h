@@ -109,6 +109,9 @@ lcsw_status lcsw_pool_keys(const lcsw_bf16 *k_idx, int64_t sk_b,
  *   q_pos     [B][T] int32 device or NULL (decode: all complete groups visible)
  *   scores    [B][T][G_max] fp32 (output)
  *   d_idx == 64; 1 <= H_i <= 16; P in {1, 2, 4, 8}.
+ * Query blocks of T >= 64 run as a tcgen05 GEMM fed by TMA when sp_b >=
+ * 64 * G_max (it reads whole 128-group tiles up to G_max rows of every
+ * sequence, so those rows must exist); otherwise the mma.sync kernel runs.
  * ------------------------------------------------------------------------- */
 lcsw_status lcsw_index_scores(const lcsw_bf16 *q_idx, const float *w_head,
                               const lcsw_bf16 *k_pooled, int64_t sp_b,

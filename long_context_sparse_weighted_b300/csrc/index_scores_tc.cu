@@ -1,14 +1,221 @@
-// Indexer scores for chunked prefill as a tcgen05 GEMM (not yet enabled).
+// Indexer scores for a chunk of prefill queries as a tcgen05 GEMM fed by TMA
+// (the indexer score of "G2C Brief -- GLM-5.3-Flash", section "DSA keeps
+// selected global access in eleven layers", over pooled keys as in the reading
+// notes, section 2):
+//
+//   scores[b][t][g] = sum_h w[b][t][h] * max(0, q[b][t][h] . k_pooled[b][g])
+//
+// for the groups visible to query t (g < seq_len[b]/P and, with q_pos,
+// P*g + P - 1 <= q_pos[b][t]), -inf for the others.
+//
+// One CTA per tile of 128 queries x 128 groups, 256 threads, two CTAs per SM.
+// TMA brings the group tile once and, per indexer head, the 128 x 64 query
+// tile of that head (both 128-byte swizzled, two query buffers).  Head h's
+// product D_h = Q_h K^T (M = 128 queries, N = 128 groups, K = 64: four MMAs)
+// lands in one of two TMEM buffers, so the MMA of head h + 1 runs while the
+// warps fold head h into their running sums: warp w reads TMEM lanes
+// 32 (w % 4) .. +31 (its query rows) and columns 64 (w / 4) .. +63, and adds
+// w_h * max(0, x) in registers.  Tiles where no group is visible to any of
+// the 128 queries are written as -inf without touching the tensor cores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/lcsw.h"
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tc_core.cuh"
 
 namespace lcsw {
+namespace {
 
-bool index_scores_tc_supported(int, int, int, int, int64_t) { return false; }
-cudaError_t launch_index_scores_tc(const uint16_t *, const float *, const uint16_t *, int64_t,
-                                   const int32_t *, const int32_t *, int, int, int, int, int,
-                                   float *, int *, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int kTM = 128;        // queries per tile
+constexpr int kTN = 128;        // groups per tile
+constexpr int kThr = 256;       // threads per CTA
+constexpr int kTile = 16384;    // one 128-row x 128-byte operand tile
+constexpr int kSmem = 3 * kTile + 1024;  // group tile, two query tiles, barriers
+constexpr long long kWaitBudget = 1ll << 22;
+constexpr unsigned kIdesc = idesc_bf16_f32(kTM, kTN, false, false);
+
+__global__ void __launch_bounds__(kThr, 2)
+    scores_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const float *__restrict__ w_head, const int32_t *__restrict__ seq_len,
+                     const int32_t *__restrict__ q_pos, int T, int H_i, int P, int G_max,
+                     float *__restrict__ scores, int *status) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    unsigned char *sk = sm, *sq = sm + kTile;  // group tile; query tiles [2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + 3 * kTile);  // k, q[2], d[2]
+    uint32_t *slot = reinterpret_cast<uint32_t *>(bars + 5);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g0 = blockIdx.x * kTN, t0 = blockIdx.y * kTM, b = blockIdx.z;
+    const int row = (warp & 3) * 32 + lane, t = t0 + row, c0 = (warp >> 2) * 64;
+
+    // groups visible to this thread's query
+    int nvis = 0;
+    if (t < T) {
+        nvis = min(max(__ldg(seq_len + b) / P, 0), G_max);
+        if (q_pos) nvis = min(nvis, max(0, (__ldg(q_pos + int64_t(b) * T + t) + 1) / P));
+    }
+    float *orow = scores + (int64_t(b) * T + t) * G_max;
+    auto store = [&](const float (&acc)[64]) {
+        if (t >= T) return;
+        const bool vec = (G_max & 3) == 0;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+            const int g = g0 + c0 + j;
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = g + e < nvis ? acc[j + e] + 0.0f : -INFINITY;
+            if (vec && g + 3 < G_max) {
+                __stcs(reinterpret_cast<float4 *>(orow + g), make_float4(v[0], v[1], v[2], v[3]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (g + e < G_max) __stcs(orow + g + e, v[e]);
+            }
+        }
+    };
+    float acc[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+    if (!__syncthreads_or(g0 < nvis)) {  // nothing visible in this tile
+        store(acc);
+        return;
+    }
+    if ((smem_u32(sm) & 1023u) != 0u) {  // the swizzled tiles need 1024-byte alignment
+        if (tid == 0 && status) atomicCAS(status, 0, int(LCSW_ERR_UNSUPPORTED) * 256);
+        return;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(bars, kTile);
+        tma_load_3d(sk, &tk, bars, 0, g0, b);
+        for (int h = 0; h < min(2, H_i); ++h) {
+            mbar_expect_tx(bars + 1 + h, kTile);
+            tma_load_3d(sq + h * kTile, &tq, bars + 1 + h, 0, h, b * T + t0);
+        }
+    }
+    if (warp == 0) tmem_alloc(slot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;  // D buffers: columns 0..127 and 128..255
+    const float *wrow = w_head + (int64_t(b) * T + min(t, T - 1)) * H_i;
+
+    bool ok = true;
+    // head h's product, issued by one lane of warp 1 once its tiles have landed
+    auto issue = [&](int h) {
+        if (warp != 1) return;
+        bool good = true;
+        if (elect_one()) {
+            good = (h > 0 || mbar_wait(bars, 0, kWaitBudget)) &&
+                   mbar_wait(bars + 1 + (h & 1), (h >> 1) & 1, kWaitBudget);
+            if (good) {
+                tc_fence_after();
+                const uint32_t qa = smem_u32(sq + (h & 1) * kTile), ka = smem_u32(sk);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc_mma_bf16(tb + (h & 1) * kTN, smem_desc(qa + ks * 32, 16, 1024),
+                                smem_desc(ka + ks * 32, 16, 1024), kIdesc, ks > 0);
+                tc_commit(bars + 3 + (h & 1));
+            }
+        }
+        ok = __all_sync(0xffffffffu, good) && ok;
+    };
+    issue(0);
+    const uint32_t lane_addr = tb + (uint32_t((warp & 3) * 32) << 16) + c0;
+    for (int h = 0; h < H_i; ++h) {
+        if (h + 1 < H_i) issue(h + 1);
+        const float wh = __ldg(wrow + h);
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(bars + 3 + (h & 1), (h >> 1) & 1, kWaitBudget));
+        tc_fence_after();
+        if (ok) {
+            uint32_t r[16];
+#pragma unroll
+            for (int cc = 0; cc < 64; cc += 16) {
+                tc_ld16(lane_addr + (h & 1) * kTN + cc, r);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    acc[cc + e] = __fadd_rn(acc[cc + e],
+                                            __fmul_rn(wh, fmaxf(__uint_as_float(r[e]), 0.f)));
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // head h's buffers are free again
+        if (tid == 0 && h + 2 < H_i && ok) {
+            mbar_expect_tx(bars + 1 + (h & 1), kTile);
+            tma_load_3d(sq + (h & 1) * kTile, &tq, bars + 1 + (h & 1), 0, h + 2, b * T + t0);
+        }
+    }
+    tc_fence_after();
+    if (!__syncthreads_and(ok)) {
+        if (tid == 0 && status) atomicCAS(status, 0, int(LCSW_ERR_TIMEOUT) * 256 + 9);
+    } else {
+        store(acc);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_free(tb, 256);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool index_scores_tc_supported(int B, int T, int H_i, int G_max, int64_t sp_b) {
+    // the group tiles read up to G_max rows of every sequence's cache
+    return T >= 64 && H_i >= 1 && H_i <= 16 && B >= 1 && B <= 65535 && G_max >= 1 &&
+           (T + kTM - 1) / kTM <= 65535 && sp_b % 8 == 0 && sp_b >= int64_t(64) * G_max &&
+           encode_fn() != nullptr;
+}
+
+cudaError_t launch_index_scores_tc(const uint16_t *q_idx, const float *w_head,
+                                   const uint16_t *k_pooled, int64_t sp_b,
+                                   const int32_t *seq_len, const int32_t *q_pos, int B, int T,
+                                   int H_i, int P, int G_max, float *scores, int *status,
+                                   cudaStream_t st) {
+    if (!index_scores_tc_supported(B, T, H_i, G_max, sp_b)) return cudaErrorNotSupported;
+    auto enc = encode_fn();
+    CUtensorMap tq, tk;
+    // queries viewed as [B*T][H_i][64]: one box = 128 queries of one head
+    const cuuint64_t qdim[3] = {64, cuuint64_t(H_i), cuuint64_t(B) * T};
+    const cuuint64_t qstr[2] = {128, cuuint64_t(H_i) * 128};
+    const cuuint32_t qbox[3] = {64, 1, kTM};
+    // pooled keys viewed as [B][G_max][64] with the batch stride: one box = 128 groups
+    const cuuint64_t kdim[3] = {64, cuuint64_t(G_max), cuuint64_t(B)};
+    const cuuint64_t kstr[2] = {128, cuuint64_t(sp_b) * 2};
+    const cuuint32_t kbox[3] = {64, kTN, 1};
+    const cuuint32_t ones[3] = {1, 1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(q_idx), qdim, qstr,
+            qbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(k_pooled), kdim,
+            kstr, kbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(unsigned((G_max + kTN - 1) / kTN), unsigned((T + kTM - 1) / kTM), unsigned(B));
+    scores_tc_kernel<<<grid, kThr, kSmem, st>>>(tq, tk, w_head, seq_len, q_pos, T, H_i, P, G_max,
+                                                 scores, status);
+    return cudaGetLastError();
 }
 
 }  // namespace lcsw

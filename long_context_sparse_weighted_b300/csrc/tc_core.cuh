@@ -1,7 +1,7 @@
 // Fifth-generation tensor-core building blocks for sm_103a: shared-memory
 // matrix descriptors, the kind::f16 instruction descriptor, tensor-memory
 // (TMEM) allocation, single-thread tcgen05.mma issue with completion tracked
-// by an mbarrier (bounded wait), and tcgen05.ld read-back.
+// by an mbarrier (bounded wait), tcgen05.ld read-back, and TMA tile loads.
 //
 // Operand layouts used here are the 128-byte-swizzle canonical layouts:
 //   K-major (rows = M or N, 64 bf16 of K per 128-byte row):
@@ -70,6 +70,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
         if (done) return true;
     }
     return false;
+}
+
+// Arrive once on the mbarrier and expect `bytes` of asynchronous copies.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// -------------------------------------------------------------------- TMA -----
+// Tiled 3-D tensor load into shared memory; completion is counted in bytes on
+// the mbarrier.  `tmap` is the address of a CUtensorMap kernel parameter.  The
+// innermost coordinate must address a 16-byte boundary (here always 0).
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
+                                            int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // ------------------------------------------------------------------ TMEM -----

@@ -100,6 +100,37 @@ def test_scores_causal_multi_query(T):
     assert_scores_close(got, ref)
 
 
+# Prefill query blocks (T >= 64) score on the tcgen05 GEMM: tiles of 128 queries
+# x 128 groups, ragged in both directions; G_max % 4 != 0 takes the scalar
+# store path.
+@pytest.mark.parametrize("H_i,T,L0,L1", [(8, 300, 16012, 9001), (1, 128, 4096, 777),
+                                         (16, 77, 10004, 5000)])
+def test_scores_tensor_core_prefill(H_i, T, L0, L1):
+    spec = synth.Spec(B=2, lengths=[L0, L1], T=T, prefill=True, H_i=H_i, w_mode="signed",
+                      seed=140 + H_i)
+    c = synth.generate(spec, with_kv=False)
+    kp = oracle.pool_keys(c["k_idx"], c["pool_w"], c["seq_len"], 4)
+    ref = oracle.index_scores(c["q_idx"], c["w_head"], kp, c["seq_len"], 4, q_pos=c["q_pos"])
+    d = upload_case(c)
+    got = lcsw.index_scores(d["q_idx"], d["w_head"], dev_bf16(kp), d["seq_len"], 4,
+                            q_pos=d["q_pos"]).cpu().numpy()
+    assert_scores_close(got, ref)
+
+
+def test_scores_tensor_core_exact_integer_inputs():
+    # integer-valued keys and queries, dyadic pooling and head weights: every
+    # product and sum is exact in fp32, so the GEMM path is bit-exact
+    spec = synth.Spec(B=1, lengths=[4096 + 200], T=200, prefill=True, H_i=4, idx_values="int3",
+                      w_mode="quarter_half", pool_mode="dyadic", seed=130)
+    c = synth.generate(spec, with_kv=False)
+    kp = oracle.pool_keys(c["k_idx"], c["pool_w"], c["seq_len"], 4)
+    ref = oracle.index_scores(c["q_idx"], c["w_head"], kp, c["seq_len"], 4, q_pos=c["q_pos"])
+    d = upload_case(c)
+    got = lcsw.index_scores(d["q_idx"], d["w_head"], dev_bf16(kp), d["seq_len"], 4,
+                            q_pos=d["q_pos"]).cpu().numpy()
+    assert np.array_equal(got, ref)
+
+
 def test_visible_counts_exact():
     seq = np.array([0, 3, 4, 17, 4096], np.int32)
     q_pos = np.array([[-1, 0, 2], [0, 1, 2], [2, 3, 3], [3, 7, 16], [100, 4094, 4095]], np.int32)
