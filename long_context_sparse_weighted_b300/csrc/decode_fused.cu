@@ -71,7 +71,7 @@ constexpr int kTieCap = 256;       // threshold-bin candidates resolved by rank 
 constexpr int kMaxK = 2048;        // selected groups per sequence
 constexpr int kCtlWords = 32;      // control words per sequence
 constexpr int kMaxCtas = 160;
-constexpr long long kMbarBudget = 1ll << 22;  // polls of a tensor-core completion wait
+constexpr long long kMbarBudget = 50000;  // tries (up to 20 us each) of a tensor-core wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

@@ -35,7 +35,7 @@ constexpr int kTN = 128;        // groups per tile
 constexpr int kThr = 256;       // threads per CTA
 constexpr int kTile = 16384;    // one 128-row x 128-byte operand tile
 constexpr int kSmem = 3 * kTile + 1024;  // group tile, two query tiles, barriers
-constexpr long long kWaitBudget = 1ll << 22;
+constexpr long long kWaitBudget = 50000;  // tries of up to 20 us
 constexpr unsigned kIdesc = idesc_bf16_f32(kTM, kTN, false, false);
 
 __global__ void __launch_bounds__(kThr, 2)
@@ -161,6 +161,230 @@ __global__ void __launch_bounds__(kThr, 2)
     if (warp == 0) tmem_free(tb, 256);
 }
 
+// Persistent form for H_i <= 8: every query block's H_i query tiles stay in
+// shared memory while the CTA walks its range of group tiles, so the loop
+// never waits on a query load.  Warp roles: warps 0-15 fold products into
+// sums and store (warp w: TMEM lane quarter w % 4, 32 columns from
+// 32 (w / 4)), warp 16 is the TMA producer (query tiles per block, group
+// tiles through a 3-slot ring), warp 17 issues the MMAs (one product per head
+// into four rotating TMEM buffers).  Hand-offs are mbarriers: slot full / empty, buffer full / empty,
+// query block loaded / released.  Group tiles past a sequence's length are
+// written as -inf without a load or an MMA.
+constexpr int kPThr = 576;                    // 16 folding warps + producer + MMA warp
+constexpr int kPFold = 16;
+constexpr int kPSlots = 3;                    // group-tile ring
+constexpr int kPBufs = 4;                     // TMEM product buffers (4 x 128 columns)
+constexpr int kPQ = 8 * kTile;                // query tiles of one block
+constexpr int kPSmem = kPQ + kPSlots * kTile + 1024;
+
+struct PBars {  // mbarrier indices
+    static constexpr int qfull = 0, qfree = 1, kfull = 2, kfree = kfull + kPSlots,
+                         dfull = kfree + kPSlots, dfree = dfull + kPBufs, n = dfree + kPBufs;
+};
+
+__global__ void __launch_bounds__(kPThr, 1)
+    scores_tc_persist_kernel(const __grid_constant__ CUtensorMap tq,
+                             const __grid_constant__ CUtensorMap tk,
+                             const float *__restrict__ w_head, const int32_t *__restrict__ seq_len,
+                             const int32_t *__restrict__ q_pos, int B, int T, int H_i, int P,
+                             int G_max, float *__restrict__ scores, int *status) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    unsigned char *sq = sm, *sk = sm + kPQ;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kPQ + kPSlots * kTile);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(bars + PBars::n);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(slot + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nqb = (T + kTM - 1) / kTM, ngt = (G_max + kTN - 1) / kTN;
+    const long long n_units = (long long)B * nqb * ngt;
+    const long long u0 = n_units * blockIdx.x / gridDim.x;
+    const long long u1 = n_units * (blockIdx.x + 1) / gridDim.x;
+    if (u0 >= u1) return;
+    if ((smem_u32(sm) & 1023u) != 0u) {
+        if (tid == 0 && status) atomicCAS(status, 0, int(LCSW_ERR_UNSUPPORTED) * 256);
+        return;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < PBars::n; ++i)
+            mbar_init(bars + i, (i >= PBars::dfree && i < PBars::dfree + kPBufs) ? kPFold : 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        *abort_flag = 0;
+    }
+    if (warp == 0) tmem_alloc(slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;
+    // units are walked in order (batch, query block, group tile): one decode,
+    // then increments; Gb = the batch's complete groups (P is a power of two)
+    const int lp2 = 31 - __clz(P);
+    struct Walk {
+        int b, qb, gt, Gb;
+    };
+    auto start = [&]() {
+        Walk w;
+        w.gt = int(u0 % ngt);
+        w.qb = int((u0 / ngt) % nqb);
+        w.b = int(u0 / ((long long)ngt * nqb));
+        w.Gb = min(max(__ldg(seq_len + w.b) >> lp2, 0), G_max);
+        return w;
+    };
+    auto next = [&](Walk &w) {
+        if (++w.gt == ngt) {
+            w.gt = 0;
+            if (++w.qb == nqb) {
+                w.qb = 0;
+                ++w.b;
+                if (w.b < B) w.Gb = min(max(__ldg(seq_len + w.b) >> lp2, 0), G_max);
+            }
+        }
+    };
+    auto wait = [&](int bar, unsigned parity) {
+        if (*abort_flag) return false;
+        if (mbar_wait(bars + bar, parity, kWaitBudget)) return true;
+        *abort_flag = 1;
+        return false;
+    };
+
+    if (warp == kPFold) {  // ---------------- TMA producer
+        if (elect_one()) {
+            int kq = 0, nq = 0, prev = -1;
+            Walk w = start();
+            for (long long u = u0; u < u1 && !*abort_flag; ++u, next(w)) {
+                const int b = w.b, qb = w.qb, gt = w.gt;
+                if (b * nqb + qb != prev) {  // a new query block: reload its query tiles
+                    if (nq > 0 && !wait(PBars::qfree, (nq - 1) & 1)) break;
+                    mbar_expect_tx(bars + PBars::qfull, H_i * kTile);
+                    for (int h = 0; h < H_i; ++h)
+                        tma_load_3d(sq + h * kTile, &tq, bars + PBars::qfull, 0, h, b * T + qb * kTM);
+                    prev = b * nqb + qb;
+                    ++nq;
+                }
+                if (gt * kTN >= w.Gb) continue;
+                const int s = kq % kPSlots;
+                if (kq >= kPSlots && !wait(PBars::kfree + s, ((kq / kPSlots) - 1) & 1)) break;
+                mbar_expect_tx(bars + PBars::kfull + s, kTile);
+                tma_load_3d(sk + s * kTile, &tk, bars + PBars::kfull + s, 0, gt * kTN, b);
+                ++kq;
+            }
+        }
+        __syncwarp();
+    } else if (warp == kPFold + 1) {  // ---------------- MMA issuer
+        if (elect_one()) {
+            int kq = 0, nq = 0, nd = 0, prev = -1;
+            Walk w = start();
+            for (long long u = u0; u < u1 && !*abort_flag; ++u, next(w)) {
+                const int b = w.b, qb = w.qb, gt = w.gt;
+                if (b * nqb + qb != prev) {
+                    if (nq > 0) tc_commit(bars + PBars::qfree);  // old query tiles released
+                    if (!wait(PBars::qfull, nq & 1)) break;
+                    prev = b * nqb + qb;
+                    ++nq;
+                }
+                if (gt * kTN >= w.Gb) continue;
+                const int s = kq % kPSlots;
+                if (!wait(PBars::kfull + s, (kq / kPSlots) & 1)) break;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(sk + s * kTile);
+                bool good = true;
+                for (int h = 0; h < H_i && good; ++h, ++nd) {
+                    const int d = nd % kPBufs;
+                    if (nd >= kPBufs && !wait(PBars::dfree + d, ((nd / kPBufs) - 1) & 1)) {
+                        good = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t qa = smem_u32(sq + h * kTile);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc_mma_bf16(tb + d * kTN, smem_desc(qa + ks * 32, 16, 1024),
+                                    smem_desc(ka + ks * 32, 16, 1024), kIdesc, ks > 0);
+                    tc_commit(bars + PBars::dfull + d);
+                }
+                if (!good) break;
+                tc_commit(bars + PBars::kfree + s);  // the slot frees when these MMAs finish
+                ++kq;
+            }
+        }
+        __syncwarp();
+    } else {  // ---------------- warps 0-15: fold and store
+        const int row = (warp & 3) * 32 + lane, c0 = (warp >> 2) * 32;
+        const uint32_t lane_addr = tb + (uint32_t((warp & 3) * 32) << 16) + c0;
+        int nd = 0, prev = -1, nvis = 0, t = 0;
+        float wv[8];
+        Walk w = start();
+        for (long long u = u0; u < u1 && !*abort_flag; ++u, next(w)) {
+            const int b = w.b, qb = w.qb, gt = w.gt, Gb = w.Gb;
+            if (b * nqb + qb != prev) {
+                prev = b * nqb + qb;
+                t = qb * kTM + row;
+                nvis = 0;
+                if (t < T) {
+                    nvis = Gb;
+                    if (q_pos) nvis = min(nvis, max(0, (__ldg(q_pos + int64_t(b) * T + t) + 1) >> lp2));
+                }
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                    wv[h] = (h < H_i && t < T) ? __ldg(w_head + (int64_t(b) * T + t) * H_i + h) : 0.f;
+            }
+            const int g0 = gt * kTN + c0;
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+            if (gt * kTN < Gb) {
+                bool good = true;
+#pragma unroll 1
+                for (int h = 0; h < H_i; ++h, ++nd) {
+                    const int d = nd % kPBufs;
+                    good = __all_sync(0xffffffffu, good && wait(PBars::dfull + d, (nd / kPBufs) & 1));
+                    tc_fence_after();
+                    if (good) {
+                        float wh = wv[0];
+#pragma unroll
+                        for (int hh = 1; hh < 8; ++hh) wh = h == hh ? wv[hh] : wh;
+                        uint32_t r0[16], r1[16];
+                        tc_ld16(lane_addr + d * kTN, r0);
+                        tc_ld16(lane_addr + d * kTN + 16, r1);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            acc[e] = fmaf(wh, fmaxf(__uint_as_float(r0[e]), 0.f), acc[e]);
+                            acc[16 + e] = fmaf(wh, fmaxf(__uint_as_float(r1[e]), 0.f), acc[16 + e]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
+                                                    smem_u32(bars + PBars::dfree + d))
+                                                : "memory");
+                }
+                if (!good) break;
+            }
+            if (t < T) {
+                float *orow = scores + (int64_t(b) * T + t) * G_max;
+                const bool vec = (G_max & 3) == 0;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const int g = g0 + j;
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[e] = g + e < nvis ? acc[j + e] + 0.0f : -INFINITY;
+                    if (vec && g + 3 < G_max) {
+                        __stcs(reinterpret_cast<float4 *>(orow + g), make_float4(v[0], v[1], v[2], v[3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (g + e < G_max) __stcs(orow + g + e, v[e]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && tid == 0 && status) atomicCAS(status, 0, int(LCSW_ERR_TIMEOUT) * 256 + 9);
+    if (warp == 0) tmem_free(tb, 512);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -209,6 +433,17 @@ cudaError_t launch_index_scores_tc(const uint16_t *q_idx, const float *w_head,
             kstr, kbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    if (H_i <= 8) {
+        cudaError_t e = cudaFuncSetAttribute(scores_tc_persist_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+        if (e != cudaSuccess) return e;
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        scores_tc_persist_kernel<<<sms, kPThr, kPSmem, st>>>(tq, tk, w_head, seq_len, q_pos, B, T,
+                                                             H_i, P, G_max, scores, status);
+        return cudaGetLastError();
+    }
     cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;

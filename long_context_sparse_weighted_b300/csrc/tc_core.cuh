@@ -55,17 +55,20 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
 }
-// Wait for the phase with the given parity to complete; gives up after
-// `budget` polls and returns false.
+// Wait for the phase with the given parity to complete.  Each try suspends
+// the thread until the phase completes or kSuspendNs pass (so waiting warps
+// do not spin on issue slots); gives up after `budget` tries (about budget x
+// 20 us) and returns false.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long budget) {
     const uint32_t a = smem_u32(bar);
     for (long long i = 0; i < budget; ++i) {
         uint32_t done;
         asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
             " selp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)
-            : "r"(a), "r"(parity)
+            : "r"(a), "r"(parity), "r"(kSuspendNs)
             : "memory");
         if (done) return true;
     }
