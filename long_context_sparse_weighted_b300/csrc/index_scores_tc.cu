@@ -172,10 +172,11 @@ __global__ void __launch_bounds__(kThr, 2)
 // written as -inf without a load or an MMA.
 constexpr int kPThr = 576;                    // 16 folding warps + producer + MMA warp
 constexpr int kPFold = 16;
-constexpr int kPSlots = 3;                    // group-tile ring
+constexpr int kPSlots = 2;                    // group-tile ring
 constexpr int kPBufs = 4;                     // TMEM product buffers (4 x 128 columns)
 constexpr int kPQ = 8 * kTile;                // query tiles of one block
-constexpr int kPSmem = kPQ + kPSlots * kTile + 1024;
+constexpr int kPStage = kPFold * 32 * 128;    // per folding warp: 32 rows x 32 floats
+constexpr int kPSmem = kPQ + kPSlots * kTile + kPStage + 1024;
 
 struct PBars {  // mbarrier indices
     static constexpr int qfull = 0, qfree = 1, kfull = 2, kfree = kfull + kPSlots,
@@ -190,7 +191,8 @@ __global__ void __launch_bounds__(kPThr, 1)
                              int G_max, float *__restrict__ scores, int *status) {
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char *sq = sm, *sk = sm + kPQ;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kPQ + kPSlots * kTile);
+    float *stage_all = reinterpret_cast<float *>(sm + kPQ + kPSlots * kTile);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kPQ + kPSlots * kTile + kPStage);
     uint32_t *slot = reinterpret_cast<uint32_t *>(bars + PBars::n);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(slot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -337,46 +339,63 @@ __global__ void __launch_bounds__(kPThr, 1)
                     const int d = nd % kPBufs;
                     good = __all_sync(0xffffffffu, good && wait(PBars::dfull + d, (nd / kPBufs) & 1));
                     tc_fence_after();
+                    uint32_t r[32];
                     if (good) {
-                        float wh = wv[0];
-#pragma unroll
-                        for (int hh = 1; hh < 8; ++hh) wh = h == hh ? wv[hh] : wh;
-                        uint32_t r0[16], r1[16];
-                        tc_ld16(lane_addr + d * kTN, r0);
-                        tc_ld16(lane_addr + d * kTN + 16, r1);
+                        tc_ld32(lane_addr + d * kTN, r);
                         tc_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            acc[e] = fmaf(wh, fmaxf(__uint_as_float(r0[e]), 0.f), acc[e]);
-                            acc[16 + e] = fmaf(wh, fmaxf(__uint_as_float(r1[e]), 0.f), acc[16 + e]);
-                        }
                     }
+                    // buffer d is in registers: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
                                                     smem_u32(bars + PBars::dfree + d))
                                                 : "memory");
+                    if (good) {
+                        float wh = wv[0];
+#pragma unroll
+                        for (int hh = 1; hh < 8; ++hh) wh = h == hh ? wv[hh] : wh;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            acc[e] = fmaf(wh, fmaxf(__uint_as_float(r[e]), 0.f), acc[e]);
+                    }
                 }
                 if (!good) break;
             }
-            if (t < T) {
-                float *orow = scores + (int64_t(b) * T + t) * G_max;
-                const bool vec = (G_max & 3) == 0;
+            // masked row values -> the warp's staging block (row = lane, 16-byte
+            // chunks XOR-swizzled by row) -> eight lanes per 128-byte row segment
+            float *stg = stage_all + warp * 32 * 32;
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const int g = g0 + j;
-                    float v[4];
+            for (int j = 0; j < 32; j += 4) {
+                const int g = g0 + j;
+                float4 v;
+                v.x = g + 0 < nvis ? acc[j + 0] + 0.0f : -INFINITY;
+                v.y = g + 1 < nvis ? acc[j + 1] + 0.0f : -INFINITY;
+                v.z = g + 2 < nvis ? acc[j + 2] + 0.0f : -INFINITY;
+                v.w = g + 3 < nvis ? acc[j + 3] + 0.0f : -INFINITY;
+                *reinterpret_cast<float4 *>(stg + lane * 32 + (((j >> 2) ^ (lane & 7)) << 2)) = v;
+            }
+            __syncwarp();
+            {
+                const int ch = lane & 7, g = g0 + ch * 4;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) v[e] = g + e < nvis ? acc[j + e] + 0.0f : -INFINITY;
-                    if (vec && g + 3 < G_max) {
-                        __stcs(reinterpret_cast<float4 *>(orow + g), make_float4(v[0], v[1], v[2], v[3]));
-                    } else {
+                for (int m = 0; m < 8; ++m) {
+                    const int r = (lane >> 3) + 4 * m, tr = qb * kTM + (warp & 3) * 32 + r;
+                    if (tr < T && g < G_max) {
+                        const float4 v = *reinterpret_cast<const float4 *>(
+                            stg + r * 32 + ((ch ^ (r & 7)) << 2));
+                        float *dst = scores + (int64_t(b) * T + tr) * G_max + g;
+                        if ((G_max & 3) == 0) {
+                            __stcs(reinterpret_cast<float4 *>(dst), v);
+                        } else {
+                            const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (g + e < G_max) __stcs(orow + g + e, v[e]);
+                            for (int e = 0; e < 4; ++e)
+                                if (g + e < G_max) __stcs(dst + e, vv[e]);
+                        }
                     }
                 }
             }
+            __syncwarp();
         }
     }
     tc_fence_before();
