@@ -53,6 +53,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--copies", type=int, default=0,
                     help="rotated input copies (0: enough to exceed 3x L2)")
+    ap.add_argument("--kernel", default=None, choices=["prefill_scores"],
+                    help="time one kernel of the path instead of the decode step (not the "
+                         "headline line): prefill_scores = the chunked-prefill indexer "
+                         "scores (tcgen05 GEMM) on the prefill_4k shapes")
     return ap.parse_args()
 
 
@@ -563,8 +567,61 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_scores(args):
+    """Chunked-prefill indexer scores alone: [T x H_i x 64] against every pooled
+    key of the sequence, causal at group granularity, fp32 score matrix out."""
+    import torch
+
+    import long_context_sparse_weighted_b300 as lcsw
+    spec = synth.named("prefill_4k")
+    c = synth.generate(spec, with_kv=False)
+    P, B, T, H = spec.P, spec.B, spec.T, spec.H_i
+    G_max = spec.L_max // P
+    up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(
+        torch.bfloat16)
+    seq = torch.from_numpy(c["seq_len"]).cuda()
+    q_pos = torch.from_numpy(c["q_pos"]).cuda()
+    qi, w = up16(c["q_idx"]), torch.from_numpy(c["w_head"]).cuda()
+    kp = torch.zeros(B, G_max, 64, dtype=torch.bfloat16, device="cuda")
+    lcsw.pool_keys(up16(c["k_idx"]), torch.from_numpy(c["pool_w"]).cuda(), seq, P, kp)
+    out = torch.empty(B, T, G_max, dtype=torch.float32, device="cuda")
+    run = lambda: lcsw.index_scores(qi, w, kp, seq, P, q_pos=q_pos, out=out)
+    for _ in range(max(3, args.warmup)):
+        run()
+    torch.cuda.synchronize()
+    steps = min(args.steps, 200)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # algorithmic work: every (query, visible group) pair, all heads
+    G_vis = np.minimum(int(c["seq_len"][0]) // P, (c["q_pos"][0].astype(np.int64) + 1) // P)
+    flops = 2.0 * float(G_vis.sum()) * H * 64
+    bytes_ = T * G_max * 4 + T * H * (64 * 2 + 4) + G_max * 64 * 2
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    tf_peak = peaks.get("bf16_tflops", 1800.0)
+    hbm_peak = peaks.get("hbm_gbs", 6400.0)
+    tflops = flops / (ms / 1e3) / 1e12
+    gbs = bytes_ / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "kernel": "index_scores (tcgen05 + TMA, chunked prefill)", "workload": "prefill_4k",
+        "shape": {"T": T, "G_max": G_max, "H_i": H, "d_idx": 64}, "ms": round(ms, 5),
+        "steps": steps, "tflops": round(tflops, 1), "tensor_peak_tflops": tf_peak,
+        "frac_tensor": round(tflops / tf_peak, 4), "hbm_gbs": round(gbs, 1),
+        "hbm_peak_gbs": hbm_peak, "frac_hbm": round(gbs / hbm_peak, 4),
+        "alg_flops": flops, "alg_bytes": bytes_,
+        "bound_ms": round(max(flops / tf_peak / 1e9, bytes_ / hbm_peak / 1e6), 5)}))
+
+
 def main():
     args = parse()
+    if args.kernel == "prefill_scores":
+        run_prefill_scores(args)
+        return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

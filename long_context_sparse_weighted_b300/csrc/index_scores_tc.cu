@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThr, 2)
 // never waits on a query load.  Warp roles: warps 0-15 fold products into
 // sums and store (warp w: TMEM lane quarter w % 4, 32 columns from
 // 32 (w / 4)), warp 16 is the TMA producer (query tiles per block, group
-// tiles through a 3-slot ring), warp 17 issues the MMAs (one product per head
+// tiles through a 2-slot ring), warp 17 issues the MMAs (one product per head
 // into four rotating TMEM buffers).  Hand-offs are mbarriers: slot full / empty, buffer full / empty,
 // query block loaded / released.  Group tiles past a sequence's length are
 // written as -inf without a load or an MMA.
