@@ -268,7 +268,17 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
  * granularity.  Pools the groups the chunk completes (from the group holding
  * token seq_len[b]-T onwards), scores every visible group for every query
  * with a tensor-core GEMM, selects the top k per query and attends.
+ *
+ * With H_i <= 8, T >= 64 and G_max <= 524288, the selection is fused with the
+ * scoring: a sample of the groups sets each query's threshold, the GEMM keeps
+ * only the groups at or above it, and the exact top k is taken from those.  A
+ * query whose kept groups cannot be shown to hold its top k (too few, or more
+ * than the per-row capacity) falls back to dense scores and the radix top-k,
+ * decided on the device: the result is the same exact top k either way.
+ * flags: LCSW_PREFILL_FORCE_FALLBACK sends every query through the fallback
+ * (a test of that path).
  * ------------------------------------------------------------------------- */
+#define LCSW_PREFILL_FORCE_FALLBACK 1
 typedef struct {
     const lcsw_bf16 *q_idx;    /* [B][T][H_i][d_idx]                           */
     const float *w_head;       /* [B][T][H_i]                                  */
@@ -289,6 +299,7 @@ typedef struct {
     lcsw_bf16 *out;            /* [B][T][H_q][d_v]                             */
     float *lse;                /* [B][T][H_q] or NULL                          */
     int32_t *idx_out;          /* [B][T][k] or NULL                            */
+    int flags;                 /* LCSW_PREFILL_* bits, normally 0              */
 } lcsw_prefill_args;
 
 size_t lcsw_prefill_workspace_size(const lcsw_prefill_args *a);

@@ -44,6 +44,7 @@ class DecodeArgs(ctypes.Structure):
 FORCE_MULTIPASS_SELECT = 1
 FORCE_MULTIKERNEL = 2
 TEST_SKIP_ARRIVE = 4
+PREFILL_FORCE_FALLBACK = 1  # lcsw_prefill_args.flags
 
 
 class PrefillArgs(ctypes.Structure):
@@ -55,7 +56,7 @@ class PrefillArgs(ctypes.Structure):
         ("seq_len", _vp),
         ("B", _i32), ("T", _i32), ("G_max", _i32), ("H_i", _i32), ("d_idx", _i32), ("P", _i32),
         ("k", _i32), ("H_q", _i32), ("d_qk", _i32), ("d_v", _i32), ("scale", _f32),
-        ("out", _vp), ("lse", _vp), ("idx_out", _vp),
+        ("out", _vp), ("lse", _vp), ("idx_out", _vp), ("flags", _i32),
     ]
 
 
@@ -326,7 +327,7 @@ def decode_fused(q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale, **kw):
 
 
 def prefill(q_idx, w_head, k_pooled, k_idx, pool_w, q, K, V, seq_len, P, k, scale,
-            out=None, lse=None, idx_out=None, G_max=None, stream=None):
+            out=None, lse=None, idx_out=None, G_max=None, flags=0, stream=None):
     """Chunked prefill of T query tokens per sequence (the last T of each cache)."""
     _bf16(q_idx, "q_idx", 4)
     _bf16(q, "q", 4)
@@ -353,6 +354,7 @@ def prefill(q_idx, w_head, k_pooled, k_idx, pool_w, q, K, V, seq_len, P, k, scal
     a.H_q, a.d_qk, a.d_v, a.scale = H_q, d_qk, d_v, float(scale)
     a.out, a.lse = out.data_ptr(), lse.data_ptr()
     a.idx_out = idx_out.data_ptr() if idx_out is not None else None
+    a.flags = int(flags)
     nbytes = lib().lcsw_prefill_workspace_size(ctypes.byref(a))
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
     _check(lib().lcsw_prefill(ctypes.byref(a), ctypes.c_void_p(ws.data_ptr()), nbytes,

@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(kThr, 2)
 // query block loaded / released.  Group tiles past a sequence's length are
 // written as -inf without a load or an MMA.
 constexpr int kPThr = 576;                    // 16 folding warps + producer + MMA warp
+constexpr int kSampleTiles = 16;              // group tiles of the prefill threshold sample
 constexpr int kPFold = 16;
 constexpr int kPSlots = 2;                    // group-tile ring
 constexpr int kPBufs = 4;                     // TMEM product buffers (4 x 128 columns)
@@ -178,17 +179,40 @@ constexpr int kPQ = 8 * kTile;                // query tiles of one block
 constexpr int kPStage = kPFold * 32 * 128;    // per folding warp: 32 rows x 32 floats
 constexpr int kPSmem = kPQ + kPSlots * kTile + kPStage + 1024;
 
+}  // namespace
+
+// One pass of the persistent kernel over (batch, query block, pass tile) units;
+// pass tile j is group tile j * gt_stride.  Dense mode writes the scores of
+// pass tile j to columns [128 j, 128 j + 128) of out rows of pitch ldo (-inf
+// where not visible, columns >= ldo dropped).  Candidate mode keeps, per query
+// row, the visible groups whose score key is at or above thr[row], appending
+// (key | group << 32) to the row's list of cap entries (count in ccount[row],
+// which may exceed cap: the caller treats that row as overflowed).
+struct ScorePass {
+    int gt_count, gt_stride;
+    float *out;
+    int64_t ldo;
+    const uint32_t *thr;
+    unsigned *ccount;
+    unsigned long long *cand;
+    int cap;
+    const int *run_if;  // non-null: the pass runs only when *run_if != 0
+};
+
+namespace {
+
 struct PBars {  // mbarrier indices
     static constexpr int qfull = 0, qfree = 1, kfull = 2, kfree = kfull + kPSlots,
                          dfull = kfree + kPSlots, dfree = dfull + kPBufs, n = dfree + kPBufs;
 };
 
+template <bool kCands>
 __global__ void __launch_bounds__(kPThr, 1)
     scores_tc_persist_kernel(const __grid_constant__ CUtensorMap tq,
                              const __grid_constant__ CUtensorMap tk,
                              const float *__restrict__ w_head, const int32_t *__restrict__ seq_len,
                              const int32_t *__restrict__ q_pos, int B, int T, int H_i, int P,
-                             int G_max, float *__restrict__ scores, int *status) {
+                             int G_max, const ScorePass ps, int *status) {
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char *sq = sm, *sk = sm + kPQ;
     float *stage_all = reinterpret_cast<float *>(sm + kPQ + kPSlots * kTile);
@@ -196,7 +220,8 @@ __global__ void __launch_bounds__(kPThr, 1)
     uint32_t *slot = reinterpret_cast<uint32_t *>(bars + PBars::n);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(slot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nqb = (T + kTM - 1) / kTM, ngt = (G_max + kTN - 1) / kTN;
+    if (ps.run_if && *reinterpret_cast<const volatile int *>(ps.run_if) == 0) return;
+    const int nqb = (T + kTM - 1) / kTM, ngt = ps.gt_count;
     const long long n_units = (long long)B * nqb * ngt;
     const long long u0 = n_units * blockIdx.x / gridDim.x;
     const long long u1 = n_units * (blockIdx.x + 1) / gridDim.x;
@@ -261,11 +286,12 @@ __global__ void __launch_bounds__(kPThr, 1)
                     prev = b * nqb + qb;
                     ++nq;
                 }
-                if (gt * kTN >= w.Gb) continue;
+                const int gr = gt * ps.gt_stride;  // the group tile itself
+                if (gr * kTN >= w.Gb) continue;
                 const int s = kq % kPSlots;
                 if (kq >= kPSlots && !wait(PBars::kfree + s, ((kq / kPSlots) - 1) & 1)) break;
                 mbar_expect_tx(bars + PBars::kfull + s, kTile);
-                tma_load_3d(sk + s * kTile, &tk, bars + PBars::kfull + s, 0, gt * kTN, b);
+                tma_load_3d(sk + s * kTile, &tk, bars + PBars::kfull + s, 0, gr * kTN, b);
                 ++kq;
             }
         }
@@ -282,7 +308,7 @@ __global__ void __launch_bounds__(kPThr, 1)
                     prev = b * nqb + qb;
                     ++nq;
                 }
-                if (gt * kTN >= w.Gb) continue;
+                if (gt * ps.gt_stride * kTN >= w.Gb) continue;
                 const int s = kq % kPSlots;
                 if (!wait(PBars::kfull + s, (kq / kPSlots) & 1)) break;
                 tc_fence_after();
@@ -312,6 +338,7 @@ __global__ void __launch_bounds__(kPThr, 1)
         const int row = (warp & 3) * 32 + lane, c0 = (warp >> 2) * 32;
         const uint32_t lane_addr = tb + (uint32_t((warp & 3) * 32) << 16) + c0;
         int nd = 0, prev = -1, nvis = 0, t = 0;
+        float thr = __int_as_float(0x7FFFFFFF);  // threshold as a score (NaN: keep nothing)
         float wv[8];
         Walk w = start();
         for (long long u = u0; u < u1 && !*abort_flag; ++u, next(w)) {
@@ -327,12 +354,19 @@ __global__ void __launch_bounds__(kPThr, 1)
 #pragma unroll
                 for (int h = 0; h < 8; ++h)
                     wv[h] = (h < H_i && t < T) ? __ldg(w_head + (int64_t(b) * T + t) * H_i + h) : 0.f;
+                if (kCands) {
+                    // key >= thr key  <=>  score >= the score of that key (finite scores)
+                    const uint32_t tk = t < T ? __ldg(ps.thr + int64_t(b) * T + t) : 0xFFFFFFFFu;
+                    thr = tk == 0u ? -INFINITY
+                                   : __uint_as_float((tk & 0x80000000u) ? (tk & 0x7FFFFFFFu) : ~tk);
+                }
             }
-            const int g0 = gt * kTN + c0;
+            const int gr = gt * ps.gt_stride;
+            const int g0 = gr * kTN + c0;  // first group of this thread's 32 columns
             float acc[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-            if (gt * kTN < Gb) {
+            if (gr * kTN < Gb) {
                 bool good = true;
 #pragma unroll 1
                 for (int h = 0; h < H_i; ++h, ++nd) {
@@ -361,6 +395,38 @@ __global__ void __launch_bounds__(kPThr, 1)
                 }
                 if (!good) break;
             }
+            if (kCands) {
+                // visible groups at or above the row's threshold join its list
+                if (t < T && gr * kTN < Gb) {
+                    unsigned keep = 0u;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) keep |= unsigned(acc[e] >= thr) << e;
+                    if (g0 + 32 > nvis)  // past the visible groups
+                        keep &= nvis > g0 ? (1u << (nvis - g0)) - 1u : 0u;
+                    if (keep) {
+                        // the row's values go to the warp's staging block (row =
+                        // lane, chunks swizzled as for the dense store) so that a
+                        // kept column is one shared load, not a register select
+                        float *stg = stage_all + warp * 32 * 32 + lane * 32;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(stg + (((j >> 2) ^ (lane & 7)) << 2)) =
+                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                        const int64_t rrow = int64_t(b) * T + t;
+                        unsigned pos = atomicAdd(ps.ccount + rrow, unsigned(__popc(keep)));
+                        unsigned long long *dst = ps.cand + rrow * ps.cap;
+                        while (keep) {
+                            const int e = __ffs(keep) - 1;
+                            keep &= keep - 1u;
+                            const float v = stg[(((e >> 2) ^ (lane & 7)) << 2) + (e & 3)] + 0.0f;
+                            if (pos < unsigned(ps.cap))
+                                dst[pos] = score_key(v) | ((unsigned long long)(g0 + e) << 32);
+                            ++pos;
+                        }
+                    }
+                }
+                continue;
+            }
             // masked row values -> the warp's staging block (row = lane, 16-byte
             // chunks XOR-swizzled by row) -> eight lanes per 128-byte row segment
             float *stg = stage_all + warp * 32 * 32;
@@ -376,21 +442,22 @@ __global__ void __launch_bounds__(kPThr, 1)
             }
             __syncwarp();
             {
-                const int ch = lane & 7, g = g0 + ch * 4;
+                const int ch = lane & 7;
+                const int64_t oc = int64_t(gt) * kTN + c0 + ch * 4;  // output column
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
                     const int r = (lane >> 3) + 4 * m, tr = qb * kTM + (warp & 3) * 32 + r;
-                    if (tr < T && g < G_max) {
+                    if (tr < T && oc < ps.ldo) {
                         const float4 v = *reinterpret_cast<const float4 *>(
                             stg + r * 32 + ((ch ^ (r & 7)) << 2));
-                        float *dst = scores + (int64_t(b) * T + tr) * G_max + g;
-                        if ((G_max & 3) == 0) {
+                        float *dst = ps.out + (int64_t(b) * T + tr) * ps.ldo + oc;
+                        if ((ps.ldo & 3) == 0) {
                             __stcs(reinterpret_cast<float4 *>(dst), v);
                         } else {
                             const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                if (g + e < G_max) __stcs(dst + e, vv[e]);
+                                if (oc + e < ps.ldo) __stcs(dst + e, vv[e]);
                         }
                     }
                 }
@@ -427,42 +494,67 @@ bool index_scores_tc_supported(int B, int T, int H_i, int G_max, int64_t sp_b) {
            encode_fn() != nullptr;
 }
 
-cudaError_t launch_index_scores_tc(const uint16_t *q_idx, const float *w_head,
-                                   const uint16_t *k_pooled, int64_t sp_b,
-                                   const int32_t *seq_len, const int32_t *q_pos, int B, int T,
-                                   int H_i, int P, int G_max, float *scores, int *status,
-                                   cudaStream_t st) {
-    if (!index_scores_tc_supported(B, T, H_i, G_max, sp_b)) return cudaErrorNotSupported;
+namespace {
+
+// Tensor maps of the queries ([B*T][H_i][64]: one box = 128 queries of one
+// head) and of the pooled keys ([B][G_max][64] with the batch stride: one box
+// = 128 groups), both 128-byte swizzled.
+bool make_maps(const uint16_t *q_idx, const uint16_t *k_pooled, int64_t sp_b, int B, int T,
+               int H_i, int G_max, CUtensorMap *tq, CUtensorMap *tk) {
     auto enc = encode_fn();
-    CUtensorMap tq, tk;
-    // queries viewed as [B*T][H_i][64]: one box = 128 queries of one head
     const cuuint64_t qdim[3] = {64, cuuint64_t(H_i), cuuint64_t(B) * T};
     const cuuint64_t qstr[2] = {128, cuuint64_t(H_i) * 128};
     const cuuint32_t qbox[3] = {64, 1, kTM};
-    // pooled keys viewed as [B][G_max][64] with the batch stride: one box = 128 groups
     const cuuint64_t kdim[3] = {64, cuuint64_t(G_max), cuuint64_t(B)};
     const cuuint64_t kstr[2] = {128, cuuint64_t(sp_b) * 2};
     const cuuint32_t kbox[3] = {64, kTN, 1};
     const cuuint32_t ones[3] = {1, 1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(q_idx), qdim, qstr,
-            qbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(k_pooled), kdim,
-            kstr, kbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    return enc(tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(q_idx), qdim, qstr,
+               qbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+               CUDA_SUCCESS &&
+           enc(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(k_pooled), kdim,
+               kstr, kbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+               CUDA_SUCCESS;
+}
+
+template <bool kCands>
+cudaError_t launch_persist(const CUtensorMap &tq, const CUtensorMap &tk, const float *w_head,
+                           const int32_t *seq_len, const int32_t *q_pos, int B, int T, int H_i,
+                           int P, int G_max, const ScorePass &ps, int *status, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(scores_tc_persist_kernel<kCands>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    scores_tc_persist_kernel<kCands><<<sms, kPThr, kPSmem, st>>>(tq, tk, w_head, seq_len, q_pos, B,
+                                                                 T, H_i, P, G_max, ps, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_index_scores_tc(const uint16_t *q_idx, const float *w_head,
+                                   const uint16_t *k_pooled, int64_t sp_b,
+                                   const int32_t *seq_len, const int32_t *q_pos, int B, int T,
+                                   int H_i, int P, int G_max, float *scores, int *status,
+                                   cudaStream_t st, const int *run_if) {
+    if (!index_scores_tc_supported(B, T, H_i, G_max, sp_b)) return cudaErrorNotSupported;
+    CUtensorMap tq, tk;
+    if (!make_maps(q_idx, k_pooled, sp_b, B, T, H_i, G_max, &tq, &tk)) return cudaErrorInvalidValue;
     if (H_i <= 8) {
-        cudaError_t e = cudaFuncSetAttribute(scores_tc_persist_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
-        if (e != cudaSuccess) return e;
-        int dev = 0, sms = 148;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        scores_tc_persist_kernel<<<sms, kPThr, kPSmem, st>>>(tq, tk, w_head, seq_len, q_pos, B, T,
-                                                             H_i, P, G_max, scores, status);
-        return cudaGetLastError();
+        ScorePass ps = {};
+        ps.gt_count = (G_max + kTN - 1) / kTN;
+        ps.gt_stride = 1;
+        ps.out = scores;
+        ps.ldo = G_max;
+        ps.run_if = run_if;
+        return launch_persist<false>(tq, tk, w_head, seq_len, q_pos, B, T, H_i, P, G_max, ps,
+                                     status, st);
     }
+    if (run_if) return cudaErrorNotSupported;  // the per-tile kernel has no gated form
     cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
@@ -470,6 +562,46 @@ cudaError_t launch_index_scores_tc(const uint16_t *q_idx, const float *w_head,
     scores_tc_kernel<<<grid, kThr, kSmem, st>>>(tq, tk, w_head, seq_len, q_pos, T, H_i, P, G_max,
                                                  scores, status);
     return cudaGetLastError();
+}
+
+int prefill_sample_tiles(int G_max) { return min((G_max + kTN - 1) / kTN, kSampleTiles); }
+
+cudaError_t launch_prefill_sample_scores(const uint16_t *q_idx, const float *w_head,
+                                         const uint16_t *k_pooled, int64_t sp_b,
+                                         const int32_t *seq_len, const int32_t *q_pos, int B,
+                                         int T, int H_i, int P, int G_max, float *samp,
+                                         int *status, cudaStream_t st) {
+    if (H_i > 8 || !index_scores_tc_supported(B, T, H_i, G_max, sp_b)) return cudaErrorNotSupported;
+    CUtensorMap tq, tk;
+    if (!make_maps(q_idx, k_pooled, sp_b, B, T, H_i, G_max, &tq, &tk)) return cudaErrorInvalidValue;
+    const int ngt = (G_max + kTN - 1) / kTN, n_st = prefill_sample_tiles(G_max);
+    ScorePass ps = {};
+    ps.gt_count = n_st;
+    ps.gt_stride = ngt / n_st;  // spread over the whole sequence
+    ps.out = samp;
+    ps.ldo = int64_t(n_st) * kTN;
+    return launch_persist<false>(tq, tk, w_head, seq_len, q_pos, B, T, H_i, P, G_max, ps, status,
+                                 st);
+}
+
+cudaError_t launch_prefill_candidates(const uint16_t *q_idx, const float *w_head,
+                                      const uint16_t *k_pooled, int64_t sp_b,
+                                      const int32_t *seq_len, const int32_t *q_pos, int B, int T,
+                                      int H_i, int P, int G_max, const uint32_t *thr,
+                                      unsigned *ccount, unsigned long long *cand, int cap,
+                                      int *status, cudaStream_t st) {
+    if (H_i > 8 || !index_scores_tc_supported(B, T, H_i, G_max, sp_b)) return cudaErrorNotSupported;
+    CUtensorMap tq, tk;
+    if (!make_maps(q_idx, k_pooled, sp_b, B, T, H_i, G_max, &tq, &tk)) return cudaErrorInvalidValue;
+    ScorePass ps = {};
+    ps.gt_count = (G_max + kTN - 1) / kTN;
+    ps.gt_stride = 1;
+    ps.thr = thr;
+    ps.ccount = ccount;
+    ps.cand = cand;
+    ps.cap = cap;
+    return launch_persist<true>(tq, tk, w_head, seq_len, q_pos, B, T, H_i, P, G_max, ps, status,
+                                st);
 }
 
 }  // namespace lcsw

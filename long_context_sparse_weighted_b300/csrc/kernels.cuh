@@ -28,13 +28,42 @@ cudaError_t launch_index_scores_mma(const uint16_t *q_idx, const float *w_head,
                                     int H_i, int P, int G_max, float *scores, cudaStream_t st);
 
 // Indexer scores as a tcgen05/TMEM GEMM fed by TMA (chunked prefill).
-// Returns cudaErrorNotSupported when the shape is outside its envelope.
+// Returns cudaErrorNotSupported when the shape is outside its envelope.  With
+// run_if (H_i <= 8 only) the launch does nothing unless *run_if != 0.
 cudaError_t launch_index_scores_tc(const uint16_t *q_idx, const float *w_head,
                                    const uint16_t *k_pooled, int64_t sp_b,
                                    const int32_t *seq_len, const int32_t *q_pos, int B, int T,
                                    int H_i, int P, int G_max, float *scores, int *status,
-                                   cudaStream_t st);
+                                   cudaStream_t st, const int *run_if = nullptr);
 bool index_scores_tc_supported(int B, int T, int H_i, int G_max, int64_t sp_b);
+
+// Fused prefill selection (H_i <= 8).  Sample: dense scores of
+// prefill_sample_tiles(G_max) group tiles spread over the sequence, into
+// samp [B*T][128 * tiles].  Candidates: every visible group whose score key is
+// at or above thr[row], appended as (key | group << 32) to cand [B*T][cap],
+// counted in ccount[row] (zeroed by the caller; may exceed cap).
+int prefill_sample_tiles(int G_max);
+cudaError_t launch_prefill_sample_scores(const uint16_t *q_idx, const float *w_head,
+                                         const uint16_t *k_pooled, int64_t sp_b,
+                                         const int32_t *seq_len, const int32_t *q_pos, int B,
+                                         int T, int H_i, int P, int G_max, float *samp,
+                                         int *status, cudaStream_t st);
+cudaError_t launch_prefill_candidates(const uint16_t *q_idx, const float *w_head,
+                                      const uint16_t *k_pooled, int64_t sp_b,
+                                      const int32_t *seq_len, const int32_t *q_pos, int B, int T,
+                                      int H_i, int P, int G_max, const uint32_t *thr,
+                                      unsigned *ccount, unsigned long long *cand, int cap,
+                                      int *status, cudaStream_t st);
+// Per row: the threshold key of the candidate pass from the sample, then the
+// exact top k from the candidates (ascending groups, -1 padded).  A row whose
+// candidates cannot be proven to hold its top k gets fail[row] = 1 and
+// *any_fail = 1 (fail and any_fail zeroed by the caller).
+cudaError_t launch_prefill_thresholds(const float *samp, int n_samp, const int32_t *n_valid,
+                                      int64_t rows, int k, uint32_t *thr, bool force_fallback,
+                                      cudaStream_t st);
+cudaError_t launch_prefill_select(const unsigned long long *cand, const unsigned *ccount, int cap,
+                                  const int32_t *n_valid, int64_t rows, int G_max, int k,
+                                  int32_t *idx, int *fail, int *any_fail, cudaStream_t st);
 
 cudaError_t launch_visible_counts(const int32_t *seq_len, const int32_t *q_pos, int B, int T,
                                   int P, int32_t *n_valid, cudaStream_t st);
@@ -43,7 +72,8 @@ cudaError_t launch_visible_counts(const int32_t *seq_len, const int32_t *q_pos, 
 // row r = b*T + t has seq_len[b]/P valid groups (seq_len/P/T must be given).
 cudaError_t launch_topk_rows(const float *scores, const int32_t *n_valid,
                              const int32_t *seq_len, int P, int T, int64_t rows, int G_max,
-                             int k, int32_t *idx, cudaStream_t st);
+                             int k, int32_t *idx, cudaStream_t st,
+                             const int32_t *row_mask = nullptr);
 
 // Split-K sparse attention + combine.
 int sparse_attn_splits(int64_t rows, int H_q, int k, int P);

@@ -321,13 +321,28 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
 
 struct PrefillWs {
     int *status;
-    float *scores;
+    float *scores;  // dense scores: the fallback (and the path without fusion)
     int32_t *idx;
     int32_t *q_pos;
     int32_t *n_valid;
     void *attn;
+    // fused selection
+    bool fused;
+    int cap;
+    float *samp;
+    uint32_t *thr;
+    unsigned *ccount;
+    int32_t *fail;  // [rows], then any_fail
+    unsigned long long *cand;
     size_t total;
 };
+
+constexpr int kFusedMaxG = 524288;  // bitmap of the per-row selection in shared memory
+
+static bool prefill_fused(const lcsw_prefill_args *a) {
+    return a->H_i <= 8 && a->G_max <= kFusedMaxG &&
+           lcsw::index_scores_tc_supported(a->B, a->T, a->H_i, a->G_max, a->sp_b);
+}
 
 static PrefillWs carve_prefill(const lcsw_prefill_args *a, void *ws) {
     Carver c(ws);
@@ -339,6 +354,23 @@ static PrefillWs carve_prefill(const lcsw_prefill_args *a, void *ws) {
     w.q_pos = static_cast<int32_t *>(c.take(rows * sizeof(int32_t)));
     w.n_valid = static_cast<int32_t *>(c.take(rows * sizeof(int32_t)));
     w.attn = c.take(lcsw::sparse_attn_ws_bytes(int64_t(rows), a->H_q, a->d_v, a->k, a->P));
+    w.fused = prefill_fused(a);
+    w.cap = 0;
+    w.samp = nullptr;
+    w.thr = nullptr;
+    w.ccount = nullptr;
+    w.fail = nullptr;
+    w.cand = nullptr;
+    if (w.fused) {
+        // about 3 k candidates per row are expected; room for 8 k (at least 4096)
+        w.cap = a->k * 8 > 4096 ? a->k * 8 : 4096;
+        const int n_samp = 128 * lcsw::prefill_sample_tiles(a->G_max);
+        w.samp = static_cast<float *>(c.take(rows * n_samp * sizeof(float)));
+        w.thr = static_cast<uint32_t *>(c.take(rows * sizeof(uint32_t)));
+        w.ccount = static_cast<unsigned *>(c.take(rows * sizeof(unsigned)));
+        w.fail = static_cast<int32_t *>(c.take((rows + 1) * sizeof(int32_t)));
+        w.cand = static_cast<unsigned long long *>(c.take(rows * w.cap * sizeof(unsigned long long)));
+    }
     w.total = c.off;
     return w;
 }
@@ -386,22 +418,52 @@ lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
     if (e != cudaSuccess) return cuda_status(e, "prefill pool");
     e = lcsw::launch_prefill_positions(a->seq_len, a->B, a->T, w.q_pos, st);
     if (e != cudaSuccess) return cuda_status(e, "prefill positions");
-    if (lcsw::index_scores_tc_supported(a->B, a->T, a->H_i, a->G_max, a->sp_b)) {
-        e = lcsw::launch_index_scores_tc(a->q_idx, a->w_head, a->k_pooled, a->sp_b, a->seq_len,
-                                         w.q_pos, a->B, a->T, a->H_i, a->P, a->G_max, w.scores,
-                                         w.status, st);
-    } else {
-        CHECK(int64_t(a->B) * ((a->T + 3) / 4) <= 65535, "B * ceil(T/4) must be <= 65535");
-        e = lcsw::launch_index_scores_mma(a->q_idx, a->w_head, a->k_pooled, a->sp_b, a->seq_len,
-                                          w.q_pos, a->B, a->T, a->H_i, a->P, a->G_max, w.scores,
-                                          st);
-    }
-    if (e != cudaSuccess) return cuda_status(e, "prefill scores");
     e = lcsw::launch_visible_counts(a->seq_len, w.q_pos, a->B, a->T, a->P, w.n_valid, st);
     if (e != cudaSuccess) return cuda_status(e, "prefill visible counts");
-    e = lcsw::launch_topk_rows(w.scores, w.n_valid, nullptr, a->P, a->T, rows, a->G_max, a->k,
-                               idx, st);
-    if (e != cudaSuccess) return cuda_status(e, "prefill top-k");
+    if (w.fused) {
+        // sample -> per-row thresholds -> candidates -> exact top k; rows that
+        // cannot be proven complete take dense scores and the radix top-k
+        const int n_samp = 128 * lcsw::prefill_sample_tiles(a->G_max);
+        e = cudaMemsetAsync(w.ccount, 0, rows * sizeof(unsigned), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(w.fail, 0, (rows + 1) * sizeof(int32_t), st);
+        if (e != cudaSuccess) return cuda_status(e, "prefill clear");
+        e = lcsw::launch_prefill_sample_scores(a->q_idx, a->w_head, a->k_pooled, a->sp_b,
+                                               a->seq_len, w.q_pos, a->B, a->T, a->H_i, a->P,
+                                               a->G_max, w.samp, w.status, st);
+        if (e != cudaSuccess) return cuda_status(e, "prefill sample scores");
+        e = lcsw::launch_prefill_thresholds(w.samp, n_samp, w.n_valid, rows, a->k, w.thr,
+                                            (a->flags & LCSW_PREFILL_FORCE_FALLBACK) != 0, st);
+        if (e != cudaSuccess) return cuda_status(e, "prefill thresholds");
+        e = lcsw::launch_prefill_candidates(a->q_idx, a->w_head, a->k_pooled, a->sp_b, a->seq_len,
+                                            w.q_pos, a->B, a->T, a->H_i, a->P, a->G_max, w.thr,
+                                            w.ccount, w.cand, w.cap, w.status, st);
+        if (e != cudaSuccess) return cuda_status(e, "prefill candidates");
+        e = lcsw::launch_prefill_select(w.cand, w.ccount, w.cap, w.n_valid, rows, a->G_max, a->k,
+                                        idx, w.fail, w.fail + rows, st);
+        if (e != cudaSuccess) return cuda_status(e, "prefill select");
+        e = lcsw::launch_index_scores_tc(a->q_idx, a->w_head, a->k_pooled, a->sp_b, a->seq_len,
+                                         w.q_pos, a->B, a->T, a->H_i, a->P, a->G_max, w.scores,
+                                         w.status, st, w.fail + rows);
+        if (e != cudaSuccess) return cuda_status(e, "prefill fallback scores");
+        e = lcsw::launch_topk_rows(w.scores, w.n_valid, nullptr, a->P, a->T, rows, a->G_max,
+                                   a->k, idx, st, w.fail);
+        if (e != cudaSuccess) return cuda_status(e, "prefill fallback top-k");
+    } else {
+        if (lcsw::index_scores_tc_supported(a->B, a->T, a->H_i, a->G_max, a->sp_b)) {
+            e = lcsw::launch_index_scores_tc(a->q_idx, a->w_head, a->k_pooled, a->sp_b,
+                                             a->seq_len, w.q_pos, a->B, a->T, a->H_i, a->P,
+                                             a->G_max, w.scores, w.status, st);
+        } else {
+            CHECK(int64_t(a->B) * ((a->T + 3) / 4) <= 65535, "B * ceil(T/4) must be <= 65535");
+            e = lcsw::launch_index_scores_mma(a->q_idx, a->w_head, a->k_pooled, a->sp_b,
+                                              a->seq_len, w.q_pos, a->B, a->T, a->H_i, a->P,
+                                              a->G_max, w.scores, st);
+        }
+        if (e != cudaSuccess) return cuda_status(e, "prefill scores");
+        e = lcsw::launch_topk_rows(w.scores, w.n_valid, nullptr, a->P, a->T, rows, a->G_max,
+                                   a->k, idx, st);
+        if (e != cudaSuccess) return cuda_status(e, "prefill top-k");
+    }
     e = lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B, a->T,
                                  a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale, a->out, a->lse,
                                  w.attn, st);

@@ -25,7 +25,8 @@ constexpr int kBins = 2048;
 __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(
     const float *__restrict__ scores, const int32_t *__restrict__ n_valid,
     const int32_t *__restrict__ seq_len, int P, int T, int G_max, int k,
-    int32_t *__restrict__ idx) {
+    int32_t *__restrict__ idx, const int32_t *__restrict__ row_mask) {
+    if (row_mask && row_mask[blockIdx.x] == 0) return;  // row already selected elsewhere
     __shared__ unsigned hist[kBins];
     __shared__ int scratch[33];
     __shared__ int res[2];
@@ -116,11 +117,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(
 
 cudaError_t launch_topk_rows(const float *scores, const int32_t *n_valid,
                              const int32_t *seq_len, int P, int T, int64_t rows, int G_max,
-                             int k, int32_t *idx, cudaStream_t st) {
+                             int k, int32_t *idx, cudaStream_t st, const int32_t *row_mask) {
     if (rows == 0) return cudaSuccess;
     if (rows > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
     topk_rows_kernel<<<unsigned(rows), kTopkThreads, 0, st>>>(scores, n_valid, seq_len, P, T,
-                                                              G_max, k, idx);
+                                                              G_max, k, idx, row_mask);
     return cudaGetLastError();
 }
 

@@ -153,13 +153,13 @@ def test_decode_repeated_calls_reuse_workspace():
 
 # ----------------------------------------------------------------- prefill --
 
-def run_prefill(c, kp_cached):
+def run_prefill(c, kp_cached, flags=0):
     d = upload_case(c)
     B, T, k = c["B"], c["T"], c["k"]
     kp = dev_bf16(kp_cached).clone()
     idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
     out, lse = lcsw.prefill(d["q_idx"], d["w_head"], kp, d["k_idx"], d["pool_w"], d["q"], d["K"],
-                            d["V"], d["seq_len"], c["P"], k, c["scale"], idx_out=idx)
+                            d["V"], d["seq_len"], c["P"], k, c["scale"], idx_out=idx, flags=flags)
     return dict(out=host_bits(out), lse=lse.cpu().numpy(), idx=idx.cpu().numpy(),
                 k_pooled=host_bits(kp))
 
@@ -185,3 +185,35 @@ def test_prefill_reduced(lengths, T, k):
     assert nd == 0, f"{nd} rows differ by near-ties"
     assert_attn_close(got["out"], ref["out"])
     assert_lse_close(got["lse"], ref["lse"])
+
+
+# T >= 64 with 8 indexer heads: the selection is fused with the tensor-core
+# scoring (sample thresholds, candidates, exact top k from the candidates).
+# The ragged case has a sequence shorter than k groups (every visible group
+# selected) and group tiles past its end; the forced case sends every query
+# through the dense-scores fallback.
+@pytest.mark.parametrize("lengths,T,k,flags", [
+    ([16384 + 256, 856], 256, 512, 0),
+    ([16384 + 256], 256, 512, lcsw.PREFILL_FORCE_FALLBACK),
+])
+def test_prefill_fused_selection(lengths, T, k, flags):
+    spec = synth.Spec(B=len(lengths), lengths=lengths, T=T, prefill=True, H_i=8, k=k, H_q=32,
+                      seed=230 + len(lengths) + flags)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_prefill(c, _cached_part(ref["k_pooled"], c), flags=flags)
+    nd = selection_diff(got["idx"], ref["idx"], ref["scores"])
+    assert nd == 0, f"{nd} rows differ by near-ties"
+    assert_attn_close(got["out"], ref["out"])
+    assert_lse_close(got["lse"], ref["lse"])
+
+
+def test_prefill_fused_selection_exact_ties():
+    # integer keys and queries with dyadic weights: exact scores with many equal
+    # values, so the tie rule (lowest group first) decides many selections
+    spec = synth.Spec(B=1, lengths=[8192 + 128], T=128, prefill=True, H_i=4, k=64, H_q=16,
+                      idx_values="int3", w_mode="quarter_half", pool_mode="dyadic", seed=240)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_prefill(c, _cached_part(ref["k_pooled"], c))
+    assert np.array_equal(got["idx"], ref["idx"])
