@@ -53,10 +53,11 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--copies", type=int, default=0,
                     help="rotated input copies (0: enough to exceed 3x L2)")
-    ap.add_argument("--kernel", default=None, choices=["prefill_scores"],
+    ap.add_argument("--kernel", default=None, choices=["prefill_scores", "prefill"],
                     help="time one kernel of the path instead of the decode step (not the "
                          "headline line): prefill_scores = the chunked-prefill indexer "
-                         "scores (tcgen05 GEMM) on the prefill_4k shapes")
+                         "scores (tcgen05 GEMM) on the prefill_4k shapes; prefill = one whole "
+                         "lcsw_prefill chunk of prefill_4k (pool, fused selection, attention)")
     return ap.parse_args()
 
 
@@ -617,10 +618,56 @@ def run_prefill_scores(args):
         "bound_ms": round(max(flops / tf_peak / 1e9, bytes_ / hbm_peak / 1e6), 5)}))
 
 
+def run_prefill_chunk(args):
+    """One chunked-prefill call on prefill_4k: pool the chunk's new groups,
+    score every visible group, select the top k per query (fused with the
+    scoring) and run the sparse attention, on resident device inputs."""
+    import torch
+
+    import long_context_sparse_weighted_b300 as lcsw
+    spec = synth.named("prefill_4k")
+    c = synth.generate(spec)
+    P, B, T, k = spec.P, spec.B, spec.T, spec.k
+    G_max = spec.L_max // P
+    up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(
+        torch.bfloat16)
+    seq = torch.from_numpy(c["seq_len"]).cuda()
+    k_idx, pool_w = up16(c["k_idx"]), torch.from_numpy(c["pool_w"]).cuda()
+    kp = torch.zeros(B, G_max, 64, dtype=torch.bfloat16, device="cuda")
+    lcsw.pool_keys(k_idx, pool_w, seq, P, kp)
+    g0 = (int(c["seq_len"][0]) - T) // P
+    kp[:, g0:] = 0  # the cache as it stood before the chunk: the call pools the chunk
+    qi, w = up16(c["q_idx"]), torch.from_numpy(c["w_head"]).cuda()
+    q, K, V = up16(c["q"]), up16(c["K"]), up16(c["V"])
+    idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
+    run = lambda: lcsw.prefill(qi, w, kp, k_idx, pool_w, q, K, V, seq, P, k, c["scale"],
+                               idx_out=idx)
+    for _ in range(max(3, args.warmup)):
+        run()
+    torch.cuda.synchronize()
+    steps = min(args.steps, 50)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    print(json.dumps({
+        "kernel": "lcsw_prefill (pool, fused top-k selection, sparse attention)",
+        "workload": "prefill_4k", "shape": {"B": B, "T": T, "G_max": G_max, "k": k,
+                                            "H_i": spec.H_i, "H_q": spec.H_q},
+        "ms_per_chunk": round(ms, 4), "queries_per_s": round(B * T / (ms / 1e3), 1),
+        "steps": steps}))
+
+
 def main():
     args = parse()
     if args.kernel == "prefill_scores":
         run_prefill_scores(args)
+        return
+    if args.kernel == "prefill":
+        run_prefill_chunk(args)
         return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

@@ -81,6 +81,11 @@ constexpr int kSlowB = 1, kSlowC = 2, kSlowD = 3, kNumCounters = 4;
 constexpr int kStream = kWarps;    // streaming warps
 constexpr int kSampW = 4;          // sample bins each warp publishes (one 64-bit word)
 constexpr int kSampleN = 2 * kStream * 16;  // sample: the first groups of each block's chunk
+// Phase 1 streams the block's pooled keys through per-warp rings in shared
+// memory filled by bulk copies: warp w scores tiles w, w + 16, w + 32, ... of
+// the block's chunk (16 groups, 2 KB each) and keeps kRing of them in flight.
+constexpr int kRing = 4;
+constexpr int kTileBytes = 16 * 128;
 
 // shared memory map (bytes); region U is reused phase by phase
 constexpr int kU = 0;
@@ -112,6 +117,17 @@ template <int DQK> constexpr int q_tile_bytes() { return (DQK / 64) * 8192; }
 template <int DQK, int DV> constexpr int kv_tile_bytes() { return (DQK / 64 + DV / 64) * 8192; }
 constexpr int kPT = kScores;
 static_assert(kTie + kTieCap * 8 <= kSelG, "shared-memory map overlap");
+constexpr int kRingBase = kU;  // free while the keys stream
+static_assert(kRingBase + kWarps * kRing * kTileBytes <= kU + kUBytes, "stream ring overlap");
+// While the keys stream, the Q tile's region holds the newest group's staged
+// rows ([8][64] bf16 + [8] weights), the guess histogram [2048] and the
+// rings' mbarriers [kWarps][kRing] (invalidated before the Q tile lands).
+constexpr int kNewRows = kQT;
+constexpr int kGuessHist = kQT + 2048;
+constexpr int kRingBars = kGuessHist + 2048 * 4;
+static_assert(8 * 128 + 8 * 4 <= kGuessHist - kNewRows, "staged rows overlap");
+static_assert(kRingBars + kWarps * kRing * 8 <= kQT + q_tile_bytes<64>() + 8192,
+              "stream barriers overlap");
 static_assert((192 / 64 + 128 / 64) * 8192 <= kSpecBytes, "prefetch tile overlap");
 static_assert(kGather + 2 * (192 / 64 + 128 / 64) * 8192 <= kSelG, "gather overlap");
 
@@ -510,26 +526,29 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     int *s_ok = sv + 2;
     PHASE_MARK(1);
 
-    // ---- phase-1 prologue: first tiles, indexer query, append ----------------
+    // ---- phase-1 prologue: first tiles in flight, indexer query, append -------
+    // The block's chunk of pooled keys is one contiguous range.  Lane 0 of each
+    // warp issues the warp's first kRing tiles now, so the prologue's own loads
+    // overlap them, and refills a slot as soon as the warp has read it.
     const int r = lane >> 2, c = lane & 3;
     const uint16_t *kb = p.k_pooled + int64_t(b) * p.sp_b;
     const int n_tiles = (nloc + 15) / 16;
-    auto load_tile = [&](int t, uint4 (&A)[4]) {
-        const int ga = g_lo + t * 16 + r, gb = ga + 8;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        A[0] = A[1] = A[2] = A[3] = z;
-        if (ga < g_hi) {
-            A[0] = ld_stream16(kb + int64_t(ga) * 64 + 8 * c);
-            A[1] = ld_stream16(kb + int64_t(ga) * 64 + 32 + 8 * c);
-        }
-        if (gb < g_hi) {
-            A[2] = ld_stream16(kb + int64_t(gb) * 64 + 8 * c);
-            A[3] = ld_stream16(kb + int64_t(gb) * 64 + 32 + 8 * c);
-        }
+    const int n_mine = n_tiles > warp ? (n_tiles - warp + kStream - 1) / kStream : 0;
+    unsigned char *ring = smem + kRingBase + warp * kRing * kTileBytes;
+    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + kRingBars) + warp * kRing;
+    int n_issued = 0;  // lane 0: tiles of this warp issued so far
+    auto issue_tile = [&](int kk) {  // lane 0: this warp's tile kk into slot kk % kRing
+        const int g0 = g_lo + (warp + kk * kStream) * 16;
+        const uint32_t bytes = uint32_t(min(16, g_hi - g0)) * 128u;
+        mbar_expect_tx(wbar + kk % kRing, bytes);
+        bulk_load(ring + (kk % kRing) * kTileBytes, kb + int64_t(g0) * 64, bytes, wbar + kk % kRing);
+        ++n_issued;
     };
-    uint4 c0[4], c1[4];
-    if (warp < n_tiles) load_tile(warp, c0);
-    if (warp + kStream < n_tiles) load_tile(warp + kStream, c1);
+    if (lane == 0) {
+        for (int i = 0; i < kRing; ++i) mbar_init(wbar + i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int kk = 0; kk < min(kRing, n_mine); ++kk) issue_tile(kk);
+    }
 
     uint32_t bq[NT][4][2];
     float wv[NT][2];
@@ -554,31 +573,19 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     }
 
     PHASE_MARK(23);
-    // append: the block owning the group the newest token completes pools it
+    // append: the group the newest token completes is pooled by the warp
+    // whose tile holds it, just before it scores that tile, from rows staged
+    // here (the Q tile's region is free until the candidates are known)
     int g_new = -1;
     if (p.k_idx && G_b > 0 && L_b % P == 0) g_new = G_b - 1;
-    if (g_new >= g_lo && g_new < g_hi && tid < 8) {
-        const uint16_t *src = p.k_idx + int64_t(b) * p.sk_b + int64_t(g_new) * P * 64 + tid * 8;
-        const float *wp = p.pool_w + int64_t(b) * p.sw_b + int64_t(g_new) * P;
-        uint4 o;
-#define LCSW_APPEND(PP)                                                        \
-    {                                                                          \
-        uint4 rows[PP];                                                        \
-        float a[PP];                                                           \
-        for (int jj = 0; jj < PP; ++jj) {                                      \
-            rows[jj] = ld_nc16(src + jj * 64);                                 \
-            a[jj] = __ldg(wp + jj);                                            \
-        }                                                                      \
-        o = pool_chunk<PP>(a, rows);                                           \
-    }
-        if (P == 1) LCSW_APPEND(1)
-        else if (P == 2) LCSW_APPEND(2)
-        else if (P == 4) LCSW_APPEND(4)
-        else LCSW_APPEND(8)
-#undef LCSW_APPEND
-        *reinterpret_cast<uint4 *>(newkey + tid * 8) = o;
-        *reinterpret_cast<uint4 *>(p.k_pooled + int64_t(b) * p.sp_b + int64_t(g_new) * 64 +
-                                   tid * 8) = o;
+    const int t_new = g_new >= g_lo && g_new < g_hi ? (g_new - g_lo) / 16 : -1;
+    uint16_t *krows = reinterpret_cast<uint16_t *>(smem + kNewRows);  // [P][64]
+    float *kw = reinterpret_cast<float *>(smem + kNewRows + 8 * 128);  // [P]
+    if (t_new >= 0 && warp == t_new % kStream) {
+        const uint16_t *src = p.k_idx + int64_t(b) * p.sk_b + int64_t(g_new) * P * 64;
+        for (int e = lane; e < P * 8; e += 32) cp_async16(smem_u32(krows + e * 8), src + e * 8, 16);
+        if (lane < P) cp_async4(smem_u32(kw + lane), p.pool_w + int64_t(b) * p.sw_b + int64_t(g_new) * P + lane);
+        cp_async_commit();
     }
     PHASE_MARK(24);
     // total sample size of the sequence (the chunk split is known to every
@@ -654,96 +661,130 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
         if (lane == 0) st_relaxed_u64(samp_cur + size_t(cta) * kWarps + warp, word);
     };
-    bool first = true;
-    for (int t = warp; t < n_tiles; t += 2 * kStream) {
-        uint4 n0[4], n1[4];
-        const bool m0 = t + 2 * kStream < n_tiles, m1 = t + 3 * kStream < n_tiles;
-        if (m0) load_tile(t + 2 * kStream, n0);
-        if (m1) load_tile(t + 3 * kStream, n1);
-        const unsigned s0 = score_tile(t, c0);
-        const unsigned s1 = t + kStream < n_tiles ? score_tile(t + kStream, c1) : 0u;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (m0) c0[i] = n0[i];
-            if (m1) c1[i] = n1[i];
-        }
-        if (first) {
-            publish_sample(s0, s1);
-            first = false;
-        }
-    }
-    if (first) publish_sample(0u, 0u);
-    PHASE_MARK(4);
-
     // The guess: the need-th largest published bin of the sequence, need ~
-    // 1.5 k x (sample size)/G.  Each warp loads its share of the sequence's
-    // sample words once done streaming; the block then selects in shared memory.
-    // It is only a guess: the selection checks that at least k keys cleared it.
-    // Each thread loads its share of the sequence's sample words once its warp is
-    // done streaming (polling until every entry is written), then the block
-    // counts the entries in 2048 bins below the largest one and picks the bin
-    // where the count from the top reaches need.
-    constexpr int kQ16 = (kMaxCtas * kWarps / 2 + kThreads - 1) / kThreads;
-    const int n_q = n_b * kWarps / 2;  // 16-byte chunks of entries
-    uint4 v[kQ16];
-    unsigned emax = 1;
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(samp_cur + size_t(cb0) * kWarps);
+    // 1.5 k x (sample size)/G.  It is only a guess: the selection checks that
+    // at least k keys cleared it.  Each thread loads its share of the
+    // sequence's sample words (polling until every entry is written), then the
+    // block counts the entries in 2048 bins below the largest one and picks
+    // the bin where the count from the top reaches need.  It runs
+    // once the block is done streaming.  Returns false (block-uniform) if a
+    // stage or the sample never completed.
+    auto make_guess = [&]() -> bool {
+        constexpr int kQ16 = (kMaxCtas * kWarps / 2 + kThreads - 1) / kThreads;
+        const int n_q = n_b * kWarps / 2;  // 16-byte chunks of entries
+        uint4 v[kQ16];
+        unsigned emax = 1;
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(samp_cur + size_t(cb0) * kWarps);
 #pragma unroll
-        for (int u = 0; u < kQ16; ++u)
-            if (tid + u * kThreads < n_q) v[u] = ld_relaxed_v4(src + tid + u * kThreads);
-        const long long t0 = clock64();
-        bool ok = true;
+            for (int u = 0; u < kQ16; ++u)
+                if (tid + u * kThreads < n_q) v[u] = ld_relaxed_v4(src + tid + u * kThreads);
+            const long long t0 = clock64();
+            bool ok = true;
 #pragma unroll
-        for (int u = 0; u < kQ16; ++u) {
-            const int q = tid + u * kThreads;
-            if (q >= n_q) break;
-            for (int spin = 0; ok && !all_u16_nonzero(v[u]); ++spin) {
-                if (clock64() - t0 > kSpinBudget || ((spin & 63) == 63 && aborted(p.abort_flag))) {
-                    ok = false;
-                    break;
+            for (int u = 0; u < kQ16; ++u) {
+                const int q = tid + u * kThreads;
+                if (q >= n_q) break;
+                for (int spin = 0; ok && !all_u16_nonzero(v[u]); ++spin) {
+                    if (clock64() - t0 > kSpinBudget ||
+                        ((spin & 63) == 63 && aborted(p.abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(64);
+                    v[u] = ld_relaxed_v4(src + q);
                 }
-                __nanosleep(64);
-                v[u] = ld_relaxed_v4(src + q);
-            }
-            const unsigned w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                const unsigned w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) emax = max(emax, max(w[e] & 0xFFFFu, w[e] >> 16));
+                for (int e = 0; e < 4; ++e) emax = max(emax, max(w[e] & 0xFFFFu, w[e] >> 16));
+            }
+            if (!ok) {
+                raise_timeout(p, 1);
+                sv[19] = 1;
+            }
+            emax = __reduce_max_sync(0xffffffffu, emax);
+            if (lane == 0) atomicMax(sv + 27, int(emax));
         }
-        if (!ok) {
-            raise_timeout(p, 1);
+        // warps zero it while others may still read the ring: it lies outside
+        // the ring, in the Q tile's region (free until the candidates are known)
+        unsigned *sh = reinterpret_cast<unsigned *>(smem + kGuessHist);
+        for (int i = tid; i < 2048; i += kThreads) sh[i] = 0u;
+        __syncthreads();
+        PHASE_MARK(20);
+        if (sv[19]) return false;
+        int sguess = 0;
+        const unsigned need = unsigned(
+            max(1ull, (3ull * unsigned(k_b) * unsigned(sv[26]) + 2ull * G_b - 1) / (2ull * G_b)));
+        if (k_b > 0 && n_b > 1 && need <= unsigned(n_q * 8)) {
+            const unsigned base = unsigned(max(0, sv[27] - 2047));
+#pragma unroll
+            for (int u = 0; u < kQ16; ++u) {
+                if (tid + u * kThreads >= n_q) break;
+                const unsigned w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    atomicAdd(sh + (max(w[e] & 0xFFFFu, base) - base), 1u);
+                    atomicAdd(sh + (max(w[e] >> 16, base) - base), 1u);
+                }
+            }
+            __syncthreads();
+            PHASE_MARK(21);
+            unsigned above = 0;
+            sguess = int(base) + find_digit(sh, 2048, need, &above, scratch, sv + 12);
+            PHASE_MARK(22);
+        }
+        if (tid == 0) sv[3] = sguess;
+        return true;
+    };
+    // Warp w scores its tiles in order; its sample is its first two tiles.  A
+    // tile that never lands stops the warp's work but not its barriers.
+    unsigned key0 = 0u;
+    bool stream_ok = true;
+    for (int kk = 0; kk < n_mine; ++kk) {
+        const int slot = kk % kRing, t = warp + kk * kStream;
+        if (stream_ok &&
+            !__all_sync(0xffffffffu, mbar_wait(wbar + slot, unsigned(kk / kRing) & 1u, kMbarBudget))) {
+            stream_ok = false;  // warp-uniform: score_tile shuffles across the warp
+            raise_timeout(p, 7);
             sv[19] = 1;
         }
-        emax = __reduce_max_sync(0xffffffffu, emax);
-        if (lane == 0) atomicMax(sv + 27, int(emax));
-    }
-    unsigned *sh = reinterpret_cast<unsigned *>(smem + kSelHist);
-    for (int i = tid; i < 2048; i += kThreads) sh[i] = 0u;
-    __syncthreads();
-    PHASE_MARK(20);
-    if (sv[19]) return;  // the sample never completed
-    int sguess = 0;
-    const unsigned need = unsigned(max(1ull, (3ull * unsigned(k_b) * unsigned(sv[26]) + 2ull * G_b - 1) /
-                                                 (2ull * G_b)));
-    if (k_b > 0 && n_b > 1 && need <= unsigned(n_q * 8)) {
-        const unsigned base = unsigned(max(0, sv[27] - 2047));
-#pragma unroll
-        for (int u = 0; u < kQ16; ++u) {
-            if (tid + u * kThreads >= n_q) break;
-            const unsigned w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                atomicAdd(sh + (max(w[e] & 0xFFFFu, base) - base), 1u);
-                atomicAdd(sh + (max(w[e] >> 16, base) - base), 1u);
-            }
+        if (t == t_new) {  // this warp pools the newest group before scoring its tile
+            cp_async_wait<0>();
+            __syncwarp();
+            pool_staged(P, krows, kw, lane, newkey, p.k_pooled + int64_t(b) * p.sp_b + int64_t(g_new) * 64);
+            __syncwarp();
         }
-        __syncthreads();
-        PHASE_MARK(21);
-        unsigned above = 0;
-        sguess = int(base) + find_digit(sh, 2048, need, &above, scratch, sv + 12);
-        PHASE_MARK(22);
+        unsigned key = 0u;
+        if (stream_ok) {
+            const unsigned char *tile = ring + slot * kTileBytes;
+            uint4 A[4];
+            A[0] = *reinterpret_cast<const uint4 *>(tile + r * 128 + 16 * c);
+            A[1] = *reinterpret_cast<const uint4 *>(tile + r * 128 + 64 + 16 * c);
+            A[2] = *reinterpret_cast<const uint4 *>(tile + (r + 8) * 128 + 16 * c);
+            A[3] = *reinterpret_cast<const uint4 *>(tile + (r + 8) * 128 + 64 + 16 * c);
+            key = score_tile(t, A);
+        }
+        __syncwarp();
+        if (lane == 0 && stream_ok && kk + kRing < n_mine) {
+            fence_async_smem();  // the warp's reads of the slot come before the copy
+            issue_tile(kk + kRing);
+        }
+        if (kk == 0) key0 = key;
+        if (kk == 1) publish_sample(key0, key);
     }
-    if (tid == 0) sv[3] = sguess;
+    if (n_mine < 2) publish_sample(key0, 0u);
+    if (lane == 0) {
+        if (stream_ok) {  // every copy landed: retire the barriers (the Q tile goes there)
+            for (int i = 0; i < kRing; ++i)
+                asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(wbar + i))
+                             : "memory");
+        } else {  // let the copies in flight land before the block leaves (bounded)
+            for (int kk = max(0, n_issued - kRing); kk < n_issued; ++kk)
+                mbar_wait(wbar + kk % kRing, unsigned(kk / kRing) & 1u, 100);
+        }
+    }
+    PHASE_MARK(4);
+    if (!make_guess()) return;
     if (p.scores_out && j == 0)  // -inf past the last complete group: the full row
         for (int g = G_b + tid; g < p.G_max; g += kThreads) p.scores_out[seg + g] = -INFINITY;
     __syncthreads();

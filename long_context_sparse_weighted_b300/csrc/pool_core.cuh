@@ -70,4 +70,30 @@ __device__ __forceinline__ uint4 pool_chunk(const float (&a)[P], const uint4 (&r
     return o;
 }
 
+// One pooled key from its P rows and weights staged in shared memory
+// (rows_s: [P][64] bf16, w_s: [P]): lanes 0-7 each pool 8 dims and store them
+// to `dst_s` (shared) and `dst` (global).  Out of line: it runs once per call.
+static __device__ __noinline__ void pool_staged(int P, const uint16_t *rows_s, const float *w_s, int lane,
+                                         uint16_t *dst_s, uint16_t *dst) {
+    if (lane >= 8) return;
+    uint4 o;
+#define LCSW_POOL_STAGED(PP)                                                              \
+    {                                                                                     \
+        uint4 rows[PP];                                                                   \
+        float a[PP];                                                                      \
+        for (int j = 0; j < PP; ++j) {                                                    \
+            rows[j] = *reinterpret_cast<const uint4 *>(rows_s + j * 64 + lane * 8);       \
+            a[j] = w_s[j];                                                                \
+        }                                                                                 \
+        o = pool_chunk<PP>(a, rows);                                                      \
+    }
+    if (P == 1) LCSW_POOL_STAGED(1)
+    else if (P == 2) LCSW_POOL_STAGED(2)
+    else if (P == 4) LCSW_POOL_STAGED(4)
+    else LCSW_POOL_STAGED(8)
+#undef LCSW_POOL_STAGED
+    *reinterpret_cast<uint4 *>(dst_s + lane * 8) = o;
+    *reinterpret_cast<uint4 *>(dst + lane * 8) = o;
+}
+
 }  // namespace lcsw

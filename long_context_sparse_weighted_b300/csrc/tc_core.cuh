@@ -95,6 +95,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` contiguous bytes into shared memory (TMA
+// engine); completion is counted in bytes on the mbarrier.  Both addresses
+// 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------------ TMEM -----
 // Allocation and release are warp-wide; the base address lands in *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {

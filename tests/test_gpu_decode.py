@@ -120,6 +120,21 @@ def test_decode_bounded_wait_reports_timeout():
     assert_attn_close(host_bits(out), ref["out"][:, 0])
 
 
+# The pooled keys stream through a ring of 4 shared-memory stages of 256
+# groups.  With 148 blocks, 1024 groups per block is 4 stages (the last in the
+# last slot) and 1100 groups per block plus 9 is 5 stages with a partial last
+# stage and a ragged last tile.
+@pytest.mark.parametrize("groups", [148 * 1024, 148 * 1100 + 9])
+def test_decode_stream_ring_stage_counts(groups):
+    spec = synth.Spec(B=1, lengths=[4 * groups], H_i=8, k=512, H_q=16, plant_frac=0.05,
+                      seed=208)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_decode(c, ref["k_pooled"], append=True, corrupt_last=True)
+    assert np.array_equal(got["k_pooled"], ref["k_pooled"])
+    check_against_oracle(c, got, ref)
+
+
 def test_decode_append_repools_newest_group():
     spec = synth.Spec(B=3, lengths=[4096, 1024, 2000], H_i=8, k=128, H_q=32, seed=200)
     c = synth.generate(spec)
