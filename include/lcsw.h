@@ -277,6 +277,11 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
  * decided on the device: the result is the same exact top k either way.
  * flags: LCSW_PREFILL_FORCE_FALLBACK sends every query through the fallback
  * (a test of that path).
+ *
+ * Workspace: lcsw_prefill_workspace_size(a) bytes, 256-byte aligned.  Its
+ * first 256 bytes (the status word) must be zero before the first call;
+ * lcsw_get_status clears the word, and no other region needs clearing (each
+ * is written before it is read).  Calls sharing a workspace must not overlap.
  * ------------------------------------------------------------------------- */
 #define LCSW_PREFILL_FORCE_FALLBACK 1
 typedef struct {

@@ -327,8 +327,14 @@ def decode_fused(q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale, **kw):
 
 
 def prefill(q_idx, w_head, k_pooled, k_idx, pool_w, q, K, V, seq_len, P, k, scale,
-            out=None, lse=None, idx_out=None, G_max=None, flags=0, stream=None):
-    """Chunked prefill of T query tokens per sequence (the last T of each cache)."""
+            out=None, lse=None, idx_out=None, G_max=None, flags=0, stream=None, ws=None,
+            check=True):
+    """Chunked prefill of T query tokens per sequence (the last T of each cache).
+
+    ws: optional uint8 device workspace of at least lcsw_prefill_workspace_size
+    bytes whose first 256 bytes (the status word) are zero; reused across
+    calls it needs no clearing, since a status check clears the word.
+    check: read the status word after the call (synchronises the stream)."""
     _bf16(q_idx, "q_idx", 4)
     _bf16(q, "q", 4)
     B, T, H_i, d_idx = q_idx.shape
@@ -356,8 +362,13 @@ def prefill(q_idx, w_head, k_pooled, k_idx, pool_w, q, K, V, seq_len, P, k, scal
     a.idx_out = idx_out.data_ptr() if idx_out is not None else None
     a.flags = int(flags)
     nbytes = lib().lcsw_prefill_workspace_size(ctypes.byref(a))
-    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
-    _check(lib().lcsw_prefill(ctypes.byref(a), ctypes.c_void_p(ws.data_ptr()), nbytes,
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        ws[:256].zero_()  # the status word; every other region is written before it is read
+    elif ws.numel() < nbytes:
+        raise ValueError(f"prefill workspace too small: {ws.numel()} < {nbytes} bytes")
+    _check(lib().lcsw_prefill(ctypes.byref(a), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                               _stream(stream)))
-    _check(lib().lcsw_get_status(ctypes.c_void_p(ws.data_ptr()), _stream(stream)))
+    if check:
+        _check(lib().lcsw_get_status(ctypes.c_void_p(ws.data_ptr()), _stream(stream)))
     return out, lse

@@ -75,6 +75,16 @@ cudaError_t launch_topk_rows(const float *scores, const int32_t *n_valid,
                              int k, int32_t *idx, cudaStream_t st,
                              const int32_t *row_mask = nullptr);
 
+// Sparse attention for many query rows on tcgen05 (H_q <= 32, d_qk = d_v =
+// 128): one persistent CTA per SM, no workspace; records a timed-out wait in
+// *status (nullable).
+bool sparse_attn_tc_supported(int64_t rows, int H_q, int d_qk, int d_v, int P, int k);
+cudaError_t launch_sparse_attn_tc(const uint16_t *q, const uint16_t *K, int64_t sK_b,
+                                  const uint16_t *V, int64_t sV_b, const int32_t *seq_len,
+                                  const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
+                                  int P, int k, float scale, uint16_t *out, float *lse,
+                                  int *status, cudaStream_t st);
+
 // Split-K sparse attention + combine.
 int sparse_attn_splits(int64_t rows, int H_q, int k, int P);
 size_t sparse_attn_ws_bytes(int64_t rows, int H_q, int d_v, int k, int P);

@@ -380,6 +380,9 @@ size_t lcsw_prefill_workspace_size(const lcsw_prefill_args *a) {
     return carve_prefill(a, nullptr).total;
 }
 
+// query rows from which the prefill attention runs on the tensor cores
+constexpr int64_t kPrefillTcRows = 256;
+
 lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
                          lcsw_stream stream) {
     CHECK(a, "null args");
@@ -463,6 +466,15 @@ lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
         e = lcsw::launch_topk_rows(w.scores, w.n_valid, nullptr, a->P, a->T, rows, a->G_max,
                                    a->k, idx, st);
         if (e != cudaSuccess) return cuda_status(e, "prefill top-k");
+    }
+    // many query rows: the persistent tensor-core attention (one row per CTA
+    // step, no split of the selected tokens); few rows: the split-K kernel
+    if (rows >= kPrefillTcRows &&
+        lcsw::sparse_attn_tc_supported(rows, a->H_q, a->d_qk, a->d_v, a->P, a->k)) {
+        e = lcsw::launch_sparse_attn_tc(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B,
+                                        a->T, a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale,
+                                        a->out, a->lse, w.status, st);
+        return cuda_status(e, "prefill attention (tensor cores)");
     }
     e = lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B, a->T,
                                  a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale, a->out, a->lse,

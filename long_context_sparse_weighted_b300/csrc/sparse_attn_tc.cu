@@ -1,0 +1,506 @@
+// Sparse attention over the selected history on the fifth-generation tensor
+// cores, for many query rows at once (chunked prefill): "G2C Brief --
+// GLM-5.3-Flash", DSA section (attention over the selected tokens, one
+// shared K/V head serving every query head).  A row's k selected groups
+// expand to k*P tokens, taken in chunks of 128.
+//
+// One persistent CTA per SM walks the rows; its warps have fixed roles:
+//   warps 4-6  gather.  Ring item n (a chunk's 128 key rows or value rows)
+//              belongs to warp 4 + n % 3, which copies it with 16-byte
+//              cp.async into a 32 KB 128B-swizzled tile of a 5-slot ring
+//              (zero fill for padding and for groups past the sequence),
+//              waits for its copies, fences them for the tensor core and
+//              arrives on the slot's mbarrier.  The warp holding a row's first
+//              item also loads the row's head tile.
+//   warp 7     MMA.  S^T = K Q^T (M = 128 tokens, N = 32 heads, K = 128) into
+//              TMEM, and O_c^T = V^T P^T (M = 128 value dims, N = 64: the 32
+//              heads padded to one 128-byte row of P, K = 128 tokens).  Per
+//              row it issues QK_0, then QK_c and PV_(c-1) for c = 1..n-1, then
+//              PV_(n-1); the ring holds the matching item sequence.
+//   warps 0-3  softmax.  Thread t owns TMEM lane t.  Per chunk it reads its
+//              token's head scores; the block takes the exact chunk maximum
+//              of every head (a warp maximum of order-preserving keys, then
+//              the four warps'), and the running maximum m, the rescale
+//              a = 2^(m_old - m_new) and p = 2^(z - m) follow.  Thread t
+//              writes its token's row of P (bf16) and keeps its own partial
+//              sums of p; then it folds O_(c-1)^T (lane t = value dim t) into
+//              its running output row, o = a o + O.  At the row's end the
+//              partial sums are reduced per head, and the normalised bf16
+//              output and the log-sum-exp are written.
+// S and O_c are double-buffered in TMEM (S: columns 0-63, O: 64-191), P in
+// shared memory.  Every hand-off is an mbarrier; every wait is bounded and a
+// wait that runs out stops all roles, which record LCSW_ERR_TIMEOUT in the
+// status word.  TMEM is released on every exit.
+#include "../../include/lcsw.h"
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tc_core.cuh"
+
+namespace lcsw {
+namespace {
+
+constexpr int kTok = 128;                 // tokens per chunk (M of S^T)
+constexpr int kDim = 128;                 // d_qk = d_v
+constexpr int kNH = 32;                   // heads (N of S^T; H_q padded)
+constexpr int kNPV = 64;                  // N of O^T: one 128-byte row of P
+constexpr int kSlots = 5;                 // gather ring
+constexpr int kSlotBytes = kTok * kDim * 2;   // 32 KB: a chunk's key or value rows
+constexpr int kAtomCol = kTok * 128;          // 16 KB: 64 elements of every row
+constexpr int kQBytes = kNH * kDim * 2;       // 8 KB head tile
+constexpr int kQAtomCol = kNH * 128;          // 4 KB
+constexpr int kPBytes = kTok * 128;           // 16 KB: 128 tokens x 64 heads (bf16)
+constexpr int kSmRing = 0;
+constexpr int kSmQ = kSmRing + kSlots * kSlotBytes;
+constexpr int kSmP = kSmQ + 2 * kQBytes;
+constexpr int kSmMisc = kSmP + 2 * kPBytes;
+constexpr int kMiscBytes = 3072;
+constexpr int kSmemBytes = kSmMisc + kMiscBytes + 1024;  // + alignment slack
+constexpr int kThr = 256;                 // 8 warps: two per SM sub-partition
+constexpr int kGatherWarp0 = 4, kMmaWarp = 7;
+constexpr int kGatherWarps = kMmaWarp - kGatherWarp0;
+constexpr int kColS = 0, kColO = 64, kTmemCols = 256;
+constexpr long long kWaitTries = 50000;   // up to 20 us each
+constexpr float kLn2f = 0.6931471805599453f;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+// Item i (0-based) of a row with n chunks: (is a value chunk, chunk index).
+__device__ __forceinline__ void item_of(int i, int n, bool &is_v, int &c) {
+    if (i == 0) {
+        is_v = false;
+        c = 0;
+    } else if (i == 2 * n - 1) {
+        is_v = true;
+        c = n - 1;
+    } else if (i & 1) {
+        is_v = false;
+        c = (i + 1) >> 1;
+    } else {
+        is_v = true;
+        c = (i >> 1) - 1;
+    }
+}
+
+// Bounded wait for the phase of the given parity; gives up when the budget
+// runs out or another role has given up.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity,
+                                           const volatile int *abort_flag) {
+    const uint32_t a = smem_u32(bar);
+    for (long long i = 0; i < kWaitTries; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(a), "r"(parity), "r"(kSuspendNs)
+            : "memory");
+        if (done) return true;
+        if (*abort_flag) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier 1 over the 128 softmax threads; returns the OR of `v` over them.
+__device__ __forceinline__ bool softmax_sync_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(uint32_t(v))
+        : "memory");
+    return r != 0;
+}
+
+// Inverse of score_key for the keys of finite scores; key 0 stands for -inf.
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+    if (key == 0u) return -INFINITY;
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+__global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
+    const uint16_t *__restrict__ q, const uint16_t *__restrict__ K, int64_t sK_b,
+    const uint16_t *__restrict__ V, int64_t sV_b, const int32_t *__restrict__ seq_len,
+    const int32_t *__restrict__ idx, int T, int H_q, int P, int k, int64_t rows,
+    float scale_log2, uint16_t *__restrict__ out, float *__restrict__ lse, int *status) {
+    extern __shared__ unsigned char smem_raw[];
+    // the swizzled tiles need 1024-byte alignment
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmMisc);
+    uint64_t *full = bars, *empty = bars + kSlots;          // ring slots
+    uint64_t *qfull = bars + 2 * kSlots, *qempty = qfull + 2;  // head tiles
+    uint64_t *sfull = qempty + 2, *sfree = sfull + 2;        // S^T in TMEM
+    uint64_t *pfull = sfree + 2, *pempty = pfull + 2;        // P in shared memory
+    uint64_t *ofull = pempty + 2, *ofree = ofull + 2;        // O_c^T in TMEM
+    uint64_t *mma_done = ofree + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
+    uint32_t *wmax = reinterpret_cast<uint32_t *>(smem + kSmMisc + 256);  // [2][4][32]
+    float *mnew = reinterpret_cast<float *>(wmax + 2 * 4 * 32);           // [2][32]
+    float *alph = mnew + 2 * 32;                                          // [2][32]
+    float *lsum = alph + 2 * 32;                                          // [4][32]
+    float *ltot = lsum + 4 * 32;                                          // [32]
+    const int lp2 = 31 - __clz(P);
+    const int nck = (k * P + kTok - 1) / kTok;
+    const int gpc = kTok >> lp2;  // groups per chunk
+
+    if (tid == 0) {
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qfull + i, 1);
+            mbar_init(qempty + i, 1);
+            mbar_init(sfull + i, 1);
+            mbar_init(sfree + i, 4);
+            mbar_init(pfull + i, 4);
+            mbar_init(pempty + i, 1);
+            mbar_init(ofull + i, 1);
+            mbar_init(ofree + i, 4);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc(tslot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *tslot;
+    auto give_up = [&](int where) {
+        *abort_flag = 1;
+        if (status) atomicCAS(status, 0, int(LCSW_ERR_TIMEOUT) * 256 + where);
+    };
+
+    if (warp >= kGatherWarp0 && warp < kMmaWarp) {
+        // ------------------------------------------------------------ gather
+        const int gw = warp - kGatherWarp0;
+        uint32_t n_item = 0;
+        int qi = 0;
+        bool ok = true;
+        for (int64_t row = blockIdx.x; row < rows && ok; row += gridDim.x, ++qi) {
+            const int b = int(row / T);
+            const int G = __ldg(seq_len + b) / P;
+            const int32_t *gl = idx + row * k;
+            const uint16_t *kb = K + int64_t(b) * sK_b, *vb = V + int64_t(b) * sV_b;
+            for (int i = 0; i < 2 * nck && ok; ++i, ++n_item) {
+                if (int(n_item % kGatherWarps) != gw) continue;
+                if (i == 0) {  // the row's head tile first
+                    const int qs = qi & 1;
+                    ok = __all_sync(0xffffffffu,
+                                    wait_phase(qempty + qs, (uint32_t(qi >> 1) & 1u) ^ 1u, abort_flag));
+                    if (!ok) break;
+                    unsigned char *qt = smem + kSmQ + qs * kQBytes;
+                    const uint16_t *qrow = q + row * int64_t(H_q) * kDim;
+                    for (int e = lane; e < kNH * 16; e += 32) {
+                        const int h = e >> 4, c16 = e & 15;
+                        const bool hv = h < H_q;
+                        cp_async16(smem_u32(qt + (c16 >> 3) * kQAtomCol + sw128_offset(h, (c16 & 7) * 8, 1024)),
+                                   hv ? qrow + h * kDim + c16 * 8 : qrow, hv ? 16 : 0);
+                    }
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(qfull + qs);
+                }
+                bool is_v;
+                int c;
+                item_of(i, nck, is_v, c);
+                const int slot = int(n_item % kSlots);
+                ok = __all_sync(0xffffffffu,
+                                wait_phase(empty + slot, ((n_item / kSlots) & 1u) ^ 1u, abort_flag));
+                if (!ok) break;
+                unsigned char *tile = smem + kSmRing + slot * kSlotBytes;
+                const uint16_t *base = is_v ? vb : kb;
+                // lane: one 16-byte column c16 of every other token
+                const int c16 = lane & 15;
+                const uint32_t dcol = uint32_t(c16 >> 3) * kAtomCol;
+#pragma unroll 8
+                for (int u = 0; u < kTok / 2; ++u) {
+                    const int t = 2 * u + (lane >> 4);
+                    const int j = c * gpc + (t >> lp2);
+                    const int g = j < k ? __ldg(gl + j) : -1;
+                    const bool tv = g >= 0 && g < G;
+                    const uint16_t *src =
+                        tv ? base + (int64_t(g) * P + (t & (P - 1))) * kDim + c16 * 8 : base;
+                    cp_async16(smem_u32(tile + dcol + sw128_offset(t, (c16 & 7) * 8, 1024)), src,
+                               tv ? 16 : 0);
+                }
+                cp_async_commit();
+                cp_async_wait<0>();
+                fence_async_smem();  // the copies, for the tensor core's reads
+                __syncwarp();
+                if (lane == 0) bar_arrive(full + slot);
+            }
+        }
+        cp_async_wait<0>();
+        if (!ok && lane == 0) give_up(11);
+    } else if (warp == kMmaWarp) {
+        // --------------------------------------------------------------- MMA
+        const uint32_t id_qk = idesc_bf16_f32(128, kNH, false, false);
+        const uint32_t id_pv = idesc_bf16_f32(128, kNPV, true, true);
+        uint32_t n_item = 0, n_ck = 0;
+        int qi = 0;
+        bool ok = true;
+        for (int64_t row = blockIdx.x; row < rows && ok; row += gridDim.x, ++qi) {
+            const int qs = qi & 1;
+            ok = __all_sync(0xffffffffu, wait_phase(qfull + qs, uint32_t(qi >> 1) & 1u, abort_flag));
+            const uint32_t qa = smem_u32(smem + kSmQ + qs * kQBytes);
+            for (int i = 0; i < 2 * nck && ok; ++i, ++n_item) {
+                bool is_v;
+                int c;
+                item_of(i, nck, is_v, c);
+                const int slot = int(n_item % kSlots);
+                const uint32_t ta = smem_u32(smem + kSmRing + slot * kSlotBytes);
+                const uint32_t gc = n_ck + uint32_t(c);  // chunk index over the CTA's rows
+                const int buf = int(gc & 1u);
+                const uint32_t bpar = (gc >> 1) & 1u;
+                ok = __all_sync(0xffffffffu,
+                                wait_phase(full + slot, (n_item / kSlots) & 1u, abort_flag));
+                if (!is_v) {
+                    ok = ok && __all_sync(0xffffffffu, wait_phase(sfree + buf, bpar ^ 1u, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < kDim / 16; ++ks) {
+                            const uint32_t ka = ta + (ks >> 2) * kAtomCol + (ks & 3) * 32;
+                            const uint32_t qk = qa + (ks >> 2) * kQAtomCol + (ks & 3) * 32;
+                            tc_mma_bf16(tb + kColS + buf * kNH, smem_desc(ka, 16, 1024),
+                                        smem_desc(qk, 16, 1024), id_qk, ks > 0);
+                        }
+                        tc_commit(sfull + buf);
+                        tc_commit(empty + slot);
+                        if (c == nck - 1) tc_commit(qempty + qs);
+                    }
+                    __syncwarp();
+                } else {
+                    ok = ok && __all_sync(0xffffffffu, wait_phase(pfull + buf, bpar, abort_flag));
+                    ok = ok && __all_sync(0xffffffffu, wait_phase(ofree + buf, bpar ^ 1u, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t pa = smem_u32(smem + kSmP + buf * kPBytes);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < kTok / 16; ++ks)
+                            tc_mma_bf16(tb + kColO + buf * kNPV,
+                                        smem_desc(ta + ks * 2048, kAtomCol, 1024),
+                                        smem_desc(pa + ks * 2048, kAtomCol, 1024), id_pv, ks > 0);
+                        tc_commit(ofull + buf);
+                        tc_commit(empty + slot);
+                        tc_commit(pempty + buf);
+                    }
+                    __syncwarp();
+                }
+            }
+            n_ck += uint32_t(nck);
+        }
+        if (!ok && lane == 0) give_up(12);
+        // every product issued so far completes before TMEM is released
+        if (elect_one()) tc_commit(mma_done);
+        __syncwarp();
+        mbar_wait(mma_done, 0u, kWaitTries);  // bounded; not cut short by an abort
+    } else {
+        // ----------------------------------------------------------- softmax
+        // warps 0-3: thread tid owns TMEM lane tid -- its token of each S^T
+        // chunk and value dim tid of each O_c^T
+        const uint32_t lane_addr = tb + (uint32_t(warp * 32) << 16);
+        uint32_t n_ck = 0;
+        bool ok = true;
+        float m_run = -INFINITY;  // warp 0, lane h: running maximum of head h
+        for (int64_t row = blockIdx.x; row < rows && ok; row += gridDim.x) {
+            const int b = int(row / T);
+            const int G = __ldg(seq_len + b) / P;
+            const int32_t *gl = idx + row * k;
+            float o[kNH], lp[kNH];
+#pragma unroll
+            for (int h = 0; h < kNH; ++h) o[h] = lp[h] = 0.f;
+            m_run = -INFINITY;
+            // o = a o + O_c for the chunk with index gcf over the CTA's rows
+            auto fold = [&](uint32_t gcf) {
+                const int fb = int(gcf & 1u);
+                ok = ok && __all_sync(0xffffffffu, wait_phase(ofull + fb, (gcf >> 1) & 1u, abort_flag));
+                tc_fence_after();
+                uint32_t r[32];
+                if (ok) {
+                    tc_ld32(lane_addr + kColO + fb * kNPV, r);
+                    tc_wait_ld();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) bar_arrive(ofree + fb);
+                if (ok) {
+#pragma unroll
+                    for (int h4 = 0; h4 < kNH / 4; ++h4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(alph + fb * 32 + 4 * h4);
+                        o[4 * h4 + 0] = fmaf(o[4 * h4 + 0], a4.x, __uint_as_float(r[4 * h4 + 0]));
+                        o[4 * h4 + 1] = fmaf(o[4 * h4 + 1], a4.y, __uint_as_float(r[4 * h4 + 1]));
+                        o[4 * h4 + 2] = fmaf(o[4 * h4 + 2], a4.z, __uint_as_float(r[4 * h4 + 2]));
+                        o[4 * h4 + 3] = fmaf(o[4 * h4 + 3], a4.w, __uint_as_float(r[4 * h4 + 3]));
+                    }
+                }
+            };
+            for (int c = 0; c < nck; ++c) {
+                const uint32_t gc = n_ck + uint32_t(c);
+                const int buf = int(gc & 1u);
+                const uint32_t bpar = (gc >> 1) & 1u;
+                ok = ok && __all_sync(0xffffffffu, wait_phase(sfull + buf, bpar, abort_flag));
+                tc_fence_after();
+                uint32_t s[32];
+                if (ok) {
+                    tc_ld32(lane_addr + kColS + buf * kNH, s);
+                    tc_wait_ld();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) bar_arrive(sfree + buf);
+                // this thread's token: z = scale * q.k in the log2 domain, or
+                // -inf for padding and groups past the sequence
+                const int t = c * kTok + tid;
+                const int j = t >> lp2;
+                const int g = j < k ? __ldg(gl + j) : -1;
+                const bool tv = ok && g >= 0 && g < G;
+                uint32_t mine = 0u;
+#pragma unroll
+                for (int h = 0; h < kNH; ++h) {
+                    const float z = tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY;
+                    s[h] = __float_as_uint(z);
+                    const uint32_t wk = __reduce_max_sync(0xffffffffu, tv ? score_key(z) : 0u);
+                    if (lane == h) mine = wk;
+                }
+                wmax[(buf * 4 + warp) * 32 + lane] = mine;
+                if (softmax_sync_or(!ok)) {
+                    ok = false;
+                    break;
+                }
+                if (warp == 0) {  // lane h: head h's chunk maximum, running maximum, rescale
+                    const uint32_t *w4 = wmax + buf * 4 * 32 + lane;
+                    const uint32_t km = max(max(w4[0], w4[32]), max(w4[64], w4[96]));
+                    const float mn = fmaxf(m_run, key_to_float(km));
+                    alph[buf * 32 + lane] = mn == -INFINITY ? 1.f : exp2f(m_run - mn);
+                    mnew[buf * 32 + lane] = mn;
+                    m_run = mn;
+                }
+                softmax_sync_or(false);
+                // p = 2^(z - m) -> this token's row of P (bf16, 128B-swizzled
+                // MN-major: 8 heads per 16-byte chunk); partial sums rescaled
+                ok = ok && __all_sync(0xffffffffu, wait_phase(pempty + buf, bpar ^ 1u, abort_flag));
+                unsigned char *pt = smem + kSmP + buf * kPBytes;
+#pragma unroll
+                for (int h8 = 0; h8 < kNH / 8; ++h8) {
+                    uint32_t pw[4];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int h0 = 8 * h8 + 4 * hh;
+                        const float4 m4 = *reinterpret_cast<const float4 *>(mnew + buf * 32 + h0);
+                        const float4 a4 = *reinterpret_cast<const float4 *>(alph + buf * 32 + h0);
+                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                        const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
+                        float pp[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float z = __uint_as_float(s[h0 + e]);
+                            pp[e] = z == -INFINITY ? 0.f : exp2f(z - mm[e]);
+                            lp[h0 + e] = fmaf(lp[h0 + e], aa[e], pp[e]);
+                        }
+                        pw[2 * hh] = pack_bf2(pp[0], pp[1]);
+                        pw[2 * hh + 1] = pack_bf2(pp[2], pp[3]);
+                    }
+                    *reinterpret_cast<uint4 *>(pt + sw128_offset(tid, 8 * h8, 1024)) =
+                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                }
+                fence_async_smem();  // P, for the tensor core's reads
+                __syncwarp();
+                if (lane == 0) bar_arrive(pfull + buf);
+                if (c > 0) fold(gc - 1u);
+            }
+            if (ok) fold(n_ck + uint32_t(nck) - 1u);
+            if (softmax_sync_or(!ok)) {
+                ok = false;
+                break;
+            }
+            // per-head sums of p: halve the warp's 32 partial sums at every
+            // step so that lane h ends with the warp's sum for head h
+#pragma unroll
+            for (int hw = 16; hw >= 1; hw >>= 1) {
+                const bool upper = (lane & hw) != 0;
+#pragma unroll
+                for (int i = 0; i < hw; ++i) {
+                    const float keep = upper ? lp[i + hw] : lp[i];
+                    const float send = upper ? lp[i] : lp[i + hw];
+                    lp[i] = keep + __shfl_xor_sync(0xffffffffu, send, hw);
+                }
+            }
+            lsum[warp * 32 + lane] = lp[0];
+            softmax_sync_or(false);
+            if (warp == 0) {
+                const float L = lsum[lane] + lsum[32 + lane] + lsum[64 + lane] + lsum[96 + lane];
+                ltot[lane] = L;
+                if (lse && lane < H_q)
+                    lse[row * H_q + lane] = L > 0.f ? (m_run + log2f(L)) * kLn2f : -INFINITY;
+            }
+            softmax_sync_or(false);
+            // the normalised output: thread tid is value dim tid of every head
+            uint16_t *orow = out + row * int64_t(H_q) * kDim + tid;
+#pragma unroll
+            for (int h = 0; h < kNH; ++h) {
+                if (h < H_q) {
+                    const float L = ltot[h];
+                    orow[h * kDim] = f2bf(L > 0.f ? o[h] * (1.f / L) : 0.f);
+                }
+            }
+            n_ck += uint32_t(nck);
+        }
+        if (!ok && tid == 0) give_up(13);
+    }
+    // every role is done (the MMA warp saw its last products complete)
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_free(tb, kTmemCols);
+}
+
+int sm_count() {
+    static int n[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (n[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+            v = 148;
+        n[dev] = v;
+    }
+    return n[dev];
+}
+
+}  // namespace
+
+bool sparse_attn_tc_supported(int64_t rows, int H_q, int d_qk, int d_v, int P, int k) {
+    return rows >= 1 && H_q >= 1 && H_q <= kNH && d_qk == kDim && d_v == kDim &&
+           (P == 1 || P == 2 || P == 4 || P == 8) && k >= 1 && int64_t(k) * P <= (1 << 24);
+}
+
+cudaError_t launch_sparse_attn_tc(const uint16_t *q, const uint16_t *K, int64_t sK_b,
+                                  const uint16_t *V, int64_t sV_b, const int32_t *seq_len,
+                                  const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
+                                  int P, int k, float scale, uint16_t *out, float *lse,
+                                  int *status, cudaStream_t st) {
+    const int64_t rows = int64_t(B) * T;
+    if (rows == 0) return cudaSuccess;
+    if (!sparse_attn_tc_supported(rows, H_q, d_qk, d_v, P, k)) return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = rows < sm_count() ? rows : sm_count();
+    sparse_attn_tc_kernel<<<unsigned(grid), kThr, kSmemBytes, st>>>(
+        q, K, sK_b, V, sV_b, seq_len, idx, T, H_q, P, k, rows, scale * 1.4426950408889634f, out,
+        lse, status);
+    return cudaGetLastError();
+}
+
+}  // namespace lcsw

@@ -223,6 +223,25 @@ def test_prefill_fused_selection(lengths, T, k, flags):
     assert_lse_close(got["lse"], ref["lse"])
 
 
+# From 256 query rows the prefill attention runs on the tensor cores (chunks
+# of 128 selected tokens, S and O accumulated in TMEM).  Edges: a sequence
+# with fewer visible groups than k (padded selections), k*P not a multiple of
+# 128 (a partial last chunk), 16 query heads (half of the head tile padded),
+# and P = 2.
+@pytest.mark.parametrize("lengths,T,k,H_q,P", [([600, 5000], 128, 200, 16, 4),
+                                               ([3000], 256, 70, 32, 2)])
+def test_prefill_tensor_core_attention_edges(lengths, T, k, H_q, P):
+    spec = synth.Spec(B=len(lengths), lengths=lengths, T=T, prefill=True, H_i=8, k=k, H_q=H_q,
+                      P=P, seed=250 + P)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_prefill(c, _cached_part(ref["k_pooled"], c))
+    nd = selection_diff(got["idx"], ref["idx"], ref["scores"])
+    assert nd == 0, f"{nd} rows differ by near-ties"
+    assert_attn_close(got["out"], ref["out"])
+    assert_lse_close(got["lse"], ref["lse"])
+
+
 def test_prefill_fused_selection_exact_ties():
     # integer keys and queries with dyadic weights: exact scores with many equal
     # values, so the tie rule (lowest group first) decides many selections
