@@ -26,6 +26,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc_core.cuh"
+#include "tma_host.h"
 
 namespace lcsw {
 namespace {
@@ -471,6 +472,8 @@ __global__ void __launch_bounds__(kPThr, 1)
     if (warp == 0) tmem_free(tb, 512);
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -484,8 +487,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
-
-}  // namespace
 
 bool index_scores_tc_supported(int B, int T, int H_i, int G_max, int64_t sp_b) {
     // the group tiles read up to G_max rows of every sequence's cache

@@ -7,11 +7,13 @@
 // One persistent CTA per SM walks the rows; its warps have fixed roles:
 //   warps 4-6  gather.  Ring item n (a chunk's 128 key rows or value rows)
 //              belongs to warp 4 + n % 3, which copies it with 16-byte
-//              cp.async into a 32 KB 128B-swizzled tile of a 5-slot ring
-//              (zero fill for padding and for groups past the sequence),
-//              waits for its copies, fences them for the tensor core and
-//              arrives on the slot's mbarrier.  The warp holding a row's first
-//              item also loads the row's head tile.
+//              cp.async into slot n % 5 of a ring of 32 KB 128B-swizzled tiles
+//              (zero fill for padding and for groups past the sequence), waits
+//              for its copies, fences them for the tensor core and arrives on
+//              the slot's mbarrier.  The chunk's 128 token rows are computed
+//              once per item into shared memory (four index loads per lane),
+//              so a copy costs a shared load and a few adds.  The warp
+//              holding a row's first item also loads the row's head tile.
 //   warp 7     MMA.  S^T = K Q^T (M = 128 tokens, N = 32 heads, K = 128) into
 //              TMEM, and O_c^T = V^T P^T (M = 128 value dims, N = 64: the 32
 //              heads padded to one 128-byte row of P, K = 128 tokens).  Per
@@ -53,7 +55,7 @@ constexpr int kSmRing = 0;
 constexpr int kSmQ = kSmRing + kSlots * kSlotBytes;
 constexpr int kSmP = kSmQ + 2 * kQBytes;
 constexpr int kSmMisc = kSmP + 2 * kPBytes;
-constexpr int kMiscBytes = 3072;
+constexpr int kMiscBytes = 4096;
 constexpr int kSmemBytes = kSmMisc + kMiscBytes + 1024;  // + alignment slack
 constexpr int kThr = 256;                 // 8 warps: two per SM sub-partition
 constexpr int kGatherWarp0 = 4, kMmaWarp = 7;
@@ -115,10 +117,26 @@ __device__ __forceinline__ bool softmax_sync_or(bool v) {
     return r != 0;
 }
 
-// Inverse of score_key for the keys of finite scores; key 0 stands for -inf.
-__device__ __forceinline__ float key_to_float(uint32_t key) {
-    if (key == 0u) return -INFINITY;
-    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+// Maximum over the warp (every lane gets it).
+__device__ __forceinline__ float warp_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22; p is rounded
+// to bf16 for the product).
+__device__ __forceinline__ float exp2_hw(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Two floats -> bf16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
@@ -139,11 +157,12 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
     uint64_t *mma_done = ofree + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
-    uint32_t *wmax = reinterpret_cast<uint32_t *>(smem + kSmMisc + 256);  // [2][4][32]
+    float *wmax = reinterpret_cast<float *>(smem + kSmMisc + 256);        // [2][4][32]
     float *mnew = reinterpret_cast<float *>(wmax + 2 * 4 * 32);           // [2][32]
     float *alph = mnew + 2 * 32;                                          // [2][32]
     float *lsum = alph + 2 * 32;                                          // [4][32]
     float *ltot = lsum + 4 * 32;                                          // [32]
+    int *toff = reinterpret_cast<int *>(ltot + 32);                       // [3][128]
     const int lp2 = 31 - __clz(P);
     const int nck = (k * P + kTok - 1) / kTok;
     const int gpc = kTok >> lp2;  // groups per chunk
@@ -183,6 +202,8 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
         uint32_t n_item = 0;
         int qi = 0;
         bool ok = true;
+        const int c16 = lane & 15;                            // 16-byte column of a row
+        const uint32_t dcol = uint32_t(c16 >> 3) * kAtomCol;  // its 64-element atom column
         for (int64_t row = blockIdx.x; row < rows && ok; row += gridDim.x, ++qi) {
             const int b = int(row / T);
             const int G = __ldg(seq_len + b) / P;
@@ -190,7 +211,7 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
             const uint16_t *kb = K + int64_t(b) * sK_b, *vb = V + int64_t(b) * sV_b;
             for (int i = 0; i < 2 * nck && ok; ++i, ++n_item) {
                 if (int(n_item % kGatherWarps) != gw) continue;
-                if (i == 0) {  // the row's head tile first
+                if (i == 0) {  // the row's head tile first (heads past H_q are zero)
                     const int qs = qi & 1;
                     ok = __all_sync(0xffffffffu,
                                     wait_phase(qempty + qs, (uint32_t(qi >> 1) & 1u) ^ 1u, abort_flag));
@@ -198,10 +219,10 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                     unsigned char *qt = smem + kSmQ + qs * kQBytes;
                     const uint16_t *qrow = q + row * int64_t(H_q) * kDim;
                     for (int e = lane; e < kNH * 16; e += 32) {
-                        const int h = e >> 4, c16 = e & 15;
+                        const int h = e >> 4, cc = e & 15;
                         const bool hv = h < H_q;
-                        cp_async16(smem_u32(qt + (c16 >> 3) * kQAtomCol + sw128_offset(h, (c16 & 7) * 8, 1024)),
-                                   hv ? qrow + h * kDim + c16 * 8 : qrow, hv ? 16 : 0);
+                        cp_async16(smem_u32(qt + (cc >> 3) * kQAtomCol + sw128_offset(h, (cc & 7) * 8, 1024)),
+                                   hv ? qrow + h * kDim + cc * 8 : qrow, hv ? 16 : 0);
                     }
                     cp_async_commit();
                     cp_async_wait<0>();
@@ -216,21 +237,34 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 ok = __all_sync(0xffffffffu,
                                 wait_phase(empty + slot, ((n_item / kSlots) & 1u) ^ 1u, abort_flag));
                 if (!ok) break;
-                unsigned char *tile = smem + kSmRing + slot * kSlotBytes;
-                const uint16_t *base = is_v ? vb : kb;
-                // lane: one 16-byte column c16 of every other token
-                const int c16 = lane & 15;
-                const uint32_t dcol = uint32_t(c16 >> 3) * kAtomCol;
+                // first token row of each of the chunk's groups (-1: zero fill);
+                // lane l holds groups l, l + 32, l + 64, l + 96
+                int rb[4];
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int gi = lane + 32 * qq, j = c * gpc + gi;
+                    const int g = (gi < gpc && j < k) ? __ldg(gl + j) : -1;
+                    rb[qq] = (g >= 0 && g < G) ? g * P : -1;
+                }
+                // every token's row in the chunk (-1: zero fill)
+                int *to = toff + gw * kTok;
+#pragma unroll
+                for (int v = 0; v < kTok / 32; ++v) {
+                    const int t = lane + 32 * v, j = c * gpc + (t >> lp2);
+                    const int g = j < k ? __ldg(gl + j) : -1;
+                    to[t] = (g >= 0 && g < G) ? g * P + (t & (P - 1)) : -1;
+                }
+                __syncwarp();
+                const uint32_t tbase = smem_u32(smem + kSmRing + slot * kSlotBytes) + dcol;
+                const uint16_t *base = (is_v ? vb : kb) + c16 * 8;
+                const int hi = lane >> 4;
 #pragma unroll 8
                 for (int u = 0; u < kTok / 2; ++u) {
-                    const int t = 2 * u + (lane >> 4);
-                    const int j = c * gpc + (t >> lp2);
-                    const int g = j < k ? __ldg(gl + j) : -1;
-                    const bool tv = g >= 0 && g < G;
-                    const uint16_t *src =
-                        tv ? base + (int64_t(g) * P + (t & (P - 1))) * kDim + c16 * 8 : base;
-                    cp_async16(smem_u32(tile + dcol + sw128_offset(t, (c16 & 7) * 8, 1024)), src,
-                               tv ? 16 : 0);
+                    const int t = 2 * u + hi;
+                    const int r = to[t];
+                    cp_async16(tbase + uint32_t((t >> 3) << 10) + uint32_t((t & 7) << 7) +
+                                   uint32_t(((c16 & 7) ^ (t & 7)) << 4),
+                               r >= 0 ? base + int64_t(r) * kDim : base, r >= 0 ? 16 : 0);
                 }
                 cp_async_commit();
                 cp_async_wait<0>();
@@ -366,24 +400,28 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 const int j = t >> lp2;
                 const int g = j < k ? __ldg(gl + j) : -1;
                 const bool tv = ok && g >= 0 && g < G;
-                uint32_t mine = 0u;
+                float wm[kNH];
 #pragma unroll
                 for (int h = 0; h < kNH; ++h) {
                     const float z = tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY;
                     s[h] = __float_as_uint(z);
-                    const uint32_t wk = __reduce_max_sync(0xffffffffu, tv ? score_key(z) : 0u);
-                    if (lane == h) mine = wk;
+                    wm[h] = warp_max(z);
                 }
-                wmax[(buf * 4 + warp) * 32 + lane] = mine;
+                if (lane == 0) {
+                    float4 *w4 = reinterpret_cast<float4 *>(wmax + (buf * 4 + warp) * 32);
+#pragma unroll
+                    for (int h4 = 0; h4 < kNH / 4; ++h4)
+                        w4[h4] = make_float4(wm[4 * h4], wm[4 * h4 + 1], wm[4 * h4 + 2], wm[4 * h4 + 3]);
+                }
                 if (softmax_sync_or(!ok)) {
                     ok = false;
                     break;
                 }
                 if (warp == 0) {  // lane h: head h's chunk maximum, running maximum, rescale
-                    const uint32_t *w4 = wmax + buf * 4 * 32 + lane;
-                    const uint32_t km = max(max(w4[0], w4[32]), max(w4[64], w4[96]));
-                    const float mn = fmaxf(m_run, key_to_float(km));
-                    alph[buf * 32 + lane] = mn == -INFINITY ? 1.f : exp2f(m_run - mn);
+                    const float *w4 = wmax + buf * 4 * 32 + lane;
+                    const float cm = fmaxf(fmaxf(w4[0], w4[32]), fmaxf(w4[64], w4[96]));
+                    const float mn = fmaxf(m_run, cm);
+                    alph[buf * 32 + lane] = mn == -INFINITY ? 1.f : exp2_hw(m_run - mn);
                     mnew[buf * 32 + lane] = mn;
                     m_run = mn;
                 }
@@ -406,11 +444,11 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float z = __uint_as_float(s[h0 + e]);
-                            pp[e] = z == -INFINITY ? 0.f : exp2f(z - mm[e]);
+                            pp[e] = z == -INFINITY ? 0.f : exp2_hw(z - mm[e]);
                             lp[h0 + e] = fmaf(lp[h0 + e], aa[e], pp[e]);
                         }
-                        pw[2 * hh] = pack_bf2(pp[0], pp[1]);
-                        pw[2 * hh + 1] = pack_bf2(pp[2], pp[3]);
+                        pw[2 * hh] = pack_bf2_rn(pp[0], pp[1]);
+                        pw[2 * hh + 1] = pack_bf2_rn(pp[2], pp[3]);
                     }
                     *reinterpret_cast<uint4 *>(pt + sw128_offset(tid, 8 * h8, 1024)) =
                         make_uint4(pw[0], pw[1], pw[2], pw[3]);
