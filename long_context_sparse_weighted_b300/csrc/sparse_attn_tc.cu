@@ -5,8 +5,8 @@
 // expand to k*P tokens, taken in chunks of 128.
 //
 // One persistent CTA per SM walks the rows; its warps have fixed roles:
-//   warps 4-6  gather.  Ring item n (a chunk's 128 key rows or value rows)
-//              belongs to warp 4 + n % 3, which copies it with 16-byte
+//   warps 4-8  gather.  Ring item n (a chunk's 128 key rows or value rows)
+//              belongs to warp 4 + n % 5, which copies it with 16-byte
 //              cp.async into slot n % 5 of a ring of 32 KB 128B-swizzled tiles
 //              (zero fill for padding and for groups past the sequence), waits
 //              for its copies, fences them for the tensor core and arrives on
@@ -14,7 +14,7 @@
 //              once per item into shared memory (four index loads per lane),
 //              so a copy costs a shared load and a few adds.  The warp
 //              holding a row's first item also loads the row's head tile.
-//   warp 7     MMA.  S^T = K Q^T (M = 128 tokens, N = 32 heads, K = 128) into
+//   warp 9     MMA.  S^T = K Q^T (M = 128 tokens, N = 32 heads, K = 128) into
 //              TMEM, and O_c^T = V^T P^T (M = 128 value dims, N = 64: the 32
 //              heads padded to one 128-byte row of P, K = 128 tokens).  Per
 //              row it issues QK_0, then QK_c and PV_(c-1) for c = 1..n-1, then
@@ -24,10 +24,11 @@
 //              of every head (a warp maximum of order-preserving keys, then
 //              the four warps'), and the running maximum m, the rescale
 //              a = 2^(m_old - m_new) and p = 2^(z - m) follow.  Thread t
-//              writes its token's row of P (bf16) and keeps its own partial
-//              sums of p; then it folds O_(c-1)^T (lane t = value dim t) into
-//              its running output row, o = a o + O.  At the row's end the
-//              partial sums are reduced per head, and the normalised bf16
+//              writes its token's row of P (bf16); the warp's sums of p per
+//              head go to shared memory, and lane h of warp 0 keeps head h's
+//              running sum l = a (l + sum of the previous chunk).  Then the
+//              thread folds O_(c-1)^T (lane t = value dim t) into its running
+//              output row, o = a o + O.  At the row's end the normalised bf16
 //              output and the log-sum-exp are written.
 // S and O_c are double-buffered in TMEM (S: columns 0-63, O: 64-191), P in
 // shared memory.  Every hand-off is an mbarrier; every wait is bounded and a
@@ -55,10 +56,10 @@ constexpr int kSmRing = 0;
 constexpr int kSmQ = kSmRing + kSlots * kSlotBytes;
 constexpr int kSmP = kSmQ + 2 * kQBytes;
 constexpr int kSmMisc = kSmP + 2 * kPBytes;
-constexpr int kMiscBytes = 4096;
+constexpr int kMiscBytes = 6144;
 constexpr int kSmemBytes = kSmMisc + kMiscBytes + 1024;  // + alignment slack
-constexpr int kThr = 256;                 // 8 warps: two per SM sub-partition
-constexpr int kGatherWarp0 = 4, kMmaWarp = 7;
+constexpr int kThr = 320;                 // 10 warps
+constexpr int kGatherWarp0 = 4, kMmaWarp = 9;
 constexpr int kGatherWarps = kMmaWarp - kGatherWarp0;
 constexpr int kColS = 0, kColO = 64, kTmemCols = 256;
 constexpr long long kWaitTries = 50000;   // up to 20 us each
@@ -160,9 +161,9 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
     float *wmax = reinterpret_cast<float *>(smem + kSmMisc + 256);        // [2][4][32]
     float *mnew = reinterpret_cast<float *>(wmax + 2 * 4 * 32);           // [2][32]
     float *alph = mnew + 2 * 32;                                          // [2][32]
-    float *lsum = alph + 2 * 32;                                          // [4][32]
-    float *ltot = lsum + 4 * 32;                                          // [32]
-    int *toff = reinterpret_cast<int *>(ltot + 32);                       // [3][128]
+    float *lsum = alph + 2 * 32;                                          // [2][4][32]
+    float *ltot = lsum + 2 * 4 * 32;                                      // [32]
+    int *toff = reinterpret_cast<int *>(ltot + 32);           // [kGatherWarps][128]
     const int lp2 = 31 - __clz(P);
     const int nck = (k * P + kTok - 1) / kTok;
     const int gpc = kTok >> lp2;  // groups per chunk
@@ -348,14 +349,16 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
         uint32_t n_ck = 0;
         bool ok = true;
         float m_run = -INFINITY;  // warp 0, lane h: running maximum of head h
+        float l_run = 0.f;        // warp 0, lane h: running sum of p of head h
         for (int64_t row = blockIdx.x; row < rows && ok; row += gridDim.x) {
             const int b = int(row / T);
             const int G = __ldg(seq_len + b) / P;
             const int32_t *gl = idx + row * k;
-            float o[kNH], lp[kNH];
+            float o[kNH];
 #pragma unroll
-            for (int h = 0; h < kNH; ++h) o[h] = lp[h] = 0.f;
+            for (int h = 0; h < kNH; ++h) o[h] = 0.f;
             m_run = -INFINITY;
+            l_run = 0.f;
             // o = a o + O_c for the chunk with index gcf over the CTA's rows
             auto fold = [&](uint32_t gcf) {
                 const int fb = int(gcf & 1u);
@@ -391,27 +394,17 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                     tc_ld32(lane_addr + kColS + buf * kNH, s);
                     tc_wait_ld();
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) bar_arrive(sfree + buf);
                 // this thread's token: z = scale * q.k in the log2 domain, or
                 // -inf for padding and groups past the sequence
                 const int t = c * kTok + tid;
                 const int j = t >> lp2;
                 const int g = j < k ? __ldg(gl + j) : -1;
                 const bool tv = ok && g >= 0 && g < G;
-                float wm[kNH];
+                float *wrow = wmax + (buf * 4 + warp) * 32;
 #pragma unroll
                 for (int h = 0; h < kNH; ++h) {
-                    const float z = tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY;
-                    s[h] = __float_as_uint(z);
-                    wm[h] = warp_max(z);
-                }
-                if (lane == 0) {
-                    float4 *w4 = reinterpret_cast<float4 *>(wmax + (buf * 4 + warp) * 32);
-#pragma unroll
-                    for (int h4 = 0; h4 < kNH / 4; ++h4)
-                        w4[h4] = make_float4(wm[4 * h4], wm[4 * h4 + 1], wm[4 * h4 + 2], wm[4 * h4 + 3]);
+                    const float m = warp_max(tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY);
+                    if (lane == 0) wrow[h] = m;
                 }
                 if (softmax_sync_or(!ok)) {
                     ok = false;
@@ -421,14 +414,30 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                     const float *w4 = wmax + buf * 4 * 32 + lane;
                     const float cm = fmaxf(fmaxf(w4[0], w4[32]), fmaxf(w4[64], w4[96]));
                     const float mn = fmaxf(m_run, cm);
-                    alph[buf * 32 + lane] = mn == -INFINITY ? 1.f : exp2_hw(m_run - mn);
+                    const float a = mn == -INFINITY ? 1.f : exp2_hw(m_run - mn);
+                    alph[buf * 32 + lane] = a;
                     mnew[buf * 32 + lane] = mn;
                     m_run = mn;
+                    if (c > 0) {  // the previous chunk's sums, then the rescale
+                        const float *ls = lsum + (buf ^ 1) * 4 * 32 + lane;
+                        l_run += (ls[0] + ls[32]) + (ls[64] + ls[96]);
+                    }
+                    l_run *= a;
                 }
                 softmax_sync_or(false);
                 // p = 2^(z - m) -> this token's row of P (bf16, 128B-swizzled
                 // MN-major: 8 heads per 16-byte chunk); partial sums rescaled
                 ok = ok && __all_sync(0xffffffffu, wait_phase(pempty + buf, bpar ^ 1u, abort_flag));
+                if (ok) {  // the scores again (fewer live registers across the barriers)
+                    tc_ld32(lane_addr + kColS + buf * kNH, s);
+                    tc_wait_ld();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) bar_arrive(sfree + buf);
+#pragma unroll
+                for (int h = 0; h < kNH; ++h)
+                    s[h] = __float_as_uint(tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY);
                 unsigned char *pt = smem + kSmP + buf * kPBytes;
 #pragma unroll
                 for (int h8 = 0; h8 < kNH / 8; ++h8) {
@@ -437,15 +446,13 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                     for (int hh = 0; hh < 2; ++hh) {
                         const int h0 = 8 * h8 + 4 * hh;
                         const float4 m4 = *reinterpret_cast<const float4 *>(mnew + buf * 32 + h0);
-                        const float4 a4 = *reinterpret_cast<const float4 *>(alph + buf * 32 + h0);
                         const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                        const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
                         float pp[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float z = __uint_as_float(s[h0 + e]);
                             pp[e] = z == -INFINITY ? 0.f : exp2_hw(z - mm[e]);
-                            lp[h0 + e] = fmaf(lp[h0 + e], aa[e], pp[e]);
+                            s[h0 + e] = __float_as_uint(pp[e]);
                         }
                         pw[2 * hh] = pack_bf2_rn(pp[0], pp[1]);
                         pw[2 * hh + 1] = pack_bf2_rn(pp[2], pp[3]);
@@ -456,6 +463,19 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 fence_async_smem();  // P, for the tensor core's reads
                 __syncwarp();
                 if (lane == 0) bar_arrive(pfull + buf);
+                // the warp's sums of p: halve the 32 values at every step so
+                // that lane h ends with head h's sum
+#pragma unroll
+                for (int hw = 16; hw >= 1; hw >>= 1) {
+                    const bool upper = (lane & hw) != 0;
+#pragma unroll
+                    for (int i = 0; i < hw; ++i) {
+                        const float keep = __uint_as_float(upper ? s[i + hw] : s[i]);
+                        const float send = __uint_as_float(upper ? s[i] : s[i + hw]);
+                        s[i] = __float_as_uint(keep + __shfl_xor_sync(0xffffffffu, send, hw));
+                    }
+                }
+                lsum[(buf * 4 + warp) * 32 + lane] = __uint_as_float(s[0]);
                 if (c > 0) fold(gc - 1u);
             }
             if (ok) fold(n_ck + uint32_t(nck) - 1u);
@@ -463,22 +483,9 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 ok = false;
                 break;
             }
-            // per-head sums of p: halve the warp's 32 partial sums at every
-            // step so that lane h ends with the warp's sum for head h
-#pragma unroll
-            for (int hw = 16; hw >= 1; hw >>= 1) {
-                const bool upper = (lane & hw) != 0;
-#pragma unroll
-                for (int i = 0; i < hw; ++i) {
-                    const float keep = upper ? lp[i + hw] : lp[i];
-                    const float send = upper ? lp[i] : lp[i + hw];
-                    lp[i] = keep + __shfl_xor_sync(0xffffffffu, send, hw);
-                }
-            }
-            lsum[warp * 32 + lane] = lp[0];
-            softmax_sync_or(false);
-            if (warp == 0) {
-                const float L = lsum[lane] + lsum[32 + lane] + lsum[64 + lane] + lsum[96 + lane];
+            if (warp == 0) {  // the last chunk's sums complete the row's
+                const float *ls = lsum + ((n_ck + uint32_t(nck) - 1u) & 1u) * 4 * 32 + lane;
+                const float L = l_run + ((ls[0] + ls[32]) + (ls[64] + ls[96]));
                 ltot[lane] = L;
                 if (lse && lane < H_q)
                     lse[row * H_q + lane] = L > 0.f ? (m_run + log2f(L)) * kLn2f : -INFINITY;
