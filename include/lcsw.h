@@ -284,6 +284,12 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
  * is written before it is read).  Calls sharing a workspace must not overlap.
  * ------------------------------------------------------------------------- */
 #define LCSW_PREFILL_FORCE_FALLBACK 1
+/* Failure-detection test: in the tensor-core attention (>= 256 query rows,
+ * H_q <= 32, d_qk = d_v = 128) the first key chunk of every CTA is copied but
+ * never handed over, so the MMA warp's bounded wait (about a second) runs out
+ * and every role stops; the call reports LCSW_ERR_TIMEOUT through
+ * lcsw_get_status and its output is not valid.  The context stays usable. */
+#define LCSW_PREFILL_TEST_SKIP_GATHER 2
 typedef struct {
     const lcsw_bf16 *q_idx;    /* [B][T][H_i][d_idx]                           */
     const float *w_head;       /* [B][T][H_i]                                  */

@@ -45,6 +45,7 @@ FORCE_MULTIPASS_SELECT = 1
 FORCE_MULTIKERNEL = 2
 TEST_SKIP_ARRIVE = 4
 PREFILL_FORCE_FALLBACK = 1  # lcsw_prefill_args.flags
+PREFILL_TEST_SKIP_GATHER = 2
 
 
 class PrefillArgs(ctypes.Structure):

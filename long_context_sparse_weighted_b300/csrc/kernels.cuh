@@ -83,7 +83,7 @@ cudaError_t launch_sparse_attn_tc(const uint16_t *q, const uint16_t *K, int64_t 
                                   const uint16_t *V, int64_t sV_b, const int32_t *seq_len,
                                   const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
                                   int P, int k, float scale, uint16_t *out, float *lse,
-                                  int *status, cudaStream_t st);
+                                  int *status, cudaStream_t st, bool test_skip_gather = false);
 
 // Split-K sparse attention + combine.
 int sparse_attn_splits(int64_t rows, int H_q, int k, int P);

@@ -473,7 +473,8 @@ lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
         lcsw::sparse_attn_tc_supported(rows, a->H_q, a->d_qk, a->d_v, a->P, a->k)) {
         e = lcsw::launch_sparse_attn_tc(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B,
                                         a->T, a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale,
-                                        a->out, a->lse, w.status, st);
+                                        a->out, a->lse, w.status, st,
+                                        (a->flags & LCSW_PREFILL_TEST_SKIP_GATHER) != 0);
         return cuda_status(e, "prefill attention (tensor cores)");
     }
     e = lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B, a->T,

@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ K, int64_t sK_b,
     const uint16_t *__restrict__ V, int64_t sV_b, const int32_t *__restrict__ seq_len,
     const int32_t *__restrict__ idx, int T, int H_q, int P, int k, int64_t rows,
-    float scale_log2, uint16_t *__restrict__ out, float *__restrict__ lse, int *status) {
+    float scale_log2, uint16_t *__restrict__ out, float *__restrict__ lse, int *status,
+    int test_skip_gather) {
     extern __shared__ unsigned char smem_raw[];
     // the swizzled tiles need 1024-byte alignment
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -271,7 +272,8 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 cp_async_wait<0>();
                 fence_async_smem();  // the copies, for the tensor core's reads
                 __syncwarp();
-                if (lane == 0) bar_arrive(full + slot);
+                // (failure-detection test: the CTA's first item is never handed over)
+                if (lane == 0 && !(test_skip_gather && n_item == 0)) bar_arrive(full + slot);
             }
         }
         cp_async_wait<0>();
@@ -534,7 +536,7 @@ cudaError_t launch_sparse_attn_tc(const uint16_t *q, const uint16_t *K, int64_t 
                                   const uint16_t *V, int64_t sV_b, const int32_t *seq_len,
                                   const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
                                   int P, int k, float scale, uint16_t *out, float *lse,
-                                  int *status, cudaStream_t st) {
+                                  int *status, cudaStream_t st, bool test_skip_gather) {
     const int64_t rows = int64_t(B) * T;
     if (rows == 0) return cudaSuccess;
     if (!sparse_attn_tc_supported(rows, H_q, d_qk, d_v, P, k)) return cudaErrorNotSupported;
@@ -544,7 +546,7 @@ cudaError_t launch_sparse_attn_tc(const uint16_t *q, const uint16_t *K, int64_t 
     const int64_t grid = rows < sm_count() ? rows : sm_count();
     sparse_attn_tc_kernel<<<unsigned(grid), kThr, kSmemBytes, st>>>(
         q, K, sK_b, V, sV_b, seq_len, idx, T, H_q, P, k, rows, scale * 1.4426950408889634f, out,
-        lse, status);
+        lse, status, test_skip_gather ? 1 : 0);
     return cudaGetLastError();
 }
 

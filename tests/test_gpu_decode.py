@@ -242,6 +242,22 @@ def test_prefill_tensor_core_attention_edges(lengths, T, k, H_q, P):
     assert_lse_close(got["lse"], ref["lse"])
 
 
+def test_prefill_tensor_core_attention_bounded_wait_reports_timeout():
+    """The attention's first key chunk is never handed over: the MMA warp's
+    bounded wait runs out, every role stops, the status reads TIMEOUT, and the
+    next call on the same context is correct."""
+    spec = synth.Spec(B=1, lengths=[3000], T=256, prefill=True, H_i=8, k=64, H_q=16, seed=260)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    kp = _cached_part(ref["k_pooled"], c)
+    with pytest.raises(lcsw.LcswError) as ei:
+        run_prefill(c, kp, flags=lcsw.PREFILL_TEST_SKIP_GATHER)
+    assert ei.value.status == lcsw.ERR_TIMEOUT
+    got = run_prefill(c, kp)
+    assert_attn_close(got["out"], ref["out"])
+    assert_lse_close(got["lse"], ref["lse"])
+
+
 def test_prefill_fused_selection_exact_ties():
     # integer keys and queries with dyadic weights: exact scores with many equal
     # values, so the tie rule (lowest group first) decides many selections
