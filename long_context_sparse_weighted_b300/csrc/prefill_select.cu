@@ -37,11 +37,18 @@ __global__ void __launch_bounds__(kSelThreads) thresholds_kernel(
     const int tid = threadIdx.x;
     if (tid == 0) cnt = 0;
     __syncthreads();
+    // a sampled group past the query's visible ones is -inf: key 0, below
+    // every visible key, so the selection below (need <= visible count) never
+    // reaches it and no compaction is needed
     const float *s = samp + row * n_samp;
+    int vis = 0;
     for (int i = tid; i < n_samp; i += kSelThreads) {
         const float v = s[i];
-        if (v > -INFINITY) keys[atomicAdd(&cnt, 1)] = score_key(v);  // visible sampled groups
+        keys[i] = v > -INFINITY ? score_key(v) : 0u;
+        vis += v > -INFINITY;
     }
+    vis = __reduce_add_sync(0xffffffffu, vis);
+    if ((tid & 31) == 0) atomicAdd(&cnt, vis);
     __syncthreads();
     const int s_vis = cnt, nv = max(0, n_valid[row]), kk = min(k, nv);
     uint32_t key = 0u;  // 0: every visible group is a candidate
@@ -51,7 +58,7 @@ __global__ void __launch_bounds__(kSelThreads) thresholds_kernel(
         const long long need = max(1ll, (3ll * kk * s_vis + nv - 1) / nv);
         if (need <= s_vis) {
             unsigned take;
-            key = radix_select_smem(keys, s_vis, unsigned(need), hist, scratch, res, &take);
+            key = radix_select_smem(keys, n_samp, unsigned(need), hist, scratch, res, &take);
         }
     }
     if (tid == 0) thr[row] = key;

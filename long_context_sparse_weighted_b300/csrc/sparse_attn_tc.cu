@@ -64,6 +64,9 @@ constexpr int kGatherWarps = kMmaWarp - kGatherWarp0;
 constexpr int kColS = 0, kColO = 64, kTmemCols = 256;
 constexpr long long kWaitTries = 50000;   // up to 20 us each
 constexpr float kLn2f = 0.6931471805599453f;
+// The softmax reference of a head changes only when a score exceeds it by more
+// than kLazy (log2 units), so p <= 2^kLazy; otherwise a chunk keeps it.
+constexpr float kLazy = 8.f;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // Item i (0-based) of a row with n chunks: (is a value chunk, chunk index).
@@ -165,6 +168,7 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
     float *lsum = alph + 2 * 32;                                          // [2][4][32]
     float *ltot = lsum + 2 * 4 * 32;                                      // [32]
     int *toff = reinterpret_cast<int *>(ltot + 32);           // [kGatherWarps][128]
+    float *mcur = reinterpret_cast<float *>(toff + kGatherWarps * kTok);  // [32] reference
     const int lp2 = 31 - __clz(P);
     const int nck = (k * P + kTok - 1) / kTok;
     const int gpc = kTok >> lp2;  // groups per chunk
@@ -385,6 +389,36 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                     }
                 }
             };
+            // mcur: the row's softmax reference per head, in shared memory
+            // (uniform; only warp 0 writes it, between the slow path's barriers)
+            if (warp == 0) mcur[lane] = -INFINITY;
+            softmax_sync_or(false);
+            unsigned char *pt_base = smem + kSmP;
+            // p = 2^(z - mref) for this token's heads -> its row of P (bf16,
+            // 128B-swizzled MN-major: 8 heads per 16-byte chunk); s: z in, p out
+            auto write_p = [&](uint32_t (&s)[32], unsigned char *pt) {
+#pragma unroll
+                for (int h8 = 0; h8 < kNH / 8; ++h8) {
+                    uint32_t pw[4];
+#pragma unroll
+                    for (int hq = 0; hq < 2; ++hq) {
+                        const int h0 = 8 * h8 + 4 * hq;
+                        const float4 m4 = *reinterpret_cast<const float4 *>(mcur + h0);
+                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                        float pp[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float z = __uint_as_float(s[h0 + e]);
+                            pp[e] = z == -INFINITY ? 0.f : exp2_hw(z - mm[e]);
+                            s[h0 + e] = __float_as_uint(pp[e]);
+                        }
+                        pw[2 * hq] = pack_bf2_rn(pp[0], pp[1]);
+                        pw[2 * hq + 1] = pack_bf2_rn(pp[2], pp[3]);
+                    }
+                    *reinterpret_cast<uint4 *>(pt + sw128_offset(tid, 8 * h8, 1024)) =
+                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                }
+            };
             for (int c = 0; c < nck; ++c) {
                 const uint32_t gc = n_ck + uint32_t(c);
                 const int buf = int(gc & 1u);
@@ -402,66 +436,69 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 const int j = t >> lp2;
                 const int g = j < k ? __ldg(gl + j) : -1;
                 const bool tv = ok && g >= 0 && g < G;
-                float *wrow = wmax + (buf * 4 + warp) * 32;
+                bool exceed = false;  // a score above its head's reference + kLazy
 #pragma unroll
-                for (int h = 0; h < kNH; ++h) {
-                    const float m = warp_max(tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY);
-                    if (lane == 0) wrow[h] = m;
+                for (int h4 = 0; h4 < kNH / 4; ++h4) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(mcur + 4 * h4);
+                    const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = 4 * h4 + e;
+                        const float z = tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY;
+                        s[h] = __float_as_uint(z);
+                        exceed |= z > mm[e] + kLazy;
+                    }
                 }
-                if (softmax_sync_or(!ok)) {
-                    ok = false;
-                    break;
-                }
-                if (warp == 0) {  // lane h: head h's chunk maximum, running maximum, rescale
-                    const float *w4 = wmax + buf * 4 * 32 + lane;
-                    const float cm = fmaxf(fmaxf(w4[0], w4[32]), fmaxf(w4[64], w4[96]));
-                    const float mn = fmaxf(m_run, cm);
-                    const float a = mn == -INFINITY ? 1.f : exp2_hw(m_run - mn);
-                    alph[buf * 32 + lane] = a;
-                    mnew[buf * 32 + lane] = mn;
-                    m_run = mn;
-                    if (c > 0) {  // the previous chunk's sums, then the rescale
+                // P with the current reference (kept unless a score exceeds it)
+                ok = ok && __all_sync(0xffffffffu, wait_phase(pempty + buf, bpar ^ 1u, abort_flag));
+                unsigned char *pt = pt_base + buf * kPBytes;
+                write_p(s, pt);
+                if (softmax_sync_or(exceed || !ok)) {
+                    // a new reference: the exact chunk maximum of every head
+                    // (the scores again from TMEM; the buffer is still held)
+                    if (ok) {
+                        tc_ld32(lane_addr + kColS + buf * kNH, s);
+                        tc_wait_ld();
+                    }
+#pragma unroll
+                    for (int h = 0; h < kNH; ++h)
+                        s[h] = __float_as_uint(tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY);
+                    float *wrow = wmax + (buf * 4 + warp) * 32;
+#pragma unroll
+                    for (int h = 0; h < kNH; ++h) {
+                        const float m = warp_max(__uint_as_float(s[h]));
+                        if (lane == 0) wrow[h] = m;
+                    }
+                    if (softmax_sync_or(!ok)) {
+                        ok = false;
+                        break;
+                    }
+                    if (warp == 0) {  // lane h: head h's new reference and rescale
+                        const float *w4 = wmax + buf * 4 * 32 + lane;
+                        const float cm = fmaxf(fmaxf(w4[0], w4[32]), fmaxf(w4[64], w4[96]));
+                        const float mn = fmaxf(m_run, cm);
+                        const float a = mn == -INFINITY ? 1.f : exp2_hw(m_run - mn);
+                        alph[buf * 32 + lane] = a;
+                        mcur[lane] = mn;
+                        m_run = mn;
+                        if (c > 0) {  // the previous chunk's sums, then the rescale
+                            const float *ls = lsum + (buf ^ 1) * 4 * 32 + lane;
+                            l_run += (ls[0] + ls[32]) + (ls[64] + ls[96]);
+                        }
+                        l_run *= a;
+                    }
+                    softmax_sync_or(false);
+                    write_p(s, pt);
+                } else if (warp == 0) {  // same reference: rescale 1
+                    alph[buf * 32 + lane] = 1.f;
+                    if (c > 0) {
                         const float *ls = lsum + (buf ^ 1) * 4 * 32 + lane;
                         l_run += (ls[0] + ls[32]) + (ls[64] + ls[96]);
                     }
-                    l_run *= a;
-                }
-                softmax_sync_or(false);
-                // p = 2^(z - m) -> this token's row of P (bf16, 128B-swizzled
-                // MN-major: 8 heads per 16-byte chunk); partial sums rescaled
-                ok = ok && __all_sync(0xffffffffu, wait_phase(pempty + buf, bpar ^ 1u, abort_flag));
-                if (ok) {  // the scores again (fewer live registers across the barriers)
-                    tc_ld32(lane_addr + kColS + buf * kNH, s);
-                    tc_wait_ld();
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) bar_arrive(sfree + buf);
-#pragma unroll
-                for (int h = 0; h < kNH; ++h)
-                    s[h] = __float_as_uint(tv ? __uint_as_float(s[h]) * scale_log2 : -INFINITY);
-                unsigned char *pt = smem + kSmP + buf * kPBytes;
-#pragma unroll
-                for (int h8 = 0; h8 < kNH / 8; ++h8) {
-                    uint32_t pw[4];
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int h0 = 8 * h8 + 4 * hh;
-                        const float4 m4 = *reinterpret_cast<const float4 *>(mnew + buf * 32 + h0);
-                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                        float pp[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float z = __uint_as_float(s[h0 + e]);
-                            pp[e] = z == -INFINITY ? 0.f : exp2_hw(z - mm[e]);
-                            s[h0 + e] = __float_as_uint(pp[e]);
-                        }
-                        pw[2 * hh] = pack_bf2_rn(pp[0], pp[1]);
-                        pw[2 * hh + 1] = pack_bf2_rn(pp[2], pp[3]);
-                    }
-                    *reinterpret_cast<uint4 *>(pt + sw128_offset(tid, 8 * h8, 1024)) =
-                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                }
                 fence_async_smem();  // P, for the tensor core's reads
                 __syncwarp();
                 if (lane == 0) bar_arrive(pfull + buf);
