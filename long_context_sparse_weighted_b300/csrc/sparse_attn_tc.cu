@@ -419,10 +419,18 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                         make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 }
             };
+            // the group of this thread's token in chunk c (loaded a chunk ahead)
+            auto group_of = [&](int c) {
+                const int j = (c * kTok + tid) >> lp2;
+                return (c < nck && j < k) ? __ldg(gl + j) : -1;
+            };
+            int g_next = group_of(0);
             for (int c = 0; c < nck; ++c) {
                 const uint32_t gc = n_ck + uint32_t(c);
                 const int buf = int(gc & 1u);
                 const uint32_t bpar = (gc >> 1) & 1u;
+                const int g = g_next;
+                g_next = group_of(c + 1);
                 ok = ok && __all_sync(0xffffffffu, wait_phase(sfull + buf, bpar, abort_flag));
                 tc_fence_after();
                 uint32_t s[32];
@@ -432,9 +440,6 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 }
                 // this thread's token: z = scale * q.k in the log2 domain, or
                 // -inf for padding and groups past the sequence
-                const int t = c * kTok + tid;
-                const int j = t >> lp2;
-                const int g = j < k ? __ldg(gl + j) : -1;
                 const bool tv = ok && g >= 0 && g < G;
                 bool exceed = false;  // a score above its head's reference + kLazy
 #pragma unroll
