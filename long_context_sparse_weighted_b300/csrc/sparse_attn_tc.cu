@@ -20,16 +20,18 @@
 //              row it issues QK_0, then QK_c and PV_(c-1) for c = 1..n-1, then
 //              PV_(n-1); the ring holds the matching item sequence.
 //   warps 0-3  softmax.  Thread t owns TMEM lane t.  Per chunk it reads its
-//              token's head scores; the block takes the exact chunk maximum
-//              of every head (a warp maximum of order-preserving keys, then
-//              the four warps'), and the running maximum m, the rescale
-//              a = 2^(m_old - m_new) and p = 2^(z - m) follow.  Thread t
-//              writes its token's row of P (bf16); the warp's sums of p per
-//              head go to shared memory, and lane h of warp 0 keeps head h's
-//              running sum l = a (l + sum of the previous chunk).  Then the
-//              thread folds O_(c-1)^T (lane t = value dim t) into its running
-//              output row, o = a o + O.  At the row's end the normalised bf16
-//              output and the log-sum-exp are written.
+//              token's head scores z and writes its token's row of P (bf16),
+//              p = 2^(z - m) for the row's reference m of each head.  The
+//              reference is lazy: only when some score exceeds it by more than
+//              kLazy does the block vote to take the exact chunk maximum of
+//              every head (a warp maximum, then the four warps'), move m to
+//              it with the rescale a = 2^(m_old - m_new), and rewrite P; a
+//              row's first chunk always does.  The warp's sums of p per head go
+//              to shared memory, and lane h of warp 0 keeps head h's running
+//              sum l = a (l + sum of the previous chunk).  Then the thread
+//              folds O_(c-1)^T (lane t = value dim t) into its running output
+//              row, o = a o + O.  At the row's end the normalised bf16 output
+//              and the log-sum-exp are written.
 // S and O_c are double-buffered in TMEM (S: columns 0-63, O: 64-191), P in
 // shared memory.  Every hand-off is an mbarrier; every wait is bounded and a
 // wait that runs out stops all roles, which record LCSW_ERR_TIMEOUT in the
@@ -163,8 +165,7 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
     uint32_t *tslot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
     float *wmax = reinterpret_cast<float *>(smem + kSmMisc + 256);        // [2][4][32]
-    float *mnew = reinterpret_cast<float *>(wmax + 2 * 4 * 32);           // [2][32]
-    float *alph = mnew + 2 * 32;                                          // [2][32]
+    float *alph = wmax + 2 * 4 * 32 + 2 * 32;                             // [2][32]
     float *lsum = alph + 2 * 32;                                          // [2][4][32]
     float *ltot = lsum + 2 * 4 * 32;                                      // [32]
     int *toff = reinterpret_cast<int *>(ltot + 32);           // [kGatherWarps][128]
@@ -243,15 +244,6 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 ok = __all_sync(0xffffffffu,
                                 wait_phase(empty + slot, ((n_item / kSlots) & 1u) ^ 1u, abort_flag));
                 if (!ok) break;
-                // first token row of each of the chunk's groups (-1: zero fill);
-                // lane l holds groups l, l + 32, l + 64, l + 96
-                int rb[4];
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const int gi = lane + 32 * qq, j = c * gpc + gi;
-                    const int g = (gi < gpc && j < k) ? __ldg(gl + j) : -1;
-                    rb[qq] = (g >= 0 && g < G) ? g * P : -1;
-                }
                 // every token's row in the chunk (-1: zero fill)
                 int *to = toff + gw * kTok;
 #pragma unroll
