@@ -275,6 +275,11 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
  * query whose kept groups cannot be shown to hold its top k (too few, or more
  * than the per-row capacity) falls back to dense scores and the radix top-k,
  * decided on the device: the result is the same exact top k either way.
+ * With at least 256 query rows (B*T), H_q <= 32 and d_qk = d_v = 128, the
+ * attention runs on the tensor cores: a persistent kernel takes one query row
+ * at a time per SM, without splitting its selected tokens.  Other shapes use
+ * the split-K kernel of lcsw_sparse_attn.  Both give the same result within
+ * the attention tolerance.
  * flags: LCSW_PREFILL_FORCE_FALLBACK sends every query through the fallback
  * (a test of that path).
  *
