@@ -514,11 +514,13 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 lsum[(buf * 4 + warp) * 32 + lane] = __uint_as_float(s[0]);
                 if (c > 0) fold(gc - 1u);
             }
-            if (ok) fold(n_ck + uint32_t(nck) - 1u);
+            // (this barrier also orders warp 0's rescale of the last chunk,
+            // written after the chunk's vote, before the other warps' fold)
             if (softmax_sync_or(!ok)) {
                 ok = false;
                 break;
             }
+            if (ok) fold(n_ck + uint32_t(nck) - 1u);
             if (warp == 0) {  // the last chunk's sums complete the row's
                 const float *ls = lsum + ((n_ck + uint32_t(nck) - 1u) & 1u) * 4 * 32 + lane;
                 const float L = l_run + ((ls[0] + ls[32]) + (ls[64] + ls[96]));
@@ -526,7 +528,10 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
                 if (lse && lane < H_q)
                     lse[row * H_q + lane] = L > 0.f ? (m_run + log2f(L)) * kLn2f : -INFINITY;
             }
-            softmax_sync_or(false);
+            if (softmax_sync_or(!ok)) {  // the fold can give up: leave together
+                ok = false;
+                break;
+            }
             // the normalised output: thread tid is value dim tid of every head
             uint16_t *orow = out + row * int64_t(H_q) * kDim + tid;
 #pragma unroll

@@ -227,9 +227,11 @@ def test_prefill_fused_selection(lengths, T, k, flags):
 # of 128 selected tokens, S and O accumulated in TMEM).  Edges: a sequence
 # with fewer visible groups than k (padded selections), k*P not a multiple of
 # 128 (a partial last chunk), 16 query heads (half of the head tile padded),
-# and P = 2.
+# P = 2, and rows of exactly three chunks (the last chunk's rescale is written
+# after its vote, so the row-end fold must wait for a barrier).
 @pytest.mark.parametrize("lengths,T,k,H_q,P", [([600, 5000], 128, 200, 16, 4),
-                                               ([3000], 256, 70, 32, 2)])
+                                               ([3000], 256, 70, 32, 2),
+                                               ([4000], 256, 80, 32, 4)])
 def test_prefill_tensor_core_attention_edges(lengths, T, k, H_q, P):
     spec = synth.Spec(B=len(lengths), lengths=lengths, T=T, prefill=True, H_i=8, k=k, H_q=H_q,
                       P=P, seed=250 + P)
