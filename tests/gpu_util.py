@@ -1,11 +1,15 @@
 """Helpers shared by the GPU parity tests: upload, tolerance checks.
 
-Tolerances (the arithmetic behind each is stated in the design doc):
-  pooled keys, selected indices, visible counts   bit-exact
+Tolerances, and the arithmetic they come from:
+  pooled keys, selected indices, visible counts   bit-exact (correctly rounded
+                   bf16 of the exact pooled sum; integer work)
   indexer scores   |s_gpu - s_ref| <= 1e-5 * max(1, max_g |s_ref|)  per row
+                   (fp32 accumulation of 64 exact bf16 products against fp64)
   attention out    max |o_gpu - o_ref| <= 2e-2 and
                    ||o_gpu - o_ref||_2 / ||o_ref||_2 <= 1e-2          per (b, t) row
-  lse              |lse_gpu - lse_ref| <= 1e-3 + 1e-4 |lse_ref|
+                   (bf16 probabilities in the value product, fp32 sums,
+                   bf16 output)
+  lse              |lse_gpu - lse_ref| <= 1e-3 + 1e-4 |lse_ref|  (fp32 sums)
 """
 import numpy as np
 import torch
