@@ -119,6 +119,34 @@ def test_decode_workspace_and_validation(L):
     assert L.lcsw_decode_fused(None, None, 0, None) == lcsw.ERR_INVALID_ARG
 
 
+def test_prefill_workspace_and_validation(L):
+    a = lcsw.PrefillArgs()
+    p = 256  # non-null, 256-byte aligned stand-ins: no call below reaches the device
+    for name in ("q_idx", "w_head", "k_pooled", "k_idx", "pool_w", "q", "K", "V", "seq_len",
+                 "out", "lse"):
+        setattr(a, name, p)
+    G, L_tok = 66560, 266240
+    a.sp_b, a.sk_b, a.sw_b, a.sK_b, a.sV_b = G * 64, L_tok * 64, G * 4, L_tok * 128, L_tok * 128
+    a.B, a.T, a.G_max, a.H_i, a.d_idx, a.P, a.k = 1, 4096, G, 8, 64, 4, 512
+    a.H_q, a.d_qk, a.d_v, a.scale = 32, 128, 128, 0.088
+    n = L.lcsw_prefill_workspace_size(ctypes.byref(a))
+    assert n > 4096 * G * 4  # room for dense scores of rows that take the fallback
+    assert L.lcsw_prefill(ctypes.byref(a), ctypes.c_void_p(256), n - 1, None) == lcsw.ERR_WORKSPACE
+    a.H_q = 20  # head counts are 16, 32 or multiples of 64
+    assert L.lcsw_prefill(ctypes.byref(a), ctypes.c_void_p(256), n, None) == lcsw.ERR_INVALID_ARG
+
+
+def test_prefill_binding_rejects_a_small_workspace(L):
+    import torch
+    B, T, H_i, G, P, k, H_q = 1, 64, 8, 256, 4, 16, 16
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        lcsw.prefill(bf(B, T, H_i, 64), torch.zeros(B, T, H_i), bf(B, G, 64), bf(B, G * P, 64),
+                     torch.zeros(B, G, P), bf(B, T, H_q, 128), bf(B, G * P, 128),
+                     bf(B, G * P, 128), torch.full((B,), G * P, dtype=torch.int32), P, k, 0.1,
+                     ws=torch.zeros(16, dtype=torch.uint8))
+
+
 def test_product_package_does_not_reach_the_oracle():
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     pkg = os.path.join(root, "long_context_sparse_weighted_b300")
