@@ -37,6 +37,13 @@ def _declare(lib):
     P, I32, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
     lib.oracle_bf16_from_double.argtypes = [D]
     lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_value.restype = D
+    lib.oracle_e4m3_from_double.argtypes = [D]
+    lib.oracle_e4m3_from_double.restype = ctypes.c_uint8
+    lib.oracle_quantize_rows_e4m3.argtypes = [P, I64, I32, P, P]
+    lib.oracle_index_scores_e4m3.argtypes = [P, P, P, P, P, I64, P, P, I32, I32, I32, I32, I32,
+                                             I64, P]
     lib.oracle_pool_keys.argtypes = [P, I64, P, I64, P, I32, I32, I32, P, I64]
     lib.oracle_visible_counts.argtypes = [P, P, I32, I32, I32, P]
     lib.oracle_index_scores.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, I32, I64, P]
@@ -139,6 +146,47 @@ def index_scores(q_idx, w_head, k_pooled, seq_len, P, q_pos=None):
     out = np.empty((B, T, G_max), np.float32)
     _load().oracle_index_scores(_p(q_idx), _p(w_head), _p(k_pooled), G_max * d, _p(seq_len),
                                 _p(qp), B, T, H_i, d, P, G_max, _p(out))
+    return out
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an e4m3 code (OCP FP8 E4M3; NaN for S.1111.111)."""
+    return _load().oracle_e4m3_value(int(code))
+
+
+def e4m3_from_double(x: float) -> int:
+    """Nearest e4m3 code, ties to the even code, saturating at +-448."""
+    return int(_load().oracle_e4m3_from_double(float(x)))
+
+
+def quantize_rows_e4m3(x):
+    """bf16 rows [..., d] -> (e4m3 codes [..., d] uint8, fp32 scale per row = amax/448)."""
+    x = _c(x, np.uint16)
+    d = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1]))
+    code = np.empty(x.shape, np.uint8)
+    scale = np.empty(x.shape[:-1], np.float32)
+    _load().oracle_quantize_rows_e4m3(_p(x), rows, d, _p(code), _p(scale))
+    return code, scale
+
+
+def index_scores_e4m3(cq, sq, w_head, ck, sk, seq_len, P, q_pos=None):
+    """FP8 indexer score: sum_h w_h relu(sq_h sk_g sum_i v(cq) v(ck)); -inf if not visible.
+
+    cq [B][T][H_i][d] and ck [B][G_max][d] are e4m3 codes with one fp32 scale
+    per row (sq [B][T][H_i], sk [B][G_max])."""
+    cq = _c(cq, np.uint8)
+    ck = _c(ck, np.uint8)
+    sq = _c(sq, np.float32)
+    sk = _c(sk, np.float32)
+    w_head = _c(w_head, np.float32)
+    seq_len = _c(seq_len, np.int32)
+    B, T, H_i, d = cq.shape
+    G_max = ck.shape[1]
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    out = np.empty((B, T, G_max), np.float32)
+    _load().oracle_index_scores_e4m3(_p(cq), _p(sq), _p(w_head), _p(ck), _p(sk), G_max * d,
+                                     _p(seq_len), _p(qp), B, T, H_i, d, P, G_max, _p(out))
     return out
 
 

@@ -307,3 +307,96 @@ void oracle_retrieval_step(const uint16_t *q_idx, const float *w_head,
                        out, lse);
     free(n_valid);
 }
+
+/* ---------------------------------------------------------------- FP8 --- */
+/*
+ * FP8 pooled indexer keys and queries (a next step of the path, not yet on
+ * the GPU).  The pages say only that the serving stack quantizes its caches
+ * per tier to INT8, FP8 or BF16 (reading notes, section "The serving stack";
+ * G2C Brief, section "Serving: the architecture is only half the efficiency
+ * claim").  Format and scaling here are readings:
+ *   e4m3   the OCP 8-bit float E4M3: sign, 4 exponent bits (bias 7), 3
+ *          mantissa bits, no infinities, S.1111.111 is NaN; largest finite
+ *          magnitude 448 = 1.75 * 2^8, smallest normal 2^-6, subnormals
+ *          m * 2^-9 (m = 1..7).
+ *   round  to the nearest representable value, ties to the even code,
+ *          saturating at +-448.
+ *   scale  one per 64-element row: amax / 448 rounded to fp32 (0 for an
+ *          all-zero row); code_i = e4m3(x_i / scale).
+ *   score  s = sum_h w_h * max(0, sq_h * sk_g * sum_i v(cq_hi) * v(ck_gi)),
+ *          every step in double, rounded once to fp32, with the visibility
+ *          rule of the bf16 score.
+ */
+double oracle_e4m3_value(uint8_t c)
+{
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* exhaustive nearest over the 127 codes 0x00..0x7E (0 .. 448) */
+uint8_t oracle_e4m3_from_double(double x)
+{
+    const uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 0x80 : 0x00;
+    const double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    uint8_t best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double d = fabs(oracle_e4m3_value((uint8_t)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            bd = d;
+            best = (uint8_t)c;
+        }
+    }
+    return sign | best;
+}
+
+void oracle_quantize_rows_e4m3(const uint16_t *x, int64_t rows, int d, uint8_t *code, float *scale)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * d;
+        double amax = 0.0;
+        for (int i = 0; i < d; ++i) {
+            const double a = fabs(bf16_value(xr[i]));
+            if (a > amax) amax = a;
+        }
+        const float sc = (float)(amax / 448.0);
+        scale[r] = sc;
+        for (int i = 0; i < d; ++i)
+            code[r * d + i] = sc == 0.0f ? 0 : oracle_e4m3_from_double(bf16_value(xr[i]) / (double)sc);
+    }
+}
+
+void oracle_index_scores_e4m3(const uint8_t *cq, const float *sq, const float *w_head,
+                              const uint8_t *ck, const float *sk, int64_t sp_b,
+                              const int32_t *seq_len, const int32_t *q_pos,
+                              int B, int T, int H_i, int d, int P, int64_t G_max, float *scores)
+{
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < T; ++t) {
+            const int64_t n = visible_groups(seq_len, q_pos, b, T, t, P);
+            const int64_t bt = (int64_t)b * T + t;
+            float *st = scores + bt * G_max;
+            for (int64_t g = 0; g < G_max; ++g) {
+                if (g >= n) {
+                    st[g] = -INFINITY;
+                    continue;
+                }
+                const int64_t kr = (b * sp_b) / d + g;  /* the key's row */
+                double s = 0.0;
+                for (int h = 0; h < H_i; ++h) {
+                    const int64_t qr = bt * H_i + h;
+                    double dot = 0.0;
+                    for (int i = 0; i < d; ++i)
+                        dot += oracle_e4m3_value(cq[qr * d + i]) * oracle_e4m3_value(ck[kr * d + i]);
+                    dot *= (double)sq[qr] * (double)sk[kr];
+                    s += (double)w_head[qr] * (dot > 0.0 ? dot : 0.0);
+                }
+                const float f = (float)s;
+                st[g] = (f == 0.0f) ? 0.0f : f;
+            }
+        }
+    }
+}

@@ -1,0 +1,113 @@
+"""Pins of the oracle's FP8 leg (e4m3 codes, per-row scales, FP8 indexer score).
+
+The encodings below are worked out by hand from the OCP E4M3 definition
+(bias 7, 3 mantissa bits, no infinities, largest finite 448); the reading
+adds round-to-nearest with ties to the even code and saturation at +-448.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+# (value, code): normals, subnormals, the largest finite, signs, ties, saturation
+HAND = [
+    (1.0, 0x38),            # 0 0111 000
+    (448.0, 0x7E),          # 1.75 * 2^8
+    (2.0 ** -6, 0x08),      # smallest normal
+    (2.0 ** -9, 0x01),      # smallest subnormal
+    (7 * 2.0 ** -9, 0x07),  # largest subnormal
+    (-2.0, 0xC0),
+    (1.0625, 0x38),         # halfway 1.0 / 1.125 -> even mantissa 0
+    (1.1875, 0x3A),         # halfway 1.125 / 1.25 -> even mantissa 2
+    (3 * 2.0 ** -10, 0x02),  # halfway 2^-9 / 2^-8 -> even code
+    (2.0 ** -11, 0x00),     # below half the smallest subnormal
+    (500.0, 0x7E),          # saturates
+    (-1e9, 0xFE),
+    (0.0, 0x00),
+    (-0.0, 0x80),
+]
+
+
+@pytest.mark.parametrize("x,code", HAND)
+def test_e4m3_hand_encodings(x, code):
+    assert oracle.e4m3_from_double(x) == code
+
+
+def test_e4m3_values_round_trip_and_increase():
+    vals = [oracle.e4m3_value(c) for c in range(0x7F)]
+    assert all(b > a for a, b in zip(vals, vals[1:]))
+    assert vals[-1] == 448.0 and np.isnan(oracle.e4m3_value(0x7F))
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert oracle.e4m3_from_double(oracle.e4m3_value(c)) == c
+
+
+def test_e4m3_matches_an_independent_conversion_in_range():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.uniform(-448, 448, 3000), rng.normal(0, 1e-2, 3000),
+                        rng.normal(0, 1.0, 3000)])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_double(v) for v in x], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_quantize_rows_bounds():
+    rng = np.random.default_rng(6)
+    x = synth.bf16_bits(rng.normal(0, 3, (64, 64)).astype(np.float32))
+    x[3] = 0  # an all-zero row
+    code, scale = oracle.quantize_rows_e4m3(x)
+    xv = synth.bf16_to_f32(x).astype(np.float64)
+    assert scale[3] == 0 and not code[3].any()
+    amax = np.abs(xv).max(axis=1)
+    nz = amax > 0
+    assert np.allclose(scale[nz], (amax[nz] / 448).astype(np.float32), rtol=0, atol=0)
+    deq = np.vectorize(oracle.e4m3_value)(code).astype(np.float64) * scale[:, None]
+    # within half an e4m3 step: 2^-4 relative for normals, 2^-10 * scale absolute below
+    assert (np.abs(deq - xv) <= 2.0 ** -4 * np.abs(xv) + 2.0 ** -10 * scale[:, None]).all()
+    # the row maximum lands on +-448 exactly
+    arg = np.abs(xv).argmax(axis=1)
+    assert (np.abs(deq[nz, arg[nz]]) == 448.0 * scale[nz].astype(np.float64)).all()
+
+
+def _exact_case(rng, B, T, H_i, G, d=64):
+    """Rows of e4m3-representable values whose maximum is 448 (scale exactly 1)."""
+    def rows(n):
+        c = rng.integers(0, 0x7E, (n, d)).astype(np.uint8) | rng.integers(0, 2, (n, d)).astype(
+            np.uint8) << 7
+        c[np.arange(n), rng.integers(0, d, n)] = 0x7E
+        v = np.vectorize(oracle.e4m3_value)(c).astype(np.float32)
+        return synth.bf16_bits(v)
+    q = rows(B * T * H_i).reshape(B, T, H_i, d)
+    k = rows(B * G).reshape(B, G, d)
+    return q, k
+
+
+def test_fp8_score_with_unit_scales_equals_the_bf16_score():
+    rng = np.random.default_rng(7)
+    B, T, H_i, G, P = 2, 3, 4, 40, 4
+    q, k = _exact_case(rng, B, T, H_i, G)
+    w = rng.uniform(0, 1, (B, T, H_i)).astype(np.float32)
+    seq = np.array([G * P, (G - 7) * P], np.int32)
+    cq, sq = oracle.quantize_rows_e4m3(q)
+    ck, sk = oracle.quantize_rows_e4m3(k)
+    assert (sq == 1).all() and (sk == 1).all()
+    got = oracle.index_scores_e4m3(cq, sq, w, ck, sk, seq, P)
+    ref = oracle.index_scores(q, w, k, seq, P)
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_score_follows_the_key_scale():
+    rng = np.random.default_rng(8)
+    B, T, H_i, G, P = 1, 2, 4, 16, 4
+    q, k = _exact_case(rng, B, T, H_i, G)
+    w = rng.uniform(0, 1, (B, T, H_i)).astype(np.float32)
+    seq = np.array([G * P], np.int32)
+    cq, sq = oracle.quantize_rows_e4m3(q)
+    ck, sk = oracle.quantize_rows_e4m3(k)
+    base = oracle.index_scores_e4m3(cq, sq, w, ck, sk, seq, P)
+    k2 = synth.bf16_bits(synth.bf16_to_f32(k) * np.float32(1.0 / 64))  # exact power of two
+    ck2, sk2 = oracle.quantize_rows_e4m3(k2)
+    assert np.array_equal(ck2, ck) and np.array_equal(sk2, sk / 64)
+    got = oracle.index_scores_e4m3(cq, sq, w, ck2, sk2, seq, P)
+    assert np.array_equal(got, (base.astype(np.float64) / 64).astype(np.float32))

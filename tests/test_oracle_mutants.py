@@ -10,6 +10,7 @@ import inspect
 import pytest
 
 import oracle
+import test_oracle_fp8 as fp8_pins
 import test_oracle_pins as pins
 
 MUTANTS = {
@@ -34,6 +35,56 @@ MUTANTS = {
                               "const uint16_t *vj = K + b * sK_b + tok[j] * d_qk;"),
     "attn_lse_sign": ("*lh = (float)(m + log(l));", "*lh = (float)(m - log(l));"),
 }
+
+
+# the FP8 leg (e4m3 codes, per-row scales, FP8 score), caught by test_oracle_fp8
+FP8_MUTANTS = {
+    "e4m3_exponent_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "e4m3_ties_to_odd": ("(d == bd && (c & 1) == 0)", "(d == bd && (c & 1) == 1)"),
+    "e4m3_no_saturation": ("if (a >= 448.0) return sign | 0x7E;",
+                           "if (a >= 448.0) return sign | 0x7F;"),
+    "e4m3_sign_lost": ("    return sign | best;", "    return best;"),
+    "quantize_scale_not_applied": ("oracle_e4m3_from_double(bf16_value(xr[i]) / (double)sc)",
+                                   "oracle_e4m3_from_double(bf16_value(xr[i]))"),
+    "fp8_score_drops_key_scale": ("dot *= (double)sq[qr] * (double)sk[kr];",
+                                  "dot *= (double)sq[qr];"),
+    "fp8_score_no_relu": ("s += (double)w_head[qr] * (dot > 0.0 ? dot : 0.0);",
+                          "s += (double)w_head[qr] * dot;"),
+}
+
+
+def _fp8_pin_calls():
+    calls = [(f"hand_{x}", lambda x=x, c=c: fp8_pins.test_e4m3_hand_encodings(x, c))
+             for x, c in fp8_pins.HAND]
+    for name, fn in inspect.getmembers(fp8_pins, inspect.isfunction):
+        if name.startswith("test_") and not inspect.signature(fn).parameters:
+            calls.append((name, fn))
+    return calls
+
+
+@pytest.mark.parametrize("mutant", sorted(FP8_MUTANTS))
+def test_fp8_pins_catch_planted_mistake(mutant, tmp_path):
+    old, new = FP8_MUTANTS[mutant]
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation anchor not unique/absent: {mutant}"
+    so = str(tmp_path / f"oracle_{mutant}.so")
+    oracle.compile_variant(src.replace(old, new), so)
+    caught = []
+    with oracle.use_library(so):
+        for name, call in _fp8_pin_calls():
+            try:
+                call()
+            except Exception:
+                caught.append(name)
+    assert caught, f"no FP8 pin caught mutant {mutant}"
+
+
+def test_unmutated_copy_passes_every_fp8_pin(tmp_path):
+    so = str(tmp_path / "oracle_copy_fp8.so")
+    oracle.compile_variant(oracle.source(), so)
+    with oracle.use_library(so):
+        for name, call in _fp8_pin_calls():
+            call()
 
 
 def _pin_calls():
