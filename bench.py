@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the decode_b8 / ragged_b64 / prefill_4k entries of the line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--copies", type=int, default=0,
                     help="rotated input copies (0: enough to exceed 3x L2)")
@@ -70,6 +72,36 @@ def alg_bytes(lengths, P, H_i, d_idx, k, H_q, d_qk, d_v):
         tot += G * d_idx * 2 + P * min(k, G) * (d_qk + d_v) * 2 + H_q * (d_qk + d_v) * 2 \
             + H_i * (d_idx * 2 + 4)
     return tot
+
+
+def l2_bytes():
+    """L2 size of the current device (the nominal 126 MB where none is visible)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    except Exception:
+        pass
+    return 126 * 1024 * 1024
+
+
+def workload_config(spec, workload, L2, world=1):
+    """(rotated copies, config dict) of a decode workload; the same dict in both arms."""
+    ab = alg_bytes(spec.lengths, spec.P, spec.H_i, spec.d_idx, spec.k, spec.H_q, spec.d_qk,
+                   spec.d_v)
+    copies = max(2, math.ceil(3 * L2 / ab))
+    cfg = {"workload": workload, "batch": spec.B, "context": max(spec.lengths),
+           "pooled_groups": sum(L // spec.P for L in spec.lengths), "pool": spec.P,
+           "topk_groups": spec.k, "indexer_heads": spec.H_i, "query_heads": spec.H_q,
+           "d_qk": spec.d_qk, "d_v": spec.d_v,
+           "l2_policy": f"{copies} rotated input copies, {copies * ab / 1e6:.0f} MB touched per "
+                        f"rotation > 3x L2 ({L2 / 1e6:.0f} MB)",
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    return copies, cfg
+
+
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
 
 # ------------------------------------------------------------------ clocks --
@@ -242,8 +274,11 @@ def time_graph_steps(torch, decs, steps, warmup, world):
     full, tail = divmod(steps, gs)
     g_full = capture(gs) if full else None
     g_tail = capture(tail)
-    if g_full is not None:
-        g_full.replay()
+    # one untimed replay of every captured graph (uploads it and warms the
+    # path), so the timed region holds warm launches only
+    for g in (g_full, g_tail):
+        if g is not None:
+            g.replay()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -292,7 +327,9 @@ def run_lcsw(args, world, rank, local):
     B = spec.B
     L2 = torch.cuda.get_device_properties(local).L2_cache_size
     ab = alg_bytes(spec.lengths, P, spec.H_i, spec.d_idx, k, spec.H_q, spec.d_qk, spec.d_v)
-    copies = args.copies if args.copies > 0 else max(2, math.ceil(3 * L2 / ab))
+    copies, config = workload_config(spec, args.workload, L2, world)
+    if args.copies > 0:
+        copies = args.copies
 
     # -- build the pooled cache on the device (K1) and time it --------------
     pool_info = {}
@@ -367,14 +404,7 @@ def run_lcsw(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded, generated on the host; no dataset or weights)",
-            "config": {"workload": args.workload, "batch": B, "context": max(spec.lengths),
-                       "pooled_groups": sum(L // P for L in spec.lengths), "pool": P,
-                       "topk_groups": k, "indexer_heads": spec.H_i, "query_heads": spec.H_q,
-                       "d_qk": spec.d_qk, "d_v": spec.d_v,
-                       "l2_policy": f"{copies} rotated input copies, "
-                                    f"{copies * ab / 1e6:.0f} MB touched per rotation > 3x L2 "
-                                    f"({L2 / 1e6:.0f} MB)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": config,
             "alg_bytes_per_step": ab,
             "hbm_gbs": round(ab * world / (step_ms / 1e3) / 1e9, 1),
             "frac_of_8tbs": round(ab / (step_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
@@ -384,6 +414,10 @@ def run_lcsw(args, world, rank, local):
         line["ablation_pool1"] = ablation
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(c, args.cpu_seconds)
+    if rank == 0 and not args.no_per_config and args.workload == "decode_1m":
+        del decs, keep
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config(args, torch, lcsw, peak, peaks)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -505,9 +539,10 @@ def cpu_baseline(c, seconds):
         dt = time.perf_counter() - t0
         if dt >= seconds or n >= 200:
             break
-    return {"value": round(c["B"] * n / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": round(c["B"] * n / dt, 3), "unit": UNIT, "cores": 1,
+            "host_cores": host_cores(), "kind": "oracle",
             "sample": f"{n} full decode steps of the workload (score all groups, top-k, "
-                      f"attention), single thread, {dt:.1f} s"}
+                      f"attention), single thread of {host_cores()} host cores, {dt:.1f} s"}
 
 
 def run_reference(args, world, rank):
@@ -556,10 +591,9 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, generated on the host)", "impl": "reference",
-            "config": {"workload": args.workload, "batch": spec.B,
-                       "context": max(spec.lengths), "pool": P, "topk_groups": k},
+            "config": workload_config(spec, args.workload, l2_bytes(), world)[1],
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
-                             "kind": "oracle",
+                             "host_cores": host_cores(), "kind": "oracle",
                              "sample": f"per step: scores+top-k over {g_s} of {max(G)} groups "
                                        f"(extrapolated linearly) + attention over the full "
                                        f"top-{k} selection; single thread"},
@@ -618,10 +652,13 @@ def run_prefill_scores(args):
         "bound_ms": round(max(flops / tf_peak / 1e9, bytes_ / hbm_peak / 1e6), 5)}))
 
 
-def run_prefill_chunk(args):
+def measure_prefill_chunk(steps, warmup, peaks, oracle_rows=0):
     """One chunked-prefill call on prefill_4k: pool the chunk's new groups,
     score every visible group, select the top k per query (fused with the
-    scoring) and run the sparse attention, on resident device inputs."""
+    scoring) and run the sparse attention, on resident device inputs.
+    With oracle_rows > 0 the oracle also runs that many sampled query rows
+    (the CPU leg: timed, extrapolated to the chunk, and compared with the
+    chunk's output on those rows)."""
     import torch
 
     import long_context_sparse_weighted_b300 as lcsw
@@ -640,27 +677,156 @@ def run_prefill_chunk(args):
     qi, w = up16(c["q_idx"]), torch.from_numpy(c["w_head"]).cuda()
     q, K, V = up16(c["q"]), up16(c["K"]), up16(c["V"])
     idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, T, spec.H_q, spec.d_v, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, T, spec.H_q, dtype=torch.float32, device="cuda")
     run = lambda check=False: lcsw.prefill(qi, w, kp, k_idx, pool_w, q, K, V, seq, P, k,
-                                           c["scale"], idx_out=idx, check=check)
+                                           c["scale"], out=out, lse=lse, idx_out=idx,
+                                           check=check)
     run(True)  # status checked once; the timed calls do not synchronise
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         run()
     torch.cuda.synchronize()
-    steps = min(args.steps, 50)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        run()
-    e1.record()
-    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     run(True)
-    print(json.dumps({
+    # algorithmic work: every (query, visible group) pair of the indexer, all
+    # heads; attention over P*k tokens per query row, QK^T and PV
+    G_vis = np.minimum(int(c["seq_len"][0]) // P, (c["q_pos"][0].astype(np.int64) + 1) // P)
+    f_score = 2.0 * float(G_vis.sum()) * spec.H_i * spec.d_idx
+    f_attn = 2.0 * B * T * spec.H_q * P * k * (spec.d_qk + spec.d_v)
+    tf = (f_score + f_attn) / (ms / 1e3) / 1e12
+    tf_peak = peaks.get("bf16_tflops", 1800.0)
+    entry = {
         "kernel": "lcsw_prefill (pool, fused top-k selection, sparse attention)",
-        "workload": "prefill_4k", "shape": {"B": B, "T": T, "G_max": G_max, "k": k,
-                                            "H_i": spec.H_i, "H_q": spec.H_q},
+        "shape": {"B": B, "T": T, "cached_tokens": int(c["seq_len"][0]) - T, "G_max": G_max,
+                  "k": k, "H_i": spec.H_i, "H_q": spec.H_q},
         "ms_per_chunk": round(ms, 4), "queries_per_s": round(B * T / (ms / 1e3), 1),
-        "steps": steps}))
+        "steps": steps, "clocks": clk.summary(),
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": tf_peak,
+                     "peak_source": "measured bf16 burst" if "bf16_tflops" in peaks
+                     else "fallback", "unit": "TFLOP/s", "frac": round(tf / tf_peak, 4),
+                     "alg_flops_per_chunk": f_score + f_attn, "alg_flops_scoring": f_score,
+                     "alg_flops_attention": f_attn}}
+    if oracle_rows:
+        import oracle
+        kp_o = oracle.pool_keys(c["k_idx"], c["pool_w"], c["seq_len"], P)
+        rng = np.random.default_rng(4)
+        ts = np.sort(rng.choice(T, oracle_rows, replace=False))
+        t0 = time.perf_counter()
+        ref = oracle.retrieval_step(c["q_idx"][:, ts], c["w_head"][:, ts], kp_o, c["q"][:, ts],
+                                    c["K"], c["V"], c["seq_len"], P, k, c["scale"],
+                                    q_pos=c["q_pos"][:, ts])
+        dt = time.perf_counter() - t0
+        got_idx = idx.cpu().numpy()[:, ts]
+        entry["cpu_baseline"] = {
+            "ms_per_chunk_extrapolated": round(dt * 1e3 * T / oracle_rows, 1),
+            "queries_per_s": round(oracle_rows / dt, 3), "cores": 1, "host_cores": host_cores(),
+            "kind": "oracle", "sample": f"{oracle_rows} sampled query rows of the chunk "
+                                       f"(score every visible group, top-k, attention), "
+                                       f"single thread, {dt:.1f} s; x{T}/{oracle_rows} "
+                                       f"extrapolated"}
+        entry["parity_sampled_rows"] = dict(
+            _attn_parity(out.view(torch.int16).cpu().numpy().view(np.uint16)[:, ts], ref["out"],
+                         lse.cpu().numpy()[:, ts], ref["lse"]),
+            idx_equal=bool(np.array_equal(got_idx, ref["idx"])))
+    return entry
+
+
+def _attn_parity(out_bits, ref_bits, lse, ref_lse):
+    """Output and lse of the GPU against the oracle, under the parity tolerances
+    (max abs <= 2e-2 and relative L2 <= 1e-2 per row; lse within 1e-3 + 1e-4|lse|)."""
+    g = synth.bf16_to_f32(out_bits).astype(np.float64)
+    r = synth.bf16_to_f32(ref_bits).astype(np.float64)
+    g = g.reshape(-1, g.shape[-1])
+    r = r.reshape(-1, r.shape[-1])
+    max_abs = float(np.abs(g - r).max())
+    rel = float((np.linalg.norm(g - r, axis=1) / np.maximum(np.linalg.norm(r, axis=1),
+                                                            1e-30)).max())
+    fin = np.isfinite(ref_lse)
+    lerr = float(np.abs(lse[fin].astype(np.float64) - ref_lse[fin]).max()) if fin.any() else 0.0
+    ok = (max_abs <= 2e-2 and rel <= 1e-2 and
+          bool((np.abs(lse[fin] - ref_lse[fin]) <= 1e-3 + 1e-4 * np.abs(ref_lse[fin])).all()))
+    return {"max_abs": round(max_abs, 6), "rel_l2": round(rel, 6), "lse_max_err": round(lerr, 6),
+            "within_tolerance": ok}
+
+
+def measure_decode_config(torch, lcsw, name, steps, peak, with_oracle):
+    """The decode step on another named workload, timed like the headline (CUDA
+    graphs over rotated input copies, warm), with its HBM roofline; with_oracle
+    adds the oracle's time for one full step and the parity of the GPU step's
+    output against it."""
+    spec = synth.named(name)
+    c = synth.generate(spec)
+    P, k, B = spec.P, spec.k, spec.B
+    copies, cfg = workload_config(spec, name, l2_bytes())
+    ab = alg_bytes(spec.lengths, P, spec.H_i, spec.d_idx, k, spec.H_q, spec.d_qk, spec.d_v)
+
+    def kp_builder(k_idx, pool_w, seq):
+        kp = torch.zeros(B, spec.G_max, spec.d_idx, dtype=torch.bfloat16, device="cuda")
+        lcsw.pool_keys(k_idx, pool_w, seq, P, kp)
+        return kp
+
+    decs, keep = make_decoders(lcsw, torch, c, copies, P, k, kp_builder)
+    ms, clocks = time_graph_steps(torch, decs, steps, 5, 1)
+    step_ms = ms / steps
+    gbs = ab / (step_ms / 1e3) / 1e9
+    entry = {"tokens_per_s": round(B * steps / (ms / 1e3), 1), "ms_per_step": round(step_ms, 6),
+             "steps": steps, "config": cfg, "alg_bytes_per_step": ab,
+             "roofline": {"bound": "hbm", "kernel": "lcsw_decode_fused (persistent kernel)",
+                          "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(gbs / peak, 4),
+                          "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)},
+             "launches_per_step": decs[0].launches_per_call, "clocks": clocks}
+    if with_oracle:
+        import oracle
+        out, lse = decs[0]()
+        torch.cuda.synchronize()
+        out_bits = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        lse_h = lse.cpu().numpy()
+        del decs, keep
+        torch.cuda.empty_cache()
+        kp = oracle.pool_keys(c["k_idx"], c["pool_w"], c["seq_len"], P)
+        t0 = time.perf_counter()
+        ref = oracle.retrieval_step(c["q_idx"], c["w_head"], kp, c["q"], c["K"], c["V"],
+                                    c["seq_len"], P, k, c["scale"])
+        dt = time.perf_counter() - t0
+        entry["cpu_baseline"] = {"value": round(B / dt, 3), "unit": UNIT, "cores": 1,
+                                 "host_cores": host_cores(), "kind": "oracle",
+                                 "sample": f"one full decode step (score all groups, top-k, "
+                                           f"attention), single thread, {dt:.1f} s"}
+        entry["parity"] = _attn_parity(out_bits, ref["out"][:, 0], lse_h, ref["lse"][:, 0])
+    else:
+        del decs, keep
+        torch.cuda.empty_cache()
+    return entry
+
+
+def per_config(args, torch, lcsw, peak, peaks):
+    """The other named workloads, measured in the same run (entries of the one
+    JSON line; the headline stays decode_1m)."""
+    res = {}
+    oracle_on = not args.no_cpu_baseline
+    for name, steps in (("decode_b8", 2000), ("ragged_b64", 1000)):
+        res[name] = measure_decode_config(torch, lcsw, name, steps, peak, oracle_on)
+    res["prefill_4k"] = measure_prefill_chunk(20, 3, peaks, oracle_rows=16 if oracle_on else 0)
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_prefill_chunk(args):
+    """`--kernel prefill`: one chunked-prefill chunk of prefill_4k, timed alone."""
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    entry = measure_prefill_chunk(min(args.steps, 50), args.warmup, peaks)
+    print(json.dumps(dict(entry, workload="prefill_4k")))
 
 
 def main():

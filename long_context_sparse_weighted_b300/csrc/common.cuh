@@ -140,4 +140,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
 // Budget for device-side spin waits, in SM clock cycles (~0.5 s at 2 GHz).
 constexpr long long kSpinBudget = 1000000000LL;
 
+// Nanoseconds of the GPU-wide global timer (comparable across SMs).
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Budget for a wait on an mbarrier (tensor-core completion, bulk copies), in
+// nanoseconds of the global timer: about one second.
+constexpr unsigned long long kWaitNs = 1000000000ull;
+
 }  // namespace lcsw

@@ -71,7 +71,6 @@ constexpr int kTieCap = 256;       // threshold-bin candidates resolved by rank 
 constexpr int kMaxK = 2048;        // selected groups per sequence
 constexpr int kCtlWords = 32;      // control words per sequence
 constexpr int kMaxCtas = 160;
-constexpr long long kMbarBudget = 50000;  // tries (up to 20 us each) of a tensor-core wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -175,8 +174,8 @@ struct Params {
 };
 
 // ------------------------------------------------------------ phase timers -
-// Built with -DLCSW_PHASE_TIMERS, block 0 thread 0 of every block records the
-// first and last %globaltimer reading of each phase mark across blocks.
+// Built with -DLCSW_PHASE_TIMERS, thread 0 of every block records the
+// %globaltimer reading (ns, comparable across SMs) at each phase mark.
 #ifdef LCSW_PHASE_TIMERS
 __device__ long long g_stamp[160][40];
 __device__ unsigned g_dbg_max[4];
@@ -186,7 +185,7 @@ __device__ unsigned g_dbg_max[4];
     } while (0)
 #define PHASE_MARK(i)                                                    \
     do {                                                                 \
-        if (threadIdx.x == 0) g_stamp[blockIdx.x][i] = clock64();        \
+        if (threadIdx.x == 0) g_stamp[blockIdx.x][i] = (long long)globaltimer_ns();        \
     } while (0)
 #else
 #define PHASE_MARK(i) \
@@ -743,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     for (int kk = 0; kk < n_mine; ++kk) {
         const int slot = kk % kRing, t = warp + kk * kStream;
         if (stream_ok &&
-            !__all_sync(0xffffffffu, mbar_wait(wbar + slot, unsigned(kk / kRing) & 1u, kMbarBudget))) {
+            !__all_sync(0xffffffffu, mbar_wait(wbar + slot, unsigned(kk / kRing) & 1u, kWaitNs))) {
             stream_ok = false;  // warp-uniform: score_tile shuffles across the warp
             raise_timeout(p, 7);
             sv[19] = 1;
@@ -778,9 +777,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             for (int i = 0; i < kRing; ++i)
                 asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(wbar + i))
                              : "memory");
-        } else {  // let the copies in flight land before the block leaves (bounded)
+        } else {  // the copies in flight land before the block leaves or reuses the ring
             for (int kk = max(0, n_issued - kRing); kk < n_issued; ++kk)
-                mbar_wait(wbar + kk % kRing, unsigned(kk / kRing) & 1u, 100);
+                mbar_wait(wbar + kk % kRing, unsigned(kk / kRing) & 1u, kWaitNs);
         }
     }
     PHASE_MARK(4);
@@ -1236,7 +1235,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         // level 1: the full 16-bit-bin histogram of every block's scores.  The
         // speculative S product reads shared memory about to be reused: wait
         // for it first.
-        const bool s_done = n_s == 0 || mbar_wait(bars, 0, kMbarBudget);
+        const bool s_done = n_s == 0 || mbar_wait(bars, 0, kWaitNs);
         if (!__syncthreads_and(s_done)) {
             raise_timeout(p, 3);
             release_tmem();
@@ -1423,7 +1422,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         float m = -INFINITY, lp = 0.f;  // running max; sum of this warpgroup's columns
         // a parity wait only tells the last two phases apart: let the unused
         // speculative product complete before new ones are issued
-        bool ok = use_spec || n_s == 0 || __all_sync(0xffffffffu, mbar_wait(bars, 0, kMbarBudget));
+        bool ok = use_spec || n_s == 0 || __all_sync(0xffffffffu, mbar_wait(bars, 0, kWaitNs));
         for (int ci = 0; ci < nchunks; ++ci) {
             const int buf = ci & 1;
             unsigned char *tk = use_spec ? smem + kSpec : gbuf + buf * kv_tile_bytes<DQK, DV>();
@@ -1448,7 +1447,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             const unsigned long long vmask =
                 (unsigned long long)__ballot_sync(0xffffffffu, cg[lane >> lp2] >= 0) |
                 ((unsigned long long)__ballot_sync(0xffffffffu, cg[(lane + 32) >> lp2] >= 0) << 32);
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(bars, (n_s - 1) & 1, kMbarBudget));
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(bars, (n_s - 1) & 1, kWaitNs));
             tc_fence_after();
             PHASE_MARK(25);
             float al = 0.f;
@@ -1505,7 +1504,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 }
                 __syncwarp();
             }
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(bars + 1, ci & 1, kMbarBudget));
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(bars + 1, ci & 1, kWaitNs));
             tc_fence_after();
             PHASE_MARK(27);
             if (ok) {

@@ -36,7 +36,6 @@ constexpr int kTN = 128;        // groups per tile
 constexpr int kThr = 256;       // threads per CTA
 constexpr int kTile = 16384;    // one 128-row x 128-byte operand tile
 constexpr int kSmem = 3 * kTile + 1024;  // group tile, two query tiles, barriers
-constexpr long long kWaitBudget = 50000;  // tries of up to 20 us
 constexpr unsigned kIdesc = idesc_bf16_f32(kTM, kTN, false, false);
 
 __global__ void __launch_bounds__(kThr, 2)
@@ -111,8 +110,8 @@ __global__ void __launch_bounds__(kThr, 2)
         if (warp != 1) return;
         bool good = true;
         if (elect_one()) {
-            good = (h > 0 || mbar_wait(bars, 0, kWaitBudget)) &&
-                   mbar_wait(bars + 1 + (h & 1), (h >> 1) & 1, kWaitBudget);
+            good = (h > 0 || mbar_wait(bars, 0, kWaitNs)) &&
+                   mbar_wait(bars + 1 + (h & 1), (h >> 1) & 1, kWaitNs);
             if (good) {
                 tc_fence_after();
                 const uint32_t qa = smem_u32(sq + (h & 1) * kTile), ka = smem_u32(sk);
@@ -130,7 +129,7 @@ __global__ void __launch_bounds__(kThr, 2)
     for (int h = 0; h < H_i; ++h) {
         if (h + 1 < H_i) issue(h + 1);
         const float wh = __ldg(wrow + h);
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(bars + 3 + (h & 1), (h >> 1) & 1, kWaitBudget));
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(bars + 3 + (h & 1), (h >> 1) & 1, kWaitNs));
         tc_fence_after();
         if (ok) {
             uint32_t r[16];
@@ -268,7 +267,7 @@ __global__ void __launch_bounds__(kPThr, 1)
     };
     auto wait = [&](int bar, unsigned parity) {
         if (*abort_flag) return false;
-        if (mbar_wait(bars + bar, parity, kWaitBudget)) return true;
+        if (mbar_wait(bars + bar, parity, kWaitNs)) return true;
         *abort_flag = 1;
         return false;
     };

@@ -188,11 +188,16 @@ size_t lcsw_sparse_attn_workspace_size(int B, int T, int H_q, int d_v, int k, in
     return lcsw::sparse_attn_ws_bytes(int64_t(B) * T, H_q, d_v, k, P);
 }
 
-lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_b,
-                             const lcsw_bf16 *V, int64_t sV_b, const int32_t *seq_len,
-                             const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
-                             int P, int k, float scale, lcsw_bf16 *out, float *lse, void *ws,
-                             size_t ws_bytes, lcsw_stream stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks of the sparse attention entry points (shapes, pointers,
+// alignment), before any workspace or scratch question.
+lcsw_status check_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_b, const lcsw_bf16 *V,
+                       int64_t sV_b, const int32_t *seq_len, const int32_t *idx, int B, int T,
+                       int H_q, int d_qk, int d_v, int P, int k, const lcsw_bf16 *out,
+                       const float *lse) {
     CHECK(B >= 0 && T >= 0, "negative dimension");
     CHECK(k >= 1, "k must be >= 1");
     CHECK(p_ok(P), "P must be 1, 2, 4 or 8");
@@ -207,6 +212,23 @@ lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_
               bf16_rows_ok(out, d_v, 0),
           "q/K/V/out rows must be 16-byte aligned");
     CHECK(aligned(idx, 4) && aligned(seq_len, 4) && (!lse || aligned(lse, 4)), "misaligned array");
+    return LCSW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_b,
+                             const lcsw_bf16 *V, int64_t sV_b, const int32_t *seq_len,
+                             const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
+                             int P, int k, float scale, lcsw_bf16 *out, float *lse, void *ws,
+                             size_t ws_bytes, lcsw_stream stream) {
+    const lcsw_status chk = check_attn(q, K, sK_b, V, sV_b, seq_len, idx, B, T, H_q, d_qk, d_v,
+                                       P, k, out, lse);
+    if (chk != LCSW_OK) return chk;
+    const int64_t rows = int64_t(B) * T;
+    if (rows == 0) return LCSW_OK;
     const size_t need = lcsw::sparse_attn_ws_bytes(rows, H_q, d_v, k, P);
     if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16)))
         return fail(LCSW_ERR_WORKSPACE, "sparse_attn needs a 16-byte aligned workspace of %zu bytes",
@@ -488,15 +510,18 @@ lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int
                                      const int32_t *idx, int B, int T, int H_q, int d_qk,
                                      int d_v, int P, int k, float scale, lcsw_bf16 *out,
                                      float *lse, lcsw_stream stream) {
-    // the size check needs no device: an oversized call launches nothing
-    if (B > 0 && T > 0 && H_q > 0 && d_v > 0 && k > 0 && p_ok(P)) {
-        const size_t need = lcsw_sparse_attn_workspace_size(B, T, H_q, d_v, k, P);
-        if (need > size_t(LCSW_NOALLOC_SCRATCH_BYTES))
-            return fail(LCSW_ERR_UNSUPPORTED,
-                        "sparse_attn_noalloc: this shape needs %zu bytes of split-K scratch, above "
-                        "the fixed %zu; call lcsw_sparse_attn with a workspace instead",
-                        need, size_t(LCSW_NOALLOC_SCRATCH_BYTES));
-    }
+    // the argument checks of lcsw_sparse_attn first, then the scratch size:
+    // neither needs the device, so a rejected call launches nothing
+    const lcsw_status chk = check_attn(q, K, sK_b, V, sV_b, seq_len, idx, B, T, H_q, d_qk, d_v,
+                                       P, k, out, lse);
+    if (chk != LCSW_OK) return chk;
+    if (int64_t(B) * T == 0) return LCSW_OK;
+    const size_t need = lcsw_sparse_attn_workspace_size(B, T, H_q, d_v, k, P);
+    if (need > size_t(LCSW_NOALLOC_SCRATCH_BYTES))
+        return fail(LCSW_ERR_UNSUPPORTED,
+                    "sparse_attn_noalloc: this shape needs %zu bytes of split-K scratch, above "
+                    "the fixed %zu; call lcsw_sparse_attn with a workspace instead",
+                    need, size_t(LCSW_NOALLOC_SCRATCH_BYTES));
     void *scratch = nullptr;
     const lcsw_status s = attn_scratch(&scratch);
     if (s != LCSW_OK) return s;

@@ -64,7 +64,6 @@ constexpr int kThr = 320;                 // 10 warps
 constexpr int kGatherWarp0 = 4, kMmaWarp = 9;
 constexpr int kGatherWarps = kMmaWarp - kGatherWarp0;
 constexpr int kColS = 0, kColO = 64, kTmemCols = 256;
-constexpr long long kWaitTries = 50000;   // up to 20 us each
 constexpr float kLn2f = 0.6931471805599453f;
 // The softmax reference of a head changes only when a score exceeds it by more
 // than kLazy (log2 units), so p <= 2^kLazy; otherwise a chunk keeps it.
@@ -88,23 +87,17 @@ __device__ __forceinline__ void item_of(int i, int n, bool &is_v, int &c) {
     }
 }
 
-// Bounded wait for the phase of the given parity; gives up when the budget
-// runs out or another role has given up.
+// Bounded wait for the phase of the given parity; gives up when about a
+// second of the global timer has passed or another role has given up.
 __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity,
                                            const volatile int *abort_flag) {
     const uint32_t a = smem_u32(bar);
-    for (long long i = 0; i < kWaitTries; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(a), "r"(parity), "r"(kSuspendNs)
-            : "memory");
-        if (done) return true;
-        if (*abort_flag) return false;
+    if (mbar_try(a, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try(a, parity)) return true;
+        if (*abort_flag || globaltimer_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 
 __device__ __forceinline__ void bar_arrive(uint64_t *bar) {
@@ -338,7 +331,7 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_tc_kernel(
         // every product issued so far completes before TMEM is released
         if (elect_one()) tc_commit(mma_done);
         __syncwarp();
-        mbar_wait(mma_done, 0u, kWaitTries);  // bounded; not cut short by an abort
+        mbar_wait(mma_done, 0u, kWaitNs);  // bounded; not cut short by an abort
     } else {
         // ----------------------------------------------------------- softmax
         // warps 0-3: thread tid owns TMEM lane tid -- its token of each S^T

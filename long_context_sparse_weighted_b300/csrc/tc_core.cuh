@@ -57,22 +57,29 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 }
 // Wait for the phase with the given parity to complete.  Each try suspends
 // the thread until the phase completes or kSuspendNs pass (so waiting warps
-// do not spin on issue slots); gives up after `budget` tries (about budget x
-// 20 us) and returns false.
+// do not spin on issue slots); gives up once `budget_ns` nanoseconds of the
+// global timer have passed since the first try and returns false.  The bound
+// is elapsed time, not a count of tries: a try may return at once.
 constexpr uint32_t kSuspendNs = 20000;
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long budget) {
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return done != 0u;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long budget_ns) {
     const uint32_t a = smem_u32(bar);
-    for (long long i = 0; i < budget; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(a), "r"(parity), "r"(kSuspendNs)
-            : "memory");
-        if (done) return true;
+    if (mbar_try(a, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try(a, parity)) return true;
+        if (globaltimer_ns() - t0 > budget_ns) return false;
     }
-    return false;
 }
 
 // Arrive once on the mbarrier and expect `bytes` of asynchronous copies.

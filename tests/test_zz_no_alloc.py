@@ -3,8 +3,10 @@
 The file is named to be collected last: the entry point must pass after every
 other test has used the library in the same process, and alone in a fresh
 process.  The GPU test checks it against lcsw_sparse_attn (the entry point with a
-caller workspace) on two calls in a row; the CPU test checks that a shape whose
-split-K scratch would not fit is rejected before any device work.
+caller workspace) and against the CPU oracle on two calls in a row; the CPU
+tests check that its arguments are validated as lcsw_sparse_attn validates
+them, and that a valid shape whose split-K scratch would not fit is rejected
+before any device work.
 """
 import os
 import re
@@ -38,21 +40,52 @@ def _case(seed, B, lengths, H_q, d_qk, d_v, k, P):
     return c, idx
 
 
+# Stand-in device addresses: the host checks only look at their alignment and
+# reject the call before anything would dereference them.
+_FAKE = [0x10000 * (i + 1) for i in range(6)]
+
+
 def test_noalloc_rejects_oversized_shape():
     L = lcsw.lib()
     B, T, H_q, d_qk, d_v, k, P = 4, 1, 128, 128, 128, 2048, 4
     need = L.lcsw_sparse_attn_workspace_size(B, T, H_q, d_v, k, P)
     assert need > _scratch_bytes()
-    st = L.lcsw_sparse_attn_noalloc(None, None, 0, None, 0, None, None, B, T, H_q, d_qk, d_v,
-                                    P, k, 1.0, None, None, None)
+    q, K, V, seq, idx, out = _FAKE
+    st = L.lcsw_sparse_attn_noalloc(q, K, 0, V, 0, seq, idx, B, T, H_q, d_qk, d_v,
+                                    P, k, 1.0, out, None, None)
     assert st == lcsw.ERR_UNSUPPORTED
     msg = L.lcsw_last_error().decode()
     assert "split-K scratch" in msg and str(need) in msg
 
 
+@pytest.mark.parametrize("bad", ["null", "heads", "P", "misaligned"])
+def test_noalloc_validates_arguments_first(bad):
+    """An invalid call is an argument error, as from lcsw_sparse_attn, even
+    when its shape would also overflow the fixed scratch."""
+    L = lcsw.lib()
+    B, T, H_q, d_qk, d_v, k, P = 4, 1, 128, 128, 128, 2048, 4
+    q, K, V, seq, idx, out = _FAKE
+    if bad == "null":
+        q = None
+    elif bad == "heads":
+        H_q = 48
+    elif bad == "P":
+        P = 3
+    else:
+        K += 2
+    st = L.lcsw_sparse_attn_noalloc(q, K, 0, V, 0, seq, idx, B, T, H_q, d_qk, d_v,
+                                    P, k, 1.0, out, None, None)
+    assert st == lcsw.ERR_INVALID_ARG, L.lcsw_last_error().decode()
+    st_ws = L.lcsw_sparse_attn(q, K, 0, V, 0, seq, idx, B, T, H_q, d_qk, d_v, P, k, 1.0, out,
+                               None, None, 0, None)
+    assert st_ws == lcsw.ERR_INVALID_ARG
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_two_calls(cuda_device):
     import torch
+
+    import oracle
     from gpu_util import assert_attn_close, assert_lse_close, dev, host_bits, upload_case
 
     L = lcsw.lib()
@@ -76,3 +109,7 @@ def test_noalloc_matches_workspace_entry_two_calls(cuda_device):
         torch.cuda.synchronize()
         assert_attn_close(host_bits(out), host_bits(ref_out))
         assert_lse_close(lse.cpu().numpy(), ref_lse.cpu().numpy().astype(np.float64))
+        o_ref, l_ref = oracle.sparse_attn(c["q"], c["K"], c["V"], c["seq_len"], idx, P,
+                                          c["scale"])
+        assert_attn_close(host_bits(out), o_ref)
+        assert_lse_close(lse.cpu().numpy(), l_ref)
