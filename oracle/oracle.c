@@ -79,9 +79,123 @@ uint16_t oracle_bf16_from_double(double x)
 
 /* ---------------------------------------------------------------- pool --- */
 
+/* The pooled sum is formed exactly, then rounded once.  A product of an fp32
+ * weight (at most 24 significant bits) and a bf16 key (at most 8) is an
+ * integer m with |m| < 2^32 times 2^e, -282 <= e <= 224; a sum of P <= 8 such
+ * products is held exactly in a two's-complement integer of WIDE_LIMBS 64-bit
+ * limbs whose lowest bit weighs 2^WIDE_E0 (bits up to 2^(WIDE_E0 + 640)). */
+#define WIDE_LIMBS 10
+#define WIDE_E0 (-288)
+
+typedef struct {
+    uint64_t w[WIDE_LIMBS];
+} wide_int;
+
+static void wide_negate(wide_int *a)
+{
+    int carry = 1;
+    for (int i = 0; i < WIDE_LIMBS; ++i) {
+        a->w[i] = ~a->w[i] + (uint64_t)carry;
+        carry = carry && a->w[i] == 0;
+    }
+}
+
+/* a += m * 2^e  (|m| < 2^63, e >= WIDE_E0, m * 2^e inside the range above) */
+static void wide_add(wide_int *a, int64_t m, int e)
+{
+    if (m == 0)
+        return;
+    wide_int t;
+    memset(&t, 0, sizeof t);
+    uint64_t mag = m < 0 ? (uint64_t)(-m) : (uint64_t)m;
+    int pos = e - WIDE_E0, limb = pos / 64, sh = pos % 64;
+    t.w[limb] = mag << sh;
+    if (sh && limb + 1 < WIDE_LIMBS)
+        t.w[limb + 1] = mag >> (64 - sh);
+    if (m < 0)
+        wide_negate(&t);
+    uint64_t carry = 0;
+    for (int i = 0; i < WIDE_LIMBS; ++i) {
+        uint64_t s = a->w[i] + t.w[i];
+        uint64_t c1 = s < t.w[i];
+        uint64_t s2 = s + carry;
+        uint64_t c2 = s2 < s;
+        a->w[i] = s2;
+        carry = c1 | c2;
+    }
+}
+
+static int wide_bit(const wide_int *a, int i)
+{
+    return (int)((a->w[i / 64] >> (i % 64)) & 1u);
+}
+
+/* a finite nonzero float as m * 2^e with m an odd integer of at most 24 bits
+ * (so e is the weight of its lowest set bit: e >= -149 for fp32, >= -133 for
+ * bf16); zero as m = 0 */
+static void split_float(float f, int64_t *m, int *e)
+{
+    *m = 0;
+    *e = 0;
+    if (f == 0.0f)
+        return;
+    int ex;
+    double fr = frexp((double)f, &ex);  /* f = fr * 2^ex, 0.5 <= |fr| < 1 */
+    int64_t mm = (int64_t)ldexp(fr, 24);  /* exact */
+    int ee = ex - 24;
+    while ((mm & 1) == 0) {
+        mm /= 2;
+        ee += 1;
+    }
+    *m = mm;
+    *e = ee;
+}
+
+/* Nearest bf16 of the exact integer value (ties to even): take the 8 bits
+ * from the leading one (fewer below the subnormal quantum 2^-133), then the
+ * first bit below them and whether any lower bit is set. */
+static uint16_t wide_to_bf16(const wide_int *acc)
+{
+    wide_int a = *acc;
+    uint16_t sign = 0;
+    if (a.w[WIDE_LIMBS - 1] >> 63) {
+        sign = 0x8000u;
+        wide_negate(&a);
+    }
+    int top = -1;
+    for (int i = WIDE_LIMBS * 64 - 1; i >= 0; --i)
+        if (wide_bit(&a, i)) {
+            top = i;
+            break;
+        }
+    if (top < 0)
+        return 0;                       /* an exact zero sum is +0 */
+    int qe = top + WIDE_E0 - 7;         /* quantum of 8 significant bits */
+    if (qe < -133)
+        qe = -133;
+    int cut = qe - WIDE_E0;             /* bit index of the quantum (> 0) */
+    uint64_t r = 0;
+    for (int i = top; i >= cut; --i)
+        r = 2 * r + (uint64_t)wide_bit(&a, i);
+    int half = wide_bit(&a, cut - 1), sticky = 0;
+    for (int i = cut - 2; i >= 0 && !sticky; --i)
+        sticky = wide_bit(&a, i);
+    if (half && (sticky || (r & 1u)))
+        r += 1;
+    double y = ldexp((double)r, qe);
+    if (y >= 0x1p128)
+        return sign | 0x7F80u;
+    float f = (float)y;                 /* exact: at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)((u >> 16) & 0x7FFFu);
+}
+
 /* IndexPool over every complete group of every sequence.
  * k_idx [B][*][d] (batch stride sk_b elements), pool_w [B][*][P] (stride sw_b),
- * k_pooled [B][*][d] (stride sp_b).  Groups g >= seq_len[b]/P are untouched. */
+ * k_pooled [B][*][d] (stride sp_b).  Groups g >= seq_len[b]/P are untouched.
+ * Finite inputs: the sum is exact and rounded once; a non-finite weight or
+ * key takes IEEE double arithmetic (inf or NaN out). */
 void oracle_pool_keys(const uint16_t *k_idx, int64_t sk_b, const float *pool_w, int64_t sw_b,
                       const int32_t *seq_len, int B, int d, int P,
                       uint16_t *k_pooled, int64_t sp_b)
@@ -91,12 +205,26 @@ void oracle_pool_keys(const uint16_t *k_idx, int64_t sk_b, const float *pool_w, 
         for (int64_t g = 0; g < G; ++g) {
             const float *alpha = pool_w + b * sw_b + g * P;
             for (int i = 0; i < d; ++i) {
+                wide_int acc;
+                memset(&acc, 0, sizeof acc);
                 double s = 0.0;
+                int finite = 1;
                 for (int j = 0; j < P; ++j) {
                     double kv = bf16_value(k_idx[b * sk_b + (P * g + j) * (int64_t)d + i]);
-                    s += (double)alpha[j] * kv;
+                    double aj = (double)alpha[j];
+                    s += aj * kv;
+                    if (!isfinite(aj) || !isfinite(kv)) {
+                        finite = 0;
+                        continue;
+                    }
+                    int64_t ma, mk;
+                    int ea, ek;
+                    split_float((float)aj, &ma, &ea);
+                    split_float((float)kv, &mk, &ek);
+                    wide_add(&acc, ma * mk, ea + ek);
                 }
-                k_pooled[b * sp_b + g * (int64_t)d + i] = oracle_bf16_from_double(s);
+                k_pooled[b * sp_b + g * (int64_t)d + i] =
+                    finite ? wide_to_bf16(&acc) : oracle_bf16_from_double(s);
             }
         }
     }

@@ -41,6 +41,25 @@ def test_pool_keys_bit_exact(P, mode):
         assert np.array_equal(got[b, G:], sentinel[b, G:]), "rows past the last group changed"
 
 
+def test_pool_keys_hard_sums_bit_exact():
+    """Sums on or a hair beside a bf16 midpoint, after cancellation of large
+    terms, or spanning hundreds of binades (tests/pool_cases.py): the kernel
+    and the exact oracle agree bit for bit, and both equal the nearest bf16 of
+    the exact rational sum."""
+    import pool_cases
+    cs = pool_cases.cases(n=800, seed=32)
+    k_idx, pool_w = pool_cases.as_arrays(cs)
+    seq = np.array([k_idx.shape[1]], np.int32)
+    ref = oracle.pool_keys(k_idx, pool_w, seq, 4)
+    for g, (a, k) in enumerate(cs[:64]):
+        assert ref[0, g, 0] == pool_cases.round_bf16(pool_cases.exact_sum(a, k))
+    out = torch.zeros(1, len(cs), 64, dtype=torch.bfloat16, device="cuda")
+    lcsw.pool_keys(dev_bf16(k_idx), dev(pool_w), dev(seq), 4, out)
+    got = host_bits(out)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} elements differ, first groups {sorted(set(bad[:, 1]))[:8]}"
+
+
 def test_pool_keys_tiny_workload_exact():
     c = synth.generate(synth.named("tiny"), with_kv=False)
     ref = oracle.pool_keys(c["k_idx"], c["pool_w"], c["seq_len"], 4)

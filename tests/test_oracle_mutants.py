@@ -16,7 +16,11 @@ import test_oracle_pins as pins
 MUTANTS = {
     "pool_drop_last_term": ("for (int j = 0; j < P; ++j) {", "for (int j = 0; j < P - 1; ++j) {"),
     "pool_wrong_token_index": ("(P * g + j) * (int64_t)d + i", "(g + j) * (int64_t)d + i"),
-    "pool_weights_reversed": ("s += (double)alpha[j] * kv;", "s += (double)alpha[P - 1 - j] * kv;"),
+    "pool_weights_reversed": ("double aj = (double)alpha[j];", "double aj = (double)alpha[P - 1 - j];"),
+    "pool_ties_away_from_zero": ("if (half && (sticky || (r & 1u)))", "if (half)"),
+    "pool_sticky_bits_ignored": ("if (half && (sticky || (r & 1u)))", "if (half && (r & 1u))"),
+    "pool_negation_drops_carry": ("carry = carry && a->w[i] == 0;", "carry = 0;"),
+    "pool_nine_significant_bits": ("int qe = top + WIDE_E0 - 7;", "int qe = top + WIDE_E0 - 8;"),
     "bf16_truncates": ("double r = rint(ldexp(a, -qe));", "double r = floor(ldexp(a, -qe));"),
     "score_no_relu": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot;"),
     "score_wrong_head_weight": ("s += (double)wt[h] * relu;", "s += (double)wt[0] * relu;"),

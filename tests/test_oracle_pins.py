@@ -123,6 +123,44 @@ def test_pool_gaussian_is_nearest_bf16_of_exact_sum():
                 assert int(got[0, g, i]) % 2 == 0  # tie -> even mantissa
 
 
+def test_pool_hard_sums_round_exactly():
+    """Sums on or a hair beside a bf16 midpoint, after cancellation, or spanning
+    hundreds of binades: the pooled key is the nearest bf16 of the exact
+    rational sum (ties to even), with no double rounding."""
+    import pool_cases
+    cs = pool_cases.cases()
+    k_idx, pool_w = pool_cases.as_arrays(cs, d=8)
+    got = oracle.pool_keys(k_idx, pool_w, np.array([k_idx.shape[1]], np.int32), 4)
+    for g, (a, k) in enumerate(cs):
+        want = pool_cases.round_bf16(pool_cases.exact_sum(a, k))
+        assert (got[0, g] == want).all(), (g, a, k, got[0, g, 0], want)
+
+
+def test_pool_hand_worked_hard_sums():
+    # worked by hand from the bf16 format (8 significant bits, ties to even):
+    #   (1 + 2^-8) * 1 + 2^-60 * 1  lies just above the midpoint of 1 and
+    #   1 + 2^-7, so it rounds up to 1 + 2^-7 = 0x3F81 (a sum formed in double
+    #   would drop the 2^-60 and tie down to 1.0);
+    #   1 * 1 + 2^-8 * 1 is exactly that midpoint: ties to even, 1.0 = 0x3F80;
+    #   1 * (1 + 2^-7) + 2^-8 * 1 is the midpoint of 1 + 2^-7 and 1 + 2^-6:
+    #   ties to the even mantissa, 1 + 2^-6 = 0x3F82;
+    #   2^100 - 2^100 + 3 - 2^-130 lies just below 3 = 0x4040;
+    #   -(1 + 2^-8) + -(2^-70) rounds away from zero to -(1 + 2^-7) = 0xBF81;
+    #   -1 - 2^-8 is exactly a midpoint: ties to even, -1.0 = 0xBF80.
+    one, rows = 0x3F80, []
+    rows.append(([1 + 2 ** -8, 2 ** -60, 0, 0], [one, one, 0, 0], 0x3F81))
+    rows.append(([1, 2 ** -8, 0, 0], [one, one, 0, 0], 0x3F80))
+    rows.append(([1, 2 ** -8, 0, 0], [0x3F81, one, 0, 0], 0x3F82))
+    rows.append(([1, 1, 1, 2 ** -130], [0x7180, 0xF180, 0x4040, 0xBF80], 0x4040))
+    rows.append(([1 + 2 ** -8, 2 ** -70, 0, 0], [0xBF80, 0xBF80, 0, 0], 0xBF81))
+    rows.append(([1, 2 ** -8, 0, 0], [0xBF80, 0xBF80, 0, 0], 0xBF80))
+    for a, k, want in rows:
+        got = oracle.pool_keys(np.array(k, np.uint16).reshape(1, 4, 1),
+                               np.array(a, np.float32).reshape(1, 1, 4),
+                               np.array([4], np.int32), 4)
+        assert int(got[0, 0, 0]) == want, (a, k, hex(int(got[0, 0, 0])), hex(want))
+
+
 def test_pool_p1_identity_and_tail_untouched():
     spec = synth.Spec(B=1, lengths=[30], P=1, pool_mode="dyadic", seed=14)
     c = synth.generate(spec, with_kv=False)
