@@ -263,6 +263,73 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
                               lcsw_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 pooled indexer keys.  The serving stack of the reading notes (section
+ * "The serving stack") quantizes caches per tier to INT8, FP8 or BF16 and
+ * gives no format; the reading here: OCP E4M3 codes with one fp32 scale per
+ * 64-value row,
+ *
+ *   scale = amax_i |x_i| / 448 (fp32),   code_i = nearest E4M3 of x_i / scale
+ *
+ * (ties to the even code, saturating at +-448; every code 0 when scale is 0).
+ * The rounding is exact: the code is the nearest to the exact quotient.
+ *
+ * Cache layout kq, per sequence b (base kq + b * sq_b bytes): tiles of 16
+ * groups, LCSW_E4M3_TILE_BYTES each -- 16 rows of 64 codes, then the 16 rows'
+ * fp32 scales.  Group g: codes at tile g/16, byte (g%16)*64; scale at byte
+ * 1024 + (g%16)*4 of the tile.  sq_b is a multiple of 16 and holds at least
+ * ceil(G_max/16) tiles (the decode step reads whole tiles).
+ *
+ * lcsw_quantize_keys_e4m3 quantizes groups [0, n_groups) of every sequence's
+ * bf16 pooled keys (k_pooled [B][*][64], batch stride sp_b elements).
+ * ------------------------------------------------------------------------- */
+#define LCSW_E4M3_TILE_BYTES 1088
+lcsw_status lcsw_quantize_keys_e4m3(const lcsw_bf16 *k_pooled, int64_t sp_b, int B,
+                                    int n_groups, uint8_t *kq, int64_t sq_b,
+                                    lcsw_stream stream);
+
+/* One decode step (as lcsw_decode_fused) whose indexer reads the FP8 cache kq
+ * instead of bf16 pooled keys.  The indexer query q_idx (bf16) is quantized
+ * per head in the same way inside the step, and
+ *
+ *   s[b][g] = sum_h w_head[b][h] * max(0, scale_q,h * scale_k,g * sum_i q_i k_i)
+ *
+ * over the codes' values; the selection and attention follow as in
+ * lcsw_decode_fused.  Append: with k_idx and pool_w, the group the newest token
+ * completes is pooled exactly (bf16, as lcsw_pool_keys) and quantized into kq
+ * before it is scored; k_pooled is not read or written (it may be NULL).
+ * Shapes outside the persistent kernel's envelope (lcsw_decode_launches(a)
+ * != 1) return LCSW_ERR_UNSUPPORTED.  Workspace: lcsw_decode_workspace_size.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_decode_fused_e4m3(const lcsw_decode_args *a, uint8_t *kq, int64_t sq_b,
+                                   void *ws, size_t ws_bytes, lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Cross-layer reuse of a selection (reading notes "GLM-5.3-Flash: Hybrid
+ * Attention, IndexPool, and Vision-in-the-Loop", section 2, sub-head
+ * "IndexPool": the cross-layer variant of the pooled-index idea is called
+ * IndexCache; the pages say nothing more).  Reading: a later DSA layer of the
+ * same decode step runs no indexer scores and no top-k of its own; it attends
+ * over the groups an earlier layer selected, e.g. the idx_out of that layer's
+ * lcsw_decode_fused call.
+ *
+ *   out[b][h][:], lse[b][h] = lcsw_sparse_attn of q over the groups
+ *   idx_in[b][0..k) of K/V (entries outside [0, seq_len[b]/P), such as -1
+ *   padding, are skipped; an empty set gives out = 0, lse = -inf).
+ *
+ * Reads q, K, sK_b, V, sV_b, seq_len, B, H_q, d_qk, d_v, P, k, scale, out and
+ * lse of `a`; its indexer fields (q_idx, w_head, k_pooled, k_idx, pool_w,
+ * H_i, d_idx, G_max), idx_out, scores_out and flags are not used.
+ *   idx_in  [B][k] int32 device
+ *   ws      a decode workspace: lcsw_decode_workspace_size(a) bytes, 256-byte
+ *           aligned (only its split-K region is written; it needs no clearing
+ *           and may be the same workspace the selecting layer's call used,
+ *           once that call has completed)
+ * Two launches on `stream`: split-K partial states, then their merge.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_decode_reuse(const lcsw_decode_args *a, const int32_t *idx_in, void *ws,
+                              size_t ws_bytes, lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
  * Chunked prefill: T new query tokens per sequence, the last T tokens of the
  * cache (positions seq_len[b]-T .. seq_len[b]-1), causal at group
  * granularity.  Pools the groups the chunk completes (from the group holding

@@ -79,6 +79,7 @@ _SIGNATURES = {
     "lcsw_decode_workspace_size": ([ctypes.POINTER(DecodeArgs)], _sz),
     "lcsw_decode_fused": ([ctypes.POINTER(DecodeArgs), _vp, _sz, _vp], _i32),
     "lcsw_decode_launches": ([ctypes.POINTER(DecodeArgs)], _i32),
+    "lcsw_decode_reuse": ([ctypes.POINTER(DecodeArgs), _vp, _vp, _sz, _vp], _i32),
     "lcsw_prefill_workspace_size": ([ctypes.POINTER(PrefillArgs)], _sz),
     "lcsw_prefill": ([ctypes.POINTER(PrefillArgs), _vp, _sz, _vp], _i32),
     "lcsw_get_status": ([_vp, _vp], _i32),
@@ -318,6 +319,47 @@ class Decoder:
 
     def status(self, stream=None):
         _check(lib().lcsw_get_status(ctypes.c_void_p(self.ws.data_ptr()), _stream(stream)))
+
+
+class ReuseStep:
+    """A DSA layer's decode step that reuses another layer's selection
+    (lcsw_decode_reuse): attention of q over the groups idx_in[b][0..k),
+    with no indexer scores or top-k of its own."""
+
+    def __init__(self, q, K, V, seq_len, idx_in, P, scale, out=None, lse=None, ws=None):
+        _bf16(q, "q", 3)
+        _bf16(K, "K", 3)
+        _bf16(V, "V", 3)
+        _dense(seq_len, torch.int32, "seq_len")
+        _dense(idx_in, torch.int32, "idx_in")
+        B, H_q, d_qk = q.shape
+        d_v = V.shape[2]
+        k = idx_in.shape[-1]
+        dev = q.device
+        self.out = out if out is not None else torch.empty(B, H_q, d_v, dtype=torch.bfloat16,
+                                                           device=dev)
+        self.lse = lse if lse is not None else torch.empty(B, H_q, dtype=torch.float32,
+                                                           device=dev)
+        self._keep = (q, K, V, seq_len, idx_in)
+        a = DecodeArgs()
+        a.q = q.data_ptr()
+        a.K, a.sK_b = K.data_ptr(), K.stride(0)
+        a.V, a.sV_b = V.data_ptr(), V.stride(0)
+        a.seq_len = seq_len.data_ptr()
+        a.B, a.G_max, a.H_i, a.d_idx, a.P, a.k = B, 0, 1, 64, P, k
+        a.H_q, a.d_qk, a.d_v, a.scale = H_q, d_qk, d_v, float(scale)
+        a.out, a.lse = self.out.data_ptr(), self.lse.data_ptr()
+        self.args = a
+        self.idx_in = idx_in
+        self.ws_bytes = lib().lcsw_decode_workspace_size(ctypes.byref(a))
+        self.ws = ws if ws is not None else torch.empty(self.ws_bytes, dtype=torch.uint8,
+                                                        device=dev)
+
+    def __call__(self, stream=None):
+        _check(lib().lcsw_decode_reuse(ctypes.byref(self.args), ctypes.c_void_p(self.idx_in.data_ptr()),
+                                       ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(),
+                                       _stream(stream)))
+        return self.out, self.lse
 
 
 def decode_fused(q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale, **kw):

@@ -1,0 +1,64 @@
+// FP8 (OCP E4M3) pooled indexer keys and queries: one fp32 scale per 64-value
+// row, codes rounded to nearest with ties to the even code, saturating at
+// +-448.  The serving stack of the reading notes ("GLM-5.3-Flash: Hybrid
+// Attention, IndexPool, and Vision-in-the-Loop", section "The serving stack")
+// quantizes caches per tier to INT8, FP8 or BF16 and says nothing more about
+// the format; this is the plainest reading:
+//
+//   scale = amax(|x|) / 448 (fp32),  code_i = e4m3(x_i / scale)  (0 if scale = 0)
+//
+// The rounding decision is exact: the fp32 quotient proposes a code, and the
+// sign of x - m * scale, with m the midpoint between that code and its
+// neighbour on the quotient's side, settles it (an FMA forms that difference
+// with one rounding, which keeps its sign).
+#pragma once
+
+#include "common.cuh"
+
+namespace lcsw {
+
+// The FP8 pooled-key cache, per sequence: tiles of 16 groups, each 16 rows of
+// 64 codes followed by the 16 rows' fp32 scales.
+constexpr int kE4m3TileBytes = 16 * 64 + 16 * 4;
+
+// Value of a code (sign, 4 exponent bits with bias 7, 3 mantissa bits; the
+// exponent field 0 holds the subnormals m * 2^-9).  Codes 0x7F/0xFF (NaN) are
+// never produced.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+    const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
+    const float mag = e == 0u ? float(m) * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return (c & 0x80u) ? -mag : mag;
+}
+
+// Nearest code of x / scale (scale > 0), ties to the even code, saturating.
+__device__ __forceinline__ uint32_t e4m3_quantize(float x, float scale) {
+    const uint32_t sign = (__float_as_uint(x) >> 24) & 0x80u;
+    const float a = fabsf(x);
+    const float q = __fdiv_rn(a, scale);
+    if (q >= 448.f) return sign | 0x7Eu;
+    // proposed code from the rounded quotient
+    uint32_t c;
+    {
+        unsigned short pair;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(q));
+        c = pair & 0x7Fu;
+    }
+    const float v = e4m3_value(c);
+    if (q == v) return sign | c;  // the exact quotient lies within half an fp32 ulp of v
+    // midpoint between c and its neighbour on the quotient's side
+    const uint32_t lo = q > v ? c : c - 1u, hi = lo + 1u;
+    const float mid = 0.5f * (e4m3_value(lo) + e4m3_value(hi));
+    const float d = __fmaf_rn(-mid, scale, a);  // sign of a - mid * scale, exactly
+    uint32_t r;
+    if (d > 0.f) r = hi;
+    else if (d < 0.f) r = lo;
+    else r = (lo & 1u) ? hi : lo;
+    return sign | min(r, 0x7Eu);
+}
+
+// Scale of a row from its largest magnitude: amax / 448 rounded to fp32 (the
+// same value as rounding the double quotient: amax has 8 significant bits, and
+// a quotient by 7 * 2^6 never lands exactly between two fp32 values).
+__device__ __forceinline__ float e4m3_row_scale(float amax) { return __fdiv_rn(amax, 448.f); }
+
+}  // namespace lcsw

@@ -13,5 +13,9 @@ bool fused_decode_supported(int B, int G_max, int H_i, int H_q, int d_qk, int d_
 size_t fused_decode_ws_bytes(int B, int G_max, int H_q, int d_v, int k, int P);
 cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status,
                                 cudaStream_t st);
+// The same step with FP8 pooled keys (tile-major E4M3 cache kq, batch stride
+// sq_b bytes; k_pooled unused).
+cudaError_t launch_fused_decode_e4m3(const lcsw_decode_args *a, uint8_t *kq, int64_t sq_b,
+                                     void *ws, int *status, cudaStream_t st);
 
 }  // namespace lcsw

@@ -17,6 +17,11 @@ cudaError_t launch_pool_keys(const uint16_t *k_idx, int64_t sk_b, const float *p
                              int B, int g_span, int d_idx, int P, int mode, int tail,
                              uint16_t *k_pooled, int64_t sp_b, cudaStream_t st);
 
+// FP8 pooled keys: groups [0, n_groups) of every sequence's bf16 pooled keys
+// into the tile-major E4M3 cache (e4m3_core.cuh).
+cudaError_t launch_quantize_keys_e4m3(const uint16_t *k_pooled, int64_t sp_b, int B, int n_groups,
+                                      uint8_t *kq, int64_t sq_b, cudaStream_t st);
+
 // q_pos[b][t] = seq_len[b] - T + t (the chunk's absolute positions).
 cudaError_t launch_prefill_positions(const int32_t *seq_len, int B, int T, int32_t *q_pos,
                                      cudaStream_t st);

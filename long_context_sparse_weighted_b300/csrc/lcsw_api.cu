@@ -339,6 +339,90 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
     return cuda_status(e, "decode attention");
 }
 
+lcsw_status lcsw_quantize_keys_e4m3(const lcsw_bf16 *k_pooled, int64_t sp_b, int B,
+                                    int n_groups, uint8_t *kq, int64_t sq_b,
+                                    lcsw_stream stream) {
+    CHECK(B >= 0 && n_groups >= 0, "negative dimension");
+    if (B == 0 || n_groups == 0) return LCSW_OK;
+    CHECK(k_pooled && kq, "null pointer argument");
+    CHECK(bf16_rows_ok(k_pooled, 64, sp_b) && sp_b >= int64_t(n_groups) * 64,
+          "k_pooled rows must be 16-byte aligned and hold n_groups rows per sequence");
+    const int64_t tiles = (int64_t(n_groups) + 15) / 16;
+    CHECK(aligned(kq, 16) && sq_b % 16 == 0 && sq_b >= tiles * LCSW_E4M3_TILE_BYTES,
+          "kq must be 16-byte aligned with a batch stride (multiple of 16) of at least "
+          "ceil(n_groups/16) tiles of %d bytes", LCSW_E4M3_TILE_BYTES);
+    return cuda_status(lcsw::launch_quantize_keys_e4m3(k_pooled, sp_b, B, n_groups, kq, sq_b,
+                                                       (cudaStream_t)stream),
+                       "quantize keys launch");
+}
+
+lcsw_status lcsw_decode_fused_e4m3(const lcsw_decode_args *a, uint8_t *kq, int64_t sq_b,
+                                   void *ws, size_t ws_bytes, lcsw_stream stream) {
+    CHECK(a, "null args");
+    CHECK(a->B >= 0 && a->G_max >= 0, "negative dimension");
+    CHECK(a->d_idx == 64, "d_idx must be 64");
+    CHECK(a->H_i >= 1 && a->H_i <= 16, "H_i must be in [1, 16]");
+    CHECK(p_ok(a->P), "P must be 1, 2, 4 or 8");
+    CHECK(a->k >= 1, "k must be >= 1");
+    CHECK(attn_shape_ok(a->H_q, a->d_qk, a->d_v), "unsupported attention shape");
+    if (a->B == 0) return LCSW_OK;
+    CHECK(a->q_idx && a->w_head && kq && a->q && a->K && a->V && a->seq_len && a->out,
+          "null pointer argument");
+    CHECK(!a->k_idx || a->pool_w, "pool_w is required with k_idx");
+    CHECK(bf16_rows_ok(a->q_idx, 64, 0) && (!a->k_idx || bf16_rows_ok(a->k_idx, 64, a->sk_b)) &&
+              bf16_rows_ok(a->q, a->d_qk, 0) && bf16_rows_ok(a->K, a->d_qk, a->sK_b) &&
+              bf16_rows_ok(a->V, a->d_v, a->sV_b) && bf16_rows_ok(a->out, a->d_v, 0),
+          "bf16 rows must be 16-byte aligned");
+    CHECK(aligned(a->w_head, 4) && aligned(a->seq_len, 4) && (!a->lse || aligned(a->lse, 4)) &&
+              (!a->idx_out || aligned(a->idx_out, 4)) &&
+              (!a->scores_out || aligned(a->scores_out, 4)) &&
+              (!a->pool_w || aligned(a->pool_w, 4)),
+          "misaligned fp32/int32 array");
+    const int64_t tiles = (int64_t(a->G_max) + 15) / 16;
+    CHECK(aligned(kq, 16) && sq_b % 16 == 0 && sq_b >= tiles * LCSW_E4M3_TILE_BYTES,
+          "kq must be 16-byte aligned with a batch stride (multiple of 16) of at least "
+          "ceil(G_max/16) tiles of %d bytes", LCSW_E4M3_TILE_BYTES);
+    if ((a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) ||
+        !lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P))
+        return fail(LCSW_ERR_UNSUPPORTED, "FP8 decode: the shape is outside the persistent "
+                    "kernel's envelope");
+    const size_t need = lcsw_decode_workspace_size(a);
+    if (!ws || ws_bytes < need || !aligned(ws, 256))
+        return fail(LCSW_ERR_WORKSPACE, "decode needs a 256-byte aligned workspace of %zu bytes",
+                    need);
+    DecodeWs w = carve_decode(a, ws);
+    return cuda_status(lcsw::launch_fused_decode_e4m3(a, kq, sq_b, w.fused, w.status,
+                                                      (cudaStream_t)stream),
+                       "FP8 fused decode");
+}
+
+lcsw_status lcsw_decode_reuse(const lcsw_decode_args *a, const int32_t *idx_in, void *ws,
+                              size_t ws_bytes, lcsw_stream stream) {
+    CHECK(a, "null args");
+    CHECK(a->B >= 0, "negative dimension");
+    CHECK(p_ok(a->P), "P must be 1, 2, 4 or 8");
+    CHECK(a->k >= 1, "k must be >= 1");
+    CHECK(attn_shape_ok(a->H_q, a->d_qk, a->d_v), "unsupported attention shape");
+    if (a->B == 0) return LCSW_OK;
+    CHECK(a->B <= 65535, "B must be <= 65535");
+    CHECK(a->q && a->K && a->V && a->seq_len && a->out && idx_in, "null pointer argument");
+    CHECK(bf16_rows_ok(a->q, a->d_qk, 0) && bf16_rows_ok(a->K, a->d_qk, a->sK_b) &&
+              bf16_rows_ok(a->V, a->d_v, a->sV_b) && bf16_rows_ok(a->out, a->d_v, 0),
+          "bf16 rows must be 16-byte aligned");
+    CHECK(aligned(a->seq_len, 4) && aligned(idx_in, 4) && (!a->lse || aligned(a->lse, 4)),
+          "misaligned int32/fp32 array");
+    const size_t need = lcsw_decode_workspace_size(a);
+    if (!ws || ws_bytes < need || !aligned(ws, 256))
+        return fail(LCSW_ERR_WORKSPACE, "decode reuse needs a 256-byte aligned workspace of %zu bytes",
+                    need);
+    DecodeWs w = carve_decode(a, ws);
+    return cuda_status(lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len,
+                                                idx_in, a->B, 1, a->H_q, a->d_qk, a->d_v, a->P,
+                                                a->k, a->scale, a->out, a->lse, w.attn,
+                                                (cudaStream_t)stream),
+                       "decode reuse attention");
+}
+
 // ----------------------------------------------------------------- prefill --
 
 struct PrefillWs {

@@ -72,7 +72,8 @@ __device__ __forceinline__ uint4 pool_chunk(const float (&a)[P], const uint4 (&r
 
 // One pooled key from its P rows and weights staged in shared memory
 // (rows_s: [P][64] bf16, w_s: [P]): lanes 0-7 each pool 8 dims and store them
-// to `dst_s` (shared) and `dst` (global).  Out of line: it runs once per call.
+// to `dst_s` (shared) and, unless null, `dst` (global).  Out of line: it runs
+// once per call.
 static __device__ __noinline__ void pool_staged(int P, const uint16_t *rows_s, const float *w_s, int lane,
                                          uint16_t *dst_s, uint16_t *dst) {
     if (lane >= 8) return;
@@ -93,7 +94,7 @@ static __device__ __noinline__ void pool_staged(int P, const uint16_t *rows_s, c
     else LCSW_POOL_STAGED(8)
 #undef LCSW_POOL_STAGED
     *reinterpret_cast<uint4 *>(dst_s + lane * 8) = o;
-    *reinterpret_cast<uint4 *>(dst + lane * 8) = o;
+    if (dst) *reinterpret_cast<uint4 *>(dst + lane * 8) = o;
 }
 
 }  // namespace lcsw

@@ -155,3 +155,20 @@ def test_product_package_does_not_reach_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_decode_reuse_validates_arguments(L):
+    import ctypes
+
+    import long_context_sparse_weighted_b300 as lcsw
+    a = lcsw.DecodeArgs()
+    a.B, a.P, a.k, a.H_q, a.d_qk, a.d_v, a.scale = 2, 4, 16, 32, 128, 128, 0.1
+    a.q, a.K, a.V, a.seq_len, a.out = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    a.sK_b = a.sV_b = 128 * 64
+    ws = 0x100000
+    assert L.lcsw_decode_reuse(ctypes.byref(a), None, ws, 1 << 30, None) == lcsw.ERR_INVALID_ARG
+    assert L.lcsw_decode_reuse(ctypes.byref(a), 0x60002, ws, 1 << 30, None) == lcsw.ERR_INVALID_ARG
+    a.H_q = 48
+    assert L.lcsw_decode_reuse(ctypes.byref(a), 0x60000, ws, 1 << 30, None) == lcsw.ERR_INVALID_ARG
+    a.H_q = 32
+    assert L.lcsw_decode_reuse(ctypes.byref(a), 0x60000, ws, 16, None) == lcsw.ERR_WORKSPACE
