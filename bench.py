@@ -862,6 +862,82 @@ def measure_reuse(torch, lcsw, peak, full_step_ms):
                          "unit": "GB/s", "frac": round(gbs / peak, 4)}}
 
 
+def measure_decode_fp8(torch, lcsw, peak, with_oracle):
+    """decode_1m with FP8 (E4M3) pooled indexer keys (lcsw_decode_fused_e4m3):
+    the same step and timing as the headline, with the cache quantized on the
+    device from the bf16 pooled keys.  Bytes per step count the keys at 68 per
+    group (64 codes and a 4-byte scale)."""
+    spec = synth.named("decode_1m")
+    c = synth.generate(spec)
+    P, k, B = spec.P, spec.k, spec.B
+    dev = "cuda"
+    up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    seq = torch.from_numpy(c["seq_len"]).to(dev)
+    k_idx, pool_w = up16(c["k_idx"]), torch.from_numpy(c["pool_w"]).to(dev)
+    kp = torch.zeros(B, spec.G_max, 64, dtype=torch.bfloat16, device=dev)
+    lcsw.pool_keys(k_idx, pool_w, seq, P, kp)
+    kq0 = lcsw.e4m3_key_cache(B, spec.G_max)
+    lcsw.quantize_keys_e4m3(kp, kq0)
+    del kp
+    G = sum(L // P for L in spec.lengths)
+    ab = G * 68 + P * k * (spec.d_qk + spec.d_v) * 2 + spec.H_q * (spec.d_qk + spec.d_v) * 2 \
+        + spec.H_i * (64 * 2 + 4)
+    L2 = l2_bytes()
+    copies = max(2, math.ceil(3 * L2 / ab))
+    q_idx0 = up16(c["q_idx"][:, 0])
+    w0 = torch.from_numpy(np.ascontiguousarray(c["w_head"][:, 0])).to(dev)
+    q0 = up16(c["q"][:, 0])
+    K0, V0 = up16(c["K"]), up16(c["V"])
+    decs, keep = [], []
+    for r in range(copies):
+        kq = kq0 if r == 0 else kq0.clone()
+        K = K0 if r == 0 else K0.clone()
+        V = V0 if r == 0 else V0.clone()
+        qi, w, q = q_idx0.clone(), w0.clone(), q0.clone()
+        decs.append(lcsw.Decoder(qi, w, None, q, K, V, seq, P, k, c["scale"], k_idx=k_idx,
+                                 pool_w=pool_w, G_max=spec.G_max, kq=kq))
+        keep.append((kq, K, V, qi, w, q))
+    torch.cuda.synchronize()
+    steps = 2000
+    ms, clocks = time_graph_steps(torch, decs, steps, 5, 1)
+    step_ms = ms / steps
+    gbs = ab / (step_ms / 1e3) / 1e9
+    entry = {"kernel": "lcsw_decode_fused_e4m3 (persistent kernel, FP8 pooled keys)",
+             "tokens_per_s": round(B * steps / (ms / 1e3), 1), "ms_per_step": round(step_ms, 6),
+             "steps": steps, "alg_bytes_per_step": ab, "dtype": "e4m3 keys, bf16 K/V",
+             "l2_policy": f"{copies} rotated input copies",
+             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(gbs / peak, 4),
+                          "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)},
+             "clocks": clocks}
+    if with_oracle:
+        import oracle
+        out, lse = decs[0]()
+        torch.cuda.synchronize()
+        out_bits = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        lse_h = lse.cpu().numpy()
+        del decs, keep
+        torch.cuda.empty_cache()
+        kpo = oracle.pool_keys(c["k_idx"], c["pool_w"], c["seq_len"], P)
+        t0 = time.perf_counter()
+        ck, sk = oracle.quantize_rows_e4m3(kpo)
+        cq, sq = oracle.quantize_rows_e4m3(c["q_idx"])
+        s = oracle.index_scores_e4m3(cq, sq, c["w_head"], ck, sk, c["seq_len"], P)
+        idx = oracle.topk(s, oracle.visible_counts(c["seq_len"], None, B, 1, P), k)
+        o_ref, l_ref = oracle.sparse_attn(c["q"], c["K"], c["V"], c["seq_len"], idx, P,
+                                          c["scale"])
+        dt = time.perf_counter() - t0
+        entry["cpu_baseline"] = {"value": round(B / dt, 3), "unit": UNIT, "cores": 1,
+                                 "host_cores": host_cores(), "kind": "oracle",
+                                 "sample": f"one full FP8 decode step, single thread, {dt:.1f} s"}
+        entry["parity_vs_fp8_oracle"] = _attn_parity(out_bits, o_ref[:, 0], lse_h, l_ref[:, 0])
+    else:
+        del decs, keep
+        torch.cuda.empty_cache()
+    return entry
+
+
 def per_config(args, torch, lcsw, peak, peaks):
     """The other named workloads, measured in the same run (entries of the one
     JSON line; the headline stays decode_1m)."""
@@ -872,6 +948,7 @@ def per_config(args, torch, lcsw, peak, peaks):
     res["prefill_4k"] = measure_prefill_chunk(20, 3, peaks, oracle_rows=16 if oracle_on else 0)
     torch.cuda.empty_cache()
     res["indexcache_reuse_1m"] = measure_reuse(torch, lcsw, peak, args._headline_step_ms)
+    res["decode_1m_fp8_keys"] = measure_decode_fp8(torch, lcsw, peak, oracle_on)
     return res
 
 

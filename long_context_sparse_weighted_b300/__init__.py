@@ -80,6 +80,8 @@ _SIGNATURES = {
     "lcsw_decode_fused": ([ctypes.POINTER(DecodeArgs), _vp, _sz, _vp], _i32),
     "lcsw_decode_launches": ([ctypes.POINTER(DecodeArgs)], _i32),
     "lcsw_decode_reuse": ([ctypes.POINTER(DecodeArgs), _vp, _vp, _sz, _vp], _i32),
+    "lcsw_quantize_keys_e4m3": ([_vp, _i64, _i32, _i32, _vp, _i64, _vp], _i32),
+    "lcsw_decode_fused_e4m3": ([ctypes.POINTER(DecodeArgs), _vp, _i64, _vp, _sz, _vp], _i32),
     "lcsw_prefill_workspace_size": ([ctypes.POINTER(PrefillArgs)], _sz),
     "lcsw_prefill": ([ctypes.POINTER(PrefillArgs), _vp, _sz, _vp], _i32),
     "lcsw_get_status": ([_vp, _vp], _i32),
@@ -253,6 +255,27 @@ def sparse_attn_noalloc(q, K, V, seq_len, idx, P, scale, out, lse=None, stream=N
     return out, lse
 
 
+E4M3_TILE_BYTES = 1088  # 16 rows of 64 E4M3 codes, then their 16 fp32 scales
+
+
+def e4m3_key_cache(B, G_max, device="cuda"):
+    """An FP8 pooled-key cache of B sequences x ceil(G_max/16) tiles (uint8)."""
+    return torch.zeros(B, (G_max + 15) // 16 * E4M3_TILE_BYTES, dtype=torch.uint8, device=device)
+
+
+def quantize_keys_e4m3(k_pooled, kq, n_groups=None, stream=None):
+    """Groups [0, n_groups) of every sequence's bf16 pooled keys into the FP8
+    cache kq ([B][tiles * 1088] uint8): per-row scale amax/448, E4M3 codes."""
+    _bf16(k_pooled, "k_pooled", 3)
+    if kq.dtype != torch.uint8 or not kq.is_cuda or not kq[0].is_contiguous():
+        raise ValueError("kq must be a CUDA uint8 tensor [B][bytes]")
+    B = k_pooled.shape[0]
+    n = k_pooled.shape[1] if n_groups is None else int(n_groups)
+    _check(lib().lcsw_quantize_keys_e4m3(_ptr(k_pooled), k_pooled.stride(0), B, n, _ptr(kq),
+                                         kq.stride(0), _stream(stream)))
+    return kq
+
+
 # ------------------------------------------------------------ decode step ---
 
 class Decoder:
@@ -264,9 +287,13 @@ class Decoder:
 
     def __init__(self, q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale,
                  k_idx=None, pool_w=None, out=None, lse=None, idx_out=None, scores_out=None,
-                 G_max=None, flags=0):
+                 G_max=None, flags=0, kq=None):
+        """kq: an FP8 pooled-key cache (e4m3_key_cache) to score from instead of
+        the bf16 k_pooled (lcsw_decode_fused_e4m3); k_pooled may then be None
+        when G_max is given."""
         _bf16(q_idx, "q_idx", 3)
-        _bf16(k_pooled, "k_pooled", 3)
+        if kq is None or k_pooled is not None:
+            _bf16(k_pooled, "k_pooled", 3)
         _bf16(q, "q", 3)
         _bf16(K, "K", 3)
         _bf16(V, "V", 3)
@@ -284,7 +311,8 @@ class Decoder:
         self._keep = (q_idx, w_head, k_pooled, q, K, V, seq_len, k_idx, pool_w)
         a = DecodeArgs()
         a.q_idx, a.w_head = q_idx.data_ptr(), w_head.data_ptr()
-        a.k_pooled, a.sp_b = k_pooled.data_ptr(), k_pooled.stride(0)
+        if k_pooled is not None:
+            a.k_pooled, a.sp_b = k_pooled.data_ptr(), k_pooled.stride(0)
         if k_idx is not None:
             _bf16(k_idx, "k_idx", 3)
             a.k_idx, a.sk_b = k_idx.data_ptr(), k_idx.stride(0)
@@ -294,6 +322,9 @@ class Decoder:
         a.V, a.sV_b = V.data_ptr(), V.stride(0)
         a.seq_len = seq_len.data_ptr()
         a.B, a.G_max = B, int(G_max if G_max is not None else k_pooled.shape[1])
+        self.kq = kq
+        if kq is not None and (kq.dtype != torch.uint8 or not kq.is_cuda):
+            raise ValueError("kq must be a CUDA uint8 tensor")
         a.H_i, a.d_idx, a.P, a.k = H_i, d_idx, P, k
         a.H_q, a.d_qk, a.d_v, a.scale = H_q, d_qk, d_v, float(scale)
         a.out, a.lse = self.out.data_ptr(), self.lse.data_ptr()
@@ -302,7 +333,9 @@ class Decoder:
         a.flags = int(flags)
         self.args = a
         self.ws_bytes = lib().lcsw_decode_workspace_size(ctypes.byref(a))
-        self.launches_per_call = lib().lcsw_decode_launches(ctypes.byref(a))
+        # the FP8 step is always the one persistent launch (or an error)
+        self.launches_per_call = 1 if kq is not None else \
+            lib().lcsw_decode_launches(ctypes.byref(a))
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
 
     def rebind(self, **tensors):
@@ -313,8 +346,15 @@ class Decoder:
         self._rebound = tensors
 
     def __call__(self, stream=None):
-        _check(lib().lcsw_decode_fused(ctypes.byref(self.args), ctypes.c_void_p(self.ws.data_ptr()),
-                                       self.ws_bytes, _stream(stream)))
+        if self.kq is not None:
+            _check(lib().lcsw_decode_fused_e4m3(ctypes.byref(self.args), _ptr(self.kq),
+                                                self.kq.stride(0),
+                                                ctypes.c_void_p(self.ws.data_ptr()),
+                                                self.ws_bytes, _stream(stream)))
+        else:
+            _check(lib().lcsw_decode_fused(ctypes.byref(self.args),
+                                           ctypes.c_void_p(self.ws.data_ptr()), self.ws_bytes,
+                                           _stream(stream)))
         return self.out, self.lse
 
     def status(self, stream=None):

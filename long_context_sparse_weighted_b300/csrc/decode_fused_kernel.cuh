@@ -219,11 +219,18 @@ __device__ unsigned g_dbg_max[4];
     do {                                                                 \
         if (threadIdx.x == 0) atomicMax(&g_dbg_max[i], unsigned(v));     \
     } while (0)
+#define DBG_ADD(i, v)                                                    \
+    do {                                                                 \
+        if (threadIdx.x == 0) atomicAdd(&g_dbg_max[i], unsigned(v));     \
+    } while (0)
 #define PHASE_MARK(i)                                                    \
     do {                                                                 \
         if (threadIdx.x == 0) g_stamp[blockIdx.x][i] = (long long)globaltimer_ns();        \
     } while (0)
 #else
+#define DBG_ADD(i, v) \
+    do {              \
+    } while (0)
 #define PHASE_MARK(i) \
     do {              \
     } while (0)
@@ -767,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
 
     // ---- roles: blocks per sequence, proportional to its cost ------------------
     int b, cb0, n_b, L_b, G_b;
-    if (tid == 0) { sv[19] = 0; sv[27] = 0; sv[31] = 0; }
+    if (tid == 0) { sv[19] = 0; sv[27] = 0; sv[31] = 0; sv[32] = 0; sv[33] = 0; sv[34] = 0; }
     if (B == 1) {
         L_b = L_first;
         G_b = L_b / P;
@@ -1078,15 +1085,25 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     PHASE_MARK(3);
 
     // ---- candidates: this block's keys at or above its threshold -------------
+    // The prefetch list (spec_g) takes the keys above the threshold bin first
+    // (fewer than the quota, so all of them fit): the block's selected groups
+    // are its highest keys.
     const unsigned tj = unsigned(sv[3]);
     int cand_tot;
     {
         const int per = (nloc + kThreads - 1) / kThreads;
         const int i0 = min(nloc, tid * per), i1 = min(nloc, i0 + per);
-        int nc = 0;
-        for (int i = i0; i < i1; ++i) nc += (score_key(score_at(i)) >> 16) >= tj;
+        int nc = 0, na = 0;
+        for (int i = i0; i < i1; ++i) {
+            const unsigned k16 = score_key(score_at(i)) >> 16;
+            nc += k16 >= tj;
+            na += k16 > tj;
+        }
+        na = __reduce_add_sync(0xffffffffu, na);
+        if (lane == 0 && na) atomicAdd(sv + 32, na);
         PHASE_MARK(5);
-        int pos = block_exclusive_scan(nc, scratch, &cand_tot);
+        int pos = block_exclusive_scan(nc, scratch, &cand_tot);  // (synchronises)
+        const int n_above = sv[32];
         unsigned long long *slot = slots_cur + size_t(cta) * kSlotWords;
         // the header (count + 1, nonzero once written, and t_j) goes out first:
         // readers check every entry it announces for themselves
@@ -1100,7 +1117,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 const unsigned long long e = key | ((unsigned long long)(g_lo + i) << 32);
                 if (pos < kSlot) st_relaxed_u64(slot + 1 + pos, e);
                 else st_relaxed_u64(cand_cur + seg + g_lo + pos - kSlot, e);
-                if (pos < kChunk / P) spec_g[pos] = g_lo + i;
+                const int sp = (key >> 16) > tj ? atomicAdd(sv + 33, 1)
+                                                : n_above + atomicAdd(sv + 34, 1);
+                if (sp < kChunk / P) spec_g[sp] = g_lo + i;
                 ++pos;
             }
         }
@@ -1346,9 +1365,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             const unsigned long long rl = lane < m_own ? crank[own0 + lane] : ~0ull;
             const bool pick = lane < m_own && rank[lane] < k_b;
             const unsigned bsel = __ballot_sync(0xffffffffu, pick);
-            if (pick) own[__popc(bsel & ((1u << lane) - 1u))] = int(0xFFFFFFFFu - unsigned(rl));
-            // the prefetch holds this block's first n_spec candidates
-            const bool cover = n_spec >= 32 || (bsel >> n_spec) == 0u;
+            const int grp = int(0xFFFFFFFFu - unsigned(rl));
+            if (pick) own[__popc(bsel & ((1u << lane) - 1u))] = grp;
+            // the prefetch covers the block if it holds every selected group
+            bool found = !pick;
+            for (int s2 = 0; s2 < n_spec && !found; ++s2) found = spec_g[s2] == grp;
+            const bool cover = __all_sync(0xffffffffu, found);
             if (lane == 0) {
                 sv[16] = __popc(bsel);
                 sv[18] = cover ? 1 : 0;
@@ -1357,8 +1379,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         __syncthreads();
         n_own = sv[16];
         use_spec = sv[18] != 0;
-        if (use_spec && tid < spec_cap && !(tid < m_own && rank[tid] < k_b))
-            spec_sg[tid] = -1;  // prefetched but not selected: masked
+        if (use_spec && tid < spec_cap) {
+            bool keep = false;
+            if (tid < n_spec)
+                for (int i = 0; i < n_own; ++i) keep |= own[i] == spec_g[tid];
+            if (!keep) spec_sg[tid] = -1;  // prefetched but not selected: masked
+        }
     } else if (fast) {
         unsigned kth = 0xFFFFFFFFu, take_eq = 0;
         if (k_b > 0) {
@@ -1504,6 +1530,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         __syncthreads();
     }
     PHASE_MARK(14);
+    DBG_ADD(0, fast && !by_rank);
+    DBG_ADD(1, fast && !use_spec && n_own > 0);
+    DBG_MAX(2, m_own);
+    DBG_ADD(3, !fast);
     if (!fast) {
         cp_async_wait<0>();  // the prefetch lands before region U is reused
         __syncthreads();
