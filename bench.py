@@ -55,11 +55,15 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--copies", type=int, default=0,
                     help="rotated input copies (0: enough to exceed 3x L2)")
-    ap.add_argument("--kernel", default=None, choices=["prefill_scores", "prefill"],
+    ap.add_argument("--kernel", default=None,
+                    choices=["prefill_scores", "prefill", "pool_keys", "index_scores", "topk",
+                             "sparse_attn", "decode", "decode_fp8"],
                     help="time one kernel of the path instead of the decode step (not the "
                          "headline line): prefill_scores = the chunked-prefill indexer "
                          "scores (tcgen05 GEMM) on the prefill_4k shapes; prefill = one whole "
-                         "lcsw_prefill chunk of prefill_4k (pool, fused selection, attention)")
+                         "lcsw_prefill chunk of prefill_4k (pool, fused selection, attention); "
+                         "pool_keys / index_scores / topk / sparse_attn = one standalone step on "
+                         "the decode_1m shapes; decode / decode_fp8 = single fused decode calls")
     return ap.parse_args()
 
 
@@ -962,8 +966,85 @@ def run_prefill_chunk(args):
     print(json.dumps(dict(entry, workload="prefill_4k")))
 
 
+def run_kernel_alone(args):
+    """One step of the path on the decode_1m shapes, timed alone: CUDA events
+    around each call, inputs larger than L2 (the 128 MB raw keys, the 32 MB
+    pooled keys with the 1 MB of scores), median over the calls.  Prints the
+    kernel's algorithmic bytes and its fraction of the measured HBM peak."""
+    import torch
+
+    import long_context_sparse_weighted_b300 as lcsw
+    spec = synth.named("decode_1m")
+    c = synth.generate(spec, with_kv=args.kernel in ("sparse_attn", "decode", "decode_fp8"))
+    P, B, k = spec.P, spec.B, spec.k
+    dev = "cuda"
+    up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    seq = torch.from_numpy(c["seq_len"]).to(dev)
+    k_idx, pool_w = up16(c["k_idx"]), torch.from_numpy(c["pool_w"]).to(dev)
+    kp = torch.zeros(B, spec.G_max, 64, dtype=torch.bfloat16, device=dev)
+    lcsw.pool_keys(k_idx, pool_w, seq, P, kp)
+    G = spec.G_max
+    qi, w = up16(c["q_idx"]), torch.from_numpy(c["w_head"]).to(dev)
+    scores = torch.empty(B, 1, G, dtype=torch.float32, device=dev)
+    nv = lcsw.visible_counts(seq, None, B, 1, P)
+    if args.kernel == "pool_keys":
+        fn = lambda: lcsw.pool_keys(k_idx, pool_w, seq, P, kp)
+        ab = G * (P * 128 + P * 4 + 128)
+    elif args.kernel == "index_scores":
+        fn = lambda: lcsw.index_scores(qi, w, kp, seq, P, out=scores)
+        ab = G * 128 + G * 4 + spec.H_i * (128 + 4)
+    elif args.kernel == "topk":
+        lcsw.index_scores(qi, w, kp, seq, P, out=scores)
+        idx = torch.empty(B, 1, k, dtype=torch.int32, device=dev)
+        fn = lambda: lcsw.topk_groups(scores, nv, k, out=idx)
+        ab = G * 4 + k * 4
+    else:
+        lcsw.index_scores(qi, w, kp, seq, P, out=scores)
+        idx = lcsw.topk_groups(scores, nv, k)
+        q, K, V = up16(c["q"]), up16(c["K"]), up16(c["V"])
+        ab = P * k * (spec.d_qk + spec.d_v) * 2 + spec.H_q * (spec.d_qk + spec.d_v) * 2
+        if args.kernel == "sparse_attn":
+            ws = torch.empty(lcsw.lib().lcsw_sparse_attn_workspace_size(B, 1, spec.H_q, spec.d_v,
+                                                                       k, P), dtype=torch.uint8,
+                             device=dev)
+            fn = lambda: lcsw.sparse_attn(q, K, V, seq, idx, P, c["scale"], ws=ws)
+        else:
+            ab += G * (68 if args.kernel == "decode_fp8" else 128) + spec.H_i * (128 + 4)
+            kq = None
+            if args.kernel == "decode_fp8":
+                kq = lcsw.e4m3_key_cache(B, G)
+                lcsw.quantize_keys_e4m3(kp, kq)
+            dec = lcsw.Decoder(qi[:, 0], w[:, 0], None if kq is not None else kp, q[:, 0], K, V,
+                               seq, P, k, c["scale"], k_idx=k_idx, pool_w=pool_w, G_max=G, kq=kq)
+            fn = dec
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 200))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in evs)[n // 2]
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = peaks.get("hbm_gbs", 6400.0)
+    gbs = ab / (ms / 1e3) / 1e9
+    print(json.dumps({"kernel": args.kernel, "workload": "decode_1m", "ms": round(ms, 5),
+                      "calls": n, "alg_bytes": ab, "gbs": round(gbs, 1), "hbm_peak_gbs": peak,
+                      "frac": round(gbs / peak, 4)}))
+
+
 def main():
     args = parse()
+    if args.kernel in ("pool_keys", "index_scores", "topk", "sparse_attn", "decode",
+                       "decode_fp8"):
+        run_kernel_alone(args)
+        return
     if args.kernel == "prefill_scores":
         run_prefill_scores(args)
         return

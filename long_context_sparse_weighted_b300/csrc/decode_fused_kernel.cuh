@@ -89,9 +89,12 @@ constexpr int kSlowB = 1, kSlowC = 2, kSlowD = 3, kNumCounters = 4;
 constexpr int kStream = kWarps;    // streaming warps
 // Phase 1 streams the block's pooled keys through per-warp rings in shared
 // memory filled by bulk copies: warp w scores tiles w, w + 16, w + 32, ... of
-// the block's chunk (16 groups, 2 KB each) and keeps kRing of them in flight.
+// the block's chunk (16 groups, 2 KB each) and keeps kRing of them in flight;
+// FP8 tiles are 1088 bytes, so their rings hold kRingF8 of them.
 constexpr int kRing = 4;
 constexpr int kTileBytes = 16 * 128;
+constexpr int kRingF8 = 7;
+constexpr int kRingMax = kRingF8 > kRing ? kRingF8 : kRing;
 
 // shared memory map (bytes); region U is reused phase by phase:
 //   stream      per-warp rings [kWarps][kRing][kTileBytes]
@@ -105,6 +108,7 @@ constexpr int kTileBytes = 16 * 128;
 constexpr int kU = 0;
 constexpr int kUBytes = kFine * 2;
 static_assert(kWarps * kRing * kTileBytes <= kUBytes, "stream rings overflow region U");
+static_assert(kWarps * kRingF8 * (16 * 64 + 16 * 4) <= kUBytes, "FP8 rings overflow region U");
 constexpr int kScores = kU + kUBytes;                 // [kChunkCap] floats
 constexpr int kMisc = kScores + kChunkCap * 4;        // small arrays and scalars
 constexpr int kMiscBytes = 128 + (3 * (kMaxCtas + 1) + 64 + 40 + 64 + kChunk + 32) * 4;
@@ -112,8 +116,8 @@ static_assert(kMiscBytes <= 4096, "small arrays overflow their region");
 constexpr int kSelList = kMisc + 4096;                // own selected groups [kMaxK]
 constexpr int kNewRows = kSelList + kMaxK * 4;        // newest group: [8][64] bf16, [8] f32
 constexpr int kNewCode = kNewRows + 8 * 128 + 8 * 4;  // its FP8 row: [64] codes, scale
-constexpr int kRingBars = kNewCode + 64 + 16;         // [kWarps][kRing] mbarriers
-constexpr int kSmemBytes = kRingBars + kWarps * kRing * 8;
+constexpr int kRingBars = kNewCode + 64 + 16;         // [kWarps][ring depth] mbarriers
+constexpr int kSmemBytes = kRingBars + kWarps * kRingMax * 8;
 static_assert(kRingBars % 8 == 0, "mbarrier alignment");
 
 // Attention operands: Q [64 heads][QP], NBUF chunk buffers (each K [64
@@ -198,15 +202,25 @@ struct Params {
     int *abort_flag;      // ws word 1
 };
 
-// D = A(16x32, row) * B(32x8, col) + D with E4M3 inputs and fp32 accumulators.
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
+// D = A(16x16, row) * B(16x8, col) + D, f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (bits 0-15 of w, the lower code in bits 0-7) as an f16x2 pair;
+// every E4M3 value is exact in f16.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n .reg .b16 t;\n mov.b16 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
+        : "=r"(r)
+        : "h"((unsigned short)(w & 0xFFFFu)));
+    return r;
 }
 
 // ------------------------------------------------------------ phase timers -
@@ -663,10 +677,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     // the end of this one)
     const int2 ovf_old = p.ovf[(par ^ 1) * ncta + cta];
 
-    // Each warp streams through its own ring of kRing tiles (lane 0 issues the
+    // Each warp streams through its own ring of RING tiles (lane 0 issues the
     // bulk copies; completion on the slot's mbarrier).
-    unsigned char *ring = smem + kU + warp * kRing * kTileBytes;
-    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + kRingBars) + warp * kRing;
+    constexpr int RING = F8 ? kRingF8 : kRing;
+    constexpr int SLOT = F8 ? kE4m3TileBytes : kTileBytes;
+    unsigned char *ring = smem + kU + warp * RING * SLOT;
+    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + kRingBars) + warp * RING;
     int n_issued = 0;  // lane 0: tiles of this warp issued so far
     // lane 0: this warp's tile kk of the chunk [lo, hi) of sequence bb's pooled
     // keys (bf16 rows, or whole FP8 tiles of 16 groups)
@@ -681,8 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             src = p.k_pooled + int64_t(bb) * p.sp_b + int64_t(g0) * 64;
             bytes = uint32_t(min(16, hi - g0)) * 128u;
         }
-        mbar_expect_tx(wbar + kk % kRing, bytes);
-        bulk_load(ring + (kk % kRing) * kTileBytes, src, bytes, wbar + kk % kRing);
+        mbar_expect_tx(wbar + kk % RING, bytes);
+        bulk_load(ring + (kk % RING) * SLOT, src, bytes, wbar + kk % RING);
         ++n_issued;
     };
     auto warp_tiles = [&](int lo, int hi) {
@@ -690,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         return nt > warp ? (nt - warp + kStream - 1) / kStream : 0;
     };
     if (lane == 0) {
-        for (int i = 0; i < kRing; ++i) mbar_init(wbar + i, 1);
+        for (int i = 0; i < RING; ++i) mbar_init(wbar + i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // the indexer query of sequence bb as mma.sync B fragments (head nt*8 + r,
@@ -698,20 +714,35 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     const int r = lane >> 2, c = lane & 3;
     uint32_t bq[NT][4][2];
     float wv[NT][2];
-    float sqh[NT];  // FP8: scale of head nt*8 + r
-    auto load_query = [&](int bb) {
+    // The indexer query of sequence bb: raw bf16 loads first (fetch_query),
+    // then its fragments (prep_query).  bf16: head nt*8 + r as mma.sync B
+    // fragments, k-permuted like the keys.  FP8: dims [16c, 16c + 16) of the
+    // head quantized under the head's scale (the four lanes c of a head share
+    // its amax), as f16 pairs of the codes; k-step s takes the codes of dims
+    // 16c + 4s .. 16c + 4s + 3.
+    uint4 qraw[NT][2];
+    auto fetch_query = [&](int bb) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int head = nt * 8 + r;
-            uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+            qraw[nt][0] = qraw[nt][1] = make_uint4(0, 0, 0, 0);
+            if (head < p.H_i) {
+                const uint16_t *qp = p.q_idx + (int64_t(bb) * p.H_i + head) * 64;
+                qraw[nt][0] = ld_nc16(qp + (F8 ? 16 * c : 8 * c));
+                qraw[nt][1] = ld_nc16(qp + (F8 ? 16 * c + 8 : 32 + 8 * c));
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = nt * 8 + 2 * c + e;
+                wv[nt][e] = h < p.H_i ? __ldg(p.w_head + int64_t(bb) * p.H_i + h) : 0.f;
+            }
+        }
+    };
+    auto prep_query = [&]() {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint4 h0 = qraw[nt][0], h1 = qraw[nt][1];
             if constexpr (F8) {
-                // dims [16c, 16c + 16) of the head as E4M3 codes under the head's
-                // scale (the four lanes c of a head share its amax)
-                if (head < p.H_i) {
-                    const uint16_t *qp = p.q_idx + (int64_t(bb) * p.H_i + head) * 64;
-                    h0 = ld_nc16(qp + 16 * c);
-                    h1 = ld_nc16(qp + 16 * c + 8);
-                }
                 const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
                 float amax = 0.f;
 #pragma unroll
@@ -722,35 +753,26 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 const float sc = e4m3_row_scale(amax);
                 uint32_t w[4] = {0u, 0u, 0u, 0u};
                 if (sc != 0.f) {
+                    const float inv = __frcp_rn(sc);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float x = (i & 1) ? bf_hi(hw[i / 2]) : bf_lo(hw[i / 2]);
-                        w[i / 4] |= e4m3_quantize(x, sc) << (8 * (i % 4));
+                        w[i / 4] |= e4m3_quantize(x, sc, inv) << (8 * (i % 4));
                     }
                 }
-                // k-permutation: k-step s takes words 2s (a0/b0) and 2s + 1 (a2/b1)
-                bq[nt][0][0] = w[0]; bq[nt][0][1] = w[1];
-                bq[nt][1][0] = w[2]; bq[nt][1][1] = w[3];
-                sqh[nt] = sc;
-            } else {
-                if (head < p.H_i) {
-                    const uint16_t *qp = p.q_idx + (int64_t(bb) * p.H_i + head) * 64;
-                    h0 = ld_nc16(qp + 8 * c);
-                    h1 = ld_nc16(qp + 32 + 8 * c);
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2) {
+                    bq[nt][s2][0] = e4m3x2_f16x2(w[s2]);
+                    bq[nt][s2][1] = e4m3x2_f16x2(w[s2] >> 16);
                 }
+                // the accumulator's heads nt*8 + 2c + e take that head's query scale
+#pragma unroll
+                for (int e = 0; e < 2; ++e) wv[nt][e] *= __shfl_sync(0xffffffffu, sc, (2 * c + e) * 4);
+            } else {
                 bq[nt][0][0] = h0.x; bq[nt][0][1] = h0.y;
                 bq[nt][1][0] = h0.z; bq[nt][1][1] = h0.w;
                 bq[nt][2][0] = h1.x; bq[nt][2][1] = h1.y;
                 bq[nt][3][0] = h1.z; bq[nt][3][1] = h1.w;
-            }
-            // head weights of the accumulator's heads nt*8 + 2c + e (FP8: times
-            // that head's query scale)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int h = nt * 8 + 2 * c + e;
-                float wt = h < p.H_i ? __ldg(p.w_head + int64_t(bb) * p.H_i + h) : 0.f;
-                if constexpr (F8) wt *= __shfl_sync(0xffffffffu, sqh[nt], (2 * c + e) * 4);
-                wv[nt][e] = wt;
             }
         }
     };
@@ -761,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     int L_first = 0;
     if (B == 1) {
         L_first = __ldg(p.seq_len);
-        load_query(0);
+        fetch_query(0);
     }
     int spec_lo = 0, spec_hi = 0;
     if (B == 1 && lane == 0) {
@@ -769,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         spec_lo = 16 * int((long long)tiles0 * cta / ncta);
         spec_hi = min(p.G_max, 16 * int((long long)tiles0 * (cta + 1) / ncta));
         const int n0 = warp_tiles(spec_lo, spec_hi);
-        for (int kk = 0; kk < min(kRing, n0); ++kk) issue_tile_of(0, spec_lo, spec_hi, kk);
+        for (int kk = 0; kk < min(RING, n0); ++kk) issue_tile_of(0, spec_lo, spec_hi, kk);
     }
 
     // ---- roles: blocks per sequence, proportional to its cost ------------------
@@ -794,6 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             G = G < 0 ? 0 : (G > p.G_max ? p.G_max : G);
             wv = 2 * G + min(p.k, G) * P * ((DQK + DV) / 32);
         }
+        // one block per sequence, the rest in proportion to cost
         int total;
         const int pre = block_exclusive_scan(wv, scratch, &total);
         if (tid < B) offs[tid] = pre;
@@ -831,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
 
     // ---- phase-1 prologue: first tiles in flight, indexer query, append -------
     // The block's chunk of pooled keys is one contiguous range.  Lane 0 of each
-    // warp has the warp's first kRing tiles in flight (issued above when the
+    // warp has the warp's first RING tiles in flight (issued above when the
     // guessed chunk was right), so the prologue's own loads overlap them, and
     // refills a slot as soon as the warp has read it.
     const int n_mine = warp_tiles(g_lo, g_hi);
@@ -840,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         if (B == 1 && (spec_lo != g_lo || spec_hi != g_hi)) {
             // the guess was wrong: let its copies land, then start over
             for (int kk = 0; kk < n_issued; ++kk) mbar_wait(wbar + kk, 0u, kWaitNs);
-            for (int i = 0; i < kRing; ++i) {
+            for (int i = 0; i < RING; ++i) {
                 asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(wbar + i))
                              : "memory");
                 mbar_init(wbar + i, 1);
@@ -848,9 +871,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             n_issued = 0;
         }
-        for (int kk = n_issued; kk < min(kRing, n_mine); ++kk) issue_tile(kk);
+        for (int kk = n_issued; kk < min(RING, n_mine); ++kk) issue_tile(kk);
     }
-    if (B > 1) load_query(b);
+    if (B > 1) fetch_query(b);
+    prep_query();
 
     PHASE_MARK(23);
     // append: the group the newest token completes is pooled by the warp
@@ -880,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
         float ska = 1.f, skb = 1.f;  // FP8: the two rows' key scales
         if constexpr (F8) {
-            // rows r and r + 8: codes [16c, 16c + 16) (words 2s, 2s + 1 feed k-step s)
+            // rows r and r + 8: codes [16c, 16c + 16); word s feeds k-step s
             uint4 Ar = *reinterpret_cast<const uint4 *>(tile + r * 64 + 16 * c);
             uint4 Ab = *reinterpret_cast<const uint4 *>(tile + (r + 8) * 64 + 16 * c);
             ska = *reinterpret_cast<const float *>(tile + 1024 + 4 * r);
@@ -893,10 +917,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 Ab = *reinterpret_cast<const uint4 *>(newcode + 16 * c);
                 skb = *newscale;
             }
+            const uint32_t wr[4] = {Ar.x, Ar.y, Ar.z, Ar.w}, wb[4] = {Ab.x, Ab.y, Ab.z, Ab.w};
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                mma_e4m3_16832(acc[nt], Ar.x, Ab.x, Ar.y, Ab.y, bq[nt][0][0], bq[nt][0][1]);
-                mma_e4m3_16832(acc[nt], Ar.z, Ab.z, Ar.w, Ab.w, bq[nt][1][0], bq[nt][1][1]);
+            for (int s2 = 0; s2 < 4; ++s2) {
+                const uint32_t a0 = e4m3x2_f16x2(wr[s2]), a2 = e4m3x2_f16x2(wr[s2] >> 16);
+                const uint32_t a1 = e4m3x2_f16x2(wb[s2]), a3 = e4m3x2_f16x2(wb[s2] >> 16);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_f16_16816(acc[nt], a0, a1, a2, a3, bq[nt][s2][0], bq[nt][s2][1]);
             }
         } else {
             uint4 A[4];
@@ -952,9 +980,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     // warp's work but not its barriers.
     bool stream_ok = true;
     for (int kk = 0; kk < n_mine; ++kk) {
-        const int slot = kk % kRing, t = warp + kk * kStream;
+        const int slot = kk % RING, t = warp + kk * kStream;
         if (stream_ok &&
-            !__all_sync(0xffffffffu, mbar_wait(wbar + slot, unsigned(kk / kRing) & 1u, kWaitNs))) {
+            !__all_sync(0xffffffffu, mbar_wait(wbar + slot, unsigned(kk / RING) & 1u, kWaitNs))) {
             stream_ok = false;  // warp-uniform: score_tile shuffles across the warp
             raise_timeout(p, 7);
             sv[19] = 1;
@@ -979,10 +1007,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                     const float sc = e4m3_row_scale(amax);
                     uint32_t cw[2] = {0u, 0u};
                     if (sc != 0.f) {
+                        const float inv = __frcp_rn(sc);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float x = (i & 1) ? bf_hi(ws[i / 2]) : bf_lo(ws[i / 2]);
-                            cw[i / 4] |= e4m3_quantize(x, sc) << (8 * (i % 4));
+                            cw[i / 4] |= e4m3_quantize(x, sc, inv) << (8 * (i % 4));
                         }
                     }
                     uint8_t *trow = p.kq + int64_t(b) * p.sq_b +
@@ -998,21 +1027,21 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 __syncwarp();
             }
         }
-        if (stream_ok) score_tile(t, ring + slot * kTileBytes);
+        if (stream_ok) score_tile(t, ring + slot * SLOT);
         __syncwarp();
-        if (lane == 0 && stream_ok && kk + kRing < n_mine) {
+        if (lane == 0 && stream_ok && kk + RING < n_mine) {
             fence_async_smem();  // the warp's reads of the slot come before the copy
-            issue_tile(kk + kRing);
+            issue_tile(kk + RING);
         }
     }
     if (lane == 0) {
         if (stream_ok) {  // every copy landed: retire the barriers
-            for (int i = 0; i < kRing; ++i)
+            for (int i = 0; i < RING; ++i)
                 asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(wbar + i))
                              : "memory");
         } else {  // the copies in flight land before the block leaves or reuses the ring
-            for (int kk = max(0, n_issued - kRing); kk < n_issued; ++kk)
-                mbar_wait(wbar + kk % kRing, unsigned(kk / kRing) & 1u, kWaitNs);
+            for (int kk = max(0, n_issued - RING); kk < n_issued; ++kk)
+                mbar_wait(wbar + kk % RING, unsigned(kk / RING) & 1u, kWaitNs);
         }
     }
     kmax16 = __reduce_max_sync(0xffffffffu, kmax16);

@@ -7,7 +7,7 @@
 //
 //   scale = amax(|x|) / 448 (fp32),  code_i = e4m3(x_i / scale)  (0 if scale = 0)
 //
-// The rounding decision is exact: the fp32 quotient proposes a code, and the
+// The rounding decision is exact: an fp32 quotient proposes a code, and the
 // sign of x - m * scale, with m the midpoint between that code and its
 // neighbour on the quotient's side, settles it (an FMA forms that difference
 // with one rounding, which keeps its sign).
@@ -30,11 +30,15 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
     return (c & 0x80u) ? -mag : mag;
 }
 
-// Nearest code of x / scale (scale > 0), ties to the even code, saturating.
-__device__ __forceinline__ uint32_t e4m3_quantize(float x, float scale) {
+// Nearest code of x / scale (scale > 0; inv = 1 / scale, rounded), ties to
+// the even code, saturating.  The quotient only proposes a code: within a
+// few ulps of the exact one, it lands on the right code or its neighbour,
+// and the midpoint test below decides between them.
+__device__ __forceinline__ uint32_t e4m3_quantize(float x, float scale, float inv) {
     const uint32_t sign = (__float_as_uint(x) >> 24) & 0x80u;
     const float a = fabsf(x);
-    const float q = __fdiv_rn(a, scale);
+    // (a scale too small for its reciprocal to be finite takes the division)
+    const float q = isinf(inv) ? __fdiv_rn(a, scale) : __fmul_rn(a, inv);
     if (q >= 448.f) return sign | 0x7Eu;
     // proposed code from the rounded quotient
     uint32_t c;
@@ -44,7 +48,7 @@ __device__ __forceinline__ uint32_t e4m3_quantize(float x, float scale) {
         c = pair & 0x7Fu;
     }
     const float v = e4m3_value(c);
-    if (q == v) return sign | c;  // the exact quotient lies within half an fp32 ulp of v
+    if (q == v) return sign | c;  // the exact quotient is within a few ulps of the code v
     // midpoint between c and its neighbour on the quotient's side
     const uint32_t lo = q > v ? c : c - 1u, hi = lo + 1u;
     const float mid = 0.5f * (e4m3_value(lo) + e4m3_value(hi));

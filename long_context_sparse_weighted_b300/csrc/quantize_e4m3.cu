@@ -38,8 +38,9 @@ __global__ void __launch_bounds__(256) quantize_keys_kernel(const uint16_t *__re
     const float sc = e4m3_row_scale(amax);
     uint32_t c[2] = {0u, 0u};
     if (sc != 0.f) {
+        const float inv = __frcp_rn(sc);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c[i / 4] |= e4m3_quantize(x[i], sc) << (8 * (i % 4));
+        for (int i = 0; i < 8; ++i) c[i / 4] |= e4m3_quantize(x[i], sc, inv) << (8 * (i % 4));
     }
     uint8_t *tile = kq + int64_t(b) * sq_b + int64_t(g / 16) * kE4m3TileBytes;
     *reinterpret_cast<uint2 *>(tile + (g % 16) * 64 + sub * 8) = make_uint2(c[0], c[1]);

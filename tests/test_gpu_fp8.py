@@ -44,10 +44,6 @@ def unpack_tiles(kq, G):
     return codes, scales
 
 
-def _bits(x):
-    return np.asarray(x, np.float32).view(np.uint32) >> 16
-
-
 def test_quantize_keys_bit_exact():
     rng = np.random.default_rng(70)
     B, G = 3, 700
@@ -58,6 +54,7 @@ def test_quantize_keys_bit_exact():
     x[0, 1, 7] = 3.0
     x[1, 2] *= 1e-30                                  # subnormal quotients
     x[1, 3] *= 1e30                                   # large magnitudes
+    x[1, 6] *= 1e-37                                  # a scale whose reciprocal overflows
     x[2, 4, :] = np.linspace(-448.0, 448.0, 64)        # amax 448: scale 1, E4M3 grid
     x[2, 5, :] = np.arange(64) * 0.5 + 1.0             # many midpoints between codes
     kp = (x.view(np.uint32) >> 16).astype(np.uint16)
