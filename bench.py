@@ -183,6 +183,15 @@ def kernel_source_sha(files):
     return h.hexdigest()[:16]
 
 
+# sources of the fused decode kernel, hashed to tie a committed ncu summary to them
+DECODE_SHA_FILES = ["decode_fused.cu", "decode_fused_kernel.cuh", "fused.cuh", "common.cuh",
+                    "attn_core.cuh", "pool_core.cuh", "select_core.cuh", "tc_core.cuh",
+                    "e4m3_core.cuh"]
+DECODE_E4M3_SHA_FILES = ["decode_fused.cu", "decode_fused_e4m3.cu", "decode_fused_kernel.cuh",
+                         "fused.cuh", "common.cuh", "attn_core.cuh", "pool_core.cuh",
+                         "select_core.cuh", "tc_core.cuh", "e4m3_core.cuh"]
+
+
 def profiled_traffic(summary_file, files):
     """dram bytes/launch from a committed ncu summary, if its source hash matches."""
     path = os.path.join(ROOT, "profiles", summary_file)
@@ -368,8 +377,7 @@ def run_lcsw(args, world, rank, local):
         kern_ms = step_ms
         single_ms = time_launches(torch, decs, 50)
         kern_name, kern_bytes = "lcsw_decode_fused (persistent kernel)", ab
-        sha_files = ["decode_fused.cu", "fused.cuh", "common.cuh", "attn_core.cuh",
-                     "pool_core.cuh", "select_core.cuh", "tc_core.cuh"]
+        sha_files = DECODE_SHA_FILES
         prof_file = f"decode_fused_{args.workload}.md"
     else:
         # multi-kernel path: the indexer scoring kernel moves ~97% of the bytes
@@ -913,7 +921,9 @@ def measure_decode_fp8(torch, lcsw, peak, with_oracle):
              "l2_policy": f"{copies} rotated input copies",
              "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                           "frac": round(gbs / peak, 4),
-                          "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)},
+                          "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                          "traffic": profiled_traffic("decode_fused_e4m3_decode_1m.md",
+                                                      DECODE_E4M3_SHA_FILES)},
              "clocks": clocks}
     if with_oracle:
         import oracle
@@ -968,8 +978,8 @@ def run_prefill_chunk(args):
 
 def run_kernel_alone(args):
     """One step of the path on the decode_1m shapes, timed alone: CUDA events
-    around each call, inputs larger than L2 (the 128 MB raw keys, the 32 MB
-    pooled keys with the 1 MB of scores), median over the calls.  Prints the
+    around each call, L2 overwritten before every call, median over the
+    calls.  Prints the
     kernel's algorithmic bytes and its fraction of the measured HBM peak."""
     import torch
 
@@ -1024,7 +1034,14 @@ def run_kernel_alone(args):
     n = max(1, min(args.steps, 200))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n)]
+    # before each call: overwrite a buffer twice the size of L2 (the call's
+    # inputs come from DRAM), then hold the device in a short spin so that the
+    # host has enqueued the call and its closing event before the first event
+    # fires (the span is device time only, without the host launch path)
+    scrub = torch.empty(2 * l2_bytes(), dtype=torch.uint8, device=dev)
     for a, b in evs:
+        scrub.fill_(1)
+        torch.cuda._sleep(200000)
         a.record()
         fn()
         b.record()
