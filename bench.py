@@ -57,7 +57,7 @@ def parse():
                     help="rotated input copies (0: enough to exceed 3x L2)")
     ap.add_argument("--kernel", default=None,
                     choices=["prefill_scores", "prefill", "pool_keys", "index_scores", "topk",
-                             "sparse_attn", "decode", "decode_fp8"],
+                             "sparse_attn", "decode", "decode_fp8", "kda", "reuse"],
                     help="time one kernel of the path instead of the decode step (not the "
                          "headline line): prefill_scores = the chunked-prefill indexer "
                          "scores (tcgen05 GEMM) on the prefill_4k shapes; prefill = one whole "
@@ -867,8 +867,9 @@ def measure_reuse(torch, lcsw, peak, full_step_ms):
     torch.cuda.empty_cache()
     return {"kernel": "lcsw_decode_reuse (split-K attention over the earlier layer's groups)",
             "ms_per_layer_step": round(ms, 5), "tokens_per_s": round(spec.B / (ms / 1e3), 1),
-            "two_layer_step_ms": {"both_select": round(2 * full_step_ms, 5),
-                                  "second_reuses": round(full_step_ms + ms, 5)},
+            "two_layer_step_ms": None if full_step_ms is None else {
+                "both_select": round(2 * full_step_ms, 5),
+                "second_reuses": round(full_step_ms + ms, 5)},
             "alg_bytes": ab, "timing": "median of 200 calls, each after a write of 2x L2",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(gbs / peak, 4)}}
@@ -952,6 +953,95 @@ def measure_decode_fp8(torch, lcsw, peak, with_oracle):
     return entry
 
 
+def kda_alg_bytes(B, T, H, D):
+    """Bytes a KDA step must move: the fp32 state read and written once, the
+    conv history read and written, the step's inputs (projections, gates,
+    conv taps) read and its output written."""
+    C = 3 * H * D
+    return (2 * B * H * D * D * 4 + 2 * B * 3 * C * 2 + B * T * C * 2 + C * 4 * 2
+            + B * T * H * D * 4 + B * T * H * 4 + B * T * H * D * 2)
+
+
+def measure_kda(torch, lcsw, peak, steps, warmup, with_oracle):
+    """KDA decode step, 64 sequences x 64 heads x 128 x 128 fp32 state (268 MB,
+    twice L2), one token per step, graph-captured steps on the same state
+    (updated in place, as in decoding).  Before timing, one step is compared
+    with the oracle on the first and last sequences."""
+    import synth.kda as skda
+    spec = skda.named("kda_decode_b64")
+    c = skda.generate(spec)
+    dev = "cuda"
+    up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    d = dict(qkv=up16(c["qkv"]), conv_w=up16(c["conv_w"]), conv_state=up16(c["conv_state"]),
+             g=torch.from_numpy(c["g"]).to(dev), beta=torch.from_numpy(c["beta"]).to(dev),
+             state=torch.from_numpy(c["state"]).to(dev))
+    out = torch.empty(spec.B, spec.T, spec.H, spec.D, dtype=torch.bfloat16, device=dev)
+    parity = None
+    if with_oracle:
+        import oracle.kda as okda
+        lcsw.kda_step(**d, out=out)
+        torch.cuda.synchronize()
+        worst_s = worst_o = 0.0
+        for b in (0, spec.B - 1):
+            sub = {k: (v[b:b + 1] if isinstance(v, np.ndarray) and k != "conv_w" else v)
+                   for k, v in c.items()}
+            o_ref, S_ref, cs_ref = okda.kda_step(sub["qkv"], c["conv_w"], sub["conv_state"],
+                                                 sub["g"], sub["beta"], sub["state"], spec.H,
+                                                 spec.D)
+            S = d["state"][b:b + 1].cpu().numpy().astype(np.float64)
+            o = synth.bf16_to_f32(out[b:b + 1].view(torch.int16).cpu().numpy().view(
+                np.uint16)).astype(np.float64)
+            smax = np.abs(S_ref).max(axis=(-2, -1), keepdims=True)
+            worst_s = max(worst_s, float((np.abs(S - S_ref) / smax).max()))
+            omax = np.abs(o_ref).max(axis=-1, keepdims=True)
+            worst_o = max(worst_o, float((np.abs(o - o_ref) / (2.0 ** -8 * np.abs(o_ref)
+                                                                + 1e-5 * omax)).max()))
+        parity = {"sequences_checked": 2, "state_err_over_head_max": worst_s,
+                  "out_err_over_bound": worst_o,
+                  "ok": bool(worst_s <= 4e-6 and worst_o <= 1.0)}
+    fn = [lambda: lcsw.kda_step(**d, out=out)]
+    ms, clocks = time_graph_steps(torch, fn, steps, warmup, 1)
+    step_ms = ms / steps
+    ab = kda_alg_bytes(spec.B, spec.T, spec.H, spec.D)
+    gbs = ab / (step_ms / 1e3) / 1e9
+    entry = {"kernel": "lcsw_kda_step (kda_step_kernel, one block per head and sequence)",
+             "config": {"batch": spec.B, "heads": spec.H, "head_dim": spec.D,
+                        "tokens_per_step": spec.T, "state_bytes": spec.B * spec.H * spec.D ** 2 * 4},
+             "tokens_per_s": round(spec.B * spec.T * steps / (ms / 1e3), 1),
+             "ms_per_step": round(step_ms, 6), "steps": steps, "alg_bytes_per_step": ab,
+             "dtype": "fp32 state, bf16 inputs/outputs",
+             "l2_policy": "state (268 MB) larger than L2",
+             "gpu_launches": steps,
+             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(gbs / peak, 4),
+                          "traffic": profiled_traffic("kda_step_kda_decode_b64.md",
+                                                      ["kda_step.cu", "common.cuh"])},
+             "clocks": clocks, "parity_vs_oracle": parity}
+    if with_oracle:
+        entry["cpu_baseline"] = kda_cpu_baseline(c, spec)
+    del d, out
+    torch.cuda.empty_cache()
+    return entry
+
+
+def kda_cpu_baseline(c, spec):
+    """The KDA oracle on one sequence (all heads, one token), timed on the host."""
+    import oracle.kda as okda
+    sub = {k: (v[0:1] if isinstance(v, np.ndarray) and k != "conv_w" else v) for k, v in c.items()}
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        okda.kda_step(sub["qkv"], c["conv_w"], sub["conv_state"], sub["g"], sub["beta"],
+                      sub["state"], spec.H, spec.D)
+        n += 1
+        if time.perf_counter() - t0 > 2.0:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(n * spec.T / dt, 3), "unit": "tokens/s", "cores": host_cores(),
+            "kind": "oracle", "sample": f"{n} single-sequence steps ({spec.H} heads, fp64 numpy)"}
+
+
 def per_config(args, torch, lcsw, peak, peaks):
     """The other named workloads, measured in the same run (entries of the one
     JSON line; the headline stays decode_1m)."""
@@ -963,6 +1053,7 @@ def per_config(args, torch, lcsw, peak, peaks):
     torch.cuda.empty_cache()
     res["indexcache_reuse_1m"] = measure_reuse(torch, lcsw, peak, args._headline_step_ms)
     res["decode_1m_fp8_keys"] = measure_decode_fp8(torch, lcsw, peak, oracle_on)
+    res["kda_decode_b64"] = measure_kda(torch, lcsw, peak, 200, 5, oracle_on)
     return res
 
 
@@ -1061,6 +1152,25 @@ def main():
     if args.kernel in ("pool_keys", "index_scores", "topk", "sparse_attn", "decode",
                        "decode_fp8"):
         run_kernel_alone(args)
+        return
+    if args.kernel == "reuse":
+        import torch
+
+        import long_context_sparse_weighted_b300 as lcsw
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+            os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        e = measure_reuse(torch, lcsw, peaks.get("hbm_gbs", 6400.0), None)
+        print(json.dumps({"kernel": "reuse", **e}))
+        return
+    if args.kernel == "kda":
+        import torch
+
+        import long_context_sparse_weighted_b300 as lcsw
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+            os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        e = measure_kda(torch, lcsw, peaks.get("hbm_gbs", 6400.0), max(1, args.steps),
+                        args.warmup, False)
+        print(json.dumps({"kernel": "kda", **e}))
         return
     if args.kernel == "prefill_scores":
         run_prefill_scores(args)

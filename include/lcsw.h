@@ -172,6 +172,37 @@ lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_
                              void *ws, size_t ws_bytes, lcsw_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * Sparse attention in the MLA latent geometry ("G2C Brief -- GLM-5.3-Flash":
+ * MLA rank 512 per token, kv_lora_rank 512; the DSA diagram's "MLA latent
+ * cache (rank 512 per token)").  One cached row per token, shared by every
+ * query head, holds the rank-512 latent c and a rotary key part (64 wide; the
+ * pages do not give that width): kv[b][j] = [c_j (512) | r_j (64)].  The
+ * latent is both the key's first 512 dims and the value (the query is
+ * absorbed into the latent space):
+ *
+ *   z_j = scale * q[b][t][h][:] . kv[b][j][:]                 (576 dims)
+ *   out[b][t][h][:] = sum_j softmax_j(z) kv[b][j][0:512],  lse = log sum_j e^z_j
+ *
+ * over the tokens of groups idx[b][t][0..k) (entries outside [0, seq_len/P)
+ * are skipped, as in lcsw_sparse_attn).
+ *
+ *   q    [B][T][H_q][576] bf16;  kv [B][*][576] bf16, batch stride skv_b
+ *   idx  [B][T][k] int32;  out [B][T][H_q][512] bf16;  lse [B][T][H_q] or NULL
+ *   ws   lcsw_sparse_attn_mla_workspace_size bytes (0: none needed), 16-byte
+ *        aligned, no clearing needed
+ * H_q a multiple of 16, B*T <= 65535.  lcsw_decode_fused and
+ * lcsw_decode_reuse take the same geometry when d_qk = LCSW_MLA_DQK and
+ * d_v = LCSW_MLA_DV, with V = NULL (or V = K, sV_b = sK_b).
+ * ------------------------------------------------------------------------- */
+#define LCSW_MLA_DQK 576
+#define LCSW_MLA_DV 512
+size_t lcsw_sparse_attn_mla_workspace_size(int B, int T, int H_q, int k, int P);
+lcsw_status lcsw_sparse_attn_mla(const lcsw_bf16 *q, const lcsw_bf16 *kv, int64_t skv_b,
+                                 const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                 int H_q, int P, int k, float scale, lcsw_bf16 *out, float *lse,
+                                 void *ws, size_t ws_bytes, lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
  * lcsw_sparse_attn without a caller workspace.  The pages have no counterpart
  * of this entry point: it serves callers that cannot allocate device memory
  * per call -- a plain-C host over this header with no device allocator of its
@@ -318,13 +349,21 @@ lcsw_status lcsw_decode_fused_e4m3(const lcsw_decode_args *a, uint8_t *kq, int64
  *
  * Reads q, K, sK_b, V, sV_b, seq_len, B, H_q, d_qk, d_v, P, k, scale, out and
  * lse of `a`; its indexer fields (q_idx, w_head, k_pooled, k_idx, pool_w,
- * H_i, d_idx, G_max), idx_out, scores_out and flags are not used.
+ * H_i, d_idx), idx_out and scores_out are not used; G_max and flags are
+ * read as below.
  *   idx_in  [B][k] int32 device
  *   ws      a decode workspace: lcsw_decode_workspace_size(a) bytes, 256-byte
- *           aligned (only its split-K region is written; it needs no clearing
- *           and may be the same workspace the selecting layer's call used,
- *           once that call has completed)
- * Two launches on `stream`: split-K partial states, then their merge.
+ *           aligned, zero-filled before its first use like the workspace of
+ *           lcsw_decode_fused (and left ready for the next call).  a->G_max
+ *           only sizes it and may be 0.  It may be the workspace of the
+ *           selecting layer's lcsw_decode_fused call (any G_max, H_q, d_v of
+ *           that call), once that call has completed on the same stream.
+ * Within the persistent kernel's envelope (2B <= SM count, k <= 2048, H_q a
+ * multiple of 16 up to 64, and flags without LCSW_DECODE_FORCE_MULTIKERNEL):
+ * one launch, whose blocks attend over slices of idx_in[b] and merge their
+ * partial states; a bounded wait that runs out is reported through
+ * lcsw_get_status.  Otherwise two launches: split-K partial states, then
+ * their merge.
  * ------------------------------------------------------------------------- */
 lcsw_status lcsw_decode_reuse(const lcsw_decode_args *a, const int32_t *idx_in, void *ws,
                               size_t ws_bytes, lcsw_stream stream);
@@ -388,6 +427,42 @@ typedef struct {
 size_t lcsw_prefill_workspace_size(const lcsw_prefill_args *a);
 lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
                          lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * KDA step: the linear-attention half of the hybrid ("G2C Brief --
+ * GLM-5.3-Flash", section "KDA carries fixed state through most layers":
+ * Kimi Delta Attention is a gated delta-rule descendant of linear attention
+ * that updates a fixed matrix state per head; a short convolution of kernel
+ * size 4 and learned gates surround the recurrence; 64 heads of width 128).
+ * The pages print no formula; the step computes, per sequence b, head h and
+ * token t in order (S: the D x D state, key channels as rows):
+ *
+ *   a_c = SiLU(sum_{j<4} conv_w[c][j] * x_{t-3+j}[c])  for the head's q, k, v channels
+ *         (x_{t'} = qkv[b][t'] for t' >= 0, conv_state[b][3+t'] for t' < 0)
+ *   q   = a_q / sqrt(|a_q|^2 + 1e-6) / sqrt(D),   k = a_k / sqrt(|a_k|^2 + 1e-6),   v = a_v
+ *   S   = (I - beta k k^T) Diag(exp(g)) S + beta k v^T,    out = S^T q
+ *
+ * with g = g[b][t][h][:] and beta = beta[b][t][h].  After the call state
+ * holds S after the last token and conv_state the raw inputs of the last
+ * three positions (oldest first).
+ *
+ *   qkv        [B][T][3*H*D] bf16: pre-convolution projections, q | k | v,
+ *              each head-major (channel c of part p, head h: p*H*D + h*D + c)
+ *   conv_w     [3*H*D][4] bf16: depthwise taps, tap 3 on the current token
+ *   conv_state [B][3][3*H*D] bf16, read and written
+ *   g          [B][T][H][D] fp32: log of the per-key-channel decay (<= 0)
+ *   beta       [B][T][H] fp32: write strength
+ *   state      [B][H][D][D] fp32, read and written; 16-byte aligned
+ *   out        [B][T][H][D] bf16
+ *
+ * D must be 128 (LCSW_ERR_UNSUPPORTED otherwise); B = 0 or T = 0 is a no-op.
+ * The output, gates and projections around the step (dense layers of the
+ * model) are the caller's.  Work: one block per (head, sequence); the state
+ * is read once and written once per call whatever T is.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_kda_step(const lcsw_bf16 *qkv, const lcsw_bf16 *conv_w, lcsw_bf16 *conv_state,
+                          const float *g, const float *beta, float *state, lcsw_bf16 *out,
+                          int B, int T, int H, int D, lcsw_stream stream);
 
 /* ---------------------------------------------------------------------------
  * Device status word of a workspace (decode / prefill).  Synchronises

@@ -84,6 +84,10 @@ _SIGNATURES = {
     "lcsw_decode_fused_e4m3": ([ctypes.POINTER(DecodeArgs), _vp, _i64, _vp, _sz, _vp], _i32),
     "lcsw_prefill_workspace_size": ([ctypes.POINTER(PrefillArgs)], _sz),
     "lcsw_prefill": ([ctypes.POINTER(PrefillArgs), _vp, _sz, _vp], _i32),
+    "lcsw_sparse_attn_mla_workspace_size": ([_i32, _i32, _i32, _i32, _i32], _sz),
+    "lcsw_sparse_attn_mla": ([_vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
+                              _vp, _vp, _sz, _vp], _i32),
+    "lcsw_kda_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "lcsw_get_status": ([_vp, _vp], _i32),
 }
 
@@ -185,6 +189,34 @@ def index_scores(q_idx, w_head, k_pooled, seq_len, P, G_max=None, q_pos=None, ou
     return out
 
 
+def kda_step(qkv, conv_w, conv_state, g, beta, state, out=None, stream=None):
+    """KDA step over T tokens: gated delta-rule recurrence after a causal short
+    convolution (see lcsw_kda_step).  Updates `state` and `conv_state` in place
+    and returns out [B][T][H][D] (bf16).
+
+    qkv [B][T][3*H*D] bf16, conv_w [3*H*D][4] bf16, conv_state [B][3][3*H*D]
+    bf16, g [B][T][H][D] fp32, beta [B][T][H] fp32, state [B][H][D][D] fp32.
+    """
+    _dense(qkv, torch.bfloat16, "qkv")
+    _dense(conv_w, torch.bfloat16, "conv_w")
+    _dense(conv_state, torch.bfloat16, "conv_state")
+    _dense(g, torch.float32, "g")
+    _dense(beta, torch.float32, "beta")
+    _dense(state, torch.float32, "state")
+    B, H, D, _ = state.shape
+    T = qkv.shape[1]
+    if qkv.shape != (B, T, 3 * H * D) or conv_w.shape != (3 * H * D, 4) or \
+            conv_state.shape != (B, 3, 3 * H * D) or g.shape != (B, T, H, D) or \
+            beta.shape != (B, T, H):
+        raise ValueError("inconsistent KDA shapes")
+    if out is None:
+        out = torch.empty(B, T, H, D, dtype=torch.bfloat16, device=qkv.device)
+    _dense(out, torch.bfloat16, "out")
+    _check(lib().lcsw_kda_step(_ptr(qkv), _ptr(conv_w), _ptr(conv_state), _ptr(g), _ptr(beta),
+                               _ptr(state), _ptr(out), B, T, H, D, _stream(stream)))
+    return out
+
+
 def visible_counts(seq_len, q_pos, B, T, P, stream=None):
     out = torch.empty(B, T, dtype=torch.int32, device=seq_len.device)
     _check(lib().lcsw_visible_counts(_ptr(seq_len), _ptr(q_pos), B, T, P, _ptr(out),
@@ -228,6 +260,34 @@ def sparse_attn(q, K, V, seq_len, idx, P, scale, out=None, lse=None, ws=None, st
                                   _ptr(seq_len), _ptr(idx), B, T, H_q, d_qk, d_v, P, k,
                                   float(scale), _ptr(out), _ptr(lse), _ptr(ws), nbytes,
                                   _stream(stream)))
+    return out, lse
+
+
+MLA_DQK, MLA_DV = 576, 512  # latent 512 + rotary 64; the latent is the value
+
+
+def sparse_attn_mla(q, kv, seq_len, idx, P, scale, out=None, lse=None, ws=None, stream=None):
+    """Attention in the MLA latent geometry: kv rows [c (512) | rope (64)] shared
+    by every head, the latent c doubling as the value (lcsw_sparse_attn_mla).
+    q [B][T][H_q][576], kv [B][L][576], idx [B][T][k] -> out [B][T][H_q][512]."""
+    _bf16(q, "q", 4)
+    _bf16(kv, "kv", 3)
+    _dense(idx, torch.int32, "idx")
+    _dense(seq_len, torch.int32, "seq_len")
+    B, T, H_q, d_qk = q.shape
+    if d_qk != MLA_DQK or kv.shape[2] != MLA_DQK:
+        raise ValueError("MLA rows are 576 wide")
+    k = idx.shape[-1]
+    if out is None:
+        out = torch.empty(B, T, H_q, MLA_DV, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, H_q, dtype=torch.float32, device=q.device)
+    nbytes = lib().lcsw_sparse_attn_mla_workspace_size(B, T, H_q, k, P)
+    if ws is None and nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(lib().lcsw_sparse_attn_mla(_ptr(q), _ptr(kv), kv.stride(0), _ptr(seq_len), _ptr(idx),
+                                      B, T, H_q, P, k, float(scale), _ptr(out), _ptr(lse),
+                                      _ptr(ws), nbytes, _stream(stream)))
     return out, lse
 
 
@@ -296,12 +356,14 @@ class Decoder:
             _bf16(k_pooled, "k_pooled", 3)
         _bf16(q, "q", 3)
         _bf16(K, "K", 3)
-        _bf16(V, "V", 3)
+        if V is not None:
+            _bf16(V, "V", 3)
         _dense(w_head, torch.float32, "w_head")
         _dense(seq_len, torch.int32, "seq_len")
         B, H_i, d_idx = q_idx.shape
         H_q, d_qk = q.shape[1], q.shape[2]
-        d_v = V.shape[2]
+        # V None: the MLA latent geometry (576-wide K rows whose latent is the value)
+        d_v = V.shape[2] if V is not None else MLA_DV
         dev = q.device
         self.out = out if out is not None else torch.empty(B, H_q, d_v, dtype=torch.bfloat16,
                                                            device=dev)
@@ -319,7 +381,8 @@ class Decoder:
             a.pool_w, a.sw_b = pool_w.data_ptr(), pool_w.stride(0)
         a.q = q.data_ptr()
         a.K, a.sK_b = K.data_ptr(), K.stride(0)
-        a.V, a.sV_b = V.data_ptr(), V.stride(0)
+        if V is not None:
+            a.V, a.sV_b = V.data_ptr(), V.stride(0)
         a.seq_len = seq_len.data_ptr()
         a.B, a.G_max = B, int(G_max if G_max is not None else k_pooled.shape[1])
         self.kq = kq
@@ -366,14 +429,15 @@ class ReuseStep:
     (lcsw_decode_reuse): attention of q over the groups idx_in[b][0..k),
     with no indexer scores or top-k of its own."""
 
-    def __init__(self, q, K, V, seq_len, idx_in, P, scale, out=None, lse=None, ws=None):
+    def __init__(self, q, K, V, seq_len, idx_in, P, scale, out=None, lse=None, ws=None, flags=0):
         _bf16(q, "q", 3)
         _bf16(K, "K", 3)
-        _bf16(V, "V", 3)
+        if V is not None:
+            _bf16(V, "V", 3)
         _dense(seq_len, torch.int32, "seq_len")
         _dense(idx_in, torch.int32, "idx_in")
         B, H_q, d_qk = q.shape
-        d_v = V.shape[2]
+        d_v = V.shape[2] if V is not None else MLA_DV
         k = idx_in.shape[-1]
         dev = q.device
         self.out = out if out is not None else torch.empty(B, H_q, d_v, dtype=torch.bfloat16,
@@ -384,15 +448,19 @@ class ReuseStep:
         a = DecodeArgs()
         a.q = q.data_ptr()
         a.K, a.sK_b = K.data_ptr(), K.stride(0)
-        a.V, a.sV_b = V.data_ptr(), V.stride(0)
+        if V is not None:
+            a.V, a.sV_b = V.data_ptr(), V.stride(0)
         a.seq_len = seq_len.data_ptr()
         a.B, a.G_max, a.H_i, a.d_idx, a.P, a.k = B, 0, 1, 64, P, k
         a.H_q, a.d_qk, a.d_v, a.scale = H_q, d_qk, d_v, float(scale)
         a.out, a.lse = self.out.data_ptr(), self.lse.data_ptr()
+        a.flags = int(flags)
         self.args = a
         self.idx_in = idx_in
         self.ws_bytes = lib().lcsw_decode_workspace_size(ctypes.byref(a))
-        self.ws = ws if ws is not None else torch.empty(self.ws_bytes, dtype=torch.uint8,
+        # a decode workspace is zero-filled before its first use (a shared one,
+        # e.g. the selecting layer's, is already in that state between calls)
+        self.ws = ws if ws is not None else torch.zeros(self.ws_bytes, dtype=torch.uint8,
                                                         device=dev)
 
     def __call__(self, stream=None):
@@ -400,6 +468,10 @@ class ReuseStep:
                                        ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(),
                                        _stream(stream)))
         return self.out, self.lse
+
+    def status(self, stream=None):
+        """Raise if a bounded device wait of an earlier call ran out (synchronises)."""
+        _check(lib().lcsw_get_status(ctypes.c_void_p(self.ws.data_ptr()), _stream(stream)))
 
 
 def decode_fused(q_idx, w_head, k_pooled, q, K, V, seq_len, P, k, scale, **kw):

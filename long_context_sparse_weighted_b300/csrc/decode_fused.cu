@@ -51,4 +51,18 @@ cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status
     return launch_shape<false>(make_params(a, ws, status), a, st);
 }
 
+bool reuse_decode_supported(int B, int H_q, int d_qk, int d_v, int k) {
+    const int ncta = num_sms();
+    if (ncta > kMaxCtas || B < 1 || 2 * B > ncta || k < 1 || k > kMaxK) return false;
+    if (!((d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128))) return false;
+    return H_q % 16 == 0 && H_q <= 64;
+}
+
+cudaError_t launch_reuse_decode(const lcsw_decode_args *a, const int32_t *idx_in, void *ws,
+                                int *status, cudaStream_t st) {
+    Params prm = make_params(a, ws, status);
+    prm.idx_in = idx_in;
+    return launch_reuse_shape(prm, a, st);
+}
+
 }  // namespace lcsw

@@ -181,6 +181,7 @@ struct Params {
     float *lse;
     int32_t *idx_out;
     float *scores_out;
+    const int32_t *idx_in;  // a given selection [B][k] (reuse kernel only)
     // workspace
     unsigned *ctl;        // [B][kCtlWords]
     unsigned *hist;       // [B][2][kHistWords]: level 1, level 2 (zero between calls)
@@ -647,6 +648,164 @@ __device__ __forceinline__ void attend_groups(unsigned char *u, const int32_t *o
             st_part2(reinterpret_cast<float *>(part_ml + h1), l1 > 0.f ? m1 : -INFINITY, l1);
         }
     }
+}
+
+// Merge of the partial states of one sequence's blocks, head by head: block j
+// of the n_b blocks cb0.. of sequence b merges heads j, j + n_b, ...: it polls
+// the partial words of every block of the sequence until all are written,
+// writes the normalised output row, then clears the words it read for the
+// next call.  Returns false if a bounded wait ran out (the status word is set).
+template <int DV>
+__device__ __forceinline__ bool merge_partials(const Params &p, unsigned char *smem, int *sv,
+                                               float *sred, int b, int j, int n_b, int cb0) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n_src = n_b;
+    auto src_cta = [&](int u) { return cb0 + u; };
+    float *wsm = reinterpret_cast<float *>(smem + kU);       // [kMaxCtas] weights
+    float *lsm = wsm + kMaxCtas;                              // [kWarps] sums of w l
+    float *red = lsm + kMaxCtas;                              // [ngrp][DV]
+    constexpr int D4 = DV / 4;                                // float4 columns
+    const int sg = tid / D4, dc = tid % D4;                   // source group, column
+    const int ngrp = kThreads / D4;                           // 16 (DV=128) or 32 (DV=64)
+    // (no barrier: wsm, lsm and red overlap only the Q rows, which every warp
+    // of the attention finished reading before its last P V)
+    for (int h = j; h < p.H_q; h += n_b) {
+        constexpr int kU4 = (kMaxCtas + 15) / 16;
+        const int nu = (n_src - sg + ngrp - 1) / ngrp;
+        float2 *mlp = p.part_ml + int64_t(src_cta(min(tid, n_src - 1))) * p.H_q + h;
+        auto op_at = [&](int u) {
+            return p.part_o + (int64_t(src_cta(sg + u * ngrp)) * p.H_q + h) * DV + dc * 4;
+        };
+        // First every source's (m, l) word, one thread per source (a light
+        // poll while the sources are still storing; a source writes it right
+        // after its O rows); then the O rows are loaded, and any word still
+        // unwritten is polled again.
+        uint2 mlw = make_uint2(1u, 1u);
+        {
+            bool ok = true;
+            if (tid < n_src) {
+                mlw = ld_relaxed_u32x2(mlp);
+                const long long t0 = clock64();
+                for (int spin = 0; mlw.x == 0u || mlw.y == 0u; ++spin) {
+                    if (clock64() - t0 > kSpinBudget ||
+                        ((spin & 63) == 63 && aborted(p.abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(spin < 4 ? 64 : 256);
+                    mlw = ld_relaxed_u32x2(mlp);
+                }
+            }
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) raise_timeout(p, 6);
+                return false;
+            }
+        }
+        uint4 ow[kU4];
+#pragma unroll
+        for (int u = 0; u < kU4; ++u) {
+            ow[u] = make_uint4(1u, 1u, 1u, 1u);
+            if (u < nu) ow[u] = ld_relaxed_v4(reinterpret_cast<const uint4 *>(op_at(u)));
+        }
+        {
+            const long long t0 = clock64();
+            for (int spin = 0;; ++spin) {
+                bool bad = false;
+                if (mlw.x == 0u || mlw.y == 0u) {
+                    bad = true;
+                    mlw = ld_relaxed_u32x2(mlp);
+                }
+#pragma unroll
+                for (int u = 0; u < kU4; ++u) {
+                    if (ow[u].x == 0u || ow[u].y == 0u || ow[u].z == 0u || ow[u].w == 0u) {
+                        bad = true;
+                        ow[u] = ld_relaxed_v4(reinterpret_cast<const uint4 *>(op_at(u)));
+                    }
+                }
+                if (!bad) break;
+                if (clock64() - t0 > kSpinBudget ||
+                    ((spin & 63) == 63 && aborted(p.abort_flag))) {
+                    raise_timeout(p, 6);
+                    sv[19] = 1;
+                    break;
+                }
+                __nanosleep(128);
+            }
+        }
+        PHASE_MARK(30);
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (tid < n_src) ml = make_float2(part_dec(mlw.x), part_dec(mlw.y));
+        float4 ov[kU4];
+#pragma unroll
+        for (int u = 0; u < kU4; ++u) {
+            ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (u < nu)
+                ov[u] = make_float4(part_dec(ow[u].x), part_dec(ow[u].y), part_dec(ow[u].z),
+                                    part_dec(ow[u].w));
+        }
+        // M = max over sources (warp max, then over the warps' maxima)
+        float m = ml.x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) sred[warp] = m;
+        __syncthreads();
+        if (sv[19]) return false;  // a partial state never arrived
+        PHASE_MARK(31);
+        float M = lane < kWarps ? sred[lane] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float ref = M == -INFINITY ? 0.f : M;
+        // source weights 2^(m_s - M) and L = sum of w_s l_s (warp sums first)
+        float wl = 0.f;
+        if (tid < n_src) {
+            const float wgt = ml.y > 0.f ? exp2f(ml.x - ref) : 0.f;
+            wsm[tid] = wgt;
+            wl = wgt * ml.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
+        if (lane == 0) lsm[warp] = wl;
+        __syncthreads();
+        PHASE_MARK(32);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kU4; ++u) {
+            if (u < nu) {
+                const float wgt = wsm[sg + u * ngrp];
+                if (wgt != 0.f) {
+                    acc.x += wgt * ov[u].x;
+                    acc.y += wgt * ov[u].y;
+                    acc.z += wgt * ov[u].z;
+                    acc.w += wgt * ov[u].w;
+                }
+            }
+        }
+        *reinterpret_cast<float4 *>(red + sg * DV + dc * 4) = acc;
+        __syncthreads();
+        if (tid < DV / 2) {
+            float L = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) L += lsm[w];
+            float a0 = 0.f, a1 = 0.f;
+            for (int g2 = 0; g2 < ngrp; ++g2) {
+                a0 += red[g2 * DV + 2 * tid];
+                a1 += red[g2 * DV + 2 * tid + 1];
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            *reinterpret_cast<uint32_t *>(p.out + (int64_t(b) * p.H_q + h) * DV + 2 * tid) =
+                pack_bf2(a0 * inv, a1 * inv);
+            if (p.lse && tid == 0)
+                p.lse[int64_t(b) * p.H_q + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+        // the words read are cleared for the next call (after the output:
+        // a barrier right behind global stores waits for them)
+        if (tid < n_src) st_relaxed_zero2(mlp);
+#pragma unroll
+        for (int u = 0; u < kU4; ++u)
+            if (u < nu) st_relaxed_zero4(op_at(u));
+        if (h + n_b < p.H_q) __syncthreads();
+    }
+    return true;
 }
 
 template <int NT, int DQK, int DV, bool F8>
@@ -1714,157 +1873,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     PHASE_MARK(17);
 
     // ---- merge the partial states, head by head --------------------------------
-    // Block j merges heads j, j + n_b, ...: it polls the partial words of every
-    // block of the sequence until all are written, then clears them for the
-    // next call.
-    {
-        const int n_src = n_b;
-        auto src_cta = [&](int u) { return cb0 + u; };
-        float *wsm = reinterpret_cast<float *>(smem + kU);       // [kMaxCtas] weights
-        float *lsm = wsm + kMaxCtas;                              // [kWarps] sums of w l
-        float *red = lsm + kMaxCtas;                              // [ngrp][DV]
-        constexpr int D4 = DV / 4;                                // float4 columns
-        const int sg = tid / D4, dc = tid % D4;                   // source group, column
-        const int ngrp = kThreads / D4;                           // 16 (DV=128) or 32 (DV=64)
-        // (no barrier: wsm, lsm and red overlap only the Q rows, which every warp
-        // of the attention finished reading before its last P V)
-        for (int h = j; h < p.H_q; h += n_b) {
-            constexpr int kU4 = (kMaxCtas + 15) / 16;
-            const int nu = (n_src - sg + ngrp - 1) / ngrp;
-            float2 *mlp = p.part_ml + int64_t(src_cta(min(tid, n_src - 1))) * p.H_q + h;
-            auto op_at = [&](int u) {
-                return p.part_o + (int64_t(src_cta(sg + u * ngrp)) * p.H_q + h) * DV + dc * 4;
-            };
-            // First every source's (m, l) word, one thread per source (a light
-            // poll while the sources are still storing; a source writes it right
-            // after its O rows); then the O rows are loaded, and any word still
-            // unwritten is polled again.
-            uint2 mlw = make_uint2(1u, 1u);
-            {
-                bool ok = true;
-                if (tid < n_src) {
-                    mlw = ld_relaxed_u32x2(mlp);
-                    const long long t0 = clock64();
-                    for (int spin = 0; mlw.x == 0u || mlw.y == 0u; ++spin) {
-                        if (clock64() - t0 > kSpinBudget ||
-                            ((spin & 63) == 63 && aborted(p.abort_flag))) {
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(spin < 4 ? 64 : 256);
-                        mlw = ld_relaxed_u32x2(mlp);
-                    }
-                }
-                if (__syncthreads_or(!ok)) {
-                    if (tid == 0) raise_timeout(p, 6);
-                    return;
-                }
-            }
-            uint4 ow[kU4];
-#pragma unroll
-            for (int u = 0; u < kU4; ++u) {
-                ow[u] = make_uint4(1u, 1u, 1u, 1u);
-                if (u < nu) ow[u] = ld_relaxed_v4(reinterpret_cast<const uint4 *>(op_at(u)));
-            }
-            {
-                const long long t0 = clock64();
-                for (int spin = 0;; ++spin) {
-                    bool bad = false;
-                    if (mlw.x == 0u || mlw.y == 0u) {
-                        bad = true;
-                        mlw = ld_relaxed_u32x2(mlp);
-                    }
-#pragma unroll
-                    for (int u = 0; u < kU4; ++u) {
-                        if (ow[u].x == 0u || ow[u].y == 0u || ow[u].z == 0u || ow[u].w == 0u) {
-                            bad = true;
-                            ow[u] = ld_relaxed_v4(reinterpret_cast<const uint4 *>(op_at(u)));
-                        }
-                    }
-                    if (!bad) break;
-                    if (clock64() - t0 > kSpinBudget ||
-                        ((spin & 63) == 63 && aborted(p.abort_flag))) {
-                        raise_timeout(p, 6);
-                        sv[19] = 1;
-                        break;
-                    }
-                    __nanosleep(128);
-                }
-            }
-            PHASE_MARK(30);
-            float2 ml = make_float2(-INFINITY, 0.f);
-            if (tid < n_src) ml = make_float2(part_dec(mlw.x), part_dec(mlw.y));
-            float4 ov[kU4];
-#pragma unroll
-            for (int u = 0; u < kU4; ++u) {
-                ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (u < nu)
-                    ov[u] = make_float4(part_dec(ow[u].x), part_dec(ow[u].y), part_dec(ow[u].z),
-                                        part_dec(ow[u].w));
-            }
-            // M = max over sources (warp max, then over the warps' maxima)
-            float m = ml.x;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) sred[warp] = m;
-            __syncthreads();
-            if (sv[19]) return;  // a partial state never arrived
-            PHASE_MARK(31);
-            float M = lane < kWarps ? sred[lane] : -INFINITY;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            const float ref = M == -INFINITY ? 0.f : M;
-            // source weights 2^(m_s - M) and L = sum of w_s l_s (warp sums first)
-            float wl = 0.f;
-            if (tid < n_src) {
-                const float wgt = ml.y > 0.f ? exp2f(ml.x - ref) : 0.f;
-                wsm[tid] = wgt;
-                wl = wgt * ml.y;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
-            if (lane == 0) lsm[warp] = wl;
-            __syncthreads();
-            PHASE_MARK(32);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < kU4; ++u) {
-                if (u < nu) {
-                    const float wgt = wsm[sg + u * ngrp];
-                    if (wgt != 0.f) {
-                        acc.x += wgt * ov[u].x;
-                        acc.y += wgt * ov[u].y;
-                        acc.z += wgt * ov[u].z;
-                        acc.w += wgt * ov[u].w;
-                    }
-                }
-            }
-            *reinterpret_cast<float4 *>(red + sg * DV + dc * 4) = acc;
-            __syncthreads();
-            if (tid < DV / 2) {
-                float L = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) L += lsm[w];
-                float a0 = 0.f, a1 = 0.f;
-                for (int g2 = 0; g2 < ngrp; ++g2) {
-                    a0 += red[g2 * DV + 2 * tid];
-                    a1 += red[g2 * DV + 2 * tid + 1];
-                }
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                *reinterpret_cast<uint32_t *>(p.out + (int64_t(b) * p.H_q + h) * DV + 2 * tid) =
-                    pack_bf2(a0 * inv, a1 * inv);
-                if (p.lse && tid == 0)
-                    p.lse[int64_t(b) * p.H_q + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-            }
-            // the words read are cleared for the next call (after the output:
-            // a barrier right behind global stores waits for them)
-            if (tid < n_src) st_relaxed_zero2(mlp);
-#pragma unroll
-            for (int u = 0; u < kU4; ++u)
-                if (u < nu) st_relaxed_zero4(op_at(u));
-            if (h + n_b < p.H_q) __syncthreads();
-        }
-    }
+    if (!merge_partials<DV>(p, smem, sv, sred, b, j, n_b, cb0)) return;
     PHASE_MARK(19);
     __syncthreads();
     // this block's words of the other buffers were read during the previous
@@ -1886,6 +1895,69 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     }
 }
 
+// IndexCache reuse: the attention and merge phases of the fused step, over a
+// selection an earlier layer made (p.idx_in [B][k]) instead of one of its own.
+// Blocks go to sequences in proportion to their selected groups (one at
+// least); block j of a sequence attends over entries [k j / n_b, k (j+1) / n_b)
+// of its row (entries outside [0, G_b) are masked) and the blocks merge their
+// partial states head by head as in the fused step.
+template <int DQK, int DV>
+__global__ void __launch_bounds__(kThreads, 1) reuse_decode_kernel(const Params p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    int *cta_begin = reinterpret_cast<int *>(smem + kMisc + 128);             // [kMaxCtas + 1]
+    int *offs = cta_begin + kMaxCtas + 1;                                     // [kMaxCtas + 1]
+    int *lens = offs + kMaxCtas + 1;                                          // [kMaxCtas]
+    int *sv = lens + kMaxCtas;                                                // scalars [64]
+    int *scratch = sv + 64;                                                   // [40]
+    float *sred = reinterpret_cast<float *>(scratch + 40);                    // [64]
+    int32_t *own = reinterpret_cast<int32_t *>(smem + kSelList);              // [kMaxK]
+    const int tid = threadIdx.x;
+    const int cta = blockIdx.x, ncta = gridDim.x;
+    const int B = p.B, P = p.P;
+    if (tid == 0) sv[19] = 0;
+    int b, cb0, n_b, G_b;
+    if (B == 1) {
+        b = 0;
+        cb0 = 0;
+        n_b = ncta;
+        G_b = __ldg(p.seq_len) / P;
+    } else {
+        int wv = 0;
+        if (tid < B) {
+            const int L = __ldg(p.seq_len + tid);
+            lens[tid] = L;
+            wv = min(p.k, max(0, L / P)) + 1;
+        }
+        int total;
+        const int pre = block_exclusive_scan(wv, scratch, &total);
+        if (tid < B) offs[tid] = pre;
+        if (tid == 0) offs[B] = total;
+        __syncthreads();
+        const double tot = total > 0 ? double(total) : 1.0;
+        for (int bb = tid; bb <= B; bb += kThreads)
+            cta_begin[bb] = bb == B ? ncta : bb + int(double(ncta - B) * double(offs[bb]) / tot);
+        __syncthreads();
+        for (int bb = tid; bb < B; bb += kThreads)
+            if (cta_begin[bb] <= cta && cta < cta_begin[bb + 1]) sv[1] = bb;
+        __syncthreads();
+        b = sv[1];
+        cb0 = cta_begin[b];
+        n_b = cta_begin[b + 1] - cb0;
+        G_b = lens[b] / P;
+    }
+    G_b = max(0, G_b);
+    const int j = cta - cb0;
+    const int lo = int((long long)p.k * j / n_b), hi = int((long long)p.k * (j + 1) / n_b);
+    const int n_own = hi - lo;
+    for (int i = tid; i < n_own; i += kThreads) own[i] = __ldg(p.idx_in + int64_t(b) * p.k + lo + i);
+    __syncthreads();
+    attend_groups<DQK, DV>(smem + kU, own, n_own, G_b, P, p.K + int64_t(b) * p.sK_b,
+                           p.V + int64_t(b) * p.sV_b, p.q + int64_t(b) * p.H_q * DQK, p.H_q,
+                           p.scale_log2, p.part_o + int64_t(cta) * p.H_q * DV,
+                           p.part_ml + int64_t(cta) * p.H_q, false);
+    merge_partials<DV>(p, smem, sv, sred, b, j, n_b, cb0);
+}
+
 int num_sms() {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -1898,7 +1970,13 @@ struct WsLayout {
     size_t ctl, hist, slots, cand, ovf, gscore, cta_cnt, idx_ws, part_o, part_ml, total;
 };
 
+// The partial-state regions come first and are sized for the largest shape
+// (64 heads of 128 value dims), so every call on a workspace -- a decode step
+// or a reuse step, whatever its G_max, H_q or d_v -- finds them at the same
+// place; they hold only zeros between calls.
 WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int ncta) {
+    (void)H_q;
+    (void)d_v;
     WsLayout w;
     size_t off = 256;  // status + abort words
     auto take = [&](size_t bytes) {
@@ -1906,6 +1984,8 @@ WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int ncta) {
         off += (bytes + 255) & ~size_t(255);
         return o;
     };
+    w.part_ml = take(size_t(ncta) * 64 * 8);
+    w.part_o = take(size_t(ncta) * 64 * 128 * 4);
     w.ctl = take(size_t(B) * kCtlWords * 4);
     w.hist = take(size_t(B) * 2 * kHistWords * 4);
     w.slots = take(size_t(2) * ncta * kSlotBytes);
@@ -1914,8 +1994,6 @@ WsLayout ws_layout(int B, int G_max, int H_q, int d_v, int k, int ncta) {
     w.gscore = take(size_t(B) * G_max * 4);
     w.cta_cnt = take(size_t(2) * ncta * 4);
     w.idx_ws = take(size_t(B) * k * 4);
-    w.part_o = take(size_t(ncta) * H_q * d_v * 4);
-    w.part_ml = take(size_t(ncta) * H_q * 8);
     w.total = off;
     return w;
 }
@@ -1930,6 +2008,25 @@ cudaError_t launch_t(const Params &prm, int ncta, cudaStream_t st) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorCooperativeLaunchTooLarge;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ncta);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+template <int DQK, int DV>
+cudaError_t launch_reuse_t(const Params &prm, int ncta, cudaStream_t st) {
+    auto kern = reuse_decode_kernel<DQK, DV>;
+    constexpr int smem = kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ncta);
     cfg.blockDim = dim3(kThreads);
@@ -1992,6 +2089,7 @@ Params make_params(const lcsw_decode_args *a, void *ws, int *status) {
     prm.gdepart = reinterpret_cast<unsigned *>(status + 3);
     prm.kq = nullptr;
     prm.sq_b = 0;
+    prm.idx_in = nullptr;
     return prm;
 }
 
@@ -2016,6 +2114,20 @@ cudaError_t launch_shape(const Params &prm, const lcsw_decode_args *a, cudaStrea
     LCSW_FD(2, 192, 64)
     LCSW_FD(2, 64, 128)
 #undef LCSW_FD
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_reuse_shape(const Params &prm, const lcsw_decode_args *a, cudaStream_t st) {
+    const int ncta = num_sms();
+#define LCSW_RD(DQ, DVV) \
+    if (a->d_qk == DQ && a->d_v == DVV) return launch_reuse_t<DQ, DVV>(prm, ncta, st);
+    LCSW_RD(128, 128)
+    LCSW_RD(192, 128)
+    LCSW_RD(64, 64)
+    LCSW_RD(128, 64)
+    LCSW_RD(192, 64)
+    LCSW_RD(64, 128)
+#undef LCSW_RD
     return cudaErrorInvalidValue;
 }
 

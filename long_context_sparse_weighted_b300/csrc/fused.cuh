@@ -18,4 +18,11 @@ cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status
 cudaError_t launch_fused_decode_e4m3(const lcsw_decode_args *a, uint8_t *kq, int64_t sq_b,
                                      void *ws, int *status, cudaStream_t st);
 
+// IndexCache reuse on the persistent kernel: attention over idx_in [B][k] and
+// the merge of the blocks' partial states (one launch).  Supported for
+// 2B <= SMs, k <= 2048, H_q a multiple of 16 up to 64.
+bool reuse_decode_supported(int B, int H_q, int d_qk, int d_v, int k);
+cudaError_t launch_reuse_decode(const lcsw_decode_args *a, const int32_t *idx_in, void *ws,
+                                int *status, cudaStream_t st);
+
 }  // namespace lcsw

@@ -22,6 +22,11 @@ cudaError_t launch_pool_keys(const uint16_t *k_idx, int64_t sk_b, const float *p
 cudaError_t launch_quantize_keys_e4m3(const uint16_t *k_pooled, int64_t sp_b, int B, int n_groups,
                                       uint8_t *kq, int64_t sq_b, cudaStream_t st);
 
+// KDA step over T tokens for B sequences, H heads of width 128 (kda_step.cu).
+cudaError_t launch_kda_step(const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
+                            const float *g, const float *beta, float *state, uint16_t *out,
+                            int B, int T, int H, cudaStream_t st);
+
 // q_pos[b][t] = seq_len[b] - T + t (the chunk's absolute positions).
 cudaError_t launch_prefill_positions(const int32_t *seq_len, int B, int T, int32_t *q_pos,
                                      cudaStream_t st);
@@ -92,6 +97,14 @@ cudaError_t launch_sparse_attn_tc(const uint16_t *q, const uint16_t *K, int64_t 
 
 // Split-K sparse attention + combine.
 int sparse_attn_splits(int64_t rows, int H_q, int k, int P);
+// MLA latent geometry (sparse_attn_mla.cu): rows of 576 = latent 512 + rotary
+// 64, the latent doubling as the value; out rows of 512.
+int sparse_attn_mla_splits(int64_t rows, int H_q, int k, int P);
+size_t sparse_attn_mla_ws_bytes(int64_t rows, int H_q, int k, int P);
+cudaError_t launch_sparse_attn_mla(const uint16_t *q, const uint16_t *kv, int64_t skv_b,
+                                   const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                   int H_q, int P, int k, float scale, uint16_t *out, float *lse,
+                                   void *ws, cudaStream_t st);
 size_t sparse_attn_ws_bytes(int64_t rows, int H_q, int d_v, int k, int P);
 cudaError_t launch_sparse_attn(const uint16_t *q, const uint16_t *K, int64_t sK_b,
                                const uint16_t *V, int64_t sV_b, const int32_t *seq_len,

@@ -56,6 +56,10 @@ struct Carver {
     }
 };
 
+// The MLA latent geometry: 576-wide rows (latent 512 + rotary 64), the latent
+// as the value (out rows of 512).
+bool mla_shape(int d_qk, int d_v) { return d_qk == LCSW_MLA_DQK && d_v == LCSW_MLA_DV; }
+
 bool attn_shape_ok(int H_q, int d_qk, int d_v) {
     const bool heads = H_q > 0 && H_q % 16 == 0 && (H_q <= 32 || H_q % 64 == 0);
     const bool dims = (d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128);
@@ -248,16 +252,21 @@ static lcsw_status check_decode(const lcsw_decode_args *a) {
     CHECK(a->H_i >= 1 && a->H_i <= 16, "H_i must be in [1, 16]");
     CHECK(p_ok(a->P), "P must be 1, 2, 4 or 8");
     CHECK(a->k >= 1, "k must be >= 1");
-    CHECK(attn_shape_ok(a->H_q, a->d_qk, a->d_v), "unsupported attention shape");
+    const bool mla = mla_shape(a->d_qk, a->d_v);
+    CHECK(mla ? (a->H_q > 0 && a->H_q % 16 == 0) : attn_shape_ok(a->H_q, a->d_qk, a->d_v),
+          "unsupported attention shape");
+    CHECK(!mla || !a->V || (a->V == a->K && a->sV_b == a->sK_b),
+          "MLA geometry: V is the latent part of K (pass NULL or K itself)");
     if (a->B == 0) return LCSW_OK;
     CHECK(a->B <= 65535, "B must be <= 65535");
-    CHECK(a->q_idx && a->w_head && a->k_pooled && a->q && a->K && a->V && a->seq_len && a->out,
+    CHECK(a->q_idx && a->w_head && a->k_pooled && a->q && a->K && (a->V || mla) && a->seq_len &&
+              a->out,
           "null pointer argument");
     CHECK(!a->k_idx || a->pool_w, "pool_w is required with k_idx");
     CHECK(bf16_rows_ok(a->q_idx, 64, 0) && bf16_rows_ok(a->k_pooled, 64, a->sp_b) &&
               (!a->k_idx || bf16_rows_ok(a->k_idx, 64, a->sk_b)) &&
               bf16_rows_ok(a->q, a->d_qk, 0) && bf16_rows_ok(a->K, a->d_qk, a->sK_b) &&
-              bf16_rows_ok(a->V, a->d_v, a->sV_b) && bf16_rows_ok(a->out, a->d_v, 0),
+              (mla || bf16_rows_ok(a->V, a->d_v, a->sV_b)) && bf16_rows_ok(a->out, a->d_v, 0),
           "bf16 rows must be 16-byte aligned");
     CHECK(aligned(a->w_head, 4) && aligned(a->seq_len, 4) && (!a->lse || aligned(a->lse, 4)) &&
               (!a->idx_out || aligned(a->idx_out, 4)) &&
@@ -280,12 +289,28 @@ static DecodeWs carve_decode(const lcsw_decode_args *a, void *ws) {
     Carver c(ws);
     DecodeWs w;
     w.status = static_cast<int *>(ws);
+    // the persistent kernels' region first: its partial-state words sit at the
+    // same offsets for every call that shares the workspace
+    w.fused = c.take(lcsw::fused_decode_ws_bytes(a->B, a->G_max, a->H_q, a->d_v, a->k, a->P));
     w.scores = static_cast<float *>(c.take(size_t(a->B) * a->G_max * sizeof(float)));
     w.idx = static_cast<int32_t *>(c.take(size_t(a->B) * a->k * sizeof(int32_t)));
-    w.attn = c.take(lcsw::sparse_attn_ws_bytes(a->B, a->H_q, a->d_v, a->k, a->P));
-    w.fused = c.take(lcsw::fused_decode_ws_bytes(a->B, a->G_max, a->H_q, a->d_v, a->k, a->P));
+    w.attn = c.take(mla_shape(a->d_qk, a->d_v)
+                        ? lcsw::sparse_attn_mla_ws_bytes(a->B, a->H_q, a->k, a->P)
+                        : lcsw::sparse_attn_ws_bytes(a->B, a->H_q, a->d_v, a->k, a->P));
     w.total = c.off;
     return w;
+}
+
+// Attention of one decode query per sequence over idx [B][k] (split-K
+// launches), in the shape's geometry.
+static cudaError_t decode_attend(const lcsw_decode_args *a, const int32_t *idx, void *attn_ws,
+                                 cudaStream_t st) {
+    if (mla_shape(a->d_qk, a->d_v))
+        return lcsw::launch_sparse_attn_mla(a->q, a->K, a->sK_b, a->seq_len, idx, a->B, 1, a->H_q,
+                                            a->P, a->k, a->scale, a->out, a->lse, attn_ws, st);
+    return lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B, 1,
+                                    a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale, a->out, a->lse,
+                                    attn_ws, st);
 }
 
 size_t lcsw_decode_workspace_size(const lcsw_decode_args *a) {
@@ -299,7 +324,8 @@ int lcsw_decode_launches(const lcsw_decode_args *a) {
     if (!(a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) &&
         lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P))
         return 1;
-    const int S = lcsw::sparse_attn_splits(a->B, a->H_q, a->k, a->P);
+    const int S = mla_shape(a->d_qk, a->d_v) ? lcsw::sparse_attn_mla_splits(a->B, a->H_q, a->k, a->P)
+                                              : lcsw::sparse_attn_splits(a->B, a->H_q, a->k, a->P);
     return (a->k_idx ? 1 : 0) + 3 + (S > 1 ? 1 : 0);
 }
 
@@ -333,10 +359,7 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
     if (e != cudaSuccess) return cuda_status(e, "decode scores");
     e = lcsw::launch_topk_rows(scores, nullptr, a->seq_len, a->P, 1, a->B, a->G_max, a->k, idx, st);
     if (e != cudaSuccess) return cuda_status(e, "decode top-k");
-    e = lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B, 1,
-                                 a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale, a->out, a->lse,
-                                 w.attn, st);
-    return cuda_status(e, "decode attention");
+    return cuda_status(decode_attend(a, idx, w.attn, st), "decode attention");
 }
 
 lcsw_status lcsw_quantize_keys_e4m3(const lcsw_bf16 *k_pooled, int64_t sp_b, int B,
@@ -402,12 +425,17 @@ lcsw_status lcsw_decode_reuse(const lcsw_decode_args *a, const int32_t *idx_in, 
     CHECK(a->B >= 0, "negative dimension");
     CHECK(p_ok(a->P), "P must be 1, 2, 4 or 8");
     CHECK(a->k >= 1, "k must be >= 1");
-    CHECK(attn_shape_ok(a->H_q, a->d_qk, a->d_v), "unsupported attention shape");
+    const bool mla = mla_shape(a->d_qk, a->d_v);
+    CHECK(mla ? (a->H_q > 0 && a->H_q % 16 == 0) : attn_shape_ok(a->H_q, a->d_qk, a->d_v),
+          "unsupported attention shape");
+    CHECK(!mla || !a->V || (a->V == a->K && a->sV_b == a->sK_b),
+          "MLA geometry: V is the latent part of K (pass NULL or K itself)");
     if (a->B == 0) return LCSW_OK;
     CHECK(a->B <= 65535, "B must be <= 65535");
-    CHECK(a->q && a->K && a->V && a->seq_len && a->out && idx_in, "null pointer argument");
+    CHECK(a->q && a->K && (a->V || mla) && a->seq_len && a->out && idx_in,
+          "null pointer argument");
     CHECK(bf16_rows_ok(a->q, a->d_qk, 0) && bf16_rows_ok(a->K, a->d_qk, a->sK_b) &&
-              bf16_rows_ok(a->V, a->d_v, a->sV_b) && bf16_rows_ok(a->out, a->d_v, 0),
+              (mla || bf16_rows_ok(a->V, a->d_v, a->sV_b)) && bf16_rows_ok(a->out, a->d_v, 0),
           "bf16 rows must be 16-byte aligned");
     CHECK(aligned(a->seq_len, 4) && aligned(idx_in, 4) && (!a->lse || aligned(a->lse, 4)),
           "misaligned int32/fp32 array");
@@ -416,10 +444,13 @@ lcsw_status lcsw_decode_reuse(const lcsw_decode_args *a, const int32_t *idx_in, 
         return fail(LCSW_ERR_WORKSPACE, "decode reuse needs a 256-byte aligned workspace of %zu bytes",
                     need);
     DecodeWs w = carve_decode(a, ws);
-    return cuda_status(lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len,
-                                                idx_in, a->B, 1, a->H_q, a->d_qk, a->d_v, a->P,
-                                                a->k, a->scale, a->out, a->lse, w.attn,
-                                                (cudaStream_t)stream),
+    if (!(a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) &&
+        lcsw::reuse_decode_supported(a->B, a->H_q, a->d_qk, a->d_v, a->k) &&
+        lcsw::fused_decode_ws_bytes(a->B, a->G_max, a->H_q, a->d_v, a->k, a->P) > 0)
+        return cuda_status(lcsw::launch_reuse_decode(a, idx_in, w.fused, w.status,
+                                                     (cudaStream_t)stream),
+                           "decode reuse (persistent)");
+    return cuda_status(decode_attend(a, idx_in, w.attn, (cudaStream_t)stream),
                        "decode reuse attention");
 }
 
@@ -589,6 +620,37 @@ lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
     return cuda_status(e, "prefill attention");
 }
 
+size_t lcsw_sparse_attn_mla_workspace_size(int B, int T, int H_q, int k, int P) {
+    if (B <= 0 || T <= 0 || H_q <= 0 || k < 1 || !p_ok(P)) return 0;
+    return lcsw::sparse_attn_mla_ws_bytes(int64_t(B) * T, H_q, k, P);
+}
+
+lcsw_status lcsw_sparse_attn_mla(const lcsw_bf16 *q, const lcsw_bf16 *kv, int64_t skv_b,
+                                 const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                 int H_q, int P, int k, float scale, lcsw_bf16 *out, float *lse,
+                                 void *ws, size_t ws_bytes, lcsw_stream stream) {
+    CHECK(B >= 0 && T >= 0, "negative dimension");
+    CHECK(H_q > 0 && H_q % 16 == 0, "H_q must be a positive multiple of 16");
+    CHECK(p_ok(P), "P must be 1, 2, 4 or 8");
+    CHECK(k >= 1, "k must be >= 1");
+    const int64_t rows = int64_t(B) * T;
+    if (rows == 0) return LCSW_OK;
+    CHECK(rows <= 65535, "B*T must be <= 65535");
+    CHECK(q && kv && seq_len && idx && out, "null pointer argument");
+    CHECK(bf16_rows_ok(q, LCSW_MLA_DQK, 0) && bf16_rows_ok(kv, LCSW_MLA_DQK, skv_b) &&
+              bf16_rows_ok(out, LCSW_MLA_DV, 0) && skv_b >= 0,
+          "bf16 rows must be 16-byte aligned");
+    CHECK(aligned(seq_len, 4) && aligned(idx, 4) && (!lse || aligned(lse, 4)),
+          "misaligned int32/fp32 array");
+    const size_t need = lcsw::sparse_attn_mla_ws_bytes(rows, H_q, k, P);
+    if (need && (!ws || ws_bytes < need || !aligned(ws, 16)))
+        return fail(LCSW_ERR_WORKSPACE, "MLA sparse attention needs a 16-byte aligned workspace "
+                    "of %zu bytes", need);
+    return cuda_status(lcsw::launch_sparse_attn_mla(q, kv, skv_b, seq_len, idx, B, T, H_q, P, k,
+                                                    scale, out, lse, ws, (cudaStream_t)stream),
+                       "MLA sparse attention");
+}
+
 lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_b,
                                      const lcsw_bf16 *V, int64_t sV_b, const int32_t *seq_len,
                                      const int32_t *idx, int B, int T, int H_q, int d_qk,
@@ -611,6 +673,22 @@ lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int
     if (s != LCSW_OK) return s;
     return lcsw_sparse_attn(q, K, sK_b, V, sV_b, seq_len, idx, B, T, H_q, d_qk, d_v, P, k, scale,
                             out, lse, scratch, size_t(LCSW_NOALLOC_SCRATCH_BYTES), stream);
+}
+
+lcsw_status lcsw_kda_step(const lcsw_bf16 *qkv, const lcsw_bf16 *conv_w, lcsw_bf16 *conv_state,
+                          const float *g, const float *beta, float *state, lcsw_bf16 *out,
+                          int B, int T, int H, int D, lcsw_stream stream) {
+    CHECK(B >= 0 && T >= 0 && H >= 1 && D >= 1, "bad dimension");
+    if (D != 128) return fail(LCSW_ERR_UNSUPPORTED, "KDA step: head width %d (only 128)", D);
+    CHECK(B <= 65535, "B must be at most 65535");
+    if (B == 0 || T == 0) return LCSW_OK;
+    CHECK(qkv && conv_w && conv_state && g && beta && state && out, "null pointer argument");
+    CHECK(aligned(qkv, 2) && aligned(conv_w, 8) && aligned(conv_state, 2) && aligned(g, 4) &&
+              aligned(beta, 4) && aligned(state, 16) && aligned(out, 8),
+          "misaligned argument (conv_w 8 bytes, state 16, out 8)");
+    return cuda_status(lcsw::launch_kda_step(qkv, conv_w, conv_state, g, beta, state, out, B, T,
+                                             H, (cudaStream_t)stream),
+                       "KDA step launch");
 }
 
 lcsw_status lcsw_get_status(void *ws, lcsw_stream stream) {

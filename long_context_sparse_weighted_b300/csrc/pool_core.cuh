@@ -51,6 +51,63 @@ __device__ __forceinline__ uint32_t pool_pair(const float (&a)[P], const uint32_
     return round_bf16_exact(hi, lo);
 }
 
+// The same correctly rounded value by a shorter route when it is safe: an fp32
+// fma chain s approximates the exact sum X with |s - X| <= E, where E comes
+// from the chain of magnitudes m = sum |alpha_j k_j| (each fma rounds once,
+// relative 2^-24, so |s - X| <= P 2^-24 m (1 + 2^-24)^(2P) plus underflow,
+// below (P + 1) 2^-24 m + 2^-140).  If no bf16 rounding boundary lies within
+// E of s -- the midpoint between the two bf16 values around s, and a quarter
+// bf16 step for the boundaries beyond them -- X rounds like s.  Returns false
+// (undecided) otherwise, and for zero, subnormal or non-finite s.
+template <int P>
+__device__ __forceinline__ bool pool_pair_fast(const float (&a)[P], const uint32_t (&w)[P],
+                                               bool high, uint32_t &out) {
+    float s = 0.0f, m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+        const float kv = high ? bf_hi(w[j]) : bf_lo(w[j]);
+        s = __fmaf_rn(a[j], kv, s);
+        m = __fmaf_rn(fabsf(a[j]), fabsf(kv), m);
+    }
+    const float E = __fmaf_rn(m, float(P + 1) * 0x1p-24f, 0x1p-140f);
+    const uint32_t u = __float_as_uint(s);
+    const float lo = __uint_as_float(u & 0xFFFF0000u);          // s truncated to bf16
+    const float mid = __uint_as_float((u & 0xFFFF0000u) | 0x8000u);
+    // s - mid is exact (same sign and exponent); |lo| / 1024 is at most a
+    // quarter of the bf16 step at s
+    const float room = fminf(fabsf(__fsub_rn(s, mid)), fabsf(lo) * 0x1p-10f);
+    out = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+    return E < room;
+}
+
+template <int P>
+__device__ __forceinline__ uint32_t pool_pair_any(const float (&a)[P], const uint32_t (&w)[P],
+                                                  bool high) {
+    uint32_t r;
+    if (pool_pair_fast<P>(a, w, high, r)) return r;
+    return pool_pair<P>(a, w, high);
+}
+
+// Pool 8 dims (one 16-byte chunk of each of the P source rows) through the
+// shorter route where it decides the rounding.
+template <int P>
+__device__ __forceinline__ uint4 pool_chunk_fast(const float (&a)[P], const uint4 (&rows)[P]) {
+    uint32_t wx[P], wy[P], wz[P], ww[P];
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+        wx[j] = rows[j].x;
+        wy[j] = rows[j].y;
+        wz[j] = rows[j].z;
+        ww[j] = rows[j].w;
+    }
+    uint4 o;
+    o.x = pool_pair_any<P>(a, wx, false) | (pool_pair_any<P>(a, wx, true) << 16);
+    o.y = pool_pair_any<P>(a, wy, false) | (pool_pair_any<P>(a, wy, true) << 16);
+    o.z = pool_pair_any<P>(a, wz, false) | (pool_pair_any<P>(a, wz, true) << 16);
+    o.w = pool_pair_any<P>(a, ww, false) | (pool_pair_any<P>(a, ww, true) << 16);
+    return o;
+}
+
 // Pool 8 dims (one 16-byte chunk of each of the P source rows).
 template <int P>
 __device__ __forceinline__ uint4 pool_chunk(const float (&a)[P], const uint4 (&rows)[P]) {

@@ -172,3 +172,19 @@ def test_decode_reuse_validates_arguments(L):
     assert L.lcsw_decode_reuse(ctypes.byref(a), 0x60000, ws, 1 << 30, None) == lcsw.ERR_INVALID_ARG
     a.H_q = 32
     assert L.lcsw_decode_reuse(ctypes.byref(a), 0x60000, ws, 16, None) == lcsw.ERR_WORKSPACE
+
+
+def test_kda_step_validates_arguments(L):
+    import long_context_sparse_weighted_b300 as lcsw
+    p = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000]
+    # head width other than 128 is a valid shape the kernel does not cover
+    assert L.lcsw_kda_step(*p, 2, 1, 64, 64, None) == lcsw.ERR_UNSUPPORTED
+    assert L.lcsw_kda_step(*p, -1, 1, 64, 128, None) == lcsw.ERR_INVALID_ARG
+    assert L.lcsw_kda_step(*p, 2, 1, 0, 128, None) == lcsw.ERR_INVALID_ARG
+    # empty batch or no tokens: nothing to do, nothing dereferenced
+    assert L.lcsw_kda_step(None, None, None, None, None, None, None, 0, 1, 64, 128, None) == lcsw.OK
+    assert L.lcsw_kda_step(None, None, None, None, None, None, None, 2, 0, 64, 128, None) == lcsw.OK
+    assert L.lcsw_kda_step(*p[:6], None, 2, 1, 64, 128, None) == lcsw.ERR_INVALID_ARG
+    bad = list(p)
+    bad[5] = 0x60004                       # state not 16-byte aligned
+    assert L.lcsw_kda_step(*bad, 2, 1, 64, 128, None) == lcsw.ERR_INVALID_ARG
