@@ -57,7 +57,7 @@ def parse():
                     help="rotated input copies (0: enough to exceed 3x L2)")
     ap.add_argument("--kernel", default=None,
                     choices=["prefill_scores", "prefill", "pool_keys", "index_scores", "topk",
-                             "sparse_attn", "decode", "decode_fp8", "kda", "reuse"],
+                             "sparse_attn", "decode", "decode_fp8", "kda", "reuse", "mla"],
                     help="time one kernel of the path instead of the decode step (not the "
                          "headline line): prefill_scores = the chunked-prefill indexer "
                          "scores (tcgen05 GEMM) on the prefill_4k shapes; prefill = one whole "
@@ -953,6 +953,70 @@ def measure_decode_fp8(torch, lcsw, peak, with_oracle):
     return entry
 
 
+def measure_mla(torch, lcsw, peak, with_oracle):
+    """MLA latent geometry on decode_1m: attention of 64 heads over 512 groups
+    (2,048 tokens) of a 1,048,576-token cache of 576-wide rows whose latent 512
+    dims are the value (lcsw_sparse_attn_mla), each call after a write of
+    twice the L2 size.  The groups are a seeded draw (the attention's cost does
+    not depend on which groups the indexer picked)."""
+    spec = synth.named("mla_decode_1m")
+    c = synth.generate(spec)
+    dev = "cuda"
+    up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    G = spec.lengths[0] // spec.P
+    rng = np.random.default_rng(340)
+    idx_h = np.sort(rng.choice(G, spec.k, replace=False)).astype(np.int32).reshape(1, 1, spec.k)
+    q, kv = up16(c["q"]), up16(c["K"])
+    seq, idx = torch.from_numpy(c["seq_len"]).to(dev), torch.from_numpy(idx_h).to(dev)
+    out = torch.empty(1, 1, spec.H_q, spec.d_v, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(1, 1, spec.H_q, dtype=torch.float32, device=dev)
+    nb = lcsw.lib().lcsw_sparse_attn_mla_workspace_size(1, 1, spec.H_q, spec.k, spec.P)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+    fn = lambda: lcsw.sparse_attn_mla(q, kv, seq, idx, spec.P, c["scale"], out=out, lse=lse,
+                                      ws=ws)
+    parity = None
+    if with_oracle:
+        import oracle
+        fn()
+        torch.cuda.synchronize()
+        o_ref, l_ref = oracle.sparse_attn(c["q"], c["K"], c["V"], c["seq_len"], idx_h, spec.P,
+                                          c["scale"])
+        g = synth.bf16_to_f32(out.view(torch.int16).cpu().numpy().view(np.uint16))
+        r = synth.bf16_to_f32(o_ref)
+        parity = {"max_abs_err": float(np.abs(g - r).max()),
+                  "lse_max_err": float(np.abs(lse.cpu().numpy() - l_ref).max())}
+    flush = torch.empty(2 * l2_bytes() // 4, dtype=torch.float32, device=dev)
+    for _ in range(5):
+        fn()
+    torch.cuda.synchronize()
+    n = 200
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        flush.fill_(1.0)
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in evs)[n // 2]
+    ntok = spec.P * spec.k
+    ab = ntok * spec.d_qk * 2 + spec.H_q * (spec.d_qk + spec.d_v) * 2 + spec.k * 4
+    flops = 2 * spec.H_q * ntok * (spec.d_qk + spec.d_v)
+    gbs = ab / (ms / 1e3) / 1e9
+    launches = 1 if nb == 0 else 2
+    del q, kv, flush
+    torch.cuda.empty_cache()
+    return {"kernel": "lcsw_sparse_attn_mla (sparse_attn_mla_kernel + combine)",
+            "config": {"batch": 1, "context": spec.lengths[0], "heads": spec.H_q,
+                       "row_width": spec.d_qk, "latent": spec.d_v, "groups": spec.k},
+            "ms_per_call": round(ms, 5), "launches_per_call": launches, "alg_bytes": ab,
+            "alg_flops": flops, "timing": "median of 200 calls, each after a write of 2x L2",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs / peak, 4)},
+            "tflops": round(flops / (ms / 1e3) / 1e12, 2), "parity_vs_oracle": parity}
+
+
 def kda_alg_bytes(B, T, H, D):
     """Bytes a KDA step must move: the fp32 state read and written once, the
     conv history read and written, the step's inputs (projections, gates,
@@ -1054,6 +1118,7 @@ def per_config(args, torch, lcsw, peak, peaks):
     res["indexcache_reuse_1m"] = measure_reuse(torch, lcsw, peak, args._headline_step_ms)
     res["decode_1m_fp8_keys"] = measure_decode_fp8(torch, lcsw, peak, oracle_on)
     res["kda_decode_b64"] = measure_kda(torch, lcsw, peak, 200, 5, oracle_on)
+    res["mla_attn_decode_1m"] = measure_mla(torch, lcsw, peak, oracle_on)
     return res
 
 
@@ -1098,7 +1163,9 @@ def run_kernel_alone(args):
     elif args.kernel == "topk":
         lcsw.index_scores(qi, w, kp, seq, P, out=scores)
         idx = torch.empty(B, 1, k, dtype=torch.int32, device=dev)
-        fn = lambda: lcsw.topk_groups(scores, nv, k, out=idx)
+        nbw = lcsw.lib().lcsw_topk_workspace_size(B, G, k)
+        tws = torch.empty(max(nbw, 256), dtype=torch.uint8, device=dev)
+        fn = lambda: lcsw.topk_groups(scores, nv, k, out=idx, ws=tws)
         ab = G * 4 + k * 4
     else:
         lcsw.index_scores(qi, w, kp, seq, P, out=scores)
@@ -1152,6 +1219,15 @@ def main():
     if args.kernel in ("pool_keys", "index_scores", "topk", "sparse_attn", "decode",
                        "decode_fp8"):
         run_kernel_alone(args)
+        return
+    if args.kernel == "mla":
+        import torch
+
+        import long_context_sparse_weighted_b300 as lcsw
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+            os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        e = measure_mla(torch, lcsw, peaks.get("hbm_gbs", 6400.0), True)
+        print(json.dumps({"kernel": "mla", **e}))
         return
     if args.kernel == "reuse":
         import torch

@@ -135,8 +135,12 @@ lcsw_status lcsw_visible_counts(const int32_t *seq_len, const int32_t *q_pos,
  *
  *   scores [rows][G_max] fp32      n_valid [rows] int32 device
  *   idx    [rows][k] int32 (output)
- *   ws     device workspace of lcsw_topk_workspace_size(rows, G_max, k) bytes
- *          (may be NULL when that size is 0)
+ *   ws     device workspace of lcsw_topk_workspace_size(rows, G_max, k) bytes,
+ *          256-byte aligned, no clearing needed (may be NULL when that size is
+ *          0).  The size is nonzero for a few long rows (rows <= 32 and
+ *          16384 <= G_max <= 524288), which are then spread over many blocks
+ *          (a memset and three launches); with no or a smaller workspace those
+ *          rows take one block each, with the same result.
  * ------------------------------------------------------------------------- */
 size_t lcsw_topk_workspace_size(int64_t rows, int G_max, int k);
 lcsw_status lcsw_topk_groups(const float *scores, const int32_t *n_valid,

@@ -224,8 +224,10 @@ def visible_counts(seq_len, q_pos, B, T, P, stream=None):
     return out
 
 
-def topk_groups(scores, n_valid, k, out=None, stream=None):
-    """Top-k groups per row, ascending, -1 padded (rows = all leading dims)."""
+def topk_groups(scores, n_valid, k, out=None, ws=None, stream=None):
+    """Top-k groups per row, ascending, -1 padded (rows = all leading dims).
+    ws: optional uint8 workspace of lcsw_topk_workspace_size bytes (allocated
+    here when missing; few long rows use it for the multi-block selection)."""
     _dense(scores, torch.float32, "scores")
     _dense(n_valid, torch.int32, "n_valid")
     G_max = scores.shape[-1]
@@ -233,7 +235,8 @@ def topk_groups(scores, n_valid, k, out=None, stream=None):
     if out is None:
         out = torch.empty(*scores.shape[:-1], k, dtype=torch.int32, device=scores.device)
     nbytes = lib().lcsw_topk_workspace_size(rows, G_max, k)
-    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=scores.device) if nbytes else None
+    if ws is None and nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=scores.device)
     _check(lib().lcsw_topk_groups(_ptr(scores), _ptr(n_valid), rows, G_max, k, _ptr(out),
                                   _ptr(ws), nbytes, _stream(stream)))
     return out

@@ -84,6 +84,14 @@ cudaError_t launch_topk_rows(const float *scores, const int32_t *n_valid,
                              const int32_t *seq_len, int P, int T, int64_t rows, int G_max,
                              int k, int32_t *idx, cudaStream_t st,
                              const int32_t *row_mask = nullptr);
+// The same selection for a few long rows, spread over many blocks (three
+// launches and a memset; topk.cu).  Supported for rows <= 32 and
+// 16384 <= G_max <= 524288; ws of topk_wide_ws_bytes bytes, 256-aligned.
+bool topk_wide_supported(int64_t rows, int G_max, int k);
+size_t topk_wide_ws_bytes(int64_t rows, int G_max, int k);
+cudaError_t launch_topk_rows_wide(const float *scores, const int32_t *n_valid,
+                                  const int32_t *seq_len, int P, int T, int64_t rows, int G_max,
+                                  int k, int32_t *idx, void *ws, cudaStream_t st);
 
 // Sparse attention for many query rows on tcgen05 (H_q <= 32, d_qk = d_v =
 // 128): one persistent CTA per SM, no workspace; records a timed-out wait in

@@ -168,20 +168,24 @@ lcsw_status lcsw_index_scores(const lcsw_bf16 *q_idx, const float *w_head,
 }
 
 size_t lcsw_topk_workspace_size(int64_t rows, int G_max, int k) {
-    (void)rows; (void)G_max; (void)k;
-    return 0;
+    if (rows <= 0 || G_max <= 0 || k < 1) return 0;
+    return lcsw::topk_wide_ws_bytes(rows, G_max, k);
 }
 
 lcsw_status lcsw_topk_groups(const float *scores, const int32_t *n_valid, int64_t rows,
                              int G_max, int k, int32_t *idx, void *ws, size_t ws_bytes,
                              lcsw_stream stream) {
-    (void)ws; (void)ws_bytes;
     CHECK(rows >= 0 && G_max >= 0, "negative dimension");
     CHECK(k >= 1, "k must be >= 1 (got %d)", k);
     CHECK(rows <= 0x7FFFFFFF, "too many rows");
     if (rows == 0) return LCSW_OK;
     CHECK(scores && n_valid && idx, "null pointer argument");
     CHECK(aligned(scores, 4) && aligned(n_valid, 4) && aligned(idx, 4), "misaligned array");
+    const size_t wide = lcsw::topk_wide_ws_bytes(rows, G_max, k);
+    if (wide && ws && ws_bytes >= wide && aligned(ws, 256))
+        return cuda_status(lcsw::launch_topk_rows_wide(scores, n_valid, nullptr, 1, 1, rows,
+                                                       G_max, k, idx, ws, (cudaStream_t)stream),
+                           "topk launch (wide rows)");
     return cuda_status(lcsw::launch_topk_rows(scores, n_valid, nullptr, 1, 1, rows, G_max, k,
                                               idx, (cudaStream_t)stream),
                        "topk launch");
@@ -282,6 +286,8 @@ struct DecodeWs {
     int32_t *idx;
     void *attn;
     void *fused;
+    void *topk;          // the few-long-rows selection's region (or none)
+    size_t topk_bytes;
     size_t total;
 };
 
@@ -297,6 +303,8 @@ static DecodeWs carve_decode(const lcsw_decode_args *a, void *ws) {
     w.attn = c.take(mla_shape(a->d_qk, a->d_v)
                         ? lcsw::sparse_attn_mla_ws_bytes(a->B, a->H_q, a->k, a->P)
                         : lcsw::sparse_attn_ws_bytes(a->B, a->H_q, a->d_v, a->k, a->P));
+    w.topk_bytes = lcsw::topk_wide_ws_bytes(a->B, a->G_max, a->k);
+    w.topk = c.take(w.topk_bytes);
     w.total = c.off;
     return w;
 }
@@ -357,7 +365,10 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
                                                   a->seq_len, nullptr, a->B, 1, a->H_i, a->P,
                                                   a->G_max, scores, st);
     if (e != cudaSuccess) return cuda_status(e, "decode scores");
-    e = lcsw::launch_topk_rows(scores, nullptr, a->seq_len, a->P, 1, a->B, a->G_max, a->k, idx, st);
+    e = w.topk_bytes ? lcsw::launch_topk_rows_wide(scores, nullptr, a->seq_len, a->P, 1, a->B,
+                                                   a->G_max, a->k, idx, w.topk, st)
+                     : lcsw::launch_topk_rows(scores, nullptr, a->seq_len, a->P, 1, a->B,
+                                              a->G_max, a->k, idx, st);
     if (e != cudaSuccess) return cuda_status(e, "decode top-k");
     return cuda_status(decode_attend(a, idx, w.attn, st), "decode attention");
 }

@@ -86,14 +86,28 @@ cudaError_t launch_pool_keys(const uint16_t *k_idx, int64_t sk_b, const float *p
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int threads = 256;
     const int by = B < 65535 ? B : 65535;
-    // about 8 resident blocks of 256 per SM over the whole grid
-    const int64_t cap = std::max<int64_t>(1, int64_t(sms) * 8 / by);
-    const int64_t bx = std::min<int64_t>((per_b + threads - 1) / threads, cap);
     const int cpr_shift = (cpr & (cpr - 1)) == 0 ? __builtin_ctz(unsigned(cpr)) : -1;
-#define LCSW_POOL(PP)                                                                       \
-    pool_keys_kernel<PP><<<dim3(unsigned(bx), unsigned(by)), threads, 0, st>>>(             \
-        k_idx, sk_b, pool_w, sw_b, seq_len, g_begin, B, g_span, d_idx, cpr_shift, mode, tail, \
-        k_pooled, sp_b)
+    // one wave: the resident blocks of every SM over the whole grid
+    static int occ_cache[9];  // per P (a benign race: every thread computes the same value)
+    auto grid_x = [&](const void *kern) {
+        int occ = occ_cache[P];
+        if (occ < 1) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, 0) !=
+                    cudaSuccess ||
+                occ < 1)
+                occ = 4;
+            occ_cache[P] = occ;
+        }
+        const int64_t cap = std::max<int64_t>(1, int64_t(sms) * occ / by);
+        return unsigned(std::min<int64_t>((per_b + threads - 1) / threads, cap));
+    };
+#define LCSW_POOL(PP)                                                                         \
+    {                                                                                         \
+        auto kern = pool_keys_kernel<PP>;                                                     \
+        kern<<<dim3(grid_x(reinterpret_cast<const void *>(kern)), unsigned(by)), threads, 0,  \
+               st>>>(k_idx, sk_b, pool_w, sw_b, seq_len, g_begin, B, g_span, d_idx, cpr_shift, \
+                     mode, tail, k_pooled, sp_b);                                             \
+    }
     switch (P) {
         case 1: LCSW_POOL(1); break;
         case 2: LCSW_POOL(2); break;

@@ -139,21 +139,36 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(
     const int lane = threadIdx.x & 31;
     if (h >= H_q) return;
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, part_ml[(row * S + s) * H_q + h].x);
+    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(&part_ml[(row * S + s) * H_q + h].x));
     const float ref = M == -INFINITY ? 0.f : M;
-    constexpr int PER = DV / 32;
+    constexpr int PER = DV / 32;  // 2 or 4 value dims per lane
     float acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
     float Lsum = 0.f;
-    for (int s = 0; s < S; ++s) {
-        const int64_t pi = (row * S + s) * H_q + h;
-        const float2 ml = part_ml[pi];
-        const float f = exp2f(ml.x - ref);
-        Lsum += f * ml.y;
-        const float *po = part_o + pi * DV + lane * PER;
+    // eight splits at a time, their loads issued together
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        float v[8][PER];
+        float f[8];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) acc[i] += f * po[i];
+        for (int u = 0; u < 8; ++u) {
+            f[u] = 0.f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) v[u][i] = 0.f;
+            if (s0 + u < S) {
+                const int64_t pi = (row * S + s0 + u) * H_q + h;
+                const float2 ml = __ldg(&part_ml[pi]);
+                f[u] = exp2f(ml.x - ref);
+                Lsum += f[u] * ml.y;
+                const float *po = part_o + pi * DV + lane * PER;
+#pragma unroll
+                for (int i = 0; i < PER; ++i) v[u][i] = __ldg(po + i);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int i = 0; i < PER; ++i) acc[i] += f[u] * v[u][i];
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
     uint16_t *orow = out + (row * H_q + h) * DV + lane * PER;

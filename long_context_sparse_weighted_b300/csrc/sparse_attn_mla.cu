@@ -20,7 +20,7 @@
 // memory, then warp (t, q) accumulates value dims [128 q, 128 q + 128) of
 // O += P V over all 64 tokens for its 16 heads.  Each block writes its
 // partial (m, l, O) per head, or the normalised output with one split.
-// Kernel 2 (combine): one warp per (row, head) merges the splits.
+// Kernel 2 (combine): one block per (row, head) merges the splits.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -276,51 +276,52 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_mla_kernel(
     }
 }
 
-// One warp per (row, head): out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(256) mla_combine_kernel(const float *__restrict__ part_o,
-                                                          const float2 *__restrict__ part_ml,
-                                                          int H_q, int S, int64_t rows,
-                                                          uint16_t *__restrict__ out,
-                                                          float *__restrict__ lse) {
-    const int lane = threadIdx.x & 31;
-    const int64_t w = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (w >= rows * H_q) return;
+// One block of 128 threads per (row, head): out = sum_s 2^(m_s - M) o_s /
+// sum_s 2^(m_s - M) l_s.  Every thread takes the split weights (S <= 64
+// words, cached) and four value dims; the splits' rows are loaded eight at a
+// time so that their latencies overlap.
+constexpr int kCombThreads = kLat / 4;
+__global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(
+    const float *__restrict__ part_o, const float2 *__restrict__ part_ml, int H_q, int S,
+    uint16_t *__restrict__ out, float *__restrict__ lse) {
+    const int64_t w = blockIdx.x;  // row * H_q + h
     const int64_t row = w / H_q;
     const int h = int(w % H_q);
+    const int t = threadIdx.x;
+    auto pidx = [&](int s) { return (row * S + s) * H_q + h; };
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, part_ml[(row * S + s) * H_q + h].x);
+    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(&part_ml[pidx(s)].x));
     const float ref = M == -INFINITY ? 0.f : M;
-    constexpr int PER = kLat / 32;  // 16 dims per lane, as 4 float4
-    float acc[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float Lsum = 0.f;
-    for (int s = 0; s < S; ++s) {
-        const int64_t pi = (row * S + s) * H_q + h;
-        const float2 ml = part_ml[pi];
-        if (ml.y <= 0.f) continue;
-        const float wgt = exp2f(ml.x - ref);
-        Lsum += wgt * ml.y;
-        const float4 *po = reinterpret_cast<const float4 *>(part_o + pi * kLat);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        float4 v[8];
+        float wgt[8];
 #pragma unroll
-        for (int i = 0; i < PER / 4; ++i) {
-            const float4 v = po[lane + 32 * i];
-            acc[4 * i] += wgt * v.x;
-            acc[4 * i + 1] += wgt * v.y;
-            acc[4 * i + 2] += wgt * v.z;
-            acc[4 * i + 3] += wgt * v.w;
+        for (int u = 0; u < 8; ++u) {
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            wgt[u] = 0.f;
+            if (s0 + u < S) {
+                const float2 ml = __ldg(&part_ml[pidx(s0 + u)]);
+                if (ml.y > 0.f) {
+                    wgt[u] = exp2f(ml.x - ref);
+                    Lsum += wgt[u] * ml.y;
+                    v[u] = __ldg(reinterpret_cast<const float4 *>(part_o + pidx(s0 + u) * kLat) + t);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            acc.x += wgt[u] * v[u].x;
+            acc.y += wgt[u] * v[u].y;
+            acc.z += wgt[u] * v[u].z;
+            acc.w += wgt[u] * v[u].w;
         }
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    uint16_t *orow = out + w * kLat;
-#pragma unroll
-    for (int i = 0; i < PER / 4; ++i) {
-        const int d = (lane + 32 * i) * 4;
-        *reinterpret_cast<uint2 *>(orow + d) =
-            make_uint2(pack_bf2(acc[4 * i] * inv, acc[4 * i + 1] * inv),
-                       pack_bf2(acc[4 * i + 2] * inv, acc[4 * i + 3] * inv));
-    }
-    if (lse && lane == 0) lse[w] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+    *reinterpret_cast<uint2 *>(out + w * kLat + t * 4) =
+        make_uint2(pack_bf2(acc.x * inv, acc.y * inv), pack_bf2(acc.z * inv, acc.w * inv));
+    if (lse && t == 0) lse[w] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
 }
 
 }  // namespace
@@ -360,9 +361,8 @@ cudaError_t launch_sparse_attn_mla(const uint16_t *q, const uint16_t *kv, int64_
         q, kv, skv_b, seq_len, idx, T, H_q, P, k, S, scale * kLog2e, out, lse, part_o, part_ml);
     e = cudaGetLastError();
     if (e != cudaSuccess || S == 1) return e;
-    const int64_t warps = rows * H_q;
-    mla_combine_kernel<<<unsigned((warps + 7) / 8), 256, 0, st>>>(part_o, part_ml, H_q, S, rows,
-                                                                  out, lse);
+    mla_combine_kernel<<<unsigned(rows * H_q), kCombThreads, 0, st>>>(part_o, part_ml, H_q, S,
+                                                                       out, lse);
     return cudaGetLastError();
 }
 

@@ -30,6 +30,9 @@ selected global access in eleven layers": ``index_kpool: 4``,
                  seed 3.
 * ``prefill_4k`` B=1, 4096 new query tokens after 262144 cached tokens,
                  top-k 512 per query, 32 query heads, d=128, seed 4.
+* ``mla_decode_1m`` decode_1m's indexer recipe with the MLA latent cache:
+                 one 576-wide key row per token (latent 512 + rotary 64) whose
+                 first 512 dims are the value, 64 query heads, seed 5.
 
 Indexer head weights of the Gaussian workloads are U(0, 1) (the pages give
 no distribution for them).  bf16 values are stored as their raw uint16 bit
@@ -142,6 +145,7 @@ class Spec:
     plant_frac: float = 0.0          # fraction of raw indexer keys planted toward q
     seed: int = 0
     L_cap: Optional[int] = None      # allocated tokens per sequence (>= max length)
+    mla: bool = False                # one K row per token whose first d_v dims are V
 
     @property
     def L_max(self) -> int:
@@ -184,6 +188,11 @@ def named(name: str) -> Spec:
     if name == "ragged_b64":
         return Spec(name=name, B=64, lengths=ragged_lengths(64, 8192, 262144, 3), H_i=8,
                     k=512, H_q=32, d_qk=128, d_v=128, seed=3)
+    if name == "mla_decode_1m":
+        # decode_1m's indexer and selection with the MLA latent cache: one
+        # 576-wide row per token (latent 512 + rotary 64), the latent as value
+        return Spec(name=name, B=1, lengths=[1048576], H_i=8, k=512, H_q=64, d_qk=576,
+                    d_v=512, plant_frac=0.05, mla=True, seed=5)
     if name == "prefill_4k":
         return Spec(name=name, B=1, lengths=[262144 + 4096], T=4096, prefill=True, H_i=8,
                     k=512, H_q=32, d_qk=128, d_v=128, seed=4)
@@ -325,5 +334,9 @@ def generate(spec: Spec, with_kv: bool = True) -> dict:
                d_v=spec.d_v, scale=spec.softmax_scale)
     if with_kv:
         out["K"] = per_token(_TID["K"], spec.d_qk, "normal")
-        out["V"] = per_token(_TID["V"], spec.d_v, "normal")
+        if spec.mla:
+            # the MLA latent geometry: the value is the latent part of the key row
+            out["V"] = np.ascontiguousarray(out["K"][:, :, :spec.d_v])
+        else:
+            out["V"] = per_token(_TID["V"], spec.d_v, "normal")
     return out

@@ -197,6 +197,32 @@ def test_topk_long_row():
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("case", ["normal", "ties_at_k", "all_equal", "short_rows",
+                                  "one_hot_digit"])
+def test_topk_few_long_rows_multi_block(case):
+    """Few long rows take the multi-block selection (histogram, filter,
+    final); each must equal the oracle bit for bit.  all_equal overflows the
+    candidate list and takes the one-block fallback inside the last launch;
+    short_rows mixes rows with n_valid <= k and a row below the list's size."""
+    rows, G, k = 4, 262144, 512
+    s = _topk_case(rows, G, "normal", 150)
+    n_valid = np.array([G, G - 3, 200000, 131073], np.int32)
+    if case == "ties_at_k":
+        s[:, 5000:9000] = np.sort(s[0])[-400]       # a wide tie around the k-th score
+    elif case == "all_equal":
+        s[1] = 0.75
+        s[2, :] = -0.0
+        s[2, ::7] = 0.0                             # -0 and +0 tie
+    elif case == "short_rows":
+        n_valid = np.array([G, 300, 512, 20000], np.int32)
+    elif case == "one_hot_digit":
+        s[3] = np.float32(1.0) + np.arange(G, dtype=np.float32) * np.float32(2 ** -23)
+    assert lcsw.lib().lcsw_topk_workspace_size(rows, G, k) > 0
+    ref = oracle.topk(s, n_valid, k)
+    got = lcsw.topk_groups(dev(s), dev(n_valid), k).cpu().numpy()
+    assert np.array_equal(got, ref)
+
+
 # -------------------------------------------------------------- attention ---
 
 def _attn_case(B, lengths, T, H_q, d_qk, d_v, k, P, seed, pad=0):
