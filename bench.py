@@ -1050,17 +1050,23 @@ def measure_kda(torch, lcsw, peak, steps, warmup, with_oracle):
         for b in (0, spec.B - 1):
             sub = {k: (v[b:b + 1] if isinstance(v, np.ndarray) and k != "conv_w" else v)
                    for k, v in c.items()}
-            o_ref, S_ref, cs_ref = okda.kda_step(sub["qkv"], c["conv_w"], sub["conv_state"],
-                                                 sub["g"], sub["beta"], sub["state"], spec.H,
-                                                 spec.D)
+            o_ref, S_ref, cs_ref, parts = okda.kda_step(
+                sub["qkv"], c["conv_w"], sub["conv_state"], sub["g"], sub["beta"], sub["state"],
+                spec.H, spec.D, return_parts=True)
             S = d["state"][b:b + 1].cpu().numpy().astype(np.float64)
             o = synth.bf16_to_f32(out[b:b + 1].view(torch.int16).cpu().numpy().view(
                 np.uint16)).astype(np.float64)
             smax = np.abs(S_ref).max(axis=(-2, -1), keepdims=True)
             worst_s = max(worst_s, float((np.abs(S - S_ref) / smax).max()))
-            omax = np.abs(o_ref).max(axis=-1, keepdims=True)
-            worst_o = max(worst_o, float((np.abs(o - o_ref) / (2.0 ** -8 * np.abs(o_ref)
-                                                                + 1e-5 * omax)).max()))
+            # bound: one bf16 rounding plus fp32 sums of terms of total magnitude M
+            q, k_, v = parts[:, 0, 0], parts[:, 0, 1], parts[:, 0, 2]
+            Sp = np.exp(sub["g"][:, 0].astype(np.float64))[..., None] * sub["state"]
+            dw = sub["beta"][:, 0].astype(np.float64)[..., None] * (
+                v - np.einsum("bhi,bhij->bhj", k_, Sp))
+            M = (np.einsum("bhi,bhij->bhj", np.abs(q), np.abs(Sp))
+                 + np.abs((q * k_).sum(-1))[..., None] * np.abs(dw))
+            worst_o = max(worst_o, float((np.abs(o[:, 0] - o_ref[:, 0]) /
+                                          (2.0 ** -8 * np.abs(o_ref[:, 0]) + 2.0 ** -16 * M)).max()))
         parity = {"sequences_checked": 2, "state_err_over_head_max": worst_s,
                   "out_err_over_bound": worst_o,
                   "ok": bool(worst_s <= 4e-6 and worst_o <= 1.0)}

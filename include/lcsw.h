@@ -475,6 +475,19 @@ lcsw_status lcsw_kda_step(const lcsw_bf16 *qkv, const lcsw_bf16 *conv_w, lcsw_bf
  * ------------------------------------------------------------------------- */
 lcsw_status lcsw_get_status(void *ws, lcsw_stream stream);
 
+/* ---------------------------------------------------------------------------
+ * Device-side bounds checks.  A library built with -DLCSW_CHECKS=1 checks the
+ * data-dependent indices of its kernels (positions derived from candidate
+ * counts, selections and lengths) against their extents; a failed check
+ * records a nonzero code and skips the access (no trap, the context stays
+ * usable).  lcsw_check_status synchronises the device and returns the first
+ * code recorded since the last call (0: none; -1: the device could not be
+ * read), clearing them.  lcsw_checks_enabled tells which build this is; in a
+ * normal build lcsw_check_status always returns 0.
+ * ------------------------------------------------------------------------- */
+int lcsw_checks_enabled(void);
+int lcsw_check_status(void);
+
 #ifdef __cplusplus
 }
 #endif

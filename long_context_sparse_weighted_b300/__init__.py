@@ -89,6 +89,8 @@ _SIGNATURES = {
                               _vp, _vp, _sz, _vp], _i32),
     "lcsw_kda_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "lcsw_get_status": ([_vp, _vp], _i32),
+    "lcsw_checks_enabled": ([], _i32),
+    "lcsw_check_status": ([], _i32),
 }
 
 

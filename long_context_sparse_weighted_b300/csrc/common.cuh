@@ -135,6 +135,42 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
     return before;
 }
 
+// ---------------------------------------------------------- bounds checks ---
+// Built with -DLCSW_CHECKS=1, the kernels check their data-dependent indices
+// (positions derived from candidate counts, selections and lengths) against
+// the extents they were given: a failed check records its code in this
+// translation unit's check word (the first failure wins) and the access is
+// skipped -- no trap.  lcsw_check_status() collects and clears the words.  In
+// the normal build LCSW_INBOUNDS(cond, code) is the constant true.
+namespace lcsw {
+void register_check_reader(int (*reader)());
+}
+#ifdef LCSW_CHECKS
+namespace {
+__device__ int g_lcsw_check_word;
+int lcsw_read_check_word() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_lcsw_check_word, sizeof v) != cudaSuccess) return -1;
+    if (v) {
+        const int z = 0;
+        cudaMemcpyToSymbol(g_lcsw_check_word, &z, sizeof z);
+    }
+    return v;
+}
+struct CheckReaderRegistration {
+    CheckReaderRegistration() { lcsw::register_check_reader(&lcsw_read_check_word); }
+};
+const CheckReaderRegistration g_lcsw_check_registration;
+__device__ __forceinline__ bool lcsw_inbounds(bool ok, int code) {
+    if (!ok) atomicCAS(&g_lcsw_check_word, 0, code);
+    return ok;
+}
+}  // namespace
+#define LCSW_INBOUNDS(cond, code) lcsw_inbounds((cond), (code))
+#else
+#define LCSW_INBOUNDS(cond, code) true
+#endif
+
 // ------------------------------------------------------ bounded waiting ----
 
 // Budget for device-side spin waits, in SM clock cycles (~0.5 s at 2 GHz).

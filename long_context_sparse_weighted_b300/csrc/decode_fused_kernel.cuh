@@ -147,16 +147,21 @@ static_assert(AttLayout<192, 128>::total <= kAttBytes, "attention operands overf
 // Selection workspace: the sequence's slot headers, the candidates (keys and
 // groups, or packed (key << 32 | ~group) values for ranking), a 2048-bin
 // histogram and the threshold-bin ties.
+// The candidate capacity is twice kSelCap where region U has room for it
+// (d_qk <= 128: smaller Q rows and prefetch buffer).
 template <int DQK, int DV>
 struct SelLayout {
     static constexpr int hdr = (AttLayout<DQK, DV>::buf + AttLayout<DQK, DV>::kv_bytes + 15) / 16 * 16;
     static constexpr int key = hdr + kMaxCtas * 8;
-    static constexpr int grp = key + kSelCap * 4;
-    static constexpr int hist = grp + kSelCap * 4;
+    static constexpr int cap =
+        key + 2 * kSelCap * 8 + 2048 * 4 + kTieCap * 8 <= kUBytes ? 2 * kSelCap : kSelCap;
+    static constexpr int grp = key + cap * 4;
+    static constexpr int hist = grp + cap * 4;
     static constexpr int tie = hist + 2048 * 4;
     static constexpr int end = tie + kTieCap * 8;
 };
 static_assert(SelLayout<192, 128>::end <= kUBytes, "selection overflows region U");
+static_assert(SelLayout<128, 128>::end <= kUBytes, "selection overflows region U");
 
 struct Params {
     const uint16_t *q_idx;
@@ -1227,8 +1232,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             const unsigned base = unsigned(max(0, sv[27] - 2047));
             for (int i = tid; i < 2048; i += kThreads) lh[i] = 0u;
             __syncthreads();
-            for (int i = tid; i < nloc; i += kThreads)
-                atomicAdd(lh + (max(score_key(score_at(i)) >> 16, base) - base), 1u);
+            for (int i = tid; i < nloc; i += kThreads) {
+                const unsigned bin = max(score_key(score_at(i)) >> 16, base) - base;
+                if (LCSW_INBOUNDS(bin < 2048u, 103)) atomicAdd(lh + bin, 1u);
+            }
             __syncthreads();
             if (warp == 0) {
                 // lane l holds bins [2048 - 64 (l + 1), 2048 - 64 l): lane 0 the top
@@ -1304,7 +1311,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             if ((key >> 16) >= tj) {
                 const unsigned long long e = key | ((unsigned long long)(g_lo + i) << 32);
                 if (pos < kSlot) st_relaxed_u64(slot + 1 + pos, e);
-                else st_relaxed_u64(cand_cur + seg + g_lo + pos - kSlot, e);
+                else if (LCSW_INBOUNDS(pos - kSlot < nloc, 105))
+                    st_relaxed_u64(cand_cur + seg + g_lo + pos - kSlot, e);
                 const int sp = (key >> 16) > tj ? atomicAdd(sv + 33, 1)
                                                 : n_above + atomicAdd(sv + 34, 1);
                 if (sp < kChunk / P) spec_g[sp] = g_lo + i;
@@ -1410,7 +1418,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     __syncthreads();
     const int n_cand = sv[6];
     const unsigned T = unsigned(sv[7]);
-    bool fast = !p.force_slow && n_cand <= kSelCap && n_cand >= k_b;
+    bool fast = !p.force_slow && n_cand <= SelLayout<DQK, DV>::cap && n_cand >= k_b;
     // With at least k candidates at or above T, the candidates hold the true
     // top k; a block then only needs the rank of each of its own candidates
     // (keys descending, groups ascending), i.e. the order of the packed
@@ -1419,6 +1427,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     const int own0 = offs[j], m_own = offs[j + 1] - offs[j];
     const bool rank_fmt = fast && k_b > 0 && m_own <= 32 && !(p.idx_out && j == 0);
     auto put_cand = [&](int o, unsigned key, unsigned g) {
+        if (!LCSW_INBOUNDS((o >= 0 && o < SelLayout<DQK, DV>::cap), 101)) return;
         if (rank_fmt) {
             crank[o] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - g);
         } else {
@@ -1517,23 +1526,25 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     // own candidate: every thread takes candidates tid, tid + 512, ... and
     // counts, for each own candidate, how many of them rank above it
     if (fast) {
-        constexpr int kEC = kSelCap / kThreads;
+        constexpr int kEC = kSelCap / kThreads;  // candidates a thread holds per pass
         int ns = 0;
         if (rank_fmt) {
-            unsigned long long mine[kEC];
+            for (int base = 0; base < n_cand; base += kSelCap) {  // one pass per kSelCap
+                unsigned long long mine[kEC];
 #pragma unroll
-            for (int u = 0; u < kEC; ++u) {
-                const int i = tid + u * kThreads;
-                mine[u] = i < n_cand ? crank[i] : 0ull;
-                ns += i < n_cand && unsigned(mine[u] >> 48) >= T;
-            }
-            for (int o = 0; o < m_own; ++o) {
-                const unsigned long long rl = crank[own0 + o];
-                int cnt = 0;
+                for (int u = 0; u < kEC; ++u) {
+                    const int i = base + tid + u * kThreads;
+                    mine[u] = i < n_cand ? crank[i] : 0ull;
+                    ns += i < n_cand && unsigned(mine[u] >> 48) >= T;
+                }
+                for (int o = 0; o < m_own; ++o) {
+                    const unsigned long long rl = crank[own0 + o];
+                    int cnt = 0;
 #pragma unroll
-                for (int u = 0; u < kEC; ++u) cnt += mine[u] > rl;
-                cnt = __reduce_add_sync(0xffffffffu, cnt);
-                if (lane == 0 && cnt) atomicAdd(rank + o, cnt);
+                    for (int u = 0; u < kEC; ++u) cnt += mine[u] > rl;
+                    cnt = __reduce_add_sync(0xffffffffu, cnt);
+                    if (lane == 0 && cnt) atomicAdd(rank + o, cnt);
+                }
             }
         } else {
             for (int i = tid; i < n_cand; i += kThreads) ns += (ckey[i] >> 16) >= T;
@@ -1554,7 +1565,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             const bool pick = lane < m_own && rank[lane] < k_b;
             const unsigned bsel = __ballot_sync(0xffffffffu, pick);
             const int grp = int(0xFFFFFFFFu - unsigned(rl));
-            if (pick) own[__popc(bsel & ((1u << lane) - 1u))] = grp;
+            if (pick && LCSW_INBOUNDS(__popc(bsel) <= 32, 102))
+                own[__popc(bsel & ((1u << lane) - 1u))] = grp;
             // the prefetch covers the block if it holds every selected group
             bool found = !pick;
             for (int s2 = 0; s2 < n_spec && !found; ++s2) found = spec_g[s2] == grp;
@@ -1647,7 +1659,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 const int eq_rank = eqr + __popc(beq & ((1u << lane) - 1u));
                 const bool pick = gt || (eq && unsigned(eq_rank) < take_eq);
                 const unsigned bsel = __ballot_sync(0xffffffffu, pick);
-                if (pick && np + __popc(bsel & ((1u << lane) - 1u)) < kMaxK)
+                if (pick && LCSW_INBOUNDS(np + __popc(bsel & ((1u << lane) - 1u)) < kMaxK, 102))
                     own[np + __popc(bsel & ((1u << lane) - 1u))] = cgrp[i];
                 np += __popc(bsel);
                 eqr += __popc(beq);
@@ -1949,7 +1961,8 @@ __global__ void __launch_bounds__(kThreads, 1) reuse_decode_kernel(const Params 
     const int j = cta - cb0;
     const int lo = int((long long)p.k * j / n_b), hi = int((long long)p.k * (j + 1) / n_b);
     const int n_own = hi - lo;
-    for (int i = tid; i < n_own; i += kThreads) own[i] = __ldg(p.idx_in + int64_t(b) * p.k + lo + i);
+    for (int i = tid; i < n_own; i += kThreads)
+        if (LCSW_INBOUNDS(i < kMaxK, 106)) own[i] = __ldg(p.idx_in + int64_t(b) * p.k + lo + i);
     __syncthreads();
     attend_groups<DQK, DV>(smem + kU, own, n_own, G_b, P, p.K + int64_t(b) * p.sK_b,
                            p.V + int64_t(b) * p.sV_b, p.q + int64_t(b) * p.H_q * DQK, p.H_q,

@@ -2,14 +2,37 @@
 // workspace carving and kernel sequencing.  No entry point allocates device
 // memory, synchronises the host (lcsw_get_status excepted) or lets a C++
 // exception escape.
+#include <nvtx3/nvToolsExt.h>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/lcsw.h"
 #include "fused.cuh"
 #include "kernels.cuh"
+
+// NVTX ranges around the C entry points (header-only NVTX 3: free when no
+// profiler is attached), so a timeline shows which library call issued which
+// kernels.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define LCSW_RANGE(name) NvtxRange lcsw_nvtx_range_(name)
+
+// Readers of the per-translation-unit check words of a -DLCSW_CHECKS=1 build
+// (registered by static initialisers in common.cuh; none in a normal build).
+namespace lcsw {
+static std::vector<int (*)()> &check_readers() {
+    static std::vector<int (*)()> readers;
+    return readers;
+}
+void register_check_reader(int (*reader)()) { check_readers().push_back(reader); }
+}  // namespace lcsw
 
 namespace {
 
@@ -115,6 +138,7 @@ lcsw_status lcsw_pool_keys(const lcsw_bf16 *k_idx, int64_t sk_b, const float *po
                            int64_t sw_b, const int32_t *seq_len, const int32_t *g_begin, int B,
                            int g_span, int d_idx, int P, lcsw_bf16 *k_pooled, int64_t sp_b,
                            lcsw_stream stream) {
+    LCSW_RANGE("lcsw_pool_keys");
     CHECK(B >= 0 && g_span >= 0, "B and g_span must be >= 0");
     CHECK(p_ok(P), "P must be 1, 2, 4 or 8 (got %d)", P);
     CHECK(d_idx > 0 && d_idx % 8 == 0, "d_idx must be a positive multiple of 8");
@@ -133,6 +157,7 @@ lcsw_status lcsw_pool_keys(const lcsw_bf16 *k_idx, int64_t sk_b, const float *po
 
 lcsw_status lcsw_visible_counts(const int32_t *seq_len, const int32_t *q_pos, int B, int T,
                                 int P, int32_t *n_valid, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_visible_counts");
     CHECK(B >= 0 && T >= 0 && p_ok(P), "bad B/T/P");
     if (int64_t(B) * T == 0) return LCSW_OK;
     CHECK(seq_len && n_valid, "null pointer argument");
@@ -145,6 +170,7 @@ lcsw_status lcsw_index_scores(const lcsw_bf16 *q_idx, const float *w_head,
                               const lcsw_bf16 *k_pooled, int64_t sp_b, const int32_t *seq_len,
                               const int32_t *q_pos, int B, int T, int H_i, int d_idx, int P,
                               int G_max, float *scores, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_index_scores");
     CHECK(B >= 0 && T >= 0 && G_max >= 0, "negative dimension");
     CHECK(d_idx == 64, "d_idx must be 64 (got %d)", d_idx);
     CHECK(H_i >= 1 && H_i <= 16, "H_i must be in [1, 16] (got %d)", H_i);
@@ -175,6 +201,7 @@ size_t lcsw_topk_workspace_size(int64_t rows, int G_max, int k) {
 lcsw_status lcsw_topk_groups(const float *scores, const int32_t *n_valid, int64_t rows,
                              int G_max, int k, int32_t *idx, void *ws, size_t ws_bytes,
                              lcsw_stream stream) {
+    LCSW_RANGE("lcsw_topk_groups");
     CHECK(rows >= 0 && G_max >= 0, "negative dimension");
     CHECK(k >= 1, "k must be >= 1 (got %d)", k);
     CHECK(rows <= 0x7FFFFFFF, "too many rows");
@@ -232,6 +259,7 @@ lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_
                              const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
                              int P, int k, float scale, lcsw_bf16 *out, float *lse, void *ws,
                              size_t ws_bytes, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_sparse_attn");
     const lcsw_status chk = check_attn(q, K, sK_b, V, sV_b, seq_len, idx, B, T, H_q, d_qk, d_v,
                                        P, k, out, lse);
     if (chk != LCSW_OK) return chk;
@@ -339,6 +367,7 @@ int lcsw_decode_launches(const lcsw_decode_args *a) {
 
 lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_bytes,
                               lcsw_stream stream) {
+    LCSW_RANGE("lcsw_decode_fused");
     lcsw_status s = check_decode(a);
     if (s != LCSW_OK || a->B == 0) return s;
     const size_t need = lcsw_decode_workspace_size(a);
@@ -376,6 +405,7 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
 lcsw_status lcsw_quantize_keys_e4m3(const lcsw_bf16 *k_pooled, int64_t sp_b, int B,
                                     int n_groups, uint8_t *kq, int64_t sq_b,
                                     lcsw_stream stream) {
+    LCSW_RANGE("lcsw_quantize_keys_e4m3");
     CHECK(B >= 0 && n_groups >= 0, "negative dimension");
     if (B == 0 || n_groups == 0) return LCSW_OK;
     CHECK(k_pooled && kq, "null pointer argument");
@@ -392,6 +422,7 @@ lcsw_status lcsw_quantize_keys_e4m3(const lcsw_bf16 *k_pooled, int64_t sp_b, int
 
 lcsw_status lcsw_decode_fused_e4m3(const lcsw_decode_args *a, uint8_t *kq, int64_t sq_b,
                                    void *ws, size_t ws_bytes, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_decode_fused_e4m3");
     CHECK(a, "null args");
     CHECK(a->B >= 0 && a->G_max >= 0, "negative dimension");
     CHECK(a->d_idx == 64, "d_idx must be 64");
@@ -432,6 +463,7 @@ lcsw_status lcsw_decode_fused_e4m3(const lcsw_decode_args *a, uint8_t *kq, int64
 
 lcsw_status lcsw_decode_reuse(const lcsw_decode_args *a, const int32_t *idx_in, void *ws,
                               size_t ws_bytes, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_decode_reuse");
     CHECK(a, "null args");
     CHECK(a->B >= 0, "negative dimension");
     CHECK(p_ok(a->P), "P must be 1, 2, 4 or 8");
@@ -533,6 +565,7 @@ constexpr int64_t kPrefillTcRows = 256;
 
 lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
                          lcsw_stream stream) {
+    LCSW_RANGE("lcsw_prefill");
     CHECK(a, "null args");
     CHECK(a->B >= 0 && a->T >= 0 && a->G_max >= 0, "negative dimension");
     CHECK(a->d_idx == 64, "d_idx must be 64");
@@ -640,6 +673,7 @@ lcsw_status lcsw_sparse_attn_mla(const lcsw_bf16 *q, const lcsw_bf16 *kv, int64_
                                  const int32_t *seq_len, const int32_t *idx, int B, int T,
                                  int H_q, int P, int k, float scale, lcsw_bf16 *out, float *lse,
                                  void *ws, size_t ws_bytes, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_sparse_attn_mla");
     CHECK(B >= 0 && T >= 0, "negative dimension");
     CHECK(H_q > 0 && H_q % 16 == 0, "H_q must be a positive multiple of 16");
     CHECK(p_ok(P), "P must be 1, 2, 4 or 8");
@@ -667,6 +701,7 @@ lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int
                                      const int32_t *idx, int B, int T, int H_q, int d_qk,
                                      int d_v, int P, int k, float scale, lcsw_bf16 *out,
                                      float *lse, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_sparse_attn_noalloc");
     // the argument checks of lcsw_sparse_attn first, then the scratch size:
     // neither needs the device, so a rejected call launches nothing
     const lcsw_status chk = check_attn(q, K, sK_b, V, sV_b, seq_len, idx, B, T, H_q, d_qk, d_v,
@@ -689,6 +724,7 @@ lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int
 lcsw_status lcsw_kda_step(const lcsw_bf16 *qkv, const lcsw_bf16 *conv_w, lcsw_bf16 *conv_state,
                           const float *g, const float *beta, float *state, lcsw_bf16 *out,
                           int B, int T, int H, int D, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_kda_step");
     CHECK(B >= 0 && T >= 0 && H >= 1 && D >= 1, "bad dimension");
     if (D != 128) return fail(LCSW_ERR_UNSUPPORTED, "KDA step: head width %d (only 128)", D);
     CHECK(B <= 65535, "B must be at most 65535");
@@ -702,7 +738,26 @@ lcsw_status lcsw_kda_step(const lcsw_bf16 *qkv, const lcsw_bf16 *conv_w, lcsw_bf
                        "KDA step launch");
 }
 
+int lcsw_checks_enabled(void) {
+#ifdef LCSW_CHECKS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int lcsw_check_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    int first = 0;
+    for (auto reader : lcsw::check_readers()) {
+        const int v = reader();
+        if (v && !first) first = v;
+    }
+    return first;
+}
+
 lcsw_status lcsw_get_status(void *ws, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_get_status");
     CHECK(ws && aligned(ws, 4), "null or misaligned workspace");
     cudaStream_t st = (cudaStream_t)stream;
     int word = 0;

@@ -67,7 +67,9 @@ __global__ void __launch_bounds__(256) pool_keys_kernel(
 #pragma unroll
             for (int j = 0; j < P; ++j) a[j] = __ldg(w_b + g * P + j);
             const uint4 o = pool_chunk_fast<P>(a, rows);
-            *reinterpret_cast<uint4 *>(dst_b + g * d_idx + c * 8) = o;
+            // (with one sequence the strides bound nothing)
+            if (LCSW_INBOUNDS(B == 1 || (g + 1) * d_idx <= sp_b, 301))
+                *reinterpret_cast<uint4 *>(dst_b + g * d_idx + c * 8) = o;
         }
     }
 }

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
         while (bits) {
             const int b = __ffs(bits) - 1;
             bits &= bits - 1u;
-            if (pos < k) out[pos] = w * 32 + b;
+            if (LCSW_INBOUNDS(pos < k, 401)) out[pos] = w * 32 + b;
             ++pos;
         }
     }

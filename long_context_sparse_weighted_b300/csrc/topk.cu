@@ -112,7 +112,7 @@ __device__ __noinline__ void topk_row(const float *__restrict__ scores,
 #pragma unroll
         for (int j = 0; j < kItems; ++j)
             if (sel[j]) {
-                if (pos < k) out[pos] = base + tid * kItems + j;
+                if (LCSW_INBOUNDS(pos < k, 201)) out[pos] = base + tid * kItems + j;
                 ++pos;
             }
         if (tid == 0) { running[0] = eq_seen + tot_eq; running[1] = written + tot_sel; }
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kWideFilterThreads) topk_wide_filter_kernel(
             be = __shfl_sync(0xffffffffu, be, 0);
             if (up) {
                 const unsigned pos = bu + __popc(mu & lt);
-                if (pos < unsigned(k)) abl[pos] = i;
+                if (LCSW_INBOUNDS(pos < unsigned(k), 202)) abl[pos] = i;
             }
             if (eq) {
                 const unsigned pos = be + __popc(me & lt);
@@ -290,12 +290,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_wide_final_kernel(
     const int32_t *abl = w.above + row * k;
     for (int i = tid; i < n_up; i += kTopkThreads) {
         const int g = __ldcg(abl + i);
-        atomicOr(sel + (g >> 5), 1u << (g & 31));
+        if (LCSW_INBOUNDS(g >= 0 && g < n, 204)) atomicOr(sel + (g >> 5), 1u << (g & 31));
     }
     for (int i = tid; i < m; i += kTopkThreads) {
         const unsigned long long e = __ldcg(cl + i);
         const unsigned key = unsigned(e >> 32);
         const int g = int(e & 0xFFFFFFFFu);
+        if (!LCSW_INBOUNDS(g >= 0 && g < n, 204)) continue;
         if (key > kth) atomicOr(sel + (g >> 5), 1u << (g & 31));
         else if (key == kth) atomicOr(eqm + (g >> 5), 1u << (g & 31));
     }
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_wide_final_kernel(
         while (v) {
             const int b = __ffs(v) - 1;
             v &= v - 1;
-            if (pos < k) out[pos] = i * 32 + b;
+            if (LCSW_INBOUNDS(pos < k, 203)) out[pos] = i * 32 + b;
             ++pos;
         }
     }

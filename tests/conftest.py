@@ -34,3 +34,17 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _device_bounds_checks():
+    """Under the bounds-checked library (LCSW_EXPECT_CHECKS=1, set by
+    test_gpu_checks.py for its child run) every test must leave the device
+    check words clean."""
+    yield
+    if os.environ.get("LCSW_EXPECT_CHECKS") == "1":
+        import long_context_sparse_weighted_b300 as lcsw
+        L = lcsw.lib()
+        assert L.lcsw_checks_enabled() == 1, "the bounds-checked library is not the one loaded"
+        code = L.lcsw_check_status()
+        assert code == 0, f"a device-side bounds check failed (code {code})"

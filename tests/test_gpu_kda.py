@@ -6,8 +6,12 @@ Tolerances, from the arithmetic (fp32 in the kernel, fp64 in the oracle):
                  t tokens: each token rounds the decay product and the rank-one
                  update once (2^-24 relative each) on top of column sums over
                  128 channels whose errors enter through beta * k
-  out (bf16)     |o_gpu - o_ref| <= 2^-8 |o_ref| + 1e-5 * max|o_ref| per head:
-                 one bf16 rounding (2^-9 relative) plus the fp32 column sums
+  out (bf16)     |o_gpu - o_ref| <= 2^-8 |o_ref| + 2^-16 M_j, with
+                 M_j = sum_i |q_i| |S'_ij| + |q.k| |beta (v_j - u_j)| the
+                 magnitude of the terms the kernel sums in fp32 for o_j: one
+                 bf16 rounding (2^-9 relative) plus fp32 sums over 128
+                 channels (at most about 130 * 2^-24 * M_j; 2^-16 leaves a
+                 factor of two)
 """
 import numpy as np
 import pytest
@@ -39,27 +43,42 @@ def _bf16_f64(bits):
     return synth.bf16_to_f32(bits).astype(np.float64)
 
 
-def _check(c, d, o, ref, T, heads=None):
-    o_ref, S_ref, cs_ref = ref
+def _check(c, d, o, ref, T):
+    o_ref, S_ref, cs_ref, M = ref
     got_o = _bf16_f64(host_bits(o))
     got_S = d["state"].cpu().numpy().astype(np.float64)
     got_cs = host_bits(d["conv_state"])
-    if heads is not None:
-        got_o, got_S = got_o[heads[0]], got_S[heads[0]]
-        got_cs = got_cs[heads[0]]
     assert np.array_equal(got_cs, cs_ref), "conv history differs"
     smax = np.abs(S_ref).max(axis=(-2, -1), keepdims=True)
     serr = np.abs(got_S - S_ref) / np.maximum(smax, 1e-30)
     assert serr.max() <= 2e-6 * (1 + T), f"state error {serr.max():.3g} x head max"
-    omax = np.abs(o_ref).max(axis=-1, keepdims=True)
-    bound = 2.0 ** -8 * np.abs(o_ref) + 1e-5 * omax
-    bad = np.abs(got_o - o_ref) > bound
-    assert not bad.any(), f"{bad.sum()} outputs off, worst {np.abs(got_o - o_ref).max():.3g}"
+    bound = 2.0 ** -8 * np.abs(o_ref) + 2.0 ** -16 * M
+    ratio = np.abs(got_o - o_ref) / np.maximum(bound, 1e-300)
+    assert ratio.max() <= 1.0, f"{(ratio > 1).sum()} outputs off, worst at {ratio.max():.3g} x bound"
+    return ratio.max()
 
 
 def _oracle(c):
-    return okda.kda_step(c["qkv"], c["conv_w"], c["conv_state"], c["g"], c["beta"], c["state"],
-                         c["H"], c["D"])
+    """The oracle token by token, with the magnitude M of the terms summed for
+    each output (the bound's second part)."""
+    B, T, H, D = c["qkv"].shape[0], c["qkv"].shape[1], c["H"], c["D"]
+    S = np.array(c["state"], dtype=np.float64)
+    cs = c["conv_state"]
+    o = np.zeros((B, T, H, D))
+    M = np.zeros((B, T, H, D))
+    for t in range(T):
+        o_t, S_new, cs, parts = okda.kda_step(c["qkv"][:, t:t + 1], c["conv_w"], cs,
+                                              c["g"][:, t:t + 1], c["beta"][:, t:t + 1], S, H, D,
+                                              return_parts=True)
+        q, k, v = parts[:, 0, 0], parts[:, 0, 1], parts[:, 0, 2]
+        Sp = np.exp(np.asarray(c["g"][:, t], np.float64))[..., None] * S
+        u = np.einsum("bhi,bhij->bhj", k, Sp)
+        dw = np.asarray(c["beta"][:, t], np.float64)[..., None] * (v - u)
+        qk = np.abs((q * k).sum(-1))[..., None]
+        M[:, t] = np.einsum("bhi,bhij->bhj", np.abs(q), np.abs(Sp)) + qk * np.abs(dw)
+        o[:, t] = o_t[:, 0]
+        S = S_new
+    return o, S, cs, M
 
 
 @pytest.mark.parametrize("B,T,H", [(3, 1, 4), (2, 5, 3), (1, 2, 64)])
@@ -128,11 +147,10 @@ def test_full_size_decode_step_sampled():
     for b in (0, spec.B - 1):
         sub = {k: (v[b:b + 1] if isinstance(v, np.ndarray) and k != "conv_w" else v)
                for k, v in c.items()}
-        ref = _oracle(sub)
+        o_ref, S_ref, cs_ref, M = _oracle(sub)
         got_o = _bf16_f64(host_bits(o[b:b + 1]))
         got_S = d["state"][b:b + 1].cpu().numpy().astype(np.float64)
-        assert np.array_equal(host_bits(d["conv_state"][b:b + 1]), ref[2])
-        smax = np.abs(ref[1]).max(axis=(-2, -1), keepdims=True)
-        assert (np.abs(got_S - ref[1]) / smax).max() <= 4e-6
-        omax = np.abs(ref[0]).max(axis=-1, keepdims=True)
-        assert (np.abs(got_o - ref[0]) <= 2.0 ** -8 * np.abs(ref[0]) + 1e-5 * omax).all()
+        assert np.array_equal(host_bits(d["conv_state"][b:b + 1]), cs_ref)
+        smax = np.abs(S_ref).max(axis=(-2, -1), keepdims=True)
+        assert (np.abs(got_S - S_ref) / smax).max() <= 4e-6
+        assert (np.abs(got_o - o_ref) <= 2.0 ** -8 * np.abs(o_ref) + 2.0 ** -16 * M).all()
