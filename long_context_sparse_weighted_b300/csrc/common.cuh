@@ -142,9 +142,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
 // translation unit's check word (the first failure wins) and the access is
 // skipped -- no trap.  lcsw_check_status() collects and clears the words.  In
 // the normal build LCSW_INBOUNDS(cond, code) is the constant true.
-namespace lcsw {
-void register_check_reader(int (*reader)());
-}
+void register_check_reader(int (*reader)());  // lcsw_api.cu
 #ifdef LCSW_CHECKS
 namespace {
 __device__ int g_lcsw_check_word;
@@ -158,7 +156,7 @@ int lcsw_read_check_word() {
     return v;
 }
 struct CheckReaderRegistration {
-    CheckReaderRegistration() { lcsw::register_check_reader(&lcsw_read_check_word); }
+    CheckReaderRegistration() { register_check_reader(&lcsw_read_check_word); }
 };
 const CheckReaderRegistration g_lcsw_check_registration;
 __device__ __forceinline__ bool lcsw_inbounds(bool ok, int code) {

@@ -117,7 +117,8 @@ constexpr int kSelList = kMisc + 4096;                // own selected groups [kM
 constexpr int kNewRows = kSelList + kMaxK * 4;        // newest group: [8][64] bf16, [8] f32
 constexpr int kNewCode = kNewRows + 8 * 128 + 8 * 4;  // its FP8 row: [64] codes, scale
 constexpr int kRingBars = kNewCode + 64 + 16;         // [kWarps][ring depth] mbarriers
-constexpr int kSmemBytes = kRingBars + kWarps * kRingMax * 8;
+constexpr int kQCode = (kRingBars + kWarps * kRingMax * 8 + 15) / 16 * 16;  // FP8 query: [16][64] codes, [16] scales
+constexpr int kSmemBytes = kQCode + 16 * 64 + 16 * 4;
 static_assert(kRingBars % 8 == 0, "mbarrier alignment");
 
 // Attention operands: Q [64 heads][QP], NBUF chunk buffers (each K [64
@@ -655,6 +656,103 @@ __device__ __forceinline__ void attend_groups(unsigned char *u, const int32_t *o
     }
 }
 
+// Blocks per sequence for per-sequence costs w[0..B) (shared memory, B <= 96):
+// n_b = max(1, ceil(w_b / L)) for the smallest L with sum_b n_b <= ncta (warp
+// 0 bisects on L; L0 = ceil(sum_b w_b / (ncta - B)) always fits, since each
+// ceiling adds less than one block), the blocks left over go to the sequence
+// with the largest cost per block.  This minimises the largest per-block cost
+// (proportional shares rounded down can leave a short sequence with almost
+// two blocks' work on one).  Writes cta_begin[0..B] (prefix sums, shared);
+// every thread of the block calls it.
+__device__ __noinline__ void assign_blocks(const int *w, int B, int ncta, int *cta_begin) {
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
+        unsigned wl[3];
+        bool on[3];
+        unsigned tot = 0;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int bb = 3 * lane + i;
+            on[i] = bb < B;
+            wl[i] = on[i] ? unsigned(max(0, w[bb])) : 0u;
+            tot += wl[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        auto blocks = [&](unsigned L) {  // sum over the warp of max(1, ceil(w / L))
+            int c = 0;
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+                if (on[i]) c += wl[i] > 0 ? int((wl[i] + L - 1) / L) : 1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            return c;
+        };
+        // L >= tot / ncta is necessary, L = ceil(tot / (ncta - B)) sufficient;
+        // bisect to within 1/256 of the smallest feasible L
+        unsigned lo = max(1u, tot / unsigned(ncta)), hi = max(1u, (tot + (ncta - B) - 1) / (ncta - B));
+        while (hi - lo > max(1u, hi >> 8)) {  // warp-uniform
+            const unsigned mid = lo + (hi - lo) / 2;
+            if (blocks(mid) <= ncta) hi = mid;
+            else lo = mid;
+        }
+        int n[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) n[i] = on[i] ? (wl[i] > 0 ? int((wl[i] + hi - 1) / hi) : 1) : 0;
+        int left = n[0] + n[1] + n[2];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) left += __shfl_xor_sync(0xffffffffu, left, o);
+        left = ncta - left;
+        if (left > 0) {
+            // the sequence with the largest w / n (cross-multiplied; lowest index on ties)
+            unsigned bw = 0, bn = 1;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+                if (on[i] && (bi == 0x7fffffff ||
+                              (unsigned long long)wl[i] * bn > (unsigned long long)bw * n[i])) {
+                    bw = wl[i];
+                    bn = unsigned(n[i]);
+                    bi = 3 * lane + i;
+                }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned ow = __shfl_xor_sync(0xffffffffu, bw, o);
+                const unsigned on_ = __shfl_xor_sync(0xffffffffu, bn, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (oi == 0x7fffffff) continue;
+                const unsigned long long a = (unsigned long long)ow * bn,
+                                         c = (unsigned long long)bw * on_;
+                if (bi == 0x7fffffff || a > c || (a == c && oi < bi)) {
+                    bw = ow;
+                    bn = on_;
+                    bi = oi;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+                if (3 * lane + i == bi) n[i] += left;
+        }
+        // prefix sums: lane holds sequences 3 lane .. 3 lane + 2
+        const int mine = n[0] + n[1] + n[2];
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int at = incl - mine;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int bb = 3 * lane + i;
+            if (bb < B) cta_begin[bb] = at;
+            at += n[i];
+        }
+        if (lane == 31) cta_begin[B] = incl;  // = ncta
+    }
+    __syncthreads();
+}
+
 // Merge of the partial states of one sequence's blocks, head by head: block j
 // of the n_b blocks cb0.. of sequence b merges heads j, j + n_b, ...: it polls
 // the partial words of every block of the sequence until all are written,
@@ -880,50 +978,61 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     float wv[NT][2];
     // The indexer query of sequence bb: raw bf16 loads first (fetch_query),
     // then its fragments (prep_query).  bf16: head nt*8 + r as mma.sync B
-    // fragments, k-permuted like the keys.  FP8: dims [16c, 16c + 16) of the
-    // head quantized under the head's scale (the four lanes c of a head share
-    // its amax), as f16 pairs of the codes; k-step s takes the codes of dims
-    // 16c + 4s .. 16c + 4s + 3.
+    // fragments, k-permuted like the keys.  FP8: warp w quantizes head w
+    // once for the block (two dims a lane, the head's amax by shuffles) into
+    // shared memory, and every warp then takes as f16 pairs the codes of
+    // dims 16c + 4s .. 16c + 4s + 3 for k-step s.
     uint4 qraw[NT][2];
+    uint32_t qpair = 0u;  // FP8: dims 2 lane, 2 lane + 1 of head `warp`
+    uint8_t *qcode = smem + kQCode;
+    float *qscale = reinterpret_cast<float *>(smem + kQCode + 16 * 64);
     auto fetch_query = [&](int bb) {
+        if constexpr (F8) {
+            if (warp < p.H_i)
+                qpair = __ldg(reinterpret_cast<const uint32_t *>(
+                    p.q_idx + (int64_t(bb) * p.H_i + warp) * 64 + 2 * lane));
+        } else {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int head = nt * 8 + r;
-            qraw[nt][0] = qraw[nt][1] = make_uint4(0, 0, 0, 0);
-            if (head < p.H_i) {
-                const uint16_t *qp = p.q_idx + (int64_t(bb) * p.H_i + head) * 64;
-                qraw[nt][0] = ld_nc16(qp + (F8 ? 16 * c : 8 * c));
-                qraw[nt][1] = ld_nc16(qp + (F8 ? 16 * c + 8 : 32 + 8 * c));
+            for (int nt = 0; nt < NT; ++nt) {
+                const int head = nt * 8 + r;
+                qraw[nt][0] = qraw[nt][1] = make_uint4(0, 0, 0, 0);
+                if (head < p.H_i) {
+                    const uint16_t *qp = p.q_idx + (int64_t(bb) * p.H_i + head) * 64;
+                    qraw[nt][0] = ld_nc16(qp + 8 * c);
+                    qraw[nt][1] = ld_nc16(qp + 32 + 8 * c);
+                }
             }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int h = nt * 8 + 2 * c + e;
                 wv[nt][e] = h < p.H_i ? __ldg(p.w_head + int64_t(bb) * p.H_i + h) : 0.f;
             }
-        }
     };
     auto prep_query = [&]() {
+        if constexpr (F8) {
+            if (warp < NT * 8) {  // warp-uniform
+                const float x0 = bf_lo(qpair), x1 = bf_hi(qpair);
+                float amax = fmaxf(fabsf(x0), fabsf(x1));
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint4 h0 = qraw[nt][0], h1 = qraw[nt][1];
-            if constexpr (F8) {
-                const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    amax = fmaxf(amax, fmaxf(fabsf(bf_lo(hw[i])), fabsf(bf_hi(hw[i]))));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
                 const float sc = e4m3_row_scale(amax);
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
+                uint32_t cw = 0u;
                 if (sc != 0.f) {
                     const float inv = __frcp_rn(sc);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float x = (i & 1) ? bf_hi(hw[i / 2]) : bf_lo(hw[i / 2]);
-                        w[i / 4] |= e4m3_quantize(x, sc, inv) << (8 * (i % 4));
-                    }
+                    cw = e4m3_quantize(x0, sc, inv) | (e4m3_quantize(x1, sc, inv) << 8);
                 }
+                *reinterpret_cast<uint16_t *>(qcode + warp * 64 + 2 * lane) = uint16_t(cw);
+                if (lane == 0) qscale[warp] = sc;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int head = nt * 8 + r;
+                const uint4 w4 = *reinterpret_cast<const uint4 *>(qcode + head * 64 + 16 * c);
+                const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                 for (int s2 = 0; s2 < 4; ++s2) {
                     bq[nt][s2][0] = e4m3x2_f16x2(w[s2]);
@@ -931,8 +1040,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 }
                 // the accumulator's heads nt*8 + 2c + e take that head's query scale
 #pragma unroll
-                for (int e = 0; e < 2; ++e) wv[nt][e] *= __shfl_sync(0xffffffffu, sc, (2 * c + e) * 4);
-            } else {
+                for (int e = 0; e < 2; ++e) wv[nt][e] *= qscale[nt * 8 + 2 * c + e];
+            }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint4 h0 = qraw[nt][0], h1 = qraw[nt][1];
                 bq[nt][0][0] = h0.x; bq[nt][0][1] = h0.y;
                 bq[nt][1][0] = h0.z; bq[nt][1][1] = h0.w;
                 bq[nt][2][0] = h1.x; bq[nt][2][1] = h1.y;
@@ -980,16 +1093,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             G = G < 0 ? 0 : (G > p.G_max ? p.G_max : G);
             wv = 2 * G + min(p.k, G) * P * ((DQK + DV) / 32);
         }
-        // one block per sequence, the rest in proportion to cost
-        int total;
-        const int pre = block_exclusive_scan(wv, scratch, &total);
-        if (tid < B) offs[tid] = pre;
-        if (tid == 0) offs[B] = total;
+        if (tid < B) offs[tid] = wv;
         __syncthreads();
-        const double tot = total > 0 ? double(total) : 1.0;
-        for (int bb = tid; bb <= B; bb += kThreads)
-            cta_begin[bb] = bb == B ? ncta : bb + int(double(ncta - B) * double(offs[bb]) / tot);
-        __syncthreads();
+        assign_blocks(offs, B, ncta, cta_begin);
         for (int bb = tid; bb < B; bb += kThreads)
             if (cta_begin[bb] <= cta && cta < cta_begin[bb + 1]) sv[1] = bb;
         __syncthreads();
@@ -1934,21 +2040,13 @@ __global__ void __launch_bounds__(kThreads, 1) reuse_decode_kernel(const Params 
         n_b = ncta;
         G_b = __ldg(p.seq_len) / P;
     } else {
-        int wv = 0;
         if (tid < B) {
             const int L = __ldg(p.seq_len + tid);
             lens[tid] = L;
-            wv = min(p.k, max(0, L / P)) + 1;
+            offs[tid] = min(p.k, max(0, L / P)) + 1;
         }
-        int total;
-        const int pre = block_exclusive_scan(wv, scratch, &total);
-        if (tid < B) offs[tid] = pre;
-        if (tid == 0) offs[B] = total;
         __syncthreads();
-        const double tot = total > 0 ? double(total) : 1.0;
-        for (int bb = tid; bb <= B; bb += kThreads)
-            cta_begin[bb] = bb == B ? ncta : bb + int(double(ncta - B) * double(offs[bb]) / tot);
-        __syncthreads();
+        assign_blocks(offs, B, ncta, cta_begin);
         for (int bb = tid; bb < B; bb += kThreads)
             if (cta_begin[bb] <= cta && cta < cta_begin[bb + 1]) sv[1] = bb;
         __syncthreads();
