@@ -111,7 +111,9 @@ static_assert(kWarps * kRing * kTileBytes <= kUBytes, "stream rings overflow reg
 static_assert(kWarps * kRingF8 * (16 * 64 + 16 * 4) <= kUBytes, "FP8 rings overflow region U");
 constexpr int kScores = kU + kUBytes;                 // [kChunkCap] floats
 constexpr int kMisc = kScores + kChunkCap * 4;        // small arrays and scalars
-constexpr int kMiscBytes = 128 + (3 * (kMaxCtas + 1) + 64 + 40 + 64 + kChunk + 32) * 4;
+constexpr int kRankDirect = 32;    // own candidates ranked directly (else the K* path)
+constexpr int kRankMax = 96;       // capacity of the rank counters (up to three warp rounds)
+constexpr int kMiscBytes = 128 + (3 * (kMaxCtas + 1) + 64 + 40 + 64 + kChunk + kRankMax) * 4;
 static_assert(kMiscBytes <= 4096, "small arrays overflow their region");
 constexpr int kSelList = kMisc + 4096;                // own selected groups [kMaxK]
 constexpr int kNewRows = kSelList + kMaxK * 4;        // newest group: [8][64] bf16, [8] f32
@@ -688,9 +690,20 @@ __device__ __noinline__ void assign_blocks(const int *w, int B, int ncta, int *c
             for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
             return c;
         };
+        // equal costs (a uniform batch): an even split is optimal, no search
+        unsigned wmin = 0xFFFFFFFFu, wmax = 0u;
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (on[i]) {
+                wmin = min(wmin, wl[i]);
+                wmax = max(wmax, wl[i]);
+            }
+        wmin = __reduce_min_sync(0xffffffffu, wmin);
+        wmax = __reduce_max_sync(0xffffffffu, wmax);
         // L >= tot / ncta is necessary, L = ceil(tot / (ncta - B)) sufficient;
         // bisect to within 1/256 of the smallest feasible L
         unsigned lo = max(1u, tot / unsigned(ncta)), hi = max(1u, (tot + (ncta - B) - 1) / (ncta - B));
+        if (wmin == wmax) lo = hi;  // skips the search; the split below is then made even
         while (hi - lo > max(1u, hi >> 8)) {  // warp-uniform
             const unsigned mid = lo + (hi - lo) / 2;
             if (blocks(mid) <= ncta) hi = mid;
@@ -698,7 +711,13 @@ __device__ __noinline__ void assign_blocks(const int *w, int B, int ncta, int *c
         }
         int n[3];
 #pragma unroll
-        for (int i = 0; i < 3; ++i) n[i] = on[i] ? (wl[i] > 0 ? int((wl[i] + hi - 1) / hi) : 1) : 0;
+        for (int i = 0; i < 3; ++i) {
+            const int bb = 3 * lane + i;
+            if (wmin == wmax)  // floor(ncta / B) each, one more for the first ncta % B
+                n[i] = on[i] ? ncta / B + (bb < ncta % B ? 1 : 0) : 0;
+            else
+                n[i] = on[i] ? (wl[i] > 0 ? int((wl[i] + hi - 1) / hi) : 1) : 0;
+        }
         int left = n[0] + n[1] + n[2];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) left += __shfl_xor_sync(0xffffffffu, left, o);
@@ -924,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     int *scratch = sv + 64;                                                   // [40]
     float *sred = reinterpret_cast<float *>(scratch + 40);                    // [64]
     int *spec_g = reinterpret_cast<int *>(sred + 64);                         // [kChunk]
-    int *rank = spec_g + kChunk;                                              // [32]
+    int *rank = spec_g + kChunk;                                              // [kRankMax]
     int32_t *sel = reinterpret_cast<int32_t *>(smem + kSelList);              // [kMaxK]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1470,7 +1489,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             }
             hdrs[tid] = h;
         }
-        if (tid < 32) rank[tid] = 0;
+        if (tid < kRankMax) rank[tid] = 0;
         if (__syncthreads_or(!ok)) {
             if (tid == 0) raise_timeout(p, 2);
             cp_async_wait<0>();
@@ -1531,7 +1550,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     // value (key << 32) | ~group.  The k-th key K* is computed only for the
     // optional full index output or past 32 own candidates.
     const int own0 = offs[j], m_own = offs[j + 1] - offs[j];
-    const bool rank_fmt = fast && k_b > 0 && m_own <= 32 && !(p.idx_out && j == 0);
+    // (past 32 own candidates the K* path is cheaper: decode_b8, about 66 own
+    // candidates a block, ran 8.6 us slower when ranking them all)
+    const bool rank_fmt = fast && k_b > 0 && m_own <= kRankDirect && !(p.idx_out && j == 0);
     auto put_cand = [&](int o, unsigned key, unsigned g) {
         if (!LCSW_INBOUNDS((o >= 0 && o < SelLayout<DQK, DV>::cap), 101)) return;
         if (rank_fmt) {
@@ -1645,6 +1666,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 }
                 for (int o = 0; o < m_own; ++o) {
                     const unsigned long long rl = crank[own0 + o];
+                    // below T a candidate is not selected (when the survivors
+                    // are at least k) and outranks no survivor: skip it
+                    if (unsigned(rl >> 48) < T) continue;  // warp-uniform
                     int cnt = 0;
 #pragma unroll
                     for (int u = 0; u < kEC; ++u) cnt += mine[u] > rl;
@@ -1667,18 +1691,25 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     bool use_spec = false;
     if (by_rank) {
         if (warp == 0) {
-            const unsigned long long rl = lane < m_own ? crank[own0 + lane] : ~0ull;
-            const bool pick = lane < m_own && rank[lane] < k_b;
-            const unsigned bsel = __ballot_sync(0xffffffffu, pick);
-            const int grp = int(0xFFFFFFFFu - unsigned(rl));
-            if (pick && LCSW_INBOUNDS(__popc(bsel) <= 32, 102))
-                own[__popc(bsel & ((1u << lane) - 1u))] = grp;
-            // the prefetch covers the block if it holds every selected group
-            bool found = !pick;
-            for (int s2 = 0; s2 < n_spec && !found; ++s2) found = spec_g[s2] == grp;
-            const bool cover = __all_sync(0xffffffffu, found);
+            // own candidates in rounds of 32, in slot (= ascending group) order
+            int np = 0;
+            bool cover = true;
+            for (int r0 = 0; r0 < m_own; r0 += 32) {
+                const int o = r0 + lane;
+                const unsigned long long rl = o < m_own ? crank[own0 + o] : ~0ull;
+                const bool pick = o < m_own && unsigned(rl >> 48) >= T && rank[o] < k_b;
+                const unsigned bsel = __ballot_sync(0xffffffffu, pick);
+                const int grp = int(0xFFFFFFFFu - unsigned(rl));
+                if (pick && LCSW_INBOUNDS(np + __popc(bsel) <= kRankMax, 102))
+                    own[np + __popc(bsel & ((1u << lane) - 1u))] = grp;
+                np += __popc(bsel);
+                // the prefetch covers the block if it holds every selected group
+                bool found = !pick;
+                for (int s2 = 0; s2 < n_spec && !found; ++s2) found = spec_g[s2] == grp;
+                cover = __all_sync(0xffffffffu, found) && cover;
+            }
             if (lane == 0) {
-                sv[16] = __popc(bsel);
+                sv[16] = np;
                 sv[18] = cover ? 1 : 0;
             }
         }
