@@ -44,6 +44,9 @@ def _declare(lib):
     lib.oracle_quantize_rows_e4m3.argtypes = [P, I64, I32, P, P]
     lib.oracle_index_scores_e4m3.argtypes = [P, P, P, P, P, I64, P, P, I32, I32, I32, I32, I32,
                                              I64, P]
+    lib.oracle_sparse_attn_e4m3kv.argtypes = [P, P, I64, P, I64, P, I64, P, I64, P, P, I32, I32,
+                                              I32, I32, I32, I32, I32, D, P, P]
+    lib.oracle_sparse_attn_e4m3kv.restype = None
     lib.oracle_pool_keys.argtypes = [P, I64, P, I64, P, I32, I32, I32, P, I64]
     lib.oracle_visible_counts.argtypes = [P, P, I32, I32, I32, P]
     lib.oracle_index_scores.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, I32, I64, P]
@@ -168,6 +171,26 @@ def quantize_rows_e4m3(x):
     scale = np.empty(x.shape[:-1], np.float32)
     _load().oracle_quantize_rows_e4m3(_p(x), rows, d, _p(code), _p(scale))
     return code, scale
+
+
+def sparse_attn_e4m3kv(q, kc, ks, vc, vs, seq_len, idx, P, scale):
+    """Attention over an FP8 K/V cache: element = e4m3(code) * the token row's
+    scale.  kc [B][L][d_qk], vc [B][L][d_v] uint8 codes; ks, vs [B][L] fp32."""
+    q = _c(q, np.uint16)
+    kc, vc = _c(kc, np.uint8), _c(vc, np.uint8)
+    ks, vs = _c(ks, np.float32), _c(vs, np.float32)
+    seq_len = _c(seq_len, np.int32)
+    idx = _c(idx, np.int32)
+    B, T, H_q, d_qk = q.shape
+    d_v = vc.shape[2]
+    k = idx.shape[-1]
+    out = np.empty((B, T, H_q, d_v), np.uint16)
+    lse = np.empty((B, T, H_q), np.float32)
+    _load().oracle_sparse_attn_e4m3kv(_p(q), _p(kc), kc.shape[1] * d_qk, _p(ks), ks.shape[1],
+                                      _p(vc), vc.shape[1] * d_v, _p(vs), vs.shape[1],
+                                      _p(seq_len), _p(idx), B, T, H_q, d_qk, d_v, P, k,
+                                      float(scale), _p(out), _p(lse))
+    return out, lse
 
 
 def index_scores_e4m3(cq, sq, w_head, ck, sk, seq_len, P, q_pos=None):

@@ -528,3 +528,83 @@ void oracle_index_scores_e4m3(const uint8_t *cq, const float *sq, const float *w
         }
     }
 }
+
+/* -------------------------------------------------- FP8 (E4M3) K/V cache --- */
+
+/* Attention as oracle_sparse_attn, over a K/V cache held as E4M3 codes with one
+ * fp32 scale per token row (the same format as the FP8 pooled keys: scale =
+ * amax / 448, see oracle_quantize_rows_e4m3).  The serving stack of the
+ * reading notes quantizes caches per tier to INT8, FP8 or BF16 ("The serving
+ * stack"); the element value is e4m3(code) * scale, exact in double:
+ *
+ *   z_j = scale_softmax * sum_i q_i * e4m3(kc[j][i]) * ks[j]
+ *   out = sum_j softmax_j(z) * e4m3(vc[j][:]) * vs[j]
+ *
+ * kc [B][*][d_qk] and vc [B][*][d_v] codes with batch strides skc_b, svc_b
+ * elements; ks, vs [B][*] with batch strides sks_b, svs_b. */
+void oracle_sparse_attn_e4m3kv(const uint16_t *q, const uint8_t *kc, int64_t skc_b,
+                               const float *ks, int64_t sks_b, const uint8_t *vc, int64_t svc_b,
+                               const float *vs, int64_t svs_b, const int32_t *seq_len,
+                               const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
+                               int P, int k, double scale, uint16_t *out, float *lse)
+{
+    int64_t max_tok = (int64_t)k * P;
+    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_tok > 0 ? max_tok : 1));
+    double *z = (double *)malloc(sizeof(double) * (size_t)(max_tok > 0 ? max_tok : 1));
+    double *o = (double *)malloc(sizeof(double) * (size_t)d_v);
+    for (int b = 0; b < B; ++b) {
+        const int64_t G = seq_len[b] / P;
+        for (int t = 0; t < T; ++t) {
+            const int32_t *sel = idx + ((int64_t)b * T + t) * k;
+            int64_t n = 0;
+            for (int j = 0; j < k; ++j) {
+                const int64_t g = sel[j];
+                if (g < 0 || g >= G)
+                    continue;
+                for (int i = 0; i < P; ++i)
+                    tok[n++] = P * g + i;
+            }
+            for (int h = 0; h < H_q; ++h) {
+                const uint16_t *qh = q + (((int64_t)b * T + t) * H_q + h) * d_qk;
+                uint16_t *oh = out + (((int64_t)b * T + t) * H_q + h) * d_v;
+                float *lh = lse ? lse + ((int64_t)b * T + t) * H_q + h : NULL;
+                if (n == 0) {
+                    for (int i = 0; i < d_v; ++i)
+                        oh[i] = 0;
+                    if (lh)
+                        *lh = -INFINITY;
+                    continue;
+                }
+                double m = -INFINITY;
+                for (int64_t j = 0; j < n; ++j) {
+                    const uint8_t *kj = kc + b * skc_b + tok[j] * d_qk;
+                    const double sk = (double)ks[b * sks_b + tok[j]];
+                    double dot = 0.0;
+                    for (int i = 0; i < d_qk; ++i)
+                        dot += bf16_value(qh[i]) * (oracle_e4m3_value(kj[i]) * sk);
+                    z[j] = scale * dot;
+                    if (z[j] > m)
+                        m = z[j];
+                }
+                double l = 0.0;
+                for (int i = 0; i < d_v; ++i)
+                    o[i] = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    const double p = exp(z[j] - m);
+                    l += p;
+                    const uint8_t *vj = vc + b * svc_b + tok[j] * d_v;
+                    const double sv = (double)vs[b * svs_b + tok[j]];
+                    for (int i = 0; i < d_v; ++i)
+                        o[i] += p * (oracle_e4m3_value(vj[i]) * sv);
+                }
+                for (int i = 0; i < d_v; ++i)
+                    oh[i] = oracle_bf16_from_double(o[i] / l);
+                if (lh)
+                    *lh = (float)(m + log(l));
+            }
+        }
+    }
+    free(o);
+    free(z);
+    free(tok);
+}

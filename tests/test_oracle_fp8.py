@@ -111,3 +111,75 @@ def test_fp8_score_follows_the_key_scale():
     assert np.array_equal(ck2, ck) and np.array_equal(sk2, sk / 64)
     got = oracle.index_scores_e4m3(cq, sq, w, ck2, sk2, seq, P)
     assert np.array_equal(got, (base.astype(np.float64) / 64).astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# attention over an FP8 K/V cache (element = e4m3(code) * row scale)
+# ---------------------------------------------------------------------------
+
+def _kv8_case(seed, B=2, L=96, H_q=4, d_qk=16, d_v=8, k=10, P=4, pow2_scales=True):
+    rng = np.random.default_rng(seed)
+    kc = rng.integers(0, 0x7F, (B, L, d_qk)).astype(np.uint8) | (
+        rng.integers(0, 2, (B, L, d_qk)).astype(np.uint8) << 7)
+    vc = rng.integers(0, 0x7F, (B, L, d_v)).astype(np.uint8) | (
+        rng.integers(0, 2, (B, L, d_v)).astype(np.uint8) << 7)
+    if pow2_scales:
+        ks = (2.0 ** rng.integers(-12, -6, (B, L))).astype(np.float32)
+        vs = (2.0 ** rng.integers(-10, -4, (B, L))).astype(np.float32)
+    else:
+        ks = rng.uniform(0.001, 0.02, (B, L)).astype(np.float32)
+        vs = rng.uniform(0.001, 0.02, (B, L)).astype(np.float32)
+    q = synth.bf16_bits(rng.standard_normal((B, 1, H_q, d_qk)).astype(np.float32))
+    seq = np.array([L, L - 13], np.int32)[:B]
+    idx = np.full((B, 1, k), -1, np.int32)
+    for b in range(B):
+        G = int(seq[b]) // P
+        idx[b, 0, :k - 2] = np.sort(rng.choice(G, k - 2, replace=False))
+    return q, kc, ks, vc, vs, seq, idx
+
+
+def _decode(codes, scales):
+    vals = np.array([oracle.e4m3_value(c) for c in range(256)])
+    return vals[codes] * scales[..., None].astype(np.float64)
+
+
+def test_kv8_power_of_two_scales_equal_the_bf16_oracle():
+    """With power-of-two scales every dequantized element is a bf16 value, so
+    the FP8 attention must equal the bf16 oracle's bit for bit."""
+    q, kc, ks, vc, vs, seq, idx = _kv8_case(400)
+    Kf, Vf = _decode(kc, ks), _decode(vc, vs)
+    Kb, Vb = synth.bf16_bits(Kf.astype(np.float32)), synth.bf16_bits(Vf.astype(np.float32))
+    assert np.array_equal(synth.bf16_to_f32(Kb).astype(np.float64), Kf)
+    assert np.array_equal(synth.bf16_to_f32(Vb).astype(np.float64), Vf)
+    o8, l8 = oracle.sparse_attn_e4m3kv(q, kc, ks, vc, vs, seq, idx, 4, 0.25)
+    ob, lb = oracle.sparse_attn(q, Kb, Vb, seq, idx, 4, 0.25)
+    assert np.array_equal(o8, ob)
+    assert np.array_equal(l8, lb)
+
+
+def test_kv8_brute_force_softmax():
+    """Arbitrary scales: a numpy softmax (scipy logsumexp) over the decoded
+    rows of the selected tokens, rounded to bf16 the same way."""
+    from scipy.special import logsumexp
+    q, kc, ks, vc, vs, seq, idx = _kv8_case(401, pow2_scales=False)
+    o8, l8 = oracle.sparse_attn_e4m3kv(q, kc, ks, vc, vs, seq, idx, 4, 0.3)
+    Kf, Vf = _decode(kc, ks), _decode(vc, vs)
+    qf = synth.bf16_to_f32(q).astype(np.float64)
+    for b in range(q.shape[0]):
+        G = int(seq[b]) // 4
+        toks = [4 * g + i for g in idx[b, 0] if 0 <= g < G for i in range(4)]
+        z = 0.3 * qf[b, 0] @ Kf[b, toks].T                      # [H_q][n]
+        lse = logsumexp(z, axis=1)
+        out = np.exp(z - lse[:, None]) @ Vf[b, toks]
+        np.testing.assert_allclose(l8[b, 0], lse, rtol=1e-6)
+        ref_bits = np.array([[oracle.bf16_from_double(x) for x in row] for row in out])
+        assert np.array_equal(o8[b, 0], ref_bits)
+
+
+def test_kv8_scales_belong_to_their_own_cache():
+    """Swapping the key and value scales changes the result (each cache's
+    scale multiplies its own elements only)."""
+    q, kc, ks, vc, vs, seq, idx = _kv8_case(402)
+    o1, _ = oracle.sparse_attn_e4m3kv(q, kc, ks, vc, vs, seq, idx, 4, 0.25)
+    o2, _ = oracle.sparse_attn_e4m3kv(q, kc, vs, vc, ks, seq, idx, 4, 0.25)
+    assert not np.array_equal(o1, o2)

@@ -50,6 +50,12 @@ FP8_MUTANTS = {
     "e4m3_sign_lost": ("    return sign | best;", "    return best;"),
     "quantize_scale_not_applied": ("oracle_e4m3_from_double(bf16_value(xr[i]) / (double)sc)",
                                    "oracle_e4m3_from_double(bf16_value(xr[i]))"),
+    "kv8_value_scale_dropped": ("o[i] += p * (oracle_e4m3_value(vj[i]) * sv);",
+                                "o[i] += p * oracle_e4m3_value(vj[i]);"),
+    "kv8_key_scale_dropped": ("dot += bf16_value(qh[i]) * (oracle_e4m3_value(kj[i]) * sk);",
+                              "dot += bf16_value(qh[i]) * oracle_e4m3_value(kj[i]);"),
+    "kv8_scales_swapped": ("const double sv = (double)vs[b * svs_b + tok[j]];",
+                           "const double sv = (double)ks[b * sks_b + tok[j]];"),
     "fp8_score_drops_key_scale": ("dot *= (double)sq[qr] * (double)sk[kr];",
                                   "dot *= (double)sq[qr];"),
     "fp8_score_no_relu": ("s += (double)w_head[qr] * (dot > 0.0 ? dot : 0.0);",
