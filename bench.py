@@ -57,7 +57,7 @@ def parse():
                     help="rotated input copies (0: enough to exceed 3x L2)")
     ap.add_argument("--kernel", default=None,
                     choices=["prefill_scores", "prefill", "pool_keys", "index_scores", "topk",
-                             "sparse_attn", "decode", "decode_fp8", "kda", "reuse", "mla"],
+                             "sparse_attn", "decode", "decode_fp8", "kda", "reuse", "mla", "kv8"],
                     help="time one kernel of the path instead of the decode step (not the "
                          "headline line): prefill_scores = the chunked-prefill indexer "
                          "scores (tcgen05 GEMM) on the prefill_4k shapes; prefill = one whole "
@@ -1017,6 +1017,64 @@ def measure_mla(torch, lcsw, peak, with_oracle):
             "tflops": round(flops / (ms / 1e3) / 1e12, 2), "parity_vs_oracle": parity}
 
 
+def measure_kv8(torch, lcsw, peak):
+    """decode_1m's attention with an FP8 K/V cache (lcsw_sparse_attn_kv8): 64
+    heads over 512 seeded groups of the 1,048,576-token cache quantized on the
+    device, each call after a write of twice the L2 size; the bf16 split-K call
+    on the same selection is timed beside it."""
+    spec = synth.named("decode_1m")
+    c = synth.generate(spec)
+    dev = "cuda"
+    up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    G = spec.lengths[0] // spec.P
+    rng = np.random.default_rng(530)
+    idx = torch.from_numpy(np.sort(rng.choice(G, spec.k, replace=False)).astype(np.int32)
+                           .reshape(1, 1, spec.k)).to(dev)
+    q, K, V = up16(c["q"]), up16(c["K"]), up16(c["V"])
+    seq = torch.from_numpy(c["seq_len"]).to(dev)
+    kc, ks = lcsw.quantize_rows_e4m3(K)
+    vc, vs = lcsw.quantize_rows_e4m3(V)
+    out = torch.empty(1, 1, spec.H_q, spec.d_v, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(1, 1, spec.H_q, dtype=torch.float32, device=dev)
+    nb8 = lcsw.lib().lcsw_sparse_attn_kv8_workspace_size(1, 1, spec.H_q, spec.d_v, spec.k,
+                                                         spec.P)
+    ws8 = torch.empty(max(nb8, 16), dtype=torch.uint8, device=dev)
+    nb16 = lcsw.lib().lcsw_sparse_attn_workspace_size(1, 1, spec.H_q, spec.d_v, spec.k, spec.P)
+    ws16 = torch.empty(max(nb16, 16), dtype=torch.uint8, device=dev)
+    f8 = lambda: lcsw.sparse_attn_kv8(q, kc, ks, vc, vs, seq, idx, spec.P, c["scale"], out=out,
+                                      lse=lse, ws=ws8)
+    f16 = lambda: lcsw.sparse_attn(q, K, V, seq, idx, spec.P, c["scale"], out=out, lse=lse,
+                                   ws=ws16)
+    flush = torch.empty(2 * l2_bytes() // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(200)]
+        for a, b in evs:
+            flush.fill_(1.0)
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sorted(a.elapsed_time(b) for a, b in evs)[100]
+
+    ms8, ms16 = timed(f8), timed(f16)
+    ntok = spec.P * spec.k
+    ab8 = ntok * (spec.d_qk + spec.d_v + 8) + spec.H_q * (spec.d_qk + spec.d_v) * 2 + spec.k * 4
+    gbs = ab8 / (ms8 / 1e3) / 1e9
+    del q, K, V, kc, vc, flush
+    torch.cuda.empty_cache()
+    return {"kernel": "lcsw_sparse_attn_kv8 (split-K over E4M3 codes + merge)",
+            "ms_per_call": round(ms8, 5), "bf16_cache_ms_per_call": round(ms16, 5),
+            "alg_bytes": ab8, "timing": "median of 200 calls, each after a write of 2x L2",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4)}}
+
+
 def kda_alg_bytes(B, T, H, D):
     """Bytes a KDA step must move: the fp32 state read and written once, the
     conv history read and written, the step's inputs (projections, gates,
@@ -1125,6 +1183,7 @@ def per_config(args, torch, lcsw, peak, peaks):
     res["decode_1m_fp8_keys"] = measure_decode_fp8(torch, lcsw, peak, oracle_on)
     res["kda_decode_b64"] = measure_kda(torch, lcsw, peak, 200, 5, oracle_on)
     res["mla_attn_decode_1m"] = measure_mla(torch, lcsw, peak, oracle_on)
+    res["kv8_attn_decode_1m"] = measure_kv8(torch, lcsw, peak)
     return res
 
 
@@ -1225,6 +1284,15 @@ def main():
     if args.kernel in ("pool_keys", "index_scores", "topk", "sparse_attn", "decode",
                        "decode_fp8"):
         run_kernel_alone(args)
+        return
+    if args.kernel == "kv8":
+        import torch
+
+        import long_context_sparse_weighted_b300 as lcsw
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+            os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        e = measure_kv8(torch, lcsw, peaks.get("hbm_gbs", 6400.0))
+        print(json.dumps({"kernel": "kv8", **e}))
         return
     if args.kernel == "mla":
         import torch

@@ -176,6 +176,40 @@ lcsw_status lcsw_sparse_attn(const lcsw_bf16 *q, const lcsw_bf16 *K, int64_t sK_
                              void *ws, size_t ws_bytes, lcsw_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 (E4M3) K/V cache.  The serving stack of the reading notes quantizes
+ * caches per tier to INT8, FP8 or BF16 ("The serving stack"); this is the FP8
+ * tier for the attention cache, in the pooled keys' format: one fp32 scale
+ * per token row (amax / 448), codes rounded exactly to nearest, ties to even.
+ *
+ * lcsw_quantize_rows_e4m3: rows [r0_b, r0_b + n_rows) of every sequence
+ * (r0_b = row_begin[b], or 0 when row_begin is NULL) of a bf16 cache
+ * x [B][*][width] (batch stride sx_b elements) -> codes [B][*][width] uint8
+ * (batch stride sc_b bytes, a multiple of 16) and scales [B][*] fp32 (batch
+ * stride ss_b elements).  width a multiple of 16.  Rows of other positions are
+ * untouched, so a decode step quantizes just the newest token's row.
+ *
+ * lcsw_sparse_attn_kv8: lcsw_sparse_attn over such a cache,
+ *
+ *   z_j = scale * ks[b][j] * sum_i q_i e4m3(kc[b][j][i]),
+ *   out = sum_j softmax_j(z) * vs[b][j] * e4m3(vc[b][j][:])
+ *
+ * with the same selection, masking and output rules; kc, vc 16-byte aligned
+ * with strides (bytes) multiples of 16; ks, vs strides in elements.  The
+ * workspace is lcsw_sparse_attn_kv8_workspace_size bytes, 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_quantize_rows_e4m3(const lcsw_bf16 *x, int64_t sx_b, const int32_t *row_begin,
+                                    int B, int n_rows, int width, uint8_t *codes, int64_t sc_b,
+                                    float *scales, int64_t ss_b, lcsw_stream stream);
+size_t lcsw_sparse_attn_kv8_workspace_size(int B, int T, int H_q, int d_v, int k, int P);
+lcsw_status lcsw_sparse_attn_kv8(const lcsw_bf16 *q, const uint8_t *kc, int64_t skc_b,
+                                 const float *ks, int64_t sks_b, const uint8_t *vc,
+                                 int64_t svc_b, const float *vs, int64_t svs_b,
+                                 const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                 int H_q, int d_qk, int d_v, int P, int k, float scale,
+                                 lcsw_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                 lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
  * Sparse attention in the MLA latent geometry ("G2C Brief -- GLM-5.3-Flash":
  * MLA rank 512 per token, kv_lora_rank 512; the DSA diagram's "MLA latent
  * cache (rank 512 per token)").  One cached row per token, shared by every

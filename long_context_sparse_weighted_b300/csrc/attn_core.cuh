@@ -42,12 +42,18 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[DQK / 16][4], const 
 // MAXNT bounds the warp's token slice (ntok <= 8*MAXNT).  With QSMEM the Q
 // fragments are re-read from shared memory (sq, rows mt*16..) at every k-step
 // instead of living in registers (qa unused), for register-limited callers.
+//
+// With per-token scales (an FP8 K/V cache whose codes were widened exactly to
+// bf16): kscale[t] multiplies token t's scores, and vscale[t] its softmax
+// weight in the P V product (the sums l use the weights without it).
 template <int DQK, int DV, int MAXNT = kChunk / 8, bool QSMEM = false>
 __device__ __forceinline__ void attn_chunk(AttnWarpState<DV> &st, const uint32_t (&qa)[DQK / 16][4],
                                            const uint16_t *ck, const uint16_t *cv,
                                            const int *cg, int QP, int VP, int P, int tok0,
                                            int ntok, float scale_log2,
-                                           const uint16_t *sq = nullptr, int mt = 0) {
+                                           const uint16_t *sq = nullptr, int mt = 0,
+                                           const float *kscale = nullptr,
+                                           const float *vscale = nullptr) {
     const int lane = threadIdx.x & 31, c = lane & 3;
     float sacc[MAXNT][4];
 #pragma unroll
@@ -83,6 +89,13 @@ __device__ __forceinline__ void attn_chunk(AttnWarpState<DV> &st, const uint32_t
         if (nt * 8 >= ntok) break;
         const int n0 = tok0 + nt * 8 + 2 * c;
         const bool v0 = cg[n0 / P] >= 0, v1 = cg[(n0 + 1) / P] >= 0;
+        if (kscale) {
+            const float k0 = kscale[n0], k1 = kscale[n0 + 1];
+            sacc[nt][0] *= k0;
+            sacc[nt][1] *= k1;
+            sacc[nt][2] *= k0;
+            sacc[nt][3] *= k1;
+        }
         sacc[nt][0] = v0 ? sacc[nt][0] * scale_log2 : -INFINITY;
         sacc[nt][1] = v1 ? sacc[nt][1] * scale_log2 : -INFINITY;
         sacc[nt][2] = v0 ? sacc[nt][2] * scale_log2 : -INFINITY;
@@ -120,10 +133,18 @@ __device__ __forceinline__ void attn_chunk(AttnWarpState<DV> &st, const uint32_t
 #pragma unroll
     for (int kt = 0; kt < (MAXNT + 1) / 2; ++kt) {
         if (kt * 16 >= ntok) break;
-        const uint32_t pa0 = pack_bf2(sacc[2 * kt][0], sacc[2 * kt][1]);
-        const uint32_t pa1 = pack_bf2(sacc[2 * kt][2], sacc[2 * kt][3]);
-        const uint32_t pa2 = pack_bf2(sacc[2 * kt + 1][0], sacc[2 * kt + 1][1]);
-        const uint32_t pa3 = pack_bf2(sacc[2 * kt + 1][2], sacc[2 * kt + 1][3]);
+        float w0 = 1.f, w1 = 1.f, w2 = 1.f, w3 = 1.f;  // value scales of the four tokens
+        if (vscale) {
+            const int t0 = tok0 + kt * 16 + 2 * c;
+            w0 = vscale[t0];
+            w1 = vscale[t0 + 1];
+            w2 = vscale[t0 + 8];
+            w3 = vscale[t0 + 9];
+        }
+        const uint32_t pa0 = pack_bf2(sacc[2 * kt][0] * w0, sacc[2 * kt][1] * w1);
+        const uint32_t pa1 = pack_bf2(sacc[2 * kt][2] * w0, sacc[2 * kt][3] * w1);
+        const uint32_t pa2 = pack_bf2(sacc[2 * kt + 1][0] * w2, sacc[2 * kt + 1][1] * w3);
+        const uint32_t pa3 = pack_bf2(sacc[2 * kt + 1][2] * w2, sacc[2 * kt + 1][3] * w3);
         const int vrow = tok0 + kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int dt = 0; dt < DV / 8; dt += 2) {
@@ -213,5 +234,60 @@ __device__ __forceinline__ void store_warp_state(AttnWarpState<DV> &st, float *s
         state[(r0 + 8) * (DV + 2) + DV + 1] = st.l1;
     }
 }
+
+// Merge of split-K partial states (part_o [rows][S][H_q][DV] unnormalised,
+// part_ml [rows][S][H_q] = (m in log2 units, l)): one warp per (row, head),
+// grid (rows, ceil(H_q / 8)) of 256 threads.
+namespace {
+constexpr float kCombLn2 = 0.6931471805599453f;
+template <int DV>
+__global__ void __launch_bounds__(256) splitk_combine_kernel(
+    const float *__restrict__ part_o, const float2 *__restrict__ part_ml, int H_q, int S,
+    uint16_t *__restrict__ out, float *__restrict__ lse) {
+    const int64_t row = blockIdx.x;
+    const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (h >= H_q) return;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(&part_ml[(row * S + s) * H_q + h].x));
+    const float ref = M == -INFINITY ? 0.f : M;
+    constexpr int PER = DV / 32;  // 2 or 4 value dims per lane
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    float Lsum = 0.f;
+    // eight splits at a time, their loads issued together
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        float v[8][PER];
+        float f[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            f[u] = 0.f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) v[u][i] = 0.f;
+            if (s0 + u < S) {
+                const int64_t pi = (row * S + s0 + u) * H_q + h;
+                const float2 ml = __ldg(&part_ml[pi]);
+                f[u] = exp2f(ml.x - ref);
+                Lsum += f[u] * ml.y;
+                const float *po = part_o + pi * DV + lane * PER;
+#pragma unroll
+                for (int i = 0; i < PER; ++i) v[u][i] = __ldg(po + i);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int i = 0; i < PER; ++i) acc[i] += f[u] * v[u][i];
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    uint16_t *orow = out + (row * H_q + h) * DV + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; i += 2)
+        *reinterpret_cast<uint32_t *>(orow + i) = pack_bf2(acc[i] * inv, acc[i + 1] * inv);
+    if (lse && lane == 0) lse[row * H_q + h] = Lsum > 0.f ? (M + log2f(Lsum)) * kCombLn2 : -INFINITY;
+}
+
+}  // namespace
 
 }  // namespace lcsw

@@ -222,15 +222,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two E4M3 codes (bits 0-15 of w, the lower code in bits 0-7) as an f16x2 pair;
-// every E4M3 value is exact in f16.
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w) {
-    uint32_t r;
-    asm("{\n .reg .b16 t;\n mov.b16 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
-        : "=r"(r)
-        : "h"((unsigned short)(w & 0xFFFFu)));
-    return r;
-}
 
 // ------------------------------------------------------------ phase timers -
 // Built with -DLCSW_PHASE_TIMERS, thread 0 of every block records the

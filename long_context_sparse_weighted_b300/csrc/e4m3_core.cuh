@@ -13,6 +13,8 @@
 // with one rounding, which keeps its sign).
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace lcsw {
@@ -58,6 +60,25 @@ __device__ __forceinline__ uint32_t e4m3_quantize(float x, float scale, float in
     else if (d < 0.f) r = lo;
     else r = (lo & 1u) ? hi : lo;
     return sign | min(r, 0x7Eu);
+}
+
+// Two E4M3 codes (bits 0-15 of w, the lower code in bits 0-7) as an f16x2 pair;
+// every E4M3 value is exact in f16.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n .reg .b16 t;\n mov.b16 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
+        : "=r"(r)
+        : "h"((unsigned short)(w & 0xFFFFu)));
+    return r;
+}
+
+// The same two codes as a bf16x2 pair (also exact: an E4M3 value has at most
+// four significant bits and lies inside the bf16 range).
+__device__ __forceinline__ uint32_t e4m3x2_bf16x2(uint32_t w) {
+    const uint32_t h = e4m3x2_f16x2(w);
+    const float lo = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+    const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+    return pack_bf2(lo, hi);
 }
 
 // Scale of a row from its largest magnitude: amax / 448 rounded to fp32 (the

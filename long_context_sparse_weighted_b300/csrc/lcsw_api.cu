@@ -664,6 +664,61 @@ lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
     return cuda_status(e, "prefill attention");
 }
 
+lcsw_status lcsw_quantize_rows_e4m3(const lcsw_bf16 *x, int64_t sx_b, const int32_t *row_begin,
+                                    int B, int n_rows, int width, uint8_t *codes, int64_t sc_b,
+                                    float *scales, int64_t ss_b, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_quantize_rows_e4m3");
+    CHECK(B >= 0 && n_rows >= 0 && width > 0, "bad dimension");
+    CHECK(width % 16 == 0, "width must be a multiple of 16");
+    if (B == 0 || n_rows == 0) return LCSW_OK;
+    CHECK(x && codes && scales, "null pointer argument");
+    CHECK(bf16_rows_ok(x, width, sx_b) && aligned(codes, 16) && sc_b % 16 == 0 &&
+              aligned(scales, 4) && (!row_begin || aligned(row_begin, 4)),
+          "misaligned argument (x rows 16-byte aligned, codes and their stride 16 bytes)");
+    CHECK(sx_b >= 0 && sc_b >= 0 && ss_b >= 0, "strides must be >= 0");
+    return cuda_status(lcsw::launch_quantize_rows_e4m3(x, sx_b, row_begin, n_rows, width, B,
+                                                       codes, sc_b, scales, ss_b,
+                                                       (cudaStream_t)stream),
+                       "quantize rows launch");
+}
+
+size_t lcsw_sparse_attn_kv8_workspace_size(int B, int T, int H_q, int d_v, int k, int P) {
+    if (B <= 0 || T <= 0 || H_q <= 0 || d_v <= 0 || k <= 0 || !p_ok(P)) return 0;
+    return lcsw::sparse_attn_kv8_ws_bytes(int64_t(B) * T, H_q, d_v, k, P);
+}
+
+lcsw_status lcsw_sparse_attn_kv8(const lcsw_bf16 *q, const uint8_t *kc, int64_t skc_b,
+                                 const float *ks, int64_t sks_b, const uint8_t *vc,
+                                 int64_t svc_b, const float *vs, int64_t svs_b,
+                                 const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                 int H_q, int d_qk, int d_v, int P, int k, float scale,
+                                 lcsw_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                 lcsw_stream stream) {
+    LCSW_RANGE("lcsw_sparse_attn_kv8");
+    CHECK(B >= 0 && T >= 0, "negative dimension");
+    CHECK(p_ok(P), "P must be 1, 2, 4 or 8");
+    CHECK(k >= 1, "k must be >= 1");
+    CHECK(attn_shape_ok(H_q, d_qk, d_v), "unsupported attention shape");
+    const int64_t rows = int64_t(B) * T;
+    if (rows == 0) return LCSW_OK;
+    CHECK(rows <= 65535, "B*T must be <= 65535");
+    CHECK(q && kc && ks && vc && vs && seq_len && idx && out, "null pointer argument");
+    CHECK(bf16_rows_ok(q, d_qk, 0) && bf16_rows_ok(out, d_v, 0) && aligned(kc, 16) &&
+              aligned(vc, 16) && skc_b % 16 == 0 && svc_b % 16 == 0 && aligned(ks, 4) &&
+              aligned(vs, 4) && aligned(seq_len, 4) && aligned(idx, 4) &&
+              (!lse || aligned(lse, 4)),
+          "misaligned argument (code caches and their strides 16 bytes)");
+    CHECK(skc_b >= 0 && svc_b >= 0 && sks_b >= 0 && svs_b >= 0, "strides must be >= 0");
+    const size_t need = lcsw::sparse_attn_kv8_ws_bytes(rows, H_q, d_v, k, P);
+    if (need && (!ws || ws_bytes < need || !aligned(ws, 16)))
+        return fail(LCSW_ERR_WORKSPACE, "FP8 K/V attention needs a 16-byte aligned workspace "
+                    "of %zu bytes", need);
+    return cuda_status(lcsw::launch_sparse_attn_kv8(q, kc, skc_b, ks, sks_b, vc, svc_b, vs, svs_b,
+                                                    seq_len, idx, B, T, H_q, d_qk, d_v, P, k,
+                                                    scale, out, lse, ws, (cudaStream_t)stream),
+                       "FP8 K/V attention launch");
+}
+
 size_t lcsw_sparse_attn_mla_workspace_size(int B, int T, int H_q, int k, int P) {
     if (B <= 0 || T <= 0 || H_q <= 0 || k < 1 || !p_ok(P)) return 0;
     return lcsw::sparse_attn_mla_ws_bytes(int64_t(B) * T, H_q, k, P);

@@ -130,54 +130,6 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_split_kernel(
     }
 }
 
-template <int DV>
-__global__ void __launch_bounds__(256) splitk_combine_kernel(
-    const float *__restrict__ part_o, const float2 *__restrict__ part_ml, int H_q, int S,
-    uint16_t *__restrict__ out, float *__restrict__ lse) {
-    const int64_t row = blockIdx.x;
-    const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (h >= H_q) return;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(&part_ml[(row * S + s) * H_q + h].x));
-    const float ref = M == -INFINITY ? 0.f : M;
-    constexpr int PER = DV / 32;  // 2 or 4 value dims per lane
-    float acc[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    float Lsum = 0.f;
-    // eight splits at a time, their loads issued together
-    for (int s0 = 0; s0 < S; s0 += 8) {
-        float v[8][PER];
-        float f[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            f[u] = 0.f;
-#pragma unroll
-            for (int i = 0; i < PER; ++i) v[u][i] = 0.f;
-            if (s0 + u < S) {
-                const int64_t pi = (row * S + s0 + u) * H_q + h;
-                const float2 ml = __ldg(&part_ml[pi]);
-                f[u] = exp2f(ml.x - ref);
-                Lsum += f[u] * ml.y;
-                const float *po = part_o + pi * DV + lane * PER;
-#pragma unroll
-                for (int i = 0; i < PER; ++i) v[u][i] = __ldg(po + i);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-            for (int i = 0; i < PER; ++i) acc[i] += f[u] * v[u][i];
-    }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    uint16_t *orow = out + (row * H_q + h) * DV + lane * PER;
-#pragma unroll
-    for (int i = 0; i < PER; i += 2)
-        *reinterpret_cast<uint32_t *>(orow + i) = pack_bf2(acc[i] * inv, acc[i + 1] * inv);
-    if (lse && lane == 0) lse[row * H_q + h] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
-}
-
 template <int DQK, int DV>
 cudaError_t launch_typed(const uint16_t *q, const uint16_t *K, int64_t sK_b, const uint16_t *V,
                          int64_t sV_b, const int32_t *seq_len, const int32_t *idx, int B, int T,

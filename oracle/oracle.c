@@ -582,7 +582,7 @@ void oracle_sparse_attn_e4m3kv(const uint16_t *q, const uint8_t *kc, int64_t skc
                     double dot = 0.0;
                     for (int i = 0; i < d_qk; ++i)
                         dot += bf16_value(qh[i]) * (oracle_e4m3_value(kj[i]) * sk);
-                    z[j] = scale * dot;
+                    z[j] = dot * scale;
                     if (z[j] > m)
                         m = z[j];
                 }
@@ -597,10 +597,11 @@ void oracle_sparse_attn_e4m3kv(const uint16_t *q, const uint8_t *kc, int64_t skc
                     for (int i = 0; i < d_v; ++i)
                         o[i] += p * (oracle_e4m3_value(vj[i]) * sv);
                 }
+                const double lsum = l;
                 for (int i = 0; i < d_v; ++i)
-                    oh[i] = oracle_bf16_from_double(o[i] / l);
+                    oh[i] = oracle_bf16_from_double(o[i] / lsum);
                 if (lh)
-                    *lh = (float)(m + log(l));
+                    *lh = (float)(log(l) + m);
             }
         }
     }
