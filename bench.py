@@ -57,7 +57,8 @@ def parse():
                     help="rotated input copies (0: enough to exceed 3x L2)")
     ap.add_argument("--kernel", default=None,
                     choices=["prefill_scores", "prefill", "pool_keys", "index_scores", "topk",
-                             "sparse_attn", "decode", "decode_fp8", "kda", "reuse", "mla", "kv8"],
+                             "sparse_attn", "decode", "decode_fp8", "kda", "reuse", "mla", "kv8",
+                             "mla_decode"],
                     help="time one kernel of the path instead of the decode step (not the "
                          "headline line): prefill_scores = the chunked-prefill indexer "
                          "scores (tcgen05 GEMM) on the prefill_4k shapes; prefill = one whole "
@@ -1038,6 +1039,69 @@ def measure_mla(torch, lcsw, peak, with_oracle):
             "tflops": round(flops / (ms / 1e3) / 1e12, 2), "parity_vs_oracle": parity}
 
 
+def measure_mla_decode(torch, lcsw, peak, with_oracle):
+    """The whole decode step in the MLA latent geometry (lcsw_decode_fused with
+    d_qk 576, d_v 512, V = NULL): decode_1m's indexer, append and selection
+    in the persistent kernel (its attention phases off), then the attention
+    over the 576-wide latent rows and its merge; each call follows a write of
+    twice the L2 size, and a device-side spin covers the host's enqueue so
+    that the events time the launches only."""
+    spec = synth.named("mla_decode_1m")
+    c = synth.generate(spec)
+    P, k, B = spec.P, spec.k, spec.B
+    dev = "cuda"
+    up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    seq = torch.from_numpy(c["seq_len"]).to(dev)
+    k_idx, pool_w = up16(c["k_idx"]), torch.from_numpy(c["pool_w"]).to(dev)
+    kp = torch.zeros(B, spec.G_max, 64, dtype=torch.bfloat16, device=dev)
+    lcsw.pool_keys(k_idx, pool_w, seq, P, kp)
+    K = up16(c["K"])
+    idx = torch.empty(B, k, dtype=torch.int32, device=dev)
+    dec = lcsw.Decoder(up16(c["q_idx"][:, 0]), torch.from_numpy(c["w_head"][:, 0]).to(dev), kp,
+                       up16(c["q"][:, 0]), K, None, seq, P, k, c["scale"], k_idx=k_idx,
+                       pool_w=pool_w, idx_out=idx)
+    parity = None
+    if with_oracle:
+        import oracle
+        out, lse = dec()
+        dec.status()
+        ref = oracle.decode_case(c)
+        o = synth.bf16_to_f32(out.view(torch.int16).cpu().numpy().view(np.uint16))
+        r = synth.bf16_to_f32(ref["out"][:, 0])
+        parity = {"idx_equal": bool(np.array_equal(idx.cpu().numpy(), ref["idx"][:, 0])),
+                  "max_abs_err": float(np.abs(o - r).max()),
+                  "lse_max_err": float(np.abs(lse.cpu().numpy() - ref["lse"][:, 0]).max())}
+    flush = torch.empty(2 * l2_bytes() // 4, dtype=torch.float32, device=dev)
+    for _ in range(5):
+        dec()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(100)]
+    for a, b in evs:
+        flush.fill_(1.0)
+        torch.cuda._sleep(200000)
+        a.record()
+        dec()
+        b.record()
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in evs)[50]
+    G = spec.lengths[0] // P
+    ab = G * 128 + P * k * spec.d_qk * 2 + spec.H_q * (spec.d_qk + spec.d_v) * 2 + \
+        spec.H_i * (128 + 4)
+    gbs = ab / (ms / 1e3) / 1e9
+    launches = dec.launches_per_call
+    del K, flush, kp
+    torch.cuda.empty_cache()
+    return {"kernel": "lcsw_decode_fused, MLA geometry (persistent selection, latent attention)",
+            "ms_per_step": round(ms, 5), "tokens_per_s": round(B / (ms / 1e3), 1),
+            "launches_per_step": launches, "alg_bytes_per_step": ab,
+            "timing": "median of 100 calls, each after a write of 2x L2",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4)},
+            "parity_vs_oracle": parity}
+
+
 def measure_kv8(torch, lcsw, peak):
     """decode_1m's attention with an FP8 K/V cache (lcsw_sparse_attn_kv8): 64
     heads over 512 seeded groups of the 1,048,576-token cache quantized on the
@@ -1208,6 +1272,7 @@ def per_config(args, torch, lcsw, peak, peaks):
     res["kda_decode_b64"] = measure_kda(torch, lcsw, peak, 200, 5, oracle_on)
     res["mla_attn_decode_1m"] = measure_mla(torch, lcsw, peak, oracle_on)
     res["kv8_attn_decode_1m"] = measure_kv8(torch, lcsw, peak)
+    res["mla_decode_1m"] = measure_mla_decode(torch, lcsw, peak, oracle_on)
     return res
 
 
@@ -1308,6 +1373,15 @@ def main():
     if args.kernel in ("pool_keys", "index_scores", "topk", "sparse_attn", "decode",
                        "decode_fp8"):
         run_kernel_alone(args)
+        return
+    if args.kernel == "mla_decode":
+        import torch
+
+        import long_context_sparse_weighted_b300 as lcsw
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+            os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        e = measure_mla_decode(torch, lcsw, peaks.get("hbm_gbs", 6400.0), True)
+        print(json.dumps({"kernel": "mla_decode", **e}))
         return
     if args.kernel == "kv8":
         import torch

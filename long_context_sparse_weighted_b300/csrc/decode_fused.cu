@@ -51,6 +51,19 @@ cudaError_t launch_fused_decode(const lcsw_decode_args *a, void *ws, int *status
     return launch_shape<false>(make_params(a, ws, status), a, st);
 }
 
+cudaError_t launch_fused_select(const lcsw_decode_args *a, int32_t *idx_out, void *ws,
+                                int *status, cudaStream_t st) {
+    // the selection alone: the 128-wide attention instance, whose attention
+    // and merge phases are skipped (q, K, V are not read)
+    lcsw_decode_args s = *a;
+    s.d_qk = 128;
+    s.d_v = 128;
+    s.idx_out = idx_out;
+    Params prm = make_params(&s, ws, status);
+    prm.select_only = 1;
+    return launch_shape<false>(prm, &s, st);
+}
+
 bool reuse_decode_supported(int B, int H_q, int d_qk, int d_v, int k) {
     const int ncta = num_sms();
     if (ncta > kMaxCtas || B < 1 || 2 * B > ncta || k < 1 || k > kMaxK) return false;

@@ -184,6 +184,7 @@ struct Params {
     uint8_t *kq;          // FP8 pooled keys (tile-major, e4m3_core.cuh) or null
     int64_t sq_b;         // its batch stride in bytes
     int B, G_max, H_i, P, k, H_q, force_slow, skip_arrive;
+    int select_only;      // stop after the selection (idx_out required): no attention
     float scale_log2;
     uint16_t *out;
     float *lse;
@@ -1452,8 +1453,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     const int spec_cap = kChunk / P;
     const int n_spec = min(cand_tot, spec_cap);
     const uint16_t *qrow = p.q + int64_t(b) * p.H_q * DQK;
-    att_load_q<DQK, DV>(smem + kU, qrow, p.H_q);
-    att_gather<DQK, DV>(smem + kU, 0, spec_g, n_spec, G_b, P, Kb, Vb);
+    if (!p.select_only) {
+        att_load_q<DQK, DV>(smem + kU, qrow, p.H_q);
+        att_gather<DQK, DV>(smem + kU, 0, spec_g, n_spec, G_b, P, Kb, Vb);
+    }
     int *spec_sg = reinterpret_cast<int *>(smem + kU + AL::g);  // chunk buffer 0's group ids
     PHASE_MARK(9);
 
@@ -2006,14 +2009,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     }
     PHASE_MARK(15);
 
-    // ---- attention over this block's selected groups ---------------------------
-    attend_groups<DQK, DV>(smem + kU, own, n_own, G_b, P, Kb, Vb, qrow, p.H_q, p.scale_log2,
-                           p.part_o + int64_t(cta) * p.H_q * DV,
-                           p.part_ml + int64_t(cta) * p.H_q, use_spec);
-    PHASE_MARK(17);
+    if (!p.select_only) {
+        // ---- attention over this block's selected groups ---------------------------
+        attend_groups<DQK, DV>(smem + kU, own, n_own, G_b, P, Kb, Vb, qrow, p.H_q, p.scale_log2,
+                               p.part_o + int64_t(cta) * p.H_q * DV,
+                               p.part_ml + int64_t(cta) * p.H_q, use_spec);
+        PHASE_MARK(17);
 
-    // ---- merge the partial states, head by head --------------------------------
-    if (!merge_partials<DV>(p, smem, sv, sred, b, j, n_b, cb0)) return;
+        // ---- merge the partial states, head by head --------------------------------
+        if (!merge_partials<DV>(p, smem, sv, sred, b, j, n_b, cb0)) return;
+    }
     PHASE_MARK(19);
     __syncthreads();
     // this block's words of the other buffers were read during the previous
@@ -2223,6 +2228,7 @@ Params make_params(const lcsw_decode_args *a, void *ws, int *status) {
     prm.kq = nullptr;
     prm.sq_b = 0;
     prm.idx_in = nullptr;
+    prm.select_only = 0;
     return prm;
 }
 

@@ -325,7 +325,9 @@ static DecodeWs carve_decode(const lcsw_decode_args *a, void *ws) {
     w.status = static_cast<int *>(ws);
     // the persistent kernels' region first: its partial-state words sit at the
     // same offsets for every call that shares the workspace
-    w.fused = c.take(lcsw::fused_decode_ws_bytes(a->B, a->G_max, a->H_q, a->d_v, a->k, a->P));
+    // (the MLA geometry runs the persistent kernel for its selection only, at d_v 128)
+    const int dv_fused = mla_shape(a->d_qk, a->d_v) ? 128 : a->d_v;
+    w.fused = c.take(lcsw::fused_decode_ws_bytes(a->B, a->G_max, a->H_q, dv_fused, a->k, a->P));
     w.scores = static_cast<float *>(c.take(size_t(a->B) * a->G_max * sizeof(float)));
     w.idx = static_cast<int32_t *>(c.take(size_t(a->B) * a->k * sizeof(int32_t)));
     w.attn = c.take(mla_shape(a->d_qk, a->d_v)
@@ -360,9 +362,14 @@ int lcsw_decode_launches(const lcsw_decode_args *a) {
     if (!(a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) &&
         lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P))
         return 1;
+    if (!(a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) && mla_shape(a->d_qk, a->d_v) &&
+        lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, 128, 128, a->k, a->P))
+        return 1 + (lcsw::sparse_attn_mla_splits(a->B, a->H_q, a->k, a->P) > 1 ? 2 : 1);
     const int S = mla_shape(a->d_qk, a->d_v) ? lcsw::sparse_attn_mla_splits(a->B, a->H_q, a->k, a->P)
                                               : lcsw::sparse_attn_splits(a->B, a->H_q, a->k, a->P);
-    return (a->k_idx ? 1 : 0) + 3 + (S > 1 ? 1 : 0);
+    // append, scores, top-k (three kernels for a few long rows), attention (+ merge)
+    const int topk = lcsw::topk_wide_ws_bytes(a->B, a->G_max, a->k) ? 3 : 1;
+    return (a->k_idx ? 1 : 0) + 1 + topk + 1 + (S > 1 ? 1 : 0);
 }
 
 lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_bytes,
@@ -382,6 +389,13 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
     if (!(a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) &&
         lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, a->d_qk, a->d_v, a->k, a->P)) {
         return cuda_status(lcsw::launch_fused_decode(a, w.fused, w.status, st), "fused decode");
+    }
+    if (!(a->flags & LCSW_DECODE_FORCE_MULTIKERNEL) && mla_shape(a->d_qk, a->d_v) &&
+        lcsw::fused_decode_supported(a->B, a->G_max, a->H_i, a->H_q, 128, 128, a->k, a->P)) {
+        // MLA geometry: the persistent kernel selects, the latent attention follows
+        cudaError_t e = lcsw::launch_fused_select(a, idx, w.fused, w.status, st);
+        if (e != cudaSuccess) return cuda_status(e, "fused selection");
+        return cuda_status(decode_attend(a, idx, w.attn, st), "decode attention");
     }
     // Multi-kernel path (same results): append, score, select, attend.
     if (a->k_idx) {

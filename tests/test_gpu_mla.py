@@ -57,9 +57,13 @@ def test_mla_attention_matches_oracle(B, T, H_q, lengths, k):
     assert_lse_close(lse.cpu().numpy(), l_ref)
 
 
-def test_mla_decode_step_selects_and_attends_like_the_oracle():
+@pytest.mark.parametrize("flags", [0, lcsw.FORCE_MULTIKERNEL], ids=["fused_select", "launches"])
+def test_mla_decode_step_selects_and_attends_like_the_oracle(flags):
     """lcsw_decode_fused in the MLA geometry (V = NULL): the indexer selection
-    bit for bit, then attention over the latent rows."""
+    bit for bit, then attention over the latent rows.  By default the
+    persistent kernel selects (its attention skipped) and the latent attention
+    follows; the forced path runs scores, top-k and attention as separate
+    launches."""
     spec = _mla_spec(B=2, lengths=[40000, 12000], H_i=8, k=256, H_q=64, seed=310)
     c = synth.generate(spec)
     ref = oracle.decode_case(c)
@@ -67,7 +71,10 @@ def test_mla_decode_step_selects_and_attends_like_the_oracle():
     idx = torch.empty(spec.B, spec.k, dtype=torch.int32, device="cuda")
     dec = lcsw.Decoder(d["q_idx"][:, 0], d["w_head"][:, 0], dev_bf16(ref["k_pooled"]),
                        d["q"][:, 0], d["K"], None, d["seq_len"], spec.P, spec.k, c["scale"],
-                       idx_out=idx)
+                       idx_out=idx, flags=flags)
+    merge = 1 if lcsw.lib().lcsw_sparse_attn_mla_workspace_size(spec.B, 1, spec.H_q, spec.k, 4) else 0
+    topk = 3 if lcsw.lib().lcsw_topk_workspace_size(spec.B, spec.G_max, spec.k) else 1
+    assert dec.launches_per_call == (2 if flags == 0 else 2 + topk) + merge
     out, lse = dec()
     dec.status()
     assert np.array_equal(idx.cpu().numpy(), ref["idx"][:, 0])
@@ -114,3 +121,25 @@ def test_mla_attention_full_size_decode_1m():
     torch.cuda.synchronize()
     assert_attn_close(host_bits(out), o_ref)
     assert_lse_close(lse.cpu().numpy(), l_ref)
+
+
+@pytest.mark.slow
+def test_mla_decode_step_full_size():
+    """The benchmarked MLA decode step: decode_1m's indexer and selection over
+    1,048,576 tokens, attention over the 576-wide latent rows, against the
+    oracle's whole step (pool, score, top-k, attention)."""
+    spec = synth.named("mla_decode_1m")
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    d = upload_case(c)
+    kp = dev_bf16(ref["k_pooled"]).clone()
+    kp[0, -1] = 0  # the step re-pools the newest group itself
+    idx = torch.empty(spec.B, spec.k, dtype=torch.int32, device="cuda")
+    dec = lcsw.Decoder(d["q_idx"][:, 0], d["w_head"][:, 0], kp, d["q"][:, 0], d["K"], None,
+                       d["seq_len"], spec.P, spec.k, c["scale"], k_idx=d["k_idx"],
+                       pool_w=d["pool_w"], idx_out=idx)
+    out, lse = dec()
+    dec.status()
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"][:, 0])
+    assert_attn_close(host_bits(out), ref["out"][:, 0])
+    assert_lse_close(lse.cpu().numpy(), ref["lse"][:, 0])
