@@ -1192,7 +1192,7 @@ def measure_kda(torch, lcsw, peak, steps, warmup, with_oracle):
         import oracle.kda as okda
         lcsw.kda_step(**d, out=out)
         torch.cuda.synchronize()
-        worst_s = worst_o = 0.0
+        worst_s = worst_o = worst_ulp = 0.0
         for b in (0, spec.B - 1):
             sub = {k: (v[b:b + 1] if isinstance(v, np.ndarray) and k != "conv_w" else v)
                    for k, v in c.items()}
@@ -1211,10 +1211,14 @@ def measure_kda(torch, lcsw, peak, steps, warmup, with_oracle):
                 v - np.einsum("bhi,bhij->bhj", k_, Sp))
             M = (np.einsum("bhi,bhij->bhj", np.abs(q), np.abs(Sp))
                  + np.abs((q * k_).sum(-1))[..., None] * np.abs(dw))
-            worst_o = max(worst_o, float((np.abs(o[:, 0] - o_ref[:, 0]) /
-                                          (2.0 ** -8 * np.abs(o_ref[:, 0]) + 2.0 ** -16 * M)).max()))
+            err = np.abs(o[:, 0] - o_ref[:, 0])
+            worst_o = max(worst_o, float((err / (2.0 ** -8 * np.abs(o_ref[:, 0])
+                                                 + 2.0 ** -16 * M)).max()))
+            # the same error in units of the bf16 spacing at the exact value
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(o_ref[:, 0]), 1e-30))) - 7)
+            worst_ulp = max(worst_ulp, float((err / ulp).max()))
         parity = {"sequences_checked": 2, "state_err_over_head_max": worst_s,
-                  "out_err_over_bound": worst_o,
+                  "out_err_over_bound": worst_o, "out_err_bf16_ulps": worst_ulp,
                   "ok": bool(worst_s <= 4e-6 and worst_o <= 1.0)}
     fn = [lambda: lcsw.kda_step(**d, out=out)]
     ms, clocks = time_graph_steps(torch, fn, steps, warmup, 1)
