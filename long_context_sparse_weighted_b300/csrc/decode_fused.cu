@@ -11,10 +11,10 @@ bool fused_decode_supported(int B, int G_max, int H_i, int H_q, int d_qk, int d_
     if (!((d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128))) return false;
     if (!(H_q % 16 == 0 && H_q <= 64)) return false;  // one M = 128 tensor-core tile of heads
     // 16-bit shared counters: a block's chunk must stay below 65536 groups.
-    // Blocks go to sequences by cost w_b = 2 G_b + min(k, G_b) P (d_qk + d_v) / 32
+    // Blocks go to sequences by cost w_b = 2 G_b + min(k, G_b) P (d_qk + d_v) / 16
     // (64-byte units) >= 2 G_b, so a chunk holds at most sum_b w_b / (2 (ncta - B))
     // groups, plus tile rounding.
-    const long long w_max = 2LL * G_max + (long long)k * P * ((d_qk + d_v) / 32);
+    const long long w_max = 2LL * G_max + (long long)k * P * ((d_qk + d_v) / 16);
     const long long bound =
         B == 1 ? (long long)G_max / ncta + 32 : (long long)B * w_max / (2LL * (ncta - B)) + 32;
     if (bound >= 65535) return false;

@@ -769,9 +769,94 @@ __device__ __noinline__ void assign_blocks(const int *w, int B, int ncta, int *c
 // the partial words of every block of the sequence until all are written,
 // writes the normalised output row, then clears the words it read for the
 // next call.  Returns false if a bounded wait ran out (the status word is set).
+// Few sources (a sequence with at most kFewSources blocks): a warp merges a
+// whole head on its own, lane = a float4 column of the head's DV dims (two
+// heads a warp for DV = 64), running over the sources with an online
+// rescale, so the block's heads go 16 (or 32) at a time with no block-wide
+// barrier.  A sequence of one block still writes and reads its one partial
+// state, which keeps the words' protocol the same for every shape.
+constexpr int kFewSources = 16;
+template <int DV>
+__device__ __forceinline__ bool merge_few(const Params &p, int b, int j, int n_b, int cb0) {
+    constexpr int D4 = DV / 4;                 // 32 (DV = 128) or 16 lanes a head
+    constexpr int HPW = 32 / D4;               // heads a warp merges at once
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int dc = lane % D4, sub = lane / D4;
+    const int nh = (p.H_q - j + n_b - 1) / n_b;  // this block's heads: j, j + n_b, ...
+    bool ok = true;
+    for (int i0 = warp * HPW; i0 < nh && ok; i0 += kWarps * HPW) {  // warp-uniform
+        const int hi = i0 + sub;
+        const bool act = hi < nh;
+        const int h = j + hi * n_b;
+        float m_run = -INFINITY, l_run = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const long long t0 = clock64();
+        for (int u = 0; u < n_b; ++u) {
+            const int64_t pi = int64_t(cb0 + u) * p.H_q + (act ? h : 0);
+            uint2 mlw = make_uint2(1u, 1u);
+            uint4 ow = make_uint4(1u, 1u, 1u, 1u);
+            if (act) {
+                mlw = ld_relaxed_u32x2(p.part_ml + pi);
+                ow = ld_relaxed_v4(reinterpret_cast<const uint4 *>(p.part_o + pi * DV + dc * 4));
+            }
+            for (int spin = 0;; ++spin) {
+                const bool pend = act && (mlw.x == 0u || mlw.y == 0u || ow.x == 0u || ow.y == 0u ||
+                                          ow.z == 0u || ow.w == 0u);
+                if (!__any_sync(0xffffffffu, pend)) break;
+                const bool give_up = clock64() - t0 > kSpinBudget ||
+                                     ((spin & 63) == 63 && aborted(p.abort_flag));
+                if (__any_sync(0xffffffffu, give_up)) {  // (warp-uniform)
+                    ok = false;
+                    break;
+                }
+                __nanosleep(64);
+                if (pend) {
+                    mlw = ld_relaxed_u32x2(p.part_ml + pi);
+                    ow = ld_relaxed_v4(reinterpret_cast<const uint4 *>(p.part_o + pi * DV + dc * 4));
+                }
+            }
+            if (!ok) break;
+            const float ms = part_dec(mlw.x), ls = part_dec(mlw.y);
+            if (act && ls > 0.f) {
+                const float mn = fmaxf(m_run, ms);
+                const float a = m_run == -INFINITY ? 0.f : exp2f(m_run - mn);
+                const float w = exp2f(ms - mn);
+                acc.x = acc.x * a + w * part_dec(ow.x);
+                acc.y = acc.y * a + w * part_dec(ow.y);
+                acc.z = acc.z * a + w * part_dec(ow.z);
+                acc.w = acc.w * a + w * part_dec(ow.w);
+                l_run = l_run * a + w * ls;
+                m_run = mn;
+            }
+        }
+        if (!ok) break;
+        if (act) {
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            *reinterpret_cast<uint2 *>(p.out + (int64_t(b) * p.H_q + h) * DV + dc * 4) =
+                make_uint2(pack_bf2(acc.x * inv, acc.y * inv), pack_bf2(acc.z * inv, acc.w * inv));
+            if (p.lse && dc == 0)
+                p.lse[int64_t(b) * p.H_q + h] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        }
+        __syncwarp();  // every lane of the head has read the (m, l) words
+        // the words read are cleared for the next call
+        if (act)
+            for (int u = 0; u < n_b; ++u) {
+                const int64_t pi = int64_t(cb0 + u) * p.H_q + h;
+                st_relaxed_zero4(p.part_o + pi * DV + dc * 4);
+                if (dc == 0) st_relaxed_zero2(p.part_ml + pi);
+            }
+    }
+    if (!__syncthreads_and(ok)) {
+        if (threadIdx.x == 0) raise_timeout(p, 6);
+        return false;
+    }
+    return true;
+}
+
 template <int DV>
 __device__ __forceinline__ bool merge_partials(const Params &p, unsigned char *smem, int *sv,
                                                float *sred, int b, int j, int n_b, int cb0) {
+    if (n_b <= kFewSources) return merge_few<DV>(p, b, j, n_b, cb0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_src = n_b;
     auto src_cta = [&](int u) { return cb0 + u; };
@@ -1102,7 +1187,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             lens[tid] = L;
             int G = L / P;
             G = G < 0 ? 0 : (G > p.G_max ? p.G_max : G);
-            wv = 2 * G + min(p.k, G) * P * ((DQK + DV) / 32);
+            // (a selected token weighs twice its bytes: a block attends more
+            // slowly than it streams keys, about 64 tokens a microsecond)
+            wv = 2 * G + min(p.k, G) * P * ((DQK + DV) / 16);
         }
         if (tid < B) offs[tid] = wv;
         __syncthreads();
