@@ -291,7 +291,9 @@ lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int
 typedef struct {
     const lcsw_bf16 *q_idx;    /* [B][H_i][d_idx]                              */
     const float *w_head;       /* [B][H_i]                                     */
-    lcsw_bf16 *k_pooled;       /* [B][*][d_idx], batch stride sp_b; in/out     */
+    lcsw_bf16 *k_pooled;       /* [B][G_max][d_idx], batch stride sp_b; in/out:
+                                  rows 0..G_max-1 of every sequence readable (the
+                                  first copies go out before the lengths arrive) */
     int64_t sp_b;
     const lcsw_bf16 *k_idx;    /* [B][*][d_idx] raw keys (stride sk_b) or NULL */
     int64_t sk_b;

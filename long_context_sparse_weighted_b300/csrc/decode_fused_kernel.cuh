@@ -120,29 +120,30 @@ constexpr int kNewRows = kSelList + kMaxK * 4;        // newest group: [8][64] b
 constexpr int kNewCode = kNewRows + 8 * 128 + 8 * 4;  // its FP8 row: [64] codes, scale
 constexpr int kRingBars = kNewCode + 64 + 16;         // [kWarps][ring depth] mbarriers
 constexpr int kQCode = (kRingBars + kWarps * kRingMax * 8 + 15) / 16 * 16;  // FP8 query: [16][64] codes, [16] scales
-constexpr int kSmemBytes = kQCode + 16 * 64 + 16 * 4;
+// the attention chunk buffers' group ids [4][kChunk] (-1 = masked), apart from
+// region U and the scores: the prefetch writes buffer 0's row while the
+// block's scores are still live
+constexpr int kGids = (kQCode + 16 * 64 + 16 * 4 + 15) / 16 * 16;
+constexpr int kSmemBytes = kGids + 4 * kChunk * 4;
 static_assert(kRingBars % 8 == 0, "mbarrier alignment");
 
 // Attention operands: Q [64 heads][QP], NBUF chunk buffers (each K [64
 // tokens][QP] then V [64][VP]), P [64 heads][PP] bf16, per-quarter row maxima
-// and sums [4][64] f32, chunk group ids [NBUF][64].  Row pitches are padded by
-// 16 bytes so ldmatrix rows fall on distinct banks.
+// and sums [4][64] f32 (the chunks' group ids are at kGids).  Row pitches are
+// padded by 16 bytes so ldmatrix rows fall on distinct banks.
 constexpr int kAttBytes = kMisc - kU;
 template <int DQK, int DV>
 struct AttLayout {
     static constexpr int QP = DQK + 8, VP = DV + 8, PP = kChunk + 8;
     static constexpr int kv_bytes = kChunk * (QP + VP) * 2;
     static constexpr int fixed = 64 * QP * 2 + 64 * PP * 2 + 2 * 4 * 64 * 4;
-    static constexpr int NBUF = (kAttBytes - fixed) / (kv_bytes + kChunk * 4) >= 4
-                                    ? 4
-                                    : (kAttBytes - fixed) / (kv_bytes + kChunk * 4);
+    static constexpr int NBUF = (kAttBytes - fixed) / kv_bytes >= 4 ? 4 : (kAttBytes - fixed) / kv_bytes;
     static constexpr int q = 0;
     static constexpr int buf = q + 64 * QP * 2;  // chunk buffer i at buf + i * kv_bytes
     static constexpr int pt = buf + NBUF * kv_bytes;
     static constexpr int rm = pt + 64 * PP * 2;
     static constexpr int rl = rm + 4 * 64 * 4;
-    static constexpr int g = rl + 4 * 64 * 4;
-    static constexpr int total = g + NBUF * kChunk * 4;
+    static constexpr int total = rl + 4 * 64 * 4;
 };
 static_assert(AttLayout<192, 128>::NBUF >= 2, "attention chunk buffers");
 static_assert(AttLayout<192, 128>::total <= kAttBytes, "attention operands overflow");
@@ -449,14 +450,16 @@ __device__ __forceinline__ void att_load_q(unsigned char *u, const uint16_t *qro
 }
 
 // The K/V rows of groups glist[0..n) (n <= 64/P) into chunk buffer `buf`
-// (one cp.async group); their group ids (-1 = masked) into its id row.
+// (one cp.async group); their group ids (-1 = masked) into its row of gids.
 template <int DQK, int DV>
-__device__ __forceinline__ void att_gather(unsigned char *u, int buf, const int32_t *glist, int n,
-                                           int G, int P, const uint16_t *kb, const uint16_t *vb) {
+__device__ __forceinline__ void att_gather(unsigned char *u, int *gids, int buf,
+                                           const int32_t *glist, int n, int G, int P,
+                                           const uint16_t *kb, const uint16_t *vb) {
     using AL = AttLayout<DQK, DV>;
+    static_assert(AL::NBUF <= 4, "group id rows");
     uint16_t *dk = reinterpret_cast<uint16_t *>(u + AL::buf + buf * AL::kv_bytes);
-    gather_chunk<DQK, DV>(dk, dk + kChunk * AL::QP, reinterpret_cast<int *>(u + AL::g) + buf * kChunk,
-                          glist, n, P, G, kb, vb, AL::QP, AL::VP, threadIdx.x, kThreads);
+    gather_chunk<DQK, DV>(dk, dk + kChunk * AL::QP, gids + buf * kChunk, glist, n, P, G, kb, vb,
+                          AL::QP, AL::VP, threadIdx.x, kThreads);
 }
 
 // Attention of every query head over the tokens of groups own[0..n_own) of
@@ -468,12 +471,14 @@ __device__ __forceinline__ void att_gather(unsigned char *u, int buf, const int3
 // maxima of the quarters through shared memory -> P = 2^(s - m) as bf16 into
 // shared memory -> every quarter's warp adds P V for its value dims over all
 // 64 tokens.  Chunks stream through NBUF buffers.  With `prefetched` the Q
-// rows and the only chunk are already in flight in buffer 0 (att_load_q and
+// rows and a first chunk are already in flight in buffer 0 (att_load_q and
 // att_gather, with the unselected groups masked in its id row), and
-// n_own <= 64/P.  Every wait here is on the block's own copies.
+// own[0..n_own) are the selected groups it does not hold, gathered after it.
+// Group ids of the chunk buffers: gids [NBUF][kChunk].  Every wait here is on
+// the block's own copies.
 template <int DQK, int DV>
-__device__ __forceinline__ void attend_groups(unsigned char *u, const int32_t *own, int n_own,
-                                              int G, int P, const uint16_t *kb,
+__device__ __forceinline__ void attend_groups(unsigned char *u, int *gids, const int32_t *own,
+                                              int n_own, int G, int P, const uint16_t *kb,
                                               const uint16_t *vb, const uint16_t *qrow, int H_q,
                                               float scale_log2, float *part_o, float2 *part_ml,
                                               bool prefetched) {
@@ -487,22 +492,29 @@ __device__ __forceinline__ void attend_groups(unsigned char *u, const int32_t *o
     uint16_t *sp = reinterpret_cast<uint16_t *>(u + AL::pt);
     float *red_m = reinterpret_cast<float *>(u + AL::rm);  // [4][64]
     float *red_l = reinterpret_cast<float *>(u + AL::rl);  // [4][64]
-    const int *sg = reinterpret_cast<const int *>(u + AL::g);  // [NBUF][kChunk]
+    const int *sg = gids;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = lane & 3, gq = lane >> 2;
     const int mt = warp & 3, qq = warp >> 2;
     const bool wact = mt * 16 < H_q;
     const int lp2 = 31 - __clz(P);  // P is a power of two
     const int gpc = kChunk >> lp2;
-    const int nchunks = prefetched ? (n_own > 0 ? 1 : 0) : (n_own + gpc - 1) / gpc;
+    const int pre = prefetched ? 1 : 0;  // chunk 0 already in buffer 0
+    const int nchunks = pre + (n_own + gpc - 1) / gpc;
+    // chunk cc >= pre takes groups own[(cc - pre) gpc ..]
+    auto gather = [&](int cc) {
+        const int o0 = (cc - pre) * gpc;
+        att_gather<DQK, DV>(u, gids, cc % NBUF, own + o0, min(gpc, n_own - o0), G, P, kb, vb);
+    };
 
     if (!prefetched) {
         cp_async_wait<0>();  // an unused prefetch lands before its buffers are reused
         __syncthreads();
         att_load_q<DQK, DV>(u, qrow, H_q);
-        for (int c0 = 0; c0 < NBUF - 1 && c0 < nchunks; ++c0)
-            att_gather<DQK, DV>(u, c0, own + c0 * gpc, min(gpc, n_own - c0 * gpc), G, P, kb, vb);
+    } else if (nchunks > 1) {
+        __syncthreads();  // the selection's shared arrays overlap buffers 1..
     }
+    for (int c0 = pre; c0 < NBUF - 1 && c0 < nchunks; ++c0) gather(c0);
 
     float o[NTV][4];
 #pragma unroll
@@ -512,13 +524,9 @@ __device__ __forceinline__ void attend_groups(unsigned char *u, const int32_t *o
     for (int ci = 0; ci < nchunks; ++ci) {
         const int buf = ci % NBUF;
         __syncthreads();  // every warp is done with chunk ci - 1, whose buffer comes next
-        if (!prefetched && ci + NBUF - 1 < nchunks) {
-            const int cn = ci + NBUF - 1;
-            att_gather<DQK, DV>(u, cn % NBUF, own + cn * gpc, min(gpc, n_own - cn * gpc), G, P,
-                                kb, vb);
-        }
+        if (ci + NBUF - 1 < nchunks) gather(ci + NBUF - 1);
         // chunk ci has landed once at most the chunks issued after it are pending
-        const int after = prefetched ? 0 : min(nchunks - 1, ci + NBUF - 1) - ci;
+        const int after = min(nchunks - 1, ci + NBUF - 1) - ci;
         if (after >= 3) cp_async_wait<3>();
         else if (after == 2) cp_async_wait<2>();
         else if (after == 1) cp_async_wait<1>();
@@ -651,16 +659,21 @@ __device__ __forceinline__ void attend_groups(unsigned char *u, const int32_t *o
 }
 
 // Blocks per sequence for per-sequence costs w[0..B) (shared memory, B <= 96):
-// n_b = max(1, ceil(w_b / L)) for the smallest L with sum_b n_b <= ncta (warp
-// 0 bisects on L; L0 = ceil(sum_b w_b / (ncta - B)) always fits, since each
+// n_b = max(1, ceil(w_b / L)) for the smallest L with sum_b n_b <= ncta, to
+// within 1/256 (L0 = ceil(sum_b w_b / (ncta - B)) always fits, since each
 // ceiling adds less than one block), the blocks left over go to the sequence
 // with the largest cost per block.  This minimises the largest per-block cost
 // (proportional shares rounded down can leave a short sequence with almost
-// two blocks' work on one).  Writes cta_begin[0..B] (prefix sums, shared);
-// every thread of the block calls it.
-__device__ __noinline__ void assign_blocks(const int *w, int B, int ncta, int *cta_begin) {
-    const int lane = threadIdx.x & 31;
-    if (threadIdx.x < 32) {
+// two blocks' work on one).  The search for L splits its interval in 17 per
+// round, one trial L a warp (the interval shrinks 289-fold in two rounds; a
+// one-warp bisection took several microseconds at B = 64).  Writes
+// cta_begin[0..B] (prefix sums, shared); every thread of the block calls it;
+// scratch: kWarps words of shared memory.
+__device__ __noinline__ void assign_blocks(const int *w, int B, int ncta, int *cta_begin,
+                                           int *scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned lo, hi, wmin, wmax;
+    {
         unsigned wl[3];
         bool on[3];
         unsigned tot = 0;
@@ -671,19 +684,9 @@ __device__ __noinline__ void assign_blocks(const int *w, int B, int ncta, int *c
             wl[i] = on[i] ? unsigned(max(0, w[bb])) : 0u;
             tot += wl[i];
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        auto blocks = [&](unsigned L) {  // sum over the warp of max(1, ceil(w / L))
-            int c = 0;
-#pragma unroll
-            for (int i = 0; i < 3; ++i)
-                if (on[i]) c += wl[i] > 0 ? int((wl[i] + L - 1) / L) : 1;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-            return c;
-        };
-        // equal costs (a uniform batch): an even split is optimal, no search
-        unsigned wmin = 0xFFFFFFFFu, wmax = 0u;
+        tot = __reduce_add_sync(0xffffffffu, tot);
+        wmin = 0xFFFFFFFFu;
+        wmax = 0u;
 #pragma unroll
         for (int i = 0; i < 3; ++i)
             if (on[i]) {
@@ -692,14 +695,39 @@ __device__ __noinline__ void assign_blocks(const int *w, int B, int ncta, int *c
             }
         wmin = __reduce_min_sync(0xffffffffu, wmin);
         wmax = __reduce_max_sync(0xffffffffu, wmax);
-        // L >= tot / ncta is necessary, L = ceil(tot / (ncta - B)) sufficient;
-        // bisect to within 1/256 of the smallest feasible L
-        unsigned lo = max(1u, tot / unsigned(ncta)), hi = max(1u, (tot + (ncta - B) - 1) / (ncta - B));
-        if (wmin == wmax) lo = hi;  // skips the search; the split below is then made even
-        while (hi - lo > max(1u, hi >> 8)) {  // warp-uniform
-            const unsigned mid = lo + (hi - lo) / 2;
-            if (blocks(mid) <= ncta) hi = mid;
-            else lo = mid;
+        // L >= tot / ncta is necessary, L = ceil(tot / (ncta - B)) sufficient
+        lo = max(1u, tot / unsigned(ncta));
+        hi = max(1u, (tot + (ncta - B) - 1) / (ncta - B));
+        if (wmin == wmax) lo = hi;  // equal costs: no search, the split below is even
+        while (hi - lo > max(1u, hi >> 8)) {  // block-uniform
+            const unsigned step = (hi - lo + kWarps) / (kWarps + 1);
+            const unsigned L = min(hi, lo + step * unsigned(warp + 1));
+            int c = 0;
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+                if (on[i]) c += wl[i] > 0 ? int((wl[i] + L - 1) / L) : 1;
+            c = __reduce_add_sync(0xffffffffu, c);
+            if (lane == 0) scratch[warp] = c <= ncta ? 1 : 0;
+            __syncthreads();
+            // the first trial that fits is the new hi, the one before it the new lo
+            int f = kWarps;
+#pragma unroll
+            for (int w2 = kWarps - 1; w2 >= 0; --w2)
+                if (scratch[w2]) f = w2;
+            const unsigned nlo = f > 0 ? min(hi, lo + step * unsigned(f)) : lo;
+            if (f < kWarps) hi = min(hi, lo + step * unsigned(f + 1));
+            lo = nlo;
+            __syncthreads();  // scratch is rewritten next round
+        }
+    }
+    if (threadIdx.x < 32) {
+        unsigned wl[3];
+        bool on[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int bb = 3 * lane + i;
+            on[i] = bb < B;
+            wl[i] = on[i] ? unsigned(max(0, w[bb])) : 0u;
         }
         int n[3];
 #pragma unroll
@@ -1022,6 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     int *spec_g = reinterpret_cast<int *>(sred + 64);                         // [kChunk]
     int *rank = spec_g + kChunk;                                              // [kRankMax]
     int32_t *sel = reinterpret_cast<int32_t *>(smem + kSelList);              // [kMaxK]
+    int *gids = reinterpret_cast<int *>(smem + kGids);                        // [4][kChunk]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x, ncta = gridDim.x;
@@ -1153,6 +1182,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     // not queue behind the burst below), then, since the chunk split depends
     // only on G_b, the warp's first copies on the guess that the cache is full
     // (G_b = G_max); if it is not, they are waited out and reissued below.
+    // Several sequences: the copies wait for the split.  Issued before the
+    // lengths arrive, on the guess that every cache is full, they delayed the
+    // length loads behind them by about 3 us.
     int L_first = 0;
     if (B == 1) {
         L_first = __ldg(p.seq_len);
@@ -1166,10 +1198,19 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         const int n0 = warp_tiles(spec_lo, spec_hi);
         for (int kk = 0; kk < min(RING, n0); ++kk) issue_tile_of(0, spec_lo, spec_hi, kk);
     }
+    // even split: ncta / B blocks a sequence, one more for the first ncta % B
+    auto even_seq = [&](int cc) {
+        const int q = ncta / B, rr = ncta % B;
+        return cc < rr * (q + 1) ? cc / (q + 1) : rr + (cc - rr * (q + 1)) / q;
+    };
+    auto even_begin = [&](int bb) { return bb * (ncta / B) + min(bb, ncta % B); };
 
     // ---- roles: blocks per sequence, proportional to its cost ------------------
     int b, cb0, n_b, L_b, G_b;
-    if (tid == 0) { sv[19] = 0; sv[27] = 0; sv[31] = 0; sv[32] = 0; sv[33] = 0; sv[34] = 0; }
+    if (tid == 0) {
+        sv[19] = 0; sv[27] = 0; sv[31] = 0; sv[32] = 0; sv[33] = 0; sv[34] = 0;
+        sv[36] = 0; sv[37] = 0;
+    }
     if (B == 1) {
         L_b = L_first;
         G_b = L_b / P;
@@ -1193,13 +1234,20 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         }
         if (tid < B) offs[tid] = wv;
         __syncthreads();
-        assign_blocks(offs, B, ncta, cta_begin);
-        for (int bb = tid; bb < B; bb += kThreads)
-            if (cta_begin[bb] <= cta && cta < cta_begin[bb + 1]) sv[1] = bb;
-        __syncthreads();
-        b = sv[1];
-        cb0 = cta_begin[b];
-        n_b = cta_begin[b + 1] - cb0;
+        if (__syncthreads_and(tid >= B || offs[tid] == offs[0])) {
+            // equal costs: the even split, which is what assign_blocks gives them
+            b = even_seq(cta);
+            cb0 = even_begin(b);
+            n_b = even_begin(b + 1) - cb0;
+        } else {
+            assign_blocks(offs, B, ncta, cta_begin, scratch);
+            for (int bb = tid; bb < B; bb += kThreads)
+                if (cta_begin[bb] <= cta && cta < cta_begin[bb + 1]) sv[1] = bb;
+            __syncthreads();
+            b = sv[1];
+            cb0 = cta_begin[b];
+            n_b = cta_begin[b + 1] - cb0;
+        }
         L_b = lens[b];
         G_b = L_b / P;
         G_b = G_b < 0 ? 0 : (G_b > p.G_max ? p.G_max : G_b);
@@ -1222,9 +1270,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
 
     // ---- phase-1 prologue: first tiles in flight, indexer query, append -------
     // The block's chunk of pooled keys is one contiguous range.  Lane 0 of each
-    // warp has the warp's first RING tiles in flight (issued above when the
-    // guessed chunk was right), so the prologue's own loads overlap them, and
-    // refills a slot as soon as the warp has read it.
+    // warp has the warp's first RING tiles in flight (one sequence: issued
+    // above when the guessed chunk was right), so the prologue's own loads
+    // overlap them, and refills a slot as soon as the warp has read it.
     const int n_mine = warp_tiles(g_lo, g_hi);
     auto issue_tile = [&](int kk) { issue_tile_of(b, g_lo, g_hi, kk); };
     if (lane == 0) {
@@ -1542,9 +1590,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
     const uint16_t *qrow = p.q + int64_t(b) * p.H_q * DQK;
     if (!p.select_only) {
         att_load_q<DQK, DV>(smem + kU, qrow, p.H_q);
-        att_gather<DQK, DV>(smem + kU, 0, spec_g, n_spec, G_b, P, Kb, Vb);
+        att_gather<DQK, DV>(smem + kU, gids, 0, spec_g, n_spec, G_b, P, Kb, Vb);
     }
-    int *spec_sg = reinterpret_cast<int *>(smem + kU + AL::g);  // chunk buffer 0's group ids
     PHASE_MARK(9);
 
     // ---- exchange: every slot header of the sequence, then every candidate -------
@@ -1774,7 +1821,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
         if (warp == 0) {
             // own candidates in rounds of 32, in slot (= ascending group) order
             int np = 0;
-            bool cover = true;
             for (int r0 = 0; r0 < m_own; r0 += 32) {
                 const int o = r0 + lane;
                 const unsigned long long rl = o < m_own ? crank[own0 + o] : ~0ull;
@@ -1784,25 +1830,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 if (pick && LCSW_INBOUNDS(np + __popc(bsel) <= kRankMax, 102))
                     own[np + __popc(bsel & ((1u << lane) - 1u))] = grp;
                 np += __popc(bsel);
-                // the prefetch covers the block if it holds every selected group
-                bool found = !pick;
-                for (int s2 = 0; s2 < n_spec && !found; ++s2) found = spec_g[s2] == grp;
-                cover = __all_sync(0xffffffffu, found) && cover;
             }
-            if (lane == 0) {
-                sv[16] = np;
-                sv[18] = cover ? 1 : 0;
-            }
+            if (lane == 0) sv[16] = np;
         }
         __syncthreads();
         n_own = sv[16];
-        use_spec = sv[18] != 0;
-        if (use_spec && tid < spec_cap) {
-            bool keep = false;
-            if (tid < n_spec)
-                for (int i = 0; i < n_own; ++i) keep |= own[i] == spec_g[tid];
-            if (!keep) spec_sg[tid] = -1;  // prefetched but not selected: masked
-        }
     } else if (fast) {
         unsigned kth = 0xFFFFFFFFu, take_eq = 0;
         if (k_b > 0) {
@@ -1882,26 +1914,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
                 np += __popc(bsel);
                 eqr += __popc(beq);
             }
-            // the prefetched groups serve as the attention chunk if they cover ours
-            __syncwarp();
-            bool ok_l = true;
-            for (int i = lane; i < min(np, kMaxK); i += 32) {
-                bool found = false;
-                for (int s2 = 0; s2 < n_spec; ++s2) found |= spec_g[s2] == own[i];
-                ok_l = ok_l && found;
-            }
-            const bool cover = np <= n_spec && __all_sync(0xffffffffu, ok_l);
-            if (lane == 0) { sv[16] = min(np, kMaxK); sv[18] = cover ? 1 : 0; }
+            if (lane == 0) sv[16] = min(np, kMaxK);
         }
         __syncthreads();
         n_own = sv[16];
-        use_spec = sv[18] != 0;
-        if (use_spec && tid < spec_cap) {
-            bool keep = false;
-            if (tid < n_spec)
-                for (int i = 0; i < n_own; ++i) keep |= own[i] == spec_g[tid];
-            if (!keep) spec_sg[tid] = -1;  // prefetched but not selected: masked
-        }
         PHASE_MARK(13);
         // the full ascending selection, for the optional index output
         if (p.idx_out && j == 0) {
@@ -1946,6 +1962,106 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
             for (int i = k_b + tid; i < p.k; i += kThreads) p.idx_out[int64_t(b) * p.k + i] = -1;
         }
         __syncthreads();
+    }
+    // The selected groups the prefetch holds stay in chunk buffer 0 as the
+    // attention's first chunk; its other slots (prefetched groups not
+    // selected, or never filled) take the first of the selected groups it
+    // does not hold, and the rest follow in further chunks.  So the chunks
+    // are as few as without the prefetch, and only the groups it missed are
+    // gathered.
+    if (fast && !p.select_only && n_spec > 0) {
+        // (1) own[] keeps, in order, the selected groups the prefetch misses;
+        // sv[36..37]: bits of the prefetch entries selected
+        if (n_own <= 32) {
+            if (warp == 0) {
+                const int g = lane < n_own ? own[lane] : -1;
+                int hit = -1;
+                if (lane < n_own)
+                    for (int s2 = 0; s2 < n_spec; ++s2) hit = spec_g[s2] == g ? s2 : hit;
+                const unsigned keep = __ballot_sync(0xffffffffu, lane < n_own && hit < 0);
+                const unsigned h_lo = __reduce_or_sync(0xffffffffu, hit >= 0 && hit < 32 ? 1u << hit : 0u);
+                const unsigned h_hi = __reduce_or_sync(0xffffffffu, hit >= 32 ? 1u << (hit - 32) : 0u);
+                if ((keep >> lane) & 1u) own[__popc(keep & ((1u << lane) - 1u))] = g;
+                if (lane == 0) {
+                    sv[36] = int(h_lo);
+                    sv[37] = int(h_hi);
+                    sv[16] = __popc(keep);
+                }
+            }
+        } else {
+            constexpr int kPer = kMaxK / kThreads;
+            int gk[kPer];
+            int n_keep = 0;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+                const int i = tid * kPer + e;
+                gk[e] = -1;
+                if (i < n_own) {
+                    const int g = own[i];
+                    int hit = -1;
+                    for (int s2 = 0; s2 < n_spec; ++s2) hit = spec_g[s2] == g ? s2 : hit;
+                    if (hit >= 0)
+                        atomicOr(reinterpret_cast<unsigned *>(sv + 36 + (hit >> 5)), 1u << (hit & 31));
+                    else gk[e] = g;
+                    n_keep += hit < 0;
+                }
+            }
+            int n_rest;
+            int at = block_exclusive_scan(n_keep, scratch, &n_rest);  // (every own[] read is done)
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                if (gk[e] >= 0) own[at++] = gk[e];
+            if (tid == 0) sv[16] = n_rest;
+        }
+        __syncthreads();
+        const int n_rest = sv[16];
+        use_spec = n_rest < n_own;
+        if (use_spec) {
+            // (2) buffer 0's free slots, in order, take own[0 .. n_fill)
+            const unsigned long long taken =
+                unsigned(sv[36]) | ((unsigned long long)unsigned(sv[37]) << 32);
+            const unsigned long long slots = spec_cap == 64 ? ~0ull : (1ull << spec_cap) - 1ull;
+            const unsigned long long freem = slots & ~taken;
+            const int n_fill = min(n_rest, __popcll(freem));
+            int *fslot = rank;  // free slot of own[q] (the rank counters are dead)
+            if (tid < spec_cap && !((taken >> tid) & 1ull)) {
+                const int q = __popcll(freem & ((1ull << tid) - 1ull));  // tid is free slot q
+                const int g = q < n_fill ? own[q] : -1;
+                gids[tid] = (g >= 0 && g < G_b) ? g : -1;  // else: masked
+                if (q < n_fill) fslot[q] = tid;
+            }
+            if (n_fill > 0) {
+                // the prefetch has landed before its slots are written again
+                cp_async_wait<0>();
+                __syncthreads();
+                using AL = AttLayout<DQK, DV>;
+                uint16_t *dk = reinterpret_cast<uint16_t *>(smem + kU + AL::buf);
+                uint16_t *dv = dk + kChunk * AL::QP;
+                constexpr int CK = DQK / 8, CV = DV / 8;
+                const int lp2 = 31 - __clz(P);  // P is a power of two
+                // token row r of the fill (group own[r / P]) goes to row
+                // fslot[r / P] P + r % P of buffer 0; a warp a row
+                for (int r = warp; r < n_fill * P; r += kWarps) {
+                    const int q = r >> lp2, t = r & (P - 1);
+                    const int g = own[q];
+                    const bool ok = g >= 0 && g < G_b;
+                    const int row = fslot[q] * P + t;
+                    for (int c8 = lane; c8 < CK + CV; c8 += 32) {
+                        if (c8 < CK)
+                            cp_async16(smem_u32(dk + row * AL::QP + c8 * 8),
+                                       ok ? Kb + (int64_t(g) * P + t) * DQK + c8 * 8 : Kb,
+                                       ok ? 16 : 0);
+                        else
+                            cp_async16(smem_u32(dv + row * AL::VP + (c8 - CK) * 8),
+                                       ok ? Vb + (int64_t(g) * P + t) * DV + (c8 - CK) * 8 : Vb,
+                                       ok ? 16 : 0);
+                    }
+                }
+                cp_async_commit();
+            }
+            own += n_fill;
+            n_own = n_rest - n_fill;
+        }
     }
     PHASE_MARK(14);
     DBG_ADD(0, fast && !by_rank);
@@ -2098,7 +2214,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const Params 
 
     if (!p.select_only) {
         // ---- attention over this block's selected groups ---------------------------
-        attend_groups<DQK, DV>(smem + kU, own, n_own, G_b, P, Kb, Vb, qrow, p.H_q, p.scale_log2,
+        attend_groups<DQK, DV>(smem + kU, gids, own, n_own, G_b, P, Kb, Vb, qrow, p.H_q, p.scale_log2,
                                p.part_o + int64_t(cta) * p.H_q * DV,
                                p.part_ml + int64_t(cta) * p.H_q, use_spec);
         PHASE_MARK(17);
@@ -2160,7 +2276,7 @@ __global__ void __launch_bounds__(kThreads, 1) reuse_decode_kernel(const Params 
             offs[tid] = min(p.k, max(0, L / P)) + 1;
         }
         __syncthreads();
-        assign_blocks(offs, B, ncta, cta_begin);
+        assign_blocks(offs, B, ncta, cta_begin, scratch);
         for (int bb = tid; bb < B; bb += kThreads)
             if (cta_begin[bb] <= cta && cta < cta_begin[bb + 1]) sv[1] = bb;
         __syncthreads();
@@ -2176,7 +2292,8 @@ __global__ void __launch_bounds__(kThreads, 1) reuse_decode_kernel(const Params 
     for (int i = tid; i < n_own; i += kThreads)
         if (LCSW_INBOUNDS(i < kMaxK, 106)) own[i] = __ldg(p.idx_in + int64_t(b) * p.k + lo + i);
     __syncthreads();
-    attend_groups<DQK, DV>(smem + kU, own, n_own, G_b, P, p.K + int64_t(b) * p.sK_b,
+    attend_groups<DQK, DV>(smem + kU, reinterpret_cast<int *>(smem + kGids), own, n_own, G_b, P,
+                           p.K + int64_t(b) * p.sK_b,
                            p.V + int64_t(b) * p.sV_b, p.q + int64_t(b) * p.H_q * DQK, p.H_q,
                            p.scale_log2, p.part_o + int64_t(cta) * p.H_q * DV,
                            p.part_ml + int64_t(cta) * p.H_q, false);

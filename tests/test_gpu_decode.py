@@ -97,6 +97,20 @@ def test_decode_all_scores_tied(path, G):
     check_against_oracle(c, got, ref, exact=True)
 
 
+@pytest.mark.parametrize("path", ["persistent", "persistent_multipass_select"])
+def test_decode_one_block_sequences_past_9216_groups(path):
+    """76 equal sequences of 9,250 groups: the even split gives 72 of them two
+    blocks and 4 one block, whose 9,250 scores run past entry 9,216 of the
+    scores kept in shared memory.  The prefetch of a block's first
+    candidates (K/V rows and group ids) must leave every score alone: the
+    multi-pass selection reads them all after it."""
+    spec = synth.Spec(B=76, lengths=[37000] * 76, H_i=4, k=512, H_q=16, seed=209)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_decode(c, ref["k_pooled"], flags=PATHS[path])
+    check_against_oracle(c, got, ref)
+
+
 def test_decode_bounded_wait_reports_timeout():
     """A block that never arrives at a cross-block barrier: the other blocks'
     bounded waits run out, the call returns, and the status reads TIMEOUT."""
