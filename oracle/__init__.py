@@ -47,6 +47,15 @@ def _declare(lib):
     lib.oracle_sparse_attn_e4m3kv.argtypes = [P, P, I64, P, I64, P, I64, P, I64, P, P, I32, I32,
                                               I32, I32, I32, I32, I32, D, P, P]
     lib.oracle_sparse_attn_e4m3kv.restype = None
+    lib.oracle_i8_value.argtypes = [ctypes.c_int8, ctypes.c_float]
+    lib.oracle_i8_value.restype = D
+    lib.oracle_i8_from_double.argtypes = [D, ctypes.c_float]
+    lib.oracle_i8_from_double.restype = ctypes.c_int8
+    lib.oracle_quantize_rows_i8.argtypes = [P, I64, I32, P, P]
+    lib.oracle_quantize_rows_i8.restype = None
+    lib.oracle_sparse_attn_i8kv.argtypes = [P, P, I64, P, I64, P, I64, P, I64, P, P, I32, I32,
+                                            I32, I32, I32, I32, I32, D, P, P]
+    lib.oracle_sparse_attn_i8kv.restype = None
     lib.oracle_pool_keys.argtypes = [P, I64, P, I64, P, I32, I32, I32, P, I64]
     lib.oracle_visible_counts.argtypes = [P, P, I32, I32, I32, P]
     lib.oracle_index_scores.argtypes = [P, P, P, I64, P, P, I32, I32, I32, I32, I32, I64, P]
@@ -190,6 +199,46 @@ def sparse_attn_e4m3kv(q, kc, ks, vc, vs, seq_len, idx, P, scale):
                                       _p(vc), vc.shape[1] * d_v, _p(vs), vs.shape[1],
                                       _p(seq_len), _p(idx), B, T, H_q, d_qk, d_v, P, k,
                                       float(scale), _p(out), _p(lse))
+    return out, lse
+
+
+def i8_value(code: int, scale: float) -> float:
+    return _load().oracle_i8_value(int(code), float(scale))
+
+
+def i8_from_double(x: float, scale: float) -> int:
+    """Nearest integer to x / scale in [-127, 127], ties to even."""
+    return int(_load().oracle_i8_from_double(float(x), float(scale)))
+
+
+def quantize_rows_i8(x):
+    """bf16 rows [..., d] -> (int8 codes [..., d], fp32 scale per row = amax/127)."""
+    x = _c(x, np.uint16)
+    d = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1]))
+    code = np.empty(x.shape, np.int8)
+    scale = np.empty(x.shape[:-1], np.float32)
+    _load().oracle_quantize_rows_i8(_p(x), rows, d, _p(code), _p(scale))
+    return code, scale
+
+
+def sparse_attn_i8kv(q, kc, ks, vc, vs, seq_len, idx, P, scale):
+    """Attention over an INT8 K/V cache: element = code * the token row's
+    scale.  kc [B][L][d_qk], vc [B][L][d_v] int8 codes; ks, vs [B][L] fp32."""
+    q = _c(q, np.uint16)
+    kc, vc = _c(kc, np.int8), _c(vc, np.int8)
+    ks, vs = _c(ks, np.float32), _c(vs, np.float32)
+    seq_len = _c(seq_len, np.int32)
+    idx = _c(idx, np.int32)
+    B, T, H_q, d_qk = q.shape
+    d_v = vc.shape[2]
+    k = idx.shape[-1]
+    out = np.empty((B, T, H_q, d_v), np.uint16)
+    lse = np.empty((B, T, H_q), np.float32)
+    _load().oracle_sparse_attn_i8kv(_p(q), _p(kc), kc.shape[1] * d_qk, _p(ks), ks.shape[1],
+                                    _p(vc), vc.shape[1] * d_v, _p(vs), vs.shape[1],
+                                    _p(seq_len), _p(idx), B, T, H_q, d_qk, d_v, P, k,
+                                    float(scale), _p(out), _p(lse))
     return out, lse
 
 

@@ -609,3 +609,125 @@ void oracle_sparse_attn_e4m3kv(const uint16_t *q, const uint8_t *kc, int64_t skc
     free(z);
     free(tok);
 }
+
+/* ------------------------------------------------------- INT8 K/V cache --- */
+
+/* The INT8 tier of the same serving stack (reading notes, "The serving
+ * stack": caches quantized per tier to INT8, FP8 or BF16; no format given).
+ * Readings:
+ *   code   a signed 8-bit integer in [-127, 127] (symmetric, -128 unused)
+ *   scale  one per token row: amax / 127 rounded to fp32 (0 for an all-zero
+ *          row, whose codes are all 0)
+ *   round  code_i = the integer nearest to x_i / scale, ties to the even
+ *          integer; |x_i| <= amax keeps it within +-127
+ *   value  code * scale, exact in double (8 by 24 significant bits)
+ * The nearest integer is found by trying every magnitude 0..127 against |x|
+ * (c * scale is exact in double, and so is its distance to |x| wherever two
+ * candidates come close). */
+double oracle_i8_value(int8_t c, float scale)
+{
+    return (double)c * (double)scale;
+}
+
+int8_t oracle_i8_from_double(double x, float scale)
+{
+    const double a = fabs(x);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 127; ++c) {
+        const double d = fabs((double)c * (double)scale - a);
+        if (d < bd || (d == bd && c % 2 == 0)) {
+            bd = d;
+            best = c;
+        }
+    }
+    return (int8_t)(x < 0.0 ? -best : best);
+}
+
+void oracle_quantize_rows_i8(const uint16_t *x, int64_t rows, int d, int8_t *code, float *scale)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * d;
+        double amax = 0.0;
+        for (int i = 0; i < d; ++i) {
+            const double a = fabs(bf16_value(xr[i]));
+            if (a > amax) amax = a;
+        }
+        const float sc = (float)(amax / 127.0);
+        scale[r] = sc;
+        for (int i = 0; i < d; ++i)
+            code[r * d + i] = sc == 0.0f ? 0 : oracle_i8_from_double(bf16_value(xr[i]), sc);
+    }
+}
+
+/* Attention over an INT8 K/V cache, the definition written out:
+ *
+ *   z_j = scale_softmax * sum_i q_i * (kc[j][i] * ks[j])
+ *   out = sum_j softmax_j(z) * (vc[j][:] * vs[j])
+ *
+ * kc [B][*][d_qk] and vc [B][*][d_v] int8 codes with batch strides skc_b, svc_b
+ * elements; ks, vs [B][*] fp32 with batch strides sks_b, svs_b. */
+void oracle_sparse_attn_i8kv(const uint16_t *q, const int8_t *kc, int64_t skc_b,
+                             const float *ks, int64_t sks_b, const int8_t *vc, int64_t svc_b,
+                             const float *vs, int64_t svs_b, const int32_t *seq_len,
+                             const int32_t *idx, int B, int T, int H_q, int d_qk, int d_v,
+                             int P, int k, double scale, uint16_t *out, float *lse)
+{
+    const int64_t cap = (int64_t)k * P > 0 ? (int64_t)k * P : 1;
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)cap);
+    double *zs = (double *)malloc(sizeof(double) * (size_t)cap);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)d_v);
+    for (int b = 0; b < B; ++b) {
+        const int64_t n_groups = seq_len[b] / P;
+        for (int t = 0; t < T; ++t) {
+            const int32_t *chosen = idx + ((int64_t)b * T + t) * k;
+            int64_t nt = 0;  /* the tokens of the chosen complete groups */
+            for (int s = 0; s < k; ++s) {
+                if (chosen[s] < 0 || chosen[s] >= n_groups)
+                    continue;
+                for (int i = 0; i < P; ++i)
+                    rows[nt++] = (int64_t)chosen[s] * P + i;
+            }
+            for (int h = 0; h < H_q; ++h) {
+                const int64_t row = ((int64_t)b * T + t) * H_q + h;
+                const uint16_t *qv = q + row * d_qk;
+                uint16_t *ov = out + row * d_v;
+                if (nt == 0) {
+                    for (int i = 0; i < d_v; ++i)
+                        ov[i] = 0;
+                    if (lse)
+                        lse[row] = -INFINITY;
+                    continue;
+                }
+                double zmax = -INFINITY;
+                for (int64_t j = 0; j < nt; ++j) {
+                    const int8_t *kr = kc + b * skc_b + rows[j] * d_qk;
+                    const float kscale = ks[b * sks_b + rows[j]];
+                    double qk = 0.0;
+                    for (int i = 0; i < d_qk; ++i)
+                        qk += bf16_value(qv[i]) * oracle_i8_value(kr[i], kscale);
+                    zs[j] = scale * qk;
+                    zmax = zs[j] > zmax ? zs[j] : zmax;
+                }
+                double denom = 0.0;
+                for (int i = 0; i < d_v; ++i)
+                    acc[i] = 0.0;
+                for (int64_t j = 0; j < nt; ++j) {
+                    const double wj = exp(zs[j] - zmax);
+                    denom += wj;
+                    const int8_t *vr = vc + b * svc_b + rows[j] * d_v;
+                    const float vscale = vs[b * svs_b + rows[j]];
+                    for (int i = 0; i < d_v; ++i)
+                        acc[i] += wj * oracle_i8_value(vr[i], vscale);
+                }
+                for (int i = 0; i < d_v; ++i)
+                    ov[i] = oracle_bf16_from_double(acc[i] / denom);
+                if (lse)
+                    lse[row] = (float)(zmax + log(denom));
+            }
+        }
+    }
+    free(acc);
+    free(zs);
+    free(rows);
+}

@@ -183,3 +183,119 @@ def test_kv8_scales_belong_to_their_own_cache():
     o1, _ = oracle.sparse_attn_e4m3kv(q, kc, ks, vc, vs, seq, idx, 4, 0.25)
     o2, _ = oracle.sparse_attn_e4m3kv(q, kc, vs, vc, ks, seq, idx, 4, 0.25)
     assert not np.array_equal(o1, o2)
+
+
+# ------------------------------------------------------------- INT8 K/V ---
+# Reading: symmetric codes in [-127, 127], one fp32 scale per row = amax / 127,
+# code = nearest integer to x / scale with ties to the even integer.
+
+def _i8_exact(x, scale):
+    """The nearest integer to x / scale from exact rationals (ties to even)."""
+    from fractions import Fraction
+    r = Fraction(x) / Fraction(scale)
+    n = int(r)  # toward zero
+    if r < 0:
+        n, frac = -int(-r), -r - int(-r)
+    else:
+        frac = r - n
+    if frac > Fraction(1, 2) or (frac == Fraction(1, 2) and abs(n) % 2 == 1):
+        n += 1 if r >= 0 else -1
+    return max(-127, min(127, n))
+
+
+def test_i8_hand_encodings_at_unit_scale():
+    """scale 1 (amax 127): codes are the rounded values themselves."""
+    cases = [(2.5, 2), (3.5, 4), (-2.5, -2), (-3.5, -4), (0.5, 0), (1.5, 2), (126.5, 126),
+             (127.0, 127), (-127.0, -127), (0.0, 0), (-0.25, 0), (7.75, 8)]
+    for x, c in cases:
+        assert oracle.i8_from_double(x, 1.0) == c, (x, c)
+
+
+def test_i8_quantizer_matches_exact_rationals():
+    rng = np.random.default_rng(410)
+    x = synth.bf16_bits((rng.standard_normal((40, 24)) * 10.0 ** rng.integers(-3, 3, (40, 1)))
+                        .astype(np.float32))
+    code, scale = oracle.quantize_rows_i8(x)
+    xf = synth.bf16_to_f32(x).astype(np.float64)
+    from fractions import Fraction
+    for r in range(x.shape[0]):
+        amax = Fraction(float(np.abs(xf[r]).max())) / 127
+        # the fp32 nearest to amax / 127: one of the two fp32 values around the double
+        d = float(amax)
+        cands = [np.float32(d), np.nextafter(np.float32(d), np.float32(np.inf)),
+                 np.nextafter(np.float32(d), np.float32(-np.inf))]
+        best = min(cands, key=lambda c: abs(Fraction(float(c)) - amax))
+        assert scale[r] == best
+        for i in range(x.shape[1]):
+            assert code[r, i] == _i8_exact(float(xf[r, i]), float(scale[r])), (r, i)
+
+
+def test_i8_rows_bounds():
+    x = synth.bf16_bits(np.array([[0.0] * 8, [3.0, -6.0, 1.0, 0.0, 5.0, -1.0, 2.0, 6.0]],
+                                 np.float32))
+    code, scale = oracle.quantize_rows_i8(x)
+    assert scale[0] == 0.0 and (code[0] == 0).all()  # zero row
+    assert abs(int(code[1, 1])) == 127 and abs(int(code[1, 7])) == 127  # the amax elements
+    assert code[1, 1] == -127 and code[1, 7] == 127
+    assert np.float32(scale[1]) == np.float32(6.0 / 127.0)
+
+
+def _i8_case(seed, B=2, L=96, H_q=4, d_qk=16, d_v=8, k=10, P=4):
+    rng = np.random.default_rng(seed)
+    kc = rng.integers(-127, 128, (B, L, d_qk)).astype(np.int8)
+    vc = rng.integers(-127, 128, (B, L, d_v)).astype(np.int8)
+    ks = rng.uniform(0.001, 0.02, (B, L)).astype(np.float32)
+    vs = rng.uniform(0.001, 0.02, (B, L)).astype(np.float32)
+    q = synth.bf16_bits(rng.standard_normal((B, 1, H_q, d_qk)).astype(np.float32))
+    seq = np.array([L, L - 13], np.int32)[:B]
+    idx = np.full((B, 1, k), -1, np.int32)
+    for b in range(B):
+        G = int(seq[b]) // P
+        idx[b, 0, :k - 2] = np.sort(rng.choice(G, k - 2, replace=False))
+        idx[b, 0, k - 2] = G + 1  # past the sequence: skipped
+    return q, kc, ks, vc, vs, seq, idx
+
+
+def test_i8kv_unit_scales_equal_the_bf16_oracle():
+    """Scales 1 and codes that bf16 holds exactly (|c| <= 127 < 256): the INT8
+    attention must equal the bf16 oracle on the integer-valued caches."""
+    q, kc, ks, vc, vs, seq, idx = _i8_case(420)
+    one_k, one_v = np.ones_like(ks), np.ones_like(vs)
+    o8, l8 = oracle.sparse_attn_i8kv(q, kc, one_k, vc, one_v, seq, idx, 4, 0.01)
+    Kb = synth.bf16_bits(kc.astype(np.float32))
+    Vb = synth.bf16_bits(vc.astype(np.float32))
+    ob, lb = oracle.sparse_attn(q, Kb, Vb, seq, idx, 4, 0.01)
+    assert np.array_equal(o8, ob)
+    assert np.array_equal(l8, lb)
+
+
+def test_i8kv_brute_force_softmax():
+    from scipy.special import logsumexp
+    q, kc, ks, vc, vs, seq, idx = _i8_case(421)
+    o8, l8 = oracle.sparse_attn_i8kv(q, kc, ks, vc, vs, seq, idx, 4, 0.3)
+    Kf = kc.astype(np.float64) * ks[..., None].astype(np.float64)
+    Vf = vc.astype(np.float64) * vs[..., None].astype(np.float64)
+    qf = synth.bf16_to_f32(q).astype(np.float64)
+    for b in range(q.shape[0]):
+        G = int(seq[b]) // 4
+        toks = [4 * g + i for g in idx[b, 0] if 0 <= g < G for i in range(4)]
+        z = 0.3 * qf[b, 0] @ Kf[b, toks].T
+        lse = logsumexp(z, axis=1)
+        out = np.exp(z - lse[:, None]) @ Vf[b, toks]
+        np.testing.assert_allclose(l8[b, 0], lse, rtol=1e-6)
+        ref_bits = np.array([[oracle.bf16_from_double(x) for x in row] for row in out])
+        assert np.array_equal(o8[b, 0], ref_bits)
+
+
+def test_i8kv_power_of_two_rescaling():
+    """Doubling every value scale doubles the output exactly; doubling every
+    key scale while halving the softmax scale leaves the result unchanged."""
+    q, kc, ks, vc, vs, seq, idx = _i8_case(422)
+    o1, l1 = oracle.sparse_attn_i8kv(q, kc, ks, vc, vs, seq, idx, 4, 0.25)
+    o2, l2 = oracle.sparse_attn_i8kv(q, kc, ks, vc, vs * 2, seq, idx, 4, 0.25)
+    assert np.array_equal(synth.bf16_to_f32(o2), 2 * synth.bf16_to_f32(o1))
+    assert np.array_equal(l1, l2)
+    o3, l3 = oracle.sparse_attn_i8kv(q, kc, ks * 2, vc, vs, seq, idx, 4, 0.125)
+    assert np.array_equal(o3, o1) and np.array_equal(l3, l1)
+    o4, _ = oracle.sparse_attn_i8kv(q, kc, vs, vc, ks, seq, idx, 4, 0.25)
+    assert not np.array_equal(o4, o1)

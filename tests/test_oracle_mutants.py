@@ -41,8 +41,20 @@ MUTANTS = {
 }
 
 
-# the FP8 leg (e4m3 codes, per-row scales, FP8 score), caught by test_oracle_fp8
+# the quantized legs (e4m3 and INT8 codes, per-row scales, FP8 score, FP8 and
+# INT8 K/V attention), caught by test_oracle_fp8
 FP8_MUTANTS = {
+    "i8_ties_to_odd": ("(d == bd && c % 2 == 0)", "(d == bd && c % 2 == 1)"),
+    "i8_scale_divisor": ("const float sc = (float)(amax / 127.0);",
+                         "const float sc = (float)(amax / 128.0);"),
+    "i8_sign_lost": ("return (int8_t)(x < 0.0 ? -best : best);", "return (int8_t)best;"),
+    "i8kv_value_scale_dropped": ("acc[i] += wj * oracle_i8_value(vr[i], vscale);",
+                                 "acc[i] += wj * oracle_i8_value(vr[i], 1.0f);"),
+    "i8kv_key_scale_dropped": ("qk += bf16_value(qv[i]) * oracle_i8_value(kr[i], kscale);",
+                               "qk += bf16_value(qv[i]) * oracle_i8_value(kr[i], 1.0f);"),
+    "i8kv_unnormalised": ("ov[i] = oracle_bf16_from_double(acc[i] / denom);",
+                          "ov[i] = oracle_bf16_from_double(acc[i]);"),
+    "i8kv_no_softmax_scale": ("zs[j] = scale * qk;", "zs[j] = qk;"),
     "e4m3_exponent_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
     "e4m3_ties_to_odd": ("(d == bd && (c & 1) == 0)", "(d == bd && (c & 1) == 1)"),
     "e4m3_no_saturation": ("if (a >= 448.0) return sign | 0x7E;",
