@@ -58,13 +58,16 @@ def parse():
     ap.add_argument("--kernel", default=None,
                     choices=["prefill_scores", "prefill", "pool_keys", "index_scores", "topk",
                              "sparse_attn", "decode", "decode_fp8", "kda", "reuse", "mla", "kv8",
-                             "mla_decode"],
+                             "kvi8", "mla_decode"],
                     help="time one kernel of the path instead of the decode step (not the "
                          "headline line): prefill_scores = the chunked-prefill indexer "
                          "scores (tcgen05 GEMM) on the prefill_4k shapes; prefill = one whole "
                          "lcsw_prefill chunk of prefill_4k (pool, fused selection, attention); "
                          "pool_keys / index_scores / topk / sparse_attn = one standalone step on "
-                         "the decode_1m shapes; decode / decode_fp8 = single fused decode calls")
+                         "the decode_1m shapes; decode / decode_fp8 = single fused decode "
+                         "calls; kda / reuse / mla / kv8 / kvi8 / mla_decode = the KDA step, "
+                         "the IndexCache reuse layer, the MLA attention, the FP8 and INT8 K/V "
+                         "attention and the MLA decode step")
     return ap.parse_args()
 
 
@@ -1102,11 +1105,12 @@ def measure_mla_decode(torch, lcsw, peak, with_oracle):
             "parity_vs_oracle": parity}
 
 
-def measure_kv8(torch, lcsw, peak):
-    """decode_1m's attention with an FP8 K/V cache (lcsw_sparse_attn_kv8): 64
-    heads over 512 seeded groups of the 1,048,576-token cache quantized on the
-    device, each call after a write of twice the L2 size; the bf16 split-K call
-    on the same selection is timed beside it."""
+def measure_kv8(torch, lcsw, peak, fmt="e4m3"):
+    """decode_1m's attention with an FP8 (fmt "e4m3", lcsw_sparse_attn_kv8) or
+    INT8 (fmt "i8", lcsw_sparse_attn_kvi8) K/V cache: 64 heads over 512 seeded
+    groups of the 1,048,576-token cache quantized on the device, each call
+    after a write of twice the L2 size; the bf16 split-K call on the same
+    selection is timed beside it."""
     spec = synth.named("decode_1m")
     c = synth.generate(spec)
     dev = "cuda"
@@ -1118,8 +1122,10 @@ def measure_kv8(torch, lcsw, peak):
                            .reshape(1, 1, spec.k)).to(dev)
     q, K, V = up16(c["q"]), up16(c["K"]), up16(c["V"])
     seq = torch.from_numpy(c["seq_len"]).to(dev)
-    kc, ks = lcsw.quantize_rows_e4m3(K)
-    vc, vs = lcsw.quantize_rows_e4m3(V)
+    quant = lcsw.quantize_rows_i8 if fmt == "i8" else lcsw.quantize_rows_e4m3
+    attn = lcsw.sparse_attn_kvi8 if fmt == "i8" else lcsw.sparse_attn_kv8
+    kc, ks = quant(K)
+    vc, vs = quant(V)
     out = torch.empty(1, 1, spec.H_q, spec.d_v, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(1, 1, spec.H_q, dtype=torch.float32, device=dev)
     nb8 = lcsw.lib().lcsw_sparse_attn_kv8_workspace_size(1, 1, spec.H_q, spec.d_v, spec.k,
@@ -1127,8 +1133,7 @@ def measure_kv8(torch, lcsw, peak):
     ws8 = torch.empty(max(nb8, 16), dtype=torch.uint8, device=dev)
     nb16 = lcsw.lib().lcsw_sparse_attn_workspace_size(1, 1, spec.H_q, spec.d_v, spec.k, spec.P)
     ws16 = torch.empty(max(nb16, 16), dtype=torch.uint8, device=dev)
-    f8 = lambda: lcsw.sparse_attn_kv8(q, kc, ks, vc, vs, seq, idx, spec.P, c["scale"], out=out,
-                                      lse=lse, ws=ws8)
+    f8 = lambda: attn(q, kc, ks, vc, vs, seq, idx, spec.P, c["scale"], out=out, lse=lse, ws=ws8)
     f16 = lambda: lcsw.sparse_attn(q, K, V, seq, idx, spec.P, c["scale"], out=out, lse=lse,
                                    ws=ws16)
     flush = torch.empty(2 * l2_bytes() // 4, dtype=torch.float32, device=dev)
@@ -1153,14 +1158,16 @@ def measure_kv8(torch, lcsw, peak):
     gbs = ab8 / (ms8 / 1e3) / 1e9
     del q, K, V, kc, vc, flush
     torch.cuda.empty_cache()
-    return {"kernel": "lcsw_sparse_attn_kv8 (split-K over E4M3 codes + merge)",
+    return {"kernel": ("lcsw_sparse_attn_kvi8 (split-K over INT8 codes + merge)" if fmt == "i8"
+                       else "lcsw_sparse_attn_kv8 (split-K over E4M3 codes + merge)"),
             "ms_per_call": round(ms8, 5), "bf16_cache_ms_per_call": round(ms16, 5),
             "alg_bytes": ab8, "timing": "median of 200 calls, each after a write of 2x L2",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4),
-                         "traffic": profiled_traffic("sparse_attn_kv8_decode_1m.md",
-                                                     ["sparse_attn_kv8.cu", "attn_core.cuh",
-                                                      "e4m3_core.cuh", "common.cuh"])}}
+                         "traffic": None if fmt == "i8" else profiled_traffic(
+                             "sparse_attn_kv8_decode_1m.md",
+                             ["sparse_attn_kv8.cu", "attn_core.cuh", "e4m3_core.cuh",
+                              "common.cuh"])}}
 
 
 def kda_alg_bytes(B, T, H, D):
@@ -1276,6 +1283,7 @@ def per_config(args, torch, lcsw, peak, peaks):
     res["kda_decode_b64"] = measure_kda(torch, lcsw, peak, 200, 5, oracle_on)
     res["mla_attn_decode_1m"] = measure_mla(torch, lcsw, peak, oracle_on)
     res["kv8_attn_decode_1m"] = measure_kv8(torch, lcsw, peak)
+    res["kvi8_attn_decode_1m"] = measure_kv8(torch, lcsw, peak, fmt="i8")
     res["mla_decode_1m"] = measure_mla_decode(torch, lcsw, peak, oracle_on)
     return res
 
@@ -1387,14 +1395,15 @@ def main():
         e = measure_mla_decode(torch, lcsw, peaks.get("hbm_gbs", 6400.0), True)
         print(json.dumps({"kernel": "mla_decode", **e}))
         return
-    if args.kernel == "kv8":
+    if args.kernel in ("kv8", "kvi8"):
         import torch
 
         import long_context_sparse_weighted_b300 as lcsw
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
             os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
-        e = measure_kv8(torch, lcsw, peaks.get("hbm_gbs", 6400.0))
-        print(json.dumps({"kernel": "kv8", **e}))
+        e = measure_kv8(torch, lcsw, peaks.get("hbm_gbs", 6400.0),
+                        fmt="i8" if args.kernel == "kvi8" else "e4m3")
+        print(json.dumps({"kernel": args.kernel, **e}))
         return
     if args.kernel == "mla":
         import torch

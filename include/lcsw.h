@@ -210,6 +210,31 @@ lcsw_status lcsw_sparse_attn_kv8(const lcsw_bf16 *q, const uint8_t *kc, int64_t 
                                  lcsw_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * INT8 K/V cache: the INT8 tier of the same serving stack ("The serving
+ * stack"; no format given).  Reading: symmetric codes in [-127, 127], one
+ * fp32 scale per token row = amax / 127 (0 for an all-zero row, whose codes
+ * are 0), code_i = the integer nearest to x_i / scale, ties to the even
+ * integer; the rounding is exact.
+ *
+ * lcsw_quantize_rows_i8: as lcsw_quantize_rows_e4m3 (same row window, layout,
+ * strides and alignment), int8 codes.
+ *
+ * lcsw_sparse_attn_kvi8: as lcsw_sparse_attn_kv8 with element values
+ * kc[b][j][i] * ks[b][j] and vc[b][j][i] * vs[b][j]; the workspace is
+ * lcsw_sparse_attn_kv8_workspace_size bytes, 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_quantize_rows_i8(const lcsw_bf16 *x, int64_t sx_b, const int32_t *row_begin,
+                                  int B, int n_rows, int width, int8_t *codes, int64_t sc_b,
+                                  float *scales, int64_t ss_b, lcsw_stream stream);
+lcsw_status lcsw_sparse_attn_kvi8(const lcsw_bf16 *q, const int8_t *kc, int64_t skc_b,
+                                  const float *ks, int64_t sks_b, const int8_t *vc,
+                                  int64_t svc_b, const float *vs, int64_t svs_b,
+                                  const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                  int H_q, int d_qk, int d_v, int P, int k, float scale,
+                                  lcsw_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                  lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
  * Sparse attention in the MLA latent geometry ("G2C Brief -- GLM-5.3-Flash":
  * MLA rank 512 per token, kv_lora_rank 512; the DSA diagram's "MLA latent
  * cache (rank 512 per token)").  One cached row per token, shared by every

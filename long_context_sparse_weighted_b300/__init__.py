@@ -90,6 +90,11 @@ _SIGNATURES = {
     "lcsw_sparse_attn_kv8": ([_vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i32,
                               _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp],
                              _i32),
+    "lcsw_quantize_rows_i8": ([_vp, _i64, _vp, _i32, _i32, _i32, _vp, _i64, _vp, _i64, _vp],
+                              _i32),
+    "lcsw_sparse_attn_kvi8": ([_vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i32,
+                               _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp],
+                              _i32),
     "lcsw_sparse_attn_mla_workspace_size": ([_i32, _i32, _i32, _i32, _i32], _sz),
     "lcsw_sparse_attn_mla": ([_vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
                               _vp, _vp, _sz, _vp], _i32),
@@ -274,35 +279,45 @@ def sparse_attn(q, K, V, seq_len, idx, P, scale, out=None, lse=None, ws=None, st
     return out, lse
 
 
+def _quantize_rows(fn, dtype, x, codes, scales, row_begin, n_rows, stream):
+    _bf16(x, "x", 3)
+    B, L, W = x.shape
+    if codes is None:
+        codes = torch.zeros(B, L, W, dtype=dtype, device=x.device)
+    if scales is None:
+        scales = torch.zeros(B, L, dtype=torch.float32, device=x.device)
+    if n_rows is None:
+        n_rows = L
+    _check(fn(_ptr(x), x.stride(0), _ptr(row_begin), B, int(n_rows), W, _ptr(codes),
+              codes.stride(0), _ptr(scales), scales.stride(0), _stream(stream)))
+    return codes, scales
+
+
 def quantize_rows_e4m3(x, codes=None, scales=None, row_begin=None, n_rows=None, stream=None):
     """bf16 cache x [B][L][width] -> E4M3 codes [B][L][width] (uint8) and one
     fp32 scale per row [B][L] (lcsw_quantize_rows_e4m3).  With row_begin [B]
     (int32) and n_rows, only rows [row_begin[b], row_begin[b] + n_rows) of
     each sequence are written."""
-    _bf16(x, "x", 3)
-    B, L, W = x.shape
-    if codes is None:
-        codes = torch.zeros(B, L, W, dtype=torch.uint8, device=x.device)
-    if scales is None:
-        scales = torch.zeros(B, L, dtype=torch.float32, device=x.device)
-    if n_rows is None:
-        n_rows = L
-    _check(lib().lcsw_quantize_rows_e4m3(_ptr(x), x.stride(0), _ptr(row_begin), B, int(n_rows), W,
-                                         _ptr(codes), codes.stride(0), _ptr(scales),
-                                         scales.stride(0), _stream(stream)))
-    return codes, scales
+    return _quantize_rows(lib().lcsw_quantize_rows_e4m3, torch.uint8, x, codes, scales,
+                          row_begin, n_rows, stream)
 
 
-def sparse_attn_kv8(q, kc, ks, vc, vs, seq_len, idx, P, scale, out=None, lse=None, ws=None,
-                    stream=None):
-    """sparse_attn over an FP8 K/V cache (codes kc [B][L][d_qk], vc [B][L][d_v]
-    uint8; one fp32 scale per token row ks, vs [B][L])."""
+def quantize_rows_i8(x, codes=None, scales=None, row_begin=None, n_rows=None, stream=None):
+    """bf16 cache x [B][L][width] -> INT8 codes [B][L][width] (int8) and one
+    fp32 scale per row [B][L] (lcsw_quantize_rows_i8); the row window as in
+    quantize_rows_e4m3."""
+    return _quantize_rows(lib().lcsw_quantize_rows_i8, torch.int8, x, codes, scales, row_begin,
+                          n_rows, stream)
+
+
+def _quantized_kv_attn(fn, dtype, q, kc, ks, vc, vs, seq_len, idx, P, scale, out, lse, ws,
+                       stream):
     _bf16(q, "q", 4)
     _dense(idx, torch.int32, "idx")
     _dense(seq_len, torch.int32, "seq_len")
     for t, n in ((kc, "kc"), (vc, "vc")):
-        if t.dtype != torch.uint8 or not t.is_cuda or not t[0].is_contiguous():
-            raise ValueError(f"{n} must be CUDA uint8 [B][L][d], contiguous per sequence")
+        if t.dtype != dtype or not t.is_cuda or not t[0].is_contiguous():
+            raise ValueError(f"{n} must be CUDA {dtype} [B][L][d], contiguous per sequence")
     B, T, H_q, d_qk = q.shape
     d_v = vc.shape[2]
     k = idx.shape[-1]
@@ -313,12 +328,26 @@ def sparse_attn_kv8(q, kc, ks, vc, vs, seq_len, idx, P, scale, out=None, lse=Non
     nbytes = lib().lcsw_sparse_attn_kv8_workspace_size(B, T, H_q, d_v, k, P)
     if ws is None and nbytes:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    _check(lib().lcsw_sparse_attn_kv8(_ptr(q), _ptr(kc), kc.stride(0), _ptr(ks), ks.stride(0),
-                                      _ptr(vc), vc.stride(0), _ptr(vs), vs.stride(0),
-                                      _ptr(seq_len), _ptr(idx), B, T, H_q, d_qk, d_v, P, k,
-                                      float(scale), _ptr(out), _ptr(lse), _ptr(ws), nbytes,
-                                      _stream(stream)))
+    _check(fn(_ptr(q), _ptr(kc), kc.stride(0), _ptr(ks), ks.stride(0), _ptr(vc), vc.stride(0),
+              _ptr(vs), vs.stride(0), _ptr(seq_len), _ptr(idx), B, T, H_q, d_qk, d_v, P, k,
+              float(scale), _ptr(out), _ptr(lse), _ptr(ws), nbytes, _stream(stream)))
     return out, lse
+
+
+def sparse_attn_kv8(q, kc, ks, vc, vs, seq_len, idx, P, scale, out=None, lse=None, ws=None,
+                    stream=None):
+    """sparse_attn over an FP8 K/V cache (codes kc [B][L][d_qk], vc [B][L][d_v]
+    uint8; one fp32 scale per token row ks, vs [B][L])."""
+    return _quantized_kv_attn(lib().lcsw_sparse_attn_kv8, torch.uint8, q, kc, ks, vc, vs, seq_len,
+                              idx, P, scale, out, lse, ws, stream)
+
+
+def sparse_attn_kvi8(q, kc, ks, vc, vs, seq_len, idx, P, scale, out=None, lse=None, ws=None,
+                     stream=None):
+    """sparse_attn over an INT8 K/V cache (codes kc [B][L][d_qk], vc [B][L][d_v]
+    int8; one fp32 scale per token row ks, vs [B][L])."""
+    return _quantized_kv_attn(lib().lcsw_sparse_attn_kvi8, torch.int8, q, kc, ks, vc, vs, seq_len,
+                              idx, P, scale, out, lse, ws, stream)
 
 
 MLA_DQK, MLA_DV = 576, 512  # latent 512 + rotary 64; the latent is the value

@@ -33,6 +33,11 @@ cudaError_t launch_kda_step(const uint16_t *qkv, const uint16_t *conv_w, uint16_
 cudaError_t launch_quantize_rows_e4m3(const uint16_t *x, int64_t sx_b, const int32_t *row_begin,
                                       int n_rows, int width, int B, uint8_t *codes, int64_t sc_b,
                                       float *scales, int64_t ss_b, cudaStream_t st);
+// INT8 K/V cache rows, as launch_quantize_rows_e4m3: int8 codes (symmetric,
+// scale amax / 127 per row).
+cudaError_t launch_quantize_rows_i8(const uint16_t *x, int64_t sx_b, const int32_t *row_begin,
+                                    int n_rows, int width, int B, int8_t *codes, int64_t sc_b,
+                                    float *scales, int64_t ss_b, cudaStream_t st);
 
 // q_pos[b][t] = seq_len[b] - T + t (the chunk's absolute positions).
 cudaError_t launch_prefill_positions(const int32_t *seq_len, int B, int T, int32_t *q_pos,
@@ -114,7 +119,8 @@ cudaError_t launch_sparse_attn_tc(const uint16_t *q, const uint16_t *K, int64_t 
 int sparse_attn_splits(int64_t rows, int H_q, int k, int P);
 // The same attention over an FP8 (E4M3) K/V cache with one fp32 scale per
 // token row (sparse_attn_kv8.cu): codes kc [B][*][d_qk], vc [B][*][d_v]
-// (batch strides in bytes), scales ks, vs [B][*] (strides in elements).
+// (batch strides in bytes), scales ks, vs [B][*] (strides in elements); with
+// int8_codes the codes are INT8 (i8_core.cuh) instead.
 int sparse_attn_kv8_splits(int64_t rows, int H_q, int k, int P);
 size_t sparse_attn_kv8_ws_bytes(int64_t rows, int H_q, int d_v, int k, int P);
 cudaError_t launch_sparse_attn_kv8(const uint16_t *q, const uint8_t *kc, int64_t skc_b,
@@ -122,7 +128,8 @@ cudaError_t launch_sparse_attn_kv8(const uint16_t *q, const uint8_t *kc, int64_t
                                    int64_t svc_b, const float *vs, int64_t svs_b,
                                    const int32_t *seq_len, const int32_t *idx, int B, int T,
                                    int H_q, int d_qk, int d_v, int P, int k, float scale,
-                                   uint16_t *out, float *lse, void *ws, cudaStream_t st);
+                                   uint16_t *out, float *lse, void *ws, bool int8_codes,
+                                   cudaStream_t st);
 // MLA latent geometry (sparse_attn_mla.cu): rows of 576 = latent 512 + rotary
 // 64, the latent doubling as the value; out rows of 512.
 int sparse_attn_mla_splits(int64_t rows, int H_q, int k, int P);

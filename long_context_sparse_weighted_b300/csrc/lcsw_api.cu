@@ -678,10 +678,10 @@ lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
     return cuda_status(e, "prefill attention");
 }
 
-lcsw_status lcsw_quantize_rows_e4m3(const lcsw_bf16 *x, int64_t sx_b, const int32_t *row_begin,
-                                    int B, int n_rows, int width, uint8_t *codes, int64_t sc_b,
-                                    float *scales, int64_t ss_b, lcsw_stream stream) {
-    LCSW_RANGE("lcsw_quantize_rows_e4m3");
+// argument checks shared by the FP8 and INT8 row quantizers
+static lcsw_status quantize_rows_args(const lcsw_bf16 *x, int64_t sx_b, const int32_t *row_begin,
+                                      int B, int n_rows, int width, const void *codes,
+                                      int64_t sc_b, const float *scales, int64_t ss_b) {
     CHECK(B >= 0 && n_rows >= 0 && width > 0, "bad dimension");
     CHECK(width % 16 == 0, "width must be a multiple of 16");
     if (B == 0 || n_rows == 0) return LCSW_OK;
@@ -690,10 +690,32 @@ lcsw_status lcsw_quantize_rows_e4m3(const lcsw_bf16 *x, int64_t sx_b, const int3
               aligned(scales, 4) && (!row_begin || aligned(row_begin, 4)),
           "misaligned argument (x rows 16-byte aligned, codes and their stride 16 bytes)");
     CHECK(sx_b >= 0 && sc_b >= 0 && ss_b >= 0, "strides must be >= 0");
+    return LCSW_OK;
+}
+
+lcsw_status lcsw_quantize_rows_e4m3(const lcsw_bf16 *x, int64_t sx_b, const int32_t *row_begin,
+                                    int B, int n_rows, int width, uint8_t *codes, int64_t sc_b,
+                                    float *scales, int64_t ss_b, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_quantize_rows_e4m3");
+    const lcsw_status a = quantize_rows_args(x, sx_b, row_begin, B, n_rows, width, codes, sc_b,
+                                             scales, ss_b);
+    if (a != LCSW_OK || B == 0 || n_rows == 0) return a;
     return cuda_status(lcsw::launch_quantize_rows_e4m3(x, sx_b, row_begin, n_rows, width, B,
                                                        codes, sc_b, scales, ss_b,
                                                        (cudaStream_t)stream),
                        "quantize rows launch");
+}
+
+lcsw_status lcsw_quantize_rows_i8(const lcsw_bf16 *x, int64_t sx_b, const int32_t *row_begin,
+                                  int B, int n_rows, int width, int8_t *codes, int64_t sc_b,
+                                  float *scales, int64_t ss_b, lcsw_stream stream) {
+    LCSW_RANGE("lcsw_quantize_rows_i8");
+    const lcsw_status a = quantize_rows_args(x, sx_b, row_begin, B, n_rows, width, codes, sc_b,
+                                             scales, ss_b);
+    if (a != LCSW_OK || B == 0 || n_rows == 0) return a;
+    return cuda_status(lcsw::launch_quantize_rows_i8(x, sx_b, row_begin, n_rows, width, B, codes,
+                                                     sc_b, scales, ss_b, (cudaStream_t)stream),
+                       "INT8 quantize rows launch");
 }
 
 size_t lcsw_sparse_attn_kv8_workspace_size(int B, int T, int H_q, int d_v, int k, int P) {
@@ -701,14 +723,14 @@ size_t lcsw_sparse_attn_kv8_workspace_size(int B, int T, int H_q, int d_v, int k
     return lcsw::sparse_attn_kv8_ws_bytes(int64_t(B) * T, H_q, d_v, k, P);
 }
 
-lcsw_status lcsw_sparse_attn_kv8(const lcsw_bf16 *q, const uint8_t *kc, int64_t skc_b,
-                                 const float *ks, int64_t sks_b, const uint8_t *vc,
-                                 int64_t svc_b, const float *vs, int64_t svs_b,
-                                 const int32_t *seq_len, const int32_t *idx, int B, int T,
-                                 int H_q, int d_qk, int d_v, int P, int k, float scale,
-                                 lcsw_bf16 *out, float *lse, void *ws, size_t ws_bytes,
-                                 lcsw_stream stream) {
-    LCSW_RANGE("lcsw_sparse_attn_kv8");
+// the FP8 and INT8 K/V attention entries: the same checks and kernel
+static lcsw_status quantized_kv_attn(const lcsw_bf16 *q, const uint8_t *kc, int64_t skc_b,
+                                     const float *ks, int64_t sks_b, const uint8_t *vc,
+                                     int64_t svc_b, const float *vs, int64_t svs_b,
+                                     const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                     int H_q, int d_qk, int d_v, int P, int k, float scale,
+                                     lcsw_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                     bool int8_codes, lcsw_stream stream) {
     CHECK(B >= 0 && T >= 0, "negative dimension");
     CHECK(p_ok(P), "P must be 1, 2, 4 or 8");
     CHECK(k >= 1, "k must be >= 1");
@@ -725,12 +747,39 @@ lcsw_status lcsw_sparse_attn_kv8(const lcsw_bf16 *q, const uint8_t *kc, int64_t 
     CHECK(skc_b >= 0 && svc_b >= 0 && sks_b >= 0 && svs_b >= 0, "strides must be >= 0");
     const size_t need = lcsw::sparse_attn_kv8_ws_bytes(rows, H_q, d_v, k, P);
     if (need && (!ws || ws_bytes < need || !aligned(ws, 16)))
-        return fail(LCSW_ERR_WORKSPACE, "FP8 K/V attention needs a 16-byte aligned workspace "
-                    "of %zu bytes", need);
+        return fail(LCSW_ERR_WORKSPACE, "%s K/V attention needs a 16-byte aligned workspace "
+                    "of %zu bytes", int8_codes ? "INT8" : "FP8", need);
     return cuda_status(lcsw::launch_sparse_attn_kv8(q, kc, skc_b, ks, sks_b, vc, svc_b, vs, svs_b,
                                                     seq_len, idx, B, T, H_q, d_qk, d_v, P, k,
-                                                    scale, out, lse, ws, (cudaStream_t)stream),
-                       "FP8 K/V attention launch");
+                                                    scale, out, lse, ws, int8_codes,
+                                                    (cudaStream_t)stream),
+                       "quantized K/V attention launch");
+}
+
+lcsw_status lcsw_sparse_attn_kv8(const lcsw_bf16 *q, const uint8_t *kc, int64_t skc_b,
+                                 const float *ks, int64_t sks_b, const uint8_t *vc,
+                                 int64_t svc_b, const float *vs, int64_t svs_b,
+                                 const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                 int H_q, int d_qk, int d_v, int P, int k, float scale,
+                                 lcsw_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                 lcsw_stream stream) {
+    LCSW_RANGE("lcsw_sparse_attn_kv8");
+    return quantized_kv_attn(q, kc, skc_b, ks, sks_b, vc, svc_b, vs, svs_b, seq_len, idx, B, T,
+                             H_q, d_qk, d_v, P, k, scale, out, lse, ws, ws_bytes, false, stream);
+}
+
+lcsw_status lcsw_sparse_attn_kvi8(const lcsw_bf16 *q, const int8_t *kc, int64_t skc_b,
+                                  const float *ks, int64_t sks_b, const int8_t *vc,
+                                  int64_t svc_b, const float *vs, int64_t svs_b,
+                                  const int32_t *seq_len, const int32_t *idx, int B, int T,
+                                  int H_q, int d_qk, int d_v, int P, int k, float scale,
+                                  lcsw_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                  lcsw_stream stream) {
+    LCSW_RANGE("lcsw_sparse_attn_kvi8");
+    return quantized_kv_attn(q, reinterpret_cast<const uint8_t *>(kc), skc_b, ks, sks_b,
+                             reinterpret_cast<const uint8_t *>(vc), svc_b, vs, svs_b, seq_len,
+                             idx, B, T, H_q, d_qk, d_v, P, k, scale, out, lse, ws, ws_bytes, true,
+                             stream);
 }
 
 size_t lcsw_sparse_attn_mla_workspace_size(int B, int T, int H_q, int k, int P) {

@@ -13,9 +13,14 @@
 // while the next chunk's codes are in flight.  The scores of a token are then
 // multiplied by its key scale, and its softmax weight by its value scale in
 // the P V product (attn_core.cuh), so neither scale is rounded into the tiles.
+//
+// The INT8 tier (I8 = true, i8_core.cuh) runs the same kernel: its codes are
+// integers in [-127, 127], which bf16 also holds exactly, with one fp32 scale
+// per token row (amax / 127).
 #include "attn_core.cuh"
 #include "common.cuh"
 #include "e4m3_core.cuh"
+#include "i8_core.cuh"
 #include "kernels.cuh"
 
 namespace lcsw {
@@ -93,8 +98,15 @@ __device__ __forceinline__ void gather_codes(unsigned char *sb, int *sg, const i
     cp_async_commit();
 }
 
+// Four codes (one word) -> four bf16 values, exactly.
+template <bool I8>
+__device__ __forceinline__ uint2 widen4(uint32_t w) {
+    if constexpr (I8) return i8x4_bf16x4(w);
+    else return make_uint2(e4m3x2_bf16x2(w), e4m3x2_bf16x2(w >> 16));
+}
+
 // Codes of staging buffer `sb` -> bf16 K and V tiles (row pitches QP, VP).
-template <int DQK, int DV>
+template <int DQK, int DV, bool I8>
 __device__ __forceinline__ void widen_codes(const unsigned char *sb, uint16_t *sk, uint16_t *sv,
                                             int QP, int VP) {
     const uint8_t *kc = sb;
@@ -102,18 +114,16 @@ __device__ __forceinline__ void widen_codes(const unsigned char *sb, uint16_t *s
     for (int e = threadIdx.x; e < kChunk * (DQK / 4); e += kThr8) {
         const int tr = e / (DQK / 4), c4 = e % (DQK / 4);
         const uint32_t w = *reinterpret_cast<const uint32_t *>(kc + tr * DQK + c4 * 4);
-        *reinterpret_cast<uint2 *>(sk + tr * QP + c4 * 4) =
-            make_uint2(e4m3x2_bf16x2(w), e4m3x2_bf16x2(w >> 16));
+        *reinterpret_cast<uint2 *>(sk + tr * QP + c4 * 4) = widen4<I8>(w);
     }
     for (int e = threadIdx.x; e < kChunk * (DV / 4); e += kThr8) {
         const int tr = e / (DV / 4), c4 = e % (DV / 4);
         const uint32_t w = *reinterpret_cast<const uint32_t *>(vc + tr * DV + c4 * 4);
-        *reinterpret_cast<uint2 *>(sv + tr * VP + c4 * 4) =
-            make_uint2(e4m3x2_bf16x2(w), e4m3x2_bf16x2(w >> 16));
+        *reinterpret_cast<uint2 *>(sv + tr * VP + c4 * 4) = widen4<I8>(w);
     }
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool I8>
 __global__ void __launch_bounds__(kThr8) sparse_attn_kv8_kernel(
     const uint16_t *__restrict__ q, const uint8_t *__restrict__ kc, int64_t skc_b,
     const float *__restrict__ ks, int64_t sks_b, const uint8_t *__restrict__ vc, int64_t svc_b,
@@ -177,7 +187,7 @@ __global__ void __launch_bounds__(kThr8) sparse_attn_kv8_kernel(
         }
         __syncthreads();  // chunk ci's codes landed; every warp is done with the tiles
         const unsigned char *sb = stage + (ci & 1) * L::stage;
-        widen_codes<DQK, DV>(sb, sk, sv, L::QP, L::VP);
+        widen_codes<DQK, DV, I8>(sb, sk, sv, L::QP, L::VP);
         __syncthreads();
         const float *kscale = reinterpret_cast<const float *>(sb + kChunk * (DQK + DV));
         attn_chunk<DQK, DV>(st, qa, sk, sv, sgrp + (ci & 1) * kChunk, L::QP, L::VP, P, tok0,
@@ -205,7 +215,7 @@ __global__ void __launch_bounds__(kThr8) sparse_attn_kv8_kernel(
     }
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool I8>
 cudaError_t launch_kv8_typed(const uint16_t *q, const uint8_t *kc, int64_t skc_b, const float *ks,
                              int64_t sks_b, const uint8_t *vc, int64_t svc_b, const float *vs,
                              int64_t svs_b, const int32_t *seq_len, const int32_t *idx, int B,
@@ -215,7 +225,7 @@ cudaError_t launch_kv8_typed(const uint16_t *q, const uint8_t *kc, int64_t skc_b
     const int S = sparse_attn_kv8_splits(rows, H_q, k, P);
     const int HGs = (H_q + kHeadGroup8 - 1) / kHeadGroup8;
     using L = Kv8Smem<DQK, DV>;
-    auto kern = sparse_attn_kv8_kernel<DQK, DV>;
+    auto kern = sparse_attn_kv8_kernel<DQK, DV, I8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
     if (e != cudaSuccess) return e;
     float *part_o = reinterpret_cast<float *>(ws);
@@ -254,12 +264,18 @@ cudaError_t launch_sparse_attn_kv8(const uint16_t *q, const uint8_t *kc, int64_t
                                    int64_t svc_b, const float *vs, int64_t svs_b,
                                    const int32_t *seq_len, const int32_t *idx, int B, int T,
                                    int H_q, int d_qk, int d_v, int P, int k, float scale,
-                                   uint16_t *out, float *lse, void *ws, cudaStream_t st) {
+                                   uint16_t *out, float *lse, void *ws, bool int8_codes,
+                                   cudaStream_t st) {
     if (int64_t(B) * T == 0) return cudaSuccess;
 #define LCSW_KV8(DQ, DVV)                                                                     \
     if (d_qk == DQ && d_v == DVV)                                                            \
-        return launch_kv8_typed<DQ, DVV>(q, kc, skc_b, ks, sks_b, vc, svc_b, vs, svs_b, seq_len, \
-                                         idx, B, T, H_q, P, k, scale, out, lse, ws, st);
+        return int8_codes                                                                     \
+                   ? launch_kv8_typed<DQ, DVV, true>(q, kc, skc_b, ks, sks_b, vc, svc_b, vs,   \
+                                                     svs_b, seq_len, idx, B, T, H_q, P, k,    \
+                                                     scale, out, lse, ws, st)                 \
+                   : launch_kv8_typed<DQ, DVV, false>(q, kc, skc_b, ks, sks_b, vc, svc_b, vs,  \
+                                                      svs_b, seq_len, idx, B, T, H_q, P, k,   \
+                                                      scale, out, lse, ws, st);
     LCSW_KV8(64, 64)
     LCSW_KV8(128, 64)
     LCSW_KV8(128, 128)

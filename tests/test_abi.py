@@ -188,3 +188,27 @@ def test_kda_step_validates_arguments(L):
     bad = list(p)
     bad[5] = 0x60004                       # state not 16-byte aligned
     assert L.lcsw_kda_step(*bad, 2, 1, 64, 128, None) == lcsw.ERR_INVALID_ARG
+
+
+def test_int8_cache_entries_validate_arguments(L):
+    import long_context_sparse_weighted_b300 as lcsw
+    x, codes, scales = 0x10000, 0x20000, 0x30000
+    # width must be a multiple of 16; codes and their stride 16-byte aligned
+    assert L.lcsw_quantize_rows_i8(x, 24, None, 2, 3, 24, codes, 32, scales, 3, None) == \
+        lcsw.ERR_INVALID_ARG
+    assert L.lcsw_quantize_rows_i8(x, 64, None, 2, 3, 64, codes + 8, 64, scales, 3, None) == \
+        lcsw.ERR_INVALID_ARG
+    assert L.lcsw_quantize_rows_i8(x, 64, None, 2, 3, 64, None, 64, scales, 3, None) == \
+        lcsw.ERR_INVALID_ARG
+    assert L.lcsw_quantize_rows_i8(None, 64, None, 0, 3, 64, None, 64, None, 3, None) == lcsw.OK
+    p = [0x10000, 0x20000, 64 * 128, 0x30000, 64, 0x40000, 64 * 128, 0x50000, 64, 0x60000,
+         0x70000]
+    # an unsupported attention shape, then a missing workspace
+    assert L.lcsw_sparse_attn_kvi8(*p, 1, 1, 48, 128, 128, 4, 16, 0.1, 0x80000, None, None, 0,
+                                   None) == lcsw.ERR_INVALID_ARG
+    ws = L.lcsw_sparse_attn_kv8_workspace_size(1, 1, 64, 128, 512, 4)
+    if ws:
+        assert L.lcsw_sparse_attn_kvi8(*p, 1, 1, 64, 128, 128, 4, 512, 0.1, 0x80000, None, None,
+                                       0, None) == lcsw.ERR_WORKSPACE
+    assert L.lcsw_sparse_attn_kvi8(*p, 0, 1, 64, 128, 128, 4, 512, 0.1, 0x80000, None, None, 0,
+                                   None) == lcsw.OK

@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gpu_kernels.py", "tests/test_gpu_decode.py", "tests/test_gpu_reuse.py",
-          "tests/test_gpu_kda.py", "tests/test_gpu_mla.py", "tests/test_gpu_fp8.py"]
+          "tests/test_gpu_kda.py", "tests/test_gpu_mla.py", "tests/test_gpu_fp8.py",
+          "tests/test_gpu_kv8.py", "tests/test_gpu_kvi8.py"]
 
 
 def test_parity_suites_pass_under_device_bounds_checks():
