@@ -1164,10 +1164,11 @@ def measure_kv8(torch, lcsw, peak, fmt="e4m3"):
             "alg_bytes": ab8, "timing": "median of 200 calls, each after a write of 2x L2",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4),
-                         "traffic": None if fmt == "i8" else profiled_traffic(
-                             "sparse_attn_kv8_decode_1m.md",
+                         "traffic": profiled_traffic(
+                             "sparse_attn_kvi8_decode_1m.md" if fmt == "i8"
+                             else "sparse_attn_kv8_decode_1m.md",
                              ["sparse_attn_kv8.cu", "attn_core.cuh", "e4m3_core.cuh",
-                              "common.cuh"])}}
+                              "i8_core.cuh", "common.cuh"])}}
 
 
 def kda_alg_bytes(B, T, H, D):
