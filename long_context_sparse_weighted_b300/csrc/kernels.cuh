@@ -137,7 +137,8 @@ size_t sparse_attn_mla_ws_bytes(int64_t rows, int H_q, int k, int P);
 cudaError_t launch_sparse_attn_mla(const uint16_t *q, const uint16_t *kv, int64_t skv_b,
                                    const int32_t *seq_len, const int32_t *idx, int B, int T,
                                    int H_q, int P, int k, float scale, uint16_t *out, float *lse,
-                                   void *ws, cudaStream_t st);
+                                   void *ws, cudaStream_t st,
+                                   bool after_selection = false);
 size_t sparse_attn_ws_bytes(int64_t rows, int H_q, int d_v, int k, int P);
 cudaError_t launch_sparse_attn(const uint16_t *q, const uint16_t *K, int64_t sK_b,
                                const uint16_t *V, int64_t sV_b, const int32_t *seq_len,

@@ -342,10 +342,11 @@ static DecodeWs carve_decode(const lcsw_decode_args *a, void *ws) {
 // Attention of one decode query per sequence over idx [B][k] (split-K
 // launches), in the shape's geometry.
 static cudaError_t decode_attend(const lcsw_decode_args *a, const int32_t *idx, void *attn_ws,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool after_selection = false) {
     if (mla_shape(a->d_qk, a->d_v))
         return lcsw::launch_sparse_attn_mla(a->q, a->K, a->sK_b, a->seq_len, idx, a->B, 1, a->H_q,
-                                            a->P, a->k, a->scale, a->out, a->lse, attn_ws, st);
+                                            a->P, a->k, a->scale, a->out, a->lse, attn_ws, st,
+                                            after_selection);
     return lcsw::launch_sparse_attn(a->q, a->K, a->sK_b, a->V, a->sV_b, a->seq_len, idx, a->B, 1,
                                     a->H_q, a->d_qk, a->d_v, a->P, a->k, a->scale, a->out, a->lse,
                                     attn_ws, st);
@@ -395,7 +396,7 @@ lcsw_status lcsw_decode_fused(const lcsw_decode_args *a, void *ws, size_t ws_byt
         // MLA geometry: the persistent kernel selects, the latent attention follows
         cudaError_t e = lcsw::launch_fused_select(a, idx, w.fused, w.status, st);
         if (e != cudaSuccess) return cuda_status(e, "fused selection");
-        return cuda_status(decode_attend(a, idx, w.attn, st), "decode attention");
+        return cuda_status(decode_attend(a, idx, w.attn, st, true), "decode attention");
     }
     // Multi-kernel path (same results): append, score, select, attend.
     if (a->k_idx) {

@@ -21,11 +21,27 @@
 // O += P V over all 64 tokens for its 16 heads.  Each block writes its
 // partial (m, l, O) per head, or the normalised output with one split.
 // Kernel 2 (combine): one block per (row, head) merges the splits.
+//
+// Both launch as programmatic dependents of the kernel before them in the
+// stream where that is safe (sm_90+ dependent launch): the combine always
+// (its only input is the split kernel's output), the split kernel when the
+// decode step's selection kernel precedes it.  Such a kernel may be
+// scheduled before its predecessor ends; it reads what the predecessor
+// writes (idx, the partial states) only after griddepcontrol.wait, which
+// returns once that grid has completed and its writes are visible, and is
+// a no-op in a kernel launched the ordinary way.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace lcsw {
 namespace {
+
+__device__ __forceinline__ void wait_for_predecessor() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void let_dependents_start() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 constexpr int kLat = 512;              // latent (value) width
 constexpr int kDqk = 576;              // latent + rotary key width
@@ -108,6 +124,10 @@ __global__ void __launch_bounds__(kThr, 1) sparse_attn_mla_kernel(
         cp_async16(smem_u32(sq + h * kQP + c8 * 8), qrow + int64_t(h) * kDqk + c8 * 8, 16);
     }
     cp_async_commit();
+    let_dependents_start();  // the combine may be scheduled now; it waits for this grid
+    // idx is the output of the selection kernel before this one (in the
+    // decode step): read only after it has completed
+    wait_for_predecessor();
     auto issue = [&](int ci) {
         const int jb = j0 + ci * gpc;
         gather_rows(skv + (ci & 1) * kTok * kQP, sgid + (ci & 1) * kTok, irow + jb,
@@ -289,6 +309,7 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(
     const int h = int(w % H_q);
     const int t = threadIdx.x;
     auto pidx = [&](int s) { return (row * S + s) * H_q + h; };
+    wait_for_predecessor();  // the split kernel's partial states
     float M = -INFINITY;
     for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(&part_ml[pidx(s)].x));
     const float ref = M == -INFINITY ? 0.f : M;
@@ -344,7 +365,7 @@ size_t sparse_attn_mla_ws_bytes(int64_t rows, int H_q, int k, int P) {
 cudaError_t launch_sparse_attn_mla(const uint16_t *q, const uint16_t *kv, int64_t skv_b,
                                    const int32_t *seq_len, const int32_t *idx, int B, int T,
                                    int H_q, int P, int k, float scale, uint16_t *out, float *lse,
-                                   void *ws, cudaStream_t st) {
+                                   void *ws, cudaStream_t st, bool after_selection) {
     const int64_t rows = int64_t(B) * T;
     if (rows == 0) return cudaSuccess;
     if (rows > 65535) return cudaErrorInvalidConfiguration;
@@ -357,13 +378,29 @@ cudaError_t launch_sparse_attn_mla(const uint16_t *q, const uint16_t *kv, int64_
     float *part_o = reinterpret_cast<float *>(ws);
     float2 *part_ml = reinterpret_cast<float2 *>(
         reinterpret_cast<char *>(ws) + size_t(rows) * S * H_q * kLat * sizeof(float));
-    sparse_attn_mla_kernel<<<dim3(S, unsigned(rows), HGs), kThr, MlaSmem::total, st>>>(
-        q, kv, skv_b, seq_len, idx, T, H_q, P, k, S, scale * kLog2e, out, lse, part_o, part_ml);
-    e = cudaGetLastError();
+    cudaLaunchAttribute dep[1];
+    dep[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    dep[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, unsigned(rows), HGs);
+    cfg.blockDim = dim3(kThr);
+    cfg.dynamicSmemBytes = MlaSmem::total;
+    cfg.stream = st;
+    // (standalone, the kernel before may be the one that writes q: an
+    // ordinary launch; after the decode step's selection, q is an input)
+    cfg.attrs = after_selection ? dep : nullptr;
+    cfg.numAttrs = after_selection ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, sparse_attn_mla_kernel, q, kv, skv_b, seq_len, idx, T, H_q, P, k,
+                           S, scale * kLog2e, out, lse, part_o, part_ml);
     if (e != cudaSuccess || S == 1) return e;
-    mla_combine_kernel<<<unsigned(rows * H_q), kCombThreads, 0, st>>>(part_o, part_ml, H_q, S,
-                                                                       out, lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3(unsigned(rows * H_q));
+    cc.blockDim = dim3(kCombThreads);
+    cc.stream = st;
+    cc.attrs = dep;
+    cc.numAttrs = 1;
+    return cudaLaunchKernelEx(&cc, mla_combine_kernel, static_cast<const float *>(part_o),
+                              static_cast<const float2 *>(part_ml), H_q, S, out, lse);
 }
 
 }  // namespace lcsw
