@@ -214,7 +214,8 @@ lcsw_status lcsw_sparse_attn_kv8(const lcsw_bf16 *q, const uint8_t *kc, int64_t 
  * stack"; no format given).  Reading: symmetric codes in [-127, 127], one
  * fp32 scale per token row = amax / 127 (0 for an all-zero row, whose codes
  * are 0), code_i = the integer nearest to x_i / scale, ties to the even
- * integer; the rounding is exact.
+ * integer; the rounding is exact.  Rows must be finite (a row holding an
+ * infinity or a NaN gets unspecified codes).
  *
  * lcsw_quantize_rows_i8: as lcsw_quantize_rows_e4m3 (same row window, layout,
  * strides and alignment), int8 codes.
