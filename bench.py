@@ -232,13 +232,27 @@ def barrier(world):
 
 
 def allreduce_max(x, world):
+    """The largest x over the ranks (the slowest replica's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_spec(spec, rank):
+    """Replica `rank`'s workload: the same shapes with a seed of its own (rank 0
+    keeps the named workload's seed)."""
+    return synth.Spec(**{**spec.__dict__, "seed": spec.seed + 1000 * rank}) if rank else spec
+
+
+def replica_value(world, B, steps, ms_max):
+    """Whole-job tokens/s of `world` replicas of B sequences over `steps` steps,
+    timed by the slowest rank (ms_max for all the steps)."""
+    return world * B * steps / (ms_max / 1e3)
 
 
 # ------------------------------------------------------------------ lcsw ----
@@ -341,8 +355,7 @@ def run_lcsw(args, world, rank, local):
     import long_context_sparse_weighted_b300 as lcsw
     torch.cuda.set_device(local)
     lcsw.lib()
-    spec = synth.named(args.workload)
-    spec = synth.Spec(**{**spec.__dict__, "seed": spec.seed + 1000 * rank}) if rank else spec
+    spec = rank_spec(synth.named(args.workload), rank)
     c = synth.generate(spec)
     P, k = spec.P, spec.k
     B = spec.B
@@ -369,7 +382,7 @@ def run_lcsw(args, world, rank, local):
     ms, clocks = time_graph_steps(torch, decs, args.steps, args.warmup, world)
     ms = allreduce_max(ms, world)
     step_ms = ms / args.steps
-    value = world * B * args.steps / (ms / 1e3)
+    value = replica_value(world, B, args.steps, ms)
 
     # -- dominant kernel: average launch duration over single calls ---------
     launches = decs[0].launches_per_call
@@ -531,9 +544,10 @@ def run_e2e(args, torch, lcsw, c, decs, keep, spec, world):
         graphs[i % R].replay()
         stream.synchronize()
     dt = allreduce_max(time.perf_counter() - t0, world)
-    return {"value": round(world * B * n / dt, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": round(replica_value(world, B, n, dt * 1e3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n,
-            "eager_value": round(world * B * n / dt_eager, 1),
+            "eager_value": round(replica_value(world, B, n, dt_eager * 1e3), 1),
             "note": "host wall clock; per step: one pinned H2D of the packed query tensors "
                     "and newest-token rows (rows then copied into the caches on the device), "
                     "lcsw_decode_fused, one D2H of out+lse, stream sync; value: the step as "
