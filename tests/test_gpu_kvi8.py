@@ -116,3 +116,29 @@ def test_kvi8_attention_full_size_decode_1m():
     torch.cuda.synchronize()
     assert_attn_close(host_bits(out), o_ref)
     assert_lse_close(lse.cpu().numpy(), l_ref)
+
+
+@pytest.mark.parametrize("P", [1, 2, 8])
+@pytest.mark.parametrize("fmt", ["i8", "e4m3"])
+def test_quantized_kv_attention_other_pool_sizes(P, fmt):
+    """Groups of 1, 2 and 8 tokens (a chunk holds 64/P groups), both code
+    formats, a ragged pair of sequences whose lengths are not multiples of P."""
+    lengths = [5003, 1201]
+    spec = synth.Spec(B=2, lengths=lengths, H_q=32, d_qk=128, d_v=128, k=100, P=P,
+                      seed=640 + P)
+    c = synth.generate(spec)
+    quant_o = oracle.quantize_rows_i8 if fmt == "i8" else oracle.quantize_rows_e4m3
+    attn_o = oracle.sparse_attn_i8kv if fmt == "i8" else oracle.sparse_attn_e4m3kv
+    quant_g = lcsw.quantize_rows_i8 if fmt == "i8" else lcsw.quantize_rows_e4m3
+    attn_g = lcsw.sparse_attn_kvi8 if fmt == "i8" else lcsw.sparse_attn_kv8
+    kc, ks = quant_o(c["K"])
+    vc, vs = quant_o(c["V"])
+    idx = _selection([L // P for L in lengths], spec.k, spec.B, 1, spec.seed)
+    o_ref, l_ref = attn_o(c["q"], kc, ks, vc, vs, c["seq_len"], idx, P, c["scale"])
+    gkc, gks = quant_g(dev_bf16(c["K"]))
+    gvc, gvs = quant_g(dev_bf16(c["V"]))
+    out, lse = attn_g(dev_bf16(c["q"]), gkc, gks, gvc, gvs, dev(c["seq_len"]), dev(idx), P,
+                      c["scale"])
+    torch.cuda.synchronize()
+    assert_attn_close(host_bits(out), o_ref)
+    assert_lse_close(lse.cpu().numpy(), l_ref)
