@@ -143,3 +143,19 @@ def test_mla_decode_step_full_size():
     assert np.array_equal(idx.cpu().numpy(), ref["idx"][:, 0])
     assert_attn_close(host_bits(out), ref["out"][:, 0])
     assert_lse_close(lse.cpu().numpy(), ref["lse"][:, 0])
+
+
+@pytest.mark.parametrize("P", [1, 2, 8])
+def test_mla_attention_other_pool_sizes(P):
+    """Groups of 1, 2 and 8 latent rows (64/P groups a chunk), two sequences
+    whose lengths are not multiples of P."""
+    lengths = [7001, 2999]
+    spec = _mla_spec(B=2, lengths=lengths, H_q=32, k=96, P=P, seed=350 + P)
+    c = synth.generate(spec)
+    idx = _selection([L // P for L in lengths], spec.k, 2, 1, spec.seed)
+    o_ref, l_ref = oracle.sparse_attn(c["q"], c["K"], c["V"], c["seq_len"], idx, P, c["scale"])
+    out, lse = lcsw.sparse_attn_mla(dev_bf16(c["q"]), dev_bf16(c["K"]), dev(c["seq_len"]),
+                                    dev(idx), P, c["scale"])
+    torch.cuda.synchronize()
+    assert_attn_close(host_bits(out), o_ref)
+    assert_lse_close(lse.cpu().numpy(), l_ref)
