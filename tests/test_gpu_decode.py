@@ -283,3 +283,18 @@ def test_prefill_fused_selection_exact_ties():
     ref = oracle.decode_case(c)
     got = run_prefill(c, _cached_part(ref["k_pooled"], c))
     assert np.array_equal(got["idx"], ref["idx"])
+
+
+@pytest.mark.parametrize("P,k", [(1, 2048), (2, 512), (8, 256)])
+def test_decode_step_other_pool_sizes(P, k):
+    """The persistent step with groups of 1 (the IndexPool-off ablation's
+    k = 2048), 2 and 8 tokens, appending the newest group, over a ragged pair
+    of sequences."""
+    spec = synth.Spec(B=2, lengths=[96000 // P * P, 20000 // P * P], H_i=8, k=k, H_q=32, P=P,
+                      plant_frac=0.05, seed=215 + P)
+    c = synth.generate(spec)
+    ref = oracle.decode_case(c)
+    got = run_decode(c, ref["k_pooled"], append=True, corrupt_last=True)
+    assert got["launches"] == 1
+    assert np.array_equal(got["k_pooled"], ref["k_pooled"])
+    check_against_oracle(c, got, ref)
