@@ -155,3 +155,22 @@ def test_fp8_decode_append_quantizes_the_newest_group():
     assert_scores_close(got["scores"], ref["scores"][:, 0])
     assert selection_diff(got["idx"], ref["idx"][:, 0], ref["scores"][:, 0]) == 0
     assert_attn_close(got["out"], ref["out"][:, 0])
+
+
+@pytest.mark.slow
+def test_fp8_decode_full_size_decode_1m():
+    """The benchmarked FP8-keys step: decode_1m's 262,144 groups quantized on
+    the device, the newest group re-pooled and quantized by the step, against
+    the oracle's FP8 step (its own quantizer, scores, top-k, attention)."""
+    spec = synth.named("decode_1m")
+    c = synth.generate(spec)
+    kp = oracle.pool_keys(c["k_idx"], c["pool_w"], c["seq_len"], c["P"])
+    ref = _fp8_oracle(c, kp)
+    got = _run_fp8(c, pack_tiles(ref["ck"], ref["sk"]), append=True)
+    codes, scales = unpack_tiles(got["kq"], c["G_max"])
+    assert np.array_equal(codes, ref["ck"])
+    assert np.array_equal(scales.view(np.uint32), ref["sk"].view(np.uint32))
+    assert_scores_close(got["scores"], ref["scores"][:, 0])
+    assert selection_diff(got["idx"], ref["idx"][:, 0], ref["scores"][:, 0]) == 0
+    assert_attn_close(got["out"], ref["out"][:, 0])
+    assert_lse_close(got["lse"], ref["lse"][:, 0])
