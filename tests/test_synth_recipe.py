@@ -71,3 +71,19 @@ def test_regeneration_is_bit_identical():
         assert np.array_equal(a[key], b[key]), key
     other = synth.generate(synth.Spec(**{**s.__dict__, "seed": s.seed + 1}))
     assert not np.array_equal(a["K"], other["K"])
+
+
+def test_kda_recipe():
+    import synth.kda as skda
+    s = skda.named("kda_decode_b64")
+    assert (s.B, s.T, s.H, s.D) == (64, 1, 64, 128)
+    c = skda.generate(skda.KdaSpec(B=2, T=3, H=4, D=128, seed=11))
+    C = 3 * 4 * 128
+    assert c["qkv"].shape == (2, 3, C) and c["conv_w"].shape == (C, 4)
+    assert c["conv_state"].shape == (2, 3, C) and c["state"].shape == (2, 4, 128, 128)
+    g, beta = c["g"], c["beta"]
+    assert (g <= 0).all() and (g >= -0.25).all()          # alpha = e^g in [0.78, 1]
+    assert (beta >= 0).all() and (beta <= 1).all()
+    w = synth.bf16_to_f32(c["conv_w"])
+    assert (np.abs(w) <= 0.5).all()
+    assert abs(c["state"].std() - 0.05) < 0.005
