@@ -459,33 +459,35 @@ def run_lcsw(args, world, rank, local):
 def run_e2e(args, torch, lcsw, c, decs, keep, spec, world):
     """Each step: one pinned host -> device copy of the step's inputs (the
     query tensors and the newest token's key/value rows, packed in one staging
-    buffer; the decoder reads its queries from it and the rows are copied on
-    into the caches), the decode call, one device -> host read of the output
-    and lse (one staging buffer), then synchronise."""
+    buffer; the decoder reads its queries from it and lcsw_append_token writes
+    the rows into the caches), the decode call, one device -> host read of the
+    output and lse (one staging buffer), then synchronise."""
     B = spec.B
     dev = "cuda"
     R = len(decs)
     last = [int(L) - 1 for L in spec.lengths]
     al = lambda n: (n + 255) // 256 * 256
     kp0, K0, V0, qi0, w0, q0 = keep["keep"][0]
+    d_row = keep["k_idx"].shape[2] + K0.shape[2] + V0.shape[2]
     parts = [("qi", qi0.numel() * 2), ("w", w0.numel() * 4), ("q", q0.numel() * 2),
-             ("nk", B * keep["k_idx"].shape[2] * 2), ("nK", B * K0.shape[2] * 2),
-             ("nV", B * V0.shape[2] * 2)]
+             ("rows", B * d_row * 2)]
     offs, tot = {}, 0
     for name, n in parts:
         offs[name] = (tot, n)
         tot += al(n)
     o_bytes = decs[0].out.numel() * 2
     out_tot = al(o_bytes) + decs[0].lse.numel() * 4
-    new_k = torch.stack([keep["k_idx"][b, last[b]] for b in range(B)]).cpu()
-    new_K = torch.stack([decs[0]._keep[4][b, last[b]] for b in range(B)]).cpu()
-    new_V = torch.stack([decs[0]._keep[5][b, last[b]] for b in range(B)]).cpu()
+    # the newest token's rows, packed [k_idx | K | V] per sequence
+    new_rows = torch.cat([
+        torch.stack([keep["k_idx"][b, last[b]] for b in range(B)]),
+        torch.stack([decs[0]._keep[4][b, last[b]] for b in range(B)]),
+        torch.stack([decs[0]._keep[5][b, last[b]] for b in range(B)])], dim=1).cpu()
     stage = []
     for r in range(R):
         kp, K, V, qi, w, q = keep["keep"][r]
         hin = torch.empty(tot, dtype=torch.uint8).pin_memory()
         din = torch.empty(tot, dtype=torch.uint8, device=dev)
-        src = dict(qi=qi, w=w, q=q, nk=new_k, nK=new_K, nV=new_V)
+        src = dict(qi=qi, w=w, q=q, rows=new_rows)
         for name, (o, n) in offs.items():
             hin[o:o + n].copy_(src[name].contiguous().view(torch.uint8).reshape(-1).cpu())
         view = lambda name, like: din[offs[name][0]:offs[name][0] + offs[name][1]].view(
@@ -496,8 +498,7 @@ def run_e2e(args, torch, lcsw, c, decs, keep, spec, world):
         hout = torch.empty(out_tot, dtype=torch.uint8).pin_memory()
         qi_v, w_v, q_v = view("qi", qi), view("w", w), view("q", q)
         decs[r].rebind(q_idx=qi_v, w_head=w_v, q=q_v, out=out_v, lse=lse_v)
-        rows = dict(nk=view("nk", new_k), nK=view("nK", new_K), nV=view("nV", new_V))
-        stage.append(dict(hin=hin, din=din, dout=dout, hout=hout, rows=rows,
+        stage.append(dict(hin=hin, din=din, dout=dout, hout=hout, rows=view("rows", new_rows),
                           keep=(qi_v, w_v, q_v, out_v, lse_v)))
     h2d, d2h = tot, out_tot
     n = args.e2e_steps
@@ -506,10 +507,7 @@ def run_e2e(args, torch, lcsw, c, decs, keep, spec, world):
         kp, K, V, qi, w, q = keep["keep"][r]
         st = stage[r]
         st["din"].copy_(st["hin"], non_blocking=True)
-        for b in range(B):
-            keep["k_idx"][b, last[b]].copy_(st["rows"]["nk"][b], non_blocking=True)
-            K[b, last[b]].copy_(st["rows"]["nK"][b], non_blocking=True)
-            V[b, last[b]].copy_(st["rows"]["nV"][b], non_blocking=True)
+        lcsw.append_token(st["rows"], decs[r]._keep[6], keep["k_idx"], K, V)
         decs[r]()
         st["hout"].copy_(st["dout"], non_blocking=True)
 
@@ -549,7 +547,8 @@ def run_e2e(args, torch, lcsw, c, decs, keep, spec, world):
             "d2h_bytes_per_step": d2h, "steps": n,
             "eager_value": round(replica_value(world, B, n, dt_eager * 1e3), 1),
             "note": "host wall clock; per step: one pinned H2D of the packed query tensors "
-                    "and newest-token rows (rows then copied into the caches on the device), "
+                    "and newest-token rows (rows then written into the caches by "
+                    "lcsw_append_token), "
                     "lcsw_decode_fused, one D2H of out+lse, stream sync; value: the step as "
                     "one captured CUDA graph launch; eager_value: issued call by call"}
 

@@ -297,6 +297,29 @@ lcsw_status lcsw_sparse_attn_noalloc(const lcsw_bf16 *q, const lcsw_bf16 *K, int
                                      float *lse, lcsw_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * Append of a decode step's new token.  The newest token of every sequence
+ * (position seq_len[b] - 1, after the length has grown) is written into the
+ * raw indexer-key cache, the K cache and the V cache from one packed staging
+ * row per sequence, in one launch:
+ *
+ *   rows [B][*] bf16, batch stride s_rows elements:
+ *        [k_idx row (d_idx) | K row (d_qk) | V row (d_v)]
+ *   k_idx [B][*][d_idx], K [B][*][d_qk], V [B][*][d_v] bf16, batch strides in
+ *        elements; V = NULL with d_v = 0 for the MLA geometry (the value is
+ *        the latent part of K)
+ *
+ * Sequences with seq_len[b] <= 0 are skipped; nothing else is written.  The
+ * decode step (lcsw_decode_fused with k_idx) then pools the group the new row
+ * completes (IndexPool keeps its state per token: reading notes, section 2,
+ * sub-head "IndexPool").  d_idx, d_qk, d_v multiples of 8; rows, caches and
+ * strides 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+lcsw_status lcsw_append_token(const lcsw_bf16 *rows, int64_t s_rows, const int32_t *seq_len,
+                              int B, lcsw_bf16 *k_idx, int64_t sk_b, int d_idx, lcsw_bf16 *K,
+                              int64_t sK_b, int d_qk, lcsw_bf16 *V, int64_t sV_b, int d_v,
+                              lcsw_stream stream);
+
+/* ---------------------------------------------------------------------------
  * One decode step of the whole retrieval path (one query token per sequence):
  * [append] -> scores -> top-k -> sparse attention, as one persistent kernel.
  *

@@ -90,6 +90,8 @@ _SIGNATURES = {
     "lcsw_sparse_attn_kv8": ([_vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i32,
                               _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp],
                              _i32),
+    "lcsw_append_token": ([_vp, _i64, _vp, _i32, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64,
+                           _i32, _vp], _i32),
     "lcsw_quantize_rows_i8": ([_vp, _i64, _vp, _i32, _i32, _i32, _vp, _i64, _vp, _i64, _vp],
                               _i32),
     "lcsw_sparse_attn_kvi8": ([_vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i32,
@@ -277,6 +279,24 @@ def sparse_attn(q, K, V, seq_len, idx, P, scale, out=None, lse=None, ws=None, st
                                   float(scale), _ptr(out), _ptr(lse), _ptr(ws), nbytes,
                                   _stream(stream)))
     return out, lse
+
+
+def append_token(rows, seq_len, k_idx, K, V=None, stream=None):
+    """Write each sequence's newest token (row seq_len[b] - 1) into k_idx, K
+    and V from packed rows [B][d_idx + d_qk + d_v] (lcsw_append_token); V None
+    for the MLA geometry (rows then hold d_idx + d_qk values)."""
+    _bf16(rows, "rows", 2)
+    _dense(seq_len, torch.int32, "seq_len")
+    _bf16(k_idx, "k_idx", 3)
+    _bf16(K, "K", 3)
+    if V is not None:
+        _bf16(V, "V", 3)
+    B = rows.shape[0]
+    d_v = V.shape[2] if V is not None else 0
+    _check(lib().lcsw_append_token(_ptr(rows), rows.stride(0), _ptr(seq_len), B, _ptr(k_idx),
+                                   k_idx.stride(0), k_idx.shape[2], _ptr(K), K.stride(0),
+                                   K.shape[2], _ptr(V), V.stride(0) if V is not None else 0, d_v,
+                                   _stream(stream)))
 
 
 def _quantize_rows(fn, dtype, x, codes, scales, row_begin, n_rows, stream):

@@ -33,6 +33,12 @@ cudaError_t launch_kda_step(const uint16_t *qkv, const uint16_t *conv_w, uint16_
 cudaError_t launch_quantize_rows_e4m3(const uint16_t *x, int64_t sx_b, const int32_t *row_begin,
                                       int n_rows, int width, int B, uint8_t *codes, int64_t sc_b,
                                       float *scales, int64_t ss_b, cudaStream_t st);
+// The newest token's rows (position seq_len[b] - 1) of k_idx, K and V (V may
+// be null with d_v 0) from packed rows [B][d_idx + d_qk + d_v] (stride s_rows).
+cudaError_t launch_append_token(const uint16_t *rows, int64_t s_rows, const int32_t *seq_len,
+                                int B, uint16_t *k_idx, int64_t sk_b, int d_idx, uint16_t *K,
+                                int64_t sK_b, int d_qk, uint16_t *V, int64_t sV_b, int d_v,
+                                cudaStream_t st);
 // INT8 K/V cache rows, as launch_quantize_rows_e4m3: int8 codes (symmetric,
 // scale amax / 127 per row).
 cudaError_t launch_quantize_rows_i8(const uint16_t *x, int64_t sx_b, const int32_t *row_begin,

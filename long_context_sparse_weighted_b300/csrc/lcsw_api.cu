@@ -679,6 +679,27 @@ lcsw_status lcsw_prefill(const lcsw_prefill_args *a, void *ws, size_t ws_bytes,
     return cuda_status(e, "prefill attention");
 }
 
+lcsw_status lcsw_append_token(const lcsw_bf16 *rows, int64_t s_rows, const int32_t *seq_len,
+                              int B, lcsw_bf16 *k_idx, int64_t sk_b, int d_idx, lcsw_bf16 *K,
+                              int64_t sK_b, int d_qk, lcsw_bf16 *V, int64_t sV_b, int d_v,
+                              lcsw_stream stream) {
+    LCSW_RANGE("lcsw_append_token");
+    CHECK(B >= 0 && d_idx > 0 && d_qk > 0 && d_v >= 0, "bad dimension");
+    CHECK(d_idx % 8 == 0 && d_qk % 8 == 0 && d_v % 8 == 0, "row widths must be multiples of 8");
+    CHECK(!V == (d_v == 0), "V and d_v: both given or neither");
+    if (B == 0) return LCSW_OK;
+    CHECK(rows && seq_len && k_idx && K, "null pointer argument");
+    CHECK(s_rows >= d_idx + d_qk + d_v && sk_b >= 0 && sK_b >= 0 && sV_b >= 0,
+          "bad stride (a packed row holds d_idx + d_qk + d_v values)");
+    CHECK(bf16_rows_ok(rows, 8, s_rows) && bf16_rows_ok(k_idx, d_idx, sk_b) &&
+              bf16_rows_ok(K, d_qk, sK_b) && (!V || bf16_rows_ok(V, d_v, sV_b)) &&
+              aligned(seq_len, 4),
+          "bf16 rows must be 16-byte aligned");
+    return cuda_status(lcsw::launch_append_token(rows, s_rows, seq_len, B, k_idx, sk_b, d_idx, K,
+                                                 sK_b, d_qk, V, sV_b, d_v, (cudaStream_t)stream),
+                       "append launch");
+}
+
 // argument checks shared by the FP8 and INT8 row quantizers
 static lcsw_status quantize_rows_args(const lcsw_bf16 *x, int64_t sx_b, const int32_t *row_begin,
                                       int B, int n_rows, int width, const void *codes,

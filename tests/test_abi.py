@@ -212,3 +212,18 @@ def test_int8_cache_entries_validate_arguments(L):
                                        0, None) == lcsw.ERR_WORKSPACE
     assert L.lcsw_sparse_attn_kvi8(*p, 0, 1, 64, 128, 128, 4, 512, 0.1, 0x80000, None, None, 0,
                                    None) == lcsw.OK
+
+
+def test_append_token_validates_arguments(L):
+    import long_context_sparse_weighted_b300 as lcsw
+    r, s, k, K, V = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    bad_width = (r, 320, s, 2, k, 64 * 100, 60, K, 128 * 100, 128, V, 128 * 100, 128, None)
+    assert L.lcsw_append_token(*bad_width) == lcsw.ERR_INVALID_ARG
+    short_row = (r, 256, s, 2, k, 64 * 100, 64, K, 128 * 100, 128, V, 128 * 100, 128, None)
+    assert L.lcsw_append_token(*short_row) == lcsw.ERR_INVALID_ARG
+    v_mismatch = (r, 320, s, 2, k, 64 * 100, 64, K, 128 * 100, 128, None, 0, 128, None)
+    assert L.lcsw_append_token(*v_mismatch) == lcsw.ERR_INVALID_ARG
+    misaligned = (r + 8, 320, s, 2, k, 64 * 100, 64, K, 128 * 100, 128, V, 128 * 100, 128, None)
+    assert L.lcsw_append_token(*misaligned) == lcsw.ERR_INVALID_ARG
+    empty = (None, 320, None, 0, None, 0, 64, None, 0, 128, None, 0, 0, None)
+    assert L.lcsw_append_token(*empty) == lcsw.OK
